@@ -1,0 +1,11 @@
+"""Float64 CPU oracle for causal Local Linear Attention: test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of ``bench.py``
+may import this package. It shares no code with ``local_linear_attention_gb300``.
+"""
+from .lla_oracle import (  # noqa: F401
+    lla_row,
+    lla_forward_oracle,
+    lla_moments_oracle,
+    softmax_attention_oracle,
+)
