@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Throughput of the causal LLA forward (liblla, one GB300 per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lla|reference] [--workload 3]
+
+One step is one full causal LLA forward (every stage of the hot path) over the headline workload:
+B4 H8 T4096 d=dv=64, bf16 inputs and outputs, i.i.d. N(0,1) q, k, v (seed 2), h=8,
+lambda=1e-2. Inputs are resident in HBM before the timed region; the 256 MiB L2 flush between
+steps is outside the per-step CUDA events. Under torchrun every rank runs its own copy of the
+workload (weak scaling: independent heads, no collective on the data path); the step time is
+the max over ranks.
+
+The printed JSON line carries: value (queries/s, all ranks), TFLOP/s and fraction of the
+measured peak for the dominant kernel (roofline), the end-to-end rate through the C ABI on host
+buffers (e2e), the float64 oracle timed on the host cores on a bounded sample of the same
+workload (cpu_baseline), the number of liblla kernel launches in the timed region and the SM
+clocks sampled during it.
+
+--impl reference times the float64 oracle itself (the reference arm of this comparison) on the
+host cores, on bounded samples of the same workload, and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LLA fwd queries/sec and TFLOP/s on 1 GB300; fraction of tensor-core peak"
+UNIT = "queries/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+# ----------------------------------------------------------------------------- accounting
+def causal_pairs(w) -> int:
+    return w.B * w.H * w.T * (w.T + 1) // 2
+
+
+def moments_flops_per_pair(d: int) -> int:
+    """Algorithmic flops per causal pair of the moments stage: the logit q.k (2d) and the
+    kernel-weighted sums omega, sum w k and the upper triangle of sum w k k^T (2 each)."""
+    return 2 * d + 2 * (1 + d + d * (d + 1) // 2)
+
+
+def step_flops(w) -> int:
+    """Algorithmic flops of one whole forward (keys-only dense moments + solve + readout)."""
+    d, e = w.d, w.dv
+    per_pair = moments_flops_per_pair(d) + 2 * d + 2 * e + 2
+    per_query = d ** 3 // 3 + 2 * d * d + 2 * d * e
+    return causal_pairs(w) * per_pair + w.queries * per_query
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def fp32_alu_peak_tflops(peaks) -> float:
+    """FP32 FMA peak from unit counts and the maximum SM clock: SMs x lanes x 2 flop x f."""
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def kernel_source_sha(name: str) -> str:
+    p = os.path.join(ROOT, "local_linear_attention_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel_file)
+    if not ent or ent.get("source_sha") != kernel_source_sha(kernel_file):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+_POOL_INPUTS = {}
+
+
+def _pool_init(workload_index: int):
+    from local_linear_attention_gb300 import workloads as W
+    q, k, v = W.make_inputs(W.WORKLOADS[workload_index])
+    _POOL_INPUTS["qkv"] = tuple(t.float().numpy() for t in (q, k, v))
+
+
+def _oracle_rows(args):
+    h, lam, rows = args
+    from oracle import lla_forward_oracle
+    q, k, v = _POOL_INPUTS["qkv"]
+    t0 = time.perf_counter()
+    lla_forward_oracle(q, k, v, h, lam, rows=rows)
+    return time.perf_counter() - t0
+
+
+class OracleTimer:
+    """The float64 oracle, as it stands, on bounded row samples of a workload: one chunk of rows
+    per host core, in spawned single-threaded worker processes that regenerate the workload
+    from its seed once."""
+
+    def __init__(self, workload_index: int):
+        from local_linear_attention_gb300 import workloads as W
+        self.W = W
+        self.w = W.WORKLOADS[workload_index]
+        self.cores = os.cpu_count() or 1
+        env = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+        old = {x: os.environ.get(x) for x in env}
+        os.environ.update(env)
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.cores, _pool_init, (workload_index,))
+        finally:
+            for x, val in old.items():
+                if val is None:
+                    os.environ.pop(x, None)
+                else:
+                    os.environ[x] = val
+        self.pool.map(_oracle_rows, [(1.0, 1.0, [0])] * self.cores)  # workers ready
+        self.per_row = None
+
+    def _run(self, rows):
+        lam, h = self.w.points[0]
+        chunks = [(h, lam, rows[i::self.cores]) for i in range(self.cores)]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_rows, chunks)
+        return time.perf_counter() - t0
+
+    def measure(self, budget_s: float, seed: int):
+        """(queries/s, cores, sample description) for about budget_s seconds of oracle work."""
+        w = self.w
+        if self.per_row is None:  # the cost of a row grows with its prefix: calibrate once
+            rows = self.W.sample_rows(w.B * w.H, w.T, 2 * self.cores, seed=seed)
+            self.per_row = self._run(rows) / len(rows)
+        for attempt in range(3):
+            n = int(min(w.queries, max(self.cores, budget_s / max(self.per_row, 1e-6))))
+            rows = self.W.sample_rows(w.B * w.H, w.T, n, seed=seed + 1)
+            wall = self._run(rows)
+            self.per_row = wall / len(rows)
+            if wall >= 0.5 * budget_s or n >= w.queries:
+                break
+        sample = (f"{len(rows)} uniformly sampled query rows of {w.describe()} (of {w.queries}), "
+                  f"one float64 lstsq per row, {self.cores} single-threaded processes, "
+                  f"{wall:.1f} s")
+        return len(rows) / wall, self.cores, sample
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+# ----------------------------------------------------------------------------- main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    budget = float(os.environ.get("LLA_ORACLE_STEP_S", "4"))
+    vals, cores, sample = [], 1, ""
+    timer = OracleTimer(args.workload)
+    for s in range(args.warmup + args.steps):
+        v, cores, sample = timer.measure(budget, seed=500 + s)
+        if s >= args.warmup:
+            vals.append(v)
+    timer.close()
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.queries / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.describe()}, h={w.points[0][1]}, "
+                               f"lambda={w.points[0][0]}, seed {w.seed}",
+                   "note": "float64 CPU oracle; value extrapolated from row samples"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    from local_linear_attention_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    # The oracle's process pool is spawned before any GPU work (rank 0, one GPU only).
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        timer = OracleTimer(args.workload)
+        v, cores, sample = timer.measure(float(os.environ.get("LLA_ORACLE_BUDGET_S", "20")), 900)
+        timer.close()
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    from local_linear_attention_gb300 import binding as lla
+    from local_linear_attention_gb300 import build as lla_build
+    lla_build.build()
+
+    lam, h = w.points[0]
+    q, k, v = W.make_inputs(w)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    out = torch.empty(w.B, w.H, w.T, w.dv, dtype=dq.dtype, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lla.lla_forward(dq, dk, dv, h, lam, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = lla.launch_count()
+    lla.profile_enable(True)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    lla.profile_enable(False)
+    if world > 1:
+        dist.barrier()
+    n_launch = lla.launch_count() - n_launch0
+    clk = clocks.stop()
+    stage_ms, n_calls = lla.profile_collect()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during the timed steps")
+
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = w.queries * world / (ms_per_step / 1e3)
+
+    # end to end through the C ABI on pinned host buffers (H2D + compute + D2H every step)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    for _ in range(2):
+        lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    eb = q.element_size()
+
+    peaks, peak_src = load_peaks()
+    mom_ms = stage_ms["moments"] / max(n_calls, 1)
+    mom_flops = causal_pairs(w) * moments_flops_per_pair(w.d)
+    achieved = mom_flops / (mom_ms / 1e3) / 1e12
+    peak = fp32_alu_peak_tflops(peaks)
+    traffic = recorded_traffic("lla_moments_ffma.cu")
+    step_tflops = step_flops(w) * world / (ms_per_step / 1e3) / 1e12
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v, h={h}, "
+                                   f"lambda={lam}, seed {w.seed}",
+                       "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
+                       "l2": "flushed between steps (256 MiB write outside the step events)",
+                       "parallelism": f"replica per GPU x{world}"},
+            "tflops": step_tflops,
+            "bf16_peak_fraction": step_tflops / float(peaks.get("bf16_tflops", 1900.0)),
+            "roofline": {"kernel": "moments (lla_moments_ffma.cu)", "bound": "alu",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 "
+                                        f"x {peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
+                         "avg_launch_ms": mom_ms},
+            "stage_ms_per_step": {k_: v_ / max(n_calls, 1) for k_, v_ in stage_ms.items()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.queries * world / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * eb,
+                    "d2h_bytes_per_step": out.numel() * eb},
+            "gpu_launches": n_launch,
+            "clocks": clk,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,145 @@
+/*
+ * liblla: causal Local Linear Attention (LLA) forward on one NVIDIA GB300 (sm_103a).
+ *
+ * Definition (the operation every entry point below serves)
+ * ---------------------------------------------------------
+ * "Parallax" (Tilde Research blog), section 2 "Parallax & Local Linear Attention",
+ * paragraph "Canonical Formulation"; the same definition in "Parallax: Parameterized Local
+ * Linear Attention for Language Modeling" (arXiv 2605.29157), section 2, LLA paragraph.
+ * For each query q_i (0-based position i) over its causal prefix j <= i (diagonal included),
+ * LLA fits the local linear estimator b + W (x - q_i) to the pairs (k_j, v_j) by weighted
+ * least squares with kernel weights w_ij = exp(q_i . k_j / h) and ridge penalty
+ * lambda * ||W||_F^2, and outputs the intercept b. In closed form
+ *     o_i = vbar_i + C_vk (C_kk + lambda I)^-1 (q_i - kbar_i),
+ * with kbar, vbar the w-weighted means and C_kk, C_vk the (unnormalised) w-weighted centred
+ * second moments. lambda is absolute against the raw weights exp(q.k/h); h divides the logit.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ * - Layout: q, k are [B, H, T, d] and v, out are [B, H, T, dv], contiguous, row-major
+ *   (innermost index = feature). Element type is given by `dtype` (lla_dtype) and is the same
+ *   for q, k, v and out. Computation is carried out in fp32 (with compensated fp32 pairs for
+ *   the fp32 element type); bf16 is an input/output format only.
+ * - Pointers named *_host are host memory; every other data pointer is device memory of the
+ *   current CUDA device, 16-byte aligned. The caller owns every buffer; `out` must not overlap
+ *   an input.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Calls are
+ *   asynchronous on that stream unless stated otherwise; they return after validating the
+ *   arguments and enqueueing work.
+ * - Errors: every call returns an lla_status. Argument errors are detected on the host before
+ *   any work is enqueued and leave all buffers untouched. Numerical failures inside a kernel
+ *   (a non-positive pivot in a ridge solve, e.g. from non-finite inputs) are recorded in a
+ *   per-device status word read by lla_stream_status(); the affected output rows are NaN.
+ *   No entry point aborts, traps or exits.
+ * - Supported sizes: d, dv in {16, 32, 64}; B, H, T >= 0 with B*H*T < 2^31 (B*H*T == 0 is a
+ *   no-op that returns LLA_OK); h > 0 and lambda > 0, both finite.
+ */
+#ifndef LLA_H
+#define LLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LLA_VERSION_MAJOR 0
+#define LLA_VERSION_MINOR 1
+#define LLA_VERSION_PATCH 0
+
+typedef enum {
+  LLA_OK = 0,
+  LLA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad h/lambda/dtype, negative size       */
+  LLA_ERR_UNSUPPORTED = 2, /* d or dv outside {16, 32, 64}, or B*H*T >= 2^31                     */
+  LLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                         */
+  LLA_ERR_NUMERICAL = 4,   /* a ridge solve met a non-positive pivot (rows set to NaN)            */
+  LLA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (kernel returned early)          */
+} lla_status;
+
+typedef enum { LLA_F32 = 0, LLA_BF16 = 1 } lla_dtype;
+
+/* Number of timed stages recorded per lla_forward call by the profiling hooks below. */
+#define LLA_NUM_STAGES 4 /* 0 prep, 1 moments, 2 solve, 3 readout */
+
+/*
+ * Causal LLA forward (the operation defined at the top of this header).
+ * q, k: [B,H,T,d]; v: [B,H,T,dv]; out: [B,H,T,dv]; all device, element type `dtype`.
+ * Scratch memory is taken from the CUDA stream-ordered allocator on `stream`
+ * (cudaMallocAsync/cudaFreeAsync, released at the end of the call in stream order);
+ * lla_workspace_size() tells how much. Use lla_forward_ws() to supply it yourself.
+ */
+int lla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                int d, int dv, float h, float lambda, int dtype, void* stream);
+
+/* Bytes of device scratch lla_forward_ws needs for these sizes (0 for invalid sizes).
+ * Host-only; touches no device. */
+size_t lla_workspace_size(int B, int H, int T, int d, int dv, int dtype);
+
+/*
+ * lla_forward with caller-provided device scratch `workspace` (256-byte aligned, at least
+ * lla_workspace_size(...) bytes, not used by anything else until the work on `stream` is done).
+ * Allocates nothing. Returns LLA_ERR_INVALID_ARG if the workspace is missing or too small.
+ */
+int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                   int d, int dv, float h, float lambda, int dtype, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * End-to-end variant on HOST buffers: copies q_host, k_host, v_host to the device on `stream`,
+ * runs the forward, copies the result to out_host and synchronises `stream` before returning.
+ * Host buffers may be pageable or pinned (pinned copies overlap better). Device buffers and
+ * scratch come from the stream-ordered allocator and are released before the call returns.
+ * Returns the forward's status, including any device status recorded by this call's kernels.
+ */
+int lla_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                     int B, int H, int T, int d, int dv, float h, float lambda, int dtype,
+                     void* stream);
+
+/*
+ * Debug entry: raw max-shifted kernel-weighted moments for n selected queries (the sums from
+ * which the pages' omega_i, mu_i and Sigma_i follow, "Parallax" blog s.2 Canonical
+ * Formulation). idx[n] (device, int64) holds flat query indices (b*H + hh)*T + i.
+ * For each selected query: m = max_{j<=i} q_i.k_j/h, w_j = exp(q_i.k_j/h - m) and
+ *   m[n], omega[n] = sum w_j, sk[n,d] = sum w_j k_j, sv[n,dv] = sum w_j v_j,
+ *   Skk[n,d,d] = sum w_j k_j k_j^T, Svk[n,dv,d] = sum w_j v_j k_j^T   (fp32, device, row-major).
+ * Any output pointer may be NULL to skip it. Accumulation is in fp64 (not a fast path).
+ * An out-of-range idx entry sets LLA_ERR_INVALID_ARG in the device status word and leaves that
+ * query's outputs untouched.
+ */
+int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx, int n,
+                float* m, float* omega, float* sk, float* sv, float* Skk, float* Svk,
+                int B, int H, int T, int d, int dv, float h, int dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns LLA_OK, LLA_ERR_NUMERICAL, LLA_ERR_TIMEOUT, LLA_ERR_INVALID_ARG (bad idx in
+ * lla_moments) or LLA_ERR_CUDA (a sticky CUDA error or failed synchronisation).
+ */
+int lla_stream_status(void* stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* lla_status_string(int status);
+
+/* LLA_VERSION_MAJOR*10000 + LLA_VERSION_MINOR*100 + LLA_VERSION_PATCH. */
+int lla_version(void);
+
+/* Number of kernels this library has launched in this process (all devices, all streams). */
+unsigned long long lla_launch_count(void);
+
+/*
+ * Stage timing. lla_profile_enable(1) makes every later lla_forward/lla_forward_ws call record
+ * CUDA events on its stream at the LLA_NUM_STAGES stage boundaries (no synchronisation is
+ * added). lla_profile_collect() waits for the recorded events, writes the summed duration in
+ * milliseconds of each stage over all recorded calls to stage_ms[0..min(max_stages,
+ * LLA_NUM_STAGES)-1], stores the number of calls in *n_calls (if not NULL), and forgets them.
+ * lla_profile_enable(0) stops recording. Returns LLA_OK or LLA_ERR_CUDA.
+ */
+int lla_profile_enable(int on);
+int lla_profile_collect(float* stage_ms, int max_stages, int* n_calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLA_H */

@@ -1,0 +1,190 @@
+"""ctypes binding of liblla.so: the C-ABI entry points under the same names.
+
+Every function here only checks and marshals arguments (device pointers, sizes, the current
+torch stream) and calls the library; all arithmetic runs in liblla's CUDA kernels. There is no
+fallback: if the library is missing or the tensors are not on a CUDA device the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "LlaError", "library_path", "lla_forward", "lla_forward_ws", "lla_workspace_size",
+    "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
+    "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
+]
+
+LLA_OK = 0
+DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1}
+NUM_STAGES = 4
+STAGE_NAMES = ("prep", "moments", "solve", "readout")
+
+# Every function include/lla.h declares.
+EXPORTED_SYMBOLS = (
+    "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
+    "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
+    "lla_profile_enable", "lla_profile_collect",
+)
+
+_lib = None
+
+
+class LlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lla_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return os.environ.get("LLA_LIBRARY",
+                          os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblla.so"))
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"liblla.so not found at {path}; build it with "
+                          "`python -m local_linear_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fp = ctypes.POINTER(ctypes.c_float)
+    sig = {
+        "lla_forward": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
+        "lla_workspace_size": (sz, [i, i, i, i, i, i]),
+        "lla_forward_ws": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp, sz, vp]),
+        "lla_forward_host": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
+        "lla_moments": (i, [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
+        "lla_stream_status": (i, [vp]),
+        "lla_status_string": (ctypes.c_char_p, [i]),
+        "lla_version": (i, []),
+        "lla_launch_count": (ctypes.c_ulonglong, []),
+        "lla_profile_enable": (i, [i]),
+        "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def lla_status_string(status: int) -> str:
+    return _load().lla_status_string(int(status)).decode()
+
+
+def lla_version() -> int:
+    return _load().lla_version()
+
+
+def launch_count() -> int:
+    return int(_load().lla_launch_count())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st: int, where: str):
+    if st != LLA_OK:
+        raise LlaError(st, where)
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("expected q, k [B,H,T,d] and v [B,H,T,dv]")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in DTYPE_CODES:
+        raise ValueError("q, k, v must share one dtype: float32 or bfloat16")
+    B, H, T, d = q.shape
+    return B, H, T, d, v.shape[3], DTYPE_CODES[q.dtype]
+
+
+def _device_inputs(q, k, v):
+    for t in (q, k, v):
+        if not t.is_cuda:
+            raise ValueError("liblla runs on CUDA tensors only")
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    return _shapes(q, k, v)
+
+
+def lla_forward(q, k, v, h: float, lam: float, out=None, stream=None):
+    """Causal LLA forward on device tensors; returns `out` ([B,H,T,dv], dtype of the inputs)."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    st = _load().lla_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, d,
+                             dv, float(h), float(lam), code, _stream_ptr(stream))
+    _check(st, "lla_forward")
+    return out
+
+
+def lla_workspace_size(B, H, T, d, dv, dtype) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_load().lla_workspace_size(B, H, T, d, dv, code))
+
+
+def lla_forward_ws(q, k, v, h: float, lam: float, workspace, out=None, stream=None):
+    """lla_forward with a caller-owned device workspace (a uint8 CUDA tensor)."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    st = _load().lla_forward_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T,
+                                d, dv, float(h), float(lam), code, workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(st, "lla_forward_ws")
+    return out
+
+
+def lla_forward_host(q, k, v, h: float, lam: float, out=None, stream=None):
+    """End-to-end forward on HOST tensors (copies in, computes, copies out, synchronises)."""
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("lla_forward_host takes contiguous CPU tensors")
+    B, H, T, d, dv, code = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=q.dtype, pin_memory=q.is_pinned())
+    st = _load().lla_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                  T, d, dv, float(h), float(lam), code, _stream_ptr(stream))
+    _check(st, "lla_forward_host")
+    return out
+
+
+def lla_moments(q, k, v, idx, h: float, stream=None):
+    """Debug entry: raw max-shifted moments of the queries at flat indices idx (int64 CUDA)."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    idx = idx.to(device=q.device, dtype=torch.int64).contiguous()
+    n = idx.numel()
+    f = dict(dtype=torch.float32, device=q.device)
+    res = {"m": torch.empty(n, **f), "omega": torch.empty(n, **f), "sk": torch.empty(n, d, **f),
+           "sv": torch.empty(n, dv, **f), "Skk": torch.empty(n, d, d, **f),
+           "Svk": torch.empty(n, dv, d, **f)}
+    st = _load().lla_moments(q.data_ptr(), k.data_ptr(), v.data_ptr(), idx.data_ptr(), n,
+                             *(res[x].data_ptr() for x in ("m", "omega", "sk", "sv", "Skk", "Svk")),
+                             B, H, T, d, dv, float(h), code, _stream_ptr(stream))
+    _check(st, "lla_moments")
+    return res
+
+
+def lla_stream_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(_load().lla_stream_status(_stream_ptr(stream)))
+
+
+def profile_enable(on: bool = True):
+    _check(_load().lla_profile_enable(1 if on else 0), "lla_profile_enable")
+
+
+def profile_collect():
+    """(summed ms per stage as a dict, number of recorded lla_forward calls)."""
+    buf = (ctypes.c_float * NUM_STAGES)()
+    n = ctypes.c_int(0)
+    _check(_load().lla_profile_collect(buf, NUM_STAGES, ctypes.byref(n)), "lla_profile_collect")
+    return dict(zip(STAGE_NAMES, list(buf))), n.value

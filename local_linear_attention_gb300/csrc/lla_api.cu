@@ -1,0 +1,312 @@
+// C ABI of liblla: argument validation, scratch management, stage dispatch, device status word,
+// launch counting and stage timing. Kernels live in the other translation units.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "lla_internal.cuh"
+
+namespace lla {
+
+// Per-device status word; kernels receive its address (see device_status()).
+__device__ int g_status;
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int* g_status_ptr[kMaxDevices] = {};
+bool g_pool_ready[kMaxDevices] = {};
+
+// Address of the status word on the current device (resolved once per device).
+cudaError_t device_status(int** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_status);
+    if (err != cudaSuccess) return err;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  if (!g_pool_ready[dev]) {
+    // Keep memory freed with cudaFreeAsync in the device's default pool instead of returning it
+    // to the driver at every synchronisation, so repeated calls reuse their scratch.
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      unsigned long long thr = ~0ULL;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    g_pool_ready[dev] = true;
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+// ------------------------------------------------------------------------- stage timing
+struct ProfRec {
+  cudaEvent_t ev[LLA_NUM_STAGES + 1];
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point. Returns LLA_OK or an error status.
+int check_shape(int B, int H, int T, int d, int dv, int dtype) {
+  if (B < 0 || H < 0 || T < 0) return LLA_ERR_INVALID_ARG;
+  if (dtype != LLA_F32 && dtype != LLA_BF16) return LLA_ERR_INVALID_ARG;
+  if (!(d == 16 || d == 32 || d == 64) || !(dv == 16 || dv == 32 || dv == 64))
+    return LLA_ERR_UNSUPPORTED;
+  if ((long long)B * H * T >= (1LL << 31)) return LLA_ERR_UNSUPPORTED;
+  return LLA_OK;
+}
+
+int check_forward(const Args& a) {
+  int st = check_shape(a.B, a.H, a.T, a.d, a.dv, a.dtype);
+  if (st != LLA_OK) return st;
+  if (!is_finite_pos(a.h) || !is_finite_pos(a.lam)) return LLA_ERR_INVALID_ARG;
+  if (a.rows() == 0) return LLA_OK;
+  if (!a.q || !a.k || !a.v || !a.out) return LLA_ERR_INVALID_ARG;
+  if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.out))
+    return LLA_ERR_INVALID_ARG;
+  return LLA_OK;
+}
+
+Args make_args(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int d,
+               int dv, float h, float lam, int dtype) {
+  Args a;
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.B = B; a.H = H; a.T = T; a.d = d; a.dv = dv;
+  a.h = h; a.lam = lam; a.dtype = dtype;
+  return a;
+}
+
+size_t elem_bytes(int dtype) { return dtype == LLA_F32 ? 4 : 2; }
+
+// Runs every stage on `s` with scratch `base`.
+int run_forward(const Args& a, void* base, cudaStream_t s) {
+  Workspace ws;
+  carve_workspace(a, base, &ws);
+  if (device_status(&ws.status) != cudaSuccess) return LLA_ERR_CUDA;
+  ProfRec rec;
+  bool prof = false;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    for (auto& e : rec.ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return LLA_ERR_CUDA;
+    cudaEventRecord(rec.ev[0], s);
+  }
+  cudaError_t (*stages[LLA_NUM_STAGES])(const Args&, const Workspace&, cudaStream_t) = {
+      launch_prep, launch_moments_ffma, launch_solve, launch_readout};
+  for (int i = 0; i < LLA_NUM_STAGES; ++i) {
+    if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
+    if (prof) cudaEventRecord(rec.ev[i + 1], s);
+  }
+  if (prof) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back(rec);
+  }
+  return LLA_OK;
+}
+
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+size_t workspace_bytes(const Args& a) {
+  const size_t BH = (size_t)a.BH(), R = (size_t)a.rows();
+  const size_t G = (size_t)gram_floats(a.d);
+  size_t n = 0;
+  n += align_up(BH * a.d * sizeof(float));               // kmean
+  n += align_up(BH * a.dv * sizeof(float));              // vmean
+  n += align_up(R * sizeof(float));                      // m
+  n += align_up(R * G * sizeof(float));                  // mom
+  if (a.dtype == LLA_F32) n += align_up(R * G * sizeof(float));  // mom_lo
+  n += align_up(R * a.d * sizeof(float));                // y
+  n += align_up(R * a.d * sizeof(float));                // kbar
+  return n;
+}
+
+void carve_workspace(const Args& a, void* base, Workspace* ws) {
+  const size_t BH = (size_t)a.BH(), R = (size_t)a.rows();
+  const size_t G = (size_t)gram_floats(a.d);
+  char* p = static_cast<char*>(base);
+  auto take = [&](size_t bytes) { char* r = p; p += align_up(bytes); return reinterpret_cast<float*>(r); };
+  ws->kmean = take(BH * a.d * sizeof(float));
+  ws->vmean = take(BH * a.dv * sizeof(float));
+  ws->m = take(R * sizeof(float));
+  ws->mom = take(R * G * sizeof(float));
+  ws->mom_lo = a.dtype == LLA_F32 ? take(R * G * sizeof(float)) : nullptr;
+  ws->y = take(R * a.d * sizeof(float));
+  ws->kbar = take(R * a.d * sizeof(float));
+  ws->status = nullptr;
+}
+
+}  // namespace lla
+
+using namespace lla;
+
+extern "C" {
+
+size_t lla_workspace_size(int B, int H, int T, int d, int dv, int dtype) {
+  if (check_shape(B, H, T, d, dv, dtype) != LLA_OK) return 0;
+  Args a = make_args(nullptr, nullptr, nullptr, nullptr, B, H, T, d, dv, 1.f, 1.f, dtype);
+  return a.rows() == 0 ? 0 : workspace_bytes(a);
+}
+
+int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                   int d, int dv, float h, float lambda, int dtype, void* workspace,
+                   size_t workspace_bytes_, void* stream) {
+  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
+  int st = check_forward(a);
+  if (st != LLA_OK || a.rows() == 0) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 256) != 0 ||
+      workspace_bytes_ < workspace_bytes(a))
+    return LLA_ERR_INVALID_ARG;
+  return run_forward(a, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int lla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int d,
+                int dv, float h, float lambda, int dtype, void* stream) {
+  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
+  int st = check_forward(a);
+  if (st != LLA_OK || a.rows() == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* dummy;
+  if (device_status(&dummy) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
+  st = run_forward(a, ws, s);
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
+  return st;
+}
+
+int lla_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                     int B, int H, int T, int d, int dv, float h, float lambda, int dtype,
+                     void* stream) {
+  Args a = make_args(q_host, k_host, v_host, out_host, B, H, T, d, dv, h, lambda, dtype);
+  int st = check_shape(B, H, T, d, dv, dtype);
+  if (st != LLA_OK) return st;
+  if (!is_finite_pos(h) || !is_finite_pos(lambda)) return LLA_ERR_INVALID_ARG;
+  if (a.rows() == 0) return LLA_OK;
+  if (!q_host || !k_host || !v_host || !out_host) return LLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = nullptr;
+  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;
+  const size_t eb = elem_bytes(dtype);
+  const size_t nqk = (size_t)a.rows() * d * eb, nv = (size_t)a.rows() * dv * eb;
+  const size_t off_k = align_up(nqk), off_v = off_k + align_up(nqk), off_o = off_v + align_up(nv);
+  const size_t off_ws = off_o + align_up(nv);
+  char* dev = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&dev), off_ws + workspace_bytes(a), s) != cudaSuccess)
+    return LLA_ERR_CUDA;
+  bool ok = cudaMemcpyAsync(dev, q_host, nqk, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            cudaMemcpyAsync(dev + off_k, k_host, nqk, cudaMemcpyHostToDevice, s) == cudaSuccess &&
+            cudaMemcpyAsync(dev + off_v, v_host, nv, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  if (ok) {
+    Args ad = make_args(dev, dev + off_k, dev + off_v, dev + off_o, B, H, T, d, dv, h, lambda, dtype);
+    st = run_forward(ad, dev + off_ws, s);
+    ok = st == LLA_OK &&
+         cudaMemcpyAsync(out_host, dev + off_o, nv, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  }
+  cudaFreeAsync(dev, s);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LLA_ERR_CUDA;
+  if (!ok) return st != LLA_OK ? st : LLA_ERR_CUDA;
+  return lla_stream_status(stream);
+}
+
+int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx, int n, float* m,
+                float* omega, float* sk, float* sv, float* Skk, float* Svk, int B, int H, int T,
+                int d, int dv, float h, int dtype, void* stream) {
+  int st = check_shape(B, H, T, d, dv, dtype);
+  if (st != LLA_OK) return st;
+  if (!is_finite_pos(h) || n < 0) return LLA_ERR_INVALID_ARG;
+  if (n == 0) return LLA_OK;
+  if (!q || !k || !v || !idx) return LLA_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;
+  const Args a = make_args(q, k, v, nullptr, B, H, T, d, dv, h, 1.f, dtype);
+  return launch_debug_moments(a, idx, n, m, omega, sk, sv, Skk, Svk, status,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LLA_OK
+             : LLA_ERR_CUDA;
+}
+
+int lla_stream_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return LLA_ERR_CUDA;
+  int* dummy;
+  if (device_status(&dummy) != cudaSuccess) return LLA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status, sizeof(int)) != cudaSuccess) return LLA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return LLA_ERR_CUDA;
+  if (word & kStatusBadIndex) return LLA_ERR_INVALID_ARG;
+  if (word & kStatusTimeout) return LLA_ERR_TIMEOUT;
+  if (word & kStatusNumerical) return LLA_ERR_NUMERICAL;
+  return LLA_OK;
+}
+
+const char* lla_status_string(int status) {
+  switch (status) {
+    case LLA_OK: return "LLA_OK: success";
+    case LLA_ERR_INVALID_ARG: return "LLA_ERR_INVALID_ARG: invalid argument";
+    case LLA_ERR_UNSUPPORTED: return "LLA_ERR_UNSUPPORTED: unsupported size (d, dv in {16,32,64}; B*H*T < 2^31)";
+    case LLA_ERR_CUDA: return "LLA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case LLA_ERR_NUMERICAL: return "LLA_ERR_NUMERICAL: non-positive pivot in a ridge solve";
+    case LLA_ERR_TIMEOUT: return "LLA_ERR_TIMEOUT: a bounded device wait gave up";
+  }
+  return "unknown lla status";
+}
+
+int lla_version(void) {
+  return LLA_VERSION_MAJOR * 10000 + LLA_VERSION_MINOR * 100 + LLA_VERSION_PATCH;
+}
+
+unsigned long long lla_launch_count(void) { return g_launches.load(); }
+
+int lla_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return LLA_OK;
+}
+
+int lla_profile_collect(float* stage_ms, int max_stages, int* n_calls) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  float sum[LLA_NUM_STAGES] = {0.f};
+  int st = LLA_OK;
+  for (auto& r : recs) {
+    if (cudaEventSynchronize(r.ev[LLA_NUM_STAGES]) != cudaSuccess) st = LLA_ERR_CUDA;
+    for (int i = 0; i < LLA_NUM_STAGES && st == LLA_OK; ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1]) != cudaSuccess) st = LLA_ERR_CUDA;
+      sum[i] += ms;
+    }
+    for (auto& e : r.ev) cudaEventDestroy(e);
+  }
+  if (stage_ms)
+    for (int i = 0; i < max_stages && i < LLA_NUM_STAGES; ++i) stage_ms[i] = sum[i];
+  if (n_calls) *n_calls = (int)recs.size();
+  return st;
+}
+
+}  // extern "C"

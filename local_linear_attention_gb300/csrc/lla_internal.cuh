@@ -1,0 +1,94 @@
+// Internal declarations shared by the liblla translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/lla.h"
+
+namespace lla {
+
+// Bits of the per-device status word (see lla_stream_status()).
+enum : int {
+  kStatusNumerical = 1 << 0,
+  kStatusTimeout = 1 << 1,
+  kStatusBadIndex = 1 << 2,
+};
+
+// Problem description after host-side validation.
+struct Args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  int B, H, T, d, dv;
+  float h, lam;
+  int dtype;  // lla_dtype
+  long long BH() const { return (long long)B * H; }
+  long long rows() const { return (long long)B * H * T; }
+};
+
+// Augmented-key Gram layout used by the CUDA-core moments path.
+// The augmented key is kt = [k - c, 1, 0...] of padded length DP = 4*NBLK; the moments of a
+// query are the upper-triangular 4x4 blocks of sum_j p_j kt_j kt_j^T, block (ba, bb) with
+// ba <= bb stored as 16 consecutive floats (row-major inside the block), blocks enumerated
+// row by row. G(D, D) = omega, G(a, D) = sum p (k - c)_a, G(a, b) = sum p (k - c)_a (k - c)_b.
+__host__ __device__ constexpr int gram_nblk(int D) { return (D + 1 + 3) / 4; }
+__host__ __device__ constexpr int gram_nblocks(int D) { return gram_nblk(D) * (gram_nblk(D) + 1) / 2; }
+__host__ __device__ constexpr int gram_floats(int D) { return gram_nblocks(D) * 16; }
+__host__ __device__ constexpr int gram_block_index(int D, int ba, int bb) {
+  return ba * gram_nblk(D) - ba * (ba - 1) / 2 + (bb - ba);
+}
+
+// Device scratch carved out of one workspace allocation.
+struct Workspace {
+  float* kmean;   // [BH, d]        per-head key reference point c
+  float* vmean;   // [BH, dv]       per-head value reference point c_v
+  float* m;       // [BH*T]         row max of the logits q.k/h over the causal prefix
+  float* mom;     // [BH*T, G]      augmented Gram moments (hi part)
+  float* mom_lo;  // [BH*T, G]      compensation terms (fp32 inputs only, else nullptr)
+  float* y;       // [BH*T, d]      ridge-solve result y = (C_kk + lambda' I)^-1 (q - kbar)
+  float* kbar;    // [BH*T, d]      kbar - c, the weighted key mean in the shifted frame
+  int* status;    // device status word of the current device
+};
+
+size_t workspace_bytes(const Args& a);
+void carve_workspace(const Args& a, void* base, Workspace* ws);
+
+// Kernel launchers (one per stage). Each returns the launch error, if any.
+cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_debug_moments(const Args& a, const int64_t* idx, int n, float* m,
+                                 float* omega, float* sk, float* sv, float* Skk, float* Svk,
+                                 int* status, cudaStream_t s);
+
+void count_launch();
+
+// ---------------------------------------------------------------------------------------------
+// Device helpers.
+__device__ __forceinline__ float ldf(const float* p, long long i) { return p[i]; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p, long long i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void stf(float* p, long long i, float x) { p[i] = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, long long i, float x) {
+  p[i] = __float2bfloat16_rn(x);
+}
+
+// Error-free transforms on fp32 pairs (Knuth's TwoSum; the FMA-based exact product).
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+  float t = hi + x;
+  float z = t - hi;
+  lo += (hi - (t - z)) + (x - z);
+  hi = t;
+}
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+  p = a * b;
+  e = fmaf(a, b, -p);
+}
+
+}  // namespace lla

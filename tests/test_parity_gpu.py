@@ -1,0 +1,200 @@
+"""GPU parity: liblla's causal LLA forward against the float64 oracle, through the C ABI.
+
+Tolerances (relative Frobenius error over the checked rows): 1e-3 for fp32 inputs, 2e-2 for
+bf16 inputs (bf16 is the input/output format; the bf16 output rounding is part of the budget).
+Inputs are rounded to their element type first and the oracle reads the rounded values, so
+the error measures the computation, not input quantisation.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from local_linear_attention_gb300 import workloads as W
+from oracle import lla_forward_oracle, lla_moments_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-3, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def lla():
+    from local_linear_attention_gb300 import binding, build
+    build.build()
+    return binding
+
+
+def rel_err(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def run(lla, q, k, v, h, lam):
+    out = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), h, lam)
+    assert lla.lla_stream_status() == 0
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def check(lla, q, k, v, h, lam, dtype, rows=None, tol=None):
+    got = run(lla, q, k, v, h, lam)
+    e = got.shape[-1]
+    flat = got.reshape(-1, e)
+    if rows is None:
+        ref = lla_forward_oracle(q, k, v, h, lam).reshape(-1, e)
+    else:
+        ref = lla_forward_oracle(q, k, v, h, lam, rows=rows)
+        flat = flat[rows]
+    err = rel_err(flat, ref)
+    assert np.isfinite(flat).all()
+    assert err <= (tol or TOL[dtype]), f"relative error {err:.3e}"
+    return err
+
+
+# ------------------------------------------------------------------ benchmark workloads
+
+def test_workload_tiny_fp32_all_rows(lla):
+    w = W.WORKLOADS[1]
+    q, k, v = W.make_inputs(w)
+    check(lla, q, k, v, w.h, w.lam, w.dtype)
+
+
+def test_workload_small_bf16_all_rows(lla):
+    w = W.WORKLOADS[2]
+    q, k, v = W.make_inputs(w)
+    check(lla, q, k, v, w.h, w.lam, w.dtype)
+
+
+def test_workload_headline_bf16_sampled(lla):
+    w = W.WORKLOADS[3]
+    q, k, v = W.make_inputs(w)
+    rows = W.sample_rows(w.B * w.H, w.T, 384, seed=11)
+    check(lla, q, k, v, w.h, w.lam, w.dtype, rows=rows)
+
+
+@pytest.mark.parametrize("point", range(9))
+def test_workload_stress_fp32_sweep(lla, point):
+    w = W.WORKLOADS[4]
+    q, k, v = _stress_inputs()
+    lam, h = w.points[point]
+    rows = W.sample_rows(w.B * w.H, w.T, 160, seed=100 + point)
+    rows = sorted(set(rows) | {0, 1, 2, 17, 63, 64, 65, 200})  # early, rank-deficient prefixes
+    check(lla, q, k, v, h, lam, w.dtype, rows=rows)
+
+
+_STRESS = {}
+
+
+def _stress_inputs():
+    if "x" not in _STRESS:
+        _STRESS["x"] = W.make_inputs(W.WORKLOADS[4])
+    return _STRESS["x"]
+
+
+def test_workload_long_bf16_sampled(lla):
+    w = W.WORKLOADS[5]
+    q, k, v = W.make_inputs(w)
+    rows = W.sample_rows(w.B * w.H, w.T, w.oracle_rows, seed=4)
+    check(lla, q, k, v, w.h, w.lam, w.dtype, rows=rows)
+
+
+# ------------------------------------------------------------------ shapes and edge cases
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,dv", [(16, 16), (32, 32), (64, 64), (16, 64), (64, 16), (32, 64)])
+def test_ragged_shapes(lla, dtype, d, dv):
+    # T spans several query/key tiles of every stage and leaves a ragged tail.
+    B, H, T = 1, 2, 203
+    q, k, v = W.make_iid(B, H, T, d, dv, dtype, seed=1000 + d + dv)
+    check(lla, q, k, v, math.sqrt(d), 1e-2, dtype)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 31, 32, 33, 65])
+def test_short_sequences(lla, T):
+    q, k, v = W.make_iid(2, 1, T, 16, 32, "f32", seed=T)
+    check(lla, q, k, v, 4.0, 1e-2, "f32")
+
+
+def test_first_token_returns_v1(lla):
+    q, k, v = W.make_iid(2, 3, 9, 32, 32, "f32", seed=5)
+    out = run(lla, q, k, v, 5.0, 0.3)
+    assert np.abs(out[:, :, 0] - v[:, :, 0].numpy()).max() < 1e-5
+
+
+def test_large_ridge_is_softmax(lla):
+    q, k, v = W.make_iid(1, 2, 150, 32, 32, "f32", seed=6)
+    out = run(lla, q, k, v, 5.657, 1e30)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q.double(), k.double(), v.double(), is_causal=True, scale=1 / 5.657).numpy()
+    assert rel_err(out, ref) < 1e-5
+
+
+def test_empty_problem_is_noop(lla):
+    q = torch.zeros(1, 1, 0, 16, device="cuda")
+    out = lla.lla_forward(q, q, q, 4.0, 0.01)
+    assert out.shape == (1, 1, 0, 16)
+
+
+def test_nonfinite_input_reports_numerical(lla):
+    q, k, v = W.make_iid(1, 1, 40, 16, 16, "f32", seed=7)
+    k[0, 0, 10, 3] = float("nan")
+    out = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), 4.0, 0.01)
+    assert lla.lla_stream_status() == 4  # LLA_ERR_NUMERICAL
+    assert lla.lla_stream_status() == 0  # cleared by the read
+    o = out.cpu()
+    assert torch.isfinite(o[0, 0, :10]).all() and torch.isnan(o[0, 0, 10:]).all()
+
+
+def test_invalid_arguments_raise(lla):
+    q = torch.zeros(1, 1, 8, 48, device="cuda")
+    with pytest.raises(lla.LlaError) as ei:
+        lla.lla_forward(q, q, q, 4.0, 0.01)
+    assert ei.value.status == 2
+    q = torch.zeros(1, 1, 8, 16, device="cuda")
+    with pytest.raises(lla.LlaError):
+        lla.lla_forward(q, q, q, -1.0, 0.01)
+
+
+# ------------------------------------------------------------------ other entry points
+
+def test_workspace_and_host_entries_match_forward(lla):
+    q, k, v = W.make_iid(2, 2, 300, 64, 64, "bf16", seed=8)
+    ref = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 0.01).cpu()
+    nbytes = lla.lla_workspace_size(2, 2, 300, 64, 64, torch.bfloat16)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    o_ws = lla.lla_forward_ws(q.cuda(), k.cuda(), v.cuda(), 8.0, 0.01, ws).cpu()
+    o_host = lla.lla_forward_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), 8.0, 0.01)
+    assert torch.equal(ref, o_ws) and torch.equal(ref, o_host)
+    with pytest.raises(lla.LlaError):
+        lla.lla_forward_ws(q.cuda(), k.cuda(), v.cuda(), 8.0, 0.01, ws[: nbytes // 2])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_moments_entry_matches_oracle(lla, dtype):
+    B, H, T, d, dv = 1, 2, 150, 32, 16
+    q, k, v = W.make_iid(B, H, T, d, dv, dtype, seed=9)
+    idx = [0, 1, 64, 149, 150, 299]
+    res = lla.lla_moments(q.cuda(), k.cuda(), v.cuda(), torch.tensor(idx), 5.657)
+    assert lla.lla_stream_status() == 0
+    ref = lla_moments_oracle(q, k, v, 5.657, idx)
+    for key in ("m", "omega", "sk", "sv", "Skk", "Svk"):
+        got = res[key].cpu().numpy().astype(np.float64)
+        assert np.abs(got - ref[key]).max() <= 1e-5 * max(1.0, np.abs(ref[key]).max()), key
+
+
+def test_moments_bad_index_sets_status(lla):
+    q, k, v = W.make_iid(1, 1, 20, 16, 16, "f32", seed=10)
+    lla.lla_moments(q.cuda(), k.cuda(), v.cuda(), torch.tensor([3, 20]), 4.0)
+    assert lla.lla_stream_status() == 1  # LLA_ERR_INVALID_ARG from the device status word
+
+
+def test_profiling_and_launch_count(lla):
+    q, k, v = (t.cuda() for t in W.make_iid(1, 2, 256, 64, 64, "bf16", seed=12))
+    n0 = lla.launch_count()
+    lla.profile_enable(True)
+    for _ in range(3):
+        lla.lla_forward(q, k, v, 8.0, 0.01)
+    lla.profile_enable(False)
+    stages, calls = lla.profile_collect()
+    assert calls == 3 and all(t > 0 for t in stages.values())
+    assert lla.launch_count() - n0 == 3 * 4
