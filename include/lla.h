@@ -85,6 +85,34 @@ int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B
                    int d, int dv, float h, float lambda, int dtype, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch that lla_forward_noalloc uses: 64 MiB. */
+#define LLA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+/*
+ * lla_forward for callers that cannot allocate device memory. (The pages have no counterpart:
+ * this is a deployment convenience, not part of the method.)
+ *
+ * Some callers are not allowed to allocate GPU memory themselves -- a plugin that its host
+ * application only hands input and output buffers, or a latency-critical loop that must not call
+ * the allocator while it runs, since an allocation can block on the device or fail under memory
+ * pressure at an unpredictable moment. This entry point calls no allocator at all: its scratch is
+ * one fixed array of LLA_NOALLOC_SCRATCH_BYTES in device memory owned by the library, which every
+ * GPU that loads this part of the library keeps until the process exits. The caller still passes
+ * q, k, v and out exactly as for lla_forward, and the result is the same.
+ *
+ * - Size limit: returns LLA_ERR_UNSUPPORTED, before touching the device, when
+ *   lla_workspace_size(B, H, T, d, dv, dtype) exceeds LLA_NOALLOC_SCRATCH_BYTES (e.g. bf16
+ *   d = dv = 64 fits about 6500 rows B*H*T). Other argument errors are those of lla_forward.
+ * - Set-up: the first call on each device looks up the scratch array's device address (with that
+ *   device current) and caches it; make that first call before any stream capture.
+ * - Sharing: all calls on a device share the one array. Calls whose work overlaps on the GPU
+ *   (other streams, other host threads, without ordering between them) race on it and corrupt
+ *   each other's results; order them on one stream or synchronise between them. Each call
+ *   overwrites whatever an earlier call left, and nothing from an earlier call is read.
+ */
+int lla_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H,
+                        int T, int d, int dv, float h, float lambda, int dtype, void* stream);
+
 /*
  * End-to-end variant on HOST buffers: copies q_host, k_host, v_host to the device on `stream`,
  * runs the forward, copies the result to out_host and synchronises `stream` before returning.

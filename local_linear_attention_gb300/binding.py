@@ -15,6 +15,7 @@ __all__ = [
     "LlaError", "library_path", "lla_forward", "lla_forward_ws", "lla_workspace_size",
     "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
+    "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 LLA_OK = 0
@@ -26,8 +27,11 @@ STAGE_NAMES = ("prep", "moments", "solve", "readout")
 EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
-    "lla_profile_enable", "lla_profile_collect",
+    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc",
 )
+
+# LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -66,6 +70,7 @@ def _load():
         "lla_launch_count": (ctypes.c_ulonglong, []),
         "lla_profile_enable": (i, [i]),
         "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
+        "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -123,6 +128,16 @@ def lla_forward(q, k, v, h: float, lam: float, out=None, stream=None):
     st = _load().lla_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, d,
                              dv, float(h), float(lam), code, _stream_ptr(stream))
     _check(st, "lla_forward")
+    return out
+
+
+def lla_forward_noalloc(q, k, v, h: float, lam: float, out, stream=None):
+    """lla_forward for callers that must not allocate device memory: the library's fixed scratch
+    array is used, and `out` (a preallocated [B,H,T,dv] tensor) is required."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    st = _load().lla_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
+                                     H, T, d, dv, float(h), float(lam), code, _stream_ptr(stream))
+    _check(st, "lla_forward_noalloc")
     return out
 
 
