@@ -55,6 +55,12 @@ def moments_flops_per_pair(d: int) -> int:
     return 2 * d + 2 * (1 + d + d * (d + 1) // 2)
 
 
+def tc_executed_flops_per_pair(d: int) -> int:
+    """Tensor flops the tcgen05 moments kernel executes per causal pair: q.k in 7 sweeps (one max
+    pass, six feature passes) and hi + lo contractions over 6 x 368 feature columns."""
+    return 7 * 2 * d + 2 * 2 * 2208
+
+
 def step_flops(w) -> int:
     """Algorithmic flops of one whole forward (keys-only dense moments + solve + readout)."""
     d, e = w.d, w.dv
@@ -276,11 +282,21 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,T,d,dv,dtype: an i.i.d. N(0,1) workload of this shape instead "
+                         "(for profiling captures; h = sqrt(d), lambda = 1e-2, seed 2)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
     from local_linear_attention_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
+    if args.shape:
+        B, H, T, d, dv, dt = args.shape.split(",")
+        d = int(d)
+        w = W.Workload("custom", int(B), int(H), int(T), d, int(dv), dt, 2, "iid",
+                       h=math.sqrt(d), lam=1e-2)
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -355,35 +371,55 @@ def main(argv=None):
     value = w.queries * world / (ms_per_step / 1e3)
 
     # end to end through the C ABI on pinned host buffers (H2D + compute + D2H every step)
-    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    for _ in range(2):
-        lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
-    e2e_steps = max(3, min(args.steps, 10))
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e = None
     eb = q.element_size()
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        for _ in range(2):
+            lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
+        e2e_steps = max(3, min(args.steps, 10))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * eb,
+               "d2h_bytes_per_step": out.numel() * eb}
 
     peaks, peak_src = load_peaks()
+    tensor_path = w.dtype == "bf16" and w.d == 64
     mom_ms = stage_ms["moments"] / max(n_calls, 1)
     mom_flops = causal_pairs(w) * moments_flops_per_pair(w.d)
     achieved = mom_flops / (mom_ms / 1e3) / 1e12
-    peak = fp32_alu_peak_tflops(peaks)
-    traffic = recorded_traffic("lla_moments_ffma.cu")
+    if tensor_path:
+        kernel_file = "lla_moments_tc.cu"
+        peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+        roof = {"kernel": "moments (lla_moments_tc.cu, tcgen05)", "bound": "tensor",
+                "peak_source": f"bf16 dense, burst ({peak_src})",
+                "executed_tflops": causal_pairs(w) * tc_executed_flops_per_pair(w.d)
+                / (mom_ms / 1e3) / 1e12}
+    else:
+        kernel_file = "lla_moments_ffma.cu"
+        peak = fp32_alu_peak_tflops(peaks)
+        roof = {"kernel": "moments (lla_moments_ffma.cu)", "bound": "alu",
+                "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
+    roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                 "traffic": recorded_traffic(kernel_file), "avg_launch_ms": mom_ms})
     step_tflops = step_flops(w) * world / (ms_per_step / 1e3) / 1e12
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if tensor_path else "f32",
             "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v, h={h}, "
                                    f"lambda={lam}, seed {w.seed}",
@@ -392,17 +428,10 @@ def main(argv=None):
                        "parallelism": f"replica per GPU x{world}"},
             "tflops": step_tflops,
             "bf16_peak_fraction": step_tflops / float(peaks.get("bf16_tflops", 1900.0)),
-            "roofline": {"kernel": "moments (lla_moments_ffma.cu)", "bound": "alu",
-                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 "
-                                        f"x {peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
-                         "avg_launch_ms": mom_ms},
+            "roofline": roof,
             "stage_ms_per_step": {k_: v_ / max(n_calls, 1) for k_, v_ in stage_ms.items()},
             "cpu_baseline": cpu,
-            "e2e": {"value": w.queries * world / e2e_s, "unit": UNIT,
-                    "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * eb,
-                    "d2h_bytes_per_step": out.numel() * eb},
+            "e2e": e2e,
             "gpu_launches": n_launch,
             "clocks": clk,
             "wall_s_timed": t_wall,

@@ -18,8 +18,10 @@
  * --------------------------------------
  * - Layout: q, k are [B, H, T, d] and v, out are [B, H, T, dv], contiguous, row-major
  *   (innermost index = feature). Element type is given by `dtype` (lla_dtype) and is the same
- *   for q, k, v and out. Computation is carried out in fp32 (with compensated fp32 pairs for
- *   the fp32 element type); bf16 is an input/output format only.
+ *   for q, k, v and out. Sums are accumulated in fp32 (in compensated fp32 pairs for the fp32
+ *   element type). For bf16 inputs with d = 64 the moments run on the tensor cores: the kernel
+ *   weights enter the contraction rounded to bf16, the key products k_a*k_b exactly (as an exact
+ *   pair of bf16 values).
  * - Pointers named *_host are host memory; every other data pointer is device memory of the
  *   current CUDA device, 16-byte aligned. The caller owns every buffer; `out` must not overlap
  *   an input.
@@ -151,6 +153,15 @@ const char* lla_status_string(int status);
 
 /* LLA_VERSION_MAJOR*10000 + LLA_VERSION_MINOR*100 + LLA_VERSION_PATCH. */
 int lla_version(void);
+
+/*
+ * Selects the implementation of the moments stage for lla_forward* calls made afterwards by this
+ * process: 0 = automatic (tensor cores -- tcgen05 with exact bf16 hi/lo products -- for bf16
+ * inputs with d = 64, CUDA cores otherwise), 1 = CUDA cores always, 2 = tensor cores wherever
+ * supported (currently the same as 0). Both compute the same moments; the choice exists for
+ * testing and measurement. Returns LLA_ERR_INVALID_ARG for any other value. Host-only.
+ */
+int lla_set_moments_path(int path);
 
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 unsigned long long lla_launch_count(void);

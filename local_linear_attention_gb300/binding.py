@@ -15,7 +15,8 @@ __all__ = [
     "LlaError", "library_path", "lla_forward", "lla_forward_ws", "lla_workspace_size",
     "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
-    "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
+    "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
 ]
 
 LLA_OK = 0
@@ -27,7 +28,7 @@ STAGE_NAMES = ("prep", "moments", "solve", "readout")
 EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
-    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc",
+    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path",
 )
 
 # LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
@@ -71,6 +72,7 @@ def _load():
         "lla_profile_enable": (i, [i]),
         "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
         "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
+        "lla_set_moments_path": (i, [i]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -85,6 +87,14 @@ def lla_status_string(status: int) -> str:
 
 def lla_version() -> int:
     return _load().lla_version()
+
+
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+
+
+def lla_set_moments_path(path: int):
+    """Select the moments stage (0 auto, 1 CUDA cores, 2 tensor cores where supported)."""
+    _check(_load().lla_set_moments_path(int(path)), "lla_set_moments_path")
 
 
 def launch_count() -> int:

@@ -16,6 +16,7 @@ __device__ int g_status;
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_path_request{0};  // 0 auto, kPathCudaCore, kPathTensorCore
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -112,7 +113,9 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
     cudaEventRecord(rec.ev[0], s);
   }
   cudaError_t (*stages[LLA_NUM_STAGES])(const Args&, const Workspace&, cudaStream_t) = {
-      launch_prep, launch_moments_ffma, launch_solve, launch_readout};
+      launch_prep,
+      ws.path == kPathTensorCore ? launch_moments_tc : launch_moments_ffma,
+      launch_solve, launch_readout};
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
     if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);
@@ -128,6 +131,13 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+int choose_path(const Args& a) {
+  const bool tc_ok = a.dtype == LLA_BF16 && a.d == 64;
+  const int req = g_path_request.load();
+  if (req == kPathCudaCore || !tc_ok) return kPathCudaCore;
+  return kPathTensorCore;
+}
+
 size_t workspace_bytes(const Args& a) {
   const size_t BH = (size_t)a.BH(), R = (size_t)a.rows();
   const size_t G = (size_t)gram_floats(a.d);
@@ -139,6 +149,7 @@ size_t workspace_bytes(const Args& a) {
   if (a.dtype == LLA_F32) n += align_up(R * G * sizeof(float));  // mom_lo
   n += align_up(R * a.d * sizeof(float));                // y
   n += align_up(R * a.d * sizeof(float));                // kbar
+  n += align_up(R * sizeof(float));                      // omega
   return n;
 }
 
@@ -154,7 +165,9 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->mom_lo = a.dtype == LLA_F32 ? take(R * G * sizeof(float)) : nullptr;
   ws->y = take(R * a.d * sizeof(float));
   ws->kbar = take(R * a.d * sizeof(float));
+  ws->omega = take(R * sizeof(float));
   ws->status = nullptr;
+  ws->path = choose_path(a);
 }
 
 }  // namespace lla
@@ -279,6 +292,12 @@ int lla_version(void) {
 }
 
 unsigned long long lla_launch_count(void) { return g_launches.load(); }
+
+int lla_set_moments_path(int path) {
+  if (path < 0 || path > 2) return LLA_ERR_INVALID_ARG;
+  g_path_request.store(path);
+  return LLA_OK;
+}
 
 int lla_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);

@@ -51,8 +51,16 @@ struct Workspace {
   float* mom_lo;  // [BH*T, G]      compensation terms (fp32 inputs only, else nullptr)
   float* y;       // [BH*T, d]      ridge-solve result y = (C_kk + lambda' I)^-1 (q - kbar)
   float* kbar;    // [BH*T, d]      kbar - c, the weighted key mean in the shifted frame
+  float* omega;   // [BH*T]         sum of the weights (tensor-core moments path)
   int* status;    // device status word of the current device
+  int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
 };
+
+// Moments implementations. The tensor-core stage handles bf16 inputs with d = 64 and leaves the
+// keys unshifted (c = 0: shifted bf16 keys would no longer multiply exactly); everything else
+// uses the CUDA-core stage.
+enum : int { kPathCudaCore = 1, kPathTensorCore = 2 };
+int choose_path(const Args& a);
 
 size_t workspace_bytes(const Args& a);
 void carve_workspace(const Args& a, void* base, Workspace* ws);
@@ -60,6 +68,8 @@ void carve_workspace(const Args& a, void* base, Workspace* ws);
 // Kernel launchers (one per stage). Each returns the launch error, if any.
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+size_t moments_tc_row_floats();
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_debug_moments(const Args& a, const int64_t* idx, int n, float* m,

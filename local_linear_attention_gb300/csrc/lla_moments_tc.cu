@@ -1,0 +1,457 @@
+// Tensor-core moments stage of the causal LLA forward (bf16 inputs, d = 64; tcgen05 + TMEM).
+//
+// Computes, for every query i of a 128-query tile and its causal prefix j <= i, the kernel-
+// weighted moments that the closed form of LLA needs ("Parallax" blog, s.2 Canonical
+// Formulation): omega = sum p_j, sk = sum p_j k_j and the upper triangle of S = sum p_j k_j k_j^T,
+// with p_j = exp((q_i.k_j - m_i)/h) and m_i the exact row max of q_i.k_j over the prefix.
+//
+// As a GEMM: [128 queries x keys] (P) times [keys x 2144 features] (F, the products
+// k_a * 1 and k_a * k_b, a <= b) into fp32 accumulators in tensor memory. Two facts shape it:
+//  * The products must be exact: rounding k_a k_b to bf16 breaks the Gram structure of S and
+//    makes the ridge system indefinite, whereas rounding the weights p to bf16 only perturbs the
+//    weights (all moments still describe one weighted problem). Each product of two bf16 values
+//    (16 significant bits) is split exactly into hi = bf16(k_a k_b) and lo = k_a k_b - hi, both
+//    exact bf16, with one packed multiply and one packed fused multiply-add; every feature column
+//    is then contracted twice (hi and lo) into the same accumulator.
+//  * 2144 fp32 accumulator columns do not fit the 512 columns of tensor memory, so the features
+//    are swept in 6 passes of 368 columns; each pass streams the key prefix again and recomputes
+//    S = Q K^T and P (cheap next to the 2 x 368-column contraction it feeds).
+// A first pass over the prefix computes the exact row max m_i (only S = Q K^T and a max).
+//
+// Warp roles (10 warps): 0 issues every tcgen05.mma (one thread) and owns the TMEM allocation;
+// 1 stages key blocks (32 keys x 64) into shared memory; 2-5 turn S into P (one thread per query,
+// = TMEM lane) and drain the accumulators after each pass; 6-9 generate the exact hi/lo feature
+// tiles for each key block (one lane per key) into shared memory. P lives in TMEM and is the A
+// operand of the feature contraction (tcgen05.mma with A in tensor memory). All operands in
+// shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is bounded.
+//
+// Output per query row (fp32): mom_tc[row][f] for f < 2208 (f < 64: sk, then the upper triangle
+// of S row by row, then zero padding), omega[row], m[row] = m_i / h.
+#include <cstdint>
+#include <type_traits>
+
+#include "lla_internal.cuh"
+#include "lla_tc_ptx.cuh"
+
+namespace lla {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 64;
+constexpr int BM = 128;                     // queries per CTA = MMA M = TMEM lanes
+constexpr int KB = 32;                      // keys per block
+constexpr int NF = D + D * (D + 1) / 2;     // 2144 features
+constexpr int NCH = 368;                    // features (accumulator columns) per pass
+constexpr int NPASS = 6;
+constexpr int NFP = NPASS * NCH;            // 2208, padded feature count (row stride of mom_tc)
+constexpr int GPP = NCH / 8;                // 46 groups of 8 features per pass
+constexpr int NA = 192, NB_ = NCH - NA;     // split of a pass into two MMAs (N <= 256)
+constexpr int KS = 4;                       // key-tile pipeline stages
+constexpr int NWARPS = 10;
+constexpr int NTHREADS = NWARPS * 32;
+
+// tensor-memory columns
+constexpr uint32_t T_ACC = 0;
+constexpr uint32_t T_S = NCH;               // 2 x 32 columns of fp32 logits
+constexpr uint32_t T_P = T_S + 2 * KB;      // 2 x 16 columns of packed bf16 weights
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(T_P + 2 * (KB / 2) <= TMEM_COLS, "tensor memory budget");
+
+// shared-memory layout (bytes)
+constexpr int SM_Q = 0;                              // 128 x 64 bf16, K-major core layout
+constexpr int SM_K = SM_Q + BM * D * 2;              // KS x (32 x 64 bf16)
+constexpr int K_STAGE = KB * D * 2;
+constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
+constexpr int F_HALF = GPP * 512;
+constexpr int F_BUF = 2 * F_HALF;
+constexpr int SM_BAR = SM_F + 2 * F_BUF;
+constexpr int SMEM_BYTES = SM_BAR + 256;
+
+// Feature f -> (a, b); index D stands for the constant 1 (so f < 64 gives sk).
+struct Pair { int a, b; };
+__host__ __device__ constexpr Pair feature(int f) {
+  if (f < D) return Pair{f, D};
+  if (f >= NF) return Pair{-1, -1};
+  int u = f - D, a = 0;
+  while (u >= D - a) { u -= D - a; ++a; }
+  return Pair{a, a + u};
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t x, uint32_t y, uint32_t z) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(z));
+  return r;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packs k[a0] (low half) and k[a1] (high half) from the key words kw (kw[t] = k[2t] | k[2t+1]<<16;
+// kw[32] holds two bf16 ones for the constant feature).
+template <int A0, int A1>
+__device__ __forceinline__ uint32_t gather2(const uint32_t (&kw)[33]) {
+  constexpr uint32_t s0 = (A0 & 1) ? 0x32u : 0x10u;
+  constexpr uint32_t s1 = (A1 & 1) ? 0x76u : 0x54u;
+  return __byte_perm(kw[A0 >> 1], kw[A1 >> 1], s0 | (s1 << 8));
+}
+
+// One group of 8 features (global feature index F0..F0+7) for this lane's key: 4 hi words and
+// 4 lo words, stored as one 16-byte row of the group's core matrix.
+template <int F0>
+__device__ __forceinline__ void feature_group(const uint32_t (&kw)[33], uint8_t* hi_row,
+                                              uint8_t* lo_row) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) { h[t] = 0u; l[t] = 0u; }
+  // unrolled at compile time through the helper below
+  auto one = [&](auto tpair) {
+    constexpr int T = decltype(tpair)::value;
+    constexpr Pair p0 = feature(F0 + 2 * T), p1 = feature(F0 + 2 * T + 1);
+    if constexpr (p0.a >= 0) {
+      constexpr int a1 = p1.a >= 0 ? p1.a : D, b1 = p1.a >= 0 ? p1.b : D;
+      const uint32_t x = gather2<p0.a, a1>(kw);
+      const uint32_t y = gather2<p0.b, b1>(kw);
+      uint32_t hv = bf16x2_mul(x, y);
+      uint32_t lv = bf16x2_fma(x, y, hv ^ 0x80008000u);
+      if constexpr (p1.a < 0) { hv &= 0xFFFFu; lv &= 0xFFFFu; }
+      h[T] = hv;
+      l[T] = lv;
+    }
+  };
+  one(std::integral_constant<int, 0>{});
+  one(std::integral_constant<int, 1>{});
+  one(std::integral_constant<int, 2>{});
+  one(std::integral_constant<int, 3>{});
+  *reinterpret_cast<uint4*>(hi_row) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_row) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Groups [G0, G1) of pass PASS for one key (lane): writes into the F buffer halves at row
+// offset `row_off` (= (key / 8) * 128 + (key % 8) * 16).
+template <int PASS, int G0, int G1>
+__device__ __forceinline__ void feature_groups(const uint32_t (&kw)[33], uint8_t* fhi, uint8_t* flo,
+                                               int row_off) {
+  if constexpr (G0 < G1) {
+    feature_group<PASS * NCH + G0 * 8>(kw, fhi + G0 * 512 + row_off, flo + G0 * 512 + row_off);
+    feature_groups<PASS, G0 + 1, G1>(kw, fhi, flo, row_off);
+  }
+}
+
+// Split of the 46 groups of a pass among the 4 feature warps: 12, 12, 11, 11.
+__host__ __device__ constexpr int fw_begin(int fw) { return fw < 2 ? 12 * fw : 24 + 11 * (fw - 2); }
+
+template <int PASS>
+__device__ __forceinline__ void generate_pass(int fw, const uint32_t (&kw)[33], uint8_t* fhi,
+                                              uint8_t* flo, int row_off) {
+  switch (fw) {
+    case 0: feature_groups<PASS, fw_begin(0), fw_begin(1)>(kw, fhi, flo, row_off); break;
+    case 1: feature_groups<PASS, fw_begin(1), fw_begin(2)>(kw, fhi, flo, row_off); break;
+    case 2: feature_groups<PASS, fw_begin(2), fw_begin(3)>(kw, fhi, flo, row_off); break;
+    default: feature_groups<PASS, fw_begin(3), GPP>(kw, fhi, flo, row_off); break;
+  }
+}
+
+__device__ __forceinline__ void generate(int pass, int fw, const uint32_t (&kw)[33], uint8_t* fhi,
+                                         uint8_t* flo, int row_off) {
+  switch (pass) {
+    case 0: generate_pass<0>(fw, kw, fhi, flo, row_off); break;
+    case 1: generate_pass<1>(fw, kw, fhi, flo, row_off); break;
+    case 2: generate_pass<2>(fw, kw, fhi, flo, row_off); break;
+    case 3: generate_pass<3>(fw, kw, fhi, flo, row_off); break;
+    case 4: generate_pass<4>(fw, kw, fhi, flo, row_off); break;
+    default: generate_pass<5>(fw, kw, fhi, flo, row_off); break;
+  }
+}
+
+// Byte offset of 16-byte chunk c (elements 8c..8c+7) of row r in a K-major tile whose rows hold
+// D = 64 elements: core matrix (r / 8, c) of 128 bytes, row groups 1024 bytes apart.
+__device__ __forceinline__ int kmaj_off(int r, int c) { return (r >> 3) * 1024 + c * 128 + (r & 7) * 16; }
+
+// Wait executed by all 32 lanes of a warp; the outcome is made warp-uniform so that an abort seen
+// by one lane takes the whole warp out of its loop together.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, kStatusTimeout, abort));
+}
+
+struct Barriers {
+  uint64_t kfull[KS], kempty[KS];
+  uint64_t sfull[2], sfree[2];
+  uint64_t pfull[2], ffull[2], pfree[2];
+  uint64_t accfull, accfree, done;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
+                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ omega_out,
+                  float* __restrict__ mom, int* __restrict__ status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = (T + BM - 1) / BM;
+  const int tile = ntiles - 1 - (int)(blockIdx.x / BH);  // longest causal prefixes first
+  const long long bh = blockIdx.x % BH;
+  const int i0 = tile * BM;
+  const int nq = min(BM, T - i0);
+  const int jend = i0 + nq;
+  const int nb = (jend + KB - 1) / KB;
+  const int G = nb * (1 + NPASS);
+  const long long base = bh * T;
+
+  // Q tile -> shared memory (zero rows past the end of the sequence).
+  for (int e = tid; e < BM * (D / 8); e += NTHREADS) {
+    const int r = e >> 3, c = e & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < nq) v = *reinterpret_cast<const uint4*>(q + (base + i0 + r) * D + c * 8);
+    *reinterpret_cast<uint4*>(smem + SM_Q + kmaj_off(r, c)) = v;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 5); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.sfull[s], 1);
+      mbar_init(&bar.sfree[s], 4);
+      mbar_init(&bar.pfull[s], 4);
+      mbar_init(&bar.ffull[s], 4);
+      mbar_init(&bar.pfree[s], 1);
+    }
+    mbar_init(&bar.accfull, 1);
+    mbar_init(&bar.accfree, 4);
+    mbar_init(&bar.done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  volatile int* abort_p = &abort_flag;
+  const int TO = kStatusTimeout;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(smem + SM_Q);
+      const uint32_t k_addr = smem_u32(smem + SM_K);
+      const uint32_t f_addr = smem_u32(smem + SM_F);
+      constexpr uint32_t id_qk = idesc_bf16(BM, KB, false, false);
+      constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
+      constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
+      bool ok = true;
+      for (int g = 0; g <= G && ok; ++g) {
+        if (g < G) {
+          const int st = g % KS, sb = g & 1;
+          ok = mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p);
+          if (ok && g >= 2) ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, TO, abort_p);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s)
+            mma_ss(tbase + T_S + sb * KB, smem_desc(q_addr + s * 256, 128, 1024),
+                   smem_desc(k_addr + st * K_STAGE + s * 256, 128, 1024), id_qk, s > 0);
+          mma_commit(&bar.sfull[sb]);
+          mma_commit(&bar.kempty[st]);
+        }
+        if (g >= nb + 1) {
+          const int h = g - 1 - nb, pb = h & 1, pass = h / nb, b = h % nb;
+          ok = mbar_wait(&bar.pfull[pb], (h >> 1) & 1, status, TO, abort_p) &&
+               mbar_wait(&bar.ffull[pb], (h >> 1) & 1, status, TO, abort_p);
+          if (ok && b == 0 && pass >= 1)
+            ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t fh = f_addr + pb * F_BUF, fl = fh + F_HALF;
+#pragma unroll
+          for (int s = 0; s < KB / 16; ++s) {
+            const uint32_t a_tm = tbase + T_P + pb * (KB / 2) + s * 8;
+            const uint32_t acc0 = (b > 0 || s > 0) ? 1u : 0u;
+            mma_ts(tbase + T_ACC, a_tm, smem_desc(fh + s * 256, 128, 512), id_a, acc0);
+            mma_ts(tbase + T_ACC, a_tm, smem_desc(fl + s * 256, 128, 512), id_a, 1u);
+            mma_ts(tbase + T_ACC + NA, a_tm, smem_desc(fh + (NA / 8) * 512 + s * 256, 128, 512), id_b, acc0);
+            mma_ts(tbase + T_ACC + NA, a_tm, smem_desc(fl + (NA / 8) * 512 + s * 256, 128, 512), id_b, 1u);
+          }
+          mma_commit(&bar.pfree[pb]);
+          if (b == nb - 1) mma_commit(&bar.accfull);
+        }
+      }
+      if (!ok) *abort_p = 1;
+      // Drain: wait (bounded, whatever the abort flag says) until every MMA this thread issued
+      // has completed, so that tensor memory is not released under a running MMA.
+      mma_commit(&bar.done);
+      volatile int never = 0;
+      mbar_wait(&bar.done, 0, status, TO, &never);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ key-tile loader
+    const __nv_bfloat16* kb = k + base * D;
+    for (int g = 0; g < G; ++g) {
+      const int st = g % KS, b = g % nb;
+      if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
+      uint8_t* dst = smem + SM_K + st * K_STAGE;
+#pragma unroll
+      for (int t = 0; t < (KB * D / 8) / 32; ++t) {
+        const int e = lane + 32 * t, r = e >> 3, c = e & 7, j = b * KB + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (j < jend) v = *reinterpret_cast<const uint4*>(kb + (long long)j * D + c * 8);
+        *reinterpret_cast<uint4*>(dst + kmaj_off(r, c)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.kfull[st]);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int i = i0 + r;
+    const bool valid = r < nq;
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
+    float m = -INFINITY, om = 0.f;
+    for (int g = 0; g < G; ++g) {
+      const int sb = g & 1;
+      if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) break;
+      tc_fence_after();
+      uint32_t sv[KB];
+      tmem_ld16(lane_base + T_S + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+      tmem_ld16(lane_base + T_S + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
+      const int b = g % nb;
+      const int j0 = b * KB;
+      if (g < nb) {  // max pass
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+        continue;
+      }
+      const int h = g - nb, pass = h / nb, pb = h & 1;
+      const float mc = m * c2;
+      uint32_t pw[KB / 2];
+#pragma unroll
+      for (int c = 0; c < KB; c += 2) {
+        const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+        const float p1 =
+            (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+        pw[c / 2] = pack_bf16(p0, p1);
+      }
+      if (pass == 0) {
+#pragma unroll
+        for (int c = 0; c < KB / 2; ++c)
+          om += __uint_as_float(pw[c] << 16) + __uint_as_float(pw[c] & 0xFFFF0000u);
+      }
+      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) break;
+      tc_fence_after();
+      tmem_st8(lane_base + T_P + pb * (KB / 2), *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
+      tmem_st8(lane_base + T_P + pb * (KB / 2) + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.pfull[pb]);
+      if (b == nb - 1) {  // end of a pass: drain the accumulators
+        if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) break;
+        tc_fence_after();
+        float* dst = mom + (base + i) * NFP + pass * NCH;
+#pragma unroll 1
+        for (int c0 = 0; c0 < NCH; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + T_ACC + c0, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              *reinterpret_cast<uint4*>(dst + c0 + 4 * t) =
+                  make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.accfree);
+      }
+    }
+    if (valid) {
+      m_out[base + i] = m * inv_h;
+      omega_out[base + i] = om;
+    }
+  } else {
+    // ------------------------------------------------------------------ feature generation
+    const int fw = warp - 6;
+    const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;
+    for (int g = 0; g < G; ++g) {
+      const int st = g % KS;
+      if (!warp_wait(&bar.kfull[st], (g / KS) & 1, status, abort_p)) break;
+      if (g < nb) {  // max pass: nothing to generate
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.kempty[st]);
+        continue;
+      }
+      const int h = g - nb, pass = h / nb, pb = h & 1;
+      uint32_t kw[33];
+      const uint8_t* krow = smem + SM_K + st * K_STAGE;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(krow + kmaj_off(lane, c));
+        kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
+      }
+      kw[32] = 0x3F803F80u;  // two bf16 ones
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.kempty[st]);
+      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) break;
+      uint8_t* fhi = smem + SM_F + pb * F_BUF;
+      generate(pass, fw, kw, fhi, fhi + F_HALF, row_off);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.ffull[pb]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+size_t moments_tc_row_floats() { return NFP; }
+
+cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  auto kern = moments_tc_kernel;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, ws.status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace lla

@@ -26,7 +26,7 @@ namespace {
 template <typename TIn>
 __global__ void __launch_bounds__(256)
 mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, int DV,
-            float* __restrict__ kmean, float* __restrict__ vmean) {
+            float* __restrict__ kmean, float* __restrict__ vmean, int zero_keys) {
   extern __shared__ float red[];  // [256]
   const bool val = blockIdx.y == 1;
   const int W = val ? DV : D;
@@ -46,7 +46,7 @@ mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, 
   if (tid < W) {
     float t = 0.f;
     for (int r = 0; r < rows_per; ++r) t += red[r * W + tid];
-    mean[tid] = t / (float)T;
+    mean[tid] = (zero_keys && !val) ? 0.f : t / (float)T;
   }
 }
 
@@ -64,14 +64,27 @@ __device__ __forceinline__ int gidx(int a, int b) {  // a <= b
   return gram_block_index(D, a >> 2, b >> 2) * 16 + (a & 3) * 4 + (b & 3);
 }
 
-template <typename TIn, int D, bool PRECISE>
+// Moment layouts: FMT 0 = augmented-Gram 4x4 blocks (CUDA-core stage, gram_floats(D) per row);
+// FMT 1 = tensor-core stage ([sk (D) | upper triangle of S row by row], TC_ROW floats per row,
+// omega in its own array).
+constexpr int TC_ROW = 2208;
+
+template <int D, int FMT>
+__device__ __forceinline__ int moff(int a, int b) {  // a <= b; b == D means the constant 1
+  if (FMT == 0) return gram_block_index(D, a >> 2, b >> 2) * 16 + (a & 3) * 4 + (b & 3);
+  if (b == D) return a;
+  return D + a * D - a * (a - 1) / 2 + (b - a);
+}
+
+template <typename TIn, int D, bool PRECISE, int FMT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
              const float* __restrict__ mom, const float* __restrict__ mom_lo,
-             const float* __restrict__ mrow, int T, long long rows, float lam,
-             float* __restrict__ y_out, float* __restrict__ kbar_out, int* __restrict__ status) {
+             const float* __restrict__ omega, const float* __restrict__ mrow, int T,
+             long long rows, float lam, float* __restrict__ y_out, float* __restrict__ kbar_out,
+             int* __restrict__ status) {
   using C = SolveCfg<D>;
-  constexpr int G = gram_floats(D);
+  constexpr int G = FMT == 0 ? gram_floats(D) : TC_ROW;
   constexpr int LS = C::LS;
   extern __shared__ float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -88,11 +101,11 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   // in double for fp32 inputs (the compensated moments carry more than fp32 precision) and in
   // float otherwise.
   using R = typename std::conditional<PRECISE, double, float>::type;
-  R om = g[gidx<D, PRECISE>(D, D)];
-  if (PRECISE) om += gl[gidx<D, PRECISE>(D, D)];
+  R om = FMT == 0 ? g[gidx<D, PRECISE>(D, D)] : omega[row];
+  if (PRECISE && FMT == 0) om += gl[gidx<D, PRECISE>(D, D)];
   const R inv_om = R(1) / om;
   for (int a = lane; a < D; a += 32) {
-    const int ix = gidx<D, PRECISE>(a, D);
+    const int ix = moff<D, FMT>(a, D);
     R s = g[ix];
     if (PRECISE) s += gl[ix];
     const R kbar = s * inv_om;
@@ -109,10 +122,10 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   for (int e = lane; e < D * D; e += 32) {
     const int i = e / D, j = e % D;
     if (j > i) continue;
-    const int ix = gidx<D, PRECISE>(j, i);
+    const int ix = moff<D, FMT>(j, i);
     R sij = g[ix];
     if (PRECISE) sij += gl[ix];
-    const int si = gidx<D, PRECISE>(i, D), sj = gidx<D, PRECISE>(j, D);
+    const int si = moff<D, FMT>(i, D), sj = moff<D, FMT>(j, D);
     R s_i = g[si], s_j = g[sj];
     if (PRECISE) { s_i += gl[si]; s_j += gl[sj]; }
     R c = sij - s_i * (s_j * inv_om);
@@ -168,17 +181,17 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   }
 }
 
-template <typename TIn, int D, bool PRECISE>
+template <typename TIn, int D, bool PRECISE, int FMT = 0>
 cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
   const size_t smem = sizeof(float) * kWarpsPerBlock * SolveCfg<D>::WARP_FLOATS;
-  auto kern = solve_kernel<TIn, D, PRECISE>;
+  auto kern = solve_kernel<TIn, D, PRECISE, FMT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const long long rows = a.rows();
   const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
   kern<<<(unsigned)blocks, kWarpsPerBlock * 32, smem, s>>>(
-      static_cast<const TIn*>(a.q), ws.kmean, ws.mom, ws.mom_lo, ws.m, a.T, rows, a.lam, ws.y,
-      ws.kbar, ws.status);
+      static_cast<const TIn*>(a.q), ws.kmean, ws.mom, ws.mom_lo, ws.omega, ws.m, a.T, rows, a.lam,
+      ws.y, ws.kbar, ws.status);
   count_launch();
   return cudaGetLastError();
 }
@@ -190,16 +203,17 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
   if (a.dtype == LLA_F32)
     mean_kernel<float><<<grid, 256, 256 * sizeof(float), s>>>(
         static_cast<const float*>(a.k), static_cast<const float*>(a.v), a.T, a.d, a.dv, ws.kmean,
-        ws.vmean);
+        ws.vmean, ws.path == kPathTensorCore);
   else
     mean_kernel<__nv_bfloat16><<<grid, 256, 256 * sizeof(float), s>>>(
         static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v), a.T, a.d,
-        a.dv, ws.kmean, ws.vmean);
+        a.dv, ws.kmean, ws.vmean, ws.path == kPathTensorCore);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s) {
+  if (ws.path == kPathTensorCore) return launch_solve_t<__nv_bfloat16, 64, false, 1>(a, ws, s);
   const bool f32 = a.dtype == LLA_F32;
   switch (a.d) {
     case 16: return f32 ? launch_solve_t<float, 16, true>(a, ws, s) : launch_solve_t<__nv_bfloat16, 16, false>(a, ws, s);

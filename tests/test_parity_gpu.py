@@ -188,6 +188,23 @@ def test_moments_bad_index_sets_status(lla):
     assert lla.lla_stream_status() == 1  # LLA_ERR_INVALID_ARG from the device status word
 
 
+@pytest.mark.parametrize("T", [1, 37, 128, 129, 300])
+def test_moments_paths_agree(lla, T):
+    """The tensor-core and CUDA-core moments stages give the same forward (bf16, d = 64)."""
+    q, k, v = W.make_iid(1, 2, T, 64, 64, "bf16", seed=40 + T)
+    outs = {}
+    try:
+        for path in (lla.PATH_CUDA_CORE, lla.PATH_TENSOR_CORE):
+            lla.lla_set_moments_path(path)
+            outs[path] = run(lla, q, k, v, 8.0, 0.01)
+    finally:
+        lla.lla_set_moments_path(lla.PATH_AUTO)
+    ref = lla_forward_oracle(q, k, v, 8.0, 0.01).reshape(outs[1].shape)
+    for path, o in outs.items():
+        assert rel_err(o, ref) <= 2e-2, (path, rel_err(o, ref))
+    assert rel_err(outs[2], outs[1]) <= 2e-2
+
+
 def test_profiling_and_launch_count(lla):
     q, k, v = (t.cuda() for t in W.make_iid(1, 2, 256, 64, 64, "bf16", seed=12))
     n0 = lla.launch_count()
