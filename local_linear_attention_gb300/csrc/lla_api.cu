@@ -115,7 +115,8 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
   cudaError_t (*stages[LLA_NUM_STAGES])(const Args&, const Workspace&, cudaStream_t) = {
       launch_prep,
       ws.path == kPathTensorCore ? launch_moments_tc : launch_moments_ffma,
-      launch_solve, launch_readout};
+      launch_solve,
+      (ws.path == kPathTensorCore && a.dv == 64) ? launch_readout_tc : launch_readout};
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
     if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);
@@ -150,6 +151,7 @@ size_t workspace_bytes(const Args& a) {
   n += align_up(R * a.d * sizeof(float));                // y
   n += align_up(R * a.d * sizeof(float));                // kbar
   n += align_up(R * sizeof(float));                      // omega
+  n += align_up(R * sizeof(float));                      // mraw
   return n;
 }
 
@@ -166,6 +168,7 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->y = take(R * a.d * sizeof(float));
   ws->kbar = take(R * a.d * sizeof(float));
   ws->omega = take(R * sizeof(float));
+  ws->mraw = take(R * sizeof(float));
   ws->status = nullptr;
   ws->path = choose_path(a);
 }

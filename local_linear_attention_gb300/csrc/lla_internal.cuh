@@ -52,6 +52,7 @@ struct Workspace {
   float* y;       // [BH*T, d]      ridge-solve result y = (C_kk + lambda' I)^-1 (q - kbar)
   float* kbar;    // [BH*T, d]      kbar - c, the weighted key mean in the shifted frame
   float* omega;   // [BH*T]         sum of the weights (tensor-core moments path)
+  float* mraw;    // [BH*T]         row max of q.k (unscaled; tensor-core path, for the readout)
   int* status;    // device status word of the current device
   int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
 };
@@ -72,6 +73,7 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
 size_t moments_tc_row_floats();
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
+cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_debug_moments(const Args& a, const int64_t* idx, int n, float* m,
                                  float* omega, float* sk, float* sv, float* Skk, float* Svk,
                                  int* status, cudaStream_t s);

@@ -26,7 +26,7 @@
 // shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is bounded.
 //
 // Output per query row (fp32): mom_tc[row][f] for f < 2208 (f < 64: sk, then the upper triangle
-// of S row by row, then zero padding), omega[row], m[row] = m_i / h.
+// of S row by row, then zero padding), omega[row], m[row] = m_i / h and mraw[row] = m_i.
 #include <cstdint>
 #include <type_traits>
 
@@ -196,8 +196,9 @@ struct Barriers {
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
-                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ omega_out,
-                  float* __restrict__ mom, int* __restrict__ status) {
+                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ mraw_out,
+                  float* __restrict__ omega_out, float* __restrict__ mom,
+                  int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -394,6 +395,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     }
     if (valid) {
       m_out[base + i] = m * inv_h;
+      mraw_out[base + i] = m;
       omega_out[base + i] = om;
     }
   } else {
@@ -449,7 +451,7 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
-      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, ws.status);
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, ws.status);
   count_launch();
   return cudaGetLastError();
 }

@@ -53,20 +53,9 @@ mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, 
 // ----------------------------------------------------------------------------- solve
 constexpr int kWarpsPerBlock = 4;
 
-template <int D>
-struct SolveCfg {
-  static constexpr int LS = D + 1;                  // row stride of the factor (conflict-free)
-  static constexpr int WARP_FLOATS = D * LS + 2 * D; // factor + right-hand side + shift vector
-};
-
-template <int D, bool PRECISE>
-__device__ __forceinline__ int gidx(int a, int b) {  // a <= b
-  return gram_block_index(D, a >> 2, b >> 2) * 16 + (a & 3) * 4 + (b & 3);
-}
-
-// Moment layouts: FMT 0 = augmented-Gram 4x4 blocks (CUDA-core stage, gram_floats(D) per row);
-// FMT 1 = tensor-core stage ([sk (D) | upper triangle of S row by row], TC_ROW floats per row,
-// omega in its own array).
+// Moment layouts: FMT 0 = augmented-Gram 4x4 blocks (CUDA-core stage, gram_floats(D) per row, plus
+// as many compensation terms for fp32 inputs); FMT 1 = tensor-core stage ([sk (D) | upper
+// triangle of S row by row], TC_ROW floats per row, omega in its own array).
 constexpr int TC_ROW = 2208;
 
 template <int D, int FMT>
@@ -76,6 +65,104 @@ __device__ __forceinline__ int moff(int a, int b) {  // a <= b; b == D means the
   return D + a * D - a * (a - 1) / 2 + (b - a);
 }
 
+template <int D, bool PRECISE, int FMT>
+struct SolveCfg {
+  static constexpr int ROW = FMT == 0 ? gram_floats(D) : TC_ROW;   // floats of one moment row
+  static constexpr int STAGE = (PRECISE ? 2 : 1) * ROW;             // staged per warp (hi [+ lo])
+  static constexpr int WARP_FLOATS = STAGE + 2 * 64;                // + two column buffers
+  static constexpr int NSLOT = D == 64 ? 2 : 1;                     // rows per lane
+};
+
+// State of one lane during the factorisation: its rows, their entries (slot 0: row rr0 < 32,
+// entries 0..W0-1; slot 1 (d = 64 only): row rr1 = 63 - lane, entries 0..63), right-hand sides and
+// diagonal entries of the factor.
+template <int D>
+struct CholLane {
+  static constexpr int NS = D == 64 ? 2 : 1;
+  static constexpr int W0 = D < 32 ? D : 32;
+  static constexpr int W1 = NS == 2 ? D : 1;
+  float a0[W0], a1[W1];
+  float z[NS];
+  float ldiag[NS];
+  int rr0, rr1;
+  bool live0;
+  bool ok;
+};
+
+// Column K of the right-looking factorisation (template recursion keeps every index static).
+template <int D, int K>
+__device__ __forceinline__ void chol_column(CholLane<D>& L, float* colbuf) {
+  constexpr int NS = CholLane<D>::NS, W0 = CholLane<D>::W0;
+  constexpr bool second = NS == 2 && K >= 32;  // slot of row K in its owner lane
+  constexpr int owner = second ? D - 1 - K : K;
+  const float mine = second ? L.a1[NS == 2 ? K : 0] : L.a0[K < W0 ? K : 0];
+  float piv = __shfl_sync(0xffffffffu, mine, owner);
+  if (!(piv > 0.f)) { L.ok = false; piv = 1.f; }  // rows of a failed factorisation become NaN
+  const float lkk = sqrtf(piv), inv = 1.f / lkk;
+  const float zk = __shfl_sync(0xffffffffu, second ? L.z[NS - 1] : L.z[0], owner) * inv;
+  float* cb = colbuf + (K & 1) * 64;
+  if constexpr (K < W0) {
+    if (L.live0) {
+      if (L.rr0 > K) L.a0[K] *= inv;
+      if (L.rr0 == K) { L.a0[K] = lkk; L.ldiag[0] = lkk; L.z[0] = zk; }
+      cb[L.rr0] = L.a0[K];
+    }
+  }
+  if constexpr (NS == 2) {
+    if (L.rr1 > K) L.a1[K] *= inv;
+    if (L.rr1 == K) { L.a1[K] = lkk; L.ldiag[NS - 1] = lkk; L.z[NS - 1] = zk; }
+    cb[L.rr1] = L.a1[K];
+  }
+  __syncwarp();
+  if constexpr (K + 1 < W0) {
+    if (L.live0 && L.rr0 > K) {
+      const float lik = L.a0[K];
+#pragma unroll
+      for (int j = K + 1; j < W0; ++j)
+        if (j <= L.rr0) L.a0[j] = fmaf(-lik, cb[j], L.a0[j]);
+      L.z[0] = fmaf(-lik, zk, L.z[0]);
+    }
+  }
+  if constexpr (NS == 2) {
+    if (L.rr1 > K) {
+      const float lik = L.a1[K];
+#pragma unroll
+      for (int j = K + 1; j < D; ++j)
+        if (j <= L.rr1) L.a1[j] = fmaf(-lik, cb[j], L.a1[j]);
+      L.z[NS - 1] = fmaf(-lik, zk, L.z[NS - 1]);
+    }
+  }
+  if constexpr (K + 1 < D) chol_column<D, K + 1>(L, colbuf);
+}
+
+// Row K of the backward substitution L^T y = z (K runs from D-1 down to 0).
+template <int D, int K>
+__device__ __forceinline__ void back_row(const CholLane<D>& L, float& y0, float& y1) {
+  constexpr int NS = CholLane<D>::NS, W0 = CholLane<D>::W0;
+  float part = 0.f;
+  if constexpr (K < W0) {
+    if (L.live0 && L.rr0 > K) part = fmaf(L.a0[K], y0, part);
+  }
+  if constexpr (NS == 2) {
+    if (L.rr1 > K) part = fmaf(L.a1[K], y1, part);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  constexpr bool second = NS == 2 && K >= 32;
+  constexpr int owner = second ? D - 1 - K : K;
+  const float num = __shfl_sync(0xffffffffu, second ? L.z[NS - 1] : L.z[0], owner);
+  const float dk = __shfl_sync(0xffffffffu, second ? L.ldiag[NS - 1] : L.ldiag[0], owner);
+  const float yk = (num - part) / dk;
+  if (L.rr0 == K) y0 = yk;
+  if (NS == 2 && L.rr1 == K) y1 = yk;
+  if constexpr (K > 0) back_row<D, K - 1>(L, y0, y1);
+}
+
+// One warp solves (C_kk + lambda' I) y = q - kbar for one query, C_kk = S - s s^T / omega from that
+// query's moments, by a Cholesky factorisation held in registers: lane l owns row l and, for
+// d = 64, also row 63 - l (so that every lane holds 65 entries of the lower triangle). Column k of
+// the factor is broadcast through shared memory; the forward substitution rides along as an extra
+// column of the factorisation; the backward substitution reduces across the warp.
 template <typename TIn, int D, bool PRECISE, int FMT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
@@ -83,107 +170,111 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
              const float* __restrict__ omega, const float* __restrict__ mrow, int T,
              long long rows, float lam, float* __restrict__ y_out, float* __restrict__ kbar_out,
              int* __restrict__ status) {
-  using C = SolveCfg<D>;
-  constexpr int G = FMT == 0 ? gram_floats(D) : TC_ROW;
-  constexpr int LS = C::LS;
-  extern __shared__ float smem[];
+  using C = SolveCfg<D, PRECISE, FMT>;
+  constexpr int NS = CholLane<D>::NS;
+  constexpr int W0 = CholLane<D>::W0;
+  using R = typename std::conditional<PRECISE, double, float>::type;
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* Lw = smem + warp * C::WARP_FLOATS;  // [D][LS]
-  float* rv = Lw + D * LS;                   // [D]
-  float* kb = rv + D;                        // [D] kbar - c
+  float* g = smem + warp * C::WARP_FLOATS;  // staged moment row (hi, then lo)
+  float* colbuf = g + C::STAGE;             // [2][64]
   const long long row = (long long)blockIdx.x * kWarpsPerBlock + warp;
   if (row >= rows) return;  // whole warp leaves together
   const long long bh = row / T;
-  const float* g = mom + row * G;
-  const float* gl = PRECISE ? mom_lo + row * G : nullptr;
 
-  // omega, kbar - c and the right-hand side q - kbar = (q - c) - (kbar - c). The centring runs
-  // in double for fp32 inputs (the compensated moments carry more than fp32 precision) and in
-  // float otherwise.
-  using R = typename std::conditional<PRECISE, double, float>::type;
-  R om = FMT == 0 ? g[gidx<D, PRECISE>(D, D)] : omega[row];
-  if (PRECISE && FMT == 0) om += gl[gidx<D, PRECISE>(D, D)];
+  // Stage the moment row with 16-byte loads (rows are 16-byte aligned: ROW % 4 == 0).
+  {
+    const float4* src = reinterpret_cast<const float4*>(mom + row * C::ROW);
+    float4* dst = reinterpret_cast<float4*>(g);
+    for (int t = lane; t < C::ROW / 4; t += 32) dst[t] = src[t];
+    if (PRECISE) {
+      const float4* srl = reinterpret_cast<const float4*>(mom_lo + row * C::ROW);
+      for (int t = lane; t < C::ROW / 4; t += 32) dst[C::ROW / 4 + t] = srl[t];
+    }
+  }
+  __syncwarp();
+  auto M = [&](int a, int b) -> R {  // moment entry, hi + lo
+    const int ix = moff<D, FMT>(a, b);
+    R v = g[ix];
+    if (PRECISE) v += (R)g[C::ROW + ix];
+    return v;
+  };
+
+  const R om = FMT == 0 ? M(D, D) : (R)omega[row];
   const R inv_om = R(1) / om;
-  for (int a = lane; a < D; a += 32) {
-    const int ix = moff<D, FMT>(a, D);
-    R s = g[ix];
-    if (PRECISE) s += gl[ix];
-    const R kbar = s * inv_om;
-    kb[a] = (float)kbar;
-    const R qa = (R)ldf(q, row * D + a) - (R)kmean[bh * D + a];
-    rv[a] = (float)(qa - kbar);
-  }
-  // ridge scaled by exp(-m), kept inside the normal fp32 range
-  double lp = (double)lam * exp(-(double)mrow[row]);
-  lp = fmin(fmax(lp, (double)FLT_MIN), (double)FLT_MAX);
-  __syncwarp();
+  double lpd = (double)lam * exp(-(double)mrow[row]);  // ridge scaled by exp(-m)
+  lpd = fmin(fmax(lpd, (double)FLT_MIN), (double)FLT_MAX);
+  const R lp = (R)lpd;
 
-  // C_kk + lambda' I, lower triangle, C[i][j] = S[j][i] - s_i s_j / omega.
-  for (int e = lane; e < D * D; e += 32) {
-    const int i = e / D, j = e % D;
-    if (j > i) continue;
-    const int ix = moff<D, FMT>(j, i);
-    R sij = g[ix];
-    if (PRECISE) sij += gl[ix];
-    const int si = moff<D, FMT>(i, D), sj = moff<D, FMT>(j, D);
-    R s_i = g[si], s_j = g[sj];
-    if (PRECISE) { s_i += gl[si]; s_j += gl[sj]; }
-    R c = sij - s_i * (s_j * inv_om);
-    if (i == j) c += (R)lp;
-    Lw[i * LS + j] = (float)c;
+  // This lane's rows, their right-hand sides q - kbar and their lower-triangle entries.
+  CholLane<D> L;
+  L.rr0 = lane;
+  L.rr1 = D - 1 - lane;
+  L.live0 = lane < D;
+  L.ok = true;
+  const bool live0 = L.live0;
+  int rr[NS];
+  rr[0] = L.rr0;
+  if (NS == 2) rr[NS - 1] = L.rr1;
+  float kb[NS];
+#pragma unroll
+  for (int t = 0; t < NS; ++t) {
+    L.ldiag[t] = 1.f;
+    const int r = rr[t];
+    if (t == 0 && !live0) { L.z[0] = 0.f; kb[0] = 0.f; continue; }
+    const R sr = M(r, D);
+    const R kbar = sr * inv_om;
+    kb[t] = (float)kbar;
+    L.z[t] = (float)((R)ldf(q, row * D + r) - (R)kmean[bh * D + r] - kbar);
   }
-  __syncwarp();
-
-  // Cholesky, right-looking, column by column.
-  bool ok = true;
-  for (int kk = 0; kk < D; ++kk) {
-    const float dkk = Lw[kk * LS + kk];
-    if (!(dkk > 0.f)) { ok = false; break; }  // uniform across the warp
-    const float lkk = sqrtf(dkk);
-    const float inv = 1.f / lkk;
-    __syncwarp();
-    for (int i = kk + 1 + lane; i < D; i += 32) Lw[i * LS + kk] *= inv;
-    if (lane == 0) Lw[kk * LS + kk] = lkk;
-    __syncwarp();
-    for (int i = kk + 1 + lane; i < D; i += 32) {
-      const float lik = Lw[i * LS + kk];
-      for (int j = kk + 1; j <= i; ++j) Lw[i * LS + j] = fmaf(-lik, Lw[j * LS + kk], Lw[i * LS + j]);
+#pragma unroll
+  for (int j = 0; j < W0; ++j) {
+    float c = 0.f;
+    if (live0 && j <= rr[0]) {
+      R v = M(j, rr[0]) - M(j, D) * (M(rr[0], D) * inv_om);
+      if (j == rr[0]) v += lp;
+      c = (float)v;
     }
-    __syncwarp();
+    L.a0[j] = c;
   }
-  if (!ok) {
+  if constexpr (NS == 2) {
+#pragma unroll
+    for (int j = 0; j < D; ++j) {
+      float c = 0.f;
+      if (j <= rr[NS - 1]) {
+        R v = M(j, rr[NS - 1]) - M(j, D) * (M(rr[NS - 1], D) * inv_om);
+        if (j == rr[NS - 1]) v += lp;
+        c = (float)v;
+      }
+      L.a1[j] = c;
+    }
+  }
+
+  // Factorisation, with the forward substitution (L z' = z) as an extra column.
+  chol_column<D, 0>(L, colbuf);
+  if (!L.ok) {
     if (lane == 0) atomicOr(status, kStatusNumerical);
-    for (int a = lane; a < D; a += 32) {
-      y_out[row * D + a] = __int_as_float(0x7fc00000);
-      kbar_out[row * D + a] = __int_as_float(0x7fc00000);
-    }
+    const float qn = __int_as_float(0x7fc00000);
+    for (int a = lane; a < D; a += 32) { y_out[row * D + a] = qn; kbar_out[row * D + a] = qn; }
     return;
   }
-  // L z = r
-  for (int j = 0; j < D; ++j) {
-    const float zj = rv[j] / Lw[j * LS + j];
-    __syncwarp();
-    for (int i = j + 1 + lane; i < D; i += 32) rv[i] = fmaf(-Lw[i * LS + j], zj, rv[i]);
-    if (lane == 0) rv[j] = zj;
-    __syncwarp();
+  // Backward substitution L^T y = z'.
+  float y0 = 0.f, y1 = 0.f;
+  back_row<D, D - 1>(L, y0, y1);
+  if (live0) {
+    y_out[row * D + rr[0]] = y0;
+    kbar_out[row * D + rr[0]] = kb[0];
   }
-  // L^T y = z
-  for (int j = D - 1; j >= 0; --j) {
-    const float yj = rv[j] / Lw[j * LS + j];
-    __syncwarp();
-    for (int i = lane; i < j; i += 32) rv[i] = fmaf(-Lw[j * LS + i], yj, rv[i]);
-    if (lane == 0) rv[j] = yj;
-    __syncwarp();
-  }
-  for (int a = lane; a < D; a += 32) {
-    y_out[row * D + a] = rv[a];
-    kbar_out[row * D + a] = kb[a];
+  if (NS == 2) {
+    y_out[row * D + rr[NS - 1]] = y1;
+    kbar_out[row * D + rr[NS - 1]] = kb[NS - 1];
   }
 }
 
 template <typename TIn, int D, bool PRECISE, int FMT = 0>
 cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
-  const size_t smem = sizeof(float) * kWarpsPerBlock * SolveCfg<D>::WARP_FLOATS;
+  const size_t smem = sizeof(float) * kWarpsPerBlock * SolveCfg<D, PRECISE, FMT>::WARP_FLOATS;
   auto kern = solve_kernel<TIn, D, PRECISE, FMT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
