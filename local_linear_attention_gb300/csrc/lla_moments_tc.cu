@@ -18,15 +18,20 @@
 //    S = Q K^T and P (cheap next to the 2 x 368-column contraction it feeds).
 // A first pass over the prefix computes the exact row max m_i (only S = Q K^T and a max).
 //
-// Warp roles (10 warps): 0 issues every tcgen05.mma (one thread) and owns the TMEM allocation;
-// 1 stages key blocks (32 keys x 64) into shared memory; 2-5 turn S into P (one thread per query,
-// = TMEM lane) and drain the accumulators after each pass; 6-9 generate the exact hi/lo feature
-// tiles for each key block (one lane per key) into shared memory. P lives in TMEM and is the A
+// Warp roles (18 warps): 0 issues every tcgen05.mma (one thread) and owns the TMEM allocation;
+// 1 stages key blocks (32 keys x 64) into shared memory; 2-9 turn S into P (one thread per query
+// = TMEM lane, two warps per lane quarter splitting the keys of a block) and drain the
+// accumulators after each pass; 10-17 generate the exact hi/lo feature tiles for each key block
+// (one lane per key) into shared memory. P and the feature tiles are triple-buffered. P lives in TMEM and is the A
 // operand of the feature contraction (tcgen05.mma with A in tensor memory). All operands in
 // shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is bounded.
 //
-// Output per query row (fp32): mom_tc[row][f] for f < 2208 (f < 64: sk, then the upper triangle
-// of S row by row, then zero padding), omega[row], m[row] = m_i / h and mraw[row] = m_i.
+// Feature order (2208 slots = 1104 pairs, the layout of each output row): the upper triangle of
+// kt kt^T for the augmented key kt = [k_0..k_63, 1, 0], row by row: for row a, the pairs
+// (a, b), (a, b+1) for even b from a (even a) or a+1 (odd a) up to 64 -- so one operand of each
+// packed product is a key word exactly as loaded -- then the 16 pairs of odd diagonal entries
+// (4u+1, 4u+1), (4u+3, 4u+3). Slot (a, 64) holds sum p k_a, slots (a, 65) are zero padding.
+// Output per query row (fp32): mom_tc[row][slot], omega[row], m[row] = m_i / h, mraw[row] = m_i.
 #include <cstdint>
 #include <type_traits>
 
@@ -41,22 +46,26 @@ using namespace tc;
 constexpr int D = 64;
 constexpr int BM = 128;                     // queries per CTA = MMA M = TMEM lanes
 constexpr int KB = 32;                      // keys per block
-constexpr int NF = D + D * (D + 1) / 2;     // 2144 features
 constexpr int NCH = 368;                    // features (accumulator columns) per pass
 constexpr int NPASS = 6;
 constexpr int NFP = NPASS * NCH;            // 2208, padded feature count (row stride of mom_tc)
 constexpr int GPP = NCH / 8;                // 46 groups of 8 features per pass
 constexpr int NA = 192, NB_ = NCH - NA;     // split of a pass into two MMAs (N <= 256)
-constexpr int KS = 4;                       // key-tile pipeline stages
-constexpr int NWARPS = 10;
+constexpr int KS = 6;                       // key-tile pipeline stages
+constexpr int KLAG = KS - 2;                // key blocks the loader keeps in flight
+constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
+constexpr int NFG = 8;                      // feature-generation warps
+constexpr int NWARPS = 2 + NSM + NFG;
 constexpr int NTHREADS = NWARPS * 32;
+constexpr int NBUF = 3;                     // P (TMEM) and F (shared memory) buffers
+constexpr int NSB = 3;                      // S buffers: Q K^T runs two key blocks ahead
 
 // tensor-memory columns
 constexpr uint32_t T_ACC = 0;
-constexpr uint32_t T_S = NCH;               // 2 x 32 columns of fp32 logits
-constexpr uint32_t T_P = T_S + 2 * KB;      // 2 x 16 columns of packed bf16 weights
+constexpr uint32_t T_S = NCH;               // NSB x 32 columns of fp32 logits
+constexpr uint32_t T_P = T_S + NSB * KB;    // NBUF x 16 columns of packed bf16 weights
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(T_P + 2 * (KB / 2) <= TMEM_COLS, "tensor memory budget");
+static_assert(T_P + NBUF * (KB / 2) <= TMEM_COLS, "tensor memory budget");
 
 // shared-memory layout (bytes)
 constexpr int SM_Q = 0;                              // 128 x 64 bf16, K-major core layout
@@ -65,18 +74,24 @@ constexpr int K_STAGE = KB * D * 2;
 constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
 constexpr int F_HALF = GPP * 512;
 constexpr int F_BUF = 2 * F_HALF;
-constexpr int SM_BAR = SM_F + 2 * F_BUF;
-constexpr int SMEM_BYTES = SM_BAR + 256;
+constexpr int SM_BAR = SM_F + NBUF * F_BUF;
+constexpr int SMEM_BYTES = SM_BAR + 2048;
 
-// Feature f -> (a, b); index D stands for the constant 1 (so f < 64 gives sk).
-struct Pair { int a, b; };
-__host__ __device__ constexpr Pair feature(int f) {
-  if (f < D) return Pair{f, D};
-  if (f >= NF) return Pair{-1, -1};
-  int u = f - D, a = 0;
-  while (u >= D - a) { u -= D - a; ++a; }
-  return Pair{a, a + u};
+// Pair p of the feature order (see the file comment): row a and even column b, or, for the odd
+// diagonal pairs, u = a.
+struct PairSpec { int a, b; bool diag; };
+constexpr int kRowPairs = 1088;
+__host__ __device__ constexpr PairSpec pair_spec(int p) {
+  if (p >= kRowPairs) return PairSpec{p - kRowPairs, 0, true};
+  int a = 0;
+  while (true) {
+    const int cnt = (a % 2 == 0) ? 33 - a / 2 : 32 - (a - 1) / 2;
+    if (p < cnt) return PairSpec{a, (a % 2 == 0 ? a : a + 1) + 2 * p, false};
+    p -= cnt;
+    ++a;
+  }
 }
+static_assert(2 * (kRowPairs + 16) == NFP, "feature order fills the padded row");
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t y) {
   uint32_t r;
@@ -99,37 +114,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Packs k[a0] (low half) and k[a1] (high half) from the key words kw (kw[t] = k[2t] | k[2t+1]<<16;
-// kw[32] holds two bf16 ones for the constant feature).
-template <int A0, int A1>
-__device__ __forceinline__ uint32_t gather2(const uint32_t (&kw)[33]) {
-  constexpr uint32_t s0 = (A0 & 1) ? 0x32u : 0x10u;
-  constexpr uint32_t s1 = (A1 & 1) ? 0x76u : 0x54u;
-  return __byte_perm(kw[A0 >> 1], kw[A1 >> 1], s0 | (s1 << 8));
-}
-
-// One group of 8 features (global feature index F0..F0+7) for this lane's key: 4 hi words and
-// 4 lo words, stored as one 16-byte row of the group's core matrix.
-template <int F0>
+// One group of 8 feature slots (pairs P0..P0+3) for this lane's key: 4 hi words and 4 lo words,
+// stored as one 16-byte row of the group's core matrix. kw[t] = k[2t] | k[2t+1] << 16 for t < 32,
+// kw[32] = bf16(1) | 0 << 16 (the constant feature and the zero pad).
+template <int P0>
 __device__ __forceinline__ void feature_group(const uint32_t (&kw)[33], uint8_t* hi_row,
                                               uint8_t* lo_row) {
   uint32_t h[4], l[4];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) { h[t] = 0u; l[t] = 0u; }
-  // unrolled at compile time through the helper below
   auto one = [&](auto tpair) {
     constexpr int T = decltype(tpair)::value;
-    constexpr Pair p0 = feature(F0 + 2 * T), p1 = feature(F0 + 2 * T + 1);
-    if constexpr (p0.a >= 0) {
-      constexpr int a1 = p1.a >= 0 ? p1.a : D, b1 = p1.a >= 0 ? p1.b : D;
-      const uint32_t x = gather2<p0.a, a1>(kw);
-      const uint32_t y = gather2<p0.b, b1>(kw);
-      uint32_t hv = bf16x2_mul(x, y);
-      uint32_t lv = bf16x2_fma(x, y, hv ^ 0x80008000u);
-      if constexpr (p1.a < 0) { hv &= 0xFFFFu; lv &= 0xFFFFu; }
-      h[T] = hv;
-      l[T] = lv;
+    constexpr PairSpec ps = pair_spec(P0 + T);
+    uint32_t x, y;
+    if constexpr (ps.diag) {  // (k[4u+1], k[4u+3]) squared
+      x = __byte_perm(kw[2 * ps.a], kw[2 * ps.a + 1], 0x7632);
+      y = x;
+    } else {                  // (k[a], k[a]) times (k[b], k[b+1])
+      x = __byte_perm(kw[ps.a >> 1], 0u, (ps.a & 1) ? 0x3232 : 0x1010);
+      y = kw[ps.b >> 1];
     }
+    const uint32_t hv = bf16x2_mul(x, y);
+    h[T] = hv;
+    l[T] = bf16x2_fma(x, y, hv ^ 0x80008000u);
   };
   one(std::integral_constant<int, 0>{});
   one(std::integral_constant<int, 1>{});
@@ -145,13 +150,14 @@ template <int PASS, int G0, int G1>
 __device__ __forceinline__ void feature_groups(const uint32_t (&kw)[33], uint8_t* fhi, uint8_t* flo,
                                                int row_off) {
   if constexpr (G0 < G1) {
-    feature_group<PASS * NCH + G0 * 8>(kw, fhi + G0 * 512 + row_off, flo + G0 * 512 + row_off);
+    feature_group<(PASS * NCH + G0 * 8) / 2>(kw, fhi + G0 * 512 + row_off, flo + G0 * 512 + row_off);
     feature_groups<PASS, G0 + 1, G1>(kw, fhi, flo, row_off);
   }
 }
 
-// Split of the 46 groups of a pass among the 4 feature warps: 12, 12, 11, 11.
-__host__ __device__ constexpr int fw_begin(int fw) { return fw < 2 ? 12 * fw : 24 + 11 * (fw - 2); }
+// Split of the 46 groups of a pass among the 8 feature warps: 6 x 6, then 2 x 5.
+__host__ __device__ constexpr int fw_begin(int fw) { return fw < 6 ? 6 * fw : 36 + 5 * (fw - 6); }
+static_assert(fw_begin(NFG) == GPP, "groups split");
 
 template <int PASS>
 __device__ __forceinline__ void generate_pass(int fw, const uint32_t (&kw)[33], uint8_t* fhi,
@@ -160,7 +166,11 @@ __device__ __forceinline__ void generate_pass(int fw, const uint32_t (&kw)[33], 
     case 0: feature_groups<PASS, fw_begin(0), fw_begin(1)>(kw, fhi, flo, row_off); break;
     case 1: feature_groups<PASS, fw_begin(1), fw_begin(2)>(kw, fhi, flo, row_off); break;
     case 2: feature_groups<PASS, fw_begin(2), fw_begin(3)>(kw, fhi, flo, row_off); break;
-    default: feature_groups<PASS, fw_begin(3), GPP>(kw, fhi, flo, row_off); break;
+    case 3: feature_groups<PASS, fw_begin(3), fw_begin(4)>(kw, fhi, flo, row_off); break;
+    case 4: feature_groups<PASS, fw_begin(4), fw_begin(5)>(kw, fhi, flo, row_off); break;
+    case 5: feature_groups<PASS, fw_begin(5), fw_begin(6)>(kw, fhi, flo, row_off); break;
+    case 6: feature_groups<PASS, fw_begin(6), fw_begin(7)>(kw, fhi, flo, row_off); break;
+    default: feature_groups<PASS, fw_begin(7), GPP>(kw, fhi, flo, row_off); break;
   }
 }
 
@@ -189,9 +199,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
 
 struct Barriers {
   uint64_t kfull[KS], kempty[KS];
-  uint64_t sfull[2], sfree[2];
-  uint64_t pfull[2], ffull[2], pfree[2];
-  uint64_t accfull, accfree, done;
+  uint64_t sfull[NSB], sfree[NSB];
+  uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];
+  uint64_t accfull, accfree, done, rowx;
+  float part[2][BM];  // per-row partial results of the two softmax halves (max, then omega)
 };
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -223,17 +234,20 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     *reinterpret_cast<uint4*>(smem + SM_Q + kmaj_off(r, c)) = v;
   }
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 5); }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 1 + NFG); }
+    for (int s = 0; s < NSB; ++s) {
       mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], 4);
-      mbar_init(&bar.pfull[s], 4);
-      mbar_init(&bar.ffull[s], 4);
+      mbar_init(&bar.sfree[s], NSM);
+    }
+    for (int s = 0; s < NBUF; ++s) {
+      mbar_init(&bar.pfull[s], NSM);
+      mbar_init(&bar.ffull[s], NFG);
       mbar_init(&bar.pfree[s], 1);
     }
     mbar_init(&bar.accfull, 1);
-    mbar_init(&bar.accfree, 4);
+    mbar_init(&bar.accfree, NSM);
     mbar_init(&bar.done, 1);
+    mbar_init(&bar.rowx, NSM);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -252,45 +266,58 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(smem + SM_Q);
-      const uint32_t k_addr = smem_u32(smem + SM_K);
-      const uint32_t f_addr = smem_u32(smem + SM_F);
+      // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
+      // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
+      const uint64_t qd = smem_desc(smem_u32(smem + SM_Q), 128, 1024);
+      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
+      const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
       constexpr uint32_t id_qk = idesc_bf16(BM, KB, false, false);
       constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
       constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
+      const uint32_t t_acc = tbase + T_ACC, t_s = tbase + T_S, t_p = tbase + T_P;
       bool ok = true;
-      for (int g = 0; g <= G && ok; ++g) {
+      // Iteration g issues Q K^T of step g and the feature contraction of step g - 2, so the
+      // softmax warps have two steps of tensor work in which to turn S(g) into P(g).
+      for (int g = 0; g <= G + 1 && ok; ++g) {
         if (g < G) {
-          const int st = g % KS, sb = g & 1;
+          const int st = g % KS, sb = g % NSB;
           ok = mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p);
-          if (ok && g >= 2) ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, TO, abort_p);
+          if (ok && g >= NSB)
+            ok = mbar_wait(&bar.sfree[sb], ((g / NSB) - 1) & 1, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
-          for (int s = 0; s < D / 16; ++s)
-            mma_ss(tbase + T_S + sb * KB, smem_desc(q_addr + s * 256, 128, 1024),
-                   smem_desc(k_addr + st * K_STAGE + s * 256, 128, 1024), id_qk, s > 0);
+          const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
+          const uint32_t ts = t_s + sb * KB;
+          mma_ss(ts, qd, kst, id_qk, 0u);
+          mma_ss(ts, qd + 16, kst + 16, id_qk, 1u);
+          mma_ss(ts, qd + 32, kst + 32, id_qk, 1u);
+          mma_ss(ts, qd + 48, kst + 48, id_qk, 1u);
           mma_commit(&bar.sfull[sb]);
           mma_commit(&bar.kempty[st]);
         }
-        if (g >= nb + 1) {
-          const int h = g - 1 - nb, pb = h & 1, pass = h / nb, b = h % nb;
-          ok = mbar_wait(&bar.pfull[pb], (h >> 1) & 1, status, TO, abort_p) &&
-               mbar_wait(&bar.ffull[pb], (h >> 1) & 1, status, TO, abort_p);
+        if (g >= nb + 2) {
+          const int h = g - 2 - nb, pb = h % NBUF, pass = h / nb, b = h % nb;
+          const uint32_t ph = (h / NBUF) & 1;
+          ok = mbar_wait(&bar.pfull[pb], ph, status, TO, abort_p) &&
+               mbar_wait(&bar.ffull[pb], ph, status, TO, abort_p);
           if (ok && b == 0 && pass >= 1)
             ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t fh = f_addr + pb * F_BUF, fl = fh + F_HALF;
-#pragma unroll
-          for (int s = 0; s < KB / 16; ++s) {
-            const uint32_t a_tm = tbase + T_P + pb * (KB / 2) + s * 8;
-            const uint32_t acc0 = (b > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_ACC, a_tm, smem_desc(fh + s * 256, 128, 512), id_a, acc0);
-            mma_ts(tbase + T_ACC, a_tm, smem_desc(fl + s * 256, 128, 512), id_a, 1u);
-            mma_ts(tbase + T_ACC + NA, a_tm, smem_desc(fh + (NA / 8) * 512 + s * 256, 128, 512), id_b, acc0);
-            mma_ts(tbase + T_ACC + NA, a_tm, smem_desc(fl + (NA / 8) * 512 + s * 256, 128, 512), id_b, 1u);
-          }
+          const uint64_t fh = fd + (uint64_t)(pb * (F_BUF >> 4));
+          const uint64_t fl = fh + (F_HALF >> 4);
+          constexpr uint32_t nb_off = (NA / 8) * 512 / 16;
+          const uint32_t a0 = t_p + pb * (KB / 2);
+          const uint32_t acc0 = b > 0 ? 1u : 0u;
+          // K-step 0 (keys 0..15), then K-step 1 (keys 16..31; +256 B in the F tiles)
+          mma_ts(t_acc, a0, fh, id_a, acc0);
+          mma_ts(t_acc, a0, fl, id_a, 1u);
+          mma_ts(t_acc + NA, a0, fh + nb_off, id_b, acc0);
+          mma_ts(t_acc + NA, a0, fl + nb_off, id_b, 1u);
+          mma_ts(t_acc, a0 + 8, fh + 16, id_a, 1u);
+          mma_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
+          mma_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
+          mma_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
           mma_commit(&bar.pfree[pb]);
           if (b == nb - 1) mma_commit(&bar.accfull);
         }
@@ -305,55 +332,83 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
+    // cp.async 16-byte copies, several key blocks in flight. Lane -> (row, chunk) mapping:
+    // rows (lane & 7) + 8 * (t & 3), chunks (lane >> 3) + 4 * (t >> 2): each 8-lane phase writes
+    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors.
+    // A block becomes visible to the MMA (async proxy) only after its copies completed and this
+    // warp fenced them (cp.async writes belong to the generic proxy).
     const __nv_bfloat16* kb = k + base * D;
-    for (int g = 0; g < G; ++g) {
-      const int st = g % KS, b = g % nb;
-      if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
-      uint8_t* dst = smem + SM_K + st * K_STAGE;
+    bool ok = true;
+    for (int g = 0; g < G + KLAG; ++g) {
+      if (g < G) {
+        const int st = g % KS, b = g % nb;
+        if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = smem + SM_K + st * K_STAGE;
 #pragma unroll
-      for (int t = 0; t < (KB * D / 8) / 32; ++t) {
-        const int e = lane + 32 * t, r = e >> 3, c = e & 7, j = b * KB + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (j < jend) v = *reinterpret_cast<const uint4*>(kb + (long long)j * D + c * 8);
-        *reinterpret_cast<uint4*>(dst + kmaj_off(r, c)) = v;
+        for (int t = 0; t < 8; ++t) {
+          const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+          const int j = b * KB + r;
+          const bool in = j < jend;
+          cp_async16(dst + kmaj_off(r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
+        }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.kfull[st]);
+      cp_async_commit();
+      if (g >= KLAG) {
+        cp_async_wait<KLAG>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.kfull[(g - KLAG) % KS]);
+      }
     }
-  } else if (warp < 6) {
+    if (!ok) cp_async_wait<0>();
+  } else if (warp < 2 + NSM) {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int quarter = warp & 3;
+    // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
+    // accumulator columns [0, NA); half 1 takes keys 16..31 and columns [NA, NCH). Row max and
+    // omega are combined across the halves through shared memory (barrier rowx: phase 0 after the
+    // max pass, phase 1 at the end).
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const int c_lo = half * (KB / 2);
     const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
     float m = -INFINITY, om = 0.f;
+    bool ok = true;
     for (int g = 0; g < G; ++g) {
-      const int sb = g & 1;
-      if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) break;
+      const int sb = g % NSB;
+      if (!warp_wait(&bar.sfull[sb], (g / NSB) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[KB];
-      tmem_ld16(lane_base + T_S + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-      tmem_ld16(lane_base + T_S + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+      uint32_t sv[KB / 2];
+      tmem_ld16(lane_base + T_S + sb * KB + c_lo, sv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.sfree[sb]);
       const int b = g % nb;
-      const int j0 = b * KB;
+      const int j0 = b * KB + c_lo;
       if (g < nb) {  // max pass
 #pragma unroll
-        for (int c = 0; c < KB; ++c)
+        for (int c = 0; c < KB / 2; ++c)
           if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+        if (g == nb - 1) {  // combine the two halves' row maxima
+          bar.part[half][r] = m;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.rowx);
+          if (!warp_wait(&bar.rowx, 0, status, abort_p)) { ok = false; break; }
+          m = fmaxf(m, bar.part[half ^ 1][r]);
+        }
         continue;
       }
-      const int h = g - nb, pass = h / nb, pb = h & 1;
+      const int h = g - nb, pass = h / nb, pb = h % NBUF;
       const float mc = m * c2;
-      uint32_t pw[KB / 2];
+      uint32_t pw[KB / 4];
 #pragma unroll
-      for (int c = 0; c < KB; c += 2) {
+      for (int c = 0; c < KB / 2; c += 2) {
         const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
         const float p1 =
             (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
@@ -361,23 +416,24 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
       if (pass == 0) {
 #pragma unroll
-        for (int c = 0; c < KB / 2; ++c)
+        for (int c = 0; c < KB / 4; ++c)
           om += __uint_as_float(pw[c] << 16) + __uint_as_float(pw[c] & 0xFFFF0000u);
       }
-      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) break;
+      if (h >= NBUF &&
+          !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
-      tmem_st8(lane_base + T_P + pb * (KB / 2), *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
-      tmem_st8(lane_base + T_P + pb * (KB / 2) + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
+      tmem_st8(lane_base + T_P + pb * (KB / 2) + half * (KB / 4), pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.pfull[pb]);
-      if (b == nb - 1) {  // end of a pass: drain the accumulators
-        if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) break;
+      if (b == nb - 1) {  // end of a pass: drain this half's accumulator columns
+        if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) { ok = false; break; }
         tc_fence_after();
         float* dst = mom + (base + i) * NFP + pass * NCH;
+        const int e0 = half ? NA : 0, e1 = half ? NCH : NA;
 #pragma unroll 1
-        for (int c0 = 0; c0 < NCH; c0 += 16) {
+        for (int c0 = e0; c0 < e1; c0 += 16) {
           uint32_t v[16];
           tmem_ld16(lane_base + T_ACC + c0, v);
           tmem_ld_wait();
@@ -393,14 +449,19 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         if (lane == 0) mbar_arrive(&bar.accfree);
       }
     }
-    if (valid) {
-      m_out[base + i] = m * inv_h;
-      mraw_out[base + i] = m;
-      omega_out[base + i] = om;
+    if (ok) {  // combine the halves' omega
+      bar.part[half][r] = om;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.rowx);
+      if (warp_wait(&bar.rowx, 1, status, abort_p) && half == 0 && valid) {
+        m_out[base + i] = m * inv_h;
+        mraw_out[base + i] = m;
+        omega_out[base + i] = om + bar.part[1][r];
+      }
     }
   } else {
     // ------------------------------------------------------------------ feature generation
-    const int fw = warp - 6;
+    const int fw = warp - 2 - NSM;
     const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;
     for (int g = 0; g < G; ++g) {
       const int st = g % KS;
@@ -410,7 +471,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         if (lane == 0) mbar_arrive(&bar.kempty[st]);
         continue;
       }
-      const int h = g - nb, pass = h / nb, pb = h & 1;
+      const int h = g - nb, pass = h / nb, pb = h % NBUF;
       uint32_t kw[33];
       const uint8_t* krow = smem + SM_K + st * K_STAGE;
 #pragma unroll
@@ -418,10 +479,10 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const uint4 v = *reinterpret_cast<const uint4*>(krow + kmaj_off(lane, c));
         kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
       }
-      kw[32] = 0x3F803F80u;  // two bf16 ones
+      kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.kempty[st]);
-      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) break;
+      if (h >= NBUF && !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) break;
       uint8_t* fhi = smem + SM_F + pb * F_BUF;
       generate(pass, fw, kw, fhi, fhi + F_HALF, row_off);
       fence_proxy_async_smem();

@@ -33,7 +33,8 @@ constexpr int D = 64;
 constexpr int DV = 64;
 constexpr int BM = 128;
 constexpr int KB = 32;
-constexpr int KS = 4;
+constexpr int KS = 6;
+constexpr int KLAG = KS - 2;
 constexpr int NWARPS = 6;
 constexpr int NTHREADS = NWARPS * 32;
 
@@ -161,10 +162,17 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (warp == 0) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(smem + SM_Q), y_addr = smem_u32(smem + SM_Y);
-      const uint32_t k_addr = smem_u32(smem + SM_K), v_addr = smem_u32(smem + SM_V);
+      // Base descriptors plus start-address offsets in 16-byte units (see the moments stage).
+      const uint64_t qd = smem_desc(smem_u32(smem + SM_Q), 128, 1024);
+      const uint64_t yd = smem_desc(smem_u32(smem + SM_Y), 128, 1024);
+      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
+      // V block as the MN-major B operand: K = keys (8-key groups 1024 B apart), N = value
+      // features (8-feature groups 128 B apart).
+      const uint64_t vd = smem_desc(smem_u32(smem + SM_V), 1024, 128);
       constexpr uint32_t id_s = idesc_bf16(BM, KB, false, false);
       constexpr uint32_t id_o = idesc_bf16(BM, DV, false, true);
+      constexpr uint32_t tile16 = TILE >> 4, stage16 = KV_STAGE >> 4;
+      const uint32_t t_s = tbase + T_S, t_t = tbase + T_T;
       bool ok = true;
       for (int g = 0; g <= nb && ok; ++g) {
         if (g < nb) {
@@ -174,17 +182,16 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, kStatusTimeout, abort_p);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kb = k_addr + st * KV_STAGE;
+          const uint64_t kst = kd + (uint64_t)(st * stage16);
+          const uint32_t ts = t_s + sb * KB, tt = t_t + sb * KB;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s)
-            mma_ss(tbase + T_S + sb * KB, smem_desc(q_addr + s * 256, 128, 1024),
-                   smem_desc(kb + s * 256, 128, 1024), id_s, s > 0);
+          for (int s = 0; s < D / 16; ++s) mma_ss(ts, qd + 16 * s, kst + 16 * s, id_s, s > 0);
 #pragma unroll
           for (int part = 0; part < 3; ++part)
 #pragma unroll
             for (int s = 0; s < D / 16; ++s)
-              mma_ss(tbase + T_T + sb * KB, smem_desc(y_addr + part * TILE + s * 256, 128, 1024),
-                     smem_desc(kb + s * 256, 128, 1024), id_s, (part > 0 || s > 0) ? 1u : 0u);
+              mma_ss(tt, yd + part * tile16 + 16 * s, kst + 16 * s, id_s,
+                     (part > 0 || s > 0) ? 1u : 0u);
           mma_commit(&bar.sfull[sb]);
         }
         if (g >= 1) {
@@ -192,16 +199,14 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           ok = mbar_wait(&bar.pfull[pb], (h >> 1) & 1, status, kStatusTimeout, abort_p);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vb = v_addr + st * KV_STAGE;
+          const uint64_t vst = vd + (uint64_t)(st * stage16);
 #pragma unroll
           for (int s = 0; s < KB / 16; ++s) {
-            // V block as the MN-major B operand: K = keys (8-key groups 1024 B apart),
-            // N = value features (8-feature groups 128 B apart).
-            const uint64_t vd = smem_desc(vb + s * 2048, 1024, 128);
+            const uint64_t vds = vst + (uint64_t)(s * (2048 >> 4));
             const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_O1, tbase + T_P + pb * 16 + s * 8, vd, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2H + pb * 16 + s * 8, vd, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2L + pb * 16 + s * 8, vd, id_o, 1u);
+            mma_ts(tbase + T_O1, tbase + T_P + pb * 16 + s * 8, vds, id_o, acc);
+            mma_ts(tbase + T_O2, tbase + T_P2H + pb * 16 + s * 8, vds, id_o, acc);
+            mma_ts(tbase + T_O2, tbase + T_P2L + pb * 16 + s * 8, vds, id_o, 1u);
           }
           mma_commit(&bar.pfree[pb]);
           mma_commit(&bar.kvempty[st]);
@@ -216,28 +221,39 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V loader
-    const __nv_bfloat16* kb = k + base * D;
+    // cp.async copies with several blocks in flight; same conflict-free lane mapping and
+    // completion -> proxy fence -> arrive protocol as the moments stage's loader.
+    const __nv_bfloat16* kbp = k + base * D;
     const __nv_bfloat16* vbp = v + base * DV;
-    for (int g = 0; g < nb; ++g) {
-      const int st = g % KS;
-      if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
-      uint8_t* kd = smem + SM_K + st * KV_STAGE;
-      uint8_t* vd = smem + SM_V + st * KV_STAGE;
-#pragma unroll
-      for (int t = 0; t < (KB * D / 8) / 32; ++t) {
-        const int e = lane + 32 * t, r = e >> 3, c = e & 7, j = g * KB + r;
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-        if (j < jend) {
-          kv = *reinterpret_cast<const uint4*>(kb + (long long)j * D + c * 8);
-          vv = *reinterpret_cast<const uint4*>(vbp + (long long)j * DV + c * 8);
+    bool ok = true;
+    for (int g = 0; g < nb + KLAG; ++g) {
+      if (g < nb) {
+        const int st = g % KS;
+        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
+          ok = false;
+          break;
         }
-        *reinterpret_cast<uint4*>(kd + kmaj_off(r, c)) = kv;
-        *reinterpret_cast<uint4*>(vd + kmaj_off(r, c)) = vv;
+        uint8_t* kd = smem + SM_K + st * KV_STAGE;
+        uint8_t* vd = smem + SM_V + st * KV_STAGE;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+          const int j = g * KB + r;
+          const bool in = j < jend;
+          const long long jj = in ? j : 0;
+          cp_async16(kd + kmaj_off(r, c), kbp + jj * D + c * 8, in ? 16u : 0u);
+          cp_async16(vd + kmaj_off(r, c), vbp + jj * DV + c * 8, in ? 16u : 0u);
+        }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.kvfull[st]);
+      cp_async_commit();
+      if (g >= KLAG) {
+        cp_async_wait<KLAG>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.kvfull[(g - KLAG) % KS]);
+      }
     }
+    if (!ok) cp_async_wait<0>();
   } else {
     // ------------------------------------------------------------------ weights + output
     const int quarter = warp & 3;

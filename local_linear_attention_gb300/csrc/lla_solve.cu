@@ -54,28 +54,40 @@ mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, 
 constexpr int kWarpsPerBlock = 4;
 
 // Moment layouts: FMT 0 = augmented-Gram 4x4 blocks (CUDA-core stage, gram_floats(D) per row, plus
-// as many compensation terms for fp32 inputs); FMT 1 = tensor-core stage ([sk (D) | upper
-// triangle of S row by row], TC_ROW floats per row, omega in its own array).
+// as many compensation terms for fp32 inputs); FMT 1 = tensor-core stage (d = 64, TC_ROW floats
+// per row in the order tc_slot() decodes, omega in its own array).
 constexpr int TC_ROW = 2208;
+
+// Slot of feature (a, b), a <= b <= 64, in a tensor-core moment row (the tensor-core moments
+// stage documents the order: row pairs (a, b), (a, b+1) for even b, then odd diagonal pairs).
+__device__ __forceinline__ int tc_slot(int a, int b) {
+  if (a == b && (a & 1)) return 2 * (1088 + ((a - 1) >> 2)) + (((a - 1) >> 1) & 1);
+  const int t = a >> 1;
+  int rs = 65 * t - t * (t - 1);
+  if (a & 1) rs += 33 - t;
+  const int b0 = a + (a & 1);
+  return 2 * (rs + ((b - b0) >> 1)) + ((b - b0) & 1);
+}
 
 template <int D, int FMT>
 __device__ __forceinline__ int moff(int a, int b) {  // a <= b; b == D means the constant 1
   if (FMT == 0) return gram_block_index(D, a >> 2, b >> 2) * 16 + (a & 3) * 4 + (b & 3);
-  if (b == D) return a;
-  return D + a * D - a * (a - 1) / 2 + (b - a);
+  return tc_slot(a, b);
 }
 
 template <int D, bool PRECISE, int FMT>
 struct SolveCfg {
   static constexpr int ROW = FMT == 0 ? gram_floats(D) : TC_ROW;   // floats of one moment row
   static constexpr int STAGE = (PRECISE ? 2 : 1) * ROW;             // staged per warp (hi [+ lo])
-  static constexpr int WARP_FLOATS = STAGE + 2 * 64;                // + two column buffers
+  static constexpr int BUF = STAGE > D * 64 ? STAGE : D * 64;       // then reused for L's rows
+  static constexpr int WARP_FLOATS = BUF + 2 * 64;                  // + two column buffers
   static constexpr int NSLOT = D == 64 ? 2 : 1;                     // rows per lane
 };
 
-// State of one lane during the factorisation: its rows, their entries (slot 0: row rr0 < 32,
-// entries 0..W0-1; slot 1 (d = 64 only): row rr1 = 63 - lane, entries 0..63), right-hand sides and
-// diagonal entries of the factor.
+// State of one lane during the factorisation: its rows (slot 0: row rr0 = lane, entries
+// 0..W0-1; slot 1 (d = 64 only): row rr1 = 63 - lane, entries 0..63), right-hand sides and the
+// reciprocals of the factor's diagonal for those rows. Entries beyond a row's diagonal are
+// padding: they are updated along with the rest (that is cheaper than masking them) and never read.
 template <int D>
 struct CholLane {
   static constexpr int NS = D == 64 ? 2 : 1;
@@ -83,13 +95,14 @@ struct CholLane {
   static constexpr int W1 = NS == 2 ? D : 1;
   float a0[W0], a1[W1];
   float z[NS];
-  float ldiag[NS];
+  float invd[NS];
   int rr0, rr1;
   bool live0;
   bool ok;
 };
 
-// Column K of the right-looking factorisation (template recursion keeps every index static).
+// Column K of the right-looking factorisation, with the forward substitution as an extra column
+// (template recursion keeps every register index static).
 template <int D, int K>
 __device__ __forceinline__ void chol_column(CholLane<D>& L, float* colbuf) {
   constexpr int NS = CholLane<D>::NS, W0 = CholLane<D>::W0;
@@ -98,64 +111,65 @@ __device__ __forceinline__ void chol_column(CholLane<D>& L, float* colbuf) {
   const float mine = second ? L.a1[NS == 2 ? K : 0] : L.a0[K < W0 ? K : 0];
   float piv = __shfl_sync(0xffffffffu, mine, owner);
   if (!(piv > 0.f)) { L.ok = false; piv = 1.f; }  // rows of a failed factorisation become NaN
-  const float lkk = sqrtf(piv), inv = 1.f / lkk;
+  const float inv = rsqrtf(piv), lkk = piv * inv;
   const float zk = __shfl_sync(0xffffffffu, second ? L.z[NS - 1] : L.z[0], owner) * inv;
   float* cb = colbuf + (K & 1) * 64;
   if constexpr (K < W0) {
-    if (L.live0) {
-      if (L.rr0 > K) L.a0[K] *= inv;
-      if (L.rr0 == K) { L.a0[K] = lkk; L.ldiag[0] = lkk; L.z[0] = zk; }
-      cb[L.rr0] = L.a0[K];
-    }
+    L.a0[K] *= inv;  // L[rr0][K] below the diagonal (padding above it)
+    if (L.rr0 == K) { L.a0[K] = lkk; L.invd[0] = inv; L.z[0] = zk; }
+    if (L.live0) cb[L.rr0] = L.a0[K];
   }
   if constexpr (NS == 2) {
-    if (L.rr1 > K) L.a1[K] *= inv;
-    if (L.rr1 == K) { L.a1[K] = lkk; L.ldiag[NS - 1] = lkk; L.z[NS - 1] = zk; }
+    L.a1[K] *= inv;
+    if (L.rr1 == K) { L.a1[K] = lkk; L.invd[NS - 1] = inv; L.z[NS - 1] = zk; }
     cb[L.rr1] = L.a1[K];
   }
   __syncwarp();
+  // trailing update (rows at or above K only touch their padding), column read 4 at a time
   if constexpr (K + 1 < W0) {
-    if (L.live0 && L.rr0 > K) {
-      const float lik = L.a0[K];
+    const float lik = L.a0[K];
 #pragma unroll
-      for (int j = K + 1; j < W0; ++j)
-        if (j <= L.rr0) L.a0[j] = fmaf(-lik, cb[j], L.a0[j]);
-      L.z[0] = fmaf(-lik, zk, L.z[0]);
+    for (int jb = (K + 1) / 4; jb < W0 / 4; ++jb) {
+      const float4 c4 = reinterpret_cast<const float4*>(cb)[jb];
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (4 * jb + u > K) L.a0[4 * jb + u] = fmaf(-lik, cv[u], L.a0[4 * jb + u]);
     }
+    if (L.rr0 > K) L.z[0] = fmaf(-lik, zk, L.z[0]);
   }
   if constexpr (NS == 2) {
-    if (L.rr1 > K) {
-      const float lik = L.a1[K];
+    const float lik = L.a1[K];
 #pragma unroll
-      for (int j = K + 1; j < D; ++j)
-        if (j <= L.rr1) L.a1[j] = fmaf(-lik, cb[j], L.a1[j]);
-      L.z[NS - 1] = fmaf(-lik, zk, L.z[NS - 1]);
+    for (int jb = (K + 1) / 4; jb < D / 4; ++jb) {
+      const float4 c4 = reinterpret_cast<const float4*>(cb)[jb];
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (4 * jb + u > K) L.a1[4 * jb + u] = fmaf(-lik, cv[u], L.a1[4 * jb + u]);
     }
+    if (L.rr1 > K) L.z[NS - 1] = fmaf(-lik, zk, L.z[NS - 1]);
   }
   if constexpr (K + 1 < D) chol_column<D, K + 1>(L, colbuf);
 }
 
-// Row K of the backward substitution L^T y = z (K runs from D-1 down to 0).
+// Backward substitution L^T y = z', column by column from the last row: y_k = w_k / L[k][k],
+// then w_m -= L[k][m] y_k for m < k. Rows of L are read from shared memory (Lrows[k * 64 + m]).
 template <int D, int K>
-__device__ __forceinline__ void back_row(const CholLane<D>& L, float& y0, float& y1) {
-  constexpr int NS = CholLane<D>::NS, W0 = CholLane<D>::W0;
-  float part = 0.f;
-  if constexpr (K < W0) {
-    if (L.live0 && L.rr0 > K) part = fmaf(L.a0[K], y0, part);
-  }
-  if constexpr (NS == 2) {
-    if (L.rr1 > K) part = fmaf(L.a1[K], y1, part);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+__device__ __forceinline__ void back_column(const CholLane<D>& L, const float* Lrows, float& w0,
+                                            float& w1, float& y0, float& y1) {
+  constexpr int NS = CholLane<D>::NS;
   constexpr bool second = NS == 2 && K >= 32;
   constexpr int owner = second ? D - 1 - K : K;
-  const float num = __shfl_sync(0xffffffffu, second ? L.z[NS - 1] : L.z[0], owner);
-  const float dk = __shfl_sync(0xffffffffu, second ? L.ldiag[NS - 1] : L.ldiag[0], owner);
-  const float yk = (num - part) / dk;
+  const float l0 = Lrows[K * 64 + L.rr0];
+  const float l1 = NS == 2 ? Lrows[K * 64 + L.rr1] : 0.f;
+  const float own = second ? w1 * L.invd[NS - 1] : w0 * L.invd[0];
+  const float yk = __shfl_sync(0xffffffffu, own, owner);
   if (L.rr0 == K) y0 = yk;
   if (NS == 2 && L.rr1 == K) y1 = yk;
-  if constexpr (K > 0) back_row<D, K - 1>(L, y0, y1);
+  if (L.rr0 < K) w0 = fmaf(-l0, yk, w0);
+  if (NS == 2 && L.rr1 < K) w1 = fmaf(-l1, yk, w1);
+  if constexpr (K > 0) back_column<D, K - 1>(L, Lrows, w0, w1, y0, y1);
 }
 
 // One warp solves (C_kk + lambda' I) y = q - kbar for one query, C_kk = S - s s^T / omega from that
@@ -164,7 +178,7 @@ __device__ __forceinline__ void back_row(const CholLane<D>& L, float& y0, float&
 // the factor is broadcast through shared memory; the forward substitution rides along as an extra
 // column of the factorisation; the backward substitution reduces across the warp.
 template <typename TIn, int D, bool PRECISE, int FMT>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 3)
 solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
              const float* __restrict__ mom, const float* __restrict__ mom_lo,
              const float* __restrict__ omega, const float* __restrict__ mrow, int T,
@@ -177,8 +191,8 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* g = smem + warp * C::WARP_FLOATS;  // staged moment row (hi, then lo)
-  float* colbuf = g + C::STAGE;             // [2][64]
+  float* g = smem + warp * C::WARP_FLOATS;  // staged moment row (hi, then lo); later L's rows
+  float* colbuf = g + C::BUF;               // [2][64]
   const long long row = (long long)blockIdx.x * kWarpsPerBlock + warp;
   if (row >= rows) return;  // whole warp leaves together
   const long long bh = row / T;
@@ -220,7 +234,7 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   float kb[NS];
 #pragma unroll
   for (int t = 0; t < NS; ++t) {
-    L.ldiag[t] = 1.f;
+    L.invd[t] = 1.f;
     const int r = rr[t];
     if (t == 0 && !live0) { L.z[0] = 0.f; kb[0] = 0.f; continue; }
     const R sr = M(r, D);
@@ -252,6 +266,7 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   }
 
   // Factorisation, with the forward substitution (L z' = z) as an extra column.
+  __syncwarp();  // every lane is done with the staged moments; the buffer now holds L's rows
   chol_column<D, 0>(L, colbuf);
   if (!L.ok) {
     if (lane == 0) atomicOr(status, kStatusNumerical);
@@ -259,9 +274,24 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
     for (int a = lane; a < D; a += 32) { y_out[row * D + a] = qn; kbar_out[row * D + a] = qn; }
     return;
   }
+  // This lane's rows of L to shared memory (row-major, 64 floats per row).
+  float* Lrows = g;
+  if (live0) {
+#pragma unroll
+    for (int j = 0; j < W0; j += 4)
+      *reinterpret_cast<float4*>(Lrows + rr[0] * 64 + j) =
+          make_float4(L.a0[j], L.a0[j + 1], L.a0[j + 2], L.a0[j + 3]);
+  }
+  if constexpr (NS == 2) {
+#pragma unroll
+    for (int j = 0; j < D; j += 4)
+      *reinterpret_cast<float4*>(Lrows + rr[NS - 1] * 64 + j) =
+          make_float4(L.a1[j], L.a1[j + 1], L.a1[j + 2], L.a1[j + 3]);
+  }
+  __syncwarp();
   // Backward substitution L^T y = z'.
-  float y0 = 0.f, y1 = 0.f;
-  back_row<D, D - 1>(L, y0, y1);
+  float w0 = L.z[0], w1 = L.z[NS - 1], y0 = 0.f, y1 = 0.f;
+  back_column<D, D - 1>(L, Lrows, w0, w1, y0, y1);
   if (live0) {
     y_out[row * D + rr[0]] = y0;
     kbar_out[row * D + rr[0]] = kb[0];
