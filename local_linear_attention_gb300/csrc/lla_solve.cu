@@ -13,6 +13,7 @@
 #include <type_traits>
 
 #include "lla_internal.cuh"
+#include "lla_tc_ptx.cuh"
 
 namespace lla {
 namespace {
@@ -79,7 +80,8 @@ template <int D, bool PRECISE, int FMT>
 struct SolveCfg {
   static constexpr int ROW = FMT == 0 ? gram_floats(D) : TC_ROW;   // floats of one moment row
   static constexpr int STAGE = (PRECISE ? 2 : 1) * ROW;             // staged per warp (hi [+ lo])
-  static constexpr int BUF = STAGE > D * 64 ? STAGE : D * 64;       // then reused for L's rows
+  static constexpr int LS = 68;                                     // row stride of L in smem
+  static constexpr int BUF = STAGE > D * LS ? STAGE : D * LS;       // then reused for L's rows
   static constexpr int WARP_FLOATS = BUF + 2 * 64;                  // + two column buffers
   static constexpr int NSLOT = D == 64 ? 2 : 1;                     // rows per lane
 };
@@ -154,15 +156,15 @@ __device__ __forceinline__ void chol_column(CholLane<D>& L, float* colbuf) {
 }
 
 // Backward substitution L^T y = z', column by column from the last row: y_k = w_k / L[k][k],
-// then w_m -= L[k][m] y_k for m < k. Rows of L are read from shared memory (Lrows[k * 64 + m]).
+// then w_m -= L[k][m] y_k for m < k. Rows of L are read from shared memory (Lrows[k * 68 + m]).
 template <int D, int K>
 __device__ __forceinline__ void back_column(const CholLane<D>& L, const float* Lrows, float& w0,
                                             float& w1, float& y0, float& y1) {
   constexpr int NS = CholLane<D>::NS;
   constexpr bool second = NS == 2 && K >= 32;
   constexpr int owner = second ? D - 1 - K : K;
-  const float l0 = Lrows[K * 64 + L.rr0];
-  const float l1 = NS == 2 ? Lrows[K * 64 + L.rr1] : 0.f;
+  const float l0 = Lrows[K * 68 + L.rr0];
+  const float l1 = NS == 2 ? Lrows[K * 68 + L.rr1] : 0.f;
   const float own = second ? w1 * L.invd[NS - 1] : w0 * L.invd[0];
   const float yk = __shfl_sync(0xffffffffu, own, owner);
   if (L.rr0 == K) y0 = yk;
@@ -197,15 +199,21 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   if (row >= rows) return;  // whole warp leaves together
   const long long bh = row / T;
 
-  // Stage the moment row with 16-byte loads (rows are 16-byte aligned: ROW % 4 == 0).
+  // Stage the moment row with 16-byte asynchronous copies, all in flight at once before the one
+  // wait (rows are 16-byte aligned: ROW % 4 == 0).
   {
     const float4* src = reinterpret_cast<const float4*>(mom + row * C::ROW);
     float4* dst = reinterpret_cast<float4*>(g);
-    for (int t = lane; t < C::ROW / 4; t += 32) dst[t] = src[t];
+    constexpr int NV = C::ROW / 4;
+#pragma unroll 1
+    for (int t = lane; t < NV; t += 32) tc::cp_async16(dst + t, src + t, 16u);
     if (PRECISE) {
       const float4* srl = reinterpret_cast<const float4*>(mom_lo + row * C::ROW);
-      for (int t = lane; t < C::ROW / 4; t += 32) dst[C::ROW / 4 + t] = srl[t];
+#pragma unroll 1
+      for (int t = lane; t < NV; t += 32) tc::cp_async16(dst + NV + t, srl + t, 16u);
     }
+    tc::cp_async_commit();
+    tc::cp_async_wait<0>();
   }
   __syncwarp();
   auto M = [&](int a, int b) -> R {  // moment entry, hi + lo
@@ -274,18 +282,19 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
     for (int a = lane; a < D; a += 32) { y_out[row * D + a] = qn; kbar_out[row * D + a] = qn; }
     return;
   }
-  // This lane's rows of L to shared memory (row-major, 64 floats per row).
+  // This lane's rows of L to shared memory (row-major, stride LS = 68 floats: conflict-free
+  // 16-byte stores across the lanes of a phase).
   float* Lrows = g;
   if (live0) {
 #pragma unroll
     for (int j = 0; j < W0; j += 4)
-      *reinterpret_cast<float4*>(Lrows + rr[0] * 64 + j) =
+      *reinterpret_cast<float4*>(Lrows + rr[0] * C::LS + j) =
           make_float4(L.a0[j], L.a0[j + 1], L.a0[j + 2], L.a0[j + 3]);
   }
   if constexpr (NS == 2) {
 #pragma unroll
     for (int j = 0; j < D; j += 4)
-      *reinterpret_cast<float4*>(Lrows + rr[NS - 1] * 64 + j) =
+      *reinterpret_cast<float4*>(Lrows + rr[NS - 1] * C::LS + j) =
           make_float4(L.a1[j], L.a1[j + 1], L.a1[j + 2], L.a1[j + 3]);
   }
   __syncwarp();
