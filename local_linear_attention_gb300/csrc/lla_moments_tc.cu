@@ -58,24 +58,27 @@ constexpr int NFG = 8;                      // feature-generation warps
 constexpr int NWARPS = 2 + NSM + NFG;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 3;                     // P (TMEM) and F (shared memory) buffers
-constexpr int NSB = 3;                      // S buffers: Q K^T runs two key blocks ahead
+constexpr int NSB = 2;                      // S buffers
 
 // tensor-memory columns
 constexpr uint32_t T_ACC = 0;
 constexpr uint32_t T_S = NCH;               // NSB x 32 columns of fp32 logits
 constexpr uint32_t T_P = T_S + NSB * KB;    // NBUF x 16 columns of packed bf16 weights
+constexpr uint32_t T_Q = T_P + NBUF * (KB / 2);  // 32 columns: the Q tile, A operand of Q K^T
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(T_P + NBUF * (KB / 2) <= TMEM_COLS, "tensor memory budget");
+static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
 
 // shared-memory layout (bytes)
-constexpr int SM_Q = 0;                              // 128 x 64 bf16, K-major core layout
-constexpr int SM_K = SM_Q + BM * D * 2;              // KS x (32 x 64 bf16)
+constexpr int SM_K = 0;                              // KS x (32 x 64 bf16)
 constexpr int K_STAGE = KB * D * 2;
 constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
 constexpr int F_HALF = GPP * 512;
 constexpr int F_BUF = 2 * F_HALF;
-constexpr int SM_BAR = SM_F + NBUF * F_BUF;
+constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
+constexpr int SM_EPI = SM_F + NBUF * F_BUF;          // NSM x (32 rows x 36 floats)
+constexpr int SM_BAR = SM_EPI + NSM * 32 * EPI_LD * 4;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // Pair p of the feature order (see the file comment): row a and even column b, or, for the odd
 // diagonal pairs, u = a.
@@ -201,7 +204,7 @@ struct Barriers {
   uint64_t kfull[KS], kempty[KS];
   uint64_t sfull[NSB], sfree[NSB];
   uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];
-  uint64_t accfull, accfree, done, rowx;
+  uint64_t accfull, accfree, done, rowx, qready;
   float part[2][BM];  // per-row partial results of the two softmax halves (max, then omega)
 };
 
@@ -226,13 +229,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int G = nb * (1 + NPASS);
   const long long base = bh * T;
 
-  // Q tile -> shared memory (zero rows past the end of the sequence).
-  for (int e = tid; e < BM * (D / 8); e += NTHREADS) {
-    const int r = e >> 3, c = e & 7;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nq) v = *reinterpret_cast<const uint4*>(q + (base + i0 + r) * D + c * 8);
-    *reinterpret_cast<uint4*>(smem + SM_Q + kmaj_off(r, c)) = v;
-  }
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 1 + NFG); }
     for (int s = 0; s < NSB; ++s) {
@@ -248,6 +244,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     mbar_init(&bar.accfree, NSM);
     mbar_init(&bar.done, 1);
     mbar_init(&bar.rowx, NSM);
+    mbar_init(&bar.qready, 4);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -268,14 +265,13 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     if (lane == 0) {
       // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
       // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
-      const uint64_t qd = smem_desc(smem_u32(smem + SM_Q), 128, 1024);
       const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
       const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
       constexpr uint32_t id_qk = idesc_bf16(BM, KB, false, false);
       constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
       constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
-      const uint32_t t_acc = tbase + T_ACC, t_s = tbase + T_S, t_p = tbase + T_P;
-      bool ok = true;
+      const uint32_t t_acc = tbase + T_ACC, t_s = tbase + T_S, t_p = tbase + T_P, t_q = tbase + T_Q;
+      bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);  // Q tile in tensor memory
       // Iteration g issues Q K^T of step g and the feature contraction of step g - 2, so the
       // softmax warps have two steps of tensor work in which to turn S(g) into P(g).
       for (int g = 0; g <= G + 1 && ok; ++g) {
@@ -288,10 +284,10 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           tc_fence_after();
           const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
           const uint32_t ts = t_s + sb * KB;
-          mma_ss(ts, qd, kst, id_qk, 0u);
-          mma_ss(ts, qd + 16, kst + 16, id_qk, 1u);
-          mma_ss(ts, qd + 32, kst + 32, id_qk, 1u);
-          mma_ss(ts, qd + 48, kst + 48, id_qk, 1u);
+          mma_ts(ts, t_q, kst, id_qk, 0u);
+          mma_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
+          mma_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
+          mma_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
           mma_commit(&bar.sfull[sb]);
           mma_commit(&bar.kempty[st]);
         }
@@ -377,6 +373,21 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const int c_lo = half * (KB / 2);
     const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
+    if (half == 0) {  // this row of Q into tensor memory (packed bf16 pairs, 32 columns)
+      const uint4* qr = reinterpret_cast<const uint4*>(q + (base + i) * D);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (valid) { v0 = qr[2 * c]; v1 = qr[2 * c + 1]; }
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        tmem_st8(lane_base + T_Q + 8 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.qready);
+    }
+    float* epi = reinterpret_cast<float*>(smem + SM_EPI) + (warp - 2) * 32 * EPI_LD;
     float m = -INFINITY, om = 0.f;
     bool ok = true;
     for (int g = 0; g < G; ++g) {
@@ -430,19 +441,38 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       if (b == nb - 1) {  // end of a pass: drain this half's accumulator columns
         if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) { ok = false; break; }
         tc_fence_after();
-        float* dst = mom + (base + i) * NFP + pass * NCH;
+        // Through a per-warp shared buffer, so that each store instruction writes whole 128-byte
+        // lines of 4 rows instead of 16 bytes of 32 rows.
         const int e0 = half ? NA : 0, e1 = half ? NCH : NA;
+        const long long row0 = base + i0 + quarter * 32;
 #pragma unroll 1
-        for (int c0 = e0; c0 < e1; c0 += 16) {
+        for (int c0 = e0; c0 < e1; c0 += 32) {
+          const int w = min(32, e1 - c0);
           uint32_t v[16];
           tmem_ld16(lane_base + T_ACC + c0, v);
           tmem_ld_wait();
-          if (valid) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 4 * t) =
+                make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+          if (w > 16) {
+            tmem_ld16(lane_base + T_ACC + c0 + 16, v);
+            tmem_ld_wait();
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              *reinterpret_cast<uint4*>(dst + c0 + 4 * t) =
+              *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 16 + 4 * t) =
                   make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
           }
+          __syncwarp();
+          const int chunk = lane & 7;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = 4 * it + (lane >> 3);
+            if (quarter * 32 + rr < nq && 4 * chunk < w)
+              *reinterpret_cast<float4*>(mom + (row0 + rr) * NFP + pass * NCH + c0 + 4 * chunk) =
+                  *reinterpret_cast<const float4*>(epi + rr * EPI_LD + 4 * chunk);
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
