@@ -56,9 +56,10 @@ def moments_flops_per_pair(d: int) -> int:
 
 
 def tc_executed_flops_per_pair(d: int) -> int:
-    """Tensor flops the tcgen05 moments kernel executes per causal pair: q.k in 7 sweeps (one max
-    pass, six feature passes) and hi + lo contractions over 6 x 368 feature columns."""
-    return 7 * 2 * d + 2 * 2 * 2208
+    """Tensor flops the tcgen05 moments kernel executes per causal pair: q.k in 2 sweeps (the max
+    pass and feature pass 0; passes 1..5 reuse the stored weights) and hi + lo contractions over
+    6 x 368 feature columns."""
+    return 2 * 2 * d + 2 * 2 * 2208
 
 
 def step_flops(w) -> int:

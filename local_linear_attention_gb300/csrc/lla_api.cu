@@ -133,7 +133,7 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int choose_path(const Args& a) {
-  const bool tc_ok = a.dtype == LLA_BF16 && a.d == 64;
+  const bool tc_ok = tc_eligible(a);
   const int req = g_path_request.load();
   if (req == kPathCudaCore || !tc_ok) return kPathCudaCore;
   return kPathTensorCore;
@@ -152,6 +152,7 @@ size_t workspace_bytes(const Args& a) {
   n += align_up(R * a.d * sizeof(float));                // kbar
   n += align_up(R * sizeof(float));                      // omega
   n += align_up(R * sizeof(float));                      // mraw
+  if (tc_eligible(a)) n += align_up(moments_tc_pscratch_bytes(a.BH(), a.T));  // pscr
   return n;
 }
 
@@ -169,6 +170,7 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->kbar = take(R * a.d * sizeof(float));
   ws->omega = take(R * sizeof(float));
   ws->mraw = take(R * sizeof(float));
+  ws->pscr = tc_eligible(a) ? take(moments_tc_pscratch_bytes(a.BH(), a.T)) : nullptr;
   ws->status = nullptr;
   ws->path = choose_path(a);
 }

@@ -53,6 +53,8 @@ struct Workspace {
   float* kbar;    // [BH*T, d]      kbar - c, the weighted key mean in the shifted frame
   float* omega;   // [BH*T]         sum of the weights (tensor-core moments path)
   float* mraw;    // [BH*T]         row max of q.k (unscaled; tensor-core path, for the readout)
+  void* pscr;     // tensor-core path: the kernel weights P of feature pass 0, bf16, one 8 KiB
+                  // image per (head, query tile, key block), reused by the later passes
   int* status;    // device status word of the current device
   int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
 };
@@ -71,6 +73,10 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 size_t moments_tc_row_floats();
+long long moments_tc_pblocks_per_head(int T);
+size_t moments_tc_pscratch_bytes(long long BH, int T);
+// The tensor-core stage may run for these sizes (whatever path is requested at call time).
+inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64; }
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s);

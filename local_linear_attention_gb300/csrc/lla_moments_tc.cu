@@ -18,13 +18,14 @@
 //    S = Q K^T and P (cheap next to the 2 x 368-column contraction it feeds).
 // A first pass over the prefix computes the exact row max m_i (only S = Q K^T and a max).
 //
-// Warp roles (18 warps): 0 issues every tcgen05.mma (one thread) and owns the TMEM allocation;
-// 1 stages key blocks (32 keys x 64) into shared memory; 2-9 turn S into P (one thread per query
-// = TMEM lane, two warps per lane quarter splitting the keys of a block) and drain the
-// accumulators after each pass; 10-17 generate the exact hi/lo feature tiles for each key block
-// (one lane per key) into shared memory. P and the feature tiles are triple-buffered. P lives in TMEM and is the A
-// operand of the feature contraction (tcgen05.mma with A in tensor memory). All operands in
-// shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is bounded.
+// Warp roles (19 warps): 0 issues Q K^T (one thread) and owns the TMEM allocation; 18 issues the
+// feature contraction (one thread); 1 stages key blocks (32 keys x 64) into shared memory; 2-9
+// turn S into P (one thread per query = TMEM lane, two warps per lane quarter splitting the keys
+// of a block) and drain the accumulators after each pass; 10-17 generate the exact hi/lo feature
+// tiles for each key block (one lane per key) into shared memory. P and the feature tiles are
+// triple-buffered. P lives in TMEM and is the A operand of the feature contraction (tcgen05.mma
+// with A in tensor memory). All operands in shared memory use the no-swizzle core-matrix layout.
+// Every mbarrier wait is bounded.
 //
 // Feature order (2208 slots = 1104 pairs, the layout of each output row): the upper triangle of
 // kt kt^T for the augmented key kt = [k_0..k_63, 1, 0], row by row: for row a, the pairs
@@ -55,10 +56,14 @@ constexpr int KS = 6;                       // key-tile pipeline stages
 constexpr int KLAG = KS - 2;                // key blocks the loader keeps in flight
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int NFG = 8;                      // feature-generation warps
-constexpr int NWARPS = 2 + NSM + NFG;
+constexpr int NWARPS = 4 + NSM + NFG;       // + Q K^T issuer, key loader, feature issuer, P loader
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 3;                     // P (TMEM) and F (shared memory) buffers
+constexpr int PS = 3;                       // staged P blocks in shared memory (passes 1..5)
+constexpr int PLAG = 1;                     // P blocks the P loader keeps in flight
+static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
 constexpr int NSB = 2;                      // S buffers
+static_assert(NSB == 2, "the Q K^T issuer indexes S buffers with g & 1");
 
 // tensor-memory columns
 constexpr uint32_t T_ACC = 0;
@@ -74,8 +79,13 @@ constexpr int K_STAGE = KB * D * 2;
 constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
 constexpr int F_HALF = GPP * 512;
 constexpr int F_BUF = 2 * F_HALF;
+// One key block of P (128 rows x 32 keys, bf16) as the tcgen05.cp source image: 16-byte chunk kc
+// (keys 8kc..8kc+7) of row r at kc * 2048 + r * 16 (no-swizzle K-major core matrices, LBO 2048,
+// SBO 128). The same image is the block's layout in the global P scratch.
+constexpr int P_BLOCK = BM * KB * 2;
+constexpr int SM_P = SM_F + NBUF * F_BUF;            // PS x 8 KB
 constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
-constexpr int SM_EPI = SM_F + NBUF * F_BUF;          // NSM x (32 rows x 36 floats)
+constexpr int SM_EPI = SM_P + PS * P_BLOCK;          // NSM x (32 rows x 36 floats)
 constexpr int SM_BAR = SM_EPI + NSM * 32 * EPI_LD * 4;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -203,16 +213,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
 struct Barriers {
   uint64_t kfull[KS], kempty[KS];
   uint64_t sfull[NSB], sfree[NSB];
-  uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];
-  uint64_t accfull, accfree, done, rowx, qready;
+  uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];  // P / F of a feature step written; consumed
+  uint64_t pready[PS], pempty[PS];                 // staged P block loaded; copied to TMEM
+  uint64_t accfull, accfree, done_qk, done_f, rowx, qready, p0done;
   float part[2][BM];  // per-row partial results of the two softmax halves (max, then omega)
 };
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)), "r"(n)
+      : "memory");
+}
+
+// Copies a 128-row x 32-byte tile (16 bf16 per row) from shared memory into 8 TMEM columns.
+// Implicitly ordered before tcgen05.mma issued later by the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc));
+}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
                   int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ mraw_out,
-                  float* __restrict__ omega_out, float* __restrict__ mom,
-                  int* __restrict__ status) {
+                  float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pscr,
+                  long long pblk_per_head, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -228,6 +252,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int nb = (jend + KB - 1) / KB;
   const int G = nb * (1 + NPASS);
   const long long base = bh * T;
+  // This tile's P blocks in the scratch: earlier tiles of the head hold 4, 8, ... blocks.
+  uint4* const ptile = pscr + (bh * pblk_per_head + 2ll * tile * (tile + 1)) * (P_BLOCK / 16);
 
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 1 + NFG); }
@@ -240,11 +266,17 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mbar_init(&bar.ffull[s], NFG);
       mbar_init(&bar.pfree[s], 1);
     }
+    for (int s = 0; s < PS; ++s) {
+      mbar_init(&bar.pready[s], 1);
+      mbar_init(&bar.pempty[s], 1);
+    }
     mbar_init(&bar.accfull, 1);
     mbar_init(&bar.accfree, NSM);
-    mbar_init(&bar.done, 1);
+    mbar_init(&bar.done_qk, 1);
+    mbar_init(&bar.done_f, 1);
     mbar_init(&bar.rowx, NSM);
     mbar_init(&bar.qready, 4);
+    mbar_init(&bar.p0done, NSM);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -261,71 +293,134 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int TO = kStatusTimeout;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ Q K^T issuer
+    // Two threads issue the tensor-core work (this one and the feature issuer), because a single
+    // thread's serial issue cost -- mbarrier tests, descriptor arithmetic and the MMA/commit
+    // instructions themselves -- exceeds the tensor work of a key block. tcgen05.commit tracks
+    // the issuing thread's own MMAs, so each thread signals and drains its own. Q K^T runs only in
+    // the max pass and feature pass 0; later passes reuse the P that pass 0 stored.
     if (lane == 0) {
-      // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
-      // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
       const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
-      const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
       constexpr uint32_t id_qk = idesc_bf16(BM, KB, false, false);
-      constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
-      constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
-      const uint32_t t_acc = tbase + T_ACC, t_s = tbase + T_S, t_p = tbase + T_P, t_q = tbase + T_Q;
+      const uint32_t t_s = tbase + T_S, t_q = tbase + T_Q;
       bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);  // Q tile in tensor memory
-      // Iteration g issues Q K^T of step g and the feature contraction of step g - 2, so the
-      // softmax warps have two steps of tensor work in which to turn S(g) into P(g).
-      for (int g = 0; g <= G + 1 && ok; ++g) {
-        if (g < G) {
-          const int st = g % KS, sb = g % NSB;
-          ok = mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p);
-          if (ok && g >= NSB)
-            ok = mbar_wait(&bar.sfree[sb], ((g / NSB) - 1) & 1, status, TO, abort_p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
-          const uint32_t ts = t_s + sb * KB;
-          mma_ts(ts, t_q, kst, id_qk, 0u);
-          mma_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
-          mma_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
-          mma_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
-          mma_commit(&bar.sfull[sb]);
-          mma_commit(&bar.kempty[st]);
-        }
-        if (g >= nb + 2) {
-          const int h = g - 2 - nb, pb = h % NBUF, pass = h / nb, b = h % nb;
-          const uint32_t ph = (h / NBUF) & 1;
-          ok = mbar_wait(&bar.pfull[pb], ph, status, TO, abort_p) &&
-               mbar_wait(&bar.ffull[pb], ph, status, TO, abort_p);
-          if (ok && b == 0 && pass >= 1)
-            ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t fh = fd + (uint64_t)(pb * (F_BUF >> 4));
-          const uint64_t fl = fh + (F_HALF >> 4);
-          constexpr uint32_t nb_off = (NA / 8) * 512 / 16;
-          const uint32_t a0 = t_p + pb * (KB / 2);
-          const uint32_t acc0 = b > 0 ? 1u : 0u;
-          // K-step 0 (keys 0..15), then K-step 1 (keys 16..31; +256 B in the F tiles)
-          mma_ts(t_acc, a0, fh, id_a, acc0);
-          mma_ts(t_acc, a0, fl, id_a, 1u);
-          mma_ts(t_acc + NA, a0, fh + nb_off, id_b, acc0);
-          mma_ts(t_acc + NA, a0, fl + nb_off, id_b, 1u);
-          mma_ts(t_acc, a0 + 8, fh + 16, id_a, 1u);
-          mma_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
-          mma_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
-          mma_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
-          mma_commit(&bar.pfree[pb]);
-          if (b == nb - 1) mma_commit(&bar.accfull);
-        }
+      int st = 0;
+      uint32_t kpar = 0;  // parity of the current fill of key stage st
+      for (int g = 0; g < 2 * nb && ok; ++g) {
+        const int sb = g & 1;
+        ok = g >= NSB ? mbar_wait2(&bar.kfull[st], kpar, &bar.sfree[sb], ((g >> 1) - 1) & 1,
+                                   status, TO, abort_p)
+                      : mbar_wait(&bar.kfull[st], kpar, status, TO, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+        // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
+        // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
+        const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
+        const uint32_t ts = t_s + sb * KB;
+        mma_ts(ts, t_q, kst, id_qk, 0u);
+        mma_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
+        mma_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
+        mma_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
+        mma_commit(&bar.sfull[sb]);
+        mma_commit(&bar.kempty[st]);
+        if (++st == KS) { st = 0; kpar ^= 1; }
       }
       if (!ok) *abort_p = 1;
       // Drain: wait (bounded, whatever the abort flag says) until every MMA this thread issued
       // has completed, so that tensor memory is not released under a running MMA.
-      mma_commit(&bar.done);
+      mma_commit(&bar.done_qk);
       volatile int never = 0;
-      mbar_wait(&bar.done, 0, status, TO, &never);
+      mbar_wait(&bar.done_qk, 0, status, TO, &never);
     }
     __syncwarp();
+  } else if (warp == NWARPS - 2) {
+    // ------------------------------------------------------------------ feature-contraction issuer
+    // Pass 0 contracts the P that the softmax warps wrote to tensor memory; passes 1..5 first copy
+    // the staged P block from shared memory into the same tensor-memory buffer (tcgen05.cp, which
+    // the MMAs issued after it by this thread observe).
+    if (lane == 0) {
+      const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
+      const uint64_t pd = smem_desc(smem_u32(smem + SM_P), 2048, 128);
+      constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
+      constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
+      constexpr uint32_t nb_off = (NA / 8) * 512 / 16;
+      const uint32_t t_acc = tbase + T_ACC, t_p = tbase + T_P;
+      bool ok = true;
+      int pb = 0, b = 0, pass = 0, ps = 0;
+      uint32_t opar = 0, ppar = 0;  // parities of the current uses of buffer pb and stage ps
+      for (int h = 0; h < nb * NPASS && ok; ++h) {
+        ok = pass == 0 ? mbar_wait2(&bar.pfull[pb], opar, &bar.ffull[pb], opar, status, TO, abort_p)
+                       : mbar_wait2(&bar.pready[ps], ppar, &bar.ffull[pb], opar, status, TO, abort_p);
+        if (ok && b == 0 && pass >= 1)
+          ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t fh = fd + (uint64_t)(pb * (F_BUF >> 4));
+        const uint64_t fl = fh + (F_HALF >> 4);
+        const uint32_t a0 = t_p + pb * (KB / 2);
+        const uint32_t acc0 = b > 0 ? 1u : 0u;
+        // The tensor-memory P buffer pb is free here: the feature warps wrote F(h) only after the
+        // MMAs of step h - NBUF, the last readers of buffer pb, had completed.
+        if (pass >= 1) {
+          const uint64_t pst = pd + (uint64_t)(ps * (P_BLOCK >> 4));
+          tmem_cp_128x256b(a0, pst);                    // keys 0..15
+          tmem_cp_128x256b(a0 + 8, pst + (4096 >> 4));  // keys 16..31
+        }
+        // K-step 0 (keys 0..15), then K-step 1 (keys 16..31; +256 B in the F tiles); the hi and lo
+        // tiles of each feature column go into the same accumulator.
+        mma_ts(t_acc, a0, fh, id_a, acc0);
+        mma_ts(t_acc, a0, fl, id_a, 1u);
+        mma_ts(t_acc + NA, a0, fh + nb_off, id_b, acc0);
+        mma_ts(t_acc + NA, a0, fl + nb_off, id_b, 1u);
+        mma_ts(t_acc, a0 + 8, fh + 16, id_a, 1u);
+        mma_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
+        mma_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
+        mma_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
+        mma_commit(&bar.pfree[pb]);
+        if (pass >= 1) {
+          mma_commit(&bar.pempty[ps]);
+          if (++ps == PS) { ps = 0; ppar ^= 1; }
+        }
+        if (b == nb - 1) mma_commit(&bar.accfull);
+        if (++pb == NBUF) { pb = 0; opar ^= 1; }
+        if (++b == nb) { b = 0; ++pass; }
+      }
+      if (!ok) *abort_p = 1;
+      mma_commit(&bar.done_f);
+      volatile int never = 0;
+      mbar_wait(&bar.done_f, 0, status, TO, &never);
+    }
+    __syncwarp();
+  } else if (warp == NWARPS - 1) {
+    // ------------------------------------------------------------------ P loader
+    // Stages the P blocks of passes 1..5 from the scratch, once the softmax warps have stored all
+    // of pass 0 (barrier p0done; their stores are fenced before they arrive).
+    const int U = nb * (NPASS - 1);
+    bool ok = warp_wait(&bar.p0done, 0, status, abort_p);
+    int b = 0;
+    for (int u = 0; u < U + PLAG && ok; ++u) {
+      if (u < U) {
+        const int ps = u % PS;
+        if (u >= PS && !warp_wait(&bar.pempty[ps], ((u / PS) - 1) & 1, status, abort_p)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dst = smem + SM_P + ps * P_BLOCK;
+        const uint4* src = ptile + (long long)b * (P_BLOCK / 16);
+#pragma unroll
+        for (int t = 0; t < P_BLOCK / 512; ++t)
+          cp_async16(dst + (t * 32 + lane) * 16, src + t * 32 + lane, 16u);
+        if (++b == nb) b = 0;
+      }
+      cp_async_commit();
+      if (u >= PLAG) {
+        cp_async_wait<PLAG>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.pready[(u - PLAG) % PS]);
+      }
+    }
+    if (!ok) cp_async_wait<0>();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
     // cp.async 16-byte copies, several key blocks in flight. Lane -> (row, chunk) mapping:
@@ -365,7 +460,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
     // accumulator columns [0, NA); half 1 takes keys 16..31 and columns [NA, NCH). Row max and
     // omega are combined across the halves through shared memory (barrier rowx: phase 0 after the
-    // max pass, phase 1 at the end).
+    // max pass, phase 1 at the end). In feature pass 0 each P block also goes to the scratch, from
+    // which the later passes take it; after pass 0 these warps only drain the accumulators.
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
@@ -388,11 +484,53 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       if (lane == 0) mbar_arrive(&bar.qready);
     }
     float* epi = reinterpret_cast<float*>(smem + SM_EPI) + (warp - 2) * 32 * EPI_LD;
+    // Drains this half's accumulator columns of feature pass `pass` into its slots of mom.
+    // Through a per-warp shared buffer, so that each store instruction writes whole 128-byte
+    // lines of 4 rows instead of 16 bytes of 32 rows.
+    auto drain = [&](int pass) -> bool {
+      if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) return false;
+      tc_fence_after();
+      const int e0 = half ? NA : 0, e1 = half ? NCH : NA;
+      const long long row0 = base + i0 + quarter * 32;
+#pragma unroll 1
+      for (int c0 = e0; c0 < e1; c0 += 32) {
+        const int w = min(32, e1 - c0);
+        uint32_t v[16];
+        tmem_ld16(lane_base + T_ACC + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 4 * t) =
+              make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+        if (w > 16) {
+          tmem_ld16(lane_base + T_ACC + c0 + 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 16 + 4 * t) =
+                make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+        }
+        __syncwarp();
+        const int chunk = lane & 7;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = 4 * it + (lane >> 3);
+          if (quarter * 32 + rr < nq && 4 * chunk < w)
+            *reinterpret_cast<float4*>(mom + (row0 + rr) * NFP + pass * NCH + c0 + 4 * chunk) =
+                *reinterpret_cast<const float4*>(epi + rr * EPI_LD + 4 * chunk);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.accfree);
+      return true;
+    };
     float m = -INFINITY, om = 0.f;
     bool ok = true;
-    for (int g = 0; g < G; ++g) {
-      const int sb = g % NSB;
-      if (!warp_wait(&bar.sfull[sb], (g / NSB) & 1, status, abort_p)) { ok = false; break; }
+    for (int g = 0; g < 2 * nb; ++g) {
+      const int sb = g & 1;
+      if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[KB / 2];
       tmem_ld16(lane_base + T_S + sb * KB + c_lo, sv);
@@ -400,7 +538,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.sfree[sb]);
-      const int b = g % nb;
+      const int b = g < nb ? g : g - nb;
       const int j0 = b * KB + c_lo;
       if (g < nb) {  // max pass
 #pragma unroll
@@ -415,7 +553,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
         continue;
       }
-      const int h = g - nb, pass = h / nb, pb = h % NBUF;
+      const int pb = b % NBUF;
       const float mc = m * c2;
       uint32_t pw[KB / 4];
 #pragma unroll
@@ -424,61 +562,29 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const float p1 =
             (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
         pw[c / 2] = pack_bf16(p0, p1);
+        om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
       }
-      if (pass == 0) {
-#pragma unroll
-        for (int c = 0; c < KB / 4; ++c)
-          om += __uint_as_float(pw[c] << 16) + __uint_as_float(pw[c] & 0xFFFF0000u);
-      }
-      if (h >= NBUF &&
-          !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
+      // This row's 16 weights as chunks 2*half and 2*half + 1 of the block's image.
+      constexpr int kChunk = 2048 / 16;  // chunk stride of the image, in 16-byte units
+      uint4* pdst = ptile + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+      pdst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      pdst[kChunk] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+      if (b >= NBUF &&
+          !warp_wait(&bar.pfree[pb], ((b / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
       tmem_st8(lane_base + T_P + pb * (KB / 2) + half * (KB / 4), pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.pfull[pb]);
-      if (b == nb - 1) {  // end of a pass: drain this half's accumulator columns
-        if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) { ok = false; break; }
-        tc_fence_after();
-        // Through a per-warp shared buffer, so that each store instruction writes whole 128-byte
-        // lines of 4 rows instead of 16 bytes of 32 rows.
-        const int e0 = half ? NA : 0, e1 = half ? NCH : NA;
-        const long long row0 = base + i0 + quarter * 32;
-#pragma unroll 1
-        for (int c0 = e0; c0 < e1; c0 += 32) {
-          const int w = min(32, e1 - c0);
-          uint32_t v[16];
-          tmem_ld16(lane_base + T_ACC + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 4 * t) =
-                make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
-          if (w > 16) {
-            tmem_ld16(lane_base + T_ACC + c0 + 16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              *reinterpret_cast<uint4*>(epi + lane * EPI_LD + 16 + 4 * t) =
-                  make_uint4(v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
-          }
-          __syncwarp();
-          const int chunk = lane & 7;
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int rr = 4 * it + (lane >> 3);
-            if (quarter * 32 + rr < nq && 4 * chunk < w)
-              *reinterpret_cast<float4*>(mom + (row0 + rr) * NFP + pass * NCH + c0 + 4 * chunk) =
-                  *reinterpret_cast<const float4*>(epi + rr * EPI_LD + 4 * chunk);
-          }
-          __syncwarp();
-        }
-        tc_fence_before();
+      if (b == nb - 1) {
+        __threadfence();  // the scratch P blocks, before the P loader may read them
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.accfree);
+        if (lane == 0) mbar_arrive(&bar.p0done);
+        if (!drain(0)) { ok = false; break; }
       }
     }
+    for (int pass = 1; pass < NPASS && ok; ++pass) ok = drain(pass);
     if (ok) {  // combine the halves' omega
       bar.part[half][r] = om;
       __syncwarp();
@@ -490,7 +596,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
     }
   } else {
-    // ------------------------------------------------------------------ feature generation
+    // ------------------------------------------------------------------ feature generation (warps 10-17)
     const int fw = warp - 2 - NSM;
     const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;
     for (int g = 0; g < G; ++g) {
@@ -511,7 +617,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
       kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.kempty[st]);
+      // Passes 1..5 run no Q K^T, whose completion is the stage's other release: warp 0 of this
+      // group arrives for it.
+      if (lane == 0) mbar_arrive_cnt(&bar.kempty[st], (pass >= 1 && fw == 0) ? 2u : 1u);
       if (h >= NBUF && !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) break;
       uint8_t* fhi = smem + SM_F + pb * F_BUF;
       generate(pass, fw, kw, fhi, fhi + F_HALF, row_off);
@@ -533,6 +641,15 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
 size_t moments_tc_row_floats() { return NFP; }
 
+long long moments_tc_pblocks_per_head(int T) {
+  const long long nt = (T + BM - 1) / BM;
+  return nt > 0 ? 2 * (nt - 1) * nt + (T + KB - 1) / KB : 0;
+}
+
+size_t moments_tc_pscratch_bytes(long long BH, int T) {
+  return (size_t)BH * (size_t)moments_tc_pblocks_per_head(T) * P_BLOCK;
+}
+
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   auto kern = moments_tc_kernel;
   cudaError_t err =
@@ -542,7 +659,8 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
-      (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, ws.status);
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
+      moments_tc_pblocks_per_head(a.T), ws.status);
   count_launch();
   return cudaGetLastError();
 }

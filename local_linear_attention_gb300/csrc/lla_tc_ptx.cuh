@@ -70,6 +70,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Waits for two phases. Both first tests are issued back to back (one asm block, so that neither
+// result is consumed before the other test is in flight): when both phases are already complete,
+// the cost is one shared-memory round trip instead of two.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                           int* status, int bit, volatile int* abort) {
+  uint32_t ra, rb;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%2], %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%4], %5;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "selp.u32 %1, 1, 0, q;\n\t}"
+      : "=r"(ra), "=r"(rb)
+      : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb)
+      : "memory");
+  if (ra && rb) return true;
+  return (ra || mbar_wait(a, pa, status, bit, abort)) && (rb || mbar_wait(b, pb, status, bit, abort));
+}
+
 // ----------------------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy that bypasses L1; src_bytes = 0 writes zeros without reading.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
