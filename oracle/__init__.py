@@ -9,3 +9,4 @@ from .lla_oracle import (  # noqa: F401
     lla_moments_oracle,
     softmax_attention_oracle,
 )
+from .parallax_oracle import parallax_row, parallax_forward_oracle  # noqa: F401
