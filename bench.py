@@ -18,6 +18,10 @@ clocks sampled during it.
 
 --impl reference times the float64 oracle itself (the reference arm of this comparison) on the
 host cores, on bounded samples of the same workload, and prints the same kind of line.
+
+--op parallax measures the causal Parallax forward with a given probe instead (one kernel per
+step; probe r ~ N(0, 1/d) drawn with seed + 100) on the same workload and prints the same kind
+of line for it.
 """
 from __future__ import annotations
 
@@ -38,6 +42,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "LLA fwd queries/sec and TFLOP/s on 1 GB300; fraction of tensor-core peak"
+METRIC_PARALLAX = "Parallax fwd queries/sec and TFLOP/s on 1 GB300; fraction of tensor-core peak"
 UNIT = "queries/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SM_COUNT = 152
@@ -60,6 +65,12 @@ def tc_executed_flops_per_pair(d: int) -> int:
     pass and feature pass 0; passes 1..5 reuse the stored weights) and hi + lo contractions over
     6 x 368 feature columns."""
     return 2 * 2 * d + 2 * 2 * 2208
+
+
+def parallax_flops_per_pair(d: int, dv: int) -> int:
+    """Algorithmic flops per causal pair of the Parallax forward: q.k and r.k (2d each), and the
+    two value contractions P1 V and P2 V (2dv each). The exact-max sweep is not counted."""
+    return 2 * d + 2 * d + 2 * dv + 2 * dv
 
 
 def step_flops(w) -> int:
@@ -168,18 +179,25 @@ class ClockSampler:
 _POOL_INPUTS = {}
 
 
-def _pool_init(workload_index: int):
+def _pool_init(workload_index: int, op: str = "lla"):
     from local_linear_attention_gb300 import workloads as W
-    q, k, v = W.make_inputs(W.WORKLOADS[workload_index])
+    w = W.WORKLOADS[workload_index]
+    q, k, v = W.make_inputs(w)
     _POOL_INPUTS["qkv"] = tuple(t.float().numpy() for t in (q, k, v))
+    _POOL_INPUTS["op"] = op
+    if op == "parallax":
+        _POOL_INPUTS["r"] = W.make_probe(w.B, w.H, w.T, w.d, w.dtype, seed=w.seed + 100).float().numpy()
 
 
 def _oracle_rows(args):
     h, lam, rows = args
-    from oracle import lla_forward_oracle
+    from oracle import lla_forward_oracle, parallax_forward_oracle
     q, k, v = _POOL_INPUTS["qkv"]
     t0 = time.perf_counter()
-    lla_forward_oracle(q, k, v, h, lam, rows=rows)
+    if _POOL_INPUTS["op"] == "parallax":
+        parallax_forward_oracle(q, k, v, _POOL_INPUTS["r"], h, rows=rows)
+    else:
+        lla_forward_oracle(q, k, v, h, lam, rows=rows)
     return time.perf_counter() - t0
 
 
@@ -188,16 +206,17 @@ class OracleTimer:
     per host core, in spawned single-threaded worker processes that regenerate the workload
     from its seed once."""
 
-    def __init__(self, workload_index: int):
+    def __init__(self, workload_index: int, op: str = "lla"):
         from local_linear_attention_gb300 import workloads as W
         self.W = W
         self.w = W.WORKLOADS[workload_index]
+        self.op = op
         self.cores = os.cpu_count() or 1
         env = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
         old = {x: os.environ.get(x) for x in env}
         os.environ.update(env)
         try:
-            self.pool = mp.get_context("spawn").Pool(self.cores, _pool_init, (workload_index,))
+            self.pool = mp.get_context("spawn").Pool(self.cores, _pool_init, (workload_index, op))
         finally:
             for x, val in old.items():
                 if val is None:
@@ -227,9 +246,10 @@ class OracleTimer:
             self.per_row = wall / len(rows)
             if wall >= 0.5 * budget_s or n >= w.queries:
                 break
+        how = ("one float64 lstsq per row" if self.op == "lla"
+               else "float64 softmax weights and explicit covariance per row")
         sample = (f"{len(rows)} uniformly sampled query rows of {w.describe()} (of {w.queries}), "
-                  f"one float64 lstsq per row, {self.cores} single-threaded processes, "
-                  f"{wall:.1f} s")
+                  f"{how}, {self.cores} single-threaded processes, {wall:.1f} s")
         return len(rows) / wall, self.cores, sample
 
     def close(self):
@@ -251,7 +271,7 @@ def run_reference(args, w):
         return 0
     budget = float(os.environ.get("LLA_ORACLE_STEP_S", "4"))
     vals, cores, sample = [], 1, ""
-    timer = OracleTimer(args.workload)
+    timer = OracleTimer(args.workload, args.op)
     for s in range(args.warmup + args.steps):
         v, cores, sample = timer.measure(budget, seed=500 + s)
         if s >= args.warmup:
@@ -259,7 +279,8 @@ def run_reference(args, w):
     timer.close()
     value = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_PARALLAX if args.op == "parallax" else METRIC,
+        "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.queries / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
@@ -275,12 +296,134 @@ def run_reference(args, w):
     return 0
 
 
+def run_parallax(args, w, cpu, world, rank):
+    """One step = one lla_parallax_forward over the workload (a single kernel launch)."""
+    import torch
+    import torch.distributed as dist
+    from local_linear_attention_gb300 import binding as lla
+    from local_linear_attention_gb300 import workloads as W
+
+    _, h = w.points[0]
+    q, k, v = W.make_inputs(w)
+    r = W.make_probe(w.B, w.H, w.T, w.d, w.dtype, seed=w.seed + 100)
+    dq, dk, dv_, dr = q.cuda(), k.cuda(), v.cuda(), r.cuda()
+    out = torch.empty(w.B, w.H, w.T, w.dv, dtype=dq.dtype, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lla.lla_parallax_forward(dq, dk, dv_, dr, h, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = lla.launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    n_launch = lla.launch_count() - n_launch0
+    clk = clocks.stop()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during the timed steps")
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = w.queries * world / (ms_per_step / 1e3)
+
+    e2e = None
+    eb = q.element_size()
+    if not args.no_e2e:  # pinned host inputs -> device, forward, result -> pinned host, per step
+        hq, hk, hv, hr = (t.pin_memory() for t in (q, k, v, r))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            for hst, dst in ((hq, dq), (hk, dk), (hv, dv_), (hr, dr)):
+                dst.copy_(hst, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        e2e_steps = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel() + r.numel()) * eb,
+               "d2h_bytes_per_step": out.numel() * eb}
+
+    peaks, peak_src = load_peaks()
+    tensor_path = w.dtype == "bf16" and w.d == 64 and w.dv == 64
+    achieved = causal_pairs(w) * parallax_flops_per_pair(w.d, w.dv) / (ms_per_step / 1e3) / 1e12
+    if tensor_path:
+        peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+        roof = {"kernel": "parallax (lla_parallax.cu, tcgen05)", "bound": "tensor",
+                "peak_source": f"bf16 dense, burst ({peak_src})"}
+    else:
+        peak = fp32_alu_peak_tflops(peaks)
+        roof = {"kernel": "parallax (lla_parallax.cu, CUDA cores)", "bound": "alu",
+                "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
+    roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                 "traffic": recorded_traffic("lla_parallax.cu"), "avg_launch_ms": ms_per_step})
+    if rank == 0:
+        line = {
+            "metric": METRIC_PARALLAX, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v, probe "
+                                   f"N(0,1/d) seed {w.seed + 100}, h={h}, seed {w.seed}",
+                       "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
+                       "l2": "flushed between steps (256 MiB write outside the step events)",
+                       "parallelism": f"replica per GPU x{world}"},
+            "tflops": achieved,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": n_launch,
+            "clocks": clk,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
+    ap.add_argument("--op", choices=["lla", "parallax"], default="lla",
+                    help="the operation timed: the LLA forward (default) or the Parallax forward")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -312,7 +455,7 @@ def main(argv=None):
     # The oracle's process pool is spawned before any GPU work (rank 0, one GPU only).
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        timer = OracleTimer(args.workload)
+        timer = OracleTimer(args.workload, args.op)
         v, cores, sample = timer.measure(float(os.environ.get("LLA_ORACLE_BUDGET_S", "20")), 900)
         timer.close()
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
@@ -320,6 +463,9 @@ def main(argv=None):
     from local_linear_attention_gb300 import binding as lla
     from local_linear_attention_gb300 import build as lla_build
     lla_build.build()
+
+    if args.op == "parallax":
+        return run_parallax(args, w, cpu, world, rank)
 
     lam, h = w.points[0]
     q, k, v = W.make_inputs(w)

@@ -142,6 +142,25 @@ int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx,
                 int B, int H, int T, int d, int dv, float h, int dtype, void* stream);
 
 /*
+ * Causal Parallax forward with a given probe ("Parallax" blog, s.2 paragraph "Parallax" and
+ * Appendix B with eta = 0; streaming form in s.3 "One extra branch, no extra I/O"; output
+ * combination as printed in Appendix C): for each query i over its causal prefix j <= i,
+ *     o_i = o_SA_i - Sigma_KV^(i) r_i = (1 + d2/d1) O1/d1 - O2/d1,
+ * where p_ij = exp(q_i . k_j / h) / sum_l exp(q_i . k_l / h) are the softmax weights, o_SA_i =
+ * sum_j p_ij v_j, Sigma_KV^(i) = sum_j p_ij (v_j - vbar_i)(k_j - kbar_i)^T (dv x d), and in the
+ * streaming form P1 = exp(q.k/h), P2 = P1 * (r_i . k_j), O1 = P1 V, O2 = P2 V, d1 = sum P1,
+ * d2 = sum P2. r = 0 gives causal softmax attention with scale 1/h.
+ * q, k, r: [B,H,T,d]; v, out: [B,H,T,dv]; all device, element type `dtype`, 16-byte aligned; the
+ * conventions at the top of this header apply (lambda plays no part). bf16 inputs with
+ * d = dv = 64 run on the tensor cores (weights rounded to bf16, P2 as an exact hi/lo bf16 pair,
+ * fp32 accumulation) unless lla_set_moments_path(1) forces the CUDA cores; everything else runs
+ * on the CUDA cores in fp32. Allocates nothing. Non-finite inputs give non-finite outputs; no
+ * status is recorded.
+ */
+int lla_parallax_forward(const void* q, const void* k, const void* v, const void* r, void* out,
+                         int B, int H, int T, int d, int dv, float h, int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns LLA_OK, LLA_ERR_NUMERICAL, LLA_ERR_TIMEOUT, LLA_ERR_INVALID_ARG (bad idx in
  * lla_moments) or LLA_ERR_CUDA (a sticky CUDA error or failed synchronisation).
@@ -159,7 +178,8 @@ int lla_version(void);
  * process: 0 = automatic (tensor cores -- tcgen05 with exact bf16 hi/lo products -- for bf16
  * inputs with d = 64, CUDA cores otherwise), 1 = CUDA cores always, 2 = tensor cores wherever
  * supported (currently the same as 0). Both compute the same moments; the choice exists for
- * testing and measurement. Returns LLA_ERR_INVALID_ARG for any other value. Host-only.
+ * testing and measurement. The same choice applies to lla_parallax_forward. Returns
+ * LLA_ERR_INVALID_ARG for any other value. Host-only.
  */
 int lla_set_moments_path(int path);
 

@@ -16,7 +16,7 @@ __all__ = [
     "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
     "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
-    "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
+    "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "lla_parallax_forward",
 ]
 
 LLA_OK = 0
@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
     "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path",
+    "lla_parallax_forward",
 )
 
 # LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
@@ -73,6 +74,7 @@ def _load():
         "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
         "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_set_moments_path": (i, [i]),
+        "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -138,6 +140,20 @@ def lla_forward(q, k, v, h: float, lam: float, out=None, stream=None):
     st = _load().lla_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, d,
                              dv, float(h), float(lam), code, _stream_ptr(stream))
     _check(st, "lla_forward")
+    return out
+
+
+def lla_parallax_forward(q, k, v, r, h: float, out=None, stream=None):
+    """Causal Parallax forward with probe r ([B,H,T,d], like q); returns `out` ([B,H,T,dv])."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    if r.shape != q.shape or r.dtype != q.dtype or not r.is_cuda or not r.is_contiguous():
+        raise ValueError("r must be a contiguous CUDA tensor shaped and typed like q")
+    if out is None:
+        out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    st = _load().lla_parallax_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                      out.data_ptr(), B, H, T, d, dv, float(h), code,
+                                      _stream_ptr(stream))
+    _check(st, "lla_parallax_forward")
     return out
 
 

@@ -265,6 +265,20 @@ int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx,
              : LLA_ERR_CUDA;
 }
 
+int lla_parallax_forward(const void* q, const void* k, const void* v, const void* r, void* out,
+                         int B, int H, int T, int d, int dv, float h, int dtype, void* stream) {
+  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, 1.f, dtype);
+  int st = check_forward(a);
+  if (st != LLA_OK || a.rows() == 0) return st;
+  if (!r || !aligned16(r)) return LLA_ERR_INVALID_ARG;
+  int* status = nullptr;
+  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;
+  const int path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
+  return launch_parallax(a, r, path, status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? LLA_OK
+             : LLA_ERR_CUDA;
+}
+
 int lla_stream_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return LLA_ERR_CUDA;

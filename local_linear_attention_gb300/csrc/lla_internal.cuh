@@ -80,6 +80,9 @@ inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+// Causal Parallax forward with probe r (same layout as q); tensor cores when path ==
+// kPathTensorCore and the shape is bf16 with d = dv = 64, CUDA cores otherwise.
+cudaError_t launch_parallax(const Args& a, const void* r, int path, int* status, cudaStream_t s);
 cudaError_t launch_debug_moments(const Args& a, const int64_t* idx, int n, float* m,
                                  float* omega, float* sk, float* sv, float* Skk, float* Svk,
                                  int* status, cudaStream_t s);

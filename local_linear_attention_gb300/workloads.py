@@ -86,6 +86,14 @@ def make_iid(B, H, T, d, dv, dtype, seed):
     return _cast(q, dtype), _cast(k, dtype), _cast(v, dtype)
 
 
+def make_probe(B, H, T, d, dtype, seed):
+    """Parallax probe r ~ N(0, 1/d) [B,H,T,d] from its own generator (seed), so that r . k has
+    unit variance for unit-variance keys; q, k, v of the same workload are unchanged by it."""
+    g = torch.Generator().manual_seed(seed)
+    r = torch.randn(B, H, T, d, generator=g, dtype=torch.float32) / math.sqrt(d)
+    return _cast(r, dtype)
+
+
 def make_stress(B, H, T, d, dv, dtype, seed, rank: int = 8, key_noise: float = 1e-3,
                 value_noise: float = 0.01):
     """Ill-conditioned keys, half of the queries outside the key cloud, near-affine values.
