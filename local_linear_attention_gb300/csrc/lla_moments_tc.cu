@@ -56,11 +56,9 @@ constexpr int KS = 6;                       // key-tile pipeline stages
 constexpr int KLAG = KS - 2;                // key blocks the loader keeps in flight
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int NFG = 8;                      // feature-generation warps
-constexpr int NWARPS = 4 + NSM + NFG;       // + Q K^T issuer, key loader, feature issuer, P loader
+constexpr int NWARPS = 3 + NSM + NFG;       // + Q K^T issuer, key loader, feature issuer
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 3;                     // P (TMEM) and F (shared memory) buffers
-constexpr int PS = 3;                       // staged P blocks in shared memory (passes 1..5)
-constexpr int PLAG = 1;                     // P blocks the P loader keeps in flight
 static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
 constexpr int NSB = 2;                      // S buffers
 static_assert(NSB == 2, "the Q K^T issuer indexes S buffers with g & 1");
@@ -79,13 +77,12 @@ constexpr int K_STAGE = KB * D * 2;
 constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
 constexpr int F_HALF = GPP * 512;
 constexpr int F_BUF = 2 * F_HALF;
-// One key block of P (128 rows x 32 keys, bf16) as the tcgen05.cp source image: 16-byte chunk kc
-// (keys 8kc..8kc+7) of row r at kc * 2048 + r * 16 (no-swizzle K-major core matrices, LBO 2048,
-// SBO 128). The same image is the block's layout in the global P scratch.
+// One key block of P (128 rows x 32 keys, bf16) in the global P scratch: 16-byte chunk kc (keys
+// 8kc..8kc+7) of row r at kc * 2048 + r * 16, so that each warp's stores of one chunk are 512
+// contiguous bytes.
 constexpr int P_BLOCK = BM * KB * 2;
-constexpr int SM_P = SM_F + NBUF * F_BUF;            // PS x 8 KB
 constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
-constexpr int SM_EPI = SM_P + PS * P_BLOCK;          // NSM x (32 rows x 36 floats)
+constexpr int SM_EPI = SM_F + NBUF * F_BUF;          // NSM x (32 rows x 36 floats)
 constexpr int SM_BAR = SM_EPI + NSM * 32 * EPI_LD * 4;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -214,8 +211,7 @@ struct Barriers {
   uint64_t kfull[KS], kempty[KS];
   uint64_t sfull[NSB], sfree[NSB];
   uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];  // P / F of a feature step written; consumed
-  uint64_t pready[PS], pempty[PS];                 // staged P block loaded; copied to TMEM
-  uint64_t accfull, accfree, done_qk, done_f, rowx, qready, p0done;
+  uint64_t accfull, accfree, done_qk, done_f, rowx, qready;
   float part[2][BM];  // per-row partial results of the two softmax halves (max, then omega)
 };
 
@@ -226,11 +222,6 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
       : "memory");
 }
 
-// Copies a 128-row x 32-byte tile (16 bf16 per row) from shared memory into 8 TMEM columns.
-// Implicitly ordered before tcgen05.mma issued later by the same thread.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc));
-}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
@@ -266,17 +257,12 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mbar_init(&bar.ffull[s], NFG);
       mbar_init(&bar.pfree[s], 1);
     }
-    for (int s = 0; s < PS; ++s) {
-      mbar_init(&bar.pready[s], 1);
-      mbar_init(&bar.pempty[s], 1);
-    }
     mbar_init(&bar.accfull, 1);
     mbar_init(&bar.accfree, NSM);
     mbar_init(&bar.done_qk, 1);
     mbar_init(&bar.done_f, 1);
     mbar_init(&bar.rowx, NSM);
     mbar_init(&bar.qready, 4);
-    mbar_init(&bar.p0done, NSM);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -333,24 +319,19 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mbar_wait(&bar.done_qk, 0, status, TO, &never);
     }
     __syncwarp();
-  } else if (warp == NWARPS - 2) {
+  } else if (warp == NWARPS - 1) {
     // ------------------------------------------------------------------ feature-contraction issuer
-    // Pass 0 contracts the P that the softmax warps wrote to tensor memory; passes 1..5 first copy
-    // the staged P block from shared memory into the same tensor-memory buffer (tcgen05.cp, which
-    // the MMAs issued after it by this thread observe).
     if (lane == 0) {
       const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
-      const uint64_t pd = smem_desc(smem_u32(smem + SM_P), 2048, 128);
       constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
       constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
       constexpr uint32_t nb_off = (NA / 8) * 512 / 16;
       const uint32_t t_acc = tbase + T_ACC, t_p = tbase + T_P;
       bool ok = true;
-      int pb = 0, b = 0, pass = 0, ps = 0;
-      uint32_t opar = 0, ppar = 0;  // parities of the current uses of buffer pb and stage ps
+      int pb = 0, b = 0, pass = 0;
+      uint32_t opar = 0;  // parity of the current use of operand buffer pb
       for (int h = 0; h < nb * NPASS && ok; ++h) {
-        ok = pass == 0 ? mbar_wait2(&bar.pfull[pb], opar, &bar.ffull[pb], opar, status, TO, abort_p)
-                       : mbar_wait2(&bar.pready[ps], ppar, &bar.ffull[pb], opar, status, TO, abort_p);
+        ok = mbar_wait2(&bar.pfull[pb], opar, &bar.ffull[pb], opar, status, TO, abort_p);
         if (ok && b == 0 && pass >= 1)
           ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
         if (!ok) break;
@@ -359,13 +340,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const uint64_t fl = fh + (F_HALF >> 4);
         const uint32_t a0 = t_p + pb * (KB / 2);
         const uint32_t acc0 = b > 0 ? 1u : 0u;
-        // The tensor-memory P buffer pb is free here: the feature warps wrote F(h) only after the
-        // MMAs of step h - NBUF, the last readers of buffer pb, had completed.
-        if (pass >= 1) {
-          const uint64_t pst = pd + (uint64_t)(ps * (P_BLOCK >> 4));
-          tmem_cp_128x256b(a0, pst);                    // keys 0..15
-          tmem_cp_128x256b(a0 + 8, pst + (4096 >> 4));  // keys 16..31
-        }
         // K-step 0 (keys 0..15), then K-step 1 (keys 16..31; +256 B in the F tiles); the hi and lo
         // tiles of each feature column go into the same accumulator.
         mma_ts(t_acc, a0, fh, id_a, acc0);
@@ -377,10 +351,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         mma_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
         mma_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
         mma_commit(&bar.pfree[pb]);
-        if (pass >= 1) {
-          mma_commit(&bar.pempty[ps]);
-          if (++ps == PS) { ps = 0; ppar ^= 1; }
-        }
         if (b == nb - 1) mma_commit(&bar.accfull);
         if (++pb == NBUF) { pb = 0; opar ^= 1; }
         if (++b == nb) { b = 0; ++pass; }
@@ -391,36 +361,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mbar_wait(&bar.done_f, 0, status, TO, &never);
     }
     __syncwarp();
-  } else if (warp == NWARPS - 1) {
-    // ------------------------------------------------------------------ P loader
-    // Stages the P blocks of passes 1..5 from the scratch, once the softmax warps have stored all
-    // of pass 0 (barrier p0done; their stores are fenced before they arrive).
-    const int U = nb * (NPASS - 1);
-    bool ok = warp_wait(&bar.p0done, 0, status, abort_p);
-    int b = 0;
-    for (int u = 0; u < U + PLAG && ok; ++u) {
-      if (u < U) {
-        const int ps = u % PS;
-        if (u >= PS && !warp_wait(&bar.pempty[ps], ((u / PS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
-        uint8_t* dst = smem + SM_P + ps * P_BLOCK;
-        const uint4* src = ptile + (long long)b * (P_BLOCK / 16);
-#pragma unroll
-        for (int t = 0; t < P_BLOCK / 512; ++t)
-          cp_async16(dst + (t * 32 + lane) * 16, src + t * 32 + lane, 16u);
-        if (++b == nb) b = 0;
-      }
-      cp_async_commit();
-      if (u >= PLAG) {
-        cp_async_wait<PLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.pready[(u - PLAG) % PS]);
-      }
-    }
-    if (!ok) cp_async_wait<0>();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
     // cp.async 16-byte copies, several key blocks in flight. Lane -> (row, chunk) mapping:
@@ -460,8 +400,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
     // accumulator columns [0, NA); half 1 takes keys 16..31 and columns [NA, NCH). Row max and
     // omega are combined across the halves through shared memory (barrier rowx: phase 0 after the
-    // max pass, phase 1 at the end). In feature pass 0 each P block also goes to the scratch, from
-    // which the later passes take it; after pass 0 these warps only drain the accumulators.
+    // max pass, phase 1 at the end). In feature pass 0 each thread also stores its 16 weights of
+    // each block to the scratch; in passes 1..5 it reads its own stores back (one block ahead)
+    // and writes them to tensor memory again, so Q K^T and the exponentials run only twice.
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
@@ -577,14 +518,37 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.pfull[pb]);
-      if (b == nb - 1) {
-        __threadfence();  // the scratch P blocks, before the P loader may read them
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.p0done);
-        if (!drain(0)) { ok = false; break; }
+      if (b == nb - 1 && !drain(0)) { ok = false; break; }
+    }
+    {
+      // This thread's weights of block b (pass 0 stored them: same row, same 16 keys).
+      constexpr int kChunk = 2048 / 16;
+      auto load_p = [&](int b, uint4& x0, uint4& x1) {
+        const uint4* src = ptile + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+        x0 = __ldcg(src);
+        x1 = __ldcg(src + kChunk);
+      };
+      uint4 n0, n1;
+      if (ok) load_p(0, n0, n1);
+      int h = nb;  // feature step index (pass 0 took h = 0 .. nb-1)
+      for (int pass = 1; pass < NPASS && ok; ++pass) {
+        for (int b = 0; b < nb; ++b, ++h) {
+          const uint4 c0 = n0, c1 = n1;
+          if (h + 1 < nb * NPASS) load_p(b + 1 < nb ? b + 1 : 0, n0, n1);
+          const int pb = h % NBUF;
+          if (h >= NBUF &&
+              !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          tmem_st8(lane_base + T_P + pb * (KB / 2) + half * (KB / 4), pw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.pfull[pb]);
+        }
+        if (ok) ok = drain(pass);
       }
     }
-    for (int pass = 1; pass < NPASS && ok; ++pass) ok = drain(pass);
     if (ok) {  // combine the halves' omega
       bar.part[half][r] = om;
       __syncwarp();
