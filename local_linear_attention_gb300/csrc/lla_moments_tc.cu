@@ -1,12 +1,12 @@
 // Tensor-core moments stage of the causal LLA forward (bf16 inputs, d = 64; tcgen05 + TMEM).
 //
-// Computes, for every query i of a 128-query tile and its causal prefix j <= i, the kernel-
-// weighted moments that the closed form of LLA needs ("Parallax" blog, s.2 Canonical
-// Formulation): omega = sum p_j, sk = sum p_j k_j and the upper triangle of S = sum p_j k_j k_j^T,
-// with p_j = exp((q_i.k_j - m_i)/h) and m_i the exact row max of q_i.k_j over the prefix.
+// Computes, for every query i and its causal prefix j <= i, the kernel-weighted moments that the
+// closed form of LLA needs ("Parallax" blog, s.2 Canonical Formulation): omega = sum p_j,
+// sk = sum p_j k_j and the upper triangle of S = sum p_j k_j k_j^T, with
+// p_j = exp((q_i.k_j - m_i)/h) and m_i the exact row max of q_i.k_j over the prefix.
 //
-// As a GEMM: [128 queries x keys] (P) times [keys x 2144 features] (F, the products
-// k_a * 1 and k_a * k_b, a <= b) into fp32 accumulators in tensor memory. Two facts shape it:
+// As a GEMM: [queries x keys] (P) times [keys x 2144 features] (F, the products k_a * 1 and
+// k_a * k_b, a <= b) into fp32 accumulators in tensor memory. Three facts shape it:
 //  * The products must be exact: rounding k_a k_b to bf16 breaks the Gram structure of S and
 //    makes the ridge system indefinite, whereas rounding the weights p to bf16 only perturbs the
 //    weights (all moments still describe one weighted problem). Each product of two bf16 values
@@ -14,18 +14,28 @@
 //    exact bf16, with one packed multiply and one packed fused multiply-add; every feature column
 //    is then contracted twice (hi and lo) into the same accumulator.
 //  * 2144 fp32 accumulator columns do not fit the 512 columns of tensor memory, so the features
-//    are swept in 6 passes of 368 columns; each pass streams the key prefix again and recomputes
-//    S = Q K^T and P (cheap next to the 2 x 368-column contraction it feeds).
-// A first pass over the prefix computes the exact row max m_i (only S = Q K^T and a max).
+//    are swept in 6 passes of 368 columns; each pass streams the key prefix again. A first sweep
+//    computes the exact row max m_i (Q K^T and a max); feature pass 0 computes P and also stores
+//    it (bf16) to a scratch, from which passes 1..5 take it again.
+//  * Feature tiles are generated per key block into shared memory and read back by the MMA, so
+//    shared-memory traffic per SM bounds the stage. Two CTAs on two SMs (a cluster pair) therefore
+//    share every MMA (tcgen05 cta_group::2, M = 256): each CTA holds 128 query rows (its tensor
+//    memory lanes) and generates and holds half of every feature tile (the B operand is split
+//    N/2 + N/2 between the pair's shared memories), halving the feature work per SM.
 //
-// Warp roles (19 warps): 0 issues Q K^T (one thread) and owns the TMEM allocation; 18 issues the
-// feature contraction (one thread); 1 stages key blocks (32 keys x 64) into shared memory; 2-9
-// turn S into P (one thread per query = TMEM lane, two warps per lane quarter splitting the keys
-// of a block) and drain the accumulators after each pass; 10-17 generate the exact hi/lo feature
-// tiles for each key block (one lane per key) into shared memory. P and the feature tiles are
-// triple-buffered. P lives in TMEM and is the A operand of the feature contraction (tcgen05.mma
-// with A in tensor memory). All operands in shared memory use the no-swizzle core-matrix layout.
-// Every mbarrier wait is bounded.
+// A pair covers 256 consecutive queries of one head; both CTAs stream the same key blocks (up to
+// the pair's last query; the causal mask zeroes the keys past a row). The even CTA (the leader)
+// issues all MMAs; its barriers that gate an MMA collect arrivals from both CTAs (mapa + remote
+// arrive), and MMA completion is signalled to both CTAs (multicast commit).
+//
+// Warp roles per CTA (19 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
+// allocation; 18 issues the feature contraction (leader; one thread); 1 stages key blocks (32
+// keys x 64) into shared memory; 2-9 turn S into P (one thread per query = TMEM lane, two warps
+// per lane quarter splitting the keys of a block) and drain the accumulators after each pass;
+// 10-17 generate this CTA's half of the exact hi/lo feature tiles (one lane per key). P and the
+// feature tiles are triple-buffered; P lives in TMEM as the A operand of the feature contraction.
+// All operands in shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is
+// bounded.
 //
 // Feature order (2208 slots = 1104 pairs, the layout of each output row): the upper triangle of
 // kt kt^T for the augmented key kt = [k_0..k_63, 1, 0], row by row: for row a, the pairs
@@ -45,25 +55,29 @@ namespace {
 using namespace tc;
 
 constexpr int D = 64;
-constexpr int BM = 128;                     // queries per CTA = MMA M = TMEM lanes
+constexpr int BM = 128;                     // query rows per CTA = TMEM lanes
+constexpr int PM = 2 * BM;                  // query rows per CTA pair = MMA M
 constexpr int KB = 32;                      // keys per block
 constexpr int NCH = 368;                    // features (accumulator columns) per pass
 constexpr int NPASS = 6;
 constexpr int NFP = NPASS * NCH;            // 2208, padded feature count (row stride of mom_tc)
-constexpr int GPP = NCH / 8;                // 46 groups of 8 features per pass
 constexpr int NA = 192, NB_ = NCH - NA;     // split of a pass into two MMAs (N <= 256)
+constexpr int GA = NA / 16, GB = NB_ / 16;  // 8-feature groups each CTA holds for either MMA
+constexpr int GLOC = GA + GB;               // 23 groups per CTA per pass
 constexpr int KS = 6;                       // key-tile pipeline stages
 constexpr int KLAG = KS - 2;                // key blocks the loader keeps in flight
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
-constexpr int NFG = 8;                      // feature-generation warps
+constexpr int NFG = 12;                     // feature-generation warps: two groups of NFGW that
+constexpr int NFGW = NFG / 2;               //   take alternate key blocks
 constexpr int NWARPS = 3 + NSM + NFG;       // + Q K^T issuer, key loader, feature issuer
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int NBUF = 3;                     // P (TMEM) and F (shared memory) buffers
-static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
+constexpr int NBUF = 3;                     // P buffers (tensor memory)
+constexpr int NFB = 5;                      // F buffers (shared memory)
 constexpr int NSB = 2;                      // S buffers
 static_assert(NSB == 2, "the Q K^T issuer indexes S buffers with g & 1");
+static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
 
-// tensor-memory columns
+// tensor-memory columns (the same in both CTAs of a pair)
 constexpr uint32_t T_ACC = 0;
 constexpr uint32_t T_S = NCH;               // NSB x 32 columns of fp32 logits
 constexpr uint32_t T_P = T_S + NSB * KB;    // NBUF x 16 columns of packed bf16 weights
@@ -71,21 +85,24 @@ constexpr uint32_t T_Q = T_P + NBUF * (KB / 2);  // 32 columns: the Q tile, A op
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
 
-// shared-memory layout (bytes)
+// shared-memory layout (bytes; the same offsets in both CTAs of a pair)
 constexpr int SM_K = 0;                              // KS x (32 x 64 bf16)
 constexpr int K_STAGE = KB * D * 2;
-constexpr int SM_F = SM_K + KS * K_STAGE;            // [2 buffers][hi, lo][46 groups x 512 B]
-constexpr int F_HALF = GPP * 512;
+constexpr int SM_F = SM_K + KS * K_STAGE;            // [NFB][hi, lo][23 groups x 512 B]
+constexpr int F_HALF = GLOC * 512;
 constexpr int F_BUF = 2 * F_HALF;
 // One key block of P (128 rows x 32 keys, bf16) in the global P scratch: 16-byte chunk kc (keys
 // 8kc..8kc+7) of row r at kc * 2048 + r * 16, so that each warp's stores of one chunk are 512
 // contiguous bytes.
 constexpr int P_BLOCK = BM * KB * 2;
 constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
-constexpr int SM_EPI = SM_F + NBUF * F_BUF;          // NSM x (32 rows x 36 floats)
+constexpr int SM_EPI = SM_F + NFB * F_BUF;           // NSM x (32 rows x 36 floats)
 constexpr int SM_BAR = SM_EPI + NSM * 32 * EPI_LD * 4;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// More than half of an SM's shared memory, so that at most one CTA (and one TMEM allocation of
+// all 512 columns) is resident per SM.
+constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
 
 // Pair p of the feature order (see the file comment): row a and even column b, or, for the odd
 // diagonal pairs, u = a.
@@ -154,45 +171,58 @@ __device__ __forceinline__ void feature_group(const uint32_t (&kw)[33], uint8_t*
   *reinterpret_cast<uint4*>(lo_row) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Groups [G0, G1) of pass PASS for one key (lane): writes into the F buffer halves at row
-// offset `row_off` (= (key / 8) * 128 + (key % 8) * 16).
-template <int PASS, int G0, int G1>
+// Global 8-feature group of a pass held by CTA `RANK` as its local group LG: the first GA local
+// groups belong to the N = 192 MMA (CTA 0 holds its groups 0..11, CTA 1 its groups 12..23), the
+// other GB to the N = 176 MMA (groups 24..34 and 35..45).
+__host__ __device__ constexpr int global_group(int rank, int lg) {
+  return lg < GA ? rank * GA + lg : 2 * GA + rank * GB + (lg - GA);
+}
+
+// Local groups [LG0, LG1) of pass PASS for one key (lane), written into the F buffer halves at
+// row offset `row_off` (= (key / 8) * 128 + (key % 8) * 16).
+template <int PASS, int RANK, int LG0, int LG1>
 __device__ __forceinline__ void feature_groups(const uint32_t (&kw)[33], uint8_t* fhi, uint8_t* flo,
                                                int row_off) {
-  if constexpr (G0 < G1) {
-    feature_group<(PASS * NCH + G0 * 8) / 2>(kw, fhi + G0 * 512 + row_off, flo + G0 * 512 + row_off);
-    feature_groups<PASS, G0 + 1, G1>(kw, fhi, flo, row_off);
+  if constexpr (LG0 < LG1) {
+    feature_group<(PASS * NCH + global_group(RANK, LG0) * 8) / 2>(kw, fhi + LG0 * 512 + row_off,
+                                                                  flo + LG0 * 512 + row_off);
+    feature_groups<PASS, RANK, LG0 + 1, LG1>(kw, fhi, flo, row_off);
   }
 }
 
-// Split of the 46 groups of a pass among the 8 feature warps: 6 x 6, then 2 x 5.
-__host__ __device__ constexpr int fw_begin(int fw) { return fw < 6 ? 6 * fw : 36 + 5 * (fw - 6); }
-static_assert(fw_begin(NFG) == GPP, "groups split");
+// Split of the 23 local groups among the NFGW warps of a feature group: 5 x 4, then 3.
+__host__ __device__ constexpr int fw_begin(int fw) { return 4 * fw < GLOC ? 4 * fw : GLOC; }
+static_assert(NFGW == 6 && fw_begin(NFGW) == GLOC && fw_begin(NFGW - 1) < GLOC, "groups split");
+
+template <int PASS, int RANK>
+__device__ __forceinline__ void generate_pr(int fw, const uint32_t (&kw)[33], uint8_t* fhi,
+                                            uint8_t* flo, int row_off) {
+  switch (fw) {
+    case 0: feature_groups<PASS, RANK, fw_begin(0), fw_begin(1)>(kw, fhi, flo, row_off); break;
+    case 1: feature_groups<PASS, RANK, fw_begin(1), fw_begin(2)>(kw, fhi, flo, row_off); break;
+    case 2: feature_groups<PASS, RANK, fw_begin(2), fw_begin(3)>(kw, fhi, flo, row_off); break;
+    case 3: feature_groups<PASS, RANK, fw_begin(3), fw_begin(4)>(kw, fhi, flo, row_off); break;
+    case 4: feature_groups<PASS, RANK, fw_begin(4), fw_begin(5)>(kw, fhi, flo, row_off); break;
+    default: feature_groups<PASS, RANK, fw_begin(5), GLOC>(kw, fhi, flo, row_off); break;
+  }
+}
 
 template <int PASS>
-__device__ __forceinline__ void generate_pass(int fw, const uint32_t (&kw)[33], uint8_t* fhi,
-                                              uint8_t* flo, int row_off) {
-  switch (fw) {
-    case 0: feature_groups<PASS, fw_begin(0), fw_begin(1)>(kw, fhi, flo, row_off); break;
-    case 1: feature_groups<PASS, fw_begin(1), fw_begin(2)>(kw, fhi, flo, row_off); break;
-    case 2: feature_groups<PASS, fw_begin(2), fw_begin(3)>(kw, fhi, flo, row_off); break;
-    case 3: feature_groups<PASS, fw_begin(3), fw_begin(4)>(kw, fhi, flo, row_off); break;
-    case 4: feature_groups<PASS, fw_begin(4), fw_begin(5)>(kw, fhi, flo, row_off); break;
-    case 5: feature_groups<PASS, fw_begin(5), fw_begin(6)>(kw, fhi, flo, row_off); break;
-    case 6: feature_groups<PASS, fw_begin(6), fw_begin(7)>(kw, fhi, flo, row_off); break;
-    default: feature_groups<PASS, fw_begin(7), GPP>(kw, fhi, flo, row_off); break;
-  }
+__device__ __forceinline__ void generate_pass(int rank, int fw, const uint32_t (&kw)[33],
+                                              uint8_t* fhi, uint8_t* flo, int row_off) {
+  if (rank == 0) generate_pr<PASS, 0>(fw, kw, fhi, flo, row_off);
+  else generate_pr<PASS, 1>(fw, kw, fhi, flo, row_off);
 }
 
-__device__ __forceinline__ void generate(int pass, int fw, const uint32_t (&kw)[33], uint8_t* fhi,
-                                         uint8_t* flo, int row_off) {
+__device__ __forceinline__ void generate(int pass, int rank, int fw, const uint32_t (&kw)[33],
+                                         uint8_t* fhi, uint8_t* flo, int row_off) {
   switch (pass) {
-    case 0: generate_pass<0>(fw, kw, fhi, flo, row_off); break;
-    case 1: generate_pass<1>(fw, kw, fhi, flo, row_off); break;
-    case 2: generate_pass<2>(fw, kw, fhi, flo, row_off); break;
-    case 3: generate_pass<3>(fw, kw, fhi, flo, row_off); break;
-    case 4: generate_pass<4>(fw, kw, fhi, flo, row_off); break;
-    default: generate_pass<5>(fw, kw, fhi, flo, row_off); break;
+    case 0: generate_pass<0>(rank, fw, kw, fhi, flo, row_off); break;
+    case 1: generate_pass<1>(rank, fw, kw, fhi, flo, row_off); break;
+    case 2: generate_pass<2>(rank, fw, kw, fhi, flo, row_off); break;
+    case 3: generate_pass<3>(rank, fw, kw, fhi, flo, row_off); break;
+    case 4: generate_pass<4>(rank, fw, kw, fhi, flo, row_off); break;
+    default: generate_pass<5>(rank, fw, kw, fhi, flo, row_off); break;
   }
 }
 
@@ -207,12 +237,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, kStatusTimeout, abort));
 }
 
+// Barriers marked (L) are used in the leader CTA only and collect arrivals from both CTAs; those
+// marked (M) are arrived on by multicast commits from the leader's MMA issuers in both CTAs.
 struct Barriers {
-  uint64_t kfull[KS], kempty[KS];
-  uint64_t sfull[NSB], sfree[NSB];
-  uint64_t pfull[NBUF], ffull[NBUF], pfree[NBUF];  // P / F of a feature step written; consumed
-  uint64_t accfull, accfree, done_qk, done_f, rowx, qready;
-  float part[2][BM];  // per-row partial results of the two softmax halves (max, then omega)
+  uint64_t kfull[KS];           // key block staged by this CTA's loader
+  uint64_t kfull_peer[KS];      // (L) key block staged by the peer's loader (for Q K^T only)
+  uint64_t kempty[KS];          // key stage consumed: (M) Q K^T commit or 1 extra arrival, + NFGW
+  uint64_t sfull[NSB];          // (M) S = Q K^T in tensor memory
+  uint64_t sfree[NSB];          // (L) S read by both CTAs' softmax warps
+  uint64_t pfull[NBUF];         // (L) P written to tensor memory in both CTAs
+  uint64_t ffull[NFB];          // (L) F halves written in both CTAs
+  uint64_t pfree[NBUF];         // (M) the feature MMAs of a step completed (P buffer free)
+  uint64_t ffree[NFB];          // (M) the same, for the F buffer
+  uint64_t accfull;             // (M) the accumulators of a pass are final
+  uint64_t accfree;             // (L) both CTAs drained them
+  uint64_t qready;              // (L) both CTAs' Q tiles in tensor memory
+  uint64_t done_qk, done_f;     // (M) every MMA of either issuer completed
+  uint64_t rowx;                // this CTA's softmax halves exchanged row max / omega
+  float part[2][BM];            // per-row partial results of the two softmax halves
 };
 
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
@@ -222,8 +264,16 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
       : "memory");
 }
 
+// Arrival of one of this CTA's producers on a leader barrier (L). Every producer has completed
+// what the leader consumes before it arrives (see mbar_arrive_cluster_relaxed), so the peer's
+// arrival needs no cluster-wide release, and the leader's issuers test these barriers with the
+// ordinary (CTA-scope) wait; the leader's own producers arrive locally.
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader) {
+  if (leader) mbar_arrive(bar);
+  else mbar_arrive_cluster_relaxed(bar, 0);
+}
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
                   int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ mraw_out,
                   float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pscr,
@@ -234,140 +284,152 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ntiles = (T + BM - 1) / BM;
-  const int tile = ntiles - 1 - (int)(blockIdx.x / BH);  // longest causal prefixes first
-  const long long bh = blockIdx.x % BH;
-  const int i0 = tile * BM;
-  const int nq = min(BM, T - i0);
-  const int jend = i0 + nq;
+  const int rank = (int)cluster_ctarank();
+  const bool leader = rank == 0;
+  const int npairs = (T + PM - 1) / PM;
+  const int pair_lin = (int)(blockIdx.x >> 1);
+  const int ptile = npairs - 1 - pair_lin / BH;  // longest causal prefixes first
+  const long long bh = pair_lin % BH;
+  const int i0p = ptile * PM;
+  const int i0 = i0p + rank * BM;                // this CTA's first query row
+  const int nq = max(0, min(BM, T - i0));
+  const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
   const int nb = (jend + KB - 1) / KB;
   const int G = nb * (1 + NPASS);
   const long long base = bh * T;
-  // This tile's P blocks in the scratch: earlier tiles of the head hold 4, 8, ... blocks.
-  uint4* const ptile = pscr + (bh * pblk_per_head + 2ll * tile * (tile + 1)) * (P_BLOCK / 16);
+  // This CTA's P blocks in the scratch: earlier pairs of the head hold 2 x 8, 2 x 16, ... blocks.
+  uint4* const ptile_p =
+      pscr + (bh * pblk_per_head + 8ll * ptile * (ptile + 1) + (long long)rank * nb) * (P_BLOCK / 16);
+  // Rows of this CTA's key stage: the Q K^T operand takes rows 0..15 of each CTA's stage as its
+  // N/2 keys, so CTA 1 keeps keys 16..31 of a block in rows 0..15 (row = key ^ 16 * rank).
+  const int krot = 16 * rank;
 
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kfull[s], 1); mbar_init(&bar.kempty[s], 1 + NFG); }
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar.kfull[s], 1);
+      mbar_init(&bar.kfull_peer[s], 1);
+      mbar_init(&bar.kempty[s], 1 + NFGW);
+    }
     for (int s = 0; s < NSB; ++s) {
       mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], NSM);
+      mbar_init(&bar.sfree[s], 2 * NSM);
     }
     for (int s = 0; s < NBUF; ++s) {
-      mbar_init(&bar.pfull[s], NSM);
-      mbar_init(&bar.ffull[s], NFG);
+      mbar_init(&bar.pfull[s], 2 * NSM);
       mbar_init(&bar.pfree[s], 1);
     }
+    for (int s = 0; s < NFB; ++s) {
+      mbar_init(&bar.ffull[s], 2 * NFGW);
+      mbar_init(&bar.ffree[s], 1);
+    }
     mbar_init(&bar.accfull, 1);
-    mbar_init(&bar.accfree, NSM);
+    mbar_init(&bar.accfree, 2 * NSM);
+    mbar_init(&bar.qready, 2 * 4);
     mbar_init(&bar.done_qk, 1);
     mbar_init(&bar.done_f, 1);
     mbar_init(&bar.rowx, NSM);
-    mbar_init(&bar.qready, 4);
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base_s, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(&tmem_base_s, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
   volatile int* abort_p = &abort_flag;
   const int TO = kStatusTimeout;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ Q K^T issuer
-    // Two threads issue the tensor-core work (this one and the feature issuer), because a single
-    // thread's serial issue cost -- mbarrier tests, descriptor arithmetic and the MMA/commit
-    // instructions themselves -- exceeds the tensor work of a key block. tcgen05.commit tracks
-    // the issuing thread's own MMAs, so each thread signals and drains its own. Q K^T runs only in
-    // the max pass and feature pass 0; later passes reuse the P that pass 0 stored.
-    if (lane == 0) {
+    // ------------------------------------------------------------------ Q K^T issuer (leader)
+    // Two threads issue the tensor-core work (this one and the feature issuer): a single thread's
+    // serial issue cost -- mbarrier tests, descriptor arithmetic and the MMA/commit instructions
+    // -- exceeds the tensor work of a key block. tcgen05.commit tracks the issuing thread's own
+    // MMAs, so each thread signals and drains its own. Q K^T runs only in the max sweep and
+    // feature pass 0.
+    if (leader && lane == 0) {
       const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
-      constexpr uint32_t id_qk = idesc_bf16(BM, KB, false, false);
+      constexpr uint32_t id_qk = idesc_bf16(PM, KB, false, false);
       const uint32_t t_s = tbase + T_S, t_q = tbase + T_Q;
-      bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);  // Q tile in tensor memory
+      bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);
       int st = 0;
       uint32_t kpar = 0;  // parity of the current fill of key stage st
       for (int g = 0; g < 2 * nb && ok; ++g) {
         const int sb = g & 1;
-        ok = g >= NSB ? mbar_wait2(&bar.kfull[st], kpar, &bar.sfree[sb], ((g >> 1) - 1) & 1,
-                                   status, TO, abort_p)
-                      : mbar_wait(&bar.kfull[st], kpar, status, TO, abort_p);
+        ok = mbar_wait2(&bar.kfull[st], kpar, &bar.kfull_peer[st], kpar, status, TO, abort_p);
+        if (ok && g >= NSB)
+          ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, TO, abort_p);
         if (!ok) break;
         tc_fence_after();
         // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
         // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
         const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
         const uint32_t ts = t_s + sb * KB;
-        mma_ts(ts, t_q, kst, id_qk, 0u);
-        mma_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
-        mma_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
-        mma_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
-        mma_commit(&bar.sfull[sb]);
-        mma_commit(&bar.kempty[st]);
+        mma2_ts(ts, t_q, kst, id_qk, 0u);
+        mma2_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
+        mma2_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
+        mma2_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
+        mma2_commit_both(&bar.sfull[sb]);
+        mma2_commit_both(&bar.kempty[st]);
         if (++st == KS) { st = 0; kpar ^= 1; }
       }
       if (!ok) *abort_p = 1;
-      // Drain: wait (bounded, whatever the abort flag says) until every MMA this thread issued
-      // has completed, so that tensor memory is not released under a running MMA.
-      mma_commit(&bar.done_qk);
-      volatile int never = 0;
-      mbar_wait(&bar.done_qk, 0, status, TO, &never);
+      mma2_commit_both(&bar.done_qk);
     }
     __syncwarp();
   } else if (warp == NWARPS - 1) {
-    // ------------------------------------------------------------------ feature-contraction issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ feature issuer (leader)
+    if (leader && lane == 0) {
       const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
-      constexpr uint32_t id_a = idesc_bf16(BM, NA, false, true);
-      constexpr uint32_t id_b = idesc_bf16(BM, NB_, false, true);
-      constexpr uint32_t nb_off = (NA / 8) * 512 / 16;
+      constexpr uint32_t id_a = idesc_bf16(PM, NA, false, true);
+      constexpr uint32_t id_b = idesc_bf16(PM, NB_, false, true);
+      constexpr uint32_t nb_off = GA * 512 / 16;  // local group GA: the N = 176 MMA's half
       const uint32_t t_acc = tbase + T_ACC, t_p = tbase + T_P;
       bool ok = true;
-      int pb = 0, b = 0, pass = 0;
-      uint32_t opar = 0;  // parity of the current use of operand buffer pb
+      int pb = 0, fb = 0, b = 0, pass = 0;
+      uint32_t ppar = 0, fpar = 0;  // parities of the current uses of P buffer pb, F buffer fb
       for (int h = 0; h < nb * NPASS && ok; ++h) {
-        ok = mbar_wait2(&bar.pfull[pb], opar, &bar.ffull[pb], opar, status, TO, abort_p);
+        ok = mbar_wait2(&bar.pfull[pb], ppar, &bar.ffull[fb], fpar, status, TO, abort_p);
         if (ok && b == 0 && pass >= 1)
           ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t fh = fd + (uint64_t)(pb * (F_BUF >> 4));
+        const uint64_t fh = fd + (uint64_t)(fb * (F_BUF >> 4));
         const uint64_t fl = fh + (F_HALF >> 4);
         const uint32_t a0 = t_p + pb * (KB / 2);
         const uint32_t acc0 = b > 0 ? 1u : 0u;
         // K-step 0 (keys 0..15), then K-step 1 (keys 16..31; +256 B in the F tiles); the hi and lo
         // tiles of each feature column go into the same accumulator.
-        mma_ts(t_acc, a0, fh, id_a, acc0);
-        mma_ts(t_acc, a0, fl, id_a, 1u);
-        mma_ts(t_acc + NA, a0, fh + nb_off, id_b, acc0);
-        mma_ts(t_acc + NA, a0, fl + nb_off, id_b, 1u);
-        mma_ts(t_acc, a0 + 8, fh + 16, id_a, 1u);
-        mma_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
-        mma_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
-        mma_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
-        mma_commit(&bar.pfree[pb]);
-        if (b == nb - 1) mma_commit(&bar.accfull);
-        if (++pb == NBUF) { pb = 0; opar ^= 1; }
+        mma2_ts(t_acc, a0, fh, id_a, acc0);
+        mma2_ts(t_acc, a0, fl, id_a, 1u);
+        mma2_ts(t_acc + NA, a0, fh + nb_off, id_b, acc0);
+        mma2_ts(t_acc + NA, a0, fl + nb_off, id_b, 1u);
+        mma2_ts(t_acc, a0 + 8, fh + 16, id_a, 1u);
+        mma2_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
+        mma2_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
+        mma2_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
+        mma2_commit_both(&bar.pfree[pb]);
+        mma2_commit_both(&bar.ffree[fb]);
+        if (b == nb - 1) mma2_commit_both(&bar.accfull);
+        if (++pb == NBUF) { pb = 0; ppar ^= 1; }
+        if (++fb == NFB) { fb = 0; fpar ^= 1; }
         if (++b == nb) { b = 0; ++pass; }
       }
       if (!ok) *abort_p = 1;
-      mma_commit(&bar.done_f);
-      volatile int never = 0;
-      mbar_wait(&bar.done_f, 0, status, TO, &never);
+      mma2_commit_both(&bar.done_f);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
     // cp.async 16-byte copies, several key blocks in flight. Lane -> (row, chunk) mapping:
     // rows (lane & 7) + 8 * (t & 3), chunks (lane >> 3) + 4 * (t >> 2): each 8-lane phase writes
-    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors.
-    // A block becomes visible to the MMA (async proxy) only after its copies completed and this
-    // warp fenced them (cp.async writes belong to the generic proxy).
+    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors. A block becomes
+    // visible to the MMA (async proxy) only after its copies completed and this warp fenced them
+    // (cp.async writes belong to the generic proxy); the leader's Q K^T waits for both CTAs.
     const __nv_bfloat16* kb = k + base * D;
     bool ok = true;
     for (int g = 0; g < G + KLAG; ++g) {
@@ -381,7 +443,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
-          const int j = b * KB + r;
+          const int j = b * KB + (r ^ krot);
           const bool in = j < jend;
           cp_async16(dst + kmaj_off(r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
         }
@@ -391,7 +453,14 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         cp_async_wait<KLAG>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.kfull[(g - KLAG) % KS]);
+        if (lane == 0) {
+          const int s = (g - KLAG) % KS;
+          mbar_arrive(&bar.kfull[s]);
+          // The leader's Q K^T also reads this CTA's stage. Only steps that run Q K^T are
+          // reported: that barrier's waiter stops after them, and every refill before then
+          // waits for the Q K^T commit, so it never runs a phase ahead of its waiter.
+          if (!leader && g - KLAG < 2 * nb) mbar_arrive_cluster_relaxed(&bar.kfull_peer[s], 0);
+        }
       }
     }
     if (!ok) cp_async_wait<0>();
@@ -400,7 +469,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
     // accumulator columns [0, NA); half 1 takes keys 16..31 and columns [NA, NCH). Row max and
     // omega are combined across the halves through shared memory (barrier rowx: phase 0 after the
-    // max pass, phase 1 at the end). In feature pass 0 each thread also stores its 16 weights of
+    // max sweep, phase 1 at the end). In feature pass 0 each thread also stores its 16 weights of
     // each block to the scratch; in passes 1..5 it reads its own stores back (one block ahead)
     // and writes them to tensor memory again, so Q K^T and the exponentials run only twice.
     const int quarter = warp & 3, half = (warp - 2) >> 2;
@@ -411,7 +480,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int c_lo = half * (KB / 2);
     const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
     if (half == 0) {  // this row of Q into tensor memory (packed bf16 pairs, 32 columns)
-      const uint4* qr = reinterpret_cast<const uint4*>(q + (base + i) * D);
+      const uint4* qr = reinterpret_cast<const uint4*>(q + (base + (valid ? i : 0)) * D);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
@@ -422,7 +491,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.qready);
+      if (lane == 0) arrive_leader(&bar.qready, leader);
     }
     float* epi = reinterpret_cast<float*>(smem + SM_EPI) + (warp - 2) * 32 * EPI_LD;
     // Drains this half's accumulator columns of feature pass `pass` into its slots of mom.
@@ -464,7 +533,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.accfree);
+      if (lane == 0) arrive_leader(&bar.accfree, leader);
       return true;
     };
     float m = -INFINITY, om = 0.f;
@@ -478,10 +547,10 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
+      if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
       const int b = g < nb ? g : g - nb;
       const int j0 = b * KB + c_lo;
-      if (g < nb) {  // max pass
+      if (g < nb) {  // max sweep
 #pragma unroll
         for (int c = 0; c < KB / 2; ++c)
           if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
@@ -507,7 +576,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
       // This row's 16 weights as chunks 2*half and 2*half + 1 of the block's image.
       constexpr int kChunk = 2048 / 16;  // chunk stride of the image, in 16-byte units
-      uint4* pdst = ptile + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+      uint4* pdst = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
       pdst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       pdst[kChunk] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
       if (b >= NBUF &&
@@ -517,14 +586,14 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.pfull[pb]);
+      if (lane == 0) arrive_leader(&bar.pfull[pb], leader);
       if (b == nb - 1 && !drain(0)) { ok = false; break; }
     }
     {
       // This thread's weights of block b (pass 0 stored them: same row, same 16 keys).
       constexpr int kChunk = 2048 / 16;
       auto load_p = [&](int b, uint4& x0, uint4& x1) {
-        const uint4* src = ptile + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+        const uint4* src = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
         x0 = __ldcg(src);
         x1 = __ldcg(src + kChunk);
       };
@@ -544,7 +613,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar.pfull[pb]);
+          if (lane == 0) arrive_leader(&bar.pfull[pb], leader);
         }
         if (ok) ok = drain(pass);
       }
@@ -560,44 +629,66 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       }
     }
   } else {
-    // ------------------------------------------------------------------ feature generation (warps 10-17)
-    const int fw = warp - 2 - NSM;
-    const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;
-    for (int g = 0; g < G; ++g) {
-      const int st = g % KS;
-      if (!warp_wait(&bar.kfull[st], (g / KS) & 1, status, abort_p)) break;
-      if (g < nb) {  // max pass: nothing to generate
+    // ------------------------------------------------------------------ feature generation (warps 10-21)
+    // Group `grp` (warps 10-15 or 16-21) takes the key blocks of steps g with g % 2 == grp, so
+    // each warp has two steps' time for its serial chain (barrier tests, key-word loads, the
+    // products, the proxy fence).
+    const int fwi = warp - 2 - NSM, grp = fwi / NFGW, fw = fwi % NFGW;
+    const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;  // key `lane` in the F tiles
+    int st = grp, h = grp - nb, pass = -1, bcnt = 0;
+    uint32_t kpar = 0;
+    for (int g = grp; g < G; g += 2) {
+      if (!warp_wait(&bar.kfull[st], kpar, status, abort_p)) break;
+      if (g < nb) {  // max sweep: nothing to generate
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.kempty[st]);
-        continue;
-      }
-      const int h = g - nb, pass = h / nb, pb = h % NBUF;
-      uint32_t kw[33];
-      const uint8_t* krow = smem + SM_K + st * K_STAGE;
+      } else {
+        if (pass < 0) { pass = h / nb; bcnt = h % nb; }  // this group's first feature step
+        const int fb = h % NFB;
+        uint32_t kw[33];
+        const uint8_t* krow = smem + SM_K + st * K_STAGE;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(krow + kmaj_off(lane, c));
-        kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(krow + kmaj_off(lane ^ krot, c));
+          kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
+        }
+        kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
+        __syncwarp();
+        // Passes 1..5 run no Q K^T, whose completion is the stage's other release: warp 0 of
+        // the group arrives for it.
+        if (lane == 0) mbar_arrive_cnt(&bar.kempty[st], (pass >= 1 && fw == 0) ? 2u : 1u);
+        if (h >= NFB && !warp_wait(&bar.ffree[fb], ((h / NFB) - 1) & 1, status, abort_p)) break;
+        uint8_t* fhi = smem + SM_F + fb * F_BUF;
+        generate(pass, rank, fw, kw, fhi, fhi + F_HALF, row_off);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&bar.ffull[fb], leader);
       }
-      kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
-      __syncwarp();
-      // Passes 1..5 run no Q K^T, whose completion is the stage's other release: warp 0 of this
-      // group arrives for it.
-      if (lane == 0) mbar_arrive_cnt(&bar.kempty[st], (pass >= 1 && fw == 0) ? 2u : 1u);
-      if (h >= NBUF && !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) break;
-      uint8_t* fhi = smem + SM_F + pb * F_BUF;
-      generate(pass, fw, kw, fhi, fhi + F_HALF, row_off);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.ffull[pb]);
+      // next step of this group: g + 2
+      h += 2;
+      if (pass >= 0) {
+        bcnt += 2;
+        while (bcnt >= nb) { bcnt -= nb; ++pass; }
+      }
+      st += 2;
+      if (st >= KS) { st -= KS; kpar ^= 1; }
     }
   }
 
+  // Teardown: tensor memory is released only after every MMA of the pair has completed (bounded
+  // waits, whatever the abort flag says), and neither CTA exits before the other has made its
+  // last arrival on it.
+  if (warp == 0 && lane == 0) {
+    volatile int never = 0;
+    mbar_wait(&bar.done_qk, 0, status, TO, &never);
+    mbar_wait(&bar.done_f, 0, status, TO, &never);
+  }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tbase, TMEM_COLS);
+    tmem_dealloc_pair(tbase, TMEM_COLS);
   }
 }
 
@@ -606,8 +697,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 size_t moments_tc_row_floats() { return NFP; }
 
 long long moments_tc_pblocks_per_head(int T) {
-  const long long nt = (T + BM - 1) / BM;
-  return nt > 0 ? 2 * (nt - 1) * nt + (T + KB - 1) / KB : 0;
+  const long long np = (T + PM - 1) / PM;
+  return np > 0 ? 8 * (np - 1) * np + 2ll * ((T + KB - 1) / KB) : 0;
 }
 
 size_t moments_tc_pscratch_bytes(long long BH, int T) {
@@ -617,11 +708,11 @@ size_t moments_tc_pscratch_bytes(long long BH, int T) {
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   auto kern = moments_tc_kernel;
   cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
   if (err != cudaSuccess) return err;
-  const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
+  const long long blocks = 2ll * ((a.T + PM - 1) / PM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
+  kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
       (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
       moments_tc_pblocks_per_head(a.T), ws.status);
