@@ -311,6 +311,221 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   }
 }
 
+// ----------------------------------------------------------------------------- solve, tensor-core rows
+// d = 64 with the tensor-core stage's moment rows (2208 floats in the order tc_slot() decodes;
+// omega and the row max in their own arrays). Same factorisation as solve_kernel (lane l owns rows
+// l and 63 - l, column k broadcast through shared memory, forward substitution as an extra
+// column), arranged for throughput:
+//  * the moment row goes from global memory straight into the registers that hold the matrix (for
+//    a fixed triangle row j the slots of (j, r), r > j, are consecutive, so each load of a warp is
+//    one contiguous run), instead of being staged in shared memory;
+//  * the trailing updates run as packed fp32 pairs (fma.rn.f32x2: the same single-rounded FMA on
+//    two lanes of a 64-bit register pair), which halves their instruction count;
+//  * the factor goes to shared memory as a packed triangle (row r at r(r+1)/2): a warp's stores of
+//    one column and its loads of one row are both free of bank conflicts (the triangular numbers
+//    0..31 are distinct mod 32), and it needs 8 KB per warp instead of 17, so that 16 warps fit
+//    on an SM.
+namespace stc {
+constexpr int D = 64;
+constexpr int WARPS = 4;                 // warps (queries) per block
+constexpr int TRI = D * (D + 1) / 2;     // packed lower triangle of L
+constexpr int WARP_FLOATS = TRI + 2 * D + D;  // L, two column buffers, the vector s = sum p k
+
+__host__ __device__ constexpr int tri(int r) { return r * (r + 1) / 2; }
+// Slot of (a, b) in a tensor-core moment row for b >= a + (a & 1) (the run of row a):
+// run_base(a) + b.
+__host__ __device__ constexpr int run_base(int a) {
+  const int t = a >> 1;
+  const int rs = 65 * t - t * (t - 1) + ((a & 1) ? 33 - t : 0);
+  return 2 * rs - (a + (a & 1));
+}
+
+// x -= s * c on a packed pair (x0, x1) with c = (c0, c1); ns = -s.
+__device__ __forceinline__ void fma2(float& x0, float& x1, float ns, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, c, s;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 c, {%2, %3};\n\t"
+      "mov.b64 s, {%4, %4};\n\t"
+      "fma.rn.f32x2 x, s, c, x;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(c0), "f"(c1), "f"(ns));
+}
+
+// a[j] -= lik * cb[j] for K < j < N (ns = -lik); cb is 16-byte aligned.
+template <int N, int K>
+__device__ __forceinline__ void trail(float (&a)[N], float ns, const float* cb) {
+  constexpr int j0 = K + 1;
+  if constexpr (j0 < N) {
+    if constexpr (j0 & 1) a[j0] = fmaf(ns, cb[j0], a[j0]);
+    constexpr int je = (j0 + 1) & ~1;  // first even index >= j0
+    constexpr int jq = (je + 3) & ~3;  // first multiple of 4 >= je
+    if constexpr (je < jq && je < N) {
+      const float2 c = *reinterpret_cast<const float2*>(cb + je);
+      fma2(a[je], a[je + 1], ns, c.x, c.y);
+    }
+#pragma unroll
+    for (int j = jq; j < N; j += 4) {
+      const float4 c = *reinterpret_cast<const float4*>(cb + j);
+      fma2(a[j], a[j + 1], ns, c.x, c.y);
+      fma2(a[j + 2], a[j + 3], ns, c.z, c.w);
+    }
+  }
+}
+
+struct Lane {
+  float a0[32];   // row r0 = lane (entries 0..r0; the rest is padding, updated and never read)
+  float a1[64];   // row r1 = 63 - lane (entries 0..r1)
+  float z0, z1;   // right-hand sides, then the forward-substituted z'
+  float inv0, inv1;  // 1 / L[r][r]
+  int r0, r1;
+  bool ok;
+};
+
+template <int K>
+__device__ __forceinline__ void column(Lane& L, float* cbuf, float* Lt) {
+  constexpr bool lo = K < 32;
+  constexpr int owner = lo ? K : D - 1 - K;
+  float piv = __shfl_sync(0xffffffffu, lo ? L.a0[lo ? K : 0] : L.a1[K], owner);
+  if (!(piv > 0.f)) { L.ok = false; piv = 1.f; }  // rows of a failed factorisation become NaN
+  const float inv = rsqrtf(piv);
+  const float zk = __shfl_sync(0xffffffffu, lo ? L.z0 : L.z1, owner) * inv;
+  float* cb = cbuf + (K & 1) * D;
+  // Column K of the factor is final: into the column buffer (for the trailing update) and, for
+  // rows at or below the diagonal, into the packed triangle (for the backward substitution), so
+  // that its registers are free from here on.
+  if constexpr (lo) {
+    L.a0[K] *= inv;  // the owner's entry becomes piv * inv = L[K][K]
+    if (L.r0 == K) { L.inv0 = inv; L.z0 = zk; }
+    cb[L.r0] = L.a0[K];
+    if (L.r0 >= K) Lt[tri(L.r0) + K] = L.a0[K];
+  }
+  L.a1[K] *= inv;
+  if (L.r1 == K) { L.inv1 = inv; L.z1 = zk; }
+  cb[L.r1] = L.a1[K];
+  if (L.r1 >= K) Lt[tri(L.r1) + K] = L.a1[K];
+  __syncwarp();
+  if constexpr (lo) {
+    trail<32, K>(L.a0, -L.a0[K], cb);
+    if (L.r0 > K) L.z0 = fmaf(-L.a0[K], zk, L.z0);
+  }
+  trail<64, K>(L.a1, -L.a1[K], cb);
+  if (L.r1 > K) L.z1 = fmaf(-L.a1[K], zk, L.z1);
+  if constexpr (K + 1 < D) column<K + 1>(L, cbuf, Lt);
+}
+
+// Backward substitution L^T y = z' from the last row: y_K = w_K / L[K][K], then
+// w_r -= L[K][r] y_K for r < K, with row K of L read from the packed triangle. A runtime loop:
+// unrolled, the compiler would hoist the triangle loads of many rows at once and spill.
+__device__ __forceinline__ void back(const Lane& L, const float* Lt, float& w0, float& w1,
+                                     float& y0, float& y1) {
+#pragma unroll 2
+  for (int K = D - 1; K >= 0; --K) {
+    const bool lo = K < 32;
+    const int owner = lo ? K : D - 1 - K;
+    const float yk = __shfl_sync(0xffffffffu, lo ? w0 * L.inv0 : w1 * L.inv1, owner);
+    const float* rowK = Lt + tri(K);
+    if (L.r0 == K) y0 = yk;
+    if (L.r1 == K) y1 = yk;
+    if (L.r0 < K) w0 = fmaf(-rowK[L.r0], yk, w0);
+    if (L.r1 < K) w1 = fmaf(-rowK[L.r1], yk, w1);
+  }
+}
+}  // namespace stc
+
+__global__ void __launch_bounds__(stc::WARPS * 32, 3)
+solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mom, const float* __restrict__ omega,
+                const float* __restrict__ mrow, long long rows, float lam, float* __restrict__ y_out,
+                float* __restrict__ kbar_out, int* __restrict__ status) {
+  using namespace stc;
+  __shared__ __align__(16) float sh[WARPS][WARP_FLOATS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * WARPS + warp;
+  if (row >= rows) return;  // whole warp leaves together
+  float* Lt = sh[warp];
+  float* cbuf = Lt + TRI;
+  float* sv = cbuf + 2 * D;
+  const float* g = mom + row * TC_ROW;
+
+  Lane L;
+  L.r0 = lane;
+  L.r1 = D - 1 - lane;
+  L.ok = true;
+  L.inv0 = L.inv1 = 1.f;
+  // Every load of the row first (predicated, all in flight together), then the arithmetic.
+#pragma unroll
+  for (int j = 0; j < 32; ++j) L.a0[j] = j <= L.r0 ? __ldcs(g + run_base(j) + L.r0) : 0.f;
+#pragma unroll
+  for (int j = 0; j < D; ++j) L.a1[j] = j <= L.r1 ? __ldcs(g + run_base(j) + L.r1) : 0.f;
+  const float d0 = __ldcs(g + tc_slot(L.r0, L.r0)), d1 = __ldcs(g + tc_slot(L.r1, L.r1));
+  const float s0 = __ldcs(g + run_base(L.r0) + D), s1 = __ldcs(g + run_base(L.r1) + D);
+  const float om = omega[row];
+  const float qa = ldf(q, row * D + L.r0);  // keys are not shifted on this path (c = 0)
+  const float qb = ldf(q, row * D + L.r1);
+  double lpd = (double)lam * exp(-(double)mrow[row]);  // ridge scaled by exp(-m)
+  lpd = fmin(fmax(lpd, (double)FLT_MIN), (double)FLT_MAX);
+  const float lp = (float)lpd;
+  sv[L.r0] = s0;
+  sv[L.r1] = s1;
+  __syncwarp();
+  const float inv_om = 1.f / om;
+  const float kb0 = s0 * inv_om, kb1 = s1 * inv_om;
+  L.z0 = qa - kb0;
+  L.z1 = qb - kb1;
+  // C_kk + lambda' I = S - s s^T / omega + lambda' I, row by row (the odd diagonal entries sit
+  // outside the rows' runs).
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
+    const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float v = L.r0 == j + u ? d0 + lp : L.a0[j + u];
+      v = fmaf(-sj[u], kb0, v);
+      L.a0[j + u] = j + u <= L.r0 ? v : 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < D; j += 4) {
+    const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
+    const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float v = L.r1 == j + u ? d1 + lp : L.a1[j + u];
+      v = fmaf(-sj[u], kb1, v);
+      L.a1[j + u] = j + u <= L.r1 ? v : 0.f;
+    }
+  }
+
+  stc::column<0>(L, cbuf, Lt);
+  if (!L.ok) {
+    if (lane == 0) atomicOr(status, kStatusNumerical);
+    const float qn = __int_as_float(0x7fc00000);
+    y_out[row * D + L.r0] = qn;
+    y_out[row * D + L.r1] = qn;
+    kbar_out[row * D + L.r0] = qn;
+    kbar_out[row * D + L.r1] = qn;
+    return;
+  }
+  __syncwarp();
+  float w0 = L.z0, w1 = L.z1, y0 = 0.f, y1 = 0.f;
+  stc::back(L, Lt, w0, w1, y0, y1);
+  y_out[row * D + L.r0] = y0;
+  y_out[row * D + L.r1] = y1;
+  kbar_out[row * D + L.r0] = kb0;
+  kbar_out[row * D + L.r1] = kb1;
+}
+
+cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  const long long rows = a.rows();
+  const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
+  solve_tc_kernel<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), ws.mom, ws.omega, ws.m, rows, a.lam, ws.y, ws.kbar,
+      ws.status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 template <typename TIn, int D, bool PRECISE, int FMT = 0>
 cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
   const size_t smem = sizeof(float) * kWarpsPerBlock * SolveCfg<D, PRECISE, FMT>::WARP_FLOATS;
@@ -329,6 +544,9 @@ cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
+  // The tensor-core path leaves keys unshifted, and its readout (dv = 64) forms every value
+  // term from centred weights, so it needs neither reference point.
+  if (ws.path == kPathTensorCore && a.dv == 64) return cudaSuccess;
   const dim3 grid((unsigned)a.BH(), 2);
   if (a.dtype == LLA_F32)
     mean_kernel<float><<<grid, 256, 256 * sizeof(float), s>>>(
@@ -343,7 +561,7 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
 }
 
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s) {
-  if (ws.path == kPathTensorCore) return launch_solve_t<__nv_bfloat16, 64, false, 1>(a, ws, s);
+  if (ws.path == kPathTensorCore) return launch_solve_tc(a, ws, s);
   const bool f32 = a.dtype == LLA_F32;
   switch (a.d) {
     case 16: return f32 ? launch_solve_t<float, 16, true>(a, ws, s) : launch_solve_t<__nv_bfloat16, 16, false>(a, ws, s);

@@ -213,5 +213,7 @@ def test_profiling_and_launch_count(lla):
         lla.lla_forward(q, k, v, 8.0, 0.01)
     lla.profile_enable(False)
     stages, calls = lla.profile_collect()
-    assert calls == 3 and all(t > 0 for t in stages.values())
-    assert lla.launch_count() - n0 == 3 * 4
+    assert calls == 3 and all(t >= 0 for t in stages.values())
+    assert all(stages[s] > 0 for s in ("moments", "solve", "readout"))
+    # bf16, d = dv = 64: moments, solve and readout; this path needs no reference points (prep)
+    assert lla.launch_count() - n0 == 3 * 3
