@@ -97,7 +97,12 @@ constexpr int F_BUF = 2 * F_HALF;
 constexpr int P_BLOCK = BM * KB * 2;
 constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
 constexpr int SM_EPI = SM_F + NFB * F_BUF;           // NSM x (32 rows x 36 floats)
-constexpr int SM_BAR = SM_EPI + NSM * 32 * EPI_LD * 4;
+// Feature passes 1..5 take each thread's pass-0 weights back from the global scratch PD key
+// blocks ahead of use (a per-thread ring in shared memory filled with cp.async): the scratch does
+// not fit L2, and one block of look-ahead (~740 cycles of tensor work) is shorter than a DRAM miss.
+constexpr int PD = 4;
+constexpr int SM_PR = SM_EPI + NSM * 32 * EPI_LD * 4;  // NSM x PD x 32 lanes x 32 bytes
+constexpr int SM_BAR = SM_PR + NSM * PD * 32 * 32;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 // More than half of an SM's shared memory, so that at most one CTA (and one TMEM allocation of
@@ -590,20 +595,30 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       if (b == nb - 1 && !drain(0)) { ok = false; break; }
     }
     {
-      // This thread's weights of block b (pass 0 stored them: same row, same 16 keys).
+      // This thread's weights of feature step h (block h % nb; pass 0 stored them: same row,
+      // same 16 keys), copied PD steps ahead into slot h % PD of this thread's ring.
       constexpr int kChunk = 2048 / 16;
-      auto load_p = [&](int b, uint4& x0, uint4& x1) {
-        const uint4* src = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
-        x0 = __ldcg(src);
-        x1 = __ldcg(src + kChunk);
+      // slot s, chunk c of this lane at ring + s * 64 + c * 32 (a warp's accesses are contiguous)
+      uint4* ring = reinterpret_cast<uint4*>(smem + SM_PR) + (warp - 2) * PD * 64 + lane;
+      const int hend = nb * NPASS;
+      auto fetch = [&](int hh) {
+        if (hh < hend) {
+          const uint4* src =
+              ptile_p + (long long)(hh % nb) * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+          uint4* dst = ring + (hh % PD) * 64;
+          cp_async16(dst, src, 16u);
+          cp_async16(dst + 32, src + kChunk, 16u);
+        }
+        cp_async_commit();  // an empty group past the end keeps the wait count uniform
       };
-      uint4 n0, n1;
-      if (ok) load_p(0, n0, n1);
+      if (ok)
+        for (int t = 0; t < PD; ++t) fetch(nb + t);
       int h = nb;  // feature step index (pass 0 took h = 0 .. nb-1)
       for (int pass = 1; pass < NPASS && ok; ++pass) {
         for (int b = 0; b < nb; ++b, ++h) {
-          const uint4 c0 = n0, c1 = n1;
-          if (h + 1 < nb * NPASS) load_p(b + 1 < nb ? b + 1 : 0, n0, n1);
+          cp_async_wait<PD - 1>();
+          const uint4* slot = ring + (h % PD) * 64;
+          const uint4 c0 = slot[0], c1 = slot[32];
           const int pb = h % NBUF;
           if (h >= NBUF &&
               !warp_wait(&bar.pfree[pb], ((h / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
@@ -611,12 +626,14 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           const uint32_t pw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           tmem_st8(lane_base + T_P + pb * (KB / 2) + half * (KB / 4), pw);
           tmem_st_wait();
+          fetch(h + PD);  // the slot's values are consumed (stored to tensor memory)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) arrive_leader(&bar.pfull[pb], leader);
         }
         if (ok) ok = drain(pass);
       }
+      cp_async_wait<0>();
     }
     if (ok) {  // combine the halves' omega
       bar.part[half][r] = om;

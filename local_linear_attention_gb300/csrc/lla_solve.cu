@@ -340,16 +340,12 @@ __host__ __device__ constexpr int run_base(int a) {
   return 2 * rs - (a + (a & 1));
 }
 
-// x -= s * c on a packed pair (x0, x1) with c = (c0, c1); ns = -s.
+// x -= s * c on a packed pair (x0, x1) with c = (c0, c1); ns = -s. One packed fp32 FMA (the same
+// single-rounded FMA on both lanes of a 64-bit register pair).
 __device__ __forceinline__ void fma2(float& x0, float& x1, float ns, float c0, float c1) {
-  asm("{\n\t.reg .b64 x, c, s;\n\t"
-      "mov.b64 x, {%0, %1};\n\t"
-      "mov.b64 c, {%2, %3};\n\t"
-      "mov.b64 s, {%4, %4};\n\t"
-      "fma.rn.f32x2 x, s, c, x;\n\t"
-      "mov.b64 {%0, %1}, x;\n\t}"
-      : "+f"(x0), "+f"(x1)
-      : "f"(c0), "f"(c1), "f"(ns));
+  const float2 r = __ffma2_rn(make_float2(ns, ns), make_float2(c0, c1), make_float2(x0, x1));
+  x0 = r.x;
+  x1 = r.y;
 }
 
 // a[j] -= lik * cb[j] for K < j < N (ns = -lik); cb is 16-byte aligned.
