@@ -15,8 +15,9 @@
 //    is then contracted twice (hi and lo) into the same accumulator.
 //  * 2144 fp32 accumulator columns do not fit the 512 columns of tensor memory, so the features
 //    are swept in 6 passes of 368 columns; each pass streams the key prefix again. A first sweep
-//    computes the exact row max m_i (Q K^T and a max); feature pass 0 computes P and also stores
-//    it (bf16) to a scratch, from which passes 1..5 take it again.
+//    computes the exact row max m_i (Q K^T and a max); a second sweep computes P (bf16) and
+//    stores it to a scratch, from which every feature pass takes it again. Q K^T and the
+//    exponentials thus never wait behind a feature contraction in the tensor pipe.
 //  * Feature tiles are generated per key block into shared memory and read back by the MMA, so
 //    shared-memory traffic per SM bounds the stage. Two CTAs on two SMs (a cluster pair) therefore
 //    share every MMA (tcgen05 cta_group::2, M = 256): each CTA holds 128 query rows (its tensor
@@ -28,12 +29,14 @@
 // issues all MMAs; its barriers that gate an MMA collect arrivals from both CTAs (mapa + remote
 // arrive), and MMA completion is signalled to both CTAs (multicast commit).
 //
-// Warp roles per CTA (19 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
-// allocation; 18 issues the feature contraction (leader; one thread); 1 stages key blocks (32
+// Warp roles per CTA (23 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
+// allocation; 22 issues the feature contraction (leader; one thread); 1 stages key blocks (32
 // keys x 64) into shared memory; 2-9 turn S into P (one thread per query = TMEM lane, two warps
-// per lane quarter splitting the keys of a block) and drain the accumulators after each pass;
-// 10-17 generate this CTA's half of the exact hi/lo feature tiles (one lane per key). P and the
-// feature tiles are triple-buffered; P lives in TMEM as the A operand of the feature contraction.
+// per lane quarter splitting the keys of a block), put P into tensor memory for each feature step
+// and drain the accumulators after each pass; 10-21 generate this CTA's half of the exact hi/lo
+// feature tiles (one lane per key; two groups of six warps take alternate key blocks). P is
+// triple-buffered in tensor memory (the A operand of the feature contraction), the feature tiles
+// have five buffers in shared memory.
 // All operands in shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is
 // bounded.
 //
@@ -97,8 +100,8 @@ constexpr int F_BUF = 2 * F_HALF;
 constexpr int P_BLOCK = BM * KB * 2;
 constexpr int EPI_LD = 36;                           // row stride (floats) of the drain buffer
 constexpr int SM_EPI = SM_F + NFB * F_BUF;           // NSM x (32 rows x 36 floats)
-// Feature passes 1..5 take each thread's pass-0 weights back from the global scratch PD key
-// blocks ahead of use (a per-thread ring in shared memory filled with cp.async): the scratch does
+// Feature passes take each thread's weights back from the global scratch PD key blocks ahead of
+// use (a per-thread ring in shared memory filled with cp.async): the scratch does
 // not fit L2, and one block of look-ahead (~740 cycles of tensor work) is shorter than a DRAM miss.
 constexpr int PD = 4;
 constexpr int SM_PR = SM_EPI + NSM * 32 * EPI_LD * 4;  // NSM x PD x 32 lanes x 32 bytes
@@ -300,7 +303,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int nq = max(0, min(BM, T - i0));
   const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
   const int nb = (jend + KB - 1) / KB;
-  const int G = nb * (1 + NPASS);
+  const int G = nb * (2 + NPASS);  // key blocks streamed: max sweep, weight sweep, feature passes
   const long long base = bh * T;
   // This CTA's P blocks in the scratch: earlier pairs of the head hold 2 x 8, 2 x 16, ... blocks.
   uint4* const ptile_p =
@@ -354,8 +357,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // Two threads issue the tensor-core work (this one and the feature issuer): a single thread's
     // serial issue cost -- mbarrier tests, descriptor arithmetic and the MMA/commit instructions
     // -- exceeds the tensor work of a key block. tcgen05.commit tracks the issuing thread's own
-    // MMAs, so each thread signals and drains its own. Q K^T runs only in the max sweep and
-    // feature pass 0.
+    // MMAs, so each thread signals and drains its own. Q K^T runs only in the max and weight
+    // sweeps.
     if (leader && lane == 0) {
       const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
       constexpr uint32_t id_qk = idesc_bf16(PM, KB, false, false);
@@ -474,9 +477,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
     // accumulator columns [0, NA); half 1 takes keys 16..31 and columns [NA, NCH). Row max and
     // omega are combined across the halves through shared memory (barrier rowx: phase 0 after the
-    // max sweep, phase 1 at the end). In feature pass 0 each thread also stores its 16 weights of
-    // each block to the scratch; in passes 1..5 it reads its own stores back (one block ahead)
-    // and writes them to tensor memory again, so Q K^T and the exponentials run only twice.
+    // max sweep, phase 1 at the end). In the weight sweep each thread stores its 16 weights of
+    // each block to the scratch; in the feature passes it reads its own stores back and writes
+    // them to tensor memory, so Q K^T and the exponentials run only twice.
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
@@ -568,7 +571,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
         continue;
       }
-      const int pb = b % NBUF;
       const float mc = m * c2;
       uint32_t pw[KB / 4];
 #pragma unroll
@@ -584,19 +586,10 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       uint4* pdst = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
       pdst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       pdst[kChunk] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-      if (b >= NBUF &&
-          !warp_wait(&bar.pfree[pb], ((b / NBUF) - 1) & 1, status, abort_p)) { ok = false; break; }
-      tc_fence_after();
-      tmem_st8(lane_base + T_P + pb * (KB / 2) + half * (KB / 4), pw);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&bar.pfull[pb], leader);
-      if (b == nb - 1 && !drain(0)) { ok = false; break; }
     }
     {
-      // This thread's weights of feature step h (block h % nb; pass 0 stored them: same row,
-      // same 16 keys), copied PD steps ahead into slot h % PD of this thread's ring.
+      // This thread's weights of feature step h (block h % nb; the weight sweep stored them:
+      // same row, same 16 keys), copied PD steps ahead into slot h % PD of this thread's ring.
       constexpr int kChunk = 2048 / 16;
       // slot s, chunk c of this lane at ring + s * 64 + c * 32 (a warp's accesses are contiguous)
       uint4* ring = reinterpret_cast<uint4*>(smem + SM_PR) + (warp - 2) * PD * 64 + lane;
@@ -612,9 +605,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         cp_async_commit();  // an empty group past the end keeps the wait count uniform
       };
       if (ok)
-        for (int t = 0; t < PD; ++t) fetch(nb + t);
-      int h = nb;  // feature step index (pass 0 took h = 0 .. nb-1)
-      for (int pass = 1; pass < NPASS && ok; ++pass) {
+        for (int t = 0; t < PD; ++t) fetch(t);
+      int h = 0;  // feature step index
+      for (int pass = 0; pass < NPASS && ok; ++pass) {
         for (int b = 0; b < nb; ++b, ++h) {
           cp_async_wait<PD - 1>();
           const uint4* slot = ring + (h % PD) * 64;
@@ -652,11 +645,11 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // products, the proxy fence).
     const int fwi = warp - 2 - NSM, grp = fwi / NFGW, fw = fwi % NFGW;
     const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;  // key `lane` in the F tiles
-    int st = grp, h = grp - nb, pass = -1, bcnt = 0;
+    int st = grp, h = grp - 2 * nb, pass = -1, bcnt = 0;
     uint32_t kpar = 0;
     for (int g = grp; g < G; g += 2) {
       if (!warp_wait(&bar.kfull[st], kpar, status, abort_p)) break;
-      if (g < nb) {  // max sweep: nothing to generate
+      if (g < 2 * nb) {  // max and weight sweeps: nothing to generate
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.kempty[st]);
       } else {
@@ -671,9 +664,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
         kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
         __syncwarp();
-        // Passes 1..5 run no Q K^T, whose completion is the stage's other release: warp 0 of
+        // Feature passes run no Q K^T, whose completion is the stage's other release: warp 0 of
         // the group arrives for it.
-        if (lane == 0) mbar_arrive_cnt(&bar.kempty[st], (pass >= 1 && fw == 0) ? 2u : 1u);
+        if (lane == 0) mbar_arrive_cnt(&bar.kempty[st], fw == 0 ? 2u : 1u);
         if (h >= NFB && !warp_wait(&bar.ffree[fb], ((h / NFB) - 1) & 1, status, abort_p)) break;
         uint8_t* fhi = smem + SM_F + fb * F_BUF;
         generate(pass, rank, fw, kw, fhi, fhi + F_HALF, row_off);
