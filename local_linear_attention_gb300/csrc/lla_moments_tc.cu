@@ -29,8 +29,9 @@
 // issues all MMAs; its barriers that gate an MMA collect arrivals from both CTAs (mapa + remote
 // arrive), and MMA completion is signalled to both CTAs (multicast commit).
 //
-// Warp roles per CTA (23 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
-// allocation; 22 issues the feature contraction (leader; one thread); 1 stages key blocks (32
+// Warp roles per CTA (24 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
+// allocation; 22 and 23 issue the feature contraction (leader; one thread each, alternate key
+// blocks); 1 stages key blocks (32
 // keys x 64) into shared memory; 2-9 turn S into P (one thread per query = TMEM lane, two warps
 // per lane quarter splitting the keys of a block), put P into tensor memory for each feature step
 // and drain the accumulators after each pass; 10-21 generate this CTA's half of the exact hi/lo
@@ -72,7 +73,7 @@ constexpr int KLAG = KS - 2;                // key blocks the loader keeps in fl
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int NFG = 12;                     // feature-generation warps: two groups of NFGW that
 constexpr int NFGW = NFG / 2;               //   take alternate key blocks
-constexpr int NWARPS = 3 + NSM + NFG;       // + Q K^T issuer, key loader, feature issuer
+constexpr int NWARPS = 4 + NSM + NFG;       // + Q K^T issuer, key loader, two feature issuers
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 3;                     // P buffers (tensor memory)
 constexpr int NFB = 5;                      // F buffers (shared memory)
@@ -260,7 +261,8 @@ struct Barriers {
   uint64_t accfull;             // (M) the accumulators of a pass are final
   uint64_t accfree;             // (L) both CTAs drained them
   uint64_t qready;              // (L) both CTAs' Q tiles in tensor memory
-  uint64_t done_qk, done_f;     // (M) every MMA of either issuer completed
+  uint64_t hand[2];             // (L) feature issuer t has issued its latest step
+  uint64_t done_qk, done_f[2];  // (M) every MMA of the Q K^T issuer / feature issuer t completed
   uint64_t rowx;                // this CTA's softmax halves exchanged row max / omega
   float part[2][BM];            // per-row partial results of the two softmax halves
 };
@@ -330,11 +332,14 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mbar_init(&bar.ffull[s], 2 * NFGW);
       mbar_init(&bar.ffree[s], 1);
     }
-    mbar_init(&bar.accfull, 1);
+    mbar_init(&bar.accfull, nb >= 2 ? 2 : 1);  // one commit per feature issuer with steps in a pass
     mbar_init(&bar.accfree, 2 * NSM);
     mbar_init(&bar.qready, 2 * 4);
     mbar_init(&bar.done_qk, 1);
-    mbar_init(&bar.done_f, 1);
+    mbar_init(&bar.done_f[0], 1);
+    mbar_init(&bar.done_f[1], 1);
+    mbar_init(&bar.hand[0], 1);
+    mbar_init(&bar.hand[1], 1);
     mbar_init(&bar.rowx, NSM);
     abort_flag = 0;
     fence_mbar_init();
@@ -389,21 +394,32 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       mma2_commit_both(&bar.done_qk);
     }
     __syncwarp();
-  } else if (warp == NWARPS - 1) {
-    // ------------------------------------------------------------------ feature issuer (leader)
+  } else if (warp >= NWARPS - 2) {
+    // ------------------------------------------------------------------ feature issuers (leader)
+    // Issuing a step's 8 MMAs takes about as long as the tensor core takes to run them (the MMA
+    // queue is shallow), and one thread's barrier tests between steps left the pipe idle. Two
+    // threads therefore take alternate steps: while one issues step h, the other tests the
+    // barriers of step h + 1, then waits only for the hand-off (hand[]) that says step h is
+    // issued, so the issue order -- and the accumulation order -- stays fixed. The hand-off is
+    // bracketed by tcgen05 fences, which order one thread's MMAs after the other's. Each thread
+    // commits its own MMAs; both commit to accfull at the end of a pass.
     if (leader && lane == 0) {
+      const int t = warp - (NWARPS - 2);
       const uint64_t fd = smem_desc(smem_u32(smem + SM_F), 128, 512);
       constexpr uint32_t id_a = idesc_bf16(PM, NA, false, true);
       constexpr uint32_t id_b = idesc_bf16(PM, NB_, false, true);
       constexpr uint32_t nb_off = GA * 512 / 16;  // local group GA: the N = 176 MMA's half
       const uint32_t t_acc = tbase + T_ACC, t_p = tbase + T_P;
+      const int H = nb * NPASS;
       bool ok = true;
-      int pb = 0, fb = 0, b = 0, pass = 0;
-      uint32_t ppar = 0, fpar = 0;  // parities of the current uses of P buffer pb, F buffer fb
-      for (int h = 0; h < nb * NPASS && ok; ++h) {
-        ok = mbar_wait2(&bar.pfull[pb], ppar, &bar.ffull[fb], fpar, status, TO, abort_p);
+      int b = t % nb, pass = t / nb;  // block and pass of step h
+      for (int h = t; h < H && ok; h += 2) {
+        const int pb = h % NBUF, fb = h % NFB;
+        ok = mbar_wait2(&bar.pfull[pb], (h / NBUF) & 1, &bar.ffull[fb], (h / NFB) & 1, status, TO,
+                        abort_p);
         if (ok && b == 0 && pass >= 1)
           ok = mbar_wait(&bar.accfree, (pass - 1) & 1, status, TO, abort_p);
+        if (ok && h >= 1) ok = mbar_wait(&bar.hand[t ^ 1], ((h - 1) >> 1) & 1, status, TO, abort_p);
         if (!ok) break;
         tc_fence_after();
         const uint64_t fh = fd + (uint64_t)(fb * (F_BUF >> 4));
@@ -420,15 +436,16 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         mma2_ts(t_acc, a0 + 8, fl + 16, id_a, 1u);
         mma2_ts(t_acc + NA, a0 + 8, fh + nb_off + 16, id_b, 1u);
         mma2_ts(t_acc + NA, a0 + 8, fl + nb_off + 16, id_b, 1u);
+        tc_fence_before();
+        mbar_arrive(&bar.hand[t]);
         mma2_commit_both(&bar.pfree[pb]);
         mma2_commit_both(&bar.ffree[fb]);
-        if (b == nb - 1) mma2_commit_both(&bar.accfull);
-        if (++pb == NBUF) { pb = 0; ppar ^= 1; }
-        if (++fb == NFB) { fb = 0; fpar ^= 1; }
-        if (++b == nb) { b = 0; ++pass; }
+        if (b >= nb - 2) mma2_commit_both(&bar.accfull);  // this thread's last step of the pass
+        b += 2;
+        while (b >= nb) { b -= nb; ++pass; }
       }
       if (!ok) *abort_p = 1;
-      mma2_commit_both(&bar.done_f);
+      mma2_commit_both(&bar.done_f[t]);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -691,7 +708,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (warp == 0 && lane == 0) {
     volatile int never = 0;
     mbar_wait(&bar.done_qk, 0, status, TO, &never);
-    mbar_wait(&bar.done_f, 0, status, TO, &never);
+    mbar_wait(&bar.done_f[0], 0, status, TO, &never);
+    mbar_wait(&bar.done_f[1], 0, status, TO, &never);
   }
   tc_fence_before();
   __syncthreads();
