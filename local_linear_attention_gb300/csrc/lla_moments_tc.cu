@@ -35,9 +35,9 @@
 // keys x 64) into shared memory; 2-9 turn S into P (one thread per query = TMEM lane, two warps
 // per lane quarter splitting the keys of a block), put P into tensor memory for each feature step
 // and drain the accumulators after each pass; 10-21 generate this CTA's half of the exact hi/lo
-// feature tiles (one lane per key; two groups of six warps take alternate key blocks). P is
-// triple-buffered in tensor memory (the A operand of the feature contraction), the feature tiles
-// have five buffers in shared memory.
+// feature tiles (one lane per key; two groups of six warps take alternate key blocks). P has
+// seven buffers in tensor memory (the A operand of the feature contraction), the feature tiles
+// five in shared memory.
 // All operands in shared memory use the no-swizzle core-matrix layout. Every mbarrier wait is
 // bounded.
 //
@@ -75,18 +75,23 @@ constexpr int NFG = 12;                     // feature-generation warps: two gro
 constexpr int NFGW = NFG / 2;               //   take alternate key blocks
 constexpr int NWARPS = 4 + NSM + NFG;       // + Q K^T issuer, key loader, two feature issuers
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int NBUF = 3;                     // P buffers (tensor memory)
+constexpr int NBUF = 7;                     // P buffers (tensor memory, feature passes only)
 constexpr int NFB = 5;                      // F buffers (shared memory)
-constexpr int NSB = 2;                      // S buffers
-static_assert(NSB == 2, "the Q K^T issuer indexes S buffers with g & 1");
+constexpr int NSB = 8;                      // S buffers (sweeps only)
 static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
 
 // tensor-memory columns (the same in both CTAs of a pair)
 constexpr uint32_t T_ACC = 0;
-constexpr uint32_t T_S = NCH;               // NSB x 32 columns of fp32 logits
-constexpr uint32_t T_P = T_S + NSB * KB;    // NBUF x 16 columns of packed bf16 weights
+// The two sweeps and the feature passes use tensor memory at different times: the logits S of the
+// sweeps take the accumulator columns (idle until the first feature pass, which starts only after
+// the softmax warps have read the last S), so that Q K^T can run NSB blocks ahead of the softmax
+// warps; the weights P of the feature passes take NBUF buffers after the accumulators, so that a
+// step's weights can be in place several steps ahead of its MMAs.
+constexpr uint32_t T_S = T_ACC;             // NSB x 32 columns of fp32 logits (sweeps)
+constexpr uint32_t T_P = NCH;               // NBUF x 16 columns of packed bf16 weights (passes)
 constexpr uint32_t T_Q = T_P + NBUF * (KB / 2);  // 32 columns: the Q tile, A operand of Q K^T
 constexpr uint32_t TMEM_COLS = 512;
+static_assert(T_S + NSB * KB <= NCH, "S buffers within the accumulator columns");
 static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
 
 // shared-memory layout (bytes; the same offsets in both CTAs of a pair)
@@ -267,6 +272,8 @@ struct Barriers {
   float part[2][BM];            // per-row partial results of the two softmax halves
 };
 
+static_assert(sizeof(Barriers) <= 2048, "barrier region");
+
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -372,10 +379,10 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       int st = 0;
       uint32_t kpar = 0;  // parity of the current fill of key stage st
       for (int g = 0; g < 2 * nb && ok; ++g) {
-        const int sb = g & 1;
+        const int sb = g % NSB;
         ok = mbar_wait2(&bar.kfull[st], kpar, &bar.kfull_peer[st], kpar, status, TO, abort_p);
         if (ok && g >= NSB)
-          ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, TO, abort_p);
+          ok = mbar_wait(&bar.sfree[sb], ((g / NSB) - 1) & 1, status, TO, abort_p);
         if (!ok) break;
         tc_fence_after();
         // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
@@ -564,8 +571,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     float m = -INFINITY, om = 0.f;
     bool ok = true;
     for (int g = 0; g < 2 * nb; ++g) {
-      const int sb = g & 1;
-      if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) { ok = false; break; }
+      const int sb = g % NSB;
+      if (!warp_wait(&bar.sfull[sb], (g / NSB) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[KB / 2];
       tmem_ld16(lane_base + T_S + sb * KB + c_lo, sv);
