@@ -73,8 +73,33 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 size_t moments_tc_row_floats();
-long long moments_tc_pblocks_per_head(int T);
 size_t moments_tc_pscratch_bytes(long long BH, int T);
+
+// Layout of the tensor-core path's weight scratch: the bf16 kernel weights P of every (head,
+// query tile, key block), written by the moments stage and read back by its feature passes and by
+// the readout. Query tiles of 128 rows go in pairs (ptile: 256 queries); a pair streams key
+// blocks 0..nb-1 of 32 keys, nb = ceil(min(T, 256 (ptile + 1)) / 32). A pair's rank-0 tile's nb
+// blocks come first, then its rank-1 tile's; the pairs of a head follow one another (a full pair
+// p holds 2 x 8 (p + 1) blocks). A block is an 8 KiB image in which 16-byte chunk kc (keys
+// 8kc..8kc+7) of row r sits at kc * 2048 + r * 16: the no-swizzle K-major core-matrix layout of a
+// 128 x 32 bf16 tcgen05 operand (K-adjacent core matrices 2048 B apart, M-adjacent 128 B).
+namespace pscr {
+constexpr int kRows = 128;
+constexpr int kKeys = 32;
+constexpr int kBlockBytes = kRows * kKeys * 2;
+__host__ __device__ inline int pair_blocks(int T, int ptile) {
+  const int jend = T < 256 * (ptile + 1) ? T : 256 * (ptile + 1);
+  return (jend + kKeys - 1) / kKeys;
+}
+__host__ __device__ inline long long blocks_per_head(int T) {
+  const long long np = (T + 255) / 256;
+  return np > 0 ? 8 * (np - 1) * np + 2ll * ((T + kKeys - 1) / kKeys) : 0;
+}
+// Index (in blocks) of block 0 of tile (ptile, rank) of head bh.
+__host__ __device__ inline long long first_block(long long bh, int T, int ptile, int rank) {
+  return bh * blocks_per_head(T) + 8ll * ptile * (ptile + 1) + (long long)rank * pair_blocks(T, ptile);
+}
+}  // namespace pscr
 // The tensor-core stage may run for these sizes (whatever path is requested at call time).
 inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64; }
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);

@@ -78,7 +78,7 @@ constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 7;                     // P buffers (tensor memory, feature passes only)
 constexpr int NFB = 5;                      // F buffers (shared memory)
 constexpr int NSB = 8;                      // S buffers (sweeps only)
-static_assert(BM == 4 * KB, "P scratch offsets assume four key blocks per query tile");
+static_assert(BM == pscr::kRows && KB == pscr::kKeys && PM == 2 * BM, "weight scratch layout");
 
 // tensor-memory columns (the same in both CTAs of a pair)
 constexpr uint32_t T_ACC = 0;
@@ -293,8 +293,8 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
                   int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ mraw_out,
-                  float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pscr,
-                  long long pblk_per_head, int* __restrict__ status) {
+                  float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pimg,
+                  int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -314,9 +314,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int nb = (jend + KB - 1) / KB;
   const int G = nb * (2 + NPASS);  // key blocks streamed: max sweep, weight sweep, feature passes
   const long long base = bh * T;
-  // This CTA's P blocks in the scratch: earlier pairs of the head hold 2 x 8, 2 x 16, ... blocks.
-  uint4* const ptile_p =
-      pscr + (bh * pblk_per_head + 8ll * ptile * (ptile + 1) + (long long)rank * nb) * (P_BLOCK / 16);
+  // This CTA's P blocks in the scratch (layout: pscr:: in the internal header).
+  uint4* const ptile_p = pimg + pscr::first_block(bh, T, ptile, rank) * (P_BLOCK / 16);
   // Rows of this CTA's key stage: the Q K^T operand takes rows 0..15 of each CTA's stage as its
   // N/2 keys, so CTA 1 keeps keys 16..31 of a block in rows 0..15 (row = key ^ 16 * rank).
   const int krot = 16 * rank;
@@ -731,13 +730,8 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
 size_t moments_tc_row_floats() { return NFP; }
 
-long long moments_tc_pblocks_per_head(int T) {
-  const long long np = (T + PM - 1) / PM;
-  return np > 0 ? 8 * (np - 1) * np + 2ll * ((T + KB - 1) / KB) : 0;
-}
-
 size_t moments_tc_pscratch_bytes(long long BH, int T) {
-  return (size_t)BH * (size_t)moments_tc_pblocks_per_head(T) * P_BLOCK;
+  return (size_t)BH * (size_t)pscr::blocks_per_head(T) * P_BLOCK;
 }
 
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
@@ -750,7 +744,7 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
       (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
-      moments_tc_pblocks_per_head(a.T), ws.status);
+      ws.status);
   count_launch();
   return cudaGetLastError();
 }

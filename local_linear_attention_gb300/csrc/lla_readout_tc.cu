@@ -1,24 +1,29 @@
-// Tensor-core readout stage of the causal LLA forward (bf16 inputs, d = 64; tcgen05 + TMEM).
+// Tensor-core readout stage of the causal LLA forward (bf16 inputs, d = dv = 64; tcgen05 + TMEM).
 //
 // With y_i = (C_kk + lambda' I)^-1 (q_i - kbar_i) from the ridge solve, one streaming pass over
 // the causal prefix evaluates the centred closed form of the LLA intercept ("Parallax" blog, s.2
 // Canonical Formulation)
 //   o_i = vbar_i + C_vk y_i = O1_i / omega_i + O2_i,
 //   O1 = P V,  O2 = (P .* t) V,  t_ij = k_j . y_i - kbar_i . y_i,
-// where P holds the kernel weights exactly as the tensor-core moments stage rounded them (same
-// S = Q K^T contraction, same exponent, same bf16 rounding), so the fitted moments and this pass
-// describe one weighted problem (and sum_j p_ij t_ij = 0 up to rounding). The pass has the
-// two-branch shape of the blog's streaming algorithm (s.3 "One extra branch, no extra I/O"): a
-// softmax branch (O1, omega) and a covariance branch (O2) over the same K/V tiles.
+// where P holds the kernel weights exactly as the moments stage rounded them: the pass reads them
+// back from the moments stage's weight scratch (bf16 images already in the layout of a tcgen05
+// operand), so the fitted moments and this pass describe one weighted problem (and
+// sum_j p_ij t_ij = 0 up to rounding), and neither Q K^T nor an exponential is recomputed. The
+// pass has the two-branch shape of the blog's streaming algorithm (s.3 "One extra branch, no extra
+// I/O"): a softmax branch (O1, omega) and a covariance branch (O2) over the same K/V tiles.
 //
 // Precision: y can be large (small ridge, rank-deficient early prefixes), and its component
 // outside the span of the keys must cancel between k_j . y and kbar . y; y therefore enters the
 // Y K^T contraction as three exact bf16 parts (y = y1 + y2 + y3, 24 significant bits), and the
 // covariance-branch weights p * t enter P2 V as an exact-to-16-bits hi/lo pair.
 //
-// Warp roles (6 warps): 0 issues every tcgen05.mma and owns the TMEM allocation; 1 stages key and
-// value blocks; 2-5 (one thread per query = TMEM lane) turn S and T into P and P2 and write the
-// output. All waits are bounded.
+// One CTA per 128-query tile; keys in chunks of 64 (two weight images). Warp roles (7 warps):
+// 0 issues T = Y K^T (12 MMAs per chunk, N = 64) and owns the TMEM allocation; 6 issues
+// O1 += P V (P straight from shared memory) and O2 += P2 V (P2 from tensor memory), 12 MMAs per
+// chunk; 1 stages the key, value and weight chunks; 2-5 (one thread per query = TMEM lane) turn
+// T and P into P2 and write the output. Two issuing threads, because each tcgen05.mma costs its
+// issuing thread about as long as the tensor core takes to run one of these. All waits are
+// bounded.
 #include <cstdint>
 
 #include "lla_internal.cuh"
@@ -31,40 +36,38 @@ using namespace tc;
 
 constexpr int D = 64;
 constexpr int DV = 64;
-constexpr int BM = 128;
-constexpr int KB = 32;
-constexpr int KS = 6;
-constexpr int KLAG = KS - 2;
-constexpr int NWARPS = 6;
+constexpr int BM = 128;                 // query rows per CTA = TMEM lanes
+constexpr int CK = 64;                  // keys per chunk
+constexpr int KS = 5;                   // chunk pipeline stages
+constexpr int KLAG = KS - 2;            // chunks the loader keeps in flight
+constexpr int NWARPS = 7;
 constexpr int NTHREADS = NWARPS * 32;
+static_assert(BM == pscr::kRows && CK == 2 * pscr::kKeys, "a chunk is two weight images");
 
 // tensor-memory columns
 constexpr uint32_t T_O1 = 0;            // 64 fp32: P V
 constexpr uint32_t T_O2 = 64;           // 64 fp32: P2 V
-constexpr uint32_t T_S = 128;           // 2 x 32 fp32: Q K^T
-constexpr uint32_t T_T = 192;           // 2 x 32 fp32: Y K^T
-constexpr uint32_t T_P = 256;           // 2 x 16: bf16 P
-constexpr uint32_t T_P2H = 288;         // 2 x 16: bf16 hi part of P .* t
-constexpr uint32_t T_P2L = 320;         // 2 x 16: bf16 lo part
+constexpr uint32_t T_T = 128;           // 2 x 64 fp32: Y K^T
+constexpr uint32_t T_P2H = 256;         // 2 x 32: bf16 hi part of P .* t (64 keys)
+constexpr uint32_t T_P2L = 320;         // 2 x 32: bf16 lo part
 constexpr uint32_t TMEM_COLS = 512;
+static_assert(T_P2L + 2 * (CK / 2) <= TMEM_COLS, "tensor memory budget");
 
 // shared memory (bytes)
 constexpr int TILE = BM * D * 2;                    // 128 x 64 bf16 = 16 KiB
-constexpr int SM_Q = 0;
-constexpr int SM_Y = SM_Q + TILE;                   // 3 tiles: y1, y2, y3
-constexpr int SM_K = SM_Y + 3 * TILE;
-constexpr int KV_STAGE = KB * D * 2;                // 4 KiB
-constexpr int SM_V = SM_K + KS * KV_STAGE;
-constexpr int SM_BAR = SM_V + KS * KV_STAGE;
+constexpr int SM_Y = 0;                             // 3 tiles: y1, y2, y3
+constexpr int KV_BYTES = CK * D * 2;                // 8 KiB: one key or value chunk
+constexpr int P_BYTES = 2 * pscr::kBlockBytes;      // 16 KiB: the chunk's two weight images
+constexpr int STAGE = 2 * KV_BYTES + P_BYTES;       // K, V, P of one chunk
+constexpr int SM_ST = SM_Y + 3 * TILE;
+constexpr int SM_BAR = SM_ST + KS * STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+// Byte offset of 16-byte chunk c (elements 8c..8c+7) of row r in a K-major tile whose rows hold
+// 64 elements: core matrix (r / 8, c) of 128 bytes, row groups 1024 bytes apart.
 __device__ __forceinline__ int kmaj_off(int r, int c) { return (r >> 3) * 1024 + c * 128 + (r & 7) * 16; }
 
-__device__ __forceinline__ float ex2(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -80,17 +83,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
 
 struct Barriers {
   uint64_t kvfull[KS], kvempty[KS];
-  uint64_t sfull[2], sfree[2];
-  uint64_t pfull[2], pfree[2];
-  uint64_t accfull, done;
+  uint64_t tfull[2], tfree[2];
+  uint64_t p2full[2], p2free[2];
+  uint64_t accfull, done_t, done_o;
 };
+static_assert(sizeof(Barriers) <= 256, "barrier region");
 
 template <typename TOut>
 __global__ void __launch_bounds__(NTHREADS, 1)
-readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const __nv_bfloat16* __restrict__ v, const float* __restrict__ mraw,
-                  const float* __restrict__ y, const float* __restrict__ kbar, int T, int BH,
-                  float inv_h, TOut* __restrict__ out, int* __restrict__ status) {
+readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                  const uint4* __restrict__ pimg, const float* __restrict__ y,
+                  const float* __restrict__ kbar, int T, int BH, TOut* __restrict__ out,
+                  int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -98,23 +102,20 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = (T + BM - 1) / BM;
-  const int tile = ntiles - 1 - (int)(blockIdx.x / BH);
+  const int tile = ntiles - 1 - (int)(blockIdx.x / BH);  // longest causal prefixes first
   const long long bh = blockIdx.x % BH;
   const int i0 = tile * BM;
   const int nq = min(BM, T - i0);
   const int jend = i0 + nq;
-  const int nb = (jend + KB - 1) / KB;
+  const int nck = (jend + CK - 1) / CK;
   const long long base = bh * T;
+  // This tile's weight images: tile = 2 ptile + rank in the moments stage's pairing.
+  const int ptile = tile >> 1, rank = tile & 1;
+  const uint4* const pt = pimg + pscr::first_block(bh, T, ptile, rank) * (pscr::kBlockBytes / 16);
+  const int nimg = pscr::pair_blocks(T, ptile);
 
-  // Q tile (bf16, as the moments stage had it).
-  for (int e = tid; e < BM * (D / 8); e += NTHREADS) {
-    const int r = e >> 3, c = e & 7;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nq) val = *reinterpret_cast<const uint4*>(q + (base + i0 + r) * D + c * 8);
-    *reinterpret_cast<uint4*>(smem + SM_Q + kmaj_off(r, c)) = val;
-  }
   // y split into three exact bf16 parts; one row (query) per thread of warps 2..5.
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     const int r = (warp & 3) * 32 + lane;
     const bool valid = r < nq;
     const float* yr = y + (base + i0 + r) * D;
@@ -138,13 +139,14 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], 4);
-      mbar_init(&bar.pfull[s], 4);
-      mbar_init(&bar.pfree[s], 1);
+      mbar_init(&bar.tfull[s], 1);
+      mbar_init(&bar.tfree[s], 4);
+      mbar_init(&bar.p2full[s], 4);
+      mbar_init(&bar.p2free[s], 1);
     }
     mbar_init(&bar.accfull, 1);
-    mbar_init(&bar.done, 1);
+    mbar_init(&bar.done_t, 1);
+    mbar_init(&bar.done_o, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -158,99 +160,117 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
   volatile int* abort_p = &abort_flag;
+  constexpr uint32_t stage16 = STAGE >> 4;
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ T = Y K^T issuer
     if (lane == 0) {
       // Base descriptors plus start-address offsets in 16-byte units (see the moments stage).
-      const uint64_t qd = smem_desc(smem_u32(smem + SM_Q), 128, 1024);
       const uint64_t yd = smem_desc(smem_u32(smem + SM_Y), 128, 1024);
-      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
-      // V block as the MN-major B operand: K = keys (8-key groups 1024 B apart), N = value
-      // features (8-feature groups 128 B apart).
-      const uint64_t vd = smem_desc(smem_u32(smem + SM_V), 1024, 128);
-      constexpr uint32_t id_s = idesc_bf16(BM, KB, false, false);
-      constexpr uint32_t id_o = idesc_bf16(BM, DV, false, true);
-      constexpr uint32_t tile16 = TILE >> 4, stage16 = KV_STAGE >> 4;
-      const uint32_t t_s = tbase + T_S, t_t = tbase + T_T;
+      const uint64_t kd = smem_desc(smem_u32(smem + SM_ST), 128, 1024);
+      constexpr uint32_t id_t = idesc_bf16(BM, CK, false, false);
+      constexpr uint32_t tile16 = TILE >> 4;
       bool ok = true;
-      for (int g = 0; g <= nb && ok; ++g) {
-        if (g < nb) {
-          const int st = g % KS, sb = g & 1;
-          ok = mbar_wait(&bar.kvfull[st], (g / KS) & 1, status, kStatusTimeout, abort_p);
-          if (ok && g >= 2)
-            ok = mbar_wait(&bar.sfree[sb], ((g >> 1) - 1) & 1, status, kStatusTimeout, abort_p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kst = kd + (uint64_t)(st * stage16);
-          const uint32_t ts = t_s + sb * KB, tt = t_t + sb * KB;
+      for (int c = 0; c < nck && ok; ++c) {
+        const int st = c % KS, tb = c & 1;
+        ok = mbar_wait(&bar.kvfull[st], (c / KS) & 1, status, kStatusTimeout, abort_p);
+        if (ok && c >= 2)
+          ok = mbar_wait(&bar.tfree[tb], ((c >> 1) - 1) & 1, status, kStatusTimeout, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t kst = kd + (uint64_t)(st * stage16);
+        const uint32_t tt = tbase + T_T + tb * CK;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s) mma_ss(ts, qd + 16 * s, kst + 16 * s, id_s, s > 0);
+        for (int part = 0; part < 3; ++part)
 #pragma unroll
-          for (int part = 0; part < 3; ++part)
-#pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-              mma_ss(tt, yd + part * tile16 + 16 * s, kst + 16 * s, id_s,
-                     (part > 0 || s > 0) ? 1u : 0u);
-          mma_commit(&bar.sfull[sb]);
-        }
-        if (g >= 1) {
-          const int h = g - 1, pb = h & 1, st = h % KS;
-          ok = mbar_wait(&bar.pfull[pb], (h >> 1) & 1, status, kStatusTimeout, abort_p);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vst = vd + (uint64_t)(st * stage16);
-#pragma unroll
-          for (int s = 0; s < KB / 16; ++s) {
-            const uint64_t vds = vst + (uint64_t)(s * (2048 >> 4));
-            const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_O1, tbase + T_P + pb * 16 + s * 8, vds, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2H + pb * 16 + s * 8, vds, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2L + pb * 16 + s * 8, vds, id_o, 1u);
-          }
-          mma_commit(&bar.pfree[pb]);
-          mma_commit(&bar.kvempty[st]);
-          if (h == nb - 1) mma_commit(&bar.accfull);
-        }
+          for (int s = 0; s < D / 16; ++s)
+            mma_ss(tt, yd + part * tile16 + 16 * s, kst + 16 * s, id_t, (part > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bar.tfull[tb]);
       }
       if (!ok) *abort_p = 1;
-      mma_commit(&bar.done);
-      volatile int never = 0;
-      mbar_wait(&bar.done, 0, status, kStatusTimeout, &never);
+      mma_commit(&bar.done_t);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------ O1, O2 issuer
+    if (lane == 0) {
+      // P images as the K-major A operand (K-adjacent core matrices 2048 B apart, M-adjacent
+      // 128 B); the V chunk as the MN-major B operand: K = keys (8-key groups 1024 B apart),
+      // N = value features (8-feature groups 128 B apart).
+      const uint64_t pd = smem_desc(smem_u32(smem + SM_ST + 2 * KV_BYTES), 2048, 128);
+      const uint64_t vd = smem_desc(smem_u32(smem + SM_ST + KV_BYTES), 1024, 128);
+      constexpr uint32_t id_o = idesc_bf16(BM, DV, false, true);
+      bool ok = true;
+      for (int c = 0; c < nck && ok; ++c) {
+        const int st = c % KS, pb = c & 1;
+        ok = mbar_wait2(&bar.kvfull[st], (c / KS) & 1, &bar.p2full[pb], (c >> 1) & 1, status,
+                        kStatusTimeout, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t vst = vd + (uint64_t)(st * stage16);
+        const uint64_t pst = pd + (uint64_t)(st * stage16);
+#pragma unroll
+        for (int s = 0; s < CK / 16; ++s) {
+          const uint64_t vds = vst + (uint64_t)(s * (2048 >> 4));  // keys 16s.. : 2 x 1024 B
+          // keys 16s..16s+15: image s / 2, K-adjacent core matrices 2 (s % 2), 2 (s % 2) + 1
+          const uint64_t pds = pst + (uint64_t)((s >> 1) * (pscr::kBlockBytes >> 4) + (s & 1) * (4096 >> 4));
+          const uint32_t acc = (c > 0 || s > 0) ? 1u : 0u;
+          mma_ss(tbase + T_O1, pds, vds, id_o, acc);
+          mma_ts(tbase + T_O2, tbase + T_P2H + pb * (CK / 2) + s * 8, vds, id_o, acc);
+          mma_ts(tbase + T_O2, tbase + T_P2L + pb * (CK / 2) + s * 8, vds, id_o, 1u);
+        }
+        mma_commit(&bar.p2free[pb]);
+        mma_commit(&bar.kvempty[st]);  // T's reads of this stage completed before p2full
+        if (c == nck - 1) mma_commit(&bar.accfull);
+      }
+      if (!ok) *abort_p = 1;
+      mma_commit(&bar.done_o);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ K/V loader
-    // cp.async copies with several blocks in flight; same conflict-free lane mapping and
-    // completion -> proxy fence -> arrive protocol as the moments stage's loader.
+    // ------------------------------------------------------------------ K/V/P loader
+    // cp.async copies with several chunks in flight. K and V rows go to the core-matrix layout
+    // (lane -> (row, 16-byte chunk) mapping conflict-free per 8-lane phase); the two weight
+    // images are copied as they are (missing images past the pair's last block are zero-filled).
+    // A chunk becomes visible to the MMAs (async proxy) only after its copies completed and this
+    // warp fenced them.
     const __nv_bfloat16* kbp = k + base * D;
     const __nv_bfloat16* vbp = v + base * DV;
     bool ok = true;
-    for (int g = 0; g < nb + KLAG; ++g) {
-      if (g < nb) {
-        const int st = g % KS;
-        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
+    for (int c = 0; c < nck + KLAG; ++c) {
+      if (c < nck) {
+        const int st = c % KS;
+        if (c >= KS && !warp_wait(&bar.kvempty[st], ((c / KS) - 1) & 1, status, abort_p)) {
           ok = false;
           break;
         }
-        uint8_t* kd = smem + SM_K + st * KV_STAGE;
-        uint8_t* vd = smem + SM_V + st * KV_STAGE;
+        uint8_t* kdst = smem + SM_ST + st * STAGE;
+        uint8_t* vdst = kdst + KV_BYTES;
+        uint8_t* pdst = kdst + 2 * KV_BYTES;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
-          const int j = g * KB + r;
+        for (int t = 0; t < 16; ++t) {
+          const int r = (lane & 7) + 8 * (t & 7), cc = (lane >> 3) + 4 * (t >> 3);
+          const int j = c * CK + r;
           const bool in = j < jend;
           const long long jj = in ? j : 0;
-          cp_async16(kd + kmaj_off(r, c), kbp + jj * D + c * 8, in ? 16u : 0u);
-          cp_async16(vd + kmaj_off(r, c), vbp + jj * DV + c * 8, in ? 16u : 0u);
+          cp_async16(kdst + kmaj_off(r, cc), kbp + jj * D + cc * 8, in ? 16u : 0u);
+          cp_async16(vdst + kmaj_off(r, cc), vbp + jj * DV + cc * 8, in ? 16u : 0u);
+        }
+#pragma unroll
+        for (int t = 0; t < P_BYTES / 16 / 32; ++t) {
+          const int e = t * 32 + lane;                        // 16-byte unit of the chunk
+          const int img = 2 * c + e / (pscr::kBlockBytes / 16);
+          const bool in = img < nimg;
+          const uint4* src = pt + (in ? (long long)2 * c * (pscr::kBlockBytes / 16) + e : 0);
+          cp_async16(pdst + 16 * e, src, in ? 16u : 0u);
         }
       }
       cp_async_commit();
-      if (g >= KLAG) {
+      if (c >= KLAG) {
         cp_async_wait<KLAG>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.kvfull[(g - KLAG) % KS]);
+        if (lane == 0) mbar_arrive(&bar.kvfull[(c - KLAG) % KS]);
       }
     }
     if (!ok) cp_async_wait<0>();
@@ -261,8 +281,6 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int i = i0 + r;
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
-    const float c2 = inv_h * 1.4426950408889634f;
-    const float mc = valid ? mraw[base + i] * c2 : 0.f;
     float cy = 0.f;  // kbar . y
     if (valid) {
       const float* yr = y + (base + i) * D;
@@ -271,70 +289,84 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       for (int a = 0; a < D; ++a) cy = fmaf(kr[a], yr[a], cy);
     }
     float om = 0.f;
-    for (int g = 0; g < nb; ++g) {
-      const int sb = g & 1;
-      if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) break;
+    bool ok = true;
+    for (int c = 0; c < nck; ++c) {
+      const int st = c % KS, tb = c & 1;
+      if (!warp_wait(&bar.kvfull[st], (c / KS) & 1, status, abort_p) ||
+          !warp_wait(&bar.tfull[tb], (c >> 1) & 1, status, abort_p)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      uint32_t sv[KB], tv[KB];
-      tmem_ld16(lane_base + T_S + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-      tmem_ld16(lane_base + T_S + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
-      tmem_ld16(lane_base + T_T + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
-      tmem_ld16(lane_base + T_T + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
+      uint32_t tv[CK];
+#pragma unroll
+      for (int q4 = 0; q4 < CK / 16; ++q4)
+        tmem_ld16(lane_base + T_T + tb * CK + 16 * q4, *reinterpret_cast<uint32_t(*)[16]>(&tv[16 * q4]));
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
-      const int j0 = g * KB;
-      uint32_t pw[KB / 2], hw[KB / 2], lw[KB / 2];
+      if (lane == 0) mbar_arrive(&bar.tfree[tb]);
+      // This row's 64 weights: 16-byte chunk kc of image m at m * 8192 + kc * 2048 + r * 16.
+      const uint8_t* prow = smem + SM_ST + st * STAGE + 2 * KV_BYTES + r * 16;
+      uint32_t hw[CK / 2], lw[CK / 2];
 #pragma unroll
-      for (int c = 0; c < KB; c += 2) {
-        const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
-        const float p1 =
-            (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
-        const uint32_t w = pack_bf16(p0, p1);
-        pw[c / 2] = w;
-        const float r0 = bf16_lo(w), r1 = bf16_hi(w);
-        om += r0 + r1;
-        const float q0 = r0 * (__uint_as_float(tv[c]) - cy);
-        const float q1 = r1 * (__uint_as_float(tv[c + 1]) - cy);
-        const uint32_t hh = pack_bf16(q0, q1);
-        hw[c / 2] = hh;
-        lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+      for (int kc = 0; kc < CK / 8; ++kc) {
+        const uint4 pv = *reinterpret_cast<const uint4*>(prow + (kc >> 2) * pscr::kBlockBytes + (kc & 3) * 2048);
+        const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = 8 * kc + 2 * u;
+          const float r0 = bf16_lo(pw[u]), r1 = bf16_hi(pw[u]);
+          om += r0 + r1;
+          const float q0 = r0 * (__uint_as_float(tv[j]) - cy);
+          const float q1 = r1 * (__uint_as_float(tv[j + 1]) - cy);
+          const uint32_t hh = pack_bf16(q0, q1);
+          hw[j / 2] = hh;
+          lw[j / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+        }
       }
-      const int pb = g & 1;
-      if (g >= 2 && !warp_wait(&bar.pfree[pb], ((g >> 1) - 1) & 1, status, abort_p)) break;
+      const int pb = c & 1;
+      if (c >= 2 && !warp_wait(&bar.p2free[pb], ((c >> 1) - 1) & 1, status, abort_p)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      tmem_st8(lane_base + T_P + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
-      tmem_st8(lane_base + T_P + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
-      tmem_st8(lane_base + T_P2H + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&hw[0]));
-      tmem_st8(lane_base + T_P2H + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&hw[8]));
-      tmem_st8(lane_base + T_P2L + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&lw[0]));
-      tmem_st8(lane_base + T_P2L + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&lw[8]));
+#pragma unroll
+      for (int q4 = 0; q4 < CK / 16; ++q4) {
+        tmem_st8(lane_base + T_P2H + pb * (CK / 2) + 8 * q4, *reinterpret_cast<uint32_t(*)[8]>(&hw[8 * q4]));
+        tmem_st8(lane_base + T_P2L + pb * (CK / 2) + 8 * q4, *reinterpret_cast<uint32_t(*)[8]>(&lw[8 * q4]));
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.pfull[pb]);
-      if (g == nb - 1) {
-        if (!warp_wait(&bar.accfull, 0, status, abort_p)) break;
-        tc_fence_after();
-        const float inv = 1.f / om;
+      if (lane == 0) mbar_arrive(&bar.p2full[pb]);
+    }
+    if (ok && warp_wait(&bar.accfull, 0, status, abort_p)) {
+      tc_fence_after();
+      const float inv = 1.f / om;
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
-          uint32_t o1[16], o2[16];
-          tmem_ld16(lane_base + T_O1 + c0, o1);
-          tmem_ld16(lane_base + T_O2 + c0, o2);
-          tmem_ld_wait();
-          if (valid) {
+      for (int c0 = 0; c0 < DV; c0 += 16) {
+        uint32_t o1[16], o2[16];
+        tmem_ld16(lane_base + T_O1 + c0, o1);
+        tmem_ld16(lane_base + T_O2 + c0, o2);
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              stf(out, (base + i) * DV + c0 + t,
-                  fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
-          }
+          for (int t = 0; t < 16; ++t)
+            stf(out, (base + i) * DV + c0 + t,
+                fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
         }
       }
     }
   }
 
+  // Teardown: tensor memory is released only after every MMA of both issuers has completed
+  // (bounded waits, whatever the abort flag says).
+  if (warp == 0 && lane == 0) {
+    volatile int never = 0;
+    mbar_wait(&bar.done_t, 0, status, kStatusTimeout, &never);
+    mbar_wait(&bar.done_o, 0, status, kStatusTimeout, &never);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -353,9 +385,9 @@ cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s
   const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-      static_cast<const __nv_bfloat16*>(a.v), ws.mraw, ws.y, ws.kbar, a.T, (int)a.BH(),
-      1.0f / a.h, static_cast<__nv_bfloat16*>(a.out), ws.status);
+      static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
+      static_cast<const uint4*>(ws.pscr), ws.y, ws.kbar, a.T, (int)a.BH(),
+      static_cast<__nv_bfloat16*>(a.out), ws.status);
   count_launch();
   return cudaGetLastError();
 }
