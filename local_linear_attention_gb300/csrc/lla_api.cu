@@ -151,8 +151,11 @@ size_t workspace_bytes(const Args& a) {
   n += align_up(R * a.d * sizeof(float));                // y
   n += align_up(R * a.d * sizeof(float));                // kbar
   n += align_up(R * sizeof(float));                      // omega
-  n += align_up(R * sizeof(float));                      // mraw
-  if (tc_eligible(a)) n += align_up(moments_tc_pscratch_bytes(a.BH(), a.T));  // pscr
+  if (tc_eligible(a)) {
+    n += align_up(R * 3 * a.d * 2);                      // ytc
+    n += align_up(R * sizeof(float));                    // cy
+    n += align_up(moments_tc_pscratch_bytes(a.BH(), a.T));  // pscr
+  }
   return n;
 }
 
@@ -169,8 +172,10 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->y = take(R * a.d * sizeof(float));
   ws->kbar = take(R * a.d * sizeof(float));
   ws->omega = take(R * sizeof(float));
-  ws->mraw = take(R * sizeof(float));
-  ws->pscr = tc_eligible(a) ? take(moments_tc_pscratch_bytes(a.BH(), a.T)) : nullptr;
+  const bool tc = tc_eligible(a);
+  ws->ytc = tc ? reinterpret_cast<uint32_t*>(take(R * 3 * a.d * 2)) : nullptr;
+  ws->cy = tc ? take(R * sizeof(float)) : nullptr;
+  ws->pscr = tc ? take(moments_tc_pscratch_bytes(a.BH(), a.T)) : nullptr;
   ws->status = nullptr;
   ws->path = choose_path(a);
 }

@@ -52,7 +52,9 @@ struct Workspace {
   float* y;       // [BH*T, d]      ridge-solve result y = (C_kk + lambda' I)^-1 (q - kbar)
   float* kbar;    // [BH*T, d]      kbar - c, the weighted key mean in the shifted frame
   float* omega;   // [BH*T]         sum of the weights (tensor-core moments path)
-  float* mraw;    // [BH*T]         row max of q.k (unscaled; tensor-core path, for the readout)
+  uint32_t* ytc;  // [BH*T, 3, d/2]  tensor-core path: y as three exact bf16 parts (y = y1 + y2 + y3),
+                  //                each part a row of d bf16 (packed pairs), for the readout
+  float* cy;      // [BH*T]         tensor-core path: kbar . y
   void* pscr;     // tensor-core path: the kernel weights P of feature pass 0, bf16, one 8 KiB
                   // image per (head, query tile, key block), reused by the later passes
   int* status;    // device status word of the current device

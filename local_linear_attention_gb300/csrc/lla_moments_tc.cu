@@ -46,7 +46,8 @@
 // (a, b), (a, b+1) for even b from a (even a) or a+1 (odd a) up to 64 -- so one operand of each
 // packed product is a key word exactly as loaded -- then the 16 pairs of odd diagonal entries
 // (4u+1, 4u+1), (4u+3, 4u+3). Slot (a, 64) holds sum p k_a, slots (a, 65) are zero padding.
-// Output per query row (fp32): mom_tc[row][slot], omega[row], m[row] = m_i / h, mraw[row] = m_i.
+// Output per query row (fp32): mom_tc[row][slot], omega[row], m[row] = m_i / h; and the bf16
+// weight images in the weight scratch.
 #include <cstdint>
 #include <type_traits>
 
@@ -292,7 +293,7 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
-                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ mraw_out,
+                  int BH, float inv_h, float* __restrict__ m_out,
                   float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pimg,
                   int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -657,7 +658,6 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       if (lane == 0) mbar_arrive(&bar.rowx);
       if (warp_wait(&bar.rowx, 1, status, abort_p) && half == 0 && valid) {
         m_out[base + i] = m * inv_h;
-        mraw_out[base + i] = m;
         omega_out[base + i] = om + bar.part[1][r];
       }
     }
@@ -743,7 +743,7 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
-      (int)a.BH(), 1.0f / a.h, ws.m, ws.mraw, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
       ws.status);
   count_launch();
   return cudaGetLastError();

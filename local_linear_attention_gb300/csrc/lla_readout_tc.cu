@@ -14,8 +14,9 @@
 //
 // Precision: y can be large (small ridge, rank-deficient early prefixes), and its component
 // outside the span of the keys must cancel between k_j . y and kbar . y; y therefore enters the
-// Y K^T contraction as three exact bf16 parts (y = y1 + y2 + y3, 24 significant bits), and the
-// covariance-branch weights p * t enter P2 V as an exact-to-16-bits hi/lo pair.
+// Y K^T contraction as three exact bf16 parts (y = y1 + y2 + y3, 24 significant bits; the solve
+// writes them, with cy = kbar . y), and the covariance-branch weights p * t enter P2 V as an
+// exact-to-16-bits hi/lo pair.
 //
 // One CTA per 128-query tile; keys in chunks of 64 (two weight images). Warp roles (7 warps):
 // 0 issues T = Y K^T (12 MMAs per chunk, N = 64) and owns the TMEM allocation; 6 issues
@@ -92,8 +93,8 @@ static_assert(sizeof(Barriers) <= 256, "barrier region");
 template <typename TOut>
 __global__ void __launch_bounds__(NTHREADS, 1)
 readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                  const uint4* __restrict__ pimg, const float* __restrict__ y,
-                  const float* __restrict__ kbar, int T, int BH, TOut* __restrict__ out,
+                  const uint4* __restrict__ pimg, const uint32_t* __restrict__ ytc,
+                  const float* __restrict__ cy_in, int T, int BH, TOut* __restrict__ out,
                   int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
@@ -114,28 +115,16 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   const uint4* const pt = pimg + pscr::first_block(bh, T, ptile, rank) * (pscr::kBlockBytes / 16);
   const int nimg = pscr::pair_blocks(T, ptile);
 
-  // y split into three exact bf16 parts; one row (query) per thread of warps 2..5.
-  if (warp >= 2 && warp < 6) {
-    const int r = (warp & 3) * 32 + lane;
-    const bool valid = r < nq;
-    const float* yr = y + (base + i0 + r) * D;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t w1[4], w2[4], w3[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        float a = 0.f, b = 0.f;
-        if (valid) { a = yr[c * 8 + 2 * t]; b = yr[c * 8 + 2 * t + 1]; }
-        w1[t] = pack_bf16(a, b);
-        const float a2 = a - bf16_lo(w1[t]), b2 = b - bf16_hi(w1[t]);
-        w2[t] = pack_bf16(a2, b2);
-        w3[t] = pack_bf16(a2 - bf16_lo(w2[t]), b2 - bf16_hi(w2[t]));
-      }
-      *reinterpret_cast<uint4*>(smem + SM_Y + kmaj_off(r, c)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-      *reinterpret_cast<uint4*>(smem + SM_Y + TILE + kmaj_off(r, c)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-      *reinterpret_cast<uint4*>(smem + SM_Y + 2 * TILE + kmaj_off(r, c)) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
-    }
+  // The three parts of the tile's Y (rows of 64 bf16) into the core-matrix layout, by all
+  // threads (rows past the tile's end are zero-filled).
+  for (int e = tid; e < 3 * BM * 8; e += NTHREADS) {
+    const int part = e / (BM * 8), rem = e % (BM * 8), r = rem >> 3, c = rem & 7;
+    const bool in = r < nq;
+    const uint32_t* src = ytc + ((base + i0 + (in ? r : 0)) * 3 + part) * (D / 2) + c * 4;
+    cp_async16(smem + SM_Y + part * TILE + kmaj_off(r, c), src, in ? 16u : 0u);
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
@@ -281,13 +270,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     const int i = i0 + r;
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
-    float cy = 0.f;  // kbar . y
-    if (valid) {
-      const float* yr = y + (base + i) * D;
-      const float* kr = kbar + (base + i) * D;
-#pragma unroll 8
-      for (int a = 0; a < D; ++a) cy = fmaf(kr[a], yr[a], cy);
-    }
+    const float cy = valid ? cy_in[base + i] : 0.f;  // kbar . y
     float om = 0.f;
     bool ok = true;
     for (int c = 0; c < nck; ++c) {
@@ -386,7 +369,7 @@ cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
-      static_cast<const uint4*>(ws.pscr), ws.y, ws.kbar, a.T, (int)a.BH(),
+      static_cast<const uint4*>(ws.pscr), ws.ytc, ws.cy, a.T, (int)a.BH(),
       static_cast<__nv_bfloat16*>(a.out), ws.status);
   count_launch();
   return cudaGetLastError();

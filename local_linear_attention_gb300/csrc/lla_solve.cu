@@ -429,10 +429,21 @@ __device__ __forceinline__ void back(const Lane& L, const float* Lt, float& w0, 
 }
 }  // namespace stc
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Output for the tensor-core readout: y as three exact bf16 parts (y = y1 + y2 + y3; 24
+// significant bits, so that the readout's Y K^T keeps y's precision on the tensor cores), each
+// part a row of 64 bf16 stored as 32 packed pairs, and cy = kbar . y. For the CUDA-core readout
+// (value width other than 64) also y and kbar in fp32 (y_out, kbar_out; else null).
 __global__ void __launch_bounds__(stc::WARPS * 32, 3)
 solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mom, const float* __restrict__ omega,
-                const float* __restrict__ mrow, long long rows, float lam, float* __restrict__ y_out,
-                float* __restrict__ kbar_out, int* __restrict__ status) {
+                const float* __restrict__ mrow, long long rows, float lam, uint32_t* __restrict__ ytc,
+                float* __restrict__ cy_out, float* __restrict__ y_out, float* __restrict__ kbar_out,
+                int* __restrict__ status) {
   using namespace stc;
   __shared__ __align__(16) float sh[WARPS][WARP_FLOATS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -494,30 +505,57 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   }
 
   stc::column<0>(L, cbuf, Lt);
+  uint32_t* yrow = ytc + row * 3 * (D / 2);
   if (!L.ok) {
-    if (lane == 0) atomicOr(status, kStatusNumerical);
-    const float qn = __int_as_float(0x7fc00000);
-    y_out[row * D + L.r0] = qn;
-    y_out[row * D + L.r1] = qn;
-    kbar_out[row * D + L.r0] = qn;
-    kbar_out[row * D + L.r1] = qn;
+    if (lane == 0) {
+      atomicOr(status, kStatusNumerical);
+      cy_out[row] = __int_as_float(0x7fc00000);
+    }
+    for (int p = 0; p < 3; ++p) yrow[p * (D / 2) + lane] = 0x7FC07FC0u;  // bf16 NaN pairs
+    if (y_out) {
+      const float qn = __int_as_float(0x7fc00000);
+      y_out[row * D + L.r0] = qn;
+      y_out[row * D + L.r1] = qn;
+      kbar_out[row * D + L.r0] = qn;
+      kbar_out[row * D + L.r1] = qn;
+    }
     return;
   }
   __syncwarp();
   float w0 = L.z0, w1 = L.z1, y0 = 0.f, y1 = 0.f;
   stc::back(L, Lt, w0, w1, y0, y1);
-  y_out[row * D + L.r0] = y0;
-  y_out[row * D + L.r1] = y1;
-  kbar_out[row * D + L.r0] = kb0;
-  kbar_out[row * D + L.r1] = kb1;
+  // Lane l writes elements 2l and 2l + 1 of each part (element e < 32 is row e of lane e,
+  // element e >= 32 row e of lane 63 - e), so that each part's row is one coalesced store.
+  const int e0 = 2 * lane, e1 = 2 * lane + 1;
+  const float a_lo = __shfl_sync(0xffffffffu, y0, e0 & 31), a_hi = __shfl_sync(0xffffffffu, y1, (D - 1 - e0) & 31);
+  const float b_lo = __shfl_sync(0xffffffffu, y0, e1 & 31), b_hi = __shfl_sync(0xffffffffu, y1, (D - 1 - e1) & 31);
+  const float ya = e0 < 32 ? a_lo : a_hi, yb = e1 < 32 ? b_lo : b_hi;
+  const uint32_t p1 = pack_bf16(ya, yb);
+  const float ra = ya - __uint_as_float(p1 << 16), rb = yb - __uint_as_float(p1 & 0xFFFF0000u);
+  const uint32_t p2 = pack_bf16(ra, rb);
+  const uint32_t p3 =
+      pack_bf16(ra - __uint_as_float(p2 << 16), rb - __uint_as_float(p2 & 0xFFFF0000u));
+  yrow[lane] = p1;
+  yrow[D / 2 + lane] = p2;
+  yrow[D + lane] = p3;
+  float c = fmaf(kb0, y0, kb1 * y1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if (lane == 0) cy_out[row] = c;
+  if (y_out) {
+    y_out[row * D + L.r0] = y0;
+    y_out[row * D + L.r1] = y1;
+    kbar_out[row * D + L.r0] = kb0;
+    kbar_out[row * D + L.r1] = kb1;
+  }
 }
 
 cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long rows = a.rows();
   const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
   solve_tc_kernel<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a.q), ws.mom, ws.omega, ws.m, rows, a.lam, ws.y, ws.kbar,
-      ws.status);
+      static_cast<const __nv_bfloat16*>(a.q), ws.mom, ws.omega, ws.m, rows, a.lam, ws.ytc, ws.cy,
+      a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.status);
   count_launch();
   return cudaGetLastError();
 }
