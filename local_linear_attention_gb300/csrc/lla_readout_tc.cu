@@ -84,6 +84,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
 
 struct Barriers {
   uint64_t kvfull[KS], kvempty[KS];
+  uint64_t pfull[KS];    // the chunk's weight images have landed (bulk copy, transaction count)
   uint64_t tfull[2], tfree[2];
   uint64_t p2full[2], p2free[2];
   uint64_t accfull, done_t, done_o;
@@ -126,7 +127,11 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   cp_async_commit();
   cp_async_wait<0>();
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar.kvfull[s], 1);
+      mbar_init(&bar.kvempty[s], 1);
+      mbar_init(&bar.pfull[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.tfull[s], 1);
       mbar_init(&bar.tfree[s], 4);
@@ -193,7 +198,8 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
       for (int c = 0; c < nck && ok; ++c) {
         const int st = c % KS, pb = c & 1;
         ok = mbar_wait2(&bar.kvfull[st], (c / KS) & 1, &bar.p2full[pb], (c >> 1) & 1, status,
-                        kStatusTimeout, abort_p);
+                        kStatusTimeout, abort_p) &&
+             mbar_wait(&bar.pfull[st], (c / KS) & 1, status, kStatusTimeout, abort_p);
         if (!ok) break;
         tc_fence_after();
         const uint64_t vst = vd + (uint64_t)(st * stage16);
@@ -218,11 +224,12 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V/P loader
-    // cp.async copies with several chunks in flight. K and V rows go to the core-matrix layout
-    // (lane -> (row, 16-byte chunk) mapping conflict-free per 8-lane phase); the two weight
-    // images are copied as they are (missing images past the pair's last block are zero-filled).
-    // A chunk becomes visible to the MMAs (async proxy) only after its copies completed and this
-    // warp fenced them.
+    // K and V: cp.async copies with several chunks in flight, rows to the core-matrix layout (lane
+    // -> (row, 16-byte chunk) mapping conflict-free per 8-lane phase); they become visible to the
+    // MMAs (async proxy) only after the copies completed and this warp fenced them (kvfull). The
+    // two weight images are one contiguous bulk copy into the stage as they are (pfull, counted
+    // in transaction bytes); a missing second image (past the pair's last block) is zero-filled
+    // with ordinary stores, fenced, before the stage's kvfull arrival.
     const __nv_bfloat16* kbp = k + base * D;
     const __nv_bfloat16* vbp = v + base * DV;
     bool ok = true;
@@ -245,13 +252,17 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           cp_async16(kdst + kmaj_off(r, cc), kbp + jj * D + cc * 8, in ? 16u : 0u);
           cp_async16(vdst + kmaj_off(r, cc), vbp + jj * DV + cc * 8, in ? 16u : 0u);
         }
+        const int have = min(2, nimg - 2 * c);  // weight images of this chunk (>= 1)
+        if (have < 2) {
 #pragma unroll
-        for (int t = 0; t < P_BYTES / 16 / 32; ++t) {
-          const int e = t * 32 + lane;                        // 16-byte unit of the chunk
-          const int img = 2 * c + e / (pscr::kBlockBytes / 16);
-          const bool in = img < nimg;
-          const uint4* src = pt + (in ? (long long)2 * c * (pscr::kBlockBytes / 16) + e : 0);
-          cp_async16(pdst + 16 * e, src, in ? 16u : 0u);
+          for (int t = 0; t < pscr::kBlockBytes / 16 / 32; ++t)
+            reinterpret_cast<uint4*>(pdst + pscr::kBlockBytes)[t * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)have * pscr::kBlockBytes;
+          mbar_arrive_expect_tx(&bar.pfull[st], bytes);
+          bulk_g2s(pdst, pt + (long long)2 * c * (pscr::kBlockBytes / 16), bytes, &bar.pfull[st]);
         }
       }
       cp_async_commit();
@@ -275,7 +286,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     bool ok = true;
     for (int c = 0; c < nck; ++c) {
       const int st = c % KS, tb = c & 1;
-      if (!warp_wait(&bar.kvfull[st], (c / KS) & 1, status, abort_p) ||
+      if (!warp_wait(&bar.pfull[st], (c / KS) & 1, status, abort_p) ||
           !warp_wait(&bar.tfull[tb], (c >> 1) & 1, status, abort_p)) {
         ok = false;
         break;

@@ -105,6 +105,24 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// One-dimensional bulk copy (the TMA engine) of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to this CTA's shared memory; completion is counted on `bar` as `bytes`
+// transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Arrival on `bar` that also announces `bytes` transaction bytes still to come.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
 // ----------------------------------------------------------------------------- fences
 // Makes this thread's generic-proxy writes to shared memory visible to the async proxy
 // (tcgen05.mma operand reads).
