@@ -104,7 +104,7 @@ int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B
  *
  * - Size limit: returns LLA_ERR_UNSUPPORTED, before touching the device, when
  *   lla_workspace_size(B, H, T, d, dv, dtype) exceeds LLA_NOALLOC_SCRATCH_BYTES (e.g. bf16
- *   d = dv = 64 fits T <= 4352 at B*H = 1 and T <= 736 at B*H = 8; the tensor-core path's weight
+ *   d = dv = 64 fits T <= 4352 at B*H = 1 and T <= 711 at B*H = 8; the tensor-core path's weight
  *   scratch grows with B*H*T^2). Other argument errors are those of lla_forward.
  * - Set-up: the first call on each device looks up the scratch array's device address (with that
  *   device current) and caches it; make that first call before any stream capture.
