@@ -425,6 +425,11 @@ def main(argv=None):
     ap.add_argument("--op", choices=["lla", "parallax"], default="lla",
                     help="the operation timed: the LLA forward (default) or the Parallax forward")
     ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--strategy", choices=["dense", "cg"], default="dense",
+                    help="ridge systems from dense tensor-core moments + Cholesky (default), or "
+                         "matrix-free conjugate gradients (bf16 d = dv = 64 only)")
+    ap.add_argument("--cg-iters", type=int, default=1024)
+    ap.add_argument("--cg-tol", type=float, default=1e-3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--shape", default=None,
@@ -468,6 +473,9 @@ def main(argv=None):
         return run_parallax(args, w, cpu, world, rank)
 
     lam, h = w.points[0]
+    if args.strategy == "cg":
+        lla.lla_set_moments_path(lla.PATH_CG)
+        lla.lla_set_cg(args.cg_iters, args.cg_tol)
     q, k, v = W.make_inputs(w)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=dq.dtype, device="cuda")
@@ -559,6 +567,9 @@ def main(argv=None):
                                f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
     roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                  "traffic": recorded_traffic(kernel_file), "avg_launch_ms": mom_ms})
+    if args.strategy == "cg":
+        # The moments stage is reduced to its two weight sweeps; the CG passes vary in number.
+        roof = None
     step_tflops = step_flops(w) * world / (ms_per_step / 1e3) / 1e12
 
     if rank == 0:
@@ -572,7 +583,10 @@ def main(argv=None):
                                    f"lambda={lam}, seed {w.seed}",
                        "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
                        "l2": "flushed between steps (256 MiB write outside the step events)",
-                       "parallelism": f"replica per GPU x{world}"},
+                       "parallelism": f"replica per GPU x{world}",
+                       "strategy": (f"cg (max {args.cg_iters} passes, rel. residual "
+                                    f"{args.cg_tol:g})" if args.strategy == "cg"
+                                    else "dense moments + Cholesky")},
             "tflops": step_tflops,
             "bf16_peak_fraction": step_tflops / float(peaks.get("bf16_tflops", 1900.0)),
             "roofline": roof,

@@ -178,11 +178,28 @@ int lla_version(void);
  * Selects the implementation of the moments stage for lla_forward* calls made afterwards by this
  * process: 0 = automatic (tensor cores -- tcgen05 with exact bf16 hi/lo products -- for bf16
  * inputs with d = 64, CUDA cores otherwise), 1 = CUDA cores always, 2 = tensor cores wherever
- * supported (currently the same as 0). Both compute the same moments; the choice exists for
- * testing and measurement. The same choice applies to lla_parallax_forward. Returns
- * LLA_ERR_INVALID_ARG for any other value. Host-only.
+ * supported (currently the same as 0), 3 = the matrix-free conjugate-gradient strategy for bf16
+ * inputs with d = dv = 64 (as 0 elsewhere): the per-query ridge systems are solved by CG, each
+ * product with C_kk being one streaming pass over the prefix, as the "Parallax" blog (s.2
+ * "Difficulties in Scaling LLA") describes exact LLA being computed, instead of accumulating the
+ * d x d moments and factoring them (see lla_set_cg). Paths 0-2 compute the same moments; 3 solves
+ * the same systems iteratively. The choice exists for testing and measurement; a workspace for
+ * lla_forward_ws must be sized (lla_workspace_size) under the path it is used with. The same
+ * choice applies to lla_parallax_forward (3 as 0). Returns LLA_ERR_INVALID_ARG for any other
+ * value. Host-only.
  */
 int lla_set_moments_path(int path);
+
+/*
+ * Parameters of the conjugate-gradient strategy (lla_set_moments_path(3)) for later calls by this
+ * process: each query row iterates until ||r|| <= rel_tol ||r_0|| (r the residual of
+ * (C_kk + lambda' I) y = q - kbar, r_0 = q - kbar) or max_iters streaming passes have run
+ * (defaults 1024 and 1e-3). A call with this strategy synchronises its stream every 8 iterations to
+ * test whether any query tile is still iterating, so it cannot be captured in a CUDA graph.
+ * 1 <= max_iters <= 1024, 0 < rel_tol < 1; otherwise LLA_ERR_INVALID_ARG. Host-only.
+ * No counterpart on the pages beyond the CG solve itself (see above).
+ */
+int lla_set_cg(int max_iters, float rel_tol);
 
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 unsigned long long lla_launch_count(void);

@@ -16,7 +16,7 @@ __all__ = [
     "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
     "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
-    "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "lla_parallax_forward",
+    "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "PATH_CG", "lla_set_cg", "lla_parallax_forward",
 ]
 
 LLA_OK = 0
@@ -28,7 +28,7 @@ STAGE_NAMES = ("prep", "moments", "solve", "readout")
 EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
-    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path",
+    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg",
     "lla_parallax_forward",
 )
 
@@ -74,6 +74,7 @@ def _load():
         "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
         "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_set_moments_path": (i, [i]),
+        "lla_set_cg": (i, [i, ctypes.c_float]),
         "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
     }
     for name, (res, args) in sig.items():
@@ -91,12 +92,18 @@ def lla_version() -> int:
     return _load().lla_version()
 
 
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CG = 0, 1, 2, 3
 
 
 def lla_set_moments_path(path: int):
-    """Select the moments stage (0 auto, 1 CUDA cores, 2 tensor cores where supported)."""
+    """Select the moments stage (0 auto, 1 CUDA cores, 2 tensor cores where supported, 3 the
+    matrix-free conjugate-gradient strategy for bf16 d = dv = 64)."""
     _check(_load().lla_set_moments_path(int(path)), "lla_set_moments_path")
+
+
+def lla_set_cg(max_iters: int, rel_tol: float):
+    """Iteration cap and relative residual tolerance of the conjugate-gradient strategy."""
+    _check(_load().lla_set_cg(int(max_iters), float(rel_tol)), "lla_set_cg")
 
 
 def launch_count() -> int:

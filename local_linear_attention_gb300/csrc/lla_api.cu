@@ -16,7 +16,9 @@ __device__ int g_status;
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
-std::atomic<int> g_path_request{0};  // 0 auto, kPathCudaCore, kPathTensorCore
+std::atomic<int> g_path_request{0};  // 0 auto, kPathCudaCore, kPathTensorCore, kPathCG
+std::atomic<int> g_cg_max_iters{1024};
+std::atomic<float> g_cg_rel_tol{1e-3f};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -117,6 +119,13 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
       ws.path == kPathTensorCore ? launch_moments_tc : launch_moments_ffma,
       launch_solve,
       (ws.path == kPathTensorCore && a.dv == 64) ? launch_readout_tc : launch_readout};
+  if (ws.path == kPathCG) {  // matrix-free CG for the ridge systems (bf16, d = dv = 64)
+    stages[1] = launch_weights_tc;
+    stages[2] = [](const Args& a2, const Workspace& w2, cudaStream_t s2) {
+      return launch_cg_solve(a2, w2, s2, g_cg_max_iters.load(), g_cg_rel_tol.load());
+    };
+    stages[3] = launch_readout_tc;
+  }
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
     if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);
@@ -136,6 +145,7 @@ int choose_path(const Args& a) {
   const bool tc_ok = tc_eligible(a);
   const int req = g_path_request.load();
   if (req == kPathCudaCore || !tc_ok) return kPathCudaCore;
+  if (req == kPathCG && a.dv == 64) return kPathCG;
   return kPathTensorCore;
 }
 
@@ -318,8 +328,16 @@ int lla_version(void) {
 unsigned long long lla_launch_count(void) { return g_launches.load(); }
 
 int lla_set_moments_path(int path) {
-  if (path < 0 || path > 2) return LLA_ERR_INVALID_ARG;
+  if (path < 0 || path > 3) return LLA_ERR_INVALID_ARG;
   g_path_request.store(path);
+  return LLA_OK;
+}
+
+int lla_set_cg(int max_iters, float rel_tol) {
+  if (max_iters < 1 || max_iters > 1024 || !(rel_tol > 0.f) || !(rel_tol < 1.f))
+    return LLA_ERR_INVALID_ARG;
+  g_cg_max_iters.store(max_iters);
+  g_cg_rel_tol.store(rel_tol);
   return LLA_OK;
 }
 

@@ -64,7 +64,7 @@ struct Workspace {
 // Moments implementations. The tensor-core stage handles bf16 inputs with d = 64 and leaves the
 // keys unshifted (c = 0: shifted bf16 keys would no longer multiply exactly); everything else
 // uses the CUDA-core stage.
-enum : int { kPathCudaCore = 1, kPathTensorCore = 2 };
+enum : int { kPathCudaCore = 1, kPathTensorCore = 2, kPathCG = 3 };
 int choose_path(const Args& a);
 
 size_t workspace_bytes(const Args& a);
@@ -107,6 +107,19 @@ inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+// The tensor-core readout pass with fp32 output, values `v` (bf16, [B,H,T,64]), y given as
+// three bf16 parts and kbar . y, tiles with tile_active[tile] == 0 skipped (null: none); matvec:
+// only the covariance branch (out = C_vk y, which is C_kk y for v = k).
+cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,
+                                  const void* v, const uint32_t* ytc, const float* cy, float* out,
+                                  const int* tile_active, bool matvec);
+// The moments stage reduced to its two sweeps: m, omega and the weight images only.
+cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+// Conjugate-gradient strategy for the ridge systems (bf16, d = dv = 64): fills ytc and cy like
+// the tensor-core solve, with its state in the moments region of the workspace.
+cudaError_t launch_cg_solve(const Args& a, const Workspace& ws, cudaStream_t s, int max_iters,
+                            float rel_tol);
+size_t cg_state_bytes(const Args& a);
 // Causal Parallax forward with probe r (same layout as q); tensor cores when path ==
 // kPathTensorCore and the shape is bf16 with d = dv = 64, CUDA cores otherwise.
 cudaError_t launch_parallax(const Args& a, const void* r, int path, int* status, cudaStream_t s);

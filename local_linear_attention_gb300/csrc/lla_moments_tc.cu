@@ -295,7 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
                   int BH, float inv_h, float* __restrict__ m_out,
                   float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pimg,
-                  int* __restrict__ status) {
+                  int npass, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -313,7 +313,9 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int nq = max(0, min(BM, T - i0));
   const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
   const int nb = (jend + KB - 1) / KB;
-  const int G = nb * (2 + NPASS);  // key blocks streamed: max sweep, weight sweep, feature passes
+  // key blocks streamed: max sweep, weight sweep, npass feature passes (NPASS for the moments, 0
+  // when only the weights, m and omega are wanted)
+  const int G = nb * (2 + npass);
   const long long base = bh * T;
   // This CTA's P blocks in the scratch (layout: pscr:: in the internal header).
   uint4* const ptile_p = pimg + pscr::first_block(bh, T, ptile, rank) * (P_BLOCK / 16);
@@ -417,7 +419,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       constexpr uint32_t id_b = idesc_bf16(PM, NB_, false, true);
       constexpr uint32_t nb_off = GA * 512 / 16;  // local group GA: the N = 176 MMA's half
       const uint32_t t_acc = tbase + T_ACC, t_p = tbase + T_P;
-      const int H = nb * NPASS;
+      const int H = nb * npass;
       bool ok = true;
       int b = t % nb, pass = t / nb;  // block and pass of step h
       for (int h = t; h < H && ok; h += 2) {
@@ -617,7 +619,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       constexpr int kChunk = 2048 / 16;
       // slot s, chunk c of this lane at ring + s * 64 + c * 32 (a warp's accesses are contiguous)
       uint4* ring = reinterpret_cast<uint4*>(smem + SM_PR) + (warp - 2) * PD * 64 + lane;
-      const int hend = nb * NPASS;
+      const int hend = nb * npass;
       auto fetch = [&](int hh) {
         if (hh < hend) {
           const uint4* src =
@@ -631,7 +633,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       if (ok)
         for (int t = 0; t < PD; ++t) fetch(t);
       int h = 0;  // feature step index
-      for (int pass = 0; pass < NPASS && ok; ++pass) {
+      for (int pass = 0; pass < npass && ok; ++pass) {
         for (int b = 0; b < nb; ++b, ++h) {
           cp_async_wait<PD - 1>();
           const uint4* slot = ring + (h % PD) * 64;
@@ -734,7 +736,8 @@ size_t moments_tc_pscratch_bytes(long long BH, int T) {
   return (size_t)BH * (size_t)pscr::blocks_per_head(T) * P_BLOCK;
 }
 
-cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+namespace {
+cudaError_t launch_tc(const Args& a, const Workspace& ws, cudaStream_t s, int npass) {
   auto kern = moments_tc_kernel;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
@@ -743,10 +746,19 @@ cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
-      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr),
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr), npass,
       ws.status);
   count_launch();
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  return launch_tc(a, ws, s, NPASS);
+}
+
+cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  return launch_tc(a, ws, s, 0);
 }
 
 }  // namespace lla

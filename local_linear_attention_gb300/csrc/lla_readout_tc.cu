@@ -18,6 +18,11 @@
 // writes them, with cy = kbar . y), and the covariance-branch weights p * t enter P2 V as an
 // exact-to-16-bits hi/lo pair.
 //
+// The same pass, with V := K and y := a conjugate-gradient direction p and only the covariance
+// branch kept (kMatvec), returns C_kk p: the matrix-free product that the CG strategy for the
+// ridge system needs (C_kk p = sum_j p_ij ((k_j - kbar) . p) k_j). Tiles whose flag in
+// `tile_active` is 0 are skipped.
+//
 // One CTA per 128-query tile; keys in chunks of 64 (two weight images). Warp roles (7 warps):
 // 0 issues T = Y K^T (12 MMAs per chunk, N = 64) and owns the TMEM allocation; 6 issues
 // O1 += P V (P straight from shared memory) and O2 += P2 V (P2 from tensor memory), 12 MMAs per
@@ -91,12 +96,12 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 256, "barrier region");
 
-template <typename TOut>
+template <typename TOut, bool kMatvec>
 __global__ void __launch_bounds__(NTHREADS, 1)
 readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                   const uint4* __restrict__ pimg, const uint32_t* __restrict__ ytc,
                   const float* __restrict__ cy_in, int T, int BH, TOut* __restrict__ out,
-                  int* __restrict__ status) {
+                  const int* __restrict__ tile_active, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -111,6 +116,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   const int jend = i0 + nq;
   const int nck = (jend + CK - 1) / CK;
   const long long base = bh * T;
+  if (tile_active && !tile_active[bh * ntiles + tile]) return;  // the whole CTA, before any setup
   // This tile's weight images: tile = 2 ptile + rank in the moments stage's pairing.
   const int ptile = tile >> 1, rank = tile & 1;
   const uint4* const pt = pimg + pscr::first_block(bh, T, ptile, rank) * (pscr::kBlockBytes / 16);
@@ -210,7 +216,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           // keys 16s..16s+15: image s / 2, K-adjacent core matrices 2 (s % 2), 2 (s % 2) + 1
           const uint64_t pds = pst + (uint64_t)((s >> 1) * (pscr::kBlockBytes >> 4) + (s & 1) * (4096 >> 4));
           const uint32_t acc = (c > 0 || s > 0) ? 1u : 0u;
-          mma_ss(tbase + T_O1, pds, vds, id_o, acc);
+          if (!kMatvec) mma_ss(tbase + T_O1, pds, vds, id_o, acc);
           mma_ts(tbase + T_O2, tbase + T_P2H + pb * (CK / 2) + s * 8, vds, id_o, acc);
           mma_ts(tbase + T_O2, tbase + T_P2L + pb * (CK / 2) + s * 8, vds, id_o, 1u);
         }
@@ -341,14 +347,15 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 16) {
         uint32_t o1[16], o2[16];
-        tmem_ld16(lane_base + T_O1 + c0, o1);
+        if (!kMatvec) tmem_ld16(lane_base + T_O1 + c0, o1);
         tmem_ld16(lane_base + T_O2 + c0, o2);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
           for (int t = 0; t < 16; ++t)
             stf(out, (base + i) * DV + c0 + t,
-                fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
+                kMatvec ? __uint_as_float(o2[t])
+                        : fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
         }
       }
     }
@@ -369,21 +376,35 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   }
 }
 
-}  // namespace
-
-cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
-  auto kern = readout_tc_kernel<__nv_bfloat16>;
+template <typename TOut, bool kMatvec>
+cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* v,
+                      const uint32_t* ytc, const float* cy, TOut* out, const int* tile_active) {
+  auto kern = readout_tc_kernel<TOut, kMatvec>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
   const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
-      static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
-      static_cast<const uint4*>(ws.pscr), ws.ytc, ws.cy, a.T, (int)a.BH(),
-      static_cast<__nv_bfloat16*>(a.out), ws.status);
+      static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(v),
+      static_cast<const uint4*>(ws.pscr), ytc, cy, a.T, (int)a.BH(), out, tile_active,
+      ws.status);
   count_launch();
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  return launch_ro<__nv_bfloat16, false>(a, ws, s, a.v, ws.ytc, ws.cy,
+                                         static_cast<__nv_bfloat16*>(a.out), nullptr);
+}
+
+cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,
+                                  const void* v, const uint32_t* ytc, const float* cy, float* out,
+                                  const int* tile_active, bool matvec) {
+  return matvec ? launch_ro<float, true>(a, ws, s, v, ytc, cy, out, tile_active)
+                : launch_ro<float, false>(a, ws, s, v, ytc, cy, out, tile_active);
 }
 
 }  // namespace lla

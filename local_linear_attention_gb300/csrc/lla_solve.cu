@@ -578,9 +578,9 @@ cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
-  // The tensor-core path leaves keys unshifted, and its readout (dv = 64) forms every value
-  // term from centred weights, so it needs neither reference point.
-  if (ws.path == kPathTensorCore && a.dv == 64) return cudaSuccess;
+  // The tensor-core paths leave keys unshifted, and their readout (dv = 64) forms every value
+  // term from centred weights, so they need neither reference point.
+  if (ws.path != kPathCudaCore && a.dv == 64) return cudaSuccess;
   const dim3 grid((unsigned)a.BH(), 2);
   if (a.dtype == LLA_F32)
     mean_kernel<float><<<grid, 256, 256 * sizeof(float), s>>>(
