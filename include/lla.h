@@ -162,6 +162,33 @@ int lla_parallax_forward(const void* q, const void* k, const void* v, const void
                          int B, int H, int T, int d, int dv, float h, int dtype, void* stream);
 
 /*
+ * Decode: one query per head against a key/value cache of L positions that the query attends to
+ * in full (it is the newest token; its own key and value are already appended). The output is
+ * what lla_forward returns for its last row, o = vbar + C_vk (C_kk + lambda I)^-1 (q - kbar) with
+ * w_j = exp(q . k_j / h) over all L positions ("Parallax" blog, s.2 Canonical Formulation).
+ * q: [B,H,d]; k: [B,H,L,d]; v: [B,H,L,dv]; out: [B,H,dv]; device, element type `dtype`, 16-byte
+ * aligned; d, dv in {16, 32, 64}; B*H*L < 2^31; h, lambda finite and positive. The cache of each
+ * head is split over several CTAs that reduce their chunk to partial moments (float32, shifted by
+ * the chunk's maximum logit); the last CTA of the head to finish merges them and solves the
+ * ridge system in float64 (split-KV with a last-arriver merge, as the blog's decode kernel,
+ * Appendix C). Asynchronous on `stream`; scratch from the stream-ordered pool. B*H = 0 is a
+ * no-op; L = 0 with B*H > 0 is LLA_ERR_INVALID_ARG. A non-positive pivot (non-finite inputs)
+ * makes that head's output NaN and records LLA_ERR_NUMERICAL.
+ */
+int lla_decode(const void* q, const void* k, const void* v, void* out, int B, int H, int L, int d,
+               int dv, float h, float lambda, int dtype, void* stream);
+
+/*
+ * Parallax decode with probe r ([B,H,d], same dtype): o = vbar - Sigma_KV r over all L cached
+ * positions, as lla_parallax_forward's last row, computed as the blog's streaming combination
+ * (1 + d2/d1) O1/d1 - O2/d1 (Appendix C) with the same split-KV and last-arriver merge as
+ * lla_decode (float32 partials, the merge in float64). Otherwise as lla_decode (lambda plays no
+ * part; no status is recorded).
+ */
+int lla_parallax_decode(const void* q, const void* k, const void* v, const void* r, void* out,
+                        int B, int H, int L, int d, int dv, float h, int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns LLA_OK, LLA_ERR_NUMERICAL, LLA_ERR_TIMEOUT, LLA_ERR_INVALID_ARG (bad idx in
  * lla_moments) or LLA_ERR_CUDA (a sticky CUDA error or failed synchronisation).

@@ -17,6 +17,7 @@ __all__ = [
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
     "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
     "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "PATH_CG", "lla_set_cg", "lla_parallax_forward",
+    "lla_decode", "lla_parallax_decode",
 ]
 
 LLA_OK = 0
@@ -28,7 +29,7 @@ STAGE_NAMES = ("prep", "moments", "solve", "readout")
 EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
-    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg",
+    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg", "lla_decode", "lla_parallax_decode",
     "lla_parallax_forward",
 )
 
@@ -76,6 +77,8 @@ def _load():
         "lla_set_moments_path": (i, [i]),
         "lla_set_cg": (i, [i, ctypes.c_float]),
         "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
+        "lla_decode": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
+        "lla_parallax_decode": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -161,6 +164,45 @@ def lla_parallax_forward(q, k, v, r, h: float, out=None, stream=None):
                                       out.data_ptr(), B, H, T, d, dv, float(h), code,
                                       _stream_ptr(stream))
     _check(st, "lla_parallax_forward")
+    return out
+
+
+def _decode_inputs(q, k, v):
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if q.dim() != 3 or k.dim() != 4 or v.dim() != 4 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("decode expects q [B,H,d], k [B,H,L,d], v [B,H,L,dv] of one dtype")
+    B, H, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape[:3] != k.shape[:3]:
+        raise ValueError("inconsistent decode shapes")
+    if q.dtype not in DTYPE_CODES:
+        raise ValueError("dtype must be float32 or bfloat16")
+    return B, H, k.shape[2], d, v.shape[3], DTYPE_CODES[q.dtype]
+
+
+def lla_decode(q, k, v, h: float, lam: float, out=None, stream=None):
+    """LLA decode: q [B,H,d] against the cache k [B,H,L,d], v [B,H,L,dv]; returns [B,H,dv]."""
+    B, H, L, d, dv, code = _decode_inputs(q, k, v)
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    st = _load().lla_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, d,
+                            dv, float(h), float(lam), code, _stream_ptr(stream))
+    _check(st, "lla_decode")
+    return out
+
+
+def lla_parallax_decode(q, k, v, r, h: float, out=None, stream=None):
+    """Parallax decode with probe r [B,H,d] (like q); returns [B,H,dv]."""
+    B, H, L, d, dv, code = _decode_inputs(q, k, v)
+    if r.shape != q.shape or r.dtype != q.dtype or not r.is_cuda or not r.is_contiguous():
+        raise ValueError("r must be a contiguous CUDA tensor shaped and typed like q")
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    st = _load().lla_parallax_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                     out.data_ptr(), B, H, L, d, dv, float(h), code,
+                                     _stream_ptr(stream))
+    _check(st, "lla_parallax_decode")
     return out
 
 

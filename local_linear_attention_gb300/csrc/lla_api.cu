@@ -294,6 +294,44 @@ int lla_parallax_forward(const void* q, const void* k, const void* v, const void
              : LLA_ERR_CUDA;
 }
 
+namespace {
+int run_decode(const DecodeArgs& a, void* stream) {
+  if (a.B < 0 || a.H < 0 || a.L < 0) return LLA_ERR_INVALID_ARG;
+  if (a.dtype != LLA_F32 && a.dtype != LLA_BF16) return LLA_ERR_INVALID_ARG;
+  if (!(a.d == 16 || a.d == 32 || a.d == 64) || !(a.dv == 16 || a.dv == 32 || a.dv == 64))
+    return LLA_ERR_UNSUPPORTED;
+  if (a.BH() * (long long)a.L >= (1LL << 31)) return LLA_ERR_UNSUPPORTED;
+  if (!is_finite_pos(a.h) || (!a.r && !is_finite_pos(a.lam))) return LLA_ERR_INVALID_ARG;
+  if (a.BH() == 0) return LLA_OK;
+  if (a.L == 0) return LLA_ERR_INVALID_ARG;  // nothing to attend to
+  if (!a.q || !a.k || !a.v || !a.out || !aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) ||
+      !aligned16(a.out))
+    return LLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = nullptr;
+  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, decode_workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
+  int st = launch_decode(a, ws, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
+  return st;
+}
+}  // namespace
+
+int lla_decode(const void* q, const void* k, const void* v, void* out, int B, int H, int L, int d,
+               int dv, float h, float lambda, int dtype, void* stream) {
+  DecodeArgs a{q, k, v, nullptr, out, B, H, L, d, dv, h, lambda, dtype};
+  return run_decode(a, stream);
+}
+
+int lla_parallax_decode(const void* q, const void* k, const void* v, const void* r, void* out,
+                        int B, int H, int L, int d, int dv, float h, int dtype, void* stream) {
+  if (B > 0 && H > 0 && (!r || !aligned16(r))) return LLA_ERR_INVALID_ARG;
+  DecodeArgs a{q, k, v, r, out, B, H, L, d, dv, h, 1.f, dtype};
+  if (!r) return LLA_ERR_INVALID_ARG;
+  return run_decode(a, stream);
+}
+
 int lla_stream_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return LLA_ERR_CUDA;

@@ -1,0 +1,422 @@
+// Decode: one query per head against a key/value cache of L positions, for LLA and for Parallax.
+//
+// The query attends to every cached position (it is the newest token; its own key and value are
+// already appended), so the definitions are those of the prefill forward for its last row:
+//  * LLA ("Parallax" blog, s.2 Canonical Formulation): the intercept of the weighted ridge fit,
+//    o = vbar + C_vk (C_kk + lambda I)^-1 (q - kbar), w_j = exp(q . k_j / h);
+//  * Parallax (s.2 "Parallax", Appendix B with eta = 0): o = vbar - Sigma_KV r, computed as the
+//    blog's streaming combination (1 + d2/d1) O1/d1 - O2/d1 (Appendix C), with O1 = sum p_j v_j,
+//    O2 = sum p_j (r . k_j) v_j, d1 = sum p_j, d2 = sum p_j (r . k_j).
+//
+// With one query per head, the per-head work is a reduction over the cache; decode batches have
+// few heads and long caches, so the cache of each head is split over S CTAs ("split-KV", as the
+// blog's decode kernel does, Appendix C): each CTA reduces its chunk of keys to partial sums
+// shifted by the chunk's own maximum logit, writes them to a workspace, and the last CTA of the
+// head to finish (an atomic arrival counter after a memory fence) merges them, rescaling each by
+// exp((m_s - M) / h) with M the largest chunk maximum, in a fixed order (so the result does not
+// depend on which CTA arrives last), and writes the output. For LLA the merged moments are
+// centred and the d x d ridge system is solved by Cholesky, in double precision (one small system
+// per head). Each CTA takes the exact maximum of its chunk in a first sweep over its keys.
+//
+// The reductions are rank-1 updates per key (the query dimension is 1), so they run on the CUDA
+// cores: keys are staged in shared memory in tiles, one thread per key forms the weight, and the
+// LLA second moments accumulate in 4 x 4 register tiles (two shared loads per 16 FMAs).
+#include <cfloat>
+#include <cstdint>
+
+#include "lla_internal.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int NT = 256;   // threads per CTA
+constexpr int TK = 64;    // keys per shared-memory tile
+
+template <typename TIn>
+__device__ __forceinline__ float ld(const TIn* p, long long i) { return ldf(p, i); }
+
+// Block reduction (max) of one float per thread.
+__device__ __forceinline__ float block_max(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = x;
+  __syncthreads();
+  float r = -INFINITY;
+  for (int i = 0; i < NT / 32; ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+
+// Arrival of one CTA of head bh after its partial sums are written; true for the last one, which
+// then sees every CTA's partials.
+__device__ __forceinline__ bool last_arrival(int* counter, int S, int* flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *flag = atomicAdd(counter, 1) == S - 1;
+  __syncthreads();
+  if (*flag) __threadfence();
+  return *flag;
+}
+
+__global__ void zero_counters(int* c, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c[i] = 0;
+}
+
+// ------------------------------------------------------------------------------------ Parallax
+// Partial of a chunk: [m, d1, d2, O1[DV], O2[DV]].
+template <int D, int DV>
+constexpr int px_part() { return 3 + 2 * DV; }
+
+template <typename TIn, int D, int DV>
+__global__ void __launch_bounds__(NT)
+parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
+                       const TIn* __restrict__ v, const TIn* __restrict__ r, int L, int S,
+                       float inv_h, float* __restrict__ part, int* __restrict__ counter,
+                       TIn* __restrict__ out) {
+  constexpr int NG = NT / (2 * DV);  // key groups: thread t takes O coordinate t % 2DV, group t / 2DV
+  __shared__ float qs[D], rs[D], red[NT / 32];
+  __shared__ float kt[TK][D + 1], vt[TK][DV + 1], pt[TK], tt[TK];
+  __shared__ float og_s[NG][2 * DV], dsum[2][2], tot[2 * DV + 2];
+  __shared__ int is_last;
+  const long long bh = blockIdx.x / S;
+  const int s = blockIdx.x % S, tid = threadIdx.x;
+  const int chunk = (L + S - 1) / S;
+  const int j0 = s * chunk, j1 = min(L, j0 + chunk);
+  for (int a = tid; a < D; a += NT) {
+    qs[a] = ld(q, bh * D + a);
+    rs[a] = ld(r, bh * D + a);
+  }
+  __syncthreads();
+  const TIn* kb = k + bh * (long long)L * D;
+  const TIn* vb = v + bh * (long long)L * DV;
+  // sweep 1: the chunk's maximum logit q . k_j
+  float mx = -INFINITY;
+  for (int j = j0 + tid; j < j1; j += NT) {
+    float sj = 0.f;
+    for (int a = 0; a < D; ++a) sj = fmaf(qs[a], ld(kb, (long long)j * D + a), sj);
+    mx = fmaxf(mx, sj);
+  }
+  const float m = block_max(mx, red);
+  // sweep 2: weights and the two branches
+  float acc0 = 0.f, d1 = 0.f, d2 = 0.f;
+  const int oc = tid % (2 * DV), og = tid / (2 * DV);  // O1/O2 coordinate and key group
+  for (int t0 = j0; t0 < j1; t0 += TK) {
+    const int n = min(TK, j1 - t0);
+    __syncthreads();
+    for (int e = tid; e < TK * D; e += NT) {
+      const int jj = e / D, a = e % D;
+      kt[jj][a] = jj < n ? ld(kb, (long long)(t0 + jj) * D + a) : 0.f;
+    }
+    for (int e = tid; e < TK * DV; e += NT) {
+      const int jj = e / DV, a = e % DV;
+      vt[jj][a] = jj < n ? ld(vb, (long long)(t0 + jj) * DV + a) : 0.f;
+    }
+    __syncthreads();
+    if (tid < TK) {
+      float sj = 0.f, tj = 0.f;
+      for (int a = 0; a < D; ++a) {
+        sj = fmaf(qs[a], kt[tid][a], sj);
+        tj = fmaf(rs[a], kt[tid][a], tj);
+      }
+      const float p = tid < n ? __expf((sj - m) * inv_h) : 0.f;
+      pt[tid] = p;
+      tt[tid] = p * tj;
+      d1 += p;
+      d2 += p * tj;
+    }
+    __syncthreads();
+    {
+      const int col = oc % DV;
+      const float* w = oc < DV ? pt : tt;
+      for (int jj = og; jj < n; jj += NG) acc0 = fmaf(w[jj], vt[jj][col], acc0);
+    }
+  }
+  // Reductions in a fixed order (no atomics), so that the result is reproducible.
+  og_s[og][oc] = acc0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+  }
+  static_assert(TK == 64, "d1 and d2 are summed over the two warps of key threads");
+  if ((tid & 31) == 0 && tid < TK) { dsum[tid >> 5][0] = d1; dsum[tid >> 5][1] = d2; }
+  __syncthreads();
+  float* pp = part + blockIdx.x * (long long)px_part<D, DV>();
+  if (tid == 0) { pp[0] = m; pp[1] = dsum[0][0] + dsum[1][0]; pp[2] = dsum[0][1] + dsum[1][1]; }
+  for (int c = tid; c < 2 * DV; c += NT) {
+    float t = 0.f;
+    for (int g = 0; g < NG; ++g) t += og_s[g][c];
+    pp[3 + c] = t;
+  }
+  if (!last_arrival(counter + bh, S, &is_last)) return;
+  // merge (the last CTA of the head)
+  const float* hp = part + bh * S * (long long)px_part<D, DV>();
+  float M = -INFINITY;
+  for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * px_part<D, DV>()));
+  __syncthreads();
+  for (int c = tid; c < 2 * DV + 2; c += NT) {
+    double acc = 0.0;
+    for (int t = 0; t < S; ++t) {
+      const float* pt_ = hp + t * px_part<D, DV>();
+      const float mt = __ldcg(pt_);
+      const double al = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
+      acc += al * (double)__ldcg(pt_ + (c < 2 ? 1 + c : 3 + (c - 2)));
+    }
+    tot[c] = (float)acc;
+  }
+  __syncthreads();
+  const float D1 = tot[0], D2 = tot[1];
+  for (int c = tid; c < DV; c += NT)
+    stf(out, bh * DV + c, (1.f + D2 / D1) * tot[2 + c] / D1 - tot[2 + DV + c] / D1);
+}
+
+// ------------------------------------------------------------------------------------ LLA
+// Partial of a chunk: [m, omega, sk[D], sv[DV], Skk[D][D], Svk[DV][D]].
+template <int D, int DV>
+constexpr int lla_part() { return 2 + D + DV + D * D + DV * D; }
+
+template <typename TIn, int D, int DV>
+__global__ void __launch_bounds__(NT)
+lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
+                  int L, int S, float inv_h, float lam, float* __restrict__ part,
+                  int* __restrict__ counter, TIn* __restrict__ out, int* __restrict__ status) {
+  constexpr int P = lla_part<D, DV>();
+  constexpr int NB = (D / 4) * (D / 4 + DV / 4);  // 4 x 4 tiles of Skk (first) and Svk
+  constexpr int TPB = (NB + NT - 1) / NT;          // tiles per thread
+  extern __shared__ float dsm[];
+  __shared__ float qs[D], red[NT / 32];
+  __shared__ int is_last, fail_s;
+  float* kt = dsm;               // [TK][D]
+  float* pk = kt + TK * D;       // [TK][D]: p_j k_j
+  float* pv = pk + TK * D;       // [TK][DV]: p_j v_j
+  float* pw = pv + TK * DV;      // [TK]: p_j
+  const long long bh = blockIdx.x / S;
+  const int s = blockIdx.x % S, tid = threadIdx.x;
+  const int chunk = (L + S - 1) / S;
+  const int j0 = s * chunk, j1 = min(L, j0 + chunk);
+  for (int a = tid; a < D; a += NT) qs[a] = ld(q, bh * D + a);
+  __syncthreads();
+  const TIn* kb = k + bh * (long long)L * D;
+  const TIn* vb = v + bh * (long long)L * DV;
+  float mx = -INFINITY;
+  for (int j = j0 + tid; j < j1; j += NT) {
+    float sj = 0.f;
+    for (int a = 0; a < D; ++a) sj = fmaf(qs[a], ld(kb, (long long)j * D + a), sj);
+    mx = fmaxf(mx, sj);
+  }
+  const float m = block_max(mx, red);
+  float acc[TPB][16];
+#pragma unroll
+  for (int u = 0; u < TPB; ++u)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[u][e] = 0.f;
+  float sk = 0.f, sv = 0.f, om = 0.f;  // thread a < D: sk[a]; D <= thread < D + DV: sv[a - D]
+  for (int t0 = j0; t0 < j1; t0 += TK) {
+    const int n = min(TK, j1 - t0);
+    __syncthreads();
+    for (int e = tid; e < TK * D; e += NT) {
+      const int jj = e / D;
+      kt[e] = jj < n ? ld(kb, (long long)(t0 + jj) * D + e % D) : 0.f;
+    }
+    for (int e = tid; e < TK * DV; e += NT) {
+      const int jj = e / DV;
+      pv[e] = jj < n ? ld(vb, (long long)(t0 + jj) * DV + e % DV) : 0.f;
+    }
+    __syncthreads();
+    if (tid < TK) {
+      float sj = 0.f;
+      for (int a = 0; a < D; ++a) sj = fmaf(qs[a], kt[tid * D + a], sj);
+      pw[tid] = tid < n ? __expf((sj - m) * inv_h) : 0.f;
+    }
+    __syncthreads();
+    for (int e = tid; e < TK * D; e += NT) pk[e] = pw[e / D] * kt[e];
+    for (int e = tid; e < TK * DV; e += NT) pv[e] *= pw[e / DV];
+    __syncthreads();
+    if (tid < D) for (int jj = 0; jj < n; ++jj) sk += pk[jj * D + tid];
+    else if (tid < D + DV) for (int jj = 0; jj < n; ++jj) sv += pv[jj * DV + tid - D];
+    else if (tid == D + DV) for (int jj = 0; jj < n; ++jj) om += pw[jj];
+#pragma unroll
+    for (int u = 0; u < TPB; ++u) {
+      const int b = tid + u * NT;
+      if (b < NB) {
+        // tile b: rows a0..a0+3 of x (p k for Skk, p v for Svk), columns c0..c0+3 of k
+        const bool kk = b < (D / 4) * (D / 4);
+        const int bb = kk ? b : b - (D / 4) * (D / 4);
+        const int a0 = (bb / (D / 4)) * 4, c0 = (bb % (D / 4)) * 4;
+        const float* x = kk ? pk : pv;
+        const int xs = kk ? D : DV;
+        for (int jj = 0; jj < n; ++jj) {
+          const float4 xa = *reinterpret_cast<const float4*>(x + jj * xs + a0);
+          const float4 kc = *reinterpret_cast<const float4*>(kt + jj * D + c0);
+          const float xr[4] = {xa.x, xa.y, xa.z, xa.w}, kr[4] = {kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[u][i * 4 + c] = fmaf(xr[i], kr[c], acc[u][i * 4 + c]);
+        }
+      }
+    }
+  }
+  float* pp = part + blockIdx.x * (long long)P;
+  if (tid == 0) pp[0] = m;
+  if (tid < D) pp[2 + tid] = sk;
+  else if (tid < D + DV) pp[2 + D + tid - D] = sv;
+  else if (tid == D + DV) pp[1] = om;
+#pragma unroll
+  for (int u = 0; u < TPB; ++u) {
+    const int b = tid + u * NT;
+    if (b < NB) {
+      const bool kk = b < (D / 4) * (D / 4);
+      const int bb = kk ? b : b - (D / 4) * (D / 4);
+      const int a0 = (bb / (D / 4)) * 4, c0 = (bb % (D / 4)) * 4;
+      float* dst = pp + 2 + D + DV + (kk ? 0 : D * D);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[(a0 + i) * D + c0 + c] = acc[u][i * 4 + c];
+    }
+  }
+  if (!last_arrival(counter + bh, S, &is_last)) return;
+
+  // ---- merge, centre and solve (the last CTA of the head), in double precision
+  double* mom = reinterpret_cast<double*>(dsm);  // [P - 1]: omega, sk, sv, Skk, Svk (merged)
+  const float* hp = part + bh * S * (long long)P;
+  float M = -INFINITY;
+  for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * (long long)P));
+  for (int e = tid; e < P - 1; e += NT) {
+    double accd = 0.0;
+    for (int t = 0; t < S; ++t) {
+      const float mt = __ldcg(hp + t * (long long)P);
+      const double al = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
+      accd += al * (double)__ldcg(hp + t * (long long)P + 1 + e);
+    }
+    mom[e] = accd;
+  }
+  __syncthreads();
+  const double omega = mom[0];
+  const double* msk = mom + 1;
+  const double* msv = msk + D;
+  double* A = mom + 1 + D + DV;          // Skk -> C_kk + lambda' I -> its Cholesky factor
+  const double* Svk = A + D * D;
+  double* z = reinterpret_cast<double*>(dsm) + P;  // [D]: q - kbar, then y
+  const double lp = (double)lam * exp(-(double)M * inv_h);  // ridge scaled by exp(-M/h)
+  for (int e = tid; e < D * D; e += NT) {
+    const int a = e / D, b = e % D;
+    A[e] = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
+  }
+  for (int a = tid; a < D; a += NT) z[a] = (double)qs[a] - msk[a] / omega;
+  __syncthreads();
+  // Cholesky A = L L^T (lower triangle in place), column by column
+  if (tid == 0) fail_s = 0;
+  for (int c = 0; c < D; ++c) {
+    if (tid == 0) {
+      const double piv = A[c * D + c];
+      if (!(piv > 0.0)) fail_s = 1;
+      A[c * D + c] = sqrt(piv > 0.0 ? piv : 1.0);
+    }
+    __syncthreads();
+    for (int i = c + 1 + tid; i < D; i += NT) A[i * D + c] /= A[c * D + c];
+    __syncthreads();
+    for (int e = tid; e < D * D; e += NT) {
+      const int i = e / D, j = e % D;
+      if (j > c && i >= j) A[i * D + j] -= A[i * D + c] * A[j * D + c];
+    }
+    __syncthreads();
+  }
+  // L w = z, then L^T y = w (one thread: D is at most 64)
+  if (tid == 0) {
+    for (int i = 0; i < D; ++i) {
+      double t = z[i];
+      for (int j = 0; j < i; ++j) t -= A[i * D + j] * z[j];
+      z[i] = t / A[i * D + i];
+    }
+    for (int i = D - 1; i >= 0; --i) {
+      double t = z[i];
+      for (int j = i + 1; j < D; ++j) t -= A[j * D + i] * z[j];
+      z[i] = t / A[i * D + i];
+    }
+  }
+  __syncthreads();
+  // o = vbar + C_vk y,  C_vk = Svk - sv sk^T / omega
+  const bool bad = fail_s != 0;
+  for (int c = tid; c < DV; c += NT) {
+    double o = msv[c] / omega;
+    for (int b = 0; b < D; ++b) o += (Svk[c * D + b] - msv[c] * msk[b] / omega) * z[b];
+    stf(out, bh * DV + c, bad ? __int_as_float(0x7fc00000) : (float)o);
+  }
+  if (tid == 0 && (bad || !(omega > 0.0))) atomicOr(status, kStatusNumerical);
+}
+
+int choose_splits(long long BH, int L) {
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long s = (2ll * sms + BH - 1) / BH;  // about two CTAs per SM
+  const long long smax = (L + TK - 1) / TK;  // at least a tile of keys per CTA
+  if (s > smax) s = smax;
+  if (s > 512) s = 512;
+  return s < 1 ? 1 : (int)s;
+}
+
+template <typename TIn, int D, int DV>
+cudaError_t launch_px(const DecodeArgs& a, void* ws, cudaStream_t st) {
+  const int S = choose_splits(a.BH(), a.L);
+  float* part = static_cast<float*>(ws);
+  int* cnt = reinterpret_cast<int*>(part + a.BH() * S * px_part<D, DV>());
+  zero_counters<<<(unsigned)((a.BH() + 255) / 256), 256, 0, st>>>(cnt, (int)a.BH());
+  count_launch();
+  parallax_decode_kernel<TIn, D, DV><<<(unsigned)(a.BH() * S), NT, 0, st>>>(
+      static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
+      static_cast<const TIn*>(a.r), a.L, S, 1.f / a.h, part, cnt, static_cast<TIn*>(a.out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename TIn, int D, int DV>
+cudaError_t launch_ll(const DecodeArgs& a, void* ws, int* status, cudaStream_t st) {
+  const int S = choose_splits(a.BH(), a.L);
+  float* part = static_cast<float*>(ws);
+  int* cnt = reinterpret_cast<int*>(part + a.BH() * S * lla_part<D, DV>());
+  constexpr int P = lla_part<D, DV>();
+  const size_t tiles = sizeof(float) * (TK * D * 2 + TK * DV + TK);
+  const size_t solve = sizeof(double) * (P + D);
+  const size_t smem = tiles > solve ? tiles : solve;
+  auto kern = lla_decode_kernel<TIn, D, DV>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  zero_counters<<<(unsigned)((a.BH() + 255) / 256), 256, 0, st>>>(cnt, (int)a.BH());
+  count_launch();
+  kern<<<(unsigned)(a.BH() * S), NT, smem, st>>>(
+      static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
+      a.L, S, 1.f / a.h, a.lam, part, cnt, static_cast<TIn*>(a.out), status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t dispatch(const DecodeArgs& a, void* ws, int* status, cudaStream_t st) {
+#define LLA_DEC(DD, VV)                                                                  \
+  if (a.d == DD && a.dv == VV)                                                           \
+    return a.r ? launch_px<TIn, DD, VV>(a, ws, st) : launch_ll<TIn, DD, VV>(a, ws, status, st);
+  LLA_DEC(16, 16) LLA_DEC(16, 32) LLA_DEC(16, 64)
+  LLA_DEC(32, 16) LLA_DEC(32, 32) LLA_DEC(32, 64)
+  LLA_DEC(64, 16) LLA_DEC(64, 32) LLA_DEC(64, 64)
+#undef LLA_DEC
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(const DecodeArgs& a) {
+  const int S = choose_splits(a.BH(), a.L);
+  const size_t per = a.r ? (size_t)(3 + 2 * a.dv) : (size_t)(2 + a.d + a.dv + a.d * a.d + a.dv * a.d);
+  return sizeof(float) * per * (size_t)a.BH() * S + sizeof(int) * (size_t)a.BH() + 256;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, void* ws, int* status, cudaStream_t st) {
+  return a.dtype == LLA_F32 ? dispatch<float>(a, ws, status, st)
+                            : dispatch<__nv_bfloat16>(a, ws, status, st);
+}
+
+}  // namespace lla

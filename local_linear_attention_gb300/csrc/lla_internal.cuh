@@ -127,6 +127,22 @@ cudaError_t launch_debug_moments(const Args& a, const int64_t* idx, int n, float
                                  float* omega, float* sk, float* sv, float* Skk, float* Svk,
                                  int* status, cudaStream_t s);
 
+// Decode: one query per head against a cache of L keys/values (q, r: [B,H,d]; k: [B,H,L,d];
+// v: [B,H,L,dv]; out: [B,H,dv]). r == nullptr: LLA; otherwise Parallax with probe r.
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* r;
+  void* out;
+  int B, H, L, d, dv;
+  float h, lam;
+  int dtype;
+  long long BH() const { return (long long)B * H; }
+};
+size_t decode_workspace_bytes(const DecodeArgs& a);
+cudaError_t launch_decode(const DecodeArgs& a, void* ws, int* status, cudaStream_t s);
+
 void count_launch();
 
 // ---------------------------------------------------------------------------------------------
