@@ -416,14 +416,151 @@ def run_parallax(args, w, cpu, world, rank):
     return 0
 
 
+METRIC_DECODE = "LLA decode queries/sec (one query per head against a KV cache) on 1 GB300"
+METRIC_PX_DECODE = "Parallax decode queries/sec (one query per head against a KV cache) on 1 GB300"
+
+
+def run_decode(args, world, rank):
+    """One step = one lla_decode / lla_parallax_decode call: every head's query against its
+    cache (split-KV partials and the in-kernel last-arriver merge)."""
+    import torch
+    import torch.distributed as dist
+    from local_linear_attention_gb300 import binding as lla
+
+    B, H, L, d, dv, dt = args.decode_shape.split(",")
+    B, H, L, d, dv = int(B), int(H), int(L), int(d), int(dv)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    px = args.op == "parallax_decode"
+    h, lam = math.sqrt(d), 1e-2
+    g = torch.Generator().manual_seed(6)
+    q = torch.randn(B, H, d, generator=g).to(tdt)
+    k = torch.randn(B, H, L, d, generator=g).to(tdt)
+    v = torch.randn(B, H, L, dv, generator=g).to(tdt)
+    r = (torch.randn(B, H, d, generator=g) / math.sqrt(d)).to(tdt)
+    dq, dk, dv_, dr = q.cuda(), k.cuda(), v.cuda(), r.cuda()
+    out = torch.empty(B, H, dv, dtype=tdt, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if px:
+            lla.lla_parallax_decode(dq, dk, dv_, dr, h, out=out, stream=stream)
+        else:
+            lla.lla_decode(dq, dk, dv_, h, lam, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = lla.launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    n_launch = lla.launch_count() - n_launch0
+    clk = clocks.stop()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during the timed steps")
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    queries = B * H
+    value = queries * world / (ms_per_step / 1e3)
+    eb = q.element_size()
+
+    e2e = None
+    if not args.no_e2e:  # pinned host inputs -> device, decode, result -> pinned host, per step
+        hq, hk, hv, hr = (t.pin_memory() for t in (q, k, v, r))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            for hst, dst in ((hq, dq), (hk, dk), (hv, dv_)) + (((hr, dr),) if px else ()):
+                dst.copy_(hst, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        e2e = {"value": queries * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": (q.numel() * (2 if px else 1) + k.numel() + v.numel()) * eb,
+               "d2h_bytes_per_step": out.numel() * eb}
+
+    peaks, peak_src = load_peaks()
+    kv_bytes = B * H * L * (d + dv) * eb  # the cache, read once
+    gbs = kv_bytes / (ms_per_step / 1e3) / 1e9
+    if px:
+        peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+        roof = {"kernel": "parallax_decode_kernel (lla_decode.cu)", "bound": "hbm",
+                "peak_source": f"HBM copy ({peak_src})", "achieved": gbs, "peak": peak,
+                "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                "note": "achieved = the K and V cache bytes (read once) per call / call time"}
+    else:
+        # algorithmic per key: the logit q.k and the moments omega, sum p k, sum p v, the upper
+        # triangle of sum p k k^T and sum p v k^T
+        flops = B * H * L * (2 * d + 2 * (1 + d + dv + d * (d + 1) // 2 + dv * d))
+        achieved = flops / (ms_per_step / 1e3) / 1e12
+        peak = fp32_alu_peak_tflops(peaks)
+        roof = {"kernel": "lla_decode_kernel (lla_decode.cu)", "bound": "alu",
+                "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "cache_gbs": gbs}
+    if rank == 0:
+        line = {
+            "metric": METRIC_PX_DECODE if px else METRIC_DECODE, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dt, "data": "synthetic",
+            "config": {"workload": f"decode: B{B} H{H} L{L} d{d} dv{dv} {dt}, i.i.d. N(0,1) "
+                                   f"q/k/v" + (", probe N(0,1/d)" if px else f", lambda={lam}")
+                                   + f", h={h:g}, seed 6",
+                       "B": B, "H": H, "L": L, "d": d, "dv": dv, "io_dtype": dt,
+                       "l2": "flushed between steps (256 MiB write outside the step events)",
+                       "parallelism": f"replica per GPU x{world}"},
+            "roofline": roof, "cpu_baseline": None, "e2e": e2e, "gpu_launches": n_launch,
+            "clocks": clk, "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
-    ap.add_argument("--op", choices=["lla", "parallax"], default="lla",
-                    help="the operation timed: the LLA forward (default) or the Parallax forward")
+    ap.add_argument("--op", choices=["lla", "parallax", "decode", "parallax_decode"],
+                    default="lla",
+                    help="the operation timed: the LLA forward (default), the Parallax forward, "
+                         "or LLA / Parallax decode (one query per head against a KV cache)")
+    ap.add_argument("--decode-shape", default="32,8,16384,64,64,bf16",
+                    help="B,H,L,d,dv,dtype of the decode workload")
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--strategy", choices=["dense", "cg"], default="dense",
                     help="ridge systems from dense tensor-core moments + Cholesky (default), or "
@@ -446,6 +583,12 @@ def main(argv=None):
         w = W.Workload("custom", int(B), int(H), int(T), d, int(dv), dt, 2, "iid",
                        h=math.sqrt(d), lam=1e-2)
         args.no_cpu_baseline = True
+    if args.op in ("decode", "parallax_decode"):
+        args.no_cpu_baseline = True  # the oracle leg times the prefill workloads
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle leg times the "
+                              "prefill forward; decode has no CPU reference line"}), flush=True)
+            return 0
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -471,6 +614,8 @@ def main(argv=None):
 
     if args.op == "parallax":
         return run_parallax(args, w, cpu, world, rank)
+    if args.op in ("decode", "parallax_decode"):
+        return run_decode(args, world, rank)
 
     lam, h = w.points[0]
     if args.strategy == "cg":

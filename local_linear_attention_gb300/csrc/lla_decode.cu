@@ -63,6 +63,83 @@ __global__ void zero_counters(int* c, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c[i] = 0;
 }
 
+// Stages rows [t0, t0 + n) of a [rows x W] matrix (row-major) as fp32 into `dst` ([TK][W]),
+// rows past n as zeros, with 16-byte loads (8 bf16 or 4 fp32 per load).
+template <typename TIn, int W>
+__device__ __forceinline__ void stage(float* dst, const TIn* src, int t0, int n) {
+  constexpr int EPL = 16 / (int)sizeof(TIn);  // elements per 16-byte load
+  constexpr int CPR = W / EPL;                // loads per row
+  for (int e = threadIdx.x; e < TK * CPR; e += NT) {
+    const int jj = e / CPR, c = e % CPR;
+    float* d = dst + jj * W + c * EPL;
+    if (jj < n) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + (long long)(t0 + jj) * W + c * EPL);
+      if constexpr (sizeof(TIn) == 2) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          d[2 * i] = __uint_as_float(w[i] << 16);
+          d[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      } else {
+        d[0] = __uint_as_float(u.x); d[1] = __uint_as_float(u.y);
+        d[2] = __uint_as_float(u.z); d[3] = __uint_as_float(u.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) d[i] = 0.f;
+    }
+  }
+}
+
+// The running maximum of one tile: threads 0..TK-1 hold the logits of the tile's keys (-inf
+// past its end); returns max(m_run, tile max) to every thread (two block barriers inside).
+__device__ __forceinline__ float tile_max(float sj, float m_run, float* red) {
+  float x = threadIdx.x < TK ? sj : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  if ((threadIdx.x & 31) == 0 && threadIdx.x < TK) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  float r = m_run;
+  for (int i = 0; i < TK / 32; ++i) r = fmaxf(r, red[i]);
+  __syncthreads();
+  return r;
+}
+
+// Logits q . k_j of the tile's keys (and, with a probe, r . k_j) into sS / sT (-inf past n):
+// one warp per key, the lanes splitting the D coordinates (conflict-free shared reads), then a
+// shuffle reduction.
+template <int D, bool PROBE>
+__device__ __forceinline__ void tile_logits(const float* kt, const float* qs, const float* rs,
+                                            int n, float* sS, float* sT) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int jj = warp; jj < TK; jj += NT / 32) {
+    float a = 0.f, b = 0.f;
+    if (jj < n) {
+#pragma unroll
+      for (int c = lane; c < D; c += 32) {
+        const float kv = kt[jj * D + c];
+        a = fmaf(qs[c], kv, a);
+        if (PROBE) b = fmaf(rs[c], kv, b);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (PROBE) b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if (lane == 0) {
+      sS[jj] = jj < n ? a : -INFINITY;
+      if (PROBE) sT[jj] = b;
+    }
+  }
+}
+
+// exp((m_old - m_new) / h): the factor that moves sums shifted by m_old to the shift m_new.
+__device__ __forceinline__ float rescale(float m_old, float m_new, float inv_h) {
+  return m_old == -INFINITY ? 0.f : __expf((m_old - m_new) * inv_h);
+}
+
 // ------------------------------------------------------------------------------------ Parallax
 // Partial of a chunk: [m, d1, d2, O1[DV], O2[DV]].
 template <int D, int DV>
@@ -76,8 +153,10 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                        TIn* __restrict__ out) {
   constexpr int NG = NT / (2 * DV);  // key groups: thread t takes O coordinate t % 2DV, group t / 2DV
   __shared__ float qs[D], rs[D], red[NT / 32];
-  __shared__ float kt[TK][D + 1], vt[TK][DV + 1], pt[TK], tt[TK];
+  __shared__ __align__(16) float kt[TK * D], vt[TK * DV];
+  __shared__ float pt[TK], tt[TK], sS[TK], sT[TK];
   __shared__ float og_s[NG][2 * DV], dsum[2][2], tot[2 * DV + 2];
+  __shared__ double alpha[512];
   __shared__ int is_last;
   const long long bh = blockIdx.x / S;
   const int s = blockIdx.x % S, tid = threadIdx.x;
@@ -87,38 +166,28 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     qs[a] = ld(q, bh * D + a);
     rs[a] = ld(r, bh * D + a);
   }
-  __syncthreads();
   const TIn* kb = k + bh * (long long)L * D;
   const TIn* vb = v + bh * (long long)L * DV;
-  // sweep 1: the chunk's maximum logit q . k_j
-  float mx = -INFINITY;
-  for (int j = j0 + tid; j < j1; j += NT) {
-    float sj = 0.f;
-    for (int a = 0; a < D; ++a) sj = fmaf(qs[a], ld(kb, (long long)j * D + a), sj);
-    mx = fmaxf(mx, sj);
-  }
-  const float m = block_max(mx, red);
-  // sweep 2: weights and the two branches
-  float acc0 = 0.f, d1 = 0.f, d2 = 0.f;
+  // One pass with a running maximum m: every sum is kept shifted by the current m and rescaled
+  // when a tile raises it.
+  float m = -INFINITY, acc0 = 0.f, d1 = 0.f, d2 = 0.f;
   const int oc = tid % (2 * DV), og = tid / (2 * DV);  // O1/O2 coordinate and key group
   for (int t0 = j0; t0 < j1; t0 += TK) {
     const int n = min(TK, j1 - t0);
     __syncthreads();
-    for (int e = tid; e < TK * D; e += NT) {
-      const int jj = e / D, a = e % D;
-      kt[jj][a] = jj < n ? ld(kb, (long long)(t0 + jj) * D + a) : 0.f;
-    }
-    for (int e = tid; e < TK * DV; e += NT) {
-      const int jj = e / DV, a = e % DV;
-      vt[jj][a] = jj < n ? ld(vb, (long long)(t0 + jj) * DV + a) : 0.f;
-    }
+    stage<TIn, D>(kt, kb, t0, n);
+    stage<TIn, DV>(vt, vb, t0, n);
     __syncthreads();
+    tile_logits<D, true>(kt, qs, rs, n, sS, sT);
+    __syncthreads();
+    const float sj = tid < TK ? sS[tid] : -INFINITY, tj = tid < TK ? sT[tid] : 0.f;
+    const float mn = tile_max(sj, m, red);
+    const float sc = rescale(m, mn, inv_h);
+    m = mn;
+    acc0 *= sc;
+    d1 *= sc;
+    d2 *= sc;
     if (tid < TK) {
-      float sj = 0.f, tj = 0.f;
-      for (int a = 0; a < D; ++a) {
-        sj = fmaf(qs[a], kt[tid][a], sj);
-        tj = fmaf(rs[a], kt[tid][a], tj);
-      }
       const float p = tid < n ? __expf((sj - m) * inv_h) : 0.f;
       pt[tid] = p;
       tt[tid] = p * tj;
@@ -126,11 +195,9 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       d2 += p * tj;
     }
     __syncthreads();
-    {
-      const int col = oc % DV;
-      const float* w = oc < DV ? pt : tt;
-      for (int jj = og; jj < n; jj += NG) acc0 = fmaf(w[jj], vt[jj][col], acc0);
-    }
+    const int col = oc % DV;
+    const float* w = oc < DV ? pt : tt;
+    for (int jj = og; jj < n; jj += NG) acc0 = fmaf(w[jj], vt[jj * DV + col], acc0);
   }
   // Reductions in a fixed order (no atomics), so that the result is reproducible.
   og_s[og][oc] = acc0;
@@ -150,19 +217,19 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     pp[3 + c] = t;
   }
   if (!last_arrival(counter + bh, S, &is_last)) return;
-  // merge (the last CTA of the head)
+  // merge (the last CTA of the head): every partial moved to the largest chunk maximum M
   const float* hp = part + bh * S * (long long)px_part<D, DV>();
   float M = -INFINITY;
   for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * px_part<D, DV>()));
+  for (int t = tid; t < S; t += NT) {
+    const float mt = __ldcg(hp + t * px_part<D, DV>());
+    alpha[t] = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
+  }
   __syncthreads();
   for (int c = tid; c < 2 * DV + 2; c += NT) {
     double acc = 0.0;
-    for (int t = 0; t < S; ++t) {
-      const float* pt_ = hp + t * px_part<D, DV>();
-      const float mt = __ldcg(pt_);
-      const double al = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
-      acc += al * (double)__ldcg(pt_ + (c < 2 ? 1 + c : 3 + (c - 2)));
-    }
+    for (int t = 0; t < S; ++t)
+      acc += alpha[t] * (double)__ldcg(hp + t * px_part<D, DV>() + 1 + c);
     tot[c] = (float)acc;
   }
   __syncthreads();
@@ -172,7 +239,7 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 }
 
 // ------------------------------------------------------------------------------------ LLA
-// Partial of a chunk: [m, omega, sk[D], sv[DV], Skk[D][D], Svk[DV][D]].
+// Partial of a chunk: [m, omega, sk[D], sv[DV], Skk[D][D] (upper 4 x 4 blocks), Svk[DV][D]].
 template <int D, int DV>
 constexpr int lla_part() { return 2 + D + DV + D * D + DV * D; }
 
@@ -182,53 +249,68 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
                   int L, int S, float inv_h, float lam, float* __restrict__ part,
                   int* __restrict__ counter, TIn* __restrict__ out, int* __restrict__ status) {
   constexpr int P = lla_part<D, DV>();
-  constexpr int NB = (D / 4) * (D / 4 + DV / 4);  // 4 x 4 tiles of Skk (first) and Svk
-  constexpr int TPB = (NB + NT - 1) / NT;          // tiles per thread
+  constexpr int NBK = (D / 4) * (D / 4 + 1) / 2;   // upper-triangle 4 x 4 blocks of Skk
+  constexpr int NB = NBK + (DV / 4) * (D / 4);      // then the blocks of Svk
+  constexpr int TPB = (NB + NT - 1) / NT;           // blocks per thread
   extern __shared__ float dsm[];
-  __shared__ float qs[D], red[NT / 32];
+  __shared__ float qs[D], red[NT / 32], sS[TK];
   __shared__ int is_last, fail_s;
   float* kt = dsm;               // [TK][D]
   float* pk = kt + TK * D;       // [TK][D]: p_j k_j
-  float* pv = pk + TK * D;       // [TK][DV]: p_j v_j
+  float* pv = pk + TK * D;       // [TK][DV]: v_j, then p_j v_j
   float* pw = pv + TK * DV;      // [TK]: p_j
   const long long bh = blockIdx.x / S;
   const int s = blockIdx.x % S, tid = threadIdx.x;
   const int chunk = (L + S - 1) / S;
   const int j0 = s * chunk, j1 = min(L, j0 + chunk);
   for (int a = tid; a < D; a += NT) qs[a] = ld(q, bh * D + a);
-  __syncthreads();
   const TIn* kb = k + bh * (long long)L * D;
   const TIn* vb = v + bh * (long long)L * DV;
-  float mx = -INFINITY;
-  for (int j = j0 + tid; j < j1; j += NT) {
-    float sj = 0.f;
-    for (int a = 0; a < D; ++a) sj = fmaf(qs[a], ld(kb, (long long)j * D + a), sj);
-    mx = fmaxf(mx, sj);
+  // This thread's blocks: row block ar and column block cr (Skk: ar <= cr; Svk: rows of V).
+  int ar[TPB], cr[TPB];
+#pragma unroll
+  for (int u = 0; u < TPB; ++u) {
+    int b = tid + u * NT;
+    ar[u] = -1;
+    cr[u] = 0;
+    if (b < NBK) {
+      int row = 0;
+      while (b >= D / 4 - row) { b -= D / 4 - row; ++row; }
+      ar[u] = row;
+      cr[u] = row + b;
+    } else if (b < NB) {
+      b -= NBK;
+      ar[u] = D / 4 + b / (D / 4);  // >= D/4 marks a Svk block (its V row block is ar - D/4)
+      cr[u] = b % (D / 4);
+    }
   }
-  const float m = block_max(mx, red);
-  float acc[TPB][16];
+  float2 acc[TPB][8];  // 4 rows x 2 column pairs per block
 #pragma unroll
   for (int u = 0; u < TPB; ++u)
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[u][e] = 0.f;
-  float sk = 0.f, sv = 0.f, om = 0.f;  // thread a < D: sk[a]; D <= thread < D + DV: sv[a - D]
+    for (int e = 0; e < 8; ++e) acc[u][e] = make_float2(0.f, 0.f);
+  float m = -INFINITY, sk = 0.f, sv = 0.f, om = 0.f;  // thread a < D: sk[a]; then sv, omega
   for (int t0 = j0; t0 < j1; t0 += TK) {
     const int n = min(TK, j1 - t0);
     __syncthreads();
-    for (int e = tid; e < TK * D; e += NT) {
-      const int jj = e / D;
-      kt[e] = jj < n ? ld(kb, (long long)(t0 + jj) * D + e % D) : 0.f;
-    }
-    for (int e = tid; e < TK * DV; e += NT) {
-      const int jj = e / DV;
-      pv[e] = jj < n ? ld(vb, (long long)(t0 + jj) * DV + e % DV) : 0.f;
-    }
+    stage<TIn, D>(kt, kb, t0, n);
+    stage<TIn, DV>(pv, vb, t0, n);
     __syncthreads();
-    if (tid < TK) {
-      float sj = 0.f;
-      for (int a = 0; a < D; ++a) sj = fmaf(qs[a], kt[tid * D + a], sj);
-      pw[tid] = tid < n ? __expf((sj - m) * inv_h) : 0.f;
-    }
+    tile_logits<D, false>(kt, qs, nullptr, n, sS, nullptr);
+    __syncthreads();
+    const float sj = tid < TK ? sS[tid] : -INFINITY;
+    const float mn = tile_max(sj, m, red);
+    const float sc = rescale(m, mn, inv_h);
+    m = mn;
+    sk *= sc;
+    sv *= sc;
+    om *= sc;
+    const float2 sc2 = make_float2(sc, sc);
+#pragma unroll
+    for (int u = 0; u < TPB; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[u][e] = __fmul2_rn(acc[u][e], sc2);
+    if (tid < TK) pw[tid] = tid < n ? __expf((sj - m) * inv_h) : 0.f;
     __syncthreads();
     for (int e = tid; e < TK * D; e += NT) pk[e] = pw[e / D] * kt[e];
     for (int e = tid; e < TK * DV; e += NT) pv[e] *= pw[e / DV];
@@ -238,22 +320,22 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
     else if (tid == D + DV) for (int jj = 0; jj < n; ++jj) om += pw[jj];
 #pragma unroll
     for (int u = 0; u < TPB; ++u) {
-      const int b = tid + u * NT;
-      if (b < NB) {
-        // tile b: rows a0..a0+3 of x (p k for Skk, p v for Svk), columns c0..c0+3 of k
-        const bool kk = b < (D / 4) * (D / 4);
-        const int bb = kk ? b : b - (D / 4) * (D / 4);
-        const int a0 = (bb / (D / 4)) * 4, c0 = (bb % (D / 4)) * 4;
-        const float* x = kk ? pk : pv;
+      if (ar[u] >= 0) {
+        const bool kk = ar[u] < D / 4;
+        const float* x = kk ? pk + ar[u] * 4 : pv + (ar[u] - D / 4) * 4;
         const int xs = kk ? D : DV;
+        const float* kc = kt + cr[u] * 4;
         for (int jj = 0; jj < n; ++jj) {
-          const float4 xa = *reinterpret_cast<const float4*>(x + jj * xs + a0);
-          const float4 kc = *reinterpret_cast<const float4*>(kt + jj * D + c0);
-          const float xr[4] = {xa.x, xa.y, xa.z, xa.w}, kr[4] = {kc.x, kc.y, kc.z, kc.w};
+          const float4 xa = *reinterpret_cast<const float4*>(x + jj * xs);
+          const float4 kv4 = *reinterpret_cast<const float4*>(kc + jj * D);
+          const float2 k01 = make_float2(kv4.x, kv4.y), k23 = make_float2(kv4.z, kv4.w);
+          const float xr[4] = {xa.x, xa.y, xa.z, xa.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[u][i * 4 + c] = fmaf(xr[i], kr[c], acc[u][i * 4 + c]);
+          for (int i = 0; i < 4; ++i) {
+            const float2 xi = make_float2(xr[i], xr[i]);
+            acc[u][2 * i] = __ffma2_rn(xi, k01, acc[u][2 * i]);
+            acc[u][2 * i + 1] = __ffma2_rn(xi, k23, acc[u][2 * i + 1]);
+          }
         }
       }
     }
@@ -265,50 +347,59 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
   else if (tid == D + DV) pp[1] = om;
 #pragma unroll
   for (int u = 0; u < TPB; ++u) {
-    const int b = tid + u * NT;
-    if (b < NB) {
-      const bool kk = b < (D / 4) * (D / 4);
-      const int bb = kk ? b : b - (D / 4) * (D / 4);
-      const int a0 = (bb / (D / 4)) * 4, c0 = (bb % (D / 4)) * 4;
-      float* dst = pp + 2 + D + DV + (kk ? 0 : D * D);
+    if (ar[u] >= 0) {
+      const bool kk = ar[u] < D / 4;
+      float* dst = pp + 2 + D + DV + (kk ? ar[u] * 4 * D : D * D + (ar[u] - D / 4) * 4 * D) + cr[u] * 4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dst[(a0 + i) * D + c0 + c] = acc[u][i * 4 + c];
+      for (int i = 0; i < 4; ++i) {
+        dst[i * D] = acc[u][2 * i].x;
+        dst[i * D + 1] = acc[u][2 * i].y;
+        dst[i * D + 2] = acc[u][2 * i + 1].x;
+        dst[i * D + 3] = acc[u][2 * i + 1].y;
+      }
     }
   }
   if (!last_arrival(counter + bh, S, &is_last)) return;
 
   // ---- merge, centre and solve (the last CTA of the head), in double precision
   double* mom = reinterpret_cast<double*>(dsm);  // [P - 1]: omega, sk, sv, Skk, Svk (merged)
+  double* z = mom + P;                           // [D]: q - kbar, then y
+  double* alpha = z + D;                         // [S]
   const float* hp = part + bh * S * (long long)P;
   float M = -INFINITY;
   for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * (long long)P));
+  for (int t = tid; t < S; t += NT) {
+    const float mt = __ldcg(hp + t * (long long)P);
+    alpha[t] = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
+  }
+  __syncthreads();
+  constexpr int SKK0 = 1 + D + DV;  // offset of Skk in mom (mom[e] is partial entry 1 + e)
   for (int e = tid; e < P - 1; e += NT) {
+    const bool lower = e >= SKK0 && e < SKK0 + D * D && (e - SKK0) / D > (e - SKK0) % D;
     double accd = 0.0;
-    for (int t = 0; t < S; ++t) {
-      const float mt = __ldcg(hp + t * (long long)P);
-      const double al = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
-      accd += al * (double)__ldcg(hp + t * (long long)P + 1 + e);
-    }
+    if (!lower)
+      for (int t = 0; t < S; ++t) accd += alpha[t] * (double)__ldcg(hp + t * (long long)P + 1 + e);
     mom[e] = accd;
   }
   __syncthreads();
   const double omega = mom[0];
   const double* msk = mom + 1;
   const double* msv = msk + D;
-  double* A = mom + 1 + D + DV;          // Skk -> C_kk + lambda' I -> its Cholesky factor
+  double* A = mom + SKK0;                // Skk (upper) -> C_kk + lambda' I -> its Cholesky factor
   const double* Svk = A + D * D;
-  double* z = reinterpret_cast<double*>(dsm) + P;  // [D]: q - kbar, then y
   const double lp = (double)lam * exp(-(double)M * inv_h);  // ridge scaled by exp(-M/h)
   for (int e = tid; e < D * D; e += NT) {
     const int a = e / D, b = e % D;
-    A[e] = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
+    if (a <= b) {
+      const double c = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
+      A[e] = c;
+      A[b * D + a] = c;
+    }
   }
   for (int a = tid; a < D; a += NT) z[a] = (double)qs[a] - msk[a] / omega;
+  if (tid == 0) fail_s = 0;
   __syncthreads();
   // Cholesky A = L L^T (lower triangle in place), column by column
-  if (tid == 0) fail_s = 0;
   for (int c = 0; c < D; ++c) {
     if (tid == 0) {
       const double piv = A[c * D + c];
@@ -324,17 +415,21 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
     }
     __syncthreads();
   }
-  // L w = z, then L^T y = w (one thread: D is at most 64)
-  if (tid == 0) {
+  // L w = z, then L^T y = w, by warp 0 (dot products across its lanes)
+  if (tid < 32) {
     for (int i = 0; i < D; ++i) {
-      double t = z[i];
-      for (int j = 0; j < i; ++j) t -= A[i * D + j] * z[j];
-      z[i] = t / A[i * D + i];
+      double t = 0.0;
+      for (int j = tid; j < i; j += 32) t += A[i * D + j] * z[j];
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
+      __syncwarp();
     }
     for (int i = D - 1; i >= 0; --i) {
-      double t = z[i];
-      for (int j = i + 1; j < D; ++j) t -= A[j * D + i] * z[j];
-      z[i] = t / A[i * D + i];
+      double t = 0.0;
+      for (int j = i + 1 + tid; j < D; j += 32) t += A[j * D + i] * z[j];
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -380,7 +475,7 @@ cudaError_t launch_ll(const DecodeArgs& a, void* ws, int* status, cudaStream_t s
   int* cnt = reinterpret_cast<int*>(part + a.BH() * S * lla_part<D, DV>());
   constexpr int P = lla_part<D, DV>();
   const size_t tiles = sizeof(float) * (TK * D * 2 + TK * DV + TK);
-  const size_t solve = sizeof(double) * (P + D);
+  const size_t solve = sizeof(double) * (P + D + S);
   const size_t smem = tiles > solve ? tiles : solve;
   auto kern = lla_decode_kernel<TIn, D, DV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
