@@ -565,6 +565,9 @@ def main(argv=None):
     ap.add_argument("--strategy", choices=["dense", "cg"], default="dense",
                     help="ridge systems from dense tensor-core moments + Cholesky (default), or "
                          "matrix-free conjugate gradients (bf16 d = dv = 64 only)")
+    ap.add_argument("--form", choices=["centred", "page"], default="centred",
+                    help="closed form of the intercept: centred (default) or the page form with "
+                         "the exact-LLA two-branch epilogue (dense strategy, bf16 d = dv = 64)")
     ap.add_argument("--cg-iters", type=int, default=1024)
     ap.add_argument("--cg-tol", type=float, default=1e-3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -621,6 +624,8 @@ def main(argv=None):
     if args.strategy == "cg":
         lla.lla_set_moments_path(lla.PATH_CG)
         lla.lla_set_cg(args.cg_iters, args.cg_tol)
+    if args.form == "page":
+        lla.lla_set_form(lla.FORM_PAGE)
     q, k, v = W.make_inputs(w)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=dq.dtype, device="cuda")
@@ -731,7 +736,9 @@ def main(argv=None):
                        "parallelism": f"replica per GPU x{world}",
                        "strategy": (f"cg (max {args.cg_iters} passes, rel. residual "
                                     f"{args.cg_tol:g})" if args.strategy == "cg"
-                                    else "dense moments + Cholesky")},
+                                    else "dense moments + Cholesky"),
+                       "form": ("page form, exact-LLA epilogue (O1 - O2) / (d1 - d2)"
+                                if args.form == "page" else "centred")},
             "tflops": step_tflops,
             "bf16_peak_fraction": step_tflops / float(peaks.get("bf16_tflops", 1900.0)),
             "roofline": roof,

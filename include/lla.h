@@ -228,6 +228,22 @@ int lla_set_moments_path(int path);
  */
 int lla_set_cg(int max_iters, float rel_tol);
 
+/*
+ * Which exact closed form of the LLA intercept later lla_forward / lla_forward_ws calls by this
+ * process evaluate ("Parallax" blog, s.2 Canonical Formulation and Appendix B; both equal the
+ * intercept of the weighted ridge regression):
+ *   0 (default) the centred form  o = vbar + C_vk y,  (C_kk + lambda' I) y = q - kbar;
+ *   1 the page form  o = sum w (1 - z.rho*) v / sum w (1 - z.rho*),  z = k - q,
+ *     (sum w z z^T + lambda' I) rho* = sum w z, which the readout evaluates as the exact-LLA
+ *     two-branch epilogue (O1 - O2) / (d1 - d2).
+ * Form 1 runs on the tensor-core dense strategy only (bf16, d = dv = 64, moments path 0 or 2);
+ * a call that would take another path returns LLA_ERR_UNSUPPORTED while it is set. Its system
+ * carries the rank-one term w (kbar - q)(kbar - q)^T on top of the centred one, so it is worse
+ * conditioned for queries far from the weighted key mean. Returns LLA_ERR_INVALID_ARG for any
+ * other value. Host-only.
+ */
+int lla_set_form(int form);
+
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 unsigned long long lla_launch_count(void);
 

@@ -17,7 +17,7 @@ __all__ = [
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
     "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
     "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "PATH_CG", "lla_set_cg", "lla_parallax_forward",
-    "lla_decode", "lla_parallax_decode",
+    "lla_decode", "lla_parallax_decode", "lla_set_form", "FORM_CENTRED", "FORM_PAGE",
 ]
 
 LLA_OK = 0
@@ -30,7 +30,7 @@ EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
     "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg", "lla_decode", "lla_parallax_decode",
-    "lla_parallax_forward",
+    "lla_parallax_forward", "lla_set_form",
 )
 
 # LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
@@ -76,6 +76,7 @@ def _load():
         "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_set_moments_path": (i, [i]),
         "lla_set_cg": (i, [i, ctypes.c_float]),
+        "lla_set_form": (i, [i]),
         "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "lla_decode": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_parallax_decode": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
@@ -107,6 +108,15 @@ def lla_set_moments_path(path: int):
 def lla_set_cg(max_iters: int, rel_tol: float):
     """Iteration cap and relative residual tolerance of the conjugate-gradient strategy."""
     _check(_load().lla_set_cg(int(max_iters), float(rel_tol)), "lla_set_cg")
+
+
+FORM_CENTRED, FORM_PAGE = 0, 1
+
+
+def lla_set_form(form: int):
+    """Closed form the forward evaluates: 0 the centred form (default), 1 the page form with the
+    exact-LLA two-branch epilogue (tensor-core dense strategy, bf16 d = dv = 64 only)."""
+    _check(_load().lla_set_form(int(form)), "lla_set_form")
 
 
 def launch_count() -> int:

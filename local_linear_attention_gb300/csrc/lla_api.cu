@@ -19,6 +19,7 @@ std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_path_request{0};  // 0 auto, kPathCudaCore, kPathTensorCore, kPathCG
 std::atomic<int> g_cg_max_iters{1024};
 std::atomic<float> g_cg_rel_tol{1e-3f};
+std::atomic<int> g_form{0};  // kFormCentred or kFormPage
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -102,6 +103,7 @@ size_t elem_bytes(int dtype) { return dtype == LLA_F32 ? 4 : 2; }
 int run_forward(const Args& a, void* base, cudaStream_t s) {
   Workspace ws;
   carve_workspace(a, base, &ws);
+  if (ws.form == kFormPage && !(ws.path == kPathTensorCore && a.dv == 64)) return LLA_ERR_UNSUPPORTED;
   if (device_status(&ws.status) != cudaSuccess) return LLA_ERR_CUDA;
   ProfRec rec;
   bool prof = false;
@@ -188,6 +190,7 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->pscr = tc ? take(moments_tc_pscratch_bytes(a.BH(), a.T)) : nullptr;
   ws->status = nullptr;
   ws->path = choose_path(a);
+  ws->form = g_form.load();
 }
 
 }  // namespace lla
@@ -376,6 +379,12 @@ int lla_set_cg(int max_iters, float rel_tol) {
     return LLA_ERR_INVALID_ARG;
   g_cg_max_iters.store(max_iters);
   g_cg_rel_tol.store(rel_tol);
+  return LLA_OK;
+}
+
+int lla_set_form(int form) {
+  if (form != kFormCentred && form != kFormPage) return LLA_ERR_INVALID_ARG;
+  g_form.store(form);
   return LLA_OK;
 }
 

@@ -59,12 +59,17 @@ struct Workspace {
                   // image per (head, query tile, key block), reused by the later passes
   int* status;    // device status word of the current device
   int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
+  int form;       // kFormCentred or kFormPage: which closed form the solve and readout evaluate
 };
 
 // Moments implementations. The tensor-core stage handles bf16 inputs with d = 64 and leaves the
 // keys unshifted (c = 0: shifted bf16 keys would no longer multiply exactly); everything else
 // uses the CUDA-core stage.
 enum : int { kPathCudaCore = 1, kPathTensorCore = 2, kPathCG = 3 };
+// Closed forms of the intercept (both exact): the centred one, o = vbar + C_vk y, and the page's,
+// o = sum p (1 - z . rho*) v / sum p (1 - z . rho*) with z = k - q. The page form runs on the
+// tensor-core dense strategy with d = dv = 64 only.
+enum : int { kFormCentred = 0, kFormPage = 1 };
 int choose_path(const Args& a);
 
 size_t workspace_bytes(const Args& a);

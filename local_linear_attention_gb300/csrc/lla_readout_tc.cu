@@ -18,6 +18,11 @@
 // writes them, with cy = kbar . y), and the covariance-branch weights p * t enter P2 V as an
 // exact-to-16-bits hi/lo pair.
 //
+// With the page form of the solve (y := rho* = Sigma^-1 mu, cy := q . rho*; kPage), t_ij is the
+// page's z_ij . rho* with z = k - q, and the same two branches give the page's exact-LLA epilogue
+// ("Parallax" blog, s.2 Canonical Formulation and Appendix B):
+//   o_i = sum p (1 - t) v / sum p (1 - t) = (O1_i - O2_i) / (omega_i - d2_i),  d2 = sum_j p_ij t_ij.
+//
 // The same pass, with V := K and y := a conjugate-gradient direction p and only the covariance
 // branch kept (kMatvec), returns C_kk p: the matrix-free product that the CG strategy for the
 // ridge system needs (C_kk p = sum_j p_ij ((k_j - kbar) . p) k_j). Tiles whose flag in
@@ -96,7 +101,7 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 256, "barrier region");
 
-template <typename TOut, bool kMatvec>
+template <typename TOut, bool kMatvec, bool kPage>
 __global__ void __launch_bounds__(NTHREADS, 1)
 readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                   const uint4* __restrict__ pimg, const uint32_t* __restrict__ ytc,
@@ -287,8 +292,8 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     const int i = i0 + r;
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
-    const float cy = valid ? cy_in[base + i] : 0.f;  // kbar . y
-    float om = 0.f;
+    const float cy = valid ? cy_in[base + i] : 0.f;  // kbar . y (page form: q . rho*)
+    float om = 0.f, d2 = 0.f;
     bool ok = true;
     for (int c = 0; c < nck; ++c) {
       const int st = c % KS, tb = c & 1;
@@ -320,6 +325,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           om += r0 + r1;
           const float q0 = r0 * (__uint_as_float(tv[j]) - cy);
           const float q1 = r1 * (__uint_as_float(tv[j + 1]) - cy);
+          if (kPage) d2 += q0 + q1;
           const uint32_t hh = pack_bf16(q0, q1);
           hw[j / 2] = hh;
           lw[j / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
@@ -343,7 +349,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     }
     if (ok && warp_wait(&bar.accfull, 0, status, abort_p)) {
       tc_fence_after();
-      const float inv = 1.f / om;
+      const float inv = kPage ? 1.f / (om - d2) : 1.f / om;
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 16) {
         uint32_t o1[16], o2[16];
@@ -355,6 +361,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           for (int t = 0; t < 16; ++t)
             stf(out, (base + i) * DV + c0 + t,
                 kMatvec ? __uint_as_float(o2[t])
+                : kPage ? (__uint_as_float(o1[t]) - __uint_as_float(o2[t])) * inv
                         : fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
         }
       }
@@ -376,10 +383,10 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   }
 }
 
-template <typename TOut, bool kMatvec>
+template <typename TOut, bool kMatvec, bool kPage = false>
 cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* v,
                       const uint32_t* ytc, const float* cy, TOut* out, const int* tile_active) {
-  auto kern = readout_tc_kernel<TOut, kMatvec>;
+  auto kern = readout_tc_kernel<TOut, kMatvec, kPage>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -396,8 +403,10 @@ cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const 
 }  // namespace
 
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
-  return launch_ro<__nv_bfloat16, false>(a, ws, s, a.v, ws.ytc, ws.cy,
-                                         static_cast<__nv_bfloat16*>(a.out), nullptr);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  return ws.form == kFormPage
+             ? launch_ro<__nv_bfloat16, false, true>(a, ws, s, a.v, ws.ytc, ws.cy, out, nullptr)
+             : launch_ro<__nv_bfloat16, false>(a, ws, s, a.v, ws.ytc, ws.cy, out, nullptr);
 }
 
 cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,

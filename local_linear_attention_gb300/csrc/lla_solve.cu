@@ -329,7 +329,7 @@ namespace stc {
 constexpr int D = 64;
 constexpr int WARPS = 4;                 // warps (queries) per block
 constexpr int TRI = D * (D + 1) / 2;     // packed lower triangle of L
-constexpr int WARP_FLOATS = TRI + 2 * D + D;  // L, two column buffers, the vector s = sum p k
+constexpr int WARP_FLOATS = TRI + 2 * D + 2 * D;  // L, two column buffers, s = sum p k, mu
 
 __host__ __device__ constexpr int tri(int r) { return r * (r + 1) / 2; }
 // Slot of (a, b) in a tensor-core moment row for b >= a + (a & 1) (the run of row a):
@@ -439,6 +439,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // significant bits, so that the readout's Y K^T keeps y's precision on the tensor cores), each
 // part a row of 64 bf16 stored as 32 packed pairs, and cy = kbar . y. For the CUDA-core readout
 // (value width other than 64) also y and kbar in fp32 (y_out, kbar_out; else null).
+//
+// PAGE: the page form of the same solve ("Parallax" blog, s.2 Canonical Formulation, with the
+// query-centred z_j = k_j - q_i): rho* = Sigma^-1 mu with Sigma = sum p z z^T + lambda' I and
+// mu = sum p z = s - omega q. In the moments at hand Sigma = S - s s^T / omega + mu mu^T / omega
+// + lambda' I: the centred matrix plus one rank-one term. The output is then rho* in place of y
+// and cy = q . rho*, so that the readout's t_ij = k_j . rho* - cy is the page's z_ij . rho*.
+template <bool PAGE>
 __global__ void __launch_bounds__(stc::WARPS * 32, 3)
 solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mom, const float* __restrict__ omega,
                 const float* __restrict__ mrow, long long rows, float lam, uint32_t* __restrict__ ytc,
@@ -452,6 +459,7 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   float* Lt = sh[warp];
   float* cbuf = Lt + TRI;
   float* sv = cbuf + 2 * D;
+  float* muv = sv + D;
   const float* g = mom + row * TC_ROW;
 
   Lane L;
@@ -474,21 +482,33 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   const float lp = (float)lpd;
   sv[L.r0] = s0;
   sv[L.r1] = s1;
+  const float mu0 = fmaf(-om, qa, s0), mu1 = fmaf(-om, qb, s1);  // page form: mu = s - omega q
+  if (PAGE) {
+    muv[L.r0] = mu0;
+    muv[L.r1] = mu1;
+  }
   __syncwarp();
   const float inv_om = 1.f / om;
   const float kb0 = s0 * inv_om, kb1 = s1 * inv_om;
-  L.z0 = qa - kb0;
-  L.z1 = qb - kb1;
-  // C_kk + lambda' I = S - s s^T / omega + lambda' I, row by row (the odd diagonal entries sit
-  // outside the rows' runs).
+  const float mo0 = mu0 * inv_om, mo1 = mu1 * inv_om;
+  L.z0 = PAGE ? mu0 : qa - kb0;
+  L.z1 = PAGE ? mu1 : qb - kb1;
+  // C_kk + lambda' I = S - s s^T / omega + lambda' I (page form: + mu mu^T / omega), row by row
+  // (the odd diagonal entries sit outside the rows' runs).
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
     const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
     const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+    float mj[4] = {0.f, 0.f, 0.f, 0.f};
+    if (PAGE) {
+      const float4 m4 = *reinterpret_cast<const float4*>(muv + j);
+      mj[0] = m4.x; mj[1] = m4.y; mj[2] = m4.z; mj[3] = m4.w;
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float v = L.r0 == j + u ? d0 + lp : L.a0[j + u];
       v = fmaf(-sj[u], kb0, v);
+      if (PAGE) v = fmaf(mj[u], mo0, v);
       L.a0[j + u] = j + u <= L.r0 ? v : 0.f;
     }
   }
@@ -496,10 +516,16 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   for (int j = 0; j < D; j += 4) {
     const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
     const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+    float mj[4] = {0.f, 0.f, 0.f, 0.f};
+    if (PAGE) {
+      const float4 m4 = *reinterpret_cast<const float4*>(muv + j);
+      mj[0] = m4.x; mj[1] = m4.y; mj[2] = m4.z; mj[3] = m4.w;
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float v = L.r1 == j + u ? d1 + lp : L.a1[j + u];
       v = fmaf(-sj[u], kb1, v);
+      if (PAGE) v = fmaf(mj[u], mo1, v);
       L.a1[j + u] = j + u <= L.r1 ? v : 0.f;
     }
   }
@@ -538,7 +564,7 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   yrow[lane] = p1;
   yrow[D / 2 + lane] = p2;
   yrow[D + lane] = p3;
-  float c = fmaf(kb0, y0, kb1 * y1);
+  float c = PAGE ? fmaf(qa, y0, qb * y1) : fmaf(kb0, y0, kb1 * y1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   if (lane == 0) cy_out[row] = c;
@@ -553,7 +579,8 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
 cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long rows = a.rows();
   const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
-  solve_tc_kernel<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
+  auto kern = ws.form == kFormPage ? solve_tc_kernel<true> : solve_tc_kernel<false>;
+  kern<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), ws.mom, ws.omega, ws.m, rows, a.lam, ws.ytc, ws.cy,
       a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.status);
   count_launch();

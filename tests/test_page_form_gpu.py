@@ -1,0 +1,100 @@
+"""GPU parity of the page form of the LLA intercept (lla_set_form(1)).
+
+The page form solves (sum w z z^T + lambda' I) rho* = sum w z with the query-centred z = k - q and
+evaluates o = sum w (1 - z.rho*) v / sum w (1 - z.rho*) as the exact-LLA two-branch epilogue
+(O1 - O2) / (d1 - d2) ("Parallax" blog, s.2 Canonical Formulation and Appendix B). It is the same
+intercept as the centred form, so it must meet the same bound against the float64 oracle:
+relative Frobenius error <= 2e-2 for bf16 inputs (the only inputs it serves: bf16, d = dv = 64).
+"""
+import numpy as np
+import pytest
+import torch
+
+from local_linear_attention_gb300 import workloads as W
+from oracle import lla_forward_oracle, softmax_attention_oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module")
+def lla():
+    from local_linear_attention_gb300 import binding, build
+    build.build()
+    return binding
+
+
+@pytest.fixture
+def page(lla):
+    lla.lla_set_form(lla.FORM_PAGE)
+    yield lla
+    lla.lla_set_form(lla.FORM_CENTRED)
+
+
+def rel_err(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def run(lla, q, k, v, h, lam):
+    out = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), h, lam)
+    assert lla.lla_stream_status() == 0
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("T", [1, 2, 33, 128, 129, 300, 700])
+def test_page_form_matches_oracle_all_rows(page, T):
+    q, k, v = W.make_iid(1, 2, T, 64, 64, "bf16", seed=500 + T)
+    got = run(page, q, k, v, 8.0, 1e-2).reshape(-1, 64)
+    ref = lla_forward_oracle(q, k, v, 8.0, 1e-2).reshape(-1, 64)
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_page_form_headline_sampled_rows(page):
+    w = W.WORKLOADS[3]
+    q, k, v = W.make_inputs(w)
+    rows = W.sample_rows(w.B * w.H, w.T, 128, seed=11)
+    got = run(page, q, k, v, w.h, w.lam).reshape(-1, w.dv)[rows]
+    ref = lla_forward_oracle(q, k, v, w.h, w.lam, rows=rows)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_page_form_agrees_with_centred(lla):
+    q, k, v = W.make_iid(2, 2, 512, 64, 64, "bf16", seed=41)
+    centred = run(lla, q, k, v, 8.0, 1e-2)
+    lla.lla_set_form(lla.FORM_PAGE)
+    try:
+        pg = run(lla, q, k, v, 8.0, 1e-2)
+    finally:
+        lla.lla_set_form(lla.FORM_CENTRED)
+    assert rel_err(pg.reshape(-1, 64), centred.reshape(-1, 64)) <= TOL_BF16
+
+
+def test_page_form_large_ridge_is_softmax(page):
+    # lambda -> infinity: rho* -> 0, so the epilogue is O1 / d1, causal softmax attention.
+    q, k, v = W.make_iid(1, 1, 300, 64, 64, "bf16", seed=6)
+    got = run(page, q, k, v, 8.0, 1e12).reshape(-1, 64)
+    ref = softmax_attention_oracle(q, k, v, 8.0).reshape(-1, 64)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_page_form_other_paths_unsupported(page):
+    # fp32 inputs and d = 32 take the CUDA-core stage, which has no page form.
+    for dtype, d in (("f32", 64), ("bf16", 32)):
+        q, k, v = W.make_iid(1, 1, 64, d, d, dtype, seed=2)
+        with pytest.raises(page.LlaError):
+            page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2)
+    page.lla_set_moments_path(page.PATH_CG)
+    try:
+        q, k, v = W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3)
+        with pytest.raises(page.LlaError):
+            page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2)
+    finally:
+        page.lla_set_moments_path(page.PATH_AUTO)
+
+
+def test_set_form_rejects_other_values(lla):
+    for bad in (-1, 2, 7):
+        with pytest.raises(lla.LlaError):
+            lla.lla_set_form(bad)
