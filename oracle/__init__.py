@@ -9,4 +9,9 @@ from .lla_oracle import (  # noqa: F401
     lla_moments_oracle,
     softmax_attention_oracle,
 )
-from .parallax_oracle import parallax_row, parallax_forward_oracle  # noqa: F401
+from .parallax_oracle import (  # noqa: F401
+    parallax_row,
+    parallax_forward_oracle,
+    parallax_backward_row,
+    parallax_backward_oracle,
+)

@@ -83,3 +83,77 @@ def parallax_forward_oracle(q, k, v, r, h: float, rows=None) -> np.ndarray:
         bh, i = divmod(int(rr), T)
         out[n] = parallax_row(Q[bh, i], K[bh, : i + 1], V[bh, : i + 1], R[bh, i], h)
     return out
+
+
+# ----------------------------------------------------------------------------- backward
+# The pages' Appendix F ("Parallax backward (closed form)") names the row scalars, the cached
+# quantities (o_i, vbar_i, tbar_i, omega_i, m_i) and the row-tile / column-tile split, but its
+# formulas were lost in extraction. The backward below is the gradient of the forward above
+# (parallax_row), taken step by step in the forward's own order:
+#
+#   p_j = softmax_j(q_i . k_j / h),  t_j = r_i . k_j,  tbar = sum_j p_j t_j,
+#   o_i = vbar - Sigma_KV r_i = sum_j a_j v_j,  a_j = p_j (1 + tbar - t_j)
+#
+# (vbar - Sigma_KV r = sum p v - sum p (v - vbar)(t - tbar) = sum p (1 + tbar - t) v, since
+# sum p (t - tbar) = 0). With the upstream gradient dO_i and g_j = dO_i . v_j:
+#   dv_j += a_j dO_i;
+#   through t (directly, and through tbar = sum p t):  dt_j = p_j (G - g_j),  G = sum_j p_j g_j
+#     = dO_i . vbar, so dr_i = sum_j dt_j k_j and dk_j += dt_j r_i;
+#   through p (directly in a, and through tbar):  u_j = dL/dp_j = (1 + tbar - t_j) g_j + G t_j;
+#     the softmax gives ds_j = p_j (u_j - D),  D = sum_j p_j u_j = dO_i . o_i + G tbar, and
+#     s_j = q_i . k_j / h gives dq_i = sum_j ds_j k_j / h and dk_j += ds_j q_i / h.
+# D and G are the row scalars the pages' kernel caches beyond the softmax statistics.
+
+
+def parallax_backward_row(q_i, K, V, r_i, do_i, h):
+    """Gradient of parallax_row(q_i, K, V, r_i, h) . do_i with respect to q_i, r_i and the prefix
+    K [n, d], V [n, e]. Returns (dq_i [d], dr_i [d], dK [n, d], dV [n, e])."""
+    s = K @ q_i / h
+    w = np.exp(s - s.max())
+    p = w / w.sum()
+    t = K @ r_i
+    tbar = p @ t
+    a = p * (1.0 + tbar - t)
+    o = a @ V
+    g = V @ do_i
+    G = p @ g
+    dt = p * (G - g)
+    u = (1.0 + tbar - t) * g + G * t
+    D = do_i @ o + G * tbar
+    ds = p * (u - D)
+    dq = K.T @ ds / h
+    dr = K.T @ dt
+    dK = np.outer(ds, q_i) / h + np.outer(dt, r_i)
+    dV = np.outer(a, do_i)
+    return dq, dr, dK, dV
+
+
+def parallax_backward_oracle(q, k, v, r, do, h: float):
+    """Causal Parallax backward in float64: gradients of sum_i parallax(i) . do_i.
+
+    q, k, r: [..., T, d]; v, do: [..., T, e]. Returns (dq, dk, dv, dr) shaped like q, k, v, r.
+    """
+    Q, K, V, R, DO = _f64(q), _f64(k), _f64(v), _f64(r), _f64(do)
+    squeeze = Q.ndim == 2
+    if squeeze:
+        Q, K, V, R, DO = Q[None], K[None], V[None], R[None], DO[None]
+    lead = Q.shape[:-2]
+    T, d = Q.shape[-2:]
+    e = V.shape[-1]
+    Q, K, R = Q.reshape(-1, T, d), K.reshape(-1, T, d), R.reshape(-1, T, d)
+    V, DO = V.reshape(-1, T, e), DO.reshape(-1, T, e)
+    dq, dk, dr = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(R)
+    dv = np.zeros_like(V)
+    for bh in range(Q.shape[0]):
+        for i in range(T):
+            gq, gr, gK, gV = parallax_backward_row(Q[bh, i], K[bh, : i + 1], V[bh, : i + 1],
+                                                   R[bh, i], DO[bh, i], h)
+            dq[bh, i] = gq
+            dr[bh, i] = gr
+            dk[bh, : i + 1] += gK
+            dv[bh, : i + 1] += gV
+    outs = []
+    for x, last in ((dq, d), (dk, d), (dv, e), (dr, d)):
+        x = x.reshape(*lead, T, last)
+        outs.append(x[0] if squeeze else x)
+    return tuple(outs)
