@@ -416,6 +416,138 @@ def run_parallax(args, w, cpu, world, rank):
     return 0
 
 
+METRIC_PX_BWD = "Parallax backward queries/sec and TFLOP/s on 1 GB300; fraction of FP32 FMA peak"
+
+
+def parallax_bwd_flops_per_pair(d: int, dv: int):
+    """(algorithmic, executed) flops per causal pair of lla_parallax_backward: the forward's row
+    statistics (Q K^T, R K^T, P V, P2 V: 4d + 4dv) plus the backward proper (the same logits
+    and dO V^T once: 4d + 2dv; dq, dr: 4d; dk: 4d; dv: 2dv); executed, the row and column passes
+    each recompute the logits and dO V^T (20d + 10dv)."""
+    return 16 * d + 8 * dv, 20 * d + 10 * dv
+
+
+def run_parallax_backward(args, w, world, rank):
+    """One step = one lla_parallax_backward call (three launches) over the workload, with the
+    Parallax probe and an i.i.d. N(0,1) upstream gradient."""
+    import torch
+    import torch.distributed as dist
+    from local_linear_attention_gb300 import binding as lla
+    from local_linear_attention_gb300 import workloads as W
+
+    _, h = w.points[0]
+    q, k, v = W.make_inputs(w)
+    r = W.make_probe(w.B, w.H, w.T, w.d, w.dtype, seed=w.seed + 100)
+    g = torch.Generator().manual_seed(w.seed + 200)
+    do = torch.randn(w.B, w.H, w.T, w.dv, generator=g).to(q.dtype)
+    xs = [x.cuda() for x in (q, k, v, r, do)]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    grads = []
+
+    def step():
+        grads[:] = lla.lla_parallax_backward(*xs, h, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = lla.launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    n_launch = lla.launch_count() - n_launch0
+    clk = clocks.stop()
+    if lla.lla_stream_status() != 0:
+        raise RuntimeError("liblla reported an error during the timed steps")
+    ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = w.queries * world / (ms_per_step / 1e3)
+
+    e2e = None
+    eb = q.element_size()
+    if not args.no_e2e:  # pinned host inputs -> device, backward, gradients -> pinned host
+        hosts = [x.pin_memory() for x in (q, k, v, r, do)]
+        houts = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q, k, v, r)]
+
+        def e2e_step():
+            for hst, dst in zip(hosts, xs):
+                dst.copy_(hst, non_blocking=True)
+            step()
+            for hst, src in zip(houts, grads):
+                hst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        e2e_steps = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": sum(x.numel() for x in (q, k, v, r, do)) * eb,
+               "d2h_bytes_per_step": sum(x.numel() for x in (q, k, v, r)) * eb}
+
+    peaks, peak_src = load_peaks()
+    alg, exe = parallax_bwd_flops_per_pair(w.d, w.dv)
+    achieved = causal_pairs(w) * alg / (ms_per_step / 1e3) / 1e12
+    peak = fp32_alu_peak_tflops(peaks)
+    roof = {"kernel": "parallax backward (lla_parallax_bwd.cu, CUDA cores: stats, rows, "
+                      "columns)", "bound": "alu",
+            "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                           f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "executed_tflops": causal_pairs(w) * exe / (ms_per_step / 1e3) / 1e12,
+            "traffic": None, "avg_launch_ms": ms_per_step / 3}
+    if rank == 0:
+        line = {
+            "metric": METRIC_PX_BWD, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v and dO, probe "
+                                   f"N(0,1/d) seed {w.seed + 100}, h={h}, seed {w.seed}",
+                       "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
+                       "l2": "flushed between steps (256 MiB write outside the step events)",
+                       "parallelism": f"replica per GPU x{world}"},
+            "tflops": achieved,
+            "roofline": roof,
+            "cpu_baseline": None,
+            "e2e": e2e,
+            "gpu_launches": n_launch,
+            "clocks": clk,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 METRIC_DECODE = "LLA decode queries/sec (one query per head against a KV cache) on 1 GB300"
 METRIC_PX_DECODE = "Parallax decode queries/sec (one query per head against a KV cache) on 1 GB300"
 
@@ -555,7 +687,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
-    ap.add_argument("--op", choices=["lla", "parallax", "decode", "parallax_decode"],
+    ap.add_argument("--op", choices=["lla", "parallax", "decode", "parallax_decode",
+                                     "parallax_backward"],
                     default="lla",
                     help="the operation timed: the LLA forward (default), the Parallax forward, "
                          "or LLA / Parallax decode (one query per head against a KV cache)")
@@ -586,11 +719,11 @@ def main(argv=None):
         w = W.Workload("custom", int(B), int(H), int(T), d, int(dv), dt, 2, "iid",
                        h=math.sqrt(d), lam=1e-2)
         args.no_cpu_baseline = True
-    if args.op in ("decode", "parallax_decode"):
+    if args.op in ("decode", "parallax_decode", "parallax_backward"):
         args.no_cpu_baseline = True  # the oracle leg times the prefill workloads
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the oracle leg times the "
-                              "prefill forward; decode has no CPU reference line"}), flush=True)
+                              "prefill forward; this op has no CPU reference line"}), flush=True)
             return 0
     if args.impl == "reference":
         return run_reference(args, w)
@@ -617,6 +750,8 @@ def main(argv=None):
 
     if args.op == "parallax":
         return run_parallax(args, w, cpu, world, rank)
+    if args.op == "parallax_backward":
+        return run_parallax_backward(args, w, world, rank)
     if args.op in ("decode", "parallax_decode"):
         return run_decode(args, world, rank)
 

@@ -189,6 +189,24 @@ int lla_parallax_decode(const void* q, const void* k, const void* v, const void*
                         int B, int H, int L, int d, int dv, float h, int dtype, void* stream);
 
 /*
+ * Causal Parallax backward ("Parallax" blog, Appendix F "Parallax backward (closed form)": a
+ * forward-like pass caches per-row scalars, then a row-tile pass and a column-tile pass). Given
+ * the inputs of lla_parallax_forward (q, k, r: [B,H,T,d]; v: [B,H,T,dv]) and the upstream
+ * gradient dout = dL/do ([B,H,T,dv]), writes dq = dL/dq, dk, dr ([B,H,T,d]) and dv ([B,H,T,dv]).
+ * The appendix's formulas were lost in extraction; the gradients are those of the forward itself
+ * (o_i = sum_j p_ij (1 + tbar_i - t_ij) v_j with p_i = softmax of q_i.k_j / h over j <= i,
+ * t_ij = r_i . k_j, tbar_i = sum_j p_ij t_ij). All buffers are device pointers, contiguous
+ * row-major, 16-byte aligned, of the dtype given (gradients in the inputs' dtype; fp32
+ * arithmetic); the caller owns them; outputs must not alias inputs. d, dv in {16, 32, 64}
+ * (else LLA_ERR_UNSUPPORTED); h > 0 and finite, B, H, T >= 0 (else LLA_ERR_INVALID_ARG). Three
+ * launches on CUDA cores, asynchronous on `stream`, with a scratch of 32 bytes per query row
+ * from the stream-ordered pool. Returns LLA_OK, LLA_ERR_* for invalid arguments, LLA_ERR_CUDA.
+ */
+int lla_parallax_backward(const void* q, const void* k, const void* v, const void* r,
+                          const void* dout, void* dq, void* dk, void* dv, void* dr, int B, int H,
+                          int T, int d, int dv_, float h, int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns LLA_OK, LLA_ERR_NUMERICAL, LLA_ERR_TIMEOUT, LLA_ERR_INVALID_ARG (bad idx in
  * lla_moments) or LLA_ERR_CUDA (a sticky CUDA error or failed synchronisation).

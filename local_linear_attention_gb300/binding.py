@@ -18,6 +18,7 @@ __all__ = [
     "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
     "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "PATH_CG", "lla_set_cg", "lla_parallax_forward",
     "lla_decode", "lla_parallax_decode", "lla_set_form", "FORM_CENTRED", "FORM_PAGE",
+    "lla_parallax_backward",
 ]
 
 LLA_OK = 0
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
     "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg", "lla_decode", "lla_parallax_decode",
-    "lla_parallax_forward", "lla_set_form",
+    "lla_parallax_forward", "lla_set_form", "lla_parallax_backward",
 )
 
 # LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
@@ -80,6 +81,7 @@ def _load():
         "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "lla_decode": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_parallax_decode": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
+        "lla_parallax_backward": (i, [vp] * 9 + [i, i, i, i, i, f, i, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,6 +216,25 @@ def lla_parallax_decode(q, k, v, r, h: float, out=None, stream=None):
                                      _stream_ptr(stream))
     _check(st, "lla_parallax_decode")
     return out
+
+
+def lla_parallax_backward(q, k, v, r, dout, h: float, stream=None):
+    """Gradients (dq, dk, dv, dr) of the causal Parallax forward for the upstream gradient dout
+    ([B,H,T,dv], like the forward's output); each is shaped and typed like q, k, v, r."""
+    B, H, T, d, dv, code = _device_inputs(q, k, v)
+    for name, x, like in (("r", r, q), ("dout", dout, None)):
+        shape = q.shape if like is not None else (B, H, T, dv)
+        if tuple(x.shape) != tuple(shape) or x.dtype != q.dtype or not x.is_cuda \
+                or not x.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {tuple(shape)} "
+                             f"and dtype {q.dtype}")
+    dq, dk, dvv, dr = (torch.empty_like(x) for x in (q, k, v, r))
+    st = _load().lla_parallax_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                       dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                       dvv.data_ptr(), dr.data_ptr(), B, H, T, d, dv, float(h),
+                                       code, _stream_ptr(stream))
+    _check(st, "lla_parallax_backward")
+    return dq, dk, dvv, dr
 
 
 def lla_forward_noalloc(q, k, v, h: float, lam: float, out, stream=None):

@@ -335,6 +335,27 @@ int lla_parallax_decode(const void* q, const void* k, const void* v, const void*
   return run_decode(a, stream);
 }
 
+int lla_parallax_backward(const void* q, const void* k, const void* v, const void* r,
+                          const void* dout, void* dq, void* dk, void* dv, void* dr, int B, int H,
+                          int T, int d, int dv_, float h, int dtype, void* stream) {
+  int st = check_shape(B, H, T, d, dv_, dtype);
+  if (st != LLA_OK) return st;
+  if (!is_finite_pos(h)) return LLA_ERR_INVALID_ARG;
+  if ((long long)B * H * T == 0) return LLA_OK;
+  const void* ptrs[9] = {q, k, v, r, dout, dq, dk, dv, dr};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = nullptr;
+  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  const ParallaxBwdArgs a{q, k, v, r, dout, dq, dk, dv, dr, B, H, T, d, dv_, h, dtype};
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, parallax_bwd_workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
+  st = launch_parallax_bwd(a, ws, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
+  return st;
+}
+
 int lla_stream_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return LLA_ERR_CUDA;

@@ -145,6 +145,25 @@ struct DecodeArgs {
   int dtype;
   long long BH() const { return (long long)B * H; }
 };
+// Causal Parallax backward (the gradients of lla_parallax_forward with respect to q, k, v, r).
+struct ParallaxBwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* r;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* dr;
+  int B, H, T, d, dv_;
+  float h;
+  int dtype;
+  long long BH() const { return (long long)B * H; }
+};
+size_t parallax_bwd_workspace_bytes(const ParallaxBwdArgs& a);
+cudaError_t launch_parallax_bwd(const ParallaxBwdArgs& a, void* ws, cudaStream_t s);
+
 size_t decode_workspace_bytes(const DecodeArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a, void* ws, int* status, cudaStream_t s);
 
