@@ -422,8 +422,9 @@ METRIC_PX_BWD = "Parallax backward queries/sec and TFLOP/s on 1 GB300; fraction 
 def parallax_bwd_flops_per_pair(d: int, dv: int):
     """(algorithmic, executed) flops per causal pair of lla_parallax_backward: the forward's row
     statistics (Q K^T, R K^T, P V, P2 V: 4d + 4dv) plus the backward proper (the same logits
-    and dO V^T once: 4d + 2dv; dq, dr: 4d; dk: 4d; dv: 2dv); executed, the row and column passes
-    each recompute the logits and dO V^T (20d + 10dv)."""
+    and dO V^T once: 4d + 2dv; dq, dr: 4d; dk: 4d; dv: 2dv); executed (the CUDA-core passes),
+    the row and column passes each recompute the logits and dO V^T (20d + 10dv). The
+    tensor-core passes execute more (a max sweep in the record pass, the P2 V hi/lo pair)."""
     return 16 * d + 8 * dv, 20 * d + 10 * dv
 
 
@@ -515,20 +516,27 @@ def run_parallax_backward(args, w, world, rank):
     peaks, peak_src = load_peaks()
     alg, exe = parallax_bwd_flops_per_pair(w.d, w.dv)
     achieved = causal_pairs(w) * alg / (ms_per_step / 1e3) / 1e12
-    peak = fp32_alu_peak_tflops(peaks)
-    roof = {"kernel": "parallax backward (lla_parallax_bwd.cu, CUDA cores: stats, rows, "
-                      "columns)", "bound": "alu",
-            "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                           f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
-            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "executed_tflops": causal_pairs(w) * exe / (ms_per_step / 1e3) / 1e12,
-            "traffic": None, "avg_launch_ms": ms_per_step / 3}
+    tensor_path = w.dtype == "bf16" and w.d == 64 and w.dv == 64
+    if tensor_path:
+        peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+        roof = {"kernel": "parallax backward (tcgen05: row records from the forward kernel of "
+                          "lla_parallax.cu, rows and columns passes of lla_parallax_bwd_tc.cu)",
+                "bound": "tensor", "peak_source": f"bf16 dense, burst ({peak_src})"}
+    else:
+        peak = fp32_alu_peak_tflops(peaks)
+        roof = {"kernel": "parallax backward (lla_parallax_bwd.cu, CUDA cores: stats, rows, "
+                          "columns)", "bound": "alu",
+                "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
+    roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                 "executed_tflops": causal_pairs(w) * exe / (ms_per_step / 1e3) / 1e12,
+                 "traffic": None, "avg_launch_ms": ms_per_step / 3})
     if rank == 0:
         line = {
             "metric": METRIC_PX_BWD, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v and dO, probe "
                                    f"N(0,1/d) seed {w.seed + 100}, h={h}, seed {w.seed}",
                        "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,

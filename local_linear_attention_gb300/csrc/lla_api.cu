@@ -351,7 +351,8 @@ int lla_parallax_backward(const void* q, const void* k, const void* v, const voi
   const ParallaxBwdArgs a{q, k, v, r, dout, dq, dk, dv, dr, B, H, T, d, dv_, h, dtype};
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, parallax_bwd_workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
-  st = launch_parallax_bwd(a, ws, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  const int path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
+  st = launch_parallax_bwd(a, ws, path, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
   return st;
 }

@@ -162,7 +162,15 @@ struct ParallaxBwdArgs {
   long long BH() const { return (long long)B * H; }
 };
 size_t parallax_bwd_workspace_bytes(const ParallaxBwdArgs& a);
-cudaError_t launch_parallax_bwd(const ParallaxBwdArgs& a, void* ws, cudaStream_t s);
+// All three passes; bf16 with d = dv = 64 on tensor cores unless path == kPathCudaCore.
+cudaError_t launch_parallax_bwd(const ParallaxBwdArgs& a, void* ws, int path, int* status,
+                                cudaStream_t s);
+// Tensor-core pieces (bf16, d = dv = 64): the row records from the tensor-core forward, then
+// the rows and columns passes.
+cudaError_t launch_parallax_stats_tc(const ParallaxBwdArgs& a, float* stats, int* status,
+                                     cudaStream_t s);
+cudaError_t launch_parallax_bwd_tc(const ParallaxBwdArgs& a, float* stats, int* status,
+                                   cudaStream_t s);
 
 size_t decode_workspace_bytes(const DecodeArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a, void* ws, int* status, cudaStream_t s);

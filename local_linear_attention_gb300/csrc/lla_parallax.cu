@@ -87,10 +87,17 @@ struct Barriers {
 
 // Steps g = 0 .. nb-1 are the max sweep (Q K^T only), g = nb .. 2nb-1 the main sweep over the
 // same key blocks b = g - nb.
+//
+// STATS (the backward's row scalars, given the upstream gradient dout): instead of o, each row
+// writes the record {m, 1/omega, tbar, G, D} to stats[row * 8 ..]: m the max of the raw logits
+// q.k (before 1/h), omega = d1 the sum of its weights exp((q.k - m)/h), tbar = d2/d1,
+// G = dout . vbar with vbar = O1/d1, and D = dout . o + G tbar with o = (1 + tbar) vbar - O2/d1.
+template <bool STATS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
                    int T, int BH, float inv_h, __nv_bfloat16* __restrict__ out,
+                   const __nv_bfloat16* __restrict__ dout, float* __restrict__ stats,
                    int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
@@ -305,13 +312,31 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         tc_fence_after();
         const float inv = 1.f / d1;
         const float f1 = (1.f + d2 * inv) * inv;
+        float gs = 0.f, od = 0.f;  // STATS: dout . vbar, dout . o
 #pragma unroll
         for (int c0 = 0; c0 < DV; c0 += 16) {
           uint32_t o1[16], o2[16];
           tmem_ld16(lane_base + T_O1 + c0, o1);
           tmem_ld16(lane_base + T_O2 + c0, o2);
           tmem_ld_wait();
-          if (valid) {
+          if (STATS) {
+            if (valid) {
+              const uint4* dy = reinterpret_cast<const uint4*>(dout + (base + i) * DV + c0);
+#pragma unroll
+              for (int hv = 0; hv < 2; ++hv) {
+                const uint4 w4 = dy[hv];
+                const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                  const int cc = 8 * hv + t;
+                  const float dyv = (t & 1) ? bf16_hi(ws[t / 2]) : bf16_lo(ws[t / 2]);
+                  const float o1v = __uint_as_float(o1[cc]), o2v = __uint_as_float(o2[cc]);
+                  gs = fmaf(dyv, o1v * inv, gs);
+                  od = fmaf(dyv, fmaf(o1v, f1, -o2v * inv), od);
+                }
+              }
+            }
+          } else if (valid) {
             uint32_t packed[8];
 #pragma unroll
             for (int t = 0; t < 16; t += 2)
@@ -322,6 +347,11 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
+        }
+        if (STATS && valid) {
+          const float tbar = d2 * inv;
+          *reinterpret_cast<float4*>(stats + (base + i) * 8) = make_float4(m, inv, tbar, gs);
+          stats[(base + i) * 8 + 4] = fmaf(gs, tbar, od);
         }
       }
     }
@@ -458,9 +488,26 @@ cudaError_t dispatch_d(const Args& a, const void* r, cudaStream_t s) {
 
 }  // namespace
 
+// The backward's row scalars (bf16, d = dv = 64): the tensor-core forward with the STATS epilogue.
+cudaError_t launch_parallax_stats_tc(const ParallaxBwdArgs& a, float* stats, int* status,
+                                     cudaStream_t s) {
+  auto kern = ptc::parallax_tc_kernel<true>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  const long long blocks = (long long)((a.T + ptc::BM - 1) / ptc::BM) * a.BH();
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_BYTES, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.r), a.T,
+      (int)a.BH(), 1.0f / a.h, nullptr, static_cast<const __nv_bfloat16*>(a.dout), stats, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_parallax(const Args& a, const void* r, int path, int* status, cudaStream_t s) {
   if (path == kPathTensorCore && a.dtype == LLA_BF16 && a.d == 64 && a.dv == 64) {
-    auto kern = ptc::parallax_tc_kernel;
+    auto kern = ptc::parallax_tc_kernel<false>;
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_BYTES);
     if (err != cudaSuccess) return err;
@@ -469,7 +516,7 @@ cudaError_t launch_parallax(const Args& a, const void* r, int path, int* status,
     kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_BYTES, s>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
         static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(r), a.T,
-        (int)a.BH(), 1.0f / a.h, static_cast<__nv_bfloat16*>(a.out), status);
+        (int)a.BH(), 1.0f / a.h, static_cast<__nv_bfloat16*>(a.out), nullptr, nullptr, status);
     count_launch();
     return cudaGetLastError();
   }

@@ -11,7 +11,9 @@
 //   dq_i += ds_ij k_j / h,  dr_i += dt_ij k_j,  dk_j += ds_ij q_i / h + dt_ij r_i,
 //   dv_j += a_ij dO_i.
 //
-// Three launches on CUDA cores (every supported d, dv and dtype; fp32 arithmetic):
+// bf16 inputs with d = dv = 64 take the tensor-core passes (lla_parallax_bwd_tc.cu). Every other
+// shape and dtype (and bf16 d = dv = 64 when the CUDA-core path is requested) takes three launches
+// on CUDA cores (fp32 arithmetic):
 //  * stats: the forward's online pass (running max with rescale), ending with the row scalars
 //    m_i (max logit), 1 / omega_i, tbar_i, G_i, D_i -- 5 floats per row in a float[8] record;
 //  * rows: one block per 64-query tile streams the key/value tiles of its causal prefix and
@@ -344,8 +346,11 @@ size_t parallax_bwd_workspace_bytes(const ParallaxBwdArgs& a) {
   return (size_t)a.BH() * (size_t)a.T * STAT * sizeof(float);
 }
 
-cudaError_t launch_parallax_bwd(const ParallaxBwdArgs& a, void* ws, cudaStream_t s) {
+cudaError_t launch_parallax_bwd(const ParallaxBwdArgs& a, void* ws, int path, int* status,
+                                cudaStream_t s) {
   float* stats = static_cast<float*>(ws);
+  if (path != kPathCudaCore && a.dtype == LLA_BF16 && a.d == 64 && a.dv_ == 64)
+    return launch_parallax_bwd_tc(a, stats, status, s);
   return a.dtype == LLA_F32 ? dispatch_d<float>(a, stats, s)
                             : dispatch_d<__nv_bfloat16>(a, stats, s);
 }

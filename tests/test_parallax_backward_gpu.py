@@ -107,3 +107,29 @@ def test_parallax_backward_argument_errors(lla):
     assert lib.lla_parallax_backward(*ptrs, 1, 1, 8, 64, 64, 8.0, 5, None) == 1  # dtype
     assert lib.lla_parallax_backward(*ptrs, 0, 1, 8, 64, 64, 8.0, 1, None) == 0  # empty
     assert lib.lla_parallax_backward(*([None] + ptrs[1:]), 1, 1, 8, 64, 64, 8.0, 1, None) == 1
+
+
+@pytest.mark.parametrize("T", [1, 2, 31, 127, 128, 129, 300, 1000])
+def test_parallax_backward_tensor_cores_matches_oracle(lla, T):
+    # bf16 d = dv = 64 runs the tcgen05 passes (rows and columns tiles of 128, blocks of 32).
+    q, k, v, r, do = make(1, 2, T, 64, 64, "bf16", seed=50 + T)
+    got = lla.lla_parallax_backward(*(x.cuda() for x in (q, k, v, r, do)), 8.0)
+    assert lla.lla_stream_status() == 0
+    ref = parallax_backward_oracle(q, k, v, r, do, 8.0)
+    scale = np.linalg.norm(ref[2])
+    for name, g, rf in zip(("dq", "dk", "dv", "dr"), got, ref):
+        err = np.linalg.norm(f64(g) - rf)
+        assert err <= TOL["bf16"] * (np.linalg.norm(rf) if np.linalg.norm(rf) > 0 else scale), name
+
+
+def test_parallax_backward_tensor_and_cuda_cores_agree(lla):
+    xs = [x.cuda() for x in make(2, 2, 777, 64, 64, "bf16", seed=8)]
+    tc = lla.lla_parallax_backward(*xs, 8.0)
+    lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
+    try:
+        cc = lla.lla_parallax_backward(*xs, 8.0)
+    finally:
+        lla.lla_set_moments_path(lla.PATH_AUTO)
+    assert lla.lla_stream_status() == 0
+    for name, a, b in zip(("dq", "dk", "dv", "dr"), tc, cc):
+        assert rel_err(f64(a), f64(b)) <= TOL["bf16"], name
