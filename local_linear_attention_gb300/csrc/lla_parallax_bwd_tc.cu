@@ -101,11 +101,11 @@ struct Barriers {
 static_assert(sizeof(Barriers) <= 256, "barrier region");
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-       const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
-       const __nv_bfloat16* __restrict__ dout, const float* __restrict__ stats, int T, int BH,
-       float inv_h, __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dr,
-       int* __restrict__ status) {
+pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
+                   const __nv_bfloat16* __restrict__ dout, const float* __restrict__ stats, int T,
+                   int BH, float inv_h, __nv_bfloat16* __restrict__ dq,
+                   __nv_bfloat16* __restrict__ dr, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -348,11 +348,11 @@ struct Barriers {
 static_assert(sizeof(Barriers) <= 256, "barrier region");
 
 __global__ void __launch_bounds__(NTHREADS, 1)
-kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-       const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
-       const __nv_bfloat16* __restrict__ dout, const float* __restrict__ stats, int T, int BH,
-       float inv_h, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-       int* __restrict__ status) {
+pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
+                   const __nv_bfloat16* __restrict__ dout, const float* __restrict__ stats, int T,
+                   int BH, float inv_h, __nv_bfloat16* __restrict__ dk,
+                   __nv_bfloat16* __restrict__ dv, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -609,18 +609,18 @@ cudaError_t launch_parallax_bwd_tc(const ParallaxBwdArgs& a, float* stats, int* 
   const auto* dy = static_cast<const __nv_bfloat16*>(a.dout);
   const float inv_h = 1.0f / a.h;
   const int BH = (int)a.BH();
-  err = cudaFuncSetAttribute(rows::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(rows::pbw_rows_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              rows::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  rows::kernel<<<(unsigned)blocks, NTHREADS, rows::SMEM_BYTES, s>>>(
+  rows::pbw_rows_tc_kernel<<<(unsigned)blocks, NTHREADS, rows::SMEM_BYTES, s>>>(
       q, k, v, r, dy, stats, a.T, BH, inv_h, static_cast<__nv_bfloat16*>(a.dq),
       static_cast<__nv_bfloat16*>(a.dr), status);
   count_launch();
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(cols::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(cols::pbw_cols_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cols::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  cols::kernel<<<(unsigned)blocks, NTHREADS, cols::SMEM_BYTES, s>>>(
+  cols::pbw_cols_tc_kernel<<<(unsigned)blocks, NTHREADS, cols::SMEM_BYTES, s>>>(
       q, k, v, r, dy, stats, a.T, BH, inv_h, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), status);
   count_launch();

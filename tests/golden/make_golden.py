@@ -32,10 +32,10 @@ def tiny_inputs():
 
 
 def backward_inputs():
-    q, k, v = W.make_iid(1, 1, 8, 4, 3, "f32", seed=77)
-    r = W.make_probe(1, 1, 8, 4, "f32", seed=78)
+    q, k, v = W.make_iid(1, 1, 8, 16, 16, "f32", seed=77)
+    r = W.make_probe(1, 1, 8, 16, "f32", seed=78)
     g = torch.Generator().manual_seed(79)
-    do = torch.randn(1, 1, 8, 3, generator=g)
+    do = torch.randn(1, 1, 8, 16, generator=g)
     return q, k, v, r, do
 
 
@@ -61,7 +61,7 @@ def fixtures():
     bq, bk, bv, br, bdo = backward_inputs()
     dq, dk, dv, dr = parallax_backward_oracle(bq, bk, bv, br, bdo, 1.5)
     out["parallax_backward_tiny.json"] = {
-        "what": ("gradients of the causal Parallax forward, B1 H1 T8 d=4 dv=3 fp32: q, k, v from "
+        "what": ("gradients of the causal Parallax forward, B1 H1 T8 d=dv=16 fp32: q, k, v from "
                  "make_iid seed 77, probe from make_probe seed 78, dO ~ N(0,1) seed 79, h = 1.5"),
         "definition": ("the gradient of the 'Parallax' blog's forward (s.2, Appendix B with "
                        "eta = 0), split as its Appendix F describes"),
