@@ -25,28 +25,20 @@
 #include <cstdint>
 
 #include "lla_internal.cuh"
+#include "lla_tc_ptx.cuh"
 
 namespace lla {
 namespace {
+
+using tc::cp_async16;
+using tc::cp_async_commit;
+using tc::cp_async_wait;
 
 constexpr int NT = 256;   // threads per CTA
 constexpr int TK = 64;    // keys per shared-memory tile
 
 template <typename TIn>
 __device__ __forceinline__ float ld(const TIn* p, long long i) { return ldf(p, i); }
-
-// Block reduction (max) of one float per thread.
-__device__ __forceinline__ float block_max(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = x;
-  __syncthreads();
-  float r = -INFINITY;
-  for (int i = 0; i < NT / 32; ++i) r = fmaxf(r, red[i]);
-  return r;
-}
 
 // Arrival of one CTA of head bh after its partial sums are written; true for the last one, which
 // then sees every CTA's partials.
@@ -135,6 +127,77 @@ __device__ __forceinline__ void tile_logits(const float* kt, const float* qs, co
   }
 }
 
+// Two adjacent elements as fp32 (one 4- or 8-byte shared load).
+__device__ __forceinline__ void load_pair(const float* p, float (&x)[2]) {
+  const float2 u = *reinterpret_cast<const float2*>(p);
+  x[0] = u.x; x[1] = u.y;
+}
+__device__ __forceinline__ void load_pair(const __nv_bfloat16* p, float (&x)[2]) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+  x[0] = __uint_as_float(w << 16); x[1] = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// n contiguous elements at p (16-byte aligned when n * sizeof(TIn) is a multiple of 16, else
+// 8-byte aligned) as fp32, with 16- or 8-byte shared loads.
+template <typename TIn, int N>
+__device__ __forceinline__ void load_row(const TIn* p, float (&x)[N]) {
+  constexpr int BYTES = N * (int)sizeof(TIn);
+  if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < BYTES / 16; ++c) {
+      const uint4 u = reinterpret_cast<const uint4*>(p)[c];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (sizeof(TIn) == 2) {
+          x[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+          x[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        } else {
+          x[4 * c + i] = __uint_as_float(w[i]);
+        }
+      }
+    }
+  } else {
+    static_assert(BYTES == 8, "row segment of 8 bytes");
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    if constexpr (sizeof(TIn) == 2) {
+      x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+      x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    }
+  }
+}
+
+// Logits q . k_j and r . k_j of a tile kept in the input type (the Parallax decode's cp.async
+// ring) into sS / sT (-inf past n): four threads per key, each with a contiguous quarter of the
+// row, completed by two shuffles within the four.
+template <typename TIn, int D>
+__device__ __forceinline__ void tile_logits_raw(const TIn* kt, const float* qs, const float* rs,
+                                                int n, float* sS, float* sT) {
+  static_assert(TK * 4 == NT, "four threads per key");
+  constexpr int SEG = D / 4;
+  const int key = threadIdx.x >> 2, part = threadIdx.x & 3;
+  float a = 0.f, b = 0.f;
+  if (key < n) {
+    float kv[SEG];
+    load_row<TIn, SEG>(kt + key * D + part * SEG, kv);
+#pragma unroll
+    for (int u = 0; u < SEG; ++u) {
+      a = fmaf(qs[part * SEG + u], kv[u], a);
+      b = fmaf(rs[part * SEG + u], kv[u], b);
+    }
+  }
+  a += __shfl_xor_sync(0xffffffffu, a, 1);
+  b += __shfl_xor_sync(0xffffffffu, b, 1);
+  a += __shfl_xor_sync(0xffffffffu, a, 2);
+  b += __shfl_xor_sync(0xffffffffu, b, 2);
+  if (part == 0) {
+    sS[key] = key < n ? a : -INFINITY;
+    sT[key] = b;
+  }
+}
+
 // exp((m_old - m_new) / h): the factor that moves sums shifted by m_old to the shift m_new.
 __device__ __forceinline__ float rescale(float m_old, float m_new, float inv_h) {
   return m_old == -INFINITY ? 0.f : __expf((m_old - m_new) * inv_h);
@@ -145,15 +208,26 @@ __device__ __forceinline__ float rescale(float m_old, float m_new, float inv_h) 
 template <int D, int DV>
 constexpr int px_part() { return 3 + 2 * DV; }
 
+// The Parallax decode streams its chunk through a ring of PX_ST raw (input-type) K/V tiles
+// filled with cp.async, PX_ST - 1 tiles ahead of the one being reduced: the reduction per key is
+// small, so the kernel is bound by how many cache bytes each SM keeps in flight.
+constexpr int PX_ST = 3;
+template <typename TIn, int D, int DV>
+constexpr size_t px_smem() { return (size_t)PX_ST * TK * (D + DV) * sizeof(TIn); }
+
 template <typename TIn, int D, int DV>
 __global__ void __launch_bounds__(NT)
 parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                        const TIn* __restrict__ v, const TIn* __restrict__ r, int L, int S,
                        float inv_h, float* __restrict__ part, int* __restrict__ counter,
                        TIn* __restrict__ out) {
-  constexpr int NG = NT / (2 * DV);  // key groups: thread t takes O coordinate t % 2DV, group t / 2DV
+  // Accumulation: thread t takes value columns 2 cp, 2 cp + 1 (cp = t % (DV/2)) of both branches
+  // for the keys of group t / (DV/2) (NG groups, keys jj = group + NG i).
+  constexpr int NG = NT / (DV / 2);
   __shared__ float qs[D], rs[D], red[NT / 32];
-  __shared__ __align__(16) float kt[TK * D], vt[TK * DV];
+  extern __shared__ __align__(16) uint8_t px_ring[];
+  TIn* kring = reinterpret_cast<TIn*>(px_ring);  // [PX_ST][TK * D]
+  TIn* vring = kring + PX_ST * TK * D;           // [PX_ST][TK * DV]
   __shared__ float pt[TK], tt[TK], sS[TK], sT[TK];
   __shared__ float og_s[NG][2 * DV], dsum[2][2], tot[2 * DV + 2];
   __shared__ double alpha[512];
@@ -170,21 +244,46 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   const TIn* vb = v + bh * (long long)L * DV;
   // One pass with a running maximum m: every sum is kept shifted by the current m and rescaled
   // when a tile raises it.
-  float m = -INFINITY, acc0 = 0.f, d1 = 0.f, d2 = 0.f;
-  const int oc = tid % (2 * DV), og = tid / (2 * DV);  // O1/O2 coordinate and key group
-  for (int t0 = j0; t0 < j1; t0 += TK) {
-    const int n = min(TK, j1 - t0);
-    __syncthreads();
-    stage<TIn, D>(kt, kb, t0, n);
-    stage<TIn, DV>(vt, vb, t0, n);
-    __syncthreads();
-    tile_logits<D, true>(kt, qs, rs, n, sS, sT);
+  float m = -INFINITY, d1 = 0.f, d2 = 0.f;
+  float o1a = 0.f, o1b = 0.f, o2a = 0.f, o2b = 0.f;
+  const int cp = tid % (DV / 2), og = tid / (DV / 2);
+  const int ntl = j1 > j0 ? (j1 - j0 + TK - 1) / TK : 0;
+  // Tile `it` of the chunk into ring slot it % PX_ST (16-byte copies; rows past the chunk are
+  // zero-filled without being read). One commit group per tile, empty past the end.
+  auto prefetch = [&](int it) {
+    if (it < ntl) {
+      const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
+      constexpr int KR = D * (int)sizeof(TIn) / 16, VR = DV * (int)sizeof(TIn) / 16;
+      const char* ks = reinterpret_cast<const char*>(kb + (long long)t0 * D);
+      const char* vs = reinterpret_cast<const char*>(vb + (long long)t0 * DV);
+      char* kd = reinterpret_cast<char*>(kring + slot * TK * D);
+      char* vd = reinterpret_cast<char*>(vring + slot * TK * DV);
+      for (int e = tid; e < TK * KR; e += NT) {
+        const bool in = e / KR < n;
+        cp_async16(kd + 16 * e, ks + (in ? 16 * e : 0), in ? 16u : 0u);
+      }
+      for (int e = tid; e < TK * VR; e += NT) {
+        const bool in = e / VR < n;
+        cp_async16(vd + 16 * e, vs + (in ? 16 * e : 0), in ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+  for (int it = 0; it < PX_ST - 1; ++it) prefetch(it);
+  for (int it = 0; it < ntl; ++it) {
+    const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
+    prefetch(it + PX_ST - 1);
+    cp_async_wait<PX_ST - 1>();  // this thread's copies of tile `it` have landed
+    __syncthreads();             // ... and everyone else's
+    const TIn* kt = kring + slot * TK * D;
+    const TIn* vt = vring + slot * TK * DV;
+    tile_logits_raw<TIn, D>(kt, qs, rs, n, sS, sT);
     __syncthreads();
     const float sj = tid < TK ? sS[tid] : -INFINITY, tj = tid < TK ? sT[tid] : 0.f;
     const float mn = tile_max(sj, m, red);
     const float sc = rescale(m, mn, inv_h);
     m = mn;
-    acc0 *= sc;
+    o1a *= sc; o1b *= sc; o2a *= sc; o2b *= sc;
     d1 *= sc;
     d2 *= sc;
     if (tid < TK) {
@@ -195,12 +294,22 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       d2 += p * tj;
     }
     __syncthreads();
-    const int col = oc % DV;
-    const float* w = oc < DV ? pt : tt;
-    for (int jj = og; jj < n; jj += NG) acc0 = fmaf(w[jj], vt[jj * DV + col], acc0);
+    for (int jj = og; jj < n; jj += NG) {
+      float vv[2];
+      load_pair(vt + jj * DV + 2 * cp, vv);
+      const float p = pt[jj], pr = tt[jj];
+      o1a = fmaf(p, vv[0], o1a); o1b = fmaf(p, vv[1], o1b);
+      o2a = fmaf(pr, vv[0], o2a); o2b = fmaf(pr, vv[1], o2b);
+    }
+    __syncthreads();  // slot `it` is refilled by the prefetch PX_ST - 1 iterations on
+    (void)t0;
   }
+  cp_async_wait<0>();
   // Reductions in a fixed order (no atomics), so that the result is reproducible.
-  og_s[og][oc] = acc0;
+  og_s[og][2 * cp] = o1a;
+  og_s[og][2 * cp + 1] = o1b;
+  og_s[og][DV + 2 * cp] = o2a;
+  og_s[og][DV + 2 * cp + 1] = o2b;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     d1 += __shfl_xor_sync(0xffffffffu, d1, o);
@@ -461,7 +570,11 @@ cudaError_t launch_px(const DecodeArgs& a, void* ws, cudaStream_t st) {
   int* cnt = reinterpret_cast<int*>(part + a.BH() * S * px_part<D, DV>());
   zero_counters<<<(unsigned)((a.BH() + 255) / 256), 256, 0, st>>>(cnt, (int)a.BH());
   count_launch();
-  parallax_decode_kernel<TIn, D, DV><<<(unsigned)(a.BH() * S), NT, 0, st>>>(
+  auto kern = parallax_decode_kernel<TIn, D, DV>;
+  constexpr size_t smem = px_smem<TIn, D, DV>();
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<(unsigned)(a.BH() * S), NT, smem, st>>>(
       static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
       static_cast<const TIn*>(a.r), a.L, S, 1.f / a.h, part, cnt, static_cast<TIn*>(a.out));
   count_launch();
