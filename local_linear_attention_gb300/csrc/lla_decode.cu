@@ -19,8 +19,10 @@
 // per head). Each CTA takes the exact maximum of its chunk in a first sweep over its keys.
 //
 // The reductions are rank-1 updates per key (the query dimension is 1), so they run on the CUDA
-// cores: keys are staged in shared memory in tiles, one thread per key forms the weight, and the
-// LLA second moments accumulate in 4 x 4 register tiles (two shared loads per 16 FMAs).
+// cores: each CTA streams its chunk through a ring of raw key/value tiles in shared memory
+// (cp.async, two tiles ahead of the one being reduced), four threads per key form the logits,
+// one thread per key the weight, and the LLA second moments accumulate in 4 x 4 register tiles
+// (two shared loads per 16 FMAs).
 #include <cfloat>
 #include <cstdint>
 
@@ -55,35 +57,6 @@ __global__ void zero_counters(int* c, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) c[i] = 0;
 }
 
-// Stages rows [t0, t0 + n) of a [rows x W] matrix (row-major) as fp32 into `dst` ([TK][W]),
-// rows past n as zeros, with 16-byte loads (8 bf16 or 4 fp32 per load).
-template <typename TIn, int W>
-__device__ __forceinline__ void stage(float* dst, const TIn* src, int t0, int n) {
-  constexpr int EPL = 16 / (int)sizeof(TIn);  // elements per 16-byte load
-  constexpr int CPR = W / EPL;                // loads per row
-  for (int e = threadIdx.x; e < TK * CPR; e += NT) {
-    const int jj = e / CPR, c = e % CPR;
-    float* d = dst + jj * W + c * EPL;
-    if (jj < n) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + (long long)(t0 + jj) * W + c * EPL);
-      if constexpr (sizeof(TIn) == 2) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          d[2 * i] = __uint_as_float(w[i] << 16);
-          d[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-      } else {
-        d[0] = __uint_as_float(u.x); d[1] = __uint_as_float(u.y);
-        d[2] = __uint_as_float(u.z); d[3] = __uint_as_float(u.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) d[i] = 0.f;
-    }
-  }
-}
-
 // The running maximum of one tile: threads 0..TK-1 hold the logits of the tile's keys (-inf
 // past its end); returns max(m_run, tile max) to every thread (two block barriers inside).
 __device__ __forceinline__ float tile_max(float sj, float m_run, float* red) {
@@ -98,34 +71,8 @@ __device__ __forceinline__ float tile_max(float sj, float m_run, float* red) {
   return r;
 }
 
-// Logits q . k_j of the tile's keys (and, with a probe, r . k_j) into sS / sT (-inf past n):
-// one warp per key, the lanes splitting the D coordinates (conflict-free shared reads), then a
-// shuffle reduction.
-template <int D, bool PROBE>
-__device__ __forceinline__ void tile_logits(const float* kt, const float* qs, const float* rs,
-                                            int n, float* sS, float* sT) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int jj = warp; jj < TK; jj += NT / 32) {
-    float a = 0.f, b = 0.f;
-    if (jj < n) {
-#pragma unroll
-      for (int c = lane; c < D; c += 32) {
-        const float kv = kt[jj * D + c];
-        a = fmaf(qs[c], kv, a);
-        if (PROBE) b = fmaf(rs[c], kv, b);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (PROBE) b += __shfl_xor_sync(0xffffffffu, b, o);
-    }
-    if (lane == 0) {
-      sS[jj] = jj < n ? a : -INFINITY;
-      if (PROBE) sT[jj] = b;
-    }
-  }
-}
+__device__ __forceinline__ float tof(float x) { return x; }
+__device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // Two adjacent elements as fp32 (one 4- or 8-byte shared load).
 __device__ __forceinline__ void load_pair(const float* p, float (&x)[2]) {
@@ -172,7 +119,7 @@ __device__ __forceinline__ void load_row(const TIn* p, float (&x)[N]) {
 // Logits q . k_j and r . k_j of a tile kept in the input type (the Parallax decode's cp.async
 // ring) into sS / sT (-inf past n): four threads per key, each with a contiguous quarter of the
 // row, completed by two shuffles within the four.
-template <typename TIn, int D>
+template <typename TIn, int D, bool PROBE>
 __device__ __forceinline__ void tile_logits_raw(const TIn* kt, const float* qs, const float* rs,
                                                 int n, float* sS, float* sT) {
   static_assert(TK * 4 == NT, "four threads per key");
@@ -185,16 +132,18 @@ __device__ __forceinline__ void tile_logits_raw(const TIn* kt, const float* qs, 
 #pragma unroll
     for (int u = 0; u < SEG; ++u) {
       a = fmaf(qs[part * SEG + u], kv[u], a);
-      b = fmaf(rs[part * SEG + u], kv[u], b);
+      if (PROBE) b = fmaf(rs[part * SEG + u], kv[u], b);
     }
   }
   a += __shfl_xor_sync(0xffffffffu, a, 1);
-  b += __shfl_xor_sync(0xffffffffu, b, 1);
   a += __shfl_xor_sync(0xffffffffu, a, 2);
-  b += __shfl_xor_sync(0xffffffffu, b, 2);
+  if (PROBE) {
+    b += __shfl_xor_sync(0xffffffffu, b, 1);
+    b += __shfl_xor_sync(0xffffffffu, b, 2);
+  }
   if (part == 0) {
     sS[key] = key < n ? a : -INFINITY;
-    sT[key] = b;
+    if (PROBE) sT[key] = b;
   }
 }
 
@@ -214,6 +163,32 @@ constexpr int px_part() { return 3 + 2 * DV; }
 constexpr int PX_ST = 3;
 template <typename TIn, int D, int DV>
 constexpr size_t px_smem() { return (size_t)PX_ST * TK * (D + DV) * sizeof(TIn); }
+
+// Tile `it` of the chunk [j0, j1) of a head's cache (kb: [L, D], vb: [L, DV]) into slot
+// it % PX_ST of the raw rings (16-byte cp.async copies; rows past the chunk are zero-filled
+// without being read). One commit group per call, empty past the last tile, so that a thread's
+// cp.async.wait_group<PX_ST - 1> after prefetching tile it + PX_ST - 1 covers tile it.
+template <typename TIn, int D, int DV>
+__device__ __forceinline__ void prefetch_tile(TIn* kring, TIn* vring, const TIn* kb,
+                                              const TIn* vb, int j0, int j1, int it, int ntl) {
+  if (it < ntl) {
+    const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
+    constexpr int KR = D * (int)sizeof(TIn) / 16, VR = DV * (int)sizeof(TIn) / 16;
+    const char* ks = reinterpret_cast<const char*>(kb + (long long)t0 * D);
+    const char* vs = reinterpret_cast<const char*>(vb + (long long)t0 * DV);
+    char* kd = reinterpret_cast<char*>(kring + slot * TK * D);
+    char* vd = reinterpret_cast<char*>(vring + slot * TK * DV);
+    for (int e = threadIdx.x; e < TK * KR; e += NT) {
+      const bool in = e / KR < n;
+      cp_async16(kd + 16 * e, ks + (in ? 16 * e : 0), in ? 16u : 0u);
+    }
+    for (int e = threadIdx.x; e < TK * VR; e += NT) {
+      const bool in = e / VR < n;
+      cp_async16(vd + 16 * e, vs + (in ? 16 * e : 0), in ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+}
 
 template <typename TIn, int D, int DV>
 __global__ void __launch_bounds__(NT)
@@ -248,36 +223,15 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   float o1a = 0.f, o1b = 0.f, o2a = 0.f, o2b = 0.f;
   const int cp = tid % (DV / 2), og = tid / (DV / 2);
   const int ntl = j1 > j0 ? (j1 - j0 + TK - 1) / TK : 0;
-  // Tile `it` of the chunk into ring slot it % PX_ST (16-byte copies; rows past the chunk are
-  // zero-filled without being read). One commit group per tile, empty past the end.
-  auto prefetch = [&](int it) {
-    if (it < ntl) {
-      const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
-      constexpr int KR = D * (int)sizeof(TIn) / 16, VR = DV * (int)sizeof(TIn) / 16;
-      const char* ks = reinterpret_cast<const char*>(kb + (long long)t0 * D);
-      const char* vs = reinterpret_cast<const char*>(vb + (long long)t0 * DV);
-      char* kd = reinterpret_cast<char*>(kring + slot * TK * D);
-      char* vd = reinterpret_cast<char*>(vring + slot * TK * DV);
-      for (int e = tid; e < TK * KR; e += NT) {
-        const bool in = e / KR < n;
-        cp_async16(kd + 16 * e, ks + (in ? 16 * e : 0), in ? 16u : 0u);
-      }
-      for (int e = tid; e < TK * VR; e += NT) {
-        const bool in = e / VR < n;
-        cp_async16(vd + 16 * e, vs + (in ? 16 * e : 0), in ? 16u : 0u);
-      }
-    }
-    cp_async_commit();
-  };
-  for (int it = 0; it < PX_ST - 1; ++it) prefetch(it);
+  for (int it = 0; it < PX_ST - 1; ++it) prefetch_tile<TIn, D, DV>(kring, vring, kb, vb, j0, j1, it, ntl);
   for (int it = 0; it < ntl; ++it) {
     const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
-    prefetch(it + PX_ST - 1);
+    prefetch_tile<TIn, D, DV>(kring, vring, kb, vb, j0, j1, it + PX_ST - 1, ntl);
     cp_async_wait<PX_ST - 1>();  // this thread's copies of tile `it` have landed
     __syncthreads();             // ... and everyone else's
     const TIn* kt = kring + slot * TK * D;
     const TIn* vt = vring + slot * TK * DV;
-    tile_logits_raw<TIn, D>(kt, qs, rs, n, sS, sT);
+    tile_logits_raw<TIn, D, true>(kt, qs, rs, n, sS, sT);
     __syncthreads();
     const float sj = tid < TK ? sS[tid] : -INFINITY, tj = tid < TK ? sT[tid] : 0.f;
     const float mn = tile_max(sj, m, red);
@@ -361,13 +315,15 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
   constexpr int NBK = (D / 4) * (D / 4 + 1) / 2;   // upper-triangle 4 x 4 blocks of Skk
   constexpr int NB = NBK + (DV / 4) * (D / 4);      // then the blocks of Svk
   constexpr int TPB = (NB + NT - 1) / NT;           // blocks per thread
-  extern __shared__ float dsm[];
+  extern __shared__ __align__(16) float dsm[];
   __shared__ float qs[D], red[NT / 32], sS[TK];
   __shared__ int is_last, fail_s;
   float* kt = dsm;               // [TK][D]
   float* pk = kt + TK * D;       // [TK][D]: p_j k_j
-  float* pv = pk + TK * D;       // [TK][DV]: v_j, then p_j v_j
+  float* pv = pk + TK * D;       // [TK][DV]: p_j v_j
   float* pw = pv + TK * DV;      // [TK]: p_j
+  TIn* kring = reinterpret_cast<TIn*>(pw + TK);  // [PX_ST][TK * D] raw key tiles
+  TIn* vring = kring + PX_ST * TK * D;           // [PX_ST][TK * DV] raw value tiles
   const long long bh = blockIdx.x / S;
   const int s = blockIdx.x % S, tid = threadIdx.x;
   const int chunk = (L + S - 1) / S;
@@ -399,13 +355,18 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[u][e] = make_float2(0.f, 0.f);
   float m = -INFINITY, sk = 0.f, sv = 0.f, om = 0.f;  // thread a < D: sk[a]; then sv, omega
-  for (int t0 = j0; t0 < j1; t0 += TK) {
-    const int n = min(TK, j1 - t0);
-    __syncthreads();
-    stage<TIn, D>(kt, kb, t0, n);
-    stage<TIn, DV>(pv, vb, t0, n);
-    __syncthreads();
-    tile_logits<D, false>(kt, qs, nullptr, n, sS, nullptr);
+  // The chunk streams through the raw rings (cp.async, PX_ST - 1 tiles ahead), as in the
+  // Parallax decode; each tile is converted to fp32 (k, p k, p v) once its weights are known.
+  const int ntl = j1 > j0 ? (j1 - j0 + TK - 1) / TK : 0;
+  for (int it = 0; it < PX_ST - 1; ++it) prefetch_tile<TIn, D, DV>(kring, vring, kb, vb, j0, j1, it, ntl);
+  for (int it = 0; it < ntl; ++it) {
+    const int t0 = j0 + it * TK, n = min(TK, j1 - t0), slot = it % PX_ST;
+    prefetch_tile<TIn, D, DV>(kring, vring, kb, vb, j0, j1, it + PX_ST - 1, ntl);
+    cp_async_wait<PX_ST - 1>();
+    __syncthreads();  // tile `it` has landed; the previous tile's products are all read
+    const TIn* kr = kring + slot * TK * D;
+    const TIn* vr = vring + slot * TK * DV;
+    tile_logits_raw<TIn, D, false>(kr, qs, nullptr, n, sS, nullptr);
     __syncthreads();
     const float sj = tid < TK ? sS[tid] : -INFINITY;
     const float mn = tile_max(sj, m, red);
@@ -421,8 +382,12 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
       for (int e = 0; e < 8; ++e) acc[u][e] = __fmul2_rn(acc[u][e], sc2);
     if (tid < TK) pw[tid] = tid < n ? __expf((sj - m) * inv_h) : 0.f;
     __syncthreads();
-    for (int e = tid; e < TK * D; e += NT) pk[e] = pw[e / D] * kt[e];
-    for (int e = tid; e < TK * DV; e += NT) pv[e] *= pw[e / DV];
+    for (int e = tid; e < TK * D; e += NT) {
+      const float kv = tof(kr[e]);
+      kt[e] = kv;
+      pk[e] = pw[e / D] * kv;
+    }
+    for (int e = tid; e < TK * DV; e += NT) pv[e] = pw[e / DV] * tof(vr[e]);
     __syncthreads();
     if (tid < D) for (int jj = 0; jj < n; ++jj) sk += pk[jj * D + tid];
     else if (tid < D + DV) for (int jj = 0; jj < n; ++jj) sv += pv[jj * DV + tid - D];
@@ -448,7 +413,9 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
         }
       }
     }
+    (void)t0;
   }
+  cp_async_wait<0>();
   float* pp = part + blockIdx.x * (long long)P;
   if (tid == 0) pp[0] = m;
   if (tid < D) pp[2 + tid] = sk;
@@ -587,7 +554,7 @@ cudaError_t launch_ll(const DecodeArgs& a, void* ws, int* status, cudaStream_t s
   float* part = static_cast<float*>(ws);
   int* cnt = reinterpret_cast<int*>(part + a.BH() * S * lla_part<D, DV>());
   constexpr int P = lla_part<D, DV>();
-  const size_t tiles = sizeof(float) * (TK * D * 2 + TK * DV + TK);
+  const size_t tiles = sizeof(float) * (TK * D * 2 + TK * DV + TK) + px_smem<TIn, D, DV>();
   const size_t solve = sizeof(double) * (P + D + S);
   const size_t smem = tiles > solve ? tiles : solve;
   auto kern = lla_decode_kernel<TIn, D, DV>;
