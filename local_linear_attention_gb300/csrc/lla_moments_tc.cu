@@ -17,9 +17,11 @@
 //    are swept in 6 passes of 368 columns; each pass streams the key prefix again. A first sweep
 //    computes the exact row max m_i (Q K^T and a max); a second sweep computes P (bf16) and
 //    stores it to a scratch, from which every feature pass takes it again. Q K^T and the
-//    exponentials thus never wait behind a feature contraction in the tensor pipe.
-//  * Feature tiles are generated per key block into shared memory and read back by the MMA, so
-//    shared-memory traffic per SM bounds the stage. Two CTAs on two SMs (a cluster pair) therefore
+//    exponentials thus never wait behind a feature contraction in the tensor pipe. The sweeps
+//    run Q K^T on chunks of four key blocks (N = 128): a tcgen05.mma costs about as long at
+//    N = 32 as at N = 128.
+//  * Feature tiles are generated per key block into shared memory and read back by the MMA, a
+//    per-block cost on every SM. Two CTAs on two SMs (a cluster pair) therefore
 //    share every MMA (tcgen05 cta_group::2, M = 256): each CTA holds 128 query rows (its tensor
 //    memory lanes) and generates and holds half of every feature tile (the B operand is split
 //    N/2 + N/2 between the pair's shared memories), halving the feature work per SM.
@@ -31,8 +33,9 @@
 //
 // Warp roles per CTA (24 warps): 0 issues Q K^T (leader; one thread) and owns the TMEM
 // allocation; 22 and 23 issue the feature contraction (leader; one thread each, alternate key
-// blocks); 1 stages key blocks (32
-// keys x 64) into shared memory; 2-9 turn S into P (one thread per query = TMEM lane, two warps
+// blocks); in the peer CTA warp 0 relays its landed sweep blocks to the leader; 1 stages key
+// blocks (32 keys x 64) into shared memory (cp.async, completion counted on each stage's barrier,
+// every stage in flight); 2-9 turn S into P (one thread per query = TMEM lane, two warps
 // per lane quarter splitting the keys of a block), put P into tensor memory for each feature step
 // and drain the accumulators after each pass; 10-21 generate this CTA's half of the exact hi/lo
 // feature tiles (one lane per key; two groups of six warps take alternate key blocks). P has
@@ -69,8 +72,8 @@ constexpr int NFP = NPASS * NCH;            // 2208, padded feature count (row s
 constexpr int NA = 192, NB_ = NCH - NA;     // split of a pass into two MMAs (N <= 256)
 constexpr int GA = NA / 16, GB = NB_ / 16;  // 8-feature groups each CTA holds for either MMA
 constexpr int GLOC = GA + GB;               // 23 groups per CTA per pass
-constexpr int KS = 6;                       // key-tile pipeline stages
-constexpr int KLAG = KS - 2;                // key blocks the loader keeps in flight
+constexpr int SCH = 4;                      // key blocks per sweep chunk (one Q K^T of N = 128)
+constexpr int KS = 8;                       // key-tile pipeline stages (two sweep chunks)
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int NFG = 12;                     // feature-generation warps: two groups of NFGW that
 constexpr int NFGW = NFG / 2;               //   take alternate key blocks
@@ -78,21 +81,21 @@ constexpr int NWARPS = 4 + NSM + NFG;       // + Q K^T issuer, key loader, two f
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int NBUF = 7;                     // P buffers (tensor memory, feature passes only)
 constexpr int NFB = 5;                      // F buffers (shared memory)
-constexpr int NSB = 8;                      // S buffers (sweeps only)
+constexpr int NSC = 3;                      // S buffers of the sweeps (SCH blocks each)
 static_assert(BM == pscr::kRows && KB == pscr::kKeys && PM == 2 * BM, "weight scratch layout");
 
 // tensor-memory columns (the same in both CTAs of a pair)
 constexpr uint32_t T_ACC = 0;
 // The two sweeps and the feature passes use tensor memory at different times: the logits S of the
-// sweeps take the accumulator columns (idle until the first feature pass, which starts only after
-// the softmax warps have read the last S), so that Q K^T can run NSB blocks ahead of the softmax
-// warps; the weights P of the feature passes take NBUF buffers after the accumulators, so that a
-// step's weights can be in place several steps ahead of its MMAs.
-constexpr uint32_t T_S = T_ACC;             // NSB x 32 columns of fp32 logits (sweeps)
+// sweeps take the accumulator and weight columns (idle until the first feature pass, which starts
+// only after the softmax warps have read the last S), so that Q K^T can run NSC chunks ahead of
+// the softmax warps; the weights P of the feature passes take NBUF buffers after the
+// accumulators, so that a step's weights can be in place several steps ahead of its MMAs.
+constexpr uint32_t T_S = T_ACC;             // NSC x 128 columns of fp32 logits (sweeps)
 constexpr uint32_t T_P = NCH;               // NBUF x 16 columns of packed bf16 weights (passes)
 constexpr uint32_t T_Q = T_P + NBUF * (KB / 2);  // 32 columns: the Q tile, A operand of Q K^T
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(T_S + NSB * KB <= NCH, "S buffers within the accumulator columns");
+static_assert(T_S + NSC * SCH * KB <= T_Q, "sweep S buffers below the Q tile");
 static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
 
 // shared-memory layout (bytes; the same offsets in both CTAs of a pair)
@@ -134,6 +137,13 @@ __host__ __device__ constexpr PairSpec pair_spec(int p) {
   }
 }
 static_assert(2 * (kRowPairs + 16) == NFP, "feature order fills the padded row");
+
+// Arrives (without incrementing the expected count) on `bar` once every cp.async this thread has
+// issued so far has completed: a key stage's barrier expects one such arrival per loader lane.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t y) {
   uint32_t r;
@@ -241,9 +251,17 @@ __device__ __forceinline__ void generate(int pass, int rank, int fw, const uint3
   }
 }
 
-// Byte offset of 16-byte chunk c (elements 8c..8c+7) of row r in a K-major tile whose rows hold
-// D = 64 elements: core matrix (r / 8, c) of 128 bytes, row groups 1024 bytes apart.
-__device__ __forceinline__ int kmaj_off(int r, int c) { return (r >> 3) * 1024 + c * 128 + (r & 7) * 16; }
+// Byte offset, from the first key stage, of 16-byte chunk c (elements 8c..8c+7) of row r of key
+// stage st. Each stage is a K-major tile of 32 rows x 64 elements in 8-row groups of eight
+// 128-byte core matrices (chunks 128 bytes apart). The stages form chunks of SCH = 4 consecutive
+// stages (16 KiB), and within a chunk the row groups are ordered (rows 0..15 of stages 0..3, then
+// rows 16..31 of stages 0..3): the 16 rows that a CTA contributes to Q K^T from each of the 4
+// stages are then 8 row groups 1024 bytes apart, one N = 128 operand for the pair.
+__device__ __forceinline__ int kst_off(int st, int r, int c) {
+  return (st >> 2) * (SCH * K_STAGE) + (r >> 4) * (SCH * K_STAGE / 2) +
+         (2 * (st & 3) + ((r >> 3) & 1)) * 1024 + c * 128 + (r & 7) * 16;
+}
+static_assert(KS % SCH == 0 && SCH == 4 && K_STAGE == 4096, "key stage layout");
 
 // Wait executed by all 32 lanes of a warp; the outcome is made warp-uniform so that an abort seen
 // by one lane takes the whole warp out of its loop together.
@@ -258,8 +276,8 @@ struct Barriers {
   uint64_t kfull[KS];           // key block staged by this CTA's loader
   uint64_t kfull_peer[KS];      // (L) key block staged by the peer's loader (for Q K^T only)
   uint64_t kempty[KS];          // key stage consumed: (M) Q K^T commit or 1 extra arrival, + NFGW
-  uint64_t sfull[NSB];          // (M) S = Q K^T in tensor memory
-  uint64_t sfree[NSB];          // (L) S read by both CTAs' softmax warps
+  uint64_t sfull[NSC];          // (M) S = Q K^T of a sweep chunk in tensor memory
+  uint64_t sfree[NSC];          // (L) S read by both CTAs' softmax warps
   uint64_t pfull[NBUF];         // (L) P written to tensor memory in both CTAs
   uint64_t ffull[NFB];          // (L) F halves written in both CTAs
   uint64_t pfree[NBUF];         // (M) the feature MMAs of a step completed (P buffer free)
@@ -313,9 +331,11 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int nq = max(0, min(BM, T - i0));
   const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
   const int nb = (jend + KB - 1) / KB;
-  // key blocks streamed: max sweep, weight sweep, npass feature passes (NPASS for the moments, 0
-  // when only the weights, m and omega are wanted)
-  const int G = nb * (2 + npass);
+  // key blocks streamed: max sweep, weight sweep (each padded with zero blocks to nb4, whole
+  // chunks of SCH), npass feature passes (NPASS for the moments, 0 when only the weights, m and
+  // omega are wanted)
+  const int nb4 = (nb + SCH - 1) / SCH * SCH;
+  const int G = 2 * nb4 + npass * nb;
   const long long base = bh * T;
   // This CTA's P blocks in the scratch (layout: pscr:: in the internal header).
   uint4* const ptile_p = pimg + pscr::first_block(bh, T, ptile, rank) * (P_BLOCK / 16);
@@ -325,11 +345,11 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
-      mbar_init(&bar.kfull[s], 1);
+      mbar_init(&bar.kfull[s], 32);  // one cp.async completion arrival per loader lane
       mbar_init(&bar.kfull_peer[s], 1);
       mbar_init(&bar.kempty[s], 1 + NFGW);
     }
-    for (int s = 0; s < NSB; ++s) {
+    for (int s = 0; s < NSC; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 2 * NSM);
     }
@@ -372,35 +392,49 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // serial issue cost -- mbarrier tests, descriptor arithmetic and the MMA/commit instructions
     // -- exceeds the tensor work of a key block. tcgen05.commit tracks the issuing thread's own
     // MMAs, so each thread signals and drains its own. Q K^T runs only in the max and weight
-    // sweeps.
+    // sweeps, one chunk of SCH key blocks (N = 128) per MMA group: an MMA costs its issuer about
+    // as long at N = 32 as at N = 128.
     if (leader && lane == 0) {
       const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
-      constexpr uint32_t id_qk = idesc_bf16(PM, KB, false, false);
+      constexpr uint32_t id_qk = idesc_bf16(PM, SCH * KB, false, false);
       const uint32_t t_s = tbase + T_S, t_q = tbase + T_Q;
       bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);
-      int st = 0;
-      uint32_t kpar = 0;  // parity of the current fill of key stage st
-      for (int g = 0; g < 2 * nb && ok; ++g) {
-        const int sb = g % NSB;
-        ok = mbar_wait2(&bar.kfull[st], kpar, &bar.kfull_peer[st], kpar, status, TO, abort_p);
-        if (ok && g >= NSB)
-          ok = mbar_wait(&bar.sfree[sb], ((g / NSB) - 1) & 1, status, TO, abort_p);
+      const int nchunks = 2 * nb4 / SCH;
+      for (int u = 0; u < nchunks && ok; ++u) {
+        // chunk u: key blocks g = SCH u .. SCH u + 3 in stages st0 .. st0 + 3 (fill g / KS)
+        const int sb = u % NSC, st0 = (SCH * u) % KS;
+        const uint32_t kpar = (uint32_t)((SCH * u / KS) & 1);
+        for (int t = 0; t < SCH && ok; ++t)
+          ok = mbar_wait2(&bar.kfull[st0 + t], kpar, &bar.kfull_peer[st0 + t], kpar, status, TO,
+                          abort_p);
+        if (ok && u >= NSC)
+          ok = mbar_wait(&bar.sfree[sb], ((u / NSC) - 1) & 1, status, TO, abort_p);
         if (!ok) break;
         tc_fence_after();
+        fence_proxy_async_smem();  // the stages' cp.async writes, before the async-proxy reads
         // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
         // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
-        const uint64_t kst = kd + (uint64_t)(st * (K_STAGE >> 4));
-        const uint32_t ts = t_s + sb * KB;
+        const uint64_t kst = kd + (uint64_t)((st0 / SCH) * (SCH * K_STAGE >> 4));
+        const uint32_t ts = t_s + sb * (SCH * KB);
         mma2_ts(ts, t_q, kst, id_qk, 0u);
         mma2_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
         mma2_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
         mma2_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
         mma2_commit_both(&bar.sfull[sb]);
-        mma2_commit_both(&bar.kempty[st]);
-        if (++st == KS) { st = 0; kpar ^= 1; }
+        for (int t = 0; t < SCH; ++t) mma2_commit_both(&bar.kempty[st0 + t]);
       }
       if (!ok) *abort_p = 1;
       mma2_commit_both(&bar.done_qk);
+    } else if (!leader && lane == 0) {
+      // Relay (the peer CTA): the leader's Q K^T reads this CTA's half of every sweep block, so
+      // each landed block is fenced for the async proxy and reported to the leader. A stage is
+      // refilled only after the Q K^T that needs this report, so no phase is skipped.
+      for (int g = 0; g < 2 * nb4; ++g) {
+        const int st = g % KS;
+        if (!mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p)) break;
+        fence_proxy_async_smem();
+        mbar_arrive_cluster_relaxed(&bar.kfull_peer[st], 0);
+      }
     }
     __syncwarp();
   } else if (warp >= NWARPS - 2) {
@@ -459,45 +493,29 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
-    // cp.async 16-byte copies, several key blocks in flight. Lane -> (row, chunk) mapping:
+    // cp.async 16-byte copies, every stage in flight. Lane -> (row, chunk) mapping:
     // rows (lane & 7) + 8 * (t & 3), chunks (lane >> 3) + 4 * (t >> 2): each 8-lane phase writes
-    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors. A block becomes
-    // visible to the MMA (async proxy) only after its copies completed and this warp fenced them
-    // (cp.async writes belong to the generic proxy); the leader's Q K^T waits for both CTAs.
+    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors. Each lane's
+    // copies of a block complete on the stage's barrier (cp.async.mbarrier.arrive), so the loader
+    // never waits for its own copies; the consumers that read through the async proxy (Q K^T)
+    // fence after their wait (cp.async writes belong to the generic proxy).
     const __nv_bfloat16* kb = k + base * D;
-    bool ok = true;
-    for (int g = 0; g < G + KLAG; ++g) {
-      if (g < G) {
-        const int st = g % KS, b = g % nb;
-        if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
-        uint8_t* dst = smem + SM_K + st * K_STAGE;
+    for (int g = 0; g < G; ++g) {
+      const int st = g % KS;
+      const int b = g < 2 * nb4 ? g % nb4 : (g - 2 * nb4) % nb;  // sweep blocks >= nb: zeros
+      if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
+      uint8_t* dst = smem + SM_K;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
-          const int j = b * KB + (r ^ krot);
-          const bool in = j < jend;
-          cp_async16(dst + kmaj_off(r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
-        }
+      for (int t = 0; t < 8; ++t) {
+        const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+        const int j = b * KB + (r ^ krot);
+        const bool in = j < jend;
+        cp_async16(dst + kst_off(st, r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
       }
-      cp_async_commit();
-      if (g >= KLAG) {
-        cp_async_wait<KLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int s = (g - KLAG) % KS;
-          mbar_arrive(&bar.kfull[s]);
-          // The leader's Q K^T also reads this CTA's stage. Only steps that run Q K^T are
-          // reported: that barrier's waiter stops after them, and every refill before then
-          // waits for the Q K^T commit, so it never runs a phase ahead of its waiter.
-          if (!leader && g - KLAG < 2 * nb) mbar_arrive_cluster_relaxed(&bar.kfull_peer[s], 0);
-        }
-      }
+      cp_async_mbar_arrive(&bar.kfull[st]);
     }
-    if (!ok) cp_async_wait<0>();
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else if (warp < 2 + NSM) {
     // ------------------------------------------------------------------ softmax + epilogue
     // Two warps per TMEM lane quarter: `half` 0 takes key columns 0..15 of each block and
@@ -572,46 +590,57 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     };
     float m = -INFINITY, om = 0.f;
     bool ok = true;
-    for (int g = 0; g < 2 * nb; ++g) {
-      const int sb = g % NSB;
-      if (!warp_wait(&bar.sfull[sb], (g / NSB) & 1, status, abort_p)) { ok = false; break; }
+    // Sweep chunk u covers key blocks b0 .. b0 + SCH - 1. Column n of its S buffer holds key
+    // 16 (n / 64) + n % 16 of block (n % 64) / 16 (the pair's B operand: 64 rows from each CTA),
+    // so this thread's 16 logits of block b0 + t are columns 64 half + 16 t .. + 15.
+    for (int u = 0; u < 2 * nb4 / SCH && ok; ++u) {
+      const int sb = u % NSC;
+      if (!warp_wait(&bar.sfull[sb], (u / NSC) & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[KB / 2];
-      tmem_ld16(lane_base + T_S + sb * KB + c_lo, sv);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
-      const int b = g < nb ? g : g - nb;
-      const int j0 = b * KB + c_lo;
-      if (g < nb) {  // max sweep
-#pragma unroll
-        for (int c = 0; c < KB / 2; ++c)
-          if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
-        if (g == nb - 1) {  // combine the two halves' row maxima
-          bar.part[half][r] = m;
+      const bool max_sweep = SCH * u < nb4;
+      const int b0 = (SCH * u) % nb4;
+      for (int t = 0; t < SCH && ok; ++t) {
+        uint32_t sv[KB / 2];
+        tmem_ld16(lane_base + T_S + sb * (SCH * KB) + half * (SCH * KB / 2) + t * (KB / 2), sv);
+        tmem_ld_wait();
+        if (t == SCH - 1) {  // the chunk's S is read: the buffer is free
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar.rowx);
-          if (!warp_wait(&bar.rowx, 0, status, abort_p)) { ok = false; break; }
-          m = fmaxf(m, bar.part[half ^ 1][r]);
+          if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
         }
-        continue;
-      }
-      const float mc = m * c2;
-      uint32_t pw[KB / 4];
+        const int b = b0 + t;
+        if (b >= nb) continue;  // padding block of the chunk
+        const int j0 = b * KB + c_lo;
+        if (max_sweep) {
 #pragma unroll
-      for (int c = 0; c < KB / 2; c += 2) {
-        const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
-        const float p1 =
-            (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
-        pw[c / 2] = pack_bf16(p0, p1);
-        om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
+          for (int c = 0; c < KB / 2; ++c)
+            if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+          if (b == nb - 1) {  // combine the two halves' row maxima
+            bar.part[half][r] = m;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.rowx);
+            if (!warp_wait(&bar.rowx, 0, status, abort_p)) { ok = false; break; }
+            m = fmaxf(m, bar.part[half ^ 1][r]);
+          }
+          continue;
+        }
+        const float mc = m * c2;
+        uint32_t pw[KB / 4];
+#pragma unroll
+        for (int c = 0; c < KB / 2; c += 2) {
+          const float p0 =
+              (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+          const float p1 =
+              (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+          pw[c / 2] = pack_bf16(p0, p1);
+          om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
+        }
+        // This row's 16 weights as chunks 2*half and 2*half + 1 of the block's image.
+        constexpr int kChunk = 2048 / 16;  // chunk stride of the image, in 16-byte units
+        uint4* pdst = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
+        pdst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        pdst[kChunk] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
       }
-      // This row's 16 weights as chunks 2*half and 2*half + 1 of the block's image.
-      constexpr int kChunk = 2048 / 16;  // chunk stride of the image, in 16-byte units
-      uint4* pdst = ptile_p + (long long)b * (P_BLOCK / 16) + (2 * half) * kChunk + r;
-      pdst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      pdst[kChunk] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
     }
     {
       // This thread's weights of feature step h (block h % nb; the weight sweep stored them:
@@ -670,21 +699,21 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // products, the proxy fence).
     const int fwi = warp - 2 - NSM, grp = fwi / NFGW, fw = fwi % NFGW;
     const int row_off = (lane >> 3) * 128 + (lane & 7) * 16;  // key `lane` in the F tiles
-    int st = grp, h = grp - 2 * nb, pass = -1, bcnt = 0;
+    int st = grp, h = grp - 2 * nb4, pass = -1, bcnt = 0;
     uint32_t kpar = 0;
     for (int g = grp; g < G; g += 2) {
       if (!warp_wait(&bar.kfull[st], kpar, status, abort_p)) break;
-      if (g < 2 * nb) {  // max and weight sweeps: nothing to generate
+      if (g < 2 * nb4) {  // max and weight sweeps: nothing to generate
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.kempty[st]);
       } else {
         if (pass < 0) { pass = h / nb; bcnt = h % nb; }  // this group's first feature step
         const int fb = h % NFB;
         uint32_t kw[33];
-        const uint8_t* krow = smem + SM_K + st * K_STAGE;
+        const uint8_t* kst = smem + SM_K;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(krow + kmaj_off(lane ^ krot, c));
+          const uint4 v = *reinterpret_cast<const uint4*>(kst + kst_off(st, lane ^ krot, c));
           kw[4 * c] = v.x; kw[4 * c + 1] = v.y; kw[4 * c + 2] = v.z; kw[4 * c + 3] = v.w;
         }
         kw[32] = 0x00003F80u;  // bf16 one (constant feature) and zero (padding)
