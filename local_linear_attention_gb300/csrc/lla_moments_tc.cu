@@ -73,7 +73,7 @@ constexpr int NA = 192, NB_ = NCH - NA;     // split of a pass into two MMAs (N 
 constexpr int GA = NA / 16, GB = NB_ / 16;  // 8-feature groups each CTA holds for either MMA
 constexpr int GLOC = GA + GB;               // 23 groups per CTA per pass
 constexpr int SCH = 4;                      // key blocks per sweep chunk (one Q K^T of N = 128)
-constexpr int KS = 8;                       // key-tile pipeline stages (two sweep chunks)
+constexpr int KS = 12;                      // key-tile pipeline stages (three sweep chunks)
 constexpr int NSM = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int NFG = 12;                     // feature-generation warps: two groups of NFGW that
 constexpr int NFGW = NFG / 2;               //   take alternate key blocks
@@ -113,7 +113,7 @@ constexpr int SM_EPI = SM_F + NFB * F_BUF;           // NSM x (32 rows x 36 floa
 // Feature passes take each thread's weights back from the global scratch PD key blocks ahead of
 // use (a per-thread ring in shared memory filled with cp.async): the scratch does
 // not fit L2, and one block of look-ahead (~740 cycles of tensor work) is shorter than a DRAM miss.
-constexpr int PD = 4;
+constexpr int PD = 3;
 constexpr int SM_PR = SM_EPI + NSM * 32 * EPI_LD * 4;  // NSM x PD x 32 lanes x 32 bytes
 constexpr int SM_BAR = SM_PR + NSM * PD * 32 * 32;
 constexpr int SMEM_BYTES = SM_BAR + 2048;
