@@ -138,13 +138,6 @@ __host__ __device__ constexpr PairSpec pair_spec(int p) {
 }
 static_assert(2 * (kRowPairs + 16) == NFP, "feature order fills the padded row");
 
-// Arrives (without incrementing the expected count) on `bar` once every cp.async this thread has
-// issued so far has completed: a key stage's barrier expects one such arrival per loader lane.
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t x, uint32_t y) {
   uint32_t r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));

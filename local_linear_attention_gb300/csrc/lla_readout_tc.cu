@@ -50,7 +50,6 @@ constexpr int DV = 64;
 constexpr int BM = 128;                 // query rows per CTA = TMEM lanes
 constexpr int CK = 64;                  // keys per chunk
 constexpr int KS = 5;                   // chunk pipeline stages
-constexpr int KLAG = KS - 2;            // chunks the loader keeps in flight
 constexpr int NWARPS = 7;
 constexpr int NTHREADS = NWARPS * 32;
 static_assert(BM == pscr::kRows && CK == 2 * pscr::kKeys, "a chunk is two weight images");
@@ -139,7 +138,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   cp_async_wait<0>();
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
-      mbar_init(&bar.kvfull[s], 1);
+      mbar_init(&bar.kvfull[s], 32);  // one cp.async completion arrival per loader lane
       mbar_init(&bar.kvempty[s], 1);
       mbar_init(&bar.pfull[s], 1);
     }
@@ -183,6 +182,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           ok = mbar_wait(&bar.tfree[tb], ((c >> 1) - 1) & 1, status, kStatusTimeout, abort_p);
         if (!ok) break;
         tc_fence_after();
+        fence_proxy_async_smem();  // the stage's cp.async writes, before the async-proxy reads
         const uint64_t kst = kd + (uint64_t)(st * stage16);
         const uint32_t tt = tbase + T_T + tb * CK;
 #pragma unroll
@@ -213,6 +213,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
              mbar_wait(&bar.pfull[st], (c / KS) & 1, status, kStatusTimeout, abort_p);
         if (!ok) break;
         tc_fence_after();
+        fence_proxy_async_smem();
         const uint64_t vst = vd + (uint64_t)(st * stage16);
         const uint64_t pst = pd + (uint64_t)(st * stage16);
 #pragma unroll
@@ -235,22 +236,18 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V/P loader
-    // K and V: cp.async copies with several chunks in flight, rows to the core-matrix layout (lane
-    // -> (row, 16-byte chunk) mapping conflict-free per 8-lane phase); they become visible to the
-    // MMAs (async proxy) only after the copies completed and this warp fenced them (kvfull). The
-    // two weight images are one contiguous bulk copy into the stage as they are (pfull, counted
-    // in transaction bytes); a missing second image (past the pair's last block) is zero-filled
-    // with ordinary stores, fenced, before the stage's kvfull arrival.
+    // K and V: cp.async copies, every stage in flight, rows to the core-matrix layout (lane ->
+    // (row, 16-byte chunk) mapping conflict-free per 8-lane phase); each lane's copies of a chunk
+    // complete on the stage's barrier (cp.async.mbarrier.arrive, kvfull), and the MMA issuers
+    // fence the async proxy after their wait. The two weight images are one contiguous bulk copy
+    // into the stage as they are (pfull, counted in transaction bytes); a missing second image
+    // (past the pair's last block) is zero-filled by cp.async copies that read nothing.
     const __nv_bfloat16* kbp = k + base * D;
     const __nv_bfloat16* vbp = v + base * DV;
-    bool ok = true;
-    for (int c = 0; c < nck + KLAG; ++c) {
-      if (c < nck) {
+    for (int c = 0; c < nck; ++c) {
+      {
         const int st = c % KS;
-        if (c >= KS && !warp_wait(&bar.kvempty[st], ((c / KS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
+        if (c >= KS && !warp_wait(&bar.kvempty[st], ((c / KS) - 1) & 1, status, abort_p)) break;
         uint8_t* kdst = smem + SM_ST + st * STAGE;
         uint8_t* vdst = kdst + KV_BYTES;
         uint8_t* pdst = kdst + 2 * KV_BYTES;
@@ -267,8 +264,9 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
         if (have < 2) {
 #pragma unroll
           for (int t = 0; t < pscr::kBlockBytes / 16 / 32; ++t)
-            reinterpret_cast<uint4*>(pdst + pscr::kBlockBytes)[t * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
+            cp_async16(pdst + pscr::kBlockBytes + 16 * (t * 32 + lane), pt, 0u);
         }
+        cp_async_mbar_arrive(&bar.kvfull[st]);
         __syncwarp();
         if (lane == 0) {
           const uint32_t bytes = (uint32_t)have * pscr::kBlockBytes;
@@ -276,15 +274,9 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
           bulk_g2s(pdst, pt + (long long)2 * c * (pscr::kBlockBytes / 16), bytes, &bar.pfull[st]);
         }
       }
-      cp_async_commit();
-      if (c >= KLAG) {
-        cp_async_wait<KLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.kvfull[(c - KLAG) % KS]);
-      }
     }
-    if (!ok) cp_async_wait<0>();
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else {
     // ------------------------------------------------------------------ weights + output
     const int quarter = warp & 3;

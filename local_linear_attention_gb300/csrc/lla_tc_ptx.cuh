@@ -105,6 +105,13 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Arrives (without incrementing the expected count) on `bar` once every cp.async this thread has
+// issued so far has completed: a barrier that counts a stage's copies expects one such arrival
+// per copying thread.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 // One-dimensional bulk copy (the TMA engine) of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global to this CTA's shared memory; completion is counted on `bar` as `bytes`
 // transaction bytes.
