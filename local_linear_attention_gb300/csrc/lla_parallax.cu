@@ -34,7 +34,6 @@ constexpr int DV = 64;
 constexpr int BM = 128;
 constexpr int KB = 32;
 constexpr int KS = 6;
-constexpr int KLAG = KS - 2;
 constexpr int NWARPS = 6;
 constexpr int NTHREADS = NWARPS * 32;
 
@@ -124,7 +123,7 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     *reinterpret_cast<uint4*>(smem + (which ? SM_R : SM_Q) + kmaj_off(r, c)) = val;
   }
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 32); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 4);
@@ -172,6 +171,7 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                       : mbar_wait(&bar.kvfull[st], kpar, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
+          fence_proxy_async_smem();  // the stage's cp.async writes, before the async-proxy reads
           const uint64_t kst = kd + (uint64_t)(st * stage16);
           const uint32_t ts = tbase + T_S + sb * KB, tt = tbase + T_T + sb * KB;
 #pragma unroll
@@ -211,18 +211,15 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V loader
-    // cp.async copies with several blocks in flight (same conflict-free lane mapping and
-    // completion -> proxy fence -> arrive protocol as the LLA stages); V only in the main sweep.
+    // cp.async copies, every stage in flight (same conflict-free lane mapping as the LLA stages;
+    // each lane's copies of a block complete on the stage's barrier, and the MMA issuer fences
+    // the async proxy after its wait); V only in the main sweep.
     const __nv_bfloat16* kbp = k + base * D;
     const __nv_bfloat16* vbp = v + base * DV;
-    bool ok = true;
-    for (int g = 0; g < 2 * nb + KLAG; ++g) {
-      if (g < 2 * nb) {
+    for (int g = 0; g < 2 * nb; ++g) {
+      {
         const int st = g % KS, b = g < nb ? g : g - nb;
-        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
+        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
         uint8_t* kdst = smem + SM_K + st * KV_STAGE;
         uint8_t* vdst = smem + SM_V + st * KV_STAGE;
 #pragma unroll
@@ -234,16 +231,11 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           cp_async16(kdst + kmaj_off(r, c), kbp + jj * D + c * 8, in ? 16u : 0u);
           if (g >= nb) cp_async16(vdst + kmaj_off(r, c), vbp + jj * DV + c * 8, in ? 16u : 0u);
         }
-      }
-      cp_async_commit();
-      if (g >= KLAG) {
-        cp_async_wait<KLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.kvfull[(g - KLAG) % KS]);
+        cp_async_mbar_arrive(&bar.kvfull[st]);  // this lane's copies of the block, on completion
       }
     }
-    if (!ok) cp_async_wait<0>();
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else {
     // ------------------------------------------------------------------ weights + output
     const int quarter = warp & 3;

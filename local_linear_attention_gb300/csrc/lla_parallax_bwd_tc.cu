@@ -36,7 +36,6 @@ constexpr int D = 64;
 constexpr int BM = 128;  // rows of the resident tile (queries or keys)
 constexpr int BB = 32;   // rows of a streamed block (keys or queries)
 constexpr int KS = 6;
-constexpr int KLAG = KS - 2;
 constexpr int NWARPS = 6;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int TILE = BM * D * 2;     // 16 KiB
@@ -124,7 +123,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   load_tile(smem + SM_R, rp, base + i0, nq, tid);
   load_tile(smem + SM_Y, dout, base + i0, nq, tid);
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 32); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 4);
@@ -173,6 +172,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                       : mbar_wait(&bar.kvfull[st], kpar, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
+          fence_proxy_async_smem();  // the stage's cp.async writes, before the async-proxy reads
           const uint64_t kst = kd + (uint64_t)(st * stage16), vst = vd + (uint64_t)(st * stage16);
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
@@ -209,27 +209,18 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K / V loader
-    bool ok = true;
-    for (int g = 0; g < nb + KLAG; ++g) {
-      if (g < nb) {
+    for (int g = 0; g < nb; ++g) {
+      {
         const int st = g % KS;
-        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
+        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
         const int nrows = min(BB, jend - g * BB);
         stage_block(smem + SM_K + st * STAGE, k, base + g * BB, nrows, lane);
         stage_block(smem + SM_V + st * STAGE, v, base + g * BB, nrows, lane);
-      }
-      cp_async_commit();
-      if (g >= KLAG) {
-        cp_async_wait<KLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.kvfull[(g - KLAG) % KS]);
+        cp_async_mbar_arrive(&bar.kvfull[st]);  // this lane's copies of the block, on completion
       }
     }
-    if (!ok) cp_async_wait<0>();
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else {
     // ------------------------------------------------------------------ dS, dT and the output
     const int quarter = warp & 3;
@@ -369,7 +360,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   load_tile(smem + SM_K, k, base + j0, nk, tid);
   load_tile(smem + SM_V, v, base + j0, nk, tid);
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.qfull[s], 1); mbar_init(&bar.qempty[s], 1); }
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.qfull[s], 32); mbar_init(&bar.qempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 4);
@@ -420,6 +411,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                       : mbar_wait(&bar.qfull[st], qpar, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
+          fence_proxy_async_smem();  // the stage's cp.async writes, before the async-proxy reads
           const uint64_t o = (uint64_t)(st * stage16);
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
@@ -457,14 +449,10 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ Q / R / dO / record loader
-    bool ok = true;
-    for (int g = 0; g < nblk + KLAG; ++g) {
-      if (g < nblk) {
+    for (int g = 0; g < nblk; ++g) {
+      {
         const int st = g % KS;
-        if (g >= KS && !warp_wait(&bar.qempty[st], ((g / KS) - 1) & 1, status, abort_p)) {
-          ok = false;
-          break;
-        }
+        if (g >= KS && !warp_wait(&bar.qempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
         const int r0 = (qb0 + g) * BB;
         const int nrows = min(BB, T - r0);
         stage_block(smem + SM_QS + st * STAGE, q, base + r0, nrows, lane);
@@ -479,16 +467,11 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           cp_async16(sdst + rr * STAT + 4 * half4,
                      stats + (base + (in ? r0 + rr : 0)) * STAT + 4 * half4, in ? 16u : 0u);
         }
-      }
-      cp_async_commit();
-      if (g >= KLAG) {
-        cp_async_wait<KLAG>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.qfull[(g - KLAG) % KS]);
+        cp_async_mbar_arrive(&bar.qfull[st]);  // this lane's copies of the block, on completion
       }
     }
-    if (!ok) cp_async_wait<0>();
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else {
     // ------------------------------------------------------------------ dS^T, dT^T, A^T, output
     const int quarter = warp & 3;
