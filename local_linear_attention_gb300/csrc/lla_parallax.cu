@@ -83,6 +83,7 @@ struct Barriers {
   uint64_t pfull[2], pfree[2];
   uint64_t accfull, done;
 };
+static_assert(sizeof(Barriers) <= SMEM_BYTES - SM_BAR, "barrier region");
 
 // Steps g = 0 .. nb-1 are the max sweep (Q K^T only), g = nb .. 2nb-1 the main sweep over the
 // same key blocks b = g - nb.
