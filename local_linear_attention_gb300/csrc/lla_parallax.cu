@@ -6,7 +6,9 @@
 // (the combination printed in the blog's Appendix C). Both branches stream the same K/V blocks.
 //
 // Two implementations:
-//  * tensor cores (bf16, d = dv = 64): one CTA per 128-query tile. A first sweep over the causal
+//  * tensor cores (bf16, d = dv = 64): one CTA per 128-query tile, keys in blocks of 64 (so that
+//    Q K^T and R K^T are N = 64 MMAs: a tcgen05.mma costs about as long at N = 32). A first
+//    sweep over the causal
 //    prefix takes the exact row max of Q K^T (so no running rescale of the accumulators is
 //    needed); the second sweep computes S1 = Q K^T and S2 = R K^T with tcgen05.mma (Q, R and K
 //    from shared memory), turns them into P1 (bf16) and P2 = P1 .* S2 (an exact-to-16-bits bf16
@@ -32,7 +34,7 @@ namespace ptc {
 constexpr int D = 64;
 constexpr int DV = 64;
 constexpr int BM = 128;
-constexpr int KB = 32;
+constexpr int KB = 64;  // keys per block: N = 64 for Q K^T and R K^T
 constexpr int KS = 6;
 constexpr int NWARPS = 6;
 constexpr int NTHREADS = NWARPS * 32;
@@ -40,11 +42,11 @@ constexpr int NTHREADS = NWARPS * 32;
 // tensor-memory columns
 constexpr uint32_t T_O1 = 0;     // 64 fp32: P1 V
 constexpr uint32_t T_O2 = 64;    // 64 fp32: P2 V
-constexpr uint32_t T_S = 128;    // 2 x 32 fp32: Q K^T
-constexpr uint32_t T_T = 192;    // 2 x 32 fp32: R K^T
-constexpr uint32_t T_P = 256;    // 2 x 16: bf16 P1
-constexpr uint32_t T_P2H = 288;  // 2 x 16: bf16 hi part of P2
-constexpr uint32_t T_P2L = 320;  // 2 x 16: bf16 lo part of P2
+constexpr uint32_t T_S = 128;    // 2 x 64 fp32: Q K^T
+constexpr uint32_t T_T = 256;    // 2 x 64 fp32: R K^T
+constexpr uint32_t T_P = 384;    // 32: bf16 P1 (one buffer: the next block's is written once the
+constexpr uint32_t T_P2H = 416;  // 32: bf16 hi part of P2    previous block's P V MMAs completed)
+constexpr uint32_t T_P2L = 448;  // 32: bf16 lo part of P2
 constexpr uint32_t TMEM_COLS = 512;
 
 // shared memory (bytes)
@@ -52,7 +54,7 @@ constexpr int TILE = BM * D * 2;  // 128 x 64 bf16 = 16 KiB
 constexpr int SM_Q = 0;
 constexpr int SM_R = SM_Q + TILE;
 constexpr int SM_K = SM_R + TILE;
-constexpr int KV_STAGE = KB * D * 2;  // 4 KiB
+constexpr int KV_STAGE = KB * D * 2;  // 8 KiB
 constexpr int SM_V = SM_K + KS * KV_STAGE;
 constexpr int SM_BAR = SM_V + KS * KV_STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 256;
@@ -80,7 +82,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* s
 struct Barriers {
   uint64_t kvfull[KS], kvempty[KS];
   uint64_t sfull[2], sfree[2];
-  uint64_t pfull[2], pfree[2];
+  uint64_t pfull, pfree;
   uint64_t accfull, done;
 };
 static_assert(sizeof(Barriers) <= SMEM_BYTES - SM_BAR, "barrier region");
@@ -128,9 +130,10 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 4);
-      mbar_init(&bar.pfull[s], 4);
-      mbar_init(&bar.pfree[s], 1);
+
     }
+    mbar_init(&bar.pfull, 4);
+    mbar_init(&bar.pfree, 1);
     mbar_init(&bar.accfull, 1);
     mbar_init(&bar.done, 1);
     abort_flag = 0;
@@ -186,8 +189,8 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           if (++st == KS) { st = 0; kpar ^= 1; }
         }
         if (g >= nb + 1) {
-          const int h = g - 1 - nb, pb = h & 1, sth = (h + nb) % KS;
-          ok = mbar_wait(&bar.pfull[pb], (h >> 1) & 1, status, TO, abort_p);
+          const int h = g - 1 - nb, sth = (h + nb) % KS;
+          ok = mbar_wait(&bar.pfull, h & 1, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
           const uint64_t vst = vd + (uint64_t)(sth * stage16);
@@ -195,11 +198,11 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           for (int s = 0; s < KB / 16; ++s) {
             const uint64_t vds = vst + (uint64_t)(s * (2048 >> 4));
             const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_O1, tbase + T_P + pb * 16 + s * 8, vds, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2H + pb * 16 + s * 8, vds, id_o, acc);
-            mma_ts(tbase + T_O2, tbase + T_P2L + pb * 16 + s * 8, vds, id_o, 1u);
+            mma_ts(tbase + T_O1, tbase + T_P + s * 8, vds, id_o, acc);
+            mma_ts(tbase + T_O2, tbase + T_P2H + s * 8, vds, id_o, acc);
+            mma_ts(tbase + T_O2, tbase + T_P2L + s * 8, vds, id_o, 1u);
           }
-          mma_commit(&bar.pfree[pb]);
+          mma_commit(&bar.pfree);
           mma_commit(&bar.kvempty[sth]);
           if (h == nb - 1) mma_commit(&bar.accfull);
         }
@@ -224,8 +227,8 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         uint8_t* kdst = smem + SM_K + st * KV_STAGE;
         uint8_t* vdst = smem + SM_V + st * KV_STAGE;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+        for (int t = 0; t < 16; ++t) {
+          const int r = (lane & 7) + 8 * (t & 7), c = (lane >> 3) + 4 * (t >> 3);
           const int j = b * KB + r;
           const bool in = j < jend;
           const long long jj = in ? j : 0;
@@ -250,56 +253,71 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       const int sb = g & 1;
       if (!warp_wait(&bar.sfull[sb], (g >> 1) & 1, status, abort_p)) break;
       tc_fence_after();
-      uint32_t sv[KB], tv[KB];
-      tmem_ld16(lane_base + T_S + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-      tmem_ld16(lane_base + T_S + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
-      if (g >= nb) {
-        tmem_ld16(lane_base + T_T + sb * KB, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
-        tmem_ld16(lane_base + T_T + sb * KB + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
-      if (g < nb) {  // max sweep
-        const int j0 = g * KB;
-#pragma unroll
-        for (int c = 0; c < KB; ++c)
-          if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
-        continue;
-      }
-      const int h = g - nb, j0 = h * KB;
+      const bool main_sweep = g >= nb;
+      const int h = g - nb;
       const float mc = m * c2;
-      uint32_t pw[KB / 2], hw[KB / 2], lw[KB / 2];
+      bool ok2 = true;
+      // The block's 64 logits in two halves of 32 columns (to bound the registers); the S / T
+      // buffer is released once the second half is read. The weights of the first half are
+      // formed before waiting for the previous block's P V MMAs (one P buffer).
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[32], tv[32];
+        tmem_ld16(lane_base + T_S + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+        tmem_ld16(lane_base + T_S + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+        if (main_sweep) {
+          tmem_ld16(lane_base + T_T + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
+          tmem_ld16(lane_base + T_T + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
+        }
+        tmem_ld_wait();
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.sfree[sb]);
+        }
+        const int jb = (main_sweep ? h : g) * KB + 32 * hf;
+        if (!main_sweep) {  // max sweep
 #pragma unroll
-      for (int c = 0; c < KB; c += 2) {
-        const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
-        const float p1 =
-            (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
-        const uint32_t w = pack_bf16(p0, p1);
-        pw[c / 2] = w;
-        const float r0 = bf16_lo(w), r1 = bf16_hi(w);
-        d1 += r0 + r1;
-        const float q0 = r0 * __uint_as_float(tv[c]);
-        const float q1 = r1 * __uint_as_float(tv[c + 1]);
-        d2 += q0 + q1;
-        const uint32_t hh = pack_bf16(q0, q1);
-        hw[c / 2] = hh;
-        lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+          for (int c = 0; c < 32; ++c)
+            if (valid && jb + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+          continue;
+        }
+        uint32_t pw[16], hw[16], lw[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = (valid && jb + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+          const float p1 =
+              (valid && jb + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+          const uint32_t w = pack_bf16(p0, p1);
+          pw[c / 2] = w;
+          const float r0 = bf16_lo(w), r1 = bf16_hi(w);
+          d1 += r0 + r1;
+          const float q0 = r0 * __uint_as_float(tv[c]);
+          const float q1 = r1 * __uint_as_float(tv[c + 1]);
+          d2 += q0 + q1;
+          const uint32_t hh = pack_bf16(q0, q1);
+          hw[c / 2] = hh;
+          lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+        }
+        if (hf == 0) {
+          if (h >= 1 && !warp_wait(&bar.pfree, (h - 1) & 1, status, abort_p)) {
+            ok2 = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st8(lane_base + T_P + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
+        tmem_st8(lane_base + T_P + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
+        tmem_st8(lane_base + T_P2H + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&hw[0]));
+        tmem_st8(lane_base + T_P2H + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&hw[8]));
+        tmem_st8(lane_base + T_P2L + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&lw[0]));
+        tmem_st8(lane_base + T_P2L + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&lw[8]));
       }
-      const int pb = h & 1;
-      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) break;
-      tc_fence_after();
-      tmem_st8(lane_base + T_P + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
-      tmem_st8(lane_base + T_P + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
-      tmem_st8(lane_base + T_P2H + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&hw[0]));
-      tmem_st8(lane_base + T_P2H + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&hw[8]));
-      tmem_st8(lane_base + T_P2L + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&lw[0]));
-      tmem_st8(lane_base + T_P2L + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&lw[8]));
+      if (!ok2) break;
+      if (!main_sweep) continue;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.pfull[pb]);
+      if (lane == 0) mbar_arrive(&bar.pfull);
       if (h == nb - 1) {
         if (!warp_wait(&bar.accfull, 0, status, abort_p)) break;
         tc_fence_after();
