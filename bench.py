@@ -416,7 +416,8 @@ def run_parallax(args, w, cpu, world, rank):
     return 0
 
 
-METRIC_PX_BWD = "Parallax backward queries/sec and TFLOP/s on 1 GB300; fraction of FP32 FMA peak"
+METRIC_PX_BWD = ("Parallax backward queries/sec and TFLOP/s on 1 GB300; fraction of the bf16 tensor "
+                 "peak (FP32 FMA peak on the CUDA-core path)")
 
 
 def parallax_bwd_flops_per_pair(d: int, dv: int):

@@ -34,12 +34,12 @@ using namespace tc;
 
 constexpr int D = 64;
 constexpr int BM = 128;  // rows of the resident tile (queries or keys)
-constexpr int BB = 32;   // rows of a streamed block (keys or queries)
+constexpr int BB = 64;   // rows of a streamed block (keys or queries): N = 64 score MMAs
 constexpr int KS = 6;
 constexpr int NWARPS = 6;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int TILE = BM * D * 2;     // 16 KiB
-constexpr int STAGE = BB * D * 2;    // 4 KiB
+constexpr int STAGE = BB * D * 2;    // 8 KiB
 constexpr int STAT = 8;              // floats per row record
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -70,13 +70,14 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const __nv_bfloat16* src
   }
 }
 
-// 32 rows (r0 + row < rend, else zeros) of a [., 64] bf16 tensor into a K-major stage, by one warp:
+// BB rows (row < nrows, else zeros) of a [., 64] bf16 tensor into a K-major stage, by one warp:
 // lane -> (row, chunk) as in the other stages (each 8-lane phase writes 8 distinct bank groups).
 __device__ __forceinline__ void stage_block(uint8_t* dst, const __nv_bfloat16* src, long long r0,
                                             int nrows, int lane) {
+  static_assert(BB == 64, "lane mapping for 64-row blocks");
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+  for (int t = 0; t < 16; ++t) {
+    const int r = (lane & 7) + 8 * (t & 7), c = (lane >> 3) + 4 * (t >> 3);
     const bool in = r < nrows;
     cp_async16(dst + kmaj_off(r, c), src + (in ? r0 + r : 0) * D + c * 8, in ? 16u : 0u);
   }
@@ -84,13 +85,14 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, const __nv_bfloat16* s
 
 // ============================================================================ rows: dQ, dR
 namespace rows {
-constexpr uint32_t T_S = 0, T_T = 64, T_G = 128;  // 2 x 32 fp32 each
-constexpr uint32_t T_DS = 192, T_DT = 224;        // 2 x 16 (packed bf16) each
-constexpr uint32_t T_DQ = 256, T_DR = 320;        // 64 fp32 each
+constexpr uint32_t T_S = 0, T_T = 64, T_G = 128;  // 64 fp32 each (one buffer)
+constexpr uint32_t T_DS = 192, T_DT = 256;        // 2 x 32 (packed bf16) each
+constexpr uint32_t T_DQ = 320, T_DR = 384;        // 64 fp32 each
 constexpr int SM_Q = 0, SM_R = SM_Q + TILE, SM_Y = SM_R + TILE;
 constexpr int SM_K = SM_Y + TILE, SM_V = SM_K + KS * STAGE;
 constexpr int SM_BAR = SM_V + KS * STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Barriers {
   uint64_t kvfull[KS], kvempty[KS];
@@ -166,9 +168,9 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       uint32_t kpar = 0;
       for (int g = 0; g <= nb && ok; ++g) {
         if (g < nb) {
-          const int sb = g & 1;
-          ok = g >= 2 ? mbar_wait2(&bar.kvfull[st], kpar, &bar.sfree[sb], ((g >> 1) - 1) & 1,
-                                   status, TO, abort_p)
+          // one S / T / G buffer: free once the previous block's scores were read
+          ok = g >= 1 ? mbar_wait2(&bar.kvfull[st], kpar, &bar.sfree[0], (g - 1) & 1, status, TO,
+                                   abort_p)
                       : mbar_wait(&bar.kvfull[st], kpar, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
@@ -176,11 +178,11 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           const uint64_t kst = kd + (uint64_t)(st * stage16), vst = vd + (uint64_t)(st * stage16);
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
-            mma_ss(tbase + T_S + sb * BB, qd + 16 * s, kst + 16 * s, id_s, s > 0);
-            mma_ss(tbase + T_T + sb * BB, rd + 16 * s, kst + 16 * s, id_s, s > 0);
-            mma_ss(tbase + T_G + sb * BB, yd + 16 * s, vst + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_S, qd + 16 * s, kst + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_T, rd + 16 * s, kst + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_G, yd + 16 * s, vst + 16 * s, id_s, s > 0);
           }
-          mma_commit(&bar.sfull[sb]);
+          mma_commit(&bar.sfull[0]);
           if (++st == KS) { st = 0; kpar ^= 1; }
         }
         if (g >= 1) {
@@ -193,8 +195,8 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           for (int s = 0; s < BB / 16; ++s) {
             const uint64_t b = kms + (uint64_t)(s * (2048 >> 4));
             const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_DQ, tbase + T_DS + pb * 16 + s * 8, b, id_o, acc);
-            mma_ts(tbase + T_DR, tbase + T_DT + pb * 16 + s * 8, b, id_o, acc);
+            mma_ts(tbase + T_DQ, tbase + T_DS + pb * 32 + s * 8, b, id_o, acc);
+            mma_ts(tbase + T_DR, tbase + T_DT + pb * 32 + s * 8, b, id_o, acc);
           }
           mma_commit(&bar.pfree[pb]);
           mma_commit(&bar.kvempty[sth]);
@@ -238,47 +240,57 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     const float mc = m * c2;
     bool ok = true;
     for (int h = 0; h < nb && ok; ++h) {
-      const int sb = h & 1;
-      if (!warp_wait(&bar.sfull[sb], (h >> 1) & 1, status, abort_p)) { ok = false; break; }
+      if (!warp_wait(&bar.sfull[0], h & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[BB], tv[BB], gv[BB];
-      tmem_ld16(lane_base + T_S + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-      tmem_ld16(lane_base + T_S + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
-      tmem_ld16(lane_base + T_T + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
-      tmem_ld16(lane_base + T_T + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
-      tmem_ld16(lane_base + T_G + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
-      tmem_ld16(lane_base + T_G + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
-      const int j0 = h * BB;
-      uint32_t dsw[BB / 2], dtw[BB / 2];
-#pragma unroll
-      for (int c = 0; c < BB; c += 2) {
-        float ds[2], dt[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float p = (valid && j0 + c + u <= i)
-                              ? ex2(fmaf(__uint_as_float(sv[c + u]), c2, -mc)) * inv_om
-                              : 0.f;
-          const float t = __uint_as_float(tv[c + u]), gg = __uint_as_float(gv[c + u]);
-          ds[u] = p * (fmaf(1.f + tbar - t, gg, G * t) - Dr);
-          dt[u] = p * (G - gg);
-        }
-        dsw[c / 2] = pack_bf16(ds[0], ds[1]);
-        dtw[c / 2] = pack_bf16(dt[0], dt[1]);
-      }
       const int pb = h & 1;
-      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
-        ok = false;
-        break;
+      // the 64 columns of the block in two halves of 32 (registers)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[32], tv[32], gv[32];
+        tmem_ld16(lane_base + T_S + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+        tmem_ld16(lane_base + T_S + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+        tmem_ld16(lane_base + T_T + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
+        tmem_ld16(lane_base + T_T + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
+        tmem_ld16(lane_base + T_G + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
+        tmem_ld16(lane_base + T_G + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
+        tmem_ld_wait();
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.sfree[0]);
+        }
+        const int j0 = h * BB + 32 * hf;
+        uint32_t dsw[16], dtw[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2], dt[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float p = (valid && j0 + c + u <= i)
+                                ? ex2(fmaf(__uint_as_float(sv[c + u]), c2, -mc)) * inv_om
+                                : 0.f;
+            const float t = __uint_as_float(tv[c + u]), gg = __uint_as_float(gv[c + u]);
+            ds[u] = p * (fmaf(1.f + tbar - t, gg, G * t) - Dr);
+            dt[u] = p * (G - gg);
+          }
+          dsw[c / 2] = pack_bf16(ds[0], ds[1]);
+          dtw[c / 2] = pack_bf16(dt[0], dt[1]);
+        }
+        if (hf == 0) {
+          if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st8(lane_base + T_DS + pb * 32 + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&dsw[0]));
+        tmem_st8(lane_base + T_DS + pb * 32 + 16 * hf + 8,
+                 *reinterpret_cast<uint32_t(*)[8]>(&dsw[8]));
+        tmem_st8(lane_base + T_DT + pb * 32 + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&dtw[0]));
+        tmem_st8(lane_base + T_DT + pb * 32 + 16 * hf + 8,
+                 *reinterpret_cast<uint32_t(*)[8]>(&dtw[8]));
       }
-      tc_fence_after();
-      tmem_st8(lane_base + T_DS + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&dsw[0]));
-      tmem_st8(lane_base + T_DS + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&dsw[8]));
-      tmem_st8(lane_base + T_DT + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&dtw[0]));
-      tmem_st8(lane_base + T_DT + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&dtw[8]));
+      if (!ok) break;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -321,15 +333,16 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
 
 // ============================================================================ columns: dK, dV
 namespace cols {
-constexpr uint32_t T_S = 0, T_T = 64, T_G = 128;     // 2 x 32 fp32 each
-constexpr uint32_t T_DS = 192, T_DT = 224, T_A = 256;  // 2 x 16 (packed bf16) each
-constexpr uint32_t T_DK = 288, T_DV = 352;           // 64 fp32 each
+constexpr uint32_t T_S = 0, T_T = 64, T_G = 128;     // 64 fp32 each (one buffer)
+constexpr uint32_t T_DS = 192, T_DT = 256, T_A = 320;  // 2 x 32 (packed bf16) each
+constexpr uint32_t T_DK = 384, T_DV = 448;           // 64 fp32 each
 constexpr int SM_K = 0, SM_V = SM_K + TILE;
 constexpr int SM_QS = SM_V + TILE, SM_RS = SM_QS + KS * STAGE, SM_YS = SM_RS + KS * STAGE;
-constexpr int SM_SS = SM_YS + KS * STAGE;  // KS x 32 row records
-constexpr int SS_STAGE = BB * STAT * 4;    // 1 KiB
+constexpr int SM_SS = SM_YS + KS * STAGE;  // KS x 64 row records
+constexpr int SS_STAGE = BB * STAT * 4;    // 2 KiB
 constexpr int SM_BAR = SM_SS + KS * SS_STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Barriers {
   uint64_t qfull[KS], qempty[KS];
@@ -405,9 +418,9 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       uint32_t qpar = 0;
       for (int g = 0; g <= nblk && ok; ++g) {
         if (g < nblk) {
-          const int sb = g & 1;
-          ok = g >= 2 ? mbar_wait2(&bar.qfull[st], qpar, &bar.sfree[sb], ((g >> 1) - 1) & 1,
-                                   status, TO, abort_p)
+          // one S / T / G buffer: free once the previous block's scores were read
+          ok = g >= 1 ? mbar_wait2(&bar.qfull[st], qpar, &bar.sfree[0], (g - 1) & 1, status, TO,
+                                   abort_p)
                       : mbar_wait(&bar.qfull[st], qpar, status, TO, abort_p);
           if (!ok) break;
           tc_fence_after();
@@ -415,11 +428,11 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           const uint64_t o = (uint64_t)(st * stage16);
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
-            mma_ss(tbase + T_S + sb * BB, kd + 16 * s, qd + o + 16 * s, id_s, s > 0);
-            mma_ss(tbase + T_T + sb * BB, kd + 16 * s, rd + o + 16 * s, id_s, s > 0);
-            mma_ss(tbase + T_G + sb * BB, vd + 16 * s, yd + o + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_S, kd + 16 * s, qd + o + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_T, kd + 16 * s, rd + o + 16 * s, id_s, s > 0);
+            mma_ss(tbase + T_G, vd + 16 * s, yd + o + 16 * s, id_s, s > 0);
           }
-          mma_commit(&bar.sfull[sb]);
+          mma_commit(&bar.sfull[0]);
           if (++st == KS) { st = 0; qpar ^= 1; }
         }
         if (g >= 1) {
@@ -432,9 +445,9 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           for (int s = 0; s < BB / 16; ++s) {
             const uint64_t so = o + (uint64_t)(s * (2048 >> 4));
             const uint32_t acc = (h > 0 || s > 0) ? 1u : 0u;
-            mma_ts(tbase + T_DK, tbase + T_DS + pb * 16 + s * 8, qmn + so, id_o, acc);
-            mma_ts(tbase + T_DK, tbase + T_DT + pb * 16 + s * 8, rmn + so, id_o, 1u);
-            mma_ts(tbase + T_DV, tbase + T_A + pb * 16 + s * 8, ymn + so, id_o, acc);
+            mma_ts(tbase + T_DK, tbase + T_DS + pb * 32 + s * 8, qmn + so, id_o, acc);
+            mma_ts(tbase + T_DK, tbase + T_DT + pb * 32 + s * 8, rmn + so, id_o, 1u);
+            mma_ts(tbase + T_DV, tbase + T_A + pb * 32 + s * 8, ymn + so, id_o, acc);
           }
           mma_commit(&bar.pfree[pb]);
           mma_commit(&bar.qempty[sth]);
@@ -458,10 +471,10 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         stage_block(smem + SM_QS + st * STAGE, q, base + r0, nrows, lane);
         stage_block(smem + SM_RS + st * STAGE, rp, base + r0, nrows, lane);
         stage_block(smem + SM_YS + st * STAGE, dout, base + r0, nrows, lane);
-        // 32 records of 32 bytes: two 16-byte copies per lane
+        // 64 records of 32 bytes: four 16-byte copies per lane
         float* sdst = reinterpret_cast<float*>(smem + SM_SS + st * SS_STAGE);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < 4; ++t) {
           const int e = lane + 32 * t, rr = e >> 1, half4 = e & 1;
           const bool in = rr < nrows;
           cp_async16(sdst + rr * STAT + 4 * half4,
@@ -482,61 +495,71 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     const float c2 = inv_h * 1.4426950408889634f;
     bool ok = true;
     for (int h = 0; h < nblk && ok; ++h) {
-      const int sb = h & 1, sth = h % KS;
+      const int sth = h % KS, pb = h & 1;
       // the block's records: read after the loader's own completion signal for the stage
       if (!warp_wait(&bar.qfull[sth], (h / KS) & 1, status, abort_p) ||
-          !warp_wait(&bar.sfull[sb], (h >> 1) & 1, status, abort_p)) {
+          !warp_wait(&bar.sfull[0], h & 1, status, abort_p)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[BB], tv[BB], gv[BB];
-      tmem_ld16(lane_base + T_S + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-      tmem_ld16(lane_base + T_S + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
-      tmem_ld16(lane_base + T_T + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
-      tmem_ld16(lane_base + T_T + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
-      tmem_ld16(lane_base + T_G + sb * BB, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
-      tmem_ld16(lane_base + T_G + sb * BB + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
       const float* rec = reinterpret_cast<const float*>(smem + SM_SS + sth * SS_STAGE);
-      const int iq0 = (qb0 + h) * BB;
-      uint32_t dsw[BB / 2], dtw[BB / 2], aw[BB / 2];
+      // the 64 queries of the block in two halves of 32 (registers)
 #pragma unroll
-      for (int c = 0; c < BB; c += 2) {
-        float ds[2], dt[2], a[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int i = iq0 + c + u;
-          const float4 s4 = *reinterpret_cast<const float4*>(rec + (c + u) * STAT);
-          const float Dr = rec[(c + u) * STAT + 4];
-          const float p = (valid && j <= i && i < T)
-                              ? ex2((__uint_as_float(sv[c + u]) - s4.x) * c2) * s4.y
-                              : 0.f;
-          const float t = __uint_as_float(tv[c + u]), gg = __uint_as_float(gv[c + u]);
-          const float w = 1.f + s4.z - t;
-          ds[u] = p * (fmaf(w, gg, s4.w * t) - Dr) * inv_h;
-          dt[u] = p * (s4.w - gg);
-          a[u] = p * w;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[32], tv[32], gv[32];
+        tmem_ld16(lane_base + T_S + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+        tmem_ld16(lane_base + T_S + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+        tmem_ld16(lane_base + T_T + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
+        tmem_ld16(lane_base + T_T + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
+        tmem_ld16(lane_base + T_G + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
+        tmem_ld16(lane_base + T_G + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
+        tmem_ld_wait();
+        if (hf == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.sfree[0]);
         }
-        dsw[c / 2] = pack_bf16(ds[0], ds[1]);
-        dtw[c / 2] = pack_bf16(dt[0], dt[1]);
-        aw[c / 2] = pack_bf16(a[0], a[1]);
+        const int iq0 = (qb0 + h) * BB + 32 * hf;
+        const float* rh = rec + 32 * hf * STAT;
+        uint32_t dsw[16], dtw[16], aw[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float ds[2], dt[2], a[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int i = iq0 + c + u;
+            const float4 s4 = *reinterpret_cast<const float4*>(rh + (c + u) * STAT);
+            const float Dr = rh[(c + u) * STAT + 4];
+            const float p = (valid && j <= i && i < T)
+                                ? ex2((__uint_as_float(sv[c + u]) - s4.x) * c2) * s4.y
+                                : 0.f;
+            const float t = __uint_as_float(tv[c + u]), gg = __uint_as_float(gv[c + u]);
+            const float w = 1.f + s4.z - t;
+            ds[u] = p * (fmaf(w, gg, s4.w * t) - Dr) * inv_h;
+            dt[u] = p * (s4.w - gg);
+            a[u] = p * w;
+          }
+          dsw[c / 2] = pack_bf16(ds[0], ds[1]);
+          dtw[c / 2] = pack_bf16(dt[0], dt[1]);
+          aw[c / 2] = pack_bf16(a[0], a[1]);
+        }
+        if (hf == 0) {
+          if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t co = pb * 32 + 16 * hf;
+        tmem_st8(lane_base + T_DS + co, *reinterpret_cast<uint32_t(*)[8]>(&dsw[0]));
+        tmem_st8(lane_base + T_DS + co + 8, *reinterpret_cast<uint32_t(*)[8]>(&dsw[8]));
+        tmem_st8(lane_base + T_DT + co, *reinterpret_cast<uint32_t(*)[8]>(&dtw[0]));
+        tmem_st8(lane_base + T_DT + co + 8, *reinterpret_cast<uint32_t(*)[8]>(&dtw[8]));
+        tmem_st8(lane_base + T_A + co, *reinterpret_cast<uint32_t(*)[8]>(&aw[0]));
+        tmem_st8(lane_base + T_A + co + 8, *reinterpret_cast<uint32_t(*)[8]>(&aw[8]));
       }
-      const int pb = h & 1;
-      if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st8(lane_base + T_DS + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&dsw[0]));
-      tmem_st8(lane_base + T_DS + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&dsw[8]));
-      tmem_st8(lane_base + T_DT + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&dtw[0]));
-      tmem_st8(lane_base + T_DT + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&dtw[8]));
-      tmem_st8(lane_base + T_A + pb * 16, *reinterpret_cast<uint32_t(*)[8]>(&aw[0]));
-      tmem_st8(lane_base + T_A + pb * 16 + 8, *reinterpret_cast<uint32_t(*)[8]>(&aw[8]));
+      if (!ok) break;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
