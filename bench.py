@@ -114,6 +114,10 @@ def recorded_traffic(kernel_file: str):
     ent = rec.get(kernel_file)
     if not ent or ent.get("source_sha") != kernel_source_sha(kernel_file):
         return None
+    # a step that also launches kernels of other files is current only if they are unchanged too
+    for other, sha in ent.get("depends", {}).items():
+        if sha != kernel_source_sha(other):
+            return None
     return ent.get("dram_bytes_per_launch")
 
 
@@ -531,7 +535,8 @@ def run_parallax_backward(args, w, world, rank):
                                f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
     roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                  "executed_tflops": causal_pairs(w) * exe / (ms_per_step / 1e3) / 1e12,
-                 "traffic": None, "avg_launch_ms": ms_per_step / 3})
+                 "traffic": recorded_traffic("lla_parallax_bwd_tc.cu") if tensor_path else None,
+                 "avg_launch_ms": ms_per_step / 3})
     if rank == 0:
         line = {
             "metric": METRIC_PX_BWD, "value": value, "unit": UNIT, "n_gpus": world,
