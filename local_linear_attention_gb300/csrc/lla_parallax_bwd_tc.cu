@@ -10,18 +10,22 @@
 // The blog's Appendix F splits the backward the same way: a row-tile pass (dQ, dR) and a
 // column-tile pass (dK, dV), because the two reductions run in opposite directions.
 //
-// Rows pass: one CTA per 128-query tile; per 32-key block of its causal prefix, S = Q K^T,
+// Rows pass: one CTA per 128-query tile; per 64-key block of its causal prefix, S = Q K^T,
 // T = R K^T and G = dO V^T (tcgen05.mma, operands from shared memory, fp32 in tensor memory);
-// four warps (one thread per query row) turn them into dS and dT (bf16, written to tensor
-// memory), and dQ += dS K, dR += dT K (A from tensor memory, B = the key block read as an
-// MN-major operand) accumulate in tensor memory.
-// Columns pass: one CTA per 128-key tile; per 32-query block from the tile's first key on,
-// S^T = K Q^T, T^T = K R^T, G^T = V dO^T; the four warps (one thread per key row) take the
-// block's row records from shared memory and form dS^T / h, dT^T and A^T; dK += dS^T Q + dT^T R
-// and dV += A^T dO.
-// Warp roles (6 warps): 0 issues every MMA (one thread) and owns the tensor-memory allocation;
-// 1 stages the streamed blocks with cp.async (several in flight); 2-5 the elementwise step and
-// the output. All mbarrier waits are bounded.
+// eight warps (two per tensor-memory lane quarter, one thread per query row, each taking 32 of
+// the block's 64 keys) turn them into dS and dT (bf16, written to tensor memory), and
+// dQ += dS K, dR += dT K (A from tensor memory, B = the key block read as an MN-major operand)
+// accumulate in tensor memory.
+// Columns pass: one CTA per 128-key tile; per 64-query block from the tile's first key on,
+// S^T = K Q^T, T^T = K R^T, G^T = V dO^T; the eight warps (one thread per key row, 32 of the
+// block's queries each) take the block's row records from shared memory and form dS^T / h,
+// dT^T and A^T; dK += dS^T Q + dT^T R and dV += A^T dO.
+// The elementwise step is a chain of exponentials and shared-memory reads per element; two
+// warps per lane quarter give each scheduler a second warp to hide it behind.
+// Warp roles (10 warps): 0 issues every MMA (one thread) and owns the tensor-memory allocation;
+// 1 stages the streamed blocks with cp.async (several in flight); 2-9 the elementwise step and
+// the output (warps 2-5 the first half of each block and dQ / dK, warps 6-9 the second half and
+// dR / dV). All mbarrier waits are bounded.
 #include <cstdint>
 
 #include "lla_internal.cuh"
@@ -36,7 +40,7 @@ constexpr int D = 64;
 constexpr int BM = 128;  // rows of the resident tile (queries or keys)
 constexpr int BB = 64;   // rows of a streamed block (keys or queries): N = 64 score MMAs
 constexpr int KS = 6;
-constexpr int NWARPS = 6;
+constexpr int NWARPS = 10;  // MMA issuer, loader, 8 elementwise warps (two per lane quarter)
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int TILE = BM * D * 2;     // 16 KiB
 constexpr int STAGE = BB * D * 2;    // 8 KiB
@@ -128,8 +132,8 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 32); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], 4);
-      mbar_init(&bar.pfull[s], 4);
+      mbar_init(&bar.sfree[s], 8);
+      mbar_init(&bar.pfull[s], 8);
       mbar_init(&bar.pfree[s], 1);
     }
     mbar_init(&bar.accfull, 1);
@@ -226,6 +230,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   } else {
     // ------------------------------------------------------------------ dS, dT and the output
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;  // this warp's half of each block (32 columns)
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
     const bool valid = r < nq;
@@ -243,9 +248,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       if (!warp_wait(&bar.sfull[0], h & 1, status, abort_p)) { ok = false; break; }
       tc_fence_after();
       const int pb = h & 1;
-      // the 64 columns of the block in two halves of 32 (registers)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      {  // this warp's 32 columns of the block
         uint32_t sv[32], tv[32], gv[32];
         tmem_ld16(lane_base + T_S + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
         tmem_ld16(lane_base + T_S + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
@@ -254,7 +257,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         tmem_ld16(lane_base + T_G + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
         tmem_ld16(lane_base + T_G + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
         tmem_ld_wait();
-        if (hf == 1) {
+        {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar.sfree[0]);
@@ -276,7 +279,7 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           dsw[c / 2] = pack_bf16(ds[0], ds[1]);
           dtw[c / 2] = pack_bf16(dt[0], dt[1]);
         }
-        if (hf == 0) {
+        {
           if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
             ok = false;
             break;
@@ -300,23 +303,19 @@ pbw_rows_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t a[16], b[16];
-        tmem_ld16(lane_base + T_DQ + c0, a);
-        tmem_ld16(lane_base + T_DR + c0, b);
+        // half 0 writes dQ (the accumulated ds k, times 1/h), half 1 dR
+        uint32_t a[16];
+        tmem_ld16(lane_base + (hf ? T_DR : T_DQ) + c0, a);
         tmem_ld_wait();
         if (valid) {
-          uint32_t pa[8], pr[8];
+          const float sc = hf ? 1.f : inv_h;
+          uint32_t pa[8];
 #pragma unroll
-          for (int t = 0; t < 16; t += 2) {
-            pa[t / 2] = pack_bf16(__uint_as_float(a[t]) * inv_h, __uint_as_float(a[t + 1]) * inv_h);
-            pr[t / 2] = pack_bf16(__uint_as_float(b[t]), __uint_as_float(b[t + 1]));
-          }
-          uint4* oq = reinterpret_cast<uint4*>(dq + (base + i) * D + c0);
-          uint4* orr = reinterpret_cast<uint4*>(dr + (base + i) * D + c0);
-          oq[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-          oq[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-          orr[0] = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-          orr[1] = make_uint4(pr[4], pr[5], pr[6], pr[7]);
+          for (int t = 0; t < 16; t += 2)
+            pa[t / 2] = pack_bf16(__uint_as_float(a[t]) * sc, __uint_as_float(a[t + 1]) * sc);
+          uint4* o = reinterpret_cast<uint4*>((hf ? dr : dq) + (base + i) * D + c0);
+          o[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+          o[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
         }
       }
     }
@@ -376,8 +375,8 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.qfull[s], 32); mbar_init(&bar.qempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], 4);
-      mbar_init(&bar.pfull[s], 4);
+      mbar_init(&bar.sfree[s], 8);
+      mbar_init(&bar.pfull[s], 8);
       mbar_init(&bar.pfree[s], 1);
     }
     mbar_init(&bar.accfull, 1);
@@ -488,6 +487,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   } else {
     // ------------------------------------------------------------------ dS^T, dT^T, A^T, output
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;  // this warp's half of each block (32 columns)
     const int r = quarter * 32 + lane;
     const int j = j0 + r;
     const bool valid = r < nk;
@@ -504,9 +504,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       }
       tc_fence_after();
       const float* rec = reinterpret_cast<const float*>(smem + SM_SS + sth * SS_STAGE);
-      // the 64 queries of the block in two halves of 32 (registers)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      {  // this warp's 32 queries of the block
         uint32_t sv[32], tv[32], gv[32];
         tmem_ld16(lane_base + T_S + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
         tmem_ld16(lane_base + T_S + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
@@ -515,7 +513,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         tmem_ld16(lane_base + T_G + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&gv[0]));
         tmem_ld16(lane_base + T_G + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&gv[16]));
         tmem_ld_wait();
-        if (hf == 1) {
+        {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar.sfree[0]);
@@ -544,7 +542,7 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           dtw[c / 2] = pack_bf16(dt[0], dt[1]);
           aw[c / 2] = pack_bf16(a[0], a[1]);
         }
-        if (hf == 0) {
+        {
           if (h >= 2 && !warp_wait(&bar.pfree[pb], ((h >> 1) - 1) & 1, status, abort_p)) {
             ok = false;
             break;
@@ -569,23 +567,18 @@ pbw_cols_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t a[16], b[16];
-        tmem_ld16(lane_base + T_DK + c0, a);
-        tmem_ld16(lane_base + T_DV + c0, b);
+        // half 0 writes dK, half 1 dV
+        uint32_t a[16];
+        tmem_ld16(lane_base + (hf ? T_DV : T_DK) + c0, a);
         tmem_ld_wait();
         if (valid) {
-          uint32_t pk[8], pv[8];
+          uint32_t pk[8];
 #pragma unroll
-          for (int t = 0; t < 16; t += 2) {
+          for (int t = 0; t < 16; t += 2)
             pk[t / 2] = pack_bf16(__uint_as_float(a[t]), __uint_as_float(a[t + 1]));
-            pv[t / 2] = pack_bf16(__uint_as_float(b[t]), __uint_as_float(b[t + 1]));
-          }
-          uint4* ok4 = reinterpret_cast<uint4*>(dk + (base + j) * D + c0);
-          uint4* ov4 = reinterpret_cast<uint4*>(dv + (base + j) * D + c0);
-          ok4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          ok4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          ov4[0] = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-          ov4[1] = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+          uint4* o = reinterpret_cast<uint4*>((hf ? dv : dk) + (base + j) * D + c0);
+          o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
     }
