@@ -14,7 +14,8 @@
 //    from shared memory), turns them into P1 (bf16) and P2 = P1 .* S2 (an exact-to-16-bits bf16
 //    hi/lo pair, so that the covariance term, a difference of two sums, keeps its precision), and
 //    accumulates O1 = P1 V and O2 = P2 V in tensor memory. d1 and d2 are summed in fp32 from the
-//    same rounded weights.
+//    same rounded weights. Eight softmax warps, two per tensor-memory lane quarter, each take
+//    one 32-key half of every block (one warp per scheduler left the exponential chain exposed).
 //  * CUDA cores (every other shape and dtype): online softmax with running rescale, four threads
 //    per query (each owns a quarter of the q, r, O1 and O2 coordinates), fp32 accumulation.
 // All mbarrier waits are bounded.
@@ -36,7 +37,7 @@ constexpr int DV = 64;
 constexpr int BM = 128;
 constexpr int KB = 64;  // keys per block: N = 64 for Q K^T and R K^T
 constexpr int KS = 6;
-constexpr int NWARPS = 6;
+constexpr int NWARPS = 10;  // MMA issuer, loader, 8 softmax warps (two per lane quarter)
 constexpr int NTHREADS = NWARPS * 32;
 
 // tensor-memory columns
@@ -57,7 +58,9 @@ constexpr int SM_K = SM_R + TILE;
 constexpr int KV_STAGE = KB * D * 2;  // 8 KiB
 constexpr int SM_V = SM_K + KS * KV_STAGE;
 constexpr int SM_BAR = SM_V + KS * KV_STAGE;
-constexpr int SMEM_BYTES = SM_BAR + 256;
+constexpr int SM_X = SM_BAR + 256;  // [2 halves][5 values][BM] per-row partials of the two halves
+constexpr int NXV = 5;              // m, d1, d2, and (STATS) dout . vbar, dout . o
+constexpr int SMEM_BYTES = SM_X + 2 * NXV * BM * 4;
 
 __device__ __forceinline__ int kmaj_off(int r, int c) { return (r >> 3) * 1024 + c * 128 + (r & 7) * 16; }
 
@@ -84,8 +87,9 @@ struct Barriers {
   uint64_t sfull[2], sfree[2];
   uint64_t pfull, pfree;
   uint64_t accfull, done;
+  uint64_t rowx;  // the two halves of each row exchanged m (phase 0), d1 and d2 (1), STATS sums (2)
 };
-static_assert(sizeof(Barriers) <= SMEM_BYTES - SM_BAR, "barrier region");
+static_assert(sizeof(Barriers) <= SM_X - SM_BAR, "barrier region");
 
 // Steps g = 0 .. nb-1 are the max sweep (Q K^T only), g = nb .. 2nb-1 the main sweep over the
 // same key blocks b = g - nb.
@@ -129,10 +133,11 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 32); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
-      mbar_init(&bar.sfree[s], 4);
+      mbar_init(&bar.sfree[s], 8);
 
     }
-    mbar_init(&bar.pfull, 4);
+    mbar_init(&bar.pfull, 8);
+    mbar_init(&bar.rowx, 8);
     mbar_init(&bar.pfree, 1);
     mbar_init(&bar.accfull, 1);
     mbar_init(&bar.done, 1);
@@ -242,12 +247,18 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     cp_async_wait<0>();  // nothing of this warp is in flight at teardown
   } else {
     // ------------------------------------------------------------------ weights + output
-    const int quarter = warp & 3;
+    // Two warps per tensor-memory lane quarter (one thread per query row each): `hf` takes
+    // columns 32 hf .. 32 hf + 31 of every key block (and of the output); the halves' row max,
+    // sums and (STATS) dot products are combined through shared memory on barrier rowx.
+    const int quarter = warp & 3, hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int i = i0 + r;
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
+    float* const xp = reinterpret_cast<float*>(smem + SM_X);  // [hf][value][BM]
+    auto xput = [&](int v, float x) { xp[(hf * NXV + v) * BM + r] = x; };
+    auto xsum = [&](int v) { return xp[v * BM + r] + xp[(NXV + v) * BM + r]; };
     float m = -INFINITY, d1 = 0.f, d2 = 0.f;
     for (int g = 0; g < 2 * nb; ++g) {
       const int sb = g & 1;
@@ -256,76 +267,77 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       const bool main_sweep = g >= nb;
       const int h = g - nb;
       const float mc = m * c2;
-      bool ok2 = true;
-      // The block's 64 logits in two halves of 32 columns (to bound the registers); the S / T
-      // buffer is released once the second half is read. The weights of the first half are
-      // formed before waiting for the previous block's P V MMAs (one P buffer).
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sv[32], tv[32];
-        tmem_ld16(lane_base + T_S + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
-        tmem_ld16(lane_base + T_S + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
-        if (main_sweep) {
-          tmem_ld16(lane_base + T_T + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
-          tmem_ld16(lane_base + T_T + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
-        }
-        tmem_ld_wait();
-        if (hf == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar.sfree[sb]);
-        }
-        const int jb = (main_sweep ? h : g) * KB + 32 * hf;
-        if (!main_sweep) {  // max sweep
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (valid && jb + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
-          continue;
-        }
-        uint32_t pw[16], hw[16], lw[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float p0 = (valid && jb + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
-          const float p1 =
-              (valid && jb + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
-          const uint32_t w = pack_bf16(p0, p1);
-          pw[c / 2] = w;
-          const float r0 = bf16_lo(w), r1 = bf16_hi(w);
-          d1 += r0 + r1;
-          const float q0 = r0 * __uint_as_float(tv[c]);
-          const float q1 = r1 * __uint_as_float(tv[c + 1]);
-          d2 += q0 + q1;
-          const uint32_t hh = pack_bf16(q0, q1);
-          hw[c / 2] = hh;
-          lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
-        }
-        if (hf == 0) {
-          if (h >= 1 && !warp_wait(&bar.pfree, (h - 1) & 1, status, abort_p)) {
-            ok2 = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        tmem_st8(lane_base + T_P + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
-        tmem_st8(lane_base + T_P + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
-        tmem_st8(lane_base + T_P2H + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&hw[0]));
-        tmem_st8(lane_base + T_P2H + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&hw[8]));
-        tmem_st8(lane_base + T_P2L + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&lw[0]));
-        tmem_st8(lane_base + T_P2L + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&lw[8]));
+      uint32_t sv[32], tv[32];
+      tmem_ld16(lane_base + T_S + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&sv[0]));
+      tmem_ld16(lane_base + T_S + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&sv[16]));
+      if (main_sweep) {
+        tmem_ld16(lane_base + T_T + sb * KB + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(&tv[0]));
+        tmem_ld16(lane_base + T_T + sb * KB + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(&tv[16]));
       }
-      if (!ok2) break;
-      if (!main_sweep) continue;
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.sfree[sb]);
+      const int jb = (main_sweep ? h : g) * KB + 32 * hf;
+      if (!main_sweep) {  // max sweep
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (valid && jb + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+        if (g == nb - 1) {  // the two halves' maxima
+          xput(0, m);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.rowx);
+          if (!warp_wait(&bar.rowx, 0, status, abort_p)) break;
+          m = fmaxf(xp[r], xp[NXV * BM + r]);
+        }
+        continue;
+      }
+      uint32_t pw[16], hw[16], lw[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const float p0 = (valid && jb + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+        const float p1 =
+            (valid && jb + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+        const uint32_t w = pack_bf16(p0, p1);
+        pw[c / 2] = w;
+        const float r0 = bf16_lo(w), r1 = bf16_hi(w);
+        d1 += r0 + r1;
+        const float q0 = r0 * __uint_as_float(tv[c]);
+        const float q1 = r1 * __uint_as_float(tv[c + 1]);
+        d2 += q0 + q1;
+        const uint32_t hh = pack_bf16(q0, q1);
+        hw[c / 2] = hh;
+        lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+      }
+      // one P buffer: the previous block's P V MMAs must have completed
+      if (h >= 1 && !warp_wait(&bar.pfree, (h - 1) & 1, status, abort_p)) break;
+      tc_fence_after();
+      tmem_st8(lane_base + T_P + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&pw[0]));
+      tmem_st8(lane_base + T_P + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&pw[8]));
+      tmem_st8(lane_base + T_P2H + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&hw[0]));
+      tmem_st8(lane_base + T_P2H + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&hw[8]));
+      tmem_st8(lane_base + T_P2L + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&lw[0]));
+      tmem_st8(lane_base + T_P2L + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&lw[8]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.pfull);
       if (h == nb - 1) {
+        // the halves' d1 and d2 (summed in a fixed order), then this half's output columns
+        xput(1, d1);
+        xput(2, d2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.rowx);
+        if (!warp_wait(&bar.rowx, 1, status, abort_p)) break;
+        const float D1 = xsum(1), D2 = xsum(2);
         if (!warp_wait(&bar.accfull, 0, status, abort_p)) break;
         tc_fence_after();
-        const float inv = 1.f / d1;
-        const float f1 = (1.f + d2 * inv) * inv;
-        float gs = 0.f, od = 0.f;  // STATS: dout . vbar, dout . o
+        const float inv = 1.f / D1;
+        const float f1 = (1.f + D2 * inv) * inv;
+        float gs = 0.f, od = 0.f;  // STATS: dout . vbar, dout . o over this half's columns
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
+        for (int c1 = 0; c1 < DV / 2; c1 += 16) {
+          const int c0 = (DV / 2) * hf + c1;
           uint32_t o1[16], o2[16];
           tmem_ld16(lane_base + T_O1 + c0, o1);
           tmem_ld16(lane_base + T_O2 + c0, o2);
@@ -359,10 +371,18 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
         }
-        if (STATS && valid) {
-          const float tbar = d2 * inv;
-          *reinterpret_cast<float4*>(stats + (base + i) * 8) = make_float4(m, inv, tbar, gs);
-          stats[(base + i) * 8 + 4] = fmaf(gs, tbar, od);
+        if (STATS) {
+          xput(3, gs);
+          xput(4, od);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.rowx);
+          if (!warp_wait(&bar.rowx, 0, status, abort_p)) break;  // phase 2
+          if (hf == 0 && valid) {
+            const float G = xsum(3), Od = xsum(4);
+            const float tbar = D2 * inv;
+            *reinterpret_cast<float4*>(stats + (base + i) * 8) = make_float4(m, inv, tbar, G);
+            stats[(base + i) * 8 + 4] = fmaf(G, tbar, Od);
+          }
         }
       }
     }
