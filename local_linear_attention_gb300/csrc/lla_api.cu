@@ -313,9 +313,11 @@ int run_decode(const DecodeArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = nullptr;
   if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  DecodeArgs b = a;
+  b.path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, decode_workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
-  int st = launch_decode(a, ws, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+  if (cudaMallocAsync(&ws, decode_workspace_bytes(b), s) != cudaSuccess) return LLA_ERR_CUDA;
+  int st = launch_decode(b, ws, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
   return st;
 }

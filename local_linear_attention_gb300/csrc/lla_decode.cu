@@ -306,6 +306,101 @@ parallax_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 template <int D, int DV>
 constexpr int lla_part() { return 2 + D + DV + D * D + DV * D; }
 
+// The last CTA of head bh to arrive: merges the S partials of the head in a fixed order
+// (log-sum-exp weights computed once per split), centres the moments, solves the d x d ridge
+// system by Cholesky and writes o = vbar + C_vk y, all in double precision. qs: the query (fp32,
+// shared memory); dsm: dynamic shared memory of at least sizeof(double) * (P + D + S) bytes.
+template <typename TIn, int D, int DV>
+__device__ void lla_merge_solve(const float* qs, const float* __restrict__ part, long long bh,
+                                int S, float inv_h, float lam, float* dsm, int* fail_flag,
+                                TIn* __restrict__ out, int* __restrict__ status) {
+  constexpr int P = lla_part<D, DV>();
+  const int tid = threadIdx.x;
+  int& fail_s = *fail_flag;
+
+  // ---- merge (fp32: the partials are fp32 sums, the weights <= 1), then centre and solve in
+  // double precision
+  double* mom = reinterpret_cast<double*>(dsm);  // [P - 1]: omega, sk, sv, Skk, Svk (merged)
+  double* z = mom + P;                           // [D]: q - kbar, then y
+  float* alpha = reinterpret_cast<float*>(z + D);  // [S]
+  const float* hp = part + bh * S * (long long)P;
+  float M = -INFINITY;
+  for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * (long long)P));
+  for (int t = tid; t < S; t += NT) {
+    const float mt = __ldcg(hp + t * (long long)P);
+    alpha[t] = mt == -INFINITY ? 0.f : expf((mt - M) * inv_h);
+  }
+  __syncthreads();
+  constexpr int SKK0 = 1 + D + DV;  // offset of Skk in mom (mom[e] is partial entry 1 + e)
+  for (int e = tid; e < P - 1; e += NT) {
+    const bool lower = e >= SKK0 && e < SKK0 + D * D && (e - SKK0) / D > (e - SKK0) % D;
+    float acc = 0.f;
+    if (!lower)
+      for (int t = 0; t < S; ++t) acc = fmaf(alpha[t], __ldcg(hp + t * (long long)P + 1 + e), acc);
+    mom[e] = (double)acc;
+  }
+  __syncthreads();
+  const double omega = mom[0];
+  const double* msk = mom + 1;
+  const double* msv = msk + D;
+  double* A = mom + SKK0;                // Skk (upper) -> C_kk + lambda' I -> its Cholesky factor
+  const double* Svk = A + D * D;
+  const double lp = (double)lam * exp(-(double)M * inv_h);  // ridge scaled by exp(-M/h)
+  for (int e = tid; e < D * D; e += NT) {
+    const int a = e / D, b = e % D;
+    if (a <= b) {
+      const double c = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
+      A[e] = c;
+      A[b * D + a] = c;
+    }
+  }
+  for (int a = tid; a < D; a += NT) z[a] = (double)qs[a] - msk[a] / omega;
+  if (tid == 0) fail_s = 0;
+  __syncthreads();
+  // Cholesky A = L L^T (lower triangle in place), column by column
+  for (int c = 0; c < D; ++c) {
+    if (tid == 0) {
+      const double piv = A[c * D + c];
+      if (!(piv > 0.0)) fail_s = 1;
+      A[c * D + c] = sqrt(piv > 0.0 ? piv : 1.0);
+    }
+    __syncthreads();
+    for (int i = c + 1 + tid; i < D; i += NT) A[i * D + c] /= A[c * D + c];
+    __syncthreads();
+    for (int e = tid; e < D * D; e += NT) {
+      const int i = e / D, j = e % D;
+      if (j > c && i >= j) A[i * D + j] -= A[i * D + c] * A[j * D + c];
+    }
+    __syncthreads();
+  }
+  // L w = z, then L^T y = w, by warp 0 (dot products across its lanes)
+  if (tid < 32) {
+    for (int i = 0; i < D; ++i) {
+      double t = 0.0;
+      for (int j = tid; j < i; j += 32) t += A[i * D + j] * z[j];
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
+      __syncwarp();
+    }
+    for (int i = D - 1; i >= 0; --i) {
+      double t = 0.0;
+      for (int j = i + 1 + tid; j < D; j += 32) t += A[j * D + i] * z[j];
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // o = vbar + C_vk y,  C_vk = Svk - sv sk^T / omega
+  const bool bad = fail_s != 0;
+  for (int c = tid; c < DV; c += NT) {
+    double o = msv[c] / omega;
+    for (int b = 0; b < D; ++b) o += (Svk[c * D + b] - msv[c] * msk[b] / omega) * z[b];
+    stf(out, bh * DV + c, bad ? __int_as_float(0x7fc00000) : (float)o);
+  }
+  if (tid == 0 && (bad || !(omega > 0.0))) atomicOr(status, kStatusNumerical);
+}
+
 template <typename TIn, int D, int DV>
 __global__ void __launch_bounds__(NT)
 lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
@@ -436,94 +531,335 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
     }
   }
   if (!last_arrival(counter + bh, S, &is_last)) return;
-
-  // ---- merge, centre and solve (the last CTA of the head), in double precision
-  double* mom = reinterpret_cast<double*>(dsm);  // [P - 1]: omega, sk, sv, Skk, Svk (merged)
-  double* z = mom + P;                           // [D]: q - kbar, then y
-  double* alpha = z + D;                         // [S]
-  const float* hp = part + bh * S * (long long)P;
-  float M = -INFINITY;
-  for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * (long long)P));
-  for (int t = tid; t < S; t += NT) {
-    const float mt = __ldcg(hp + t * (long long)P);
-    alpha[t] = mt == -INFINITY ? 0.0 : exp((double)(mt - M) * inv_h);
-  }
-  __syncthreads();
-  constexpr int SKK0 = 1 + D + DV;  // offset of Skk in mom (mom[e] is partial entry 1 + e)
-  for (int e = tid; e < P - 1; e += NT) {
-    const bool lower = e >= SKK0 && e < SKK0 + D * D && (e - SKK0) / D > (e - SKK0) % D;
-    double accd = 0.0;
-    if (!lower)
-      for (int t = 0; t < S; ++t) accd += alpha[t] * (double)__ldcg(hp + t * (long long)P + 1 + e);
-    mom[e] = accd;
-  }
-  __syncthreads();
-  const double omega = mom[0];
-  const double* msk = mom + 1;
-  const double* msv = msk + D;
-  double* A = mom + SKK0;                // Skk (upper) -> C_kk + lambda' I -> its Cholesky factor
-  const double* Svk = A + D * D;
-  const double lp = (double)lam * exp(-(double)M * inv_h);  // ridge scaled by exp(-M/h)
-  for (int e = tid; e < D * D; e += NT) {
-    const int a = e / D, b = e % D;
-    if (a <= b) {
-      const double c = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
-      A[e] = c;
-      A[b * D + a] = c;
-    }
-  }
-  for (int a = tid; a < D; a += NT) z[a] = (double)qs[a] - msk[a] / omega;
-  if (tid == 0) fail_s = 0;
-  __syncthreads();
-  // Cholesky A = L L^T (lower triangle in place), column by column
-  for (int c = 0; c < D; ++c) {
-    if (tid == 0) {
-      const double piv = A[c * D + c];
-      if (!(piv > 0.0)) fail_s = 1;
-      A[c * D + c] = sqrt(piv > 0.0 ? piv : 1.0);
-    }
-    __syncthreads();
-    for (int i = c + 1 + tid; i < D; i += NT) A[i * D + c] /= A[c * D + c];
-    __syncthreads();
-    for (int e = tid; e < D * D; e += NT) {
-      const int i = e / D, j = e % D;
-      if (j > c && i >= j) A[i * D + j] -= A[i * D + c] * A[j * D + c];
-    }
-    __syncthreads();
-  }
-  // L w = z, then L^T y = w, by warp 0 (dot products across its lanes)
-  if (tid < 32) {
-    for (int i = 0; i < D; ++i) {
-      double t = 0.0;
-      for (int j = tid; j < i; j += 32) t += A[i * D + j] * z[j];
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
-      __syncwarp();
-    }
-    for (int i = D - 1; i >= 0; --i) {
-      double t = 0.0;
-      for (int j = i + 1 + tid; j < D; j += 32) t += A[j * D + i] * z[j];
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (tid == 0) z[i] = (z[i] - t) / A[i * D + i];
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  // o = vbar + C_vk y,  C_vk = Svk - sv sk^T / omega
-  const bool bad = fail_s != 0;
-  for (int c = tid; c < DV; c += NT) {
-    double o = msv[c] / omega;
-    for (int b = 0; b < D; ++b) o += (Svk[c * D + b] - msv[c] * msk[b] / omega) * z[b];
-    stf(out, bh * DV + c, bad ? __int_as_float(0x7fc00000) : (float)o);
-  }
-  if (tid == 0 && (bad || !(omega > 0.0))) atomicOr(status, kStatusNumerical);
+  lla_merge_solve<TIn, D, DV>(qs, part, bh, S, inv_h, lam, dsm, &fail_s, out, status);
 }
 
-int choose_splits(long long BH, int L) {
+// ------------------------------------------------------------------------------- LLA, tensor cores
+// bf16, d = dv = 64. The moment sums of a chunk are two contractions over its keys,
+//   Skk = sum_j (p_j k_j) k_j^T,   Svk = sum_j (p_j v_j) k_j^T,
+// which run on the tensor cores (tcgen05, one CTA, M = 128, N = 64, fp32 accumulators in tensor
+// memory): A = [hi(p_j x_j); lo(p_j x_j)] (128 rows, x = k or v: each product split exactly into
+// two bf16 values), B = the key tile. The weights are rounded to bf16 first, as in the forward's
+// moments stage, so that every product p_j x_ja k_jb is exact and only the fp32 sums round;
+// sum p k, sum p v and omega are summed on the CUDA cores from the same products. The shift of
+// the sums moves only when a tile's maximum logit exceeds it by more than 8 ln 2 h (the weights
+// stay <= 256 in between), so the accumulators in tensor memory are rescaled rarely. The partial
+// of a chunk has the layout of lla_decode_kernel's, and the merge is the same.
+namespace dtc {
+constexpr int D = 64;
+constexpr int TKT = 64;                    // keys per tile
+constexpr int ST = 3;                      // key / value ring stages
+constexpr int A_BYTES = 128 * TKT * 2;     // one A operand: 128 rows x 64 keys, bf16
+constexpr int KT_BYTES = TKT * D * 2;      // one key or value tile
+constexpr int SM_A = 0;                    // A_k, A_v
+constexpr int SM_K = SM_A + 2 * A_BYTES;   // ST key tiles (core-matrix layout: the B operand)
+constexpr int SM_V = SM_K + ST * KT_BYTES; // ST value tiles (the same layout)
+constexpr int SMEM = SM_V + ST * KT_BYTES; // 80 KiB
+constexpr int XLD = 65;                    // row stride (floats) of the accumulator copy
+static_assert(2 * 128 * XLD * 4 <= SMEM, "accumulator copy fits the tiles' space");
+constexpr uint32_t T_KK = 0, T_VK = 64, TMEM_COLS = 128;
+constexpr float kShiftSlack = 5.545177444479562f;  // 8 ln 2
+// 16-byte chunk c (elements 8c .. 8c + 7) of key row j of a key tile: core matrix (j / 8, c) of
+// 128 bytes, 8-key groups 1024 bytes apart (read by the MMA as an MN-major B operand: K = keys).
+__device__ __forceinline__ int kofs(int j, int c) { return (j >> 3) * 1024 + c * 128 + (j & 7) * 16; }
+// 16-byte chunk f (rows 8f .. 8f + 7) of key column j of an A operand: core matrix (j / 8, f),
+// 8-key groups 2048 bytes apart (an MN-major A operand: M = 128 rows, K = keys).
+__device__ __forceinline__ int aofs(int j, int f) { return (j >> 3) * 2048 + f * 128 + (j & 7) * 16; }
+__device__ __forceinline__ uint32_t bmul2(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+__device__ __forceinline__ uint32_t bfma2(uint32_t x, uint32_t y, uint32_t z) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(z));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// The exact products p * x[0..7] (x: 8 bf16 in a 16-byte word) as hi and lo bf16 words, and their
+// fp32 values added to acc[0..7].
+__device__ __forceinline__ void split_products(uint32_t pp, const uint4& x, uint4& hi, uint4& lo,
+                                               float (&acc)[8]) {
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    h[t] = bmul2(pp, xw[t]);
+    l[t] = bfma2(pp, xw[t], h[t] ^ 0x80008000u);
+    acc[2 * t] += lo16(h[t]) + lo16(l[t]);
+    acc[2 * t + 1] += hi16(h[t]) + hi16(l[t]);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+}  // namespace dtc
+
+__global__ void __launch_bounds__(NT)
+lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                     const __nv_bfloat16* __restrict__ v, int L, int S, float inv_h, float lam,
+                     float* __restrict__ part, int* __restrict__ counter,
+                     __nv_bfloat16* __restrict__ out, int* __restrict__ status) {
+  using namespace dtc;
+  using namespace tc;
+  constexpr int P = lla_part<D, D>();
+  static_assert(NT == 256 && TKT * 4 == NT, "four threads per key; eight per feature chunk");
+  extern __shared__ __align__(1024) float dtc_smem[];
+  float* const dsm = dtc_smem;
+  uint8_t* const sm = reinterpret_cast<uint8_t*>(dsm);
+  __shared__ float qs[D], red[NT / 32], sS[TKT], xo[NT / 32];
+  __shared__ float xs[NT / 32][2][D];
+  __shared__ uint64_t mbar;  // the MMAs of a tile completed (one phase per tile)
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int is_last, fail_s, abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long bh = blockIdx.x / S;
+  const int s = blockIdx.x % S;
+  const int chunk = (L + S - 1) / S;
+  const int j0 = s * chunk, j1 = min(L, j0 + chunk);
+  const int ntl = j1 > j0 ? (j1 - j0 + TKT - 1) / TKT : 0;
+  const __nv_bfloat16* kb = k + bh * (long long)L * D;
+  const __nv_bfloat16* vb = v + bh * (long long)L * D;
+  for (int a = tid; a < D; a += NT) qs[a] = __bfloat162float(q[bh * D + a]);
+  if (tid == 0) {
+    mbar_init(&mbar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  volatile int* abort_p = &abort_flag;
+
+  // Tile `it` of the chunk into ring slot it % ST (rows past the chunk zero-filled without being
+  // read); one commit group per call, empty past the last tile.
+  auto prefetch = [&](int it) {
+    if (it < ntl) {
+      const int t0 = j0 + it * TKT, n = min(TKT, j1 - t0), slot = it % ST;
+      uint8_t* kd = sm + SM_K + slot * KT_BYTES;
+      uint8_t* vd = sm + SM_V + slot * KT_BYTES;
+      for (int e = tid; e < TKT * 8; e += NT) {
+        // each group of eight lanes: eight consecutive keys, one chunk (distinct banks)
+        const int j = (e & 7) + 8 * (e >> 6), c = (e >> 3) & 7;
+        const bool in = j < n;
+        const long long row = in ? (long long)(t0 + j) : 0;
+        cp_async16(kd + kofs(j, c), kb + row * D + c * 8, in ? 16u : 0u);
+        cp_async16(vd + kofs(j, c), vb + row * D + c * 8, in ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float m = -INFINITY;  // the shift of this CTA's sums (raw logit units)
+  float acc_k[8], acc_v[8], om = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) { acc_k[e] = 0.f; acc_v[e] = 0.f; }
+  // A operands: elements 8 c8 .. 8 c8 + 7 of keys jr and jr + 32. Each group of eight lanes takes
+  // eight consecutive keys of one chunk, so that its 16-byte loads and stores (core matrices:
+  // the keys of a chunk 16 bytes apart) fall in distinct banks.
+  const int c8 = (tid >> 3) & 7, jr = (tid & 7) + 8 * (tid >> 6);
+  const float c2 = inv_h * 1.4426950408889634f;
+  for (int it = 0; it < ST - 1; ++it) prefetch(it);
+  for (int it = 0; it < ntl; ++it) {
+    const int t0 = j0 + it * TKT, n = min(TKT, j1 - t0), slot = it % ST;
+    cp_async_wait<ST - 2>();
+    __syncthreads();  // tile it has landed; every thread is past tile it - 1
+    const uint8_t* kt = sm + SM_K + slot * KT_BYTES;
+    const uint8_t* vt = sm + SM_V + slot * KT_BYTES;
+    {  // logits: four threads per key, a quarter of the row each; each warp's maximum
+      const int key = tid >> 2, q4 = tid & 3;
+      float a = 0.f;
+      if (key < n) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint4 w = *reinterpret_cast<const uint4*>(kt + kofs(key, 2 * q4 + h2));
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int f = 16 * q4 + 8 * h2 + 2 * t;
+            a = fmaf(qs[f], lo16(ww[t]), a);
+            a = fmaf(qs[f + 1], hi16(ww[t]), a);
+          }
+        }
+      }
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      const float sa = key < n ? a : -INFINITY;
+      if (q4 == 0) sS[key] = sa;
+      float wm = sa;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+      if (lane == 0) red[warp] = wm;
+    }
+    // The MMAs of tile it - 1 read the ring slot refilled below and the A operands rebuilt
+    // below; a rescale also needs their sums final. Their issuer waits, then the barrier.
+    if (tid == 0 && it >= 1 && !mbar_wait(&mbar, (it - 1) & 1, status, kStatusTimeout, abort_p))
+      *abort_p = 1;
+    __syncthreads();
+    float tm = red[0];
+#pragma unroll
+    for (int w = 1; w < NT / 32; ++w) tm = fmaxf(tm, red[w]);
+    if (m == -INFINITY || (tm - m) * inv_h > kShiftSlack) {
+      if (m != -INFINITY) {  // move the accumulated sums to the new shift
+        const float sc = __expf((m - tm) * inv_h);
+        tc_fence_after();
+        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (warp >> 2) * 64;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t x[16];
+          tmem_ld16(tl + c0, x);
+          tmem_ld_wait();
+          uint32_t y0[8], y1[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            y0[t] = __float_as_uint(__uint_as_float(x[t]) * sc);
+            y1[t] = __float_as_uint(__uint_as_float(x[8 + t]) * sc);
+          }
+          tmem_st8(tl + c0, y0);
+          tmem_st8(tl + c0 + 8, y1);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { acc_k[e] *= sc; acc_v[e] *= sc; }
+        om *= sc;
+      }
+      m = tm;
+    }
+    prefetch(it + ST - 1);  // into slot (it - 1) % ST
+    uint8_t* ak = sm + SM_A;
+    uint8_t* av = ak + A_BYTES;
+    const float mc = m * c2;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = jr + 32 * u;
+      // the weight (bf16), formed by each of the eight threads that use it
+      const float p = j < n ? lo16(pack2(ex2f_approx(fmaf(sS[j], c2, -mc)), 0.f)) : 0.f;
+      if (c8 == 0) om += p;
+      const uint32_t pp = pack2(p, p);  // exact: p is a bf16 value
+      const uint4 kw = *reinterpret_cast<const uint4*>(kt + kofs(j, c8));
+      const uint4 vw = *reinterpret_cast<const uint4*>(vt + kofs(j, c8));
+      uint4 h, l;
+      split_products(pp, kw, h, l, acc_k);
+      *reinterpret_cast<uint4*>(ak + aofs(j, c8)) = h;
+      *reinterpret_cast<uint4*>(ak + aofs(j, 8 + c8)) = l;
+      split_products(pp, vw, h, l, acc_v);
+      *reinterpret_cast<uint4*>(av + aofs(j, c8)) = h;
+      *reinterpret_cast<uint4*>(av + aofs(j, 8 + c8)) = l;
+    }
+    fence_proxy_async_smem();  // the A operands (generic-proxy writes) before the MMAs read them
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      fence_proxy_async_smem();  // the key tile's cp.async writes
+      const uint64_t adk = smem_desc(smem_u32(ak), 2048, 128);
+      const uint64_t adv = smem_desc(smem_u32(av), 2048, 128);
+      const uint64_t bd = smem_desc(smem_u32(kt), 1024, 128);
+      constexpr uint32_t id = idesc_bf16(128, D, true, true);
+#pragma unroll
+      for (int s4 = 0; s4 < TKT / 16; ++s4) {
+        const uint32_t acc = (it > 0 || s4 > 0) ? 1u : 0u;
+        mma_ss(tbase + T_KK, adk + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
+        mma_ss(tbase + T_VK, adv + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
+      }
+      mma_commit(&mbar);
+    }
+  }
+  cp_async_wait<0>();
+  {
+    // every MMA has completed before the accumulators are read and tensor memory is released
+    // (a bounded wait, whatever the abort flag says)
+    volatile int never = 0;
+    if (ntl >= 1) mbar_wait(&mbar, (ntl - 1) & 1, status, kStatusTimeout, &never);
+  }
+  tc_fence_after();
+  // sums of the CUDA-core partials: over the four key rows of each warp (lanes 8 apart), then
+  // over the warps in a fixed order
+  // over the eight keys of each lane group (lanes 1, 2, 4 apart), then in the final sums over
+  // the four key groups (warps 2 kg + c8 / 4) in a fixed order
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      acc_k[e] += __shfl_xor_sync(0xffffffffu, acc_k[e], o);
+      acc_v[e] += __shfl_xor_sync(0xffffffffu, acc_v[e], o);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) om += __shfl_xor_sync(0xffffffffu, om, o);
+  if ((lane & 7) == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      xs[warp][0][8 * (lane >> 3) + e] = acc_k[e];
+      xs[warp][1][8 * (lane >> 3) + e] = acc_v[e];
+    }
+  }
+  if (lane == 0) xo[warp] = om;
+  // the accumulators (128 rows: hi rows 0..63, lo rows 64..127) into shared memory
+  float* xm = dsm;  // [2][128][XLD]
+  {
+    const int quarter = warp & 3, mat = warp >> 2, row = quarter * 32 + lane;
+    const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + mat * 64;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      uint32_t x[16];
+      tmem_ld16(tl + c0, x);
+      tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < 16; ++t) xm[(mat * 128 + row) * XLD + c0 + t] = __uint_as_float(x[t]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+  float* pp = part + blockIdx.x * (long long)P;
+  if (tid == 0) {
+    float o = 0.f;
+    for (int w = 0; w < NT / 32; ++w) o += xo[w];
+    pp[0] = m;
+    pp[1] = o;
+  }
+  if (tid < 2 * D) {
+    const int which = tid / D, a = tid % D, c = a >> 3;  // element a: chunk c, lane group c & 3
+    float sum = 0.f;
+    for (int kg = 0; kg < 4; ++kg) sum += xs[2 * kg + (c >> 2)][which][8 * (c & 3) + (a & 7)];
+    pp[2 + tid] = sum;  // sk[a] (which 0), then sv[a]
+  }
+  for (int e = tid; e < 2 * D * D; e += NT) {
+    const int mat = e / (D * D), a = (e / D) % D, b = e % D;
+    pp[2 + 2 * D + e] = xm[(mat * 128 + a) * XLD + b] + xm[(mat * 128 + 64 + a) * XLD + b];
+  }
+  if (!last_arrival(counter + bh, S, &is_last)) return;
+  lla_merge_solve<__nv_bfloat16, D, D>(qs, part, bh, S, inv_h, lam, dsm, &fail_s, out, status);
+}
+
+bool decode_on_tc(const DecodeArgs& a) {
+  return !a.r && a.dtype == LLA_BF16 && a.d == 64 && a.dv == 64 && a.path != kPathCudaCore;
+}
+
+int choose_splits(long long BH, int L, int per_sm = 2) {
   int sms = 148;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long s = (2ll * sms + BH - 1) / BH;  // about two CTAs per SM
+  long long s = ((long long)per_sm * sms + BH - 1) / BH;  // about per_sm CTAs per SM
   const long long smax = (L + TK - 1) / TK;  // at least a tile of keys per CTA
   if (s > smax) s = smax;
   if (s > 512) s = 512;
@@ -569,8 +905,35 @@ cudaError_t launch_ll(const DecodeArgs& a, void* ws, int* status, cudaStream_t s
   return cudaGetLastError();
 }
 
+// The tensor-core split kernel takes about four CTAs' worth of chunks per SM (two resident).
+int decode_splits(const DecodeArgs& a) {
+  return decode_on_tc(a) ? choose_splits(a.BH(), a.L, 4) : choose_splits(a.BH(), a.L);
+}
+
+cudaError_t launch_ll_tc(const DecodeArgs& a, void* ws, int* status, cudaStream_t st) {
+  constexpr int D = dtc::D;
+  constexpr int P = lla_part<D, D>();
+  const int S = decode_splits(a);
+  float* part = static_cast<float*>(ws);
+  int* cnt = reinterpret_cast<int*>(part + a.BH() * S * P);
+  const size_t solve = sizeof(double) * (P + D + S);
+  const size_t smem = solve > (size_t)dtc::SMEM ? solve : (size_t)dtc::SMEM;
+  cudaError_t err = cudaFuncSetAttribute(lla_decode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  zero_counters<<<(unsigned)((a.BH() + 255) / 256), 256, 0, st>>>(cnt, (int)a.BH());
+  count_launch();
+  lla_decode_tc_kernel<<<(unsigned)(a.BH() * S), NT, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), a.L, S, 1.f / a.h, a.lam, part, cnt,
+      static_cast<__nv_bfloat16*>(a.out), status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 template <typename TIn>
 cudaError_t dispatch(const DecodeArgs& a, void* ws, int* status, cudaStream_t st) {
+  if (decode_on_tc(a)) return launch_ll_tc(a, ws, status, st);
 #define LLA_DEC(DD, VV)                                                                  \
   if (a.d == DD && a.dv == VV)                                                           \
     return a.r ? launch_px<TIn, DD, VV>(a, ws, st) : launch_ll<TIn, DD, VV>(a, ws, status, st);
@@ -584,7 +947,7 @@ cudaError_t dispatch(const DecodeArgs& a, void* ws, int* status, cudaStream_t st
 }  // namespace
 
 size_t decode_workspace_bytes(const DecodeArgs& a) {
-  const int S = choose_splits(a.BH(), a.L);
+  const int S = decode_splits(a);
   const size_t per = a.r ? (size_t)(3 + 2 * a.dv) : (size_t)(2 + a.d + a.dv + a.d * a.d + a.dv * a.d);
   return sizeof(float) * per * (size_t)a.BH() * S + sizeof(int) * (size_t)a.BH() + 256;
 }

@@ -143,6 +143,7 @@ struct DecodeArgs {
   int B, H, L, d, dv;
   float h, lam;
   int dtype;
+  int path = 0;  // LLA, bf16, d = dv = 64: tensor cores unless kPathCudaCore
   long long BH() const { return (long long)B * H; }
 };
 // Causal Parallax backward (the gradients of lla_parallax_forward with respect to q, k, v, r).

@@ -117,3 +117,51 @@ def test_decode_argument_errors(lla):
     assert lib.lla_decode(p, p, p, p, 0, 1, 8, 64, 64, 8.0, 1e-2, 1, None) == 0  # empty batch
     assert lib.lla_parallax_decode(p, p, p, None, p, 1, 1, 8, 64, 64, 8.0, 1, None) == 1
     del ctypes_ptr
+
+
+# Tensor-core split kernel (bf16, d = dv = 64): the chunk's sums as tcgen05 contractions with
+# exact hi/lo operands, the shift of the sums moved only when a tile's maximum logit exceeds it
+# by more than 8 ln 2 h (then the accumulators in tensor memory are rescaled).
+TC_LENGTHS = [1, 63, 64, 65, 200, 1000, 4099, 20000]
+
+
+@pytest.mark.parametrize("L", TC_LENGTHS)
+def test_lla_decode_tensor_cores_match_oracle_and_cuda_cores(lla, L):
+    B, H, d = 2, 3, 64
+    q, k, v, _ = make(B, H, L, d, d, "bf16", seed=100 + L)
+    h, lam = 8.0, 1e-2
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    tc = lla.lla_decode(qc, kc, vc, h, lam)
+    assert lla.lla_stream_status() == 0
+    lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
+    try:
+        cc = lla.lla_decode(qc, kc, vc, h, lam)
+        assert lla.lla_stream_status() == 0
+    finally:
+        lla.lla_set_moments_path(lla.PATH_AUTO)
+    Q, K, V = f64(q).reshape(-1, d), f64(k).reshape(-1, L, d), f64(v).reshape(-1, L, d)
+    ref = np.stack([lla_row(Q[i], K[i], V[i], h, lam) for i in range(B * H)])
+    got_tc, got_cc = f64(tc).reshape(-1, d), f64(cc).reshape(-1, d)
+    assert rel_err(got_tc, ref) <= TOL["bf16"]
+    assert rel_err(got_cc, ref) <= TOL["bf16"]
+    assert rel_err(got_tc, got_cc) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_lla_decode_tensor_cores_moving_logit_scale(lla, direction):
+    # Key norms grow (or shrink) along the cache, so each tile's maximum logit keeps exceeding the
+    # shift of the sums by more than the slack (rising: the accumulators are rescaled many times)
+    # or never does after the first tile (falling).
+    B, H, L, d = 1, 4, 6000, 64
+    g = torch.Generator().manual_seed(41 if direction == "rising" else 43)
+    q = torch.randn(B, H, d, generator=g)
+    ramp = torch.linspace(0.2, 3.0, L) if direction == "rising" else torch.linspace(3.0, 0.2, L)
+    k = torch.randn(B, H, L, d, generator=g) * ramp[None, None, :, None]
+    v = torch.randn(B, H, L, d, generator=g)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    h, lam = 8.0, 1e-2
+    out = lla.lla_decode(q.cuda(), k.cuda(), v.cuda(), h, lam)
+    assert lla.lla_stream_status() == 0
+    Q, K, V = f64(q).reshape(-1, d), f64(k).reshape(-1, L, d), f64(v).reshape(-1, L, d)
+    ref = np.stack([lla_row(Q[i], K[i], V[i], h, lam) for i in range(B * H)])
+    assert rel_err(f64(out).reshape(-1, d), ref) <= TOL["bf16"]
