@@ -315,7 +315,7 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
                                 int S, float inv_h, float lam, float* dsm, int* fail_flag,
                                 TIn* __restrict__ out, int* __restrict__ status) {
   constexpr int P = lla_part<D, DV>();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
   int& fail_s = *fail_flag;
 
   // ---- merge (fp32: the partials are fp32 sums, the weights <= 1), then centre and solve in
@@ -326,17 +326,27 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
   const float* hp = part + bh * S * (long long)P;
   float M = -INFINITY;
   for (int t = 0; t < S; ++t) M = fmaxf(M, __ldcg(hp + t * (long long)P));
-  for (int t = tid; t < S; t += NT) {
+  for (int t = tid; t < S; t += nt) {
     const float mt = __ldcg(hp + t * (long long)P);
     alpha[t] = mt == -INFINITY ? 0.f : expf((mt - M) * inv_h);
   }
   __syncthreads();
   constexpr int SKK0 = 1 + D + DV;  // offset of Skk in mom (mom[e] is partial entry 1 + e)
-  for (int e = tid; e < P - 1; e += NT) {
+  for (int e = tid; e < P - 1; e += nt) {
     const bool lower = e >= SKK0 && e < SKK0 + D * D && (e - SKK0) / D > (e - SKK0) % D;
     float acc = 0.f;
-    if (!lower)
-      for (int t = 0; t < S; ++t) acc = fmaf(alpha[t], __ldcg(hp + t * (long long)P + 1 + e), acc);
+    if (!lower) {
+      // eight independent loads in flight per step, summed in split order
+      int t = 0;
+      for (; t + 8 <= S; t += 8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __ldcg(hp + (t + u) * (long long)P + 1 + e);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc = fmaf(alpha[t + u], x[u], acc);
+      }
+      for (; t < S; ++t) acc = fmaf(alpha[t], __ldcg(hp + t * (long long)P + 1 + e), acc);
+    }
     mom[e] = (double)acc;
   }
   __syncthreads();
@@ -346,7 +356,7 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
   double* A = mom + SKK0;                // Skk (upper) -> C_kk + lambda' I -> its Cholesky factor
   const double* Svk = A + D * D;
   const double lp = (double)lam * exp(-(double)M * inv_h);  // ridge scaled by exp(-M/h)
-  for (int e = tid; e < D * D; e += NT) {
+  for (int e = tid; e < D * D; e += nt) {
     const int a = e / D, b = e % D;
     if (a <= b) {
       const double c = A[e] - msk[a] * msk[b] / omega + (a == b ? lp : 0.0);
@@ -354,7 +364,7 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
       A[b * D + a] = c;
     }
   }
-  for (int a = tid; a < D; a += NT) z[a] = (double)qs[a] - msk[a] / omega;
+  for (int a = tid; a < D; a += nt) z[a] = (double)qs[a] - msk[a] / omega;
   if (tid == 0) fail_s = 0;
   __syncthreads();
   // Cholesky A = L L^T (lower triangle in place), column by column
@@ -365,9 +375,9 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
       A[c * D + c] = sqrt(piv > 0.0 ? piv : 1.0);
     }
     __syncthreads();
-    for (int i = c + 1 + tid; i < D; i += NT) A[i * D + c] /= A[c * D + c];
+    for (int i = c + 1 + tid; i < D; i += nt) A[i * D + c] /= A[c * D + c];
     __syncthreads();
-    for (int e = tid; e < D * D; e += NT) {
+    for (int e = tid; e < D * D; e += nt) {
       const int i = e / D, j = e % D;
       if (j > c && i >= j) A[i * D + j] -= A[i * D + c] * A[j * D + c];
     }
@@ -393,7 +403,7 @@ __device__ void lla_merge_solve(const float* qs, const float* __restrict__ part,
   __syncthreads();
   // o = vbar + C_vk y,  C_vk = Svk - sv sk^T / omega
   const bool bad = fail_s != 0;
-  for (int c = tid; c < DV; c += NT) {
+  for (int c = tid; c < DV; c += nt) {
     double o = msv[c] / omega;
     for (int b = 0; b < D; ++b) o += (Svk[c * D + b] - msv[c] * msk[b] / omega) * z[b];
     stf(out, bh * DV + c, bad ? __int_as_float(0x7fc00000) : (float)o);
@@ -548,13 +558,15 @@ lla_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
 namespace dtc {
 constexpr int D = 64;
 constexpr int TKT = 64;                    // keys per tile
-constexpr int ST = 3;                      // key / value ring stages
+constexpr int ST = 4;                      // key / value ring stages
+constexpr int NCW = 8;                     // compute warps; warp NCW loads
+constexpr int NTC = (NCW + 1) * 32;
 constexpr int A_BYTES = 128 * TKT * 2;     // one A operand: 128 rows x 64 keys, bf16
 constexpr int KT_BYTES = TKT * D * 2;      // one key or value tile
 constexpr int SM_A = 0;                    // A_k, A_v
 constexpr int SM_K = SM_A + 2 * A_BYTES;   // ST key tiles (core-matrix layout: the B operand)
 constexpr int SM_V = SM_K + ST * KT_BYTES; // ST value tiles (the same layout)
-constexpr int SMEM = SM_V + ST * KT_BYTES; // 80 KiB
+constexpr int SMEM = SM_V + ST * KT_BYTES; // 96 KiB
 constexpr int XLD = 65;                    // row stride (floats) of the accumulator copy
 static_assert(2 * 128 * XLD * 4 <= SMEM, "accumulator copy fits the tiles' space");
 constexpr uint32_t T_KK = 0, T_VK = 64, TMEM_COLS = 128;
@@ -581,6 +593,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
+// Barrier among the compute warps only (named barrier 1; the loader warp does not take part).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ float ex2f_approx(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -605,7 +619,7 @@ __device__ __forceinline__ void split_products(uint32_t pp, const uint4& x, uint
 }
 }  // namespace dtc
 
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(dtc::NTC)
 lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                      const __nv_bfloat16* __restrict__ v, int L, int S, float inv_h, float lam,
                      float* __restrict__ part, int* __restrict__ counter,
@@ -613,13 +627,14 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
   using namespace dtc;
   using namespace tc;
   constexpr int P = lla_part<D, D>();
-  static_assert(NT == 256 && TKT * 4 == NT, "four threads per key; eight per feature chunk");
+  static_assert(NCW * 32 == 256 && TKT * 4 == 256, "four threads per key; eight per chunk");
   extern __shared__ __align__(1024) float dtc_smem[];
   float* const dsm = dtc_smem;
   uint8_t* const sm = reinterpret_cast<uint8_t*>(dsm);
-  __shared__ float qs[D], red[NT / 32], sS[TKT], xo[NT / 32];
-  __shared__ float xs[NT / 32][2][D];
-  __shared__ uint64_t mbar;  // the MMAs of a tile completed (one phase per tile)
+  __shared__ float qs[D], red[NCW], sS[TKT], xo[NCW];
+  __shared__ float xs[NCW][2][D];
+  __shared__ uint64_t mbar;            // the MMAs of a tile completed (one phase per tile)
+  __shared__ uint64_t full[ST], empty[ST];  // ring slot landed / released by its tile's MMAs
   __shared__ uint32_t tmem_base_s;
   __shared__ int is_last, fail_s, abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -630,9 +645,13 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
   const int ntl = j1 > j0 ? (j1 - j0 + TKT - 1) / TKT : 0;
   const __nv_bfloat16* kb = k + bh * (long long)L * D;
   const __nv_bfloat16* vb = v + bh * (long long)L * D;
-  for (int a = tid; a < D; a += NT) qs[a] = __bfloat162float(q[bh * D + a]);
+  for (int a = tid; a < D; a += dtc::NTC) qs[a] = __bfloat162float(q[bh * D + a]);
   if (tid == 0) {
     mbar_init(&mbar, 1);
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(&full[i], 32);  // one cp.async completion arrival per loader lane
+      mbar_init(&empty[i], 1);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -646,14 +665,21 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
   const uint32_t tbase = tmem_base_s;
   volatile int* abort_p = &abort_flag;
 
-  // Tile `it` of the chunk into ring slot it % ST (rows past the chunk zero-filled without being
-  // read); one commit group per call, empty past the last tile.
-  auto prefetch = [&](int it) {
-    if (it < ntl) {
-      const int t0 = j0 + it * TKT, n = min(TKT, j1 - t0), slot = it % ST;
+  float m = -INFINITY;  // the shift of this CTA's sums (raw logit units)
+  float acc_k[8], acc_v[8], om = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) { acc_k[e] = 0.f; acc_v[e] = 0.f; }
+  if (warp == NCW) {
+    // ---- loader: tile it into ring slot it % ST once the MMAs of tile it - ST released it; each
+    // lane's copies complete on the slot's barrier (rows past the chunk zero-filled unread)
+    for (int it = 0; it < ntl; ++it) {
+      const int slot = it % ST;
+      if (it >= ST && !mbar_wait(&empty[slot], ((it / ST) - 1) & 1, status, kStatusTimeout, abort_p)) break;
+      const int t0 = j0 + it * TKT, n = min(TKT, j1 - t0);
       uint8_t* kd = sm + SM_K + slot * KT_BYTES;
       uint8_t* vd = sm + SM_V + slot * KT_BYTES;
-      for (int e = tid; e < TKT * 8; e += NT) {
+#pragma unroll 4
+      for (int e = lane; e < TKT * 8; e += 32) {
         // each group of eight lanes: eight consecutive keys, one chunk (distinct banks)
         const int j = (e & 7) + 8 * (e >> 6), c = (e >> 3) & 7;
         const bool in = j < n;
@@ -661,158 +687,153 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
         cp_async16(kd + kofs(j, c), kb + row * D + c * 8, in ? 16u : 0u);
         cp_async16(vd + kofs(j, c), vb + row * D + c * 8, in ? 16u : 0u);
       }
+      cp_async_mbar_arrive(&full[slot]);
     }
     cp_async_commit();
-  };
-
-  float m = -INFINITY;  // the shift of this CTA's sums (raw logit units)
-  float acc_k[8], acc_v[8], om = 0.f;
+    cp_async_wait<0>();  // nothing of this warp is in flight past here
+  } else {
+    // ---- compute warps 0 .. NCW - 1 (named barrier 1 among them)
+    // A operands: elements 8 c8 .. 8 c8 + 7 of keys jr and jr + 32; each group of eight lanes
+    // takes eight consecutive keys of one chunk (16-byte loads and stores in distinct banks).
+    const int c8 = (tid >> 3) & 7, jr = (tid & 7) + 8 * (tid >> 6);
+    const float c2 = inv_h * 1.4426950408889634f;
+    for (int it = 0; it < ntl; ++it) {
+      const int n = min(TKT, j1 - (j0 + it * TKT)), slot = it % ST;
+      if (!mbar_wait(&full[slot], (it / ST) & 1, status, kStatusTimeout, abort_p)) *abort_p = 1;
+      const uint8_t* kt = sm + SM_K + slot * KT_BYTES;
+      const uint8_t* vt = sm + SM_V + slot * KT_BYTES;
+      {  // logits: four threads per key, a quarter of the row each; each warp's maximum
+        const int key = tid >> 2, q4 = tid & 3;
+        float a = 0.f;
+        if (key < n) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) { acc_k[e] = 0.f; acc_v[e] = 0.f; }
-  // A operands: elements 8 c8 .. 8 c8 + 7 of keys jr and jr + 32. Each group of eight lanes takes
-  // eight consecutive keys of one chunk, so that its 16-byte loads and stores (core matrices:
-  // the keys of a chunk 16 bytes apart) fall in distinct banks.
-  const int c8 = (tid >> 3) & 7, jr = (tid & 7) + 8 * (tid >> 6);
-  const float c2 = inv_h * 1.4426950408889634f;
-  for (int it = 0; it < ST - 1; ++it) prefetch(it);
-  for (int it = 0; it < ntl; ++it) {
-    const int t0 = j0 + it * TKT, n = min(TKT, j1 - t0), slot = it % ST;
-    cp_async_wait<ST - 2>();
-    __syncthreads();  // tile it has landed; every thread is past tile it - 1
-    const uint8_t* kt = sm + SM_K + slot * KT_BYTES;
-    const uint8_t* vt = sm + SM_V + slot * KT_BYTES;
-    {  // logits: four threads per key, a quarter of the row each; each warp's maximum
-      const int key = tid >> 2, q4 = tid & 3;
-      float a = 0.f;
-      if (key < n) {
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint4 w = *reinterpret_cast<const uint4*>(kt + kofs(key, 2 * q4 + h2));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint4 w = *reinterpret_cast<const uint4*>(kt + kofs(key, 2 * q4 + h2));
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int f = 16 * q4 + 8 * h2 + 2 * t;
-            a = fmaf(qs[f], lo16(ww[t]), a);
-            a = fmaf(qs[f + 1], hi16(ww[t]), a);
+            for (int t = 0; t < 4; ++t) {
+              const int f = 16 * q4 + 8 * h2 + 2 * t;
+              a = fmaf(qs[f], lo16(ww[t]), a);
+              a = fmaf(qs[f + 1], hi16(ww[t]), a);
+            }
           }
         }
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        const float sa = key < n ? a : -INFINITY;
+        if (q4 == 0) sS[key] = sa;
+        float wm = sa;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        if (lane == 0) red[warp] = wm;
       }
-      a += __shfl_xor_sync(0xffffffffu, a, 1);
-      a += __shfl_xor_sync(0xffffffffu, a, 2);
-      const float sa = key < n ? a : -INFINITY;
-      if (q4 == 0) sS[key] = sa;
-      float wm = sa;
+      // The MMAs of tile it - 1 read the A operands rebuilt below (and a rescale needs their sums
+      // final): their issuer waits for them before the barrier.
+      if (tid == 0 && it >= 1 && !mbar_wait(&mbar, (it - 1) & 1, status, kStatusTimeout, abort_p))
+        *abort_p = 1;
+      compute_sync();
+      float tm = red[0];
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-      if (lane == 0) red[warp] = wm;
-    }
-    // The MMAs of tile it - 1 read the ring slot refilled below and the A operands rebuilt
-    // below; a rescale also needs their sums final. Their issuer waits, then the barrier.
-    if (tid == 0 && it >= 1 && !mbar_wait(&mbar, (it - 1) & 1, status, kStatusTimeout, abort_p))
-      *abort_p = 1;
-    __syncthreads();
-    float tm = red[0];
-#pragma unroll
-    for (int w = 1; w < NT / 32; ++w) tm = fmaxf(tm, red[w]);
-    if (m == -INFINITY || (tm - m) * inv_h > kShiftSlack) {
-      if (m != -INFINITY) {  // move the accumulated sums to the new shift
-        const float sc = __expf((m - tm) * inv_h);
-        tc_fence_after();
-        const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (warp >> 2) * 64;
+      for (int w = 1; w < NCW; ++w) tm = fmaxf(tm, red[w]);
+      if (m == -INFINITY || (tm - m) * inv_h > kShiftSlack) {
+        if (m != -INFINITY) {  // move the accumulated sums to the new shift
+          const float sc = __expf((m - tm) * inv_h);
+          tc_fence_after();
+          const uint32_t tl = tbase + ((uint32_t)((warp & 3) * 32) << 16) + (warp >> 2) * 64;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          uint32_t x[16];
-          tmem_ld16(tl + c0, x);
-          tmem_ld_wait();
-          uint32_t y0[8], y1[8];
+          for (int c0 = 0; c0 < 64; c0 += 16) {
+            uint32_t x[16];
+            tmem_ld16(tl + c0, x);
+            tmem_ld_wait();
+            uint32_t y0[8], y1[8];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            y0[t] = __float_as_uint(__uint_as_float(x[t]) * sc);
-            y1[t] = __float_as_uint(__uint_as_float(x[8 + t]) * sc);
+            for (int t = 0; t < 8; ++t) {
+              y0[t] = __float_as_uint(__uint_as_float(x[t]) * sc);
+              y1[t] = __float_as_uint(__uint_as_float(x[8 + t]) * sc);
+            }
+            tmem_st8(tl + c0, y0);
+            tmem_st8(tl + c0 + 8, y1);
           }
-          tmem_st8(tl + c0, y0);
-          tmem_st8(tl + c0 + 8, y1);
+          tmem_st_wait();
+          tc_fence_before();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { acc_k[e] *= sc; acc_v[e] *= sc; }
+          om *= sc;
         }
-        tmem_st_wait();
-        tc_fence_before();
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { acc_k[e] *= sc; acc_v[e] *= sc; }
-        om *= sc;
+        m = tm;
       }
-      m = tm;
-    }
-    prefetch(it + ST - 1);  // into slot (it - 1) % ST
-    uint8_t* ak = sm + SM_A;
-    uint8_t* av = ak + A_BYTES;
-    const float mc = m * c2;
+      uint8_t* ak = sm + SM_A;
+      uint8_t* av = ak + A_BYTES;
+      const float mc = m * c2;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int j = jr + 32 * u;
-      // the weight (bf16), formed by each of the eight threads that use it
-      const float p = j < n ? lo16(pack2(ex2f_approx(fmaf(sS[j], c2, -mc)), 0.f)) : 0.f;
-      if (c8 == 0) om += p;
-      const uint32_t pp = pack2(p, p);  // exact: p is a bf16 value
-      const uint4 kw = *reinterpret_cast<const uint4*>(kt + kofs(j, c8));
-      const uint4 vw = *reinterpret_cast<const uint4*>(vt + kofs(j, c8));
-      uint4 h, l;
-      split_products(pp, kw, h, l, acc_k);
-      *reinterpret_cast<uint4*>(ak + aofs(j, c8)) = h;
-      *reinterpret_cast<uint4*>(ak + aofs(j, 8 + c8)) = l;
-      split_products(pp, vw, h, l, acc_v);
-      *reinterpret_cast<uint4*>(av + aofs(j, c8)) = h;
-      *reinterpret_cast<uint4*>(av + aofs(j, 8 + c8)) = l;
+      for (int u = 0; u < 2; ++u) {
+        const int j = jr + 32 * u;
+        // the weight (bf16), formed by each of the eight threads that use it
+        const float p = j < n ? lo16(pack2(ex2f_approx(fmaf(sS[j], c2, -mc)), 0.f)) : 0.f;
+        if (c8 == 0) om += p;
+        const uint32_t pp = pack2(p, p);  // exact: p is a bf16 value
+        const uint4 kw = *reinterpret_cast<const uint4*>(kt + kofs(j, c8));
+        const uint4 vw = *reinterpret_cast<const uint4*>(vt + kofs(j, c8));
+        uint4 h, l;
+        split_products(pp, kw, h, l, acc_k);
+        *reinterpret_cast<uint4*>(ak + aofs(j, c8)) = h;
+        *reinterpret_cast<uint4*>(ak + aofs(j, 8 + c8)) = l;
+        split_products(pp, vw, h, l, acc_v);
+        *reinterpret_cast<uint4*>(av + aofs(j, c8)) = h;
+        *reinterpret_cast<uint4*>(av + aofs(j, 8 + c8)) = l;
+      }
+      fence_proxy_async_smem();  // the A operands (generic-proxy writes) before the MMAs read them
+      compute_sync();
+      if (tid == 0) {
+        tc_fence_after();
+        fence_proxy_async_smem();  // the key tile's cp.async writes
+        const uint64_t adk = smem_desc(smem_u32(ak), 2048, 128);
+        const uint64_t adv = smem_desc(smem_u32(av), 2048, 128);
+        const uint64_t bd = smem_desc(smem_u32(kt), 1024, 128);
+        constexpr uint32_t id = idesc_bf16(128, D, true, true);
+#pragma unroll
+        for (int s4 = 0; s4 < TKT / 16; ++s4) {
+          const uint32_t acc = (it > 0 || s4 > 0) ? 1u : 0u;
+          mma_ss(tbase + T_KK, adk + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
+          mma_ss(tbase + T_VK, adv + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
+        }
+        mma_commit(&mbar);
+        mma_commit(&empty[slot]);  // the slot's key and value tiles are no longer read
+      }
     }
-    fence_proxy_async_smem();  // the A operands (generic-proxy writes) before the MMAs read them
-    __syncthreads();
     if (tid == 0) {
-      tc_fence_after();
-      fence_proxy_async_smem();  // the key tile's cp.async writes
-      const uint64_t adk = smem_desc(smem_u32(ak), 2048, 128);
-      const uint64_t adv = smem_desc(smem_u32(av), 2048, 128);
-      const uint64_t bd = smem_desc(smem_u32(kt), 1024, 128);
-      constexpr uint32_t id = idesc_bf16(128, D, true, true);
-#pragma unroll
-      for (int s4 = 0; s4 < TKT / 16; ++s4) {
-        const uint32_t acc = (it > 0 || s4 > 0) ? 1u : 0u;
-        mma_ss(tbase + T_KK, adk + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
-        mma_ss(tbase + T_VK, adv + (uint64_t)(s4 * (4096 >> 4)), bd + (uint64_t)(s4 * (2048 >> 4)), id, acc);
-      }
-      mma_commit(&mbar);
+      // every MMA has completed before the accumulators are read and tensor memory is released
+      // (a bounded wait, whatever the abort flag says)
+      volatile int never = 0;
+      if (ntl >= 1) mbar_wait(&mbar, (ntl - 1) & 1, status, kStatusTimeout, &never);
     }
   }
-  cp_async_wait<0>();
-  {
-    // every MMA has completed before the accumulators are read and tensor memory is released
-    // (a bounded wait, whatever the abort flag says)
-    volatile int never = 0;
-    if (ntl >= 1) mbar_wait(&mbar, (ntl - 1) & 1, status, kStatusTimeout, &never);
-  }
+  __syncthreads();
   tc_fence_after();
-  // sums of the CUDA-core partials: over the four key rows of each warp (lanes 8 apart), then
-  // over the warps in a fixed order
-  // over the eight keys of each lane group (lanes 1, 2, 4 apart), then in the final sums over
-  // the four key groups (warps 2 kg + c8 / 4) in a fixed order
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      acc_k[e] += __shfl_xor_sync(0xffffffffu, acc_k[e], o);
-      acc_v[e] += __shfl_xor_sync(0xffffffffu, acc_v[e], o);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) om += __shfl_xor_sync(0xffffffffu, om, o);
-  if ((lane & 7) == 0) {
+  if (warp < NCW) {
+    // sums of the CUDA-core partials: over the eight keys of each lane group (lanes 1, 2, 4
+    // apart), then in the final sums over the four key groups (warps 2 kg + c8 / 4) in a fixed
+    // order
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      xs[warp][0][8 * (lane >> 3) + e] = acc_k[e];
-      xs[warp][1][8 * (lane >> 3) + e] = acc_v[e];
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        acc_k[e] += __shfl_xor_sync(0xffffffffu, acc_k[e], o);
+        acc_v[e] += __shfl_xor_sync(0xffffffffu, acc_v[e], o);
+      }
     }
-  }
-  if (lane == 0) xo[warp] = om;
-  // the accumulators (128 rows: hi rows 0..63, lo rows 64..127) into shared memory
-  float* xm = dsm;  // [2][128][XLD]
-  {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) om += __shfl_xor_sync(0xffffffffu, om, o);
+    if ((lane & 7) == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        xs[warp][0][8 * (lane >> 3) + e] = acc_k[e];
+        xs[warp][1][8 * (lane >> 3) + e] = acc_v[e];
+      }
+    }
+    if (lane == 0) xo[warp] = om;
+    // the accumulators (128 rows: hi rows 0..63, lo rows 64..127) into shared memory
+    float* xm = dsm;  // [2][128][XLD]
     const int quarter = warp & 3, mat = warp >> 2, row = quarter * 32 + lane;
     const uint32_t tl = tbase + ((uint32_t)(quarter * 32) << 16) + mat * 64;
 #pragma unroll 1
@@ -830,10 +851,11 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     tc_fence_after();
     tmem_dealloc(tbase, TMEM_COLS);
   }
+  const float* xm = dsm;
   float* pp = part + blockIdx.x * (long long)P;
   if (tid == 0) {
     float o = 0.f;
-    for (int w = 0; w < NT / 32; ++w) o += xo[w];
+    for (int w = 0; w < NCW; ++w) o += xo[w];
     pp[0] = m;
     pp[1] = o;
   }
@@ -843,7 +865,7 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
     for (int kg = 0; kg < 4; ++kg) sum += xs[2 * kg + (c >> 2)][which][8 * (c & 3) + (a & 7)];
     pp[2 + tid] = sum;  // sk[a] (which 0), then sv[a]
   }
-  for (int e = tid; e < 2 * D * D; e += NT) {
+  for (int e = tid; e < 2 * D * D; e += dtc::NTC) {
     const int mat = e / (D * D), a = (e / D) % D, b = e % D;
     pp[2 + 2 * D + e] = xm[(mat * 128 + a) * XLD + b] + xm[(mat * 128 + 64 + a) * XLD + b];
   }
@@ -923,7 +945,7 @@ cudaError_t launch_ll_tc(const DecodeArgs& a, void* ws, int* status, cudaStream_
   if (err != cudaSuccess) return err;
   zero_counters<<<(unsigned)((a.BH() + 255) / 256), 256, 0, st>>>(cnt, (int)a.BH());
   count_launch();
-  lla_decode_tc_kernel<<<(unsigned)(a.BH() * S), NT, smem, st>>>(
+  lla_decode_tc_kernel<<<(unsigned)(a.BH() * S), dtc::NTC, smem, st>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.L, S, 1.f / a.h, a.lam, part, cnt,
       static_cast<__nv_bfloat16*>(a.out), status);
