@@ -663,6 +663,16 @@ def run_decode(args, world, rank):
                 "peak_source": f"HBM copy ({peak_src})", "achieved": gbs, "peak": peak,
                 "unit": "GB/s", "frac": gbs / peak, "traffic": None,
                 "note": "achieved = the K and V cache bytes (read once) per call / call time"}
+    elif dt == "bf16" and d == 64 and dv == 64:
+        # tensor-core decode: ~50 algorithmic flops per cache byte, below the bf16 ridge point
+        # (dense peak / HBM bandwidth ~ 290 flop/B), so the cache read bounds it
+        flops = B * H * L * (2 * d + 2 * (1 + d + dv + d * (d + 1) // 2 + dv * d))
+        peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+        roof = {"kernel": "lla_decode_tc_kernel (lla_decode.cu)", "bound": "hbm",
+                "peak_source": f"HBM copy ({peak_src})", "achieved": gbs, "peak": peak,
+                "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                "algorithmic_tflops": flops / (ms_per_step / 1e3) / 1e12,
+                "note": "achieved = the K and V cache bytes (read once) per call / call time"}
     else:
         # algorithmic per key: the logit q.k and the moments omega, sum p k, sum p v, the upper
         # triangle of sum p k k^T and sum p v k^T
