@@ -13,16 +13,17 @@
 // blog's decode kernel does, Appendix C): each CTA reduces its chunk of keys to partial sums
 // shifted by the chunk's own maximum logit, writes them to a workspace, and the last CTA of the
 // head to finish (an atomic arrival counter after a memory fence) merges them, rescaling each by
-// exp((m_s - M) / h) with M the largest chunk maximum, in a fixed order (so the result does not
+// exp((m_s - M) / h) with M the largest chunk shift, in a fixed order (so the result does not
 // depend on which CTA arrives last), and writes the output. For LLA the merged moments are
 // centred and the d x d ridge system is solved by Cholesky, in double precision (one small system
-// per head). Each CTA takes the exact maximum of its chunk in a first sweep over its keys.
+// per head).
 //
-// The reductions are rank-1 updates per key (the query dimension is 1), so they run on the CUDA
-// cores: each CTA streams its chunk through a ring of raw key/value tiles in shared memory
-// (cp.async, two tiles ahead of the one being reduced), four threads per key form the logits,
-// one thread per key the weight, and the LLA second moments accumulate in 4 x 4 register tiles
-// (two shared loads per 16 FMAs).
+// CUDA-core kernels (Parallax, and LLA for every shape but bf16 d = dv = 64): each CTA streams its
+// chunk through a ring of raw key/value tiles in shared memory (cp.async, two tiles ahead of the
+// one being reduced) with a running maximum, four threads per key form the logits, one thread per
+// key the weight, and the LLA second moments accumulate in 4 x 4 register tiles (two shared loads
+// per 16 FMAs). For bf16 d = dv = 64 the LLA second moments of a chunk are two tensor-core
+// contractions over its keys (lla_decode_tc_kernel, below).
 #include <cfloat>
 #include <cstdint>
 
