@@ -169,9 +169,11 @@ int lla_parallax_forward(const void* q, const void* k, const void* v, const void
  * q: [B,H,d]; k: [B,H,L,d]; v: [B,H,L,dv]; out: [B,H,dv]; device, element type `dtype`, 16-byte
  * aligned; d, dv in {16, 32, 64}; B*H*L < 2^31; h, lambda finite and positive. The cache of each
  * head is split over several CTAs that reduce their chunk to partial moments (float32, shifted by
- * the chunk's maximum logit); the last CTA of the head to finish merges them and solves the
+ * a maximum logit of the chunk); the last CTA of the head to finish merges them and solves the
  * ridge system in float64 (split-KV with a last-arriver merge, as the blog's decode kernel,
- * Appendix C). Asynchronous on `stream`; scratch from the stream-ordered pool. B*H = 0 is a
+ * Appendix C). For bf16 with d = dv = 64 the chunk's second moments run on the tensor cores
+ * (weights rounded to bf16, exact products, float32 sums) unless lla_set_moments_path(1) is in
+ * effect; otherwise on the CUDA cores with float32 weights. Asynchronous on `stream`; scratch from the stream-ordered pool. B*H = 0 is a
  * no-op; L = 0 with B*H > 0 is LLA_ERR_INVALID_ARG. A non-positive pivot (non-finite inputs)
  * makes that head's output NaN and records LLA_ERR_NUMERICAL.
  */
@@ -230,8 +232,8 @@ int lla_version(void);
  * d x d moments and factoring them (see lla_set_cg). Paths 0-2 compute the same moments; 3 solves
  * the same systems iteratively. The choice exists for testing and measurement; a workspace for
  * lla_forward_ws must be sized (lla_workspace_size) under the path it is used with. The same
- * choice applies to lla_parallax_forward (3 as 0). Returns LLA_ERR_INVALID_ARG for any other
- * value. Host-only.
+ * choice applies to lla_parallax_forward, lla_parallax_backward and lla_decode (1 selects their
+ * CUDA-core kernels; 2 and 3 as 0). Returns LLA_ERR_INVALID_ARG for any other value. Host-only.
  */
 int lla_set_moments_path(int path);
 
