@@ -842,8 +842,11 @@ lla_decode_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* _
       uint32_t x[16];
       tmem_ld16(tl + c0, x);
       tmem_ld_wait();
+      // an empty chunk (the last splits of a long cache can get none) has no sums in tensor
+      // memory: its partial is zero, weighted 0 by the merge
 #pragma unroll
-      for (int t = 0; t < 16; ++t) xm[(mat * 128 + row) * XLD + c0 + t] = __uint_as_float(x[t]);
+      for (int t = 0; t < 16; ++t)
+        xm[(mat * 128 + row) * XLD + c0 + t] = ntl > 0 ? __uint_as_float(x[t]) : 0.f;
     }
   }
   tc_fence_before();

@@ -165,3 +165,23 @@ def test_lla_decode_tensor_cores_moving_logit_scale(lla, direction):
     Q, K, V = f64(q).reshape(-1, d), f64(k).reshape(-1, L, d), f64(v).reshape(-1, L, d)
     ref = np.stack([lla_row(Q[i], K[i], V[i], h, lam) for i in range(B * H)])
     assert rel_err(f64(out).reshape(-1, d), ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("path", ["tensor", "cuda"])
+def test_lla_decode_long_cache_with_empty_splits(lla, path):
+    # One head and a long cache: the cache is split 512 ways in chunks of 196 keys, so the last
+    # splits get no keys at all; their partials must drop out of the merge.
+    B, H, L, d = 1, 1, 100000, 64
+    q, k, v, _ = make(B, H, L, d, d, "bf16", seed=61)
+    h, lam = 8.0, 1e-2
+    if path == "cuda":
+        lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
+    try:
+        out = lla.lla_decode(q.cuda(), k.cuda(), v.cuda(), h, lam)
+        assert lla.lla_stream_status() == 0
+    finally:
+        lla.lla_set_moments_path(lla.PATH_AUTO)
+    got = f64(out).reshape(-1, d)
+    assert np.isfinite(got).all()
+    ref = lla_row(f64(q).reshape(d), f64(k).reshape(L, d), f64(v).reshape(L, d), h, lam)
+    assert rel_err(got[0], ref) <= TOL["bf16"]
