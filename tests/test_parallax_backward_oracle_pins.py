@@ -16,12 +16,19 @@ backward oracle is the gradient of the forward oracle taken by the chain rule. I
 
 ``test_pins_catch_planted_mistakes`` plants plausible mistakes into copies of the row gradient and
 checks that at least one pin fails for each.
+
+The same pins (finite differences, the SDPA backward at r = 0, dr = -Sigma_KV^T dO, and agreement of
+an unbatched call with the matching head of a batched one) also run on ``parallax_backward_oracle``
+itself, the whole-tensor function the GPU tests compare against, with several heads of unequal
+content; ``test_whole_tensor_pins_catch_planted_mistakes`` plants mistakes of its bookkeeping (a
+swapped return order, a causal slice that drops the diagonal, transposed heads, values taken from
+another head) and checks that at least one pin fails for each.
 """
 import numpy as np
 import pytest
 import torch
 
-from oracle import parallax_backward_row, parallax_forward_oracle
+from oracle import parallax_backward_oracle, parallax_backward_row, parallax_forward_oracle
 
 
 def rnd(seed, *shape, scale=1.0):
@@ -142,3 +149,136 @@ def _mutant(mistake):
 def test_pins_catch_planted_mistakes(mistake):
     row = _mutant(mistake)
     assert not all(pin(row) for pin in PINS)
+
+
+# ----------------------------------------------------------------------------- the whole-tensor function
+# The GPU tests compare against parallax_backward_oracle itself ([B, H, T, .] tensors, the causal
+# accumulation of dk and dv over every row, the return order (dq, dk, dv, dr)). These pins apply
+# to that function directly, on inputs with several heads of unequal content (B = 2, H = 3), so
+# that a head mix-up, a wrong causal slice or a swapped return value fails at least one of them.
+
+def whole_inputs(seed, B=2, H=3, T=6, d=4, e=3, rscale=0.5):
+    q, k = rnd(seed, B, H, T, d), rnd(seed + 1, B, H, T, d)
+    v, do = rnd(seed + 2, B, H, T, e), rnd(seed + 3, B, H, T, e)
+    r = rnd(seed + 4, B, H, T, d, scale=rscale)
+    # heads of different scale, so that gradients of one head cannot stand in for another's
+    scale = (1.0 + np.arange(B * H)).reshape(B, H, 1, 1) / 3.0
+    return q * scale, k, v * scale, r, do
+
+
+def whole_pin_finite_differences(fn, seed=60, h=1.4):
+    q, k, v, r, do = whole_inputs(seed)
+    grads = fn(q, k, v, r, do, h)
+    if len(grads) != 4:
+        return False
+    dq, dk, dv, dr = grads
+    eps = 1e-5
+    for which, g in enumerate((dq, dk, dv, dr)):  # d/dq, d/dk, d/dv, d/dr
+        x = (q, k, v, r)[which]
+        if g.shape != x.shape:
+            return False
+        delta = rnd(seed + 20 + which, *x.shape)
+        plus = [y.copy() for y in (q, k, v, r)]
+        minus = [y.copy() for y in (q, k, v, r)]
+        plus[which] += eps * delta
+        minus[which] -= eps * delta
+        fd = (np.sum(parallax_forward_oracle(*plus, h) * do)
+              - np.sum(parallax_forward_oracle(*minus, h) * do)) / (2 * eps)
+        if not abs(fd - np.sum(g * delta)) <= 1e-7 * max(1.0, abs(fd)):
+            return False
+    return True
+
+
+def whole_pin_zero_probe_is_sdpa_backward(fn, seed=70, h=0.9):
+    q, k, v, _, do = whole_inputs(seed)
+    dq, dk, dv, _ = fn(q, k, v, np.zeros_like(q), do, h)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=1.0 / h)
+    (o * torch.tensor(do)).sum().backward()
+    return all(np.allclose(a, b.grad.numpy(), rtol=1e-10, atol=1e-12)
+               for a, b in ((dq, tq), (dk, tk), (dv, tv)))
+
+
+def whole_pin_probe_gradient_is_covariance(fn, seed=80, h=1.9):
+    q, k, v, r, do = whole_inputs(seed)
+    dr = fn(q, k, v, r, do, h)[3]
+    B, H, T, _ = q.shape
+    for b in range(B):
+        for hh in range(H):
+            for i in range(T):
+                K, V = k[b, hh, : i + 1], v[b, hh, : i + 1]
+                s = K @ q[b, hh, i] / h
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                cov = ((V - p @ V) * p[:, None]).T @ (K - p @ K)
+                if not np.allclose(dr[b, hh, i], -cov.T @ do[b, hh, i], rtol=1e-10, atol=1e-12):
+                    return False
+    return True
+
+
+def whole_pin_unbatched_matches_batched(fn, seed=90, h=1.2):
+    """A [T, .] call (no leading dimensions) equals the matching head of a batched call."""
+    q, k, v, r, do = whole_inputs(seed)
+    full = fn(q, k, v, r, do, h)
+    one = fn(q[1, 2], k[1, 2], v[1, 2], r[1, 2], do[1, 2], h)
+    return all(a.shape == b[1, 2].shape and np.allclose(a, b[1, 2], rtol=1e-12, atol=1e-14)
+               for a, b in zip(one, full))
+
+
+WHOLE_PINS = (whole_pin_finite_differences, whole_pin_zero_probe_is_sdpa_backward,
+              whole_pin_probe_gradient_is_covariance, whole_pin_unbatched_matches_batched)
+
+
+@pytest.mark.parametrize("pin", WHOLE_PINS, ids=lambda f: f.__name__)
+def test_backward_oracle_whole_tensor_pin(pin):
+    assert pin(parallax_backward_oracle)
+
+
+def _whole_mutant(mistake):
+    """parallax_backward_oracle with one planted mistake of the whole-tensor bookkeeping."""
+    def fn(q, k, v, r, do, h):
+        q, k, v, r, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, r, do))
+        squeeze = q.ndim == 2
+        if squeeze:
+            q, k, v, r, do = q[None], k[None], v[None], r[None], do[None]
+        lead, (T, d), e = q.shape[:-2], q.shape[-2:], v.shape[-1]
+        Q, K, R = q.reshape(-1, T, d), k.reshape(-1, T, d), r.reshape(-1, T, d)
+        V, DO = v.reshape(-1, T, e), do.reshape(-1, T, e)
+        dq, dk, dr, dv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(R), np.zeros_like(V)
+        nbh = Q.shape[0]
+        for bh in range(nbh):
+            src = (bh + 1) % nbh if mistake == "value_of_next_head" else bh
+            for i in range(T):
+                gq, gr, gK, gV = parallax_backward_row(Q[bh, i], K[bh, : i + 1], V[src, : i + 1],
+                                                       R[bh, i], DO[bh, i], h)
+                dq[bh, i], dr[bh, i] = gq, gr
+                if mistake == "slice_drops_diagonal":
+                    dk[bh, :i] += gK[:i]
+                    dv[bh, :i] += gV[:i]
+                else:
+                    dk[bh, : i + 1] += gK
+                    dv[bh, : i + 1] += gV
+        outs = []
+        for x, last in ((dq, d), (dk, d), (dv, e), (dr, d)):
+            if mistake == "heads_transposed" and len(lead) == 2:
+                x = x.reshape(lead[1], lead[0], T, last).swapaxes(0, 1)
+            else:
+                x = x.reshape(*lead, T, last)
+            outs.append(x[0] if squeeze else x)
+        if mistake == "swap_dk_dr":
+            outs[1], outs[3] = outs[3], outs[1]
+        return tuple(outs)
+    return fn
+
+
+@pytest.mark.parametrize("mistake", ["swap_dk_dr", "slice_drops_diagonal", "heads_transposed",
+                                     "value_of_next_head"])
+def test_whole_tensor_pins_catch_planted_mistakes(mistake):
+    fn = _whole_mutant(mistake)
+    assert not all(pin(fn) for pin in WHOLE_PINS)
+
+
+def test_whole_tensor_mutant_without_mistake_passes():
+    """The mutant scaffold itself is faithful: with no planted mistake every pin holds."""
+    fn = _whole_mutant("none")
+    assert all(pin(fn) for pin in WHOLE_PINS)
