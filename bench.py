@@ -60,11 +60,22 @@ def moments_flops_per_pair(d: int) -> int:
     return 2 * d + 2 * (1 + d + d * (d + 1) // 2)
 
 
+def contraction_flops_per_pair(d: int) -> int:
+    """Algorithmic flops per causal pair of the moment contraction alone (the tensor-core path's
+    second moments kernel): omega, sum w k and the upper triangle of sum w k k^T (2 each)."""
+    return 2 * (1 + d + d * (d + 1) // 2)
+
+
 def tc_executed_flops_per_pair(d: int) -> int:
-    """Tensor flops the tcgen05 moments kernel executes per causal pair: q.k in 2 sweeps (the max
-    pass and feature pass 0; passes 1..5 reuse the stored weights) and hi + lo contractions over
-    6 x 368 feature columns."""
-    return 2 * 2 * d + 2 * 2 * 2208
+    """Tensor flops the tcgen05 moment contraction executes per causal pair: hi + lo over
+    5 passes x 448 feature columns (2208 slots and 32 of padding)."""
+    return 2 * 2 * 5 * 448
+
+
+def tc_weights_executed_flops_per_pair(d: int) -> int:
+    """Tensor flops of the weight sweeps per causal pair: q.k twice (the exact-max sweep and the
+    weight sweep)."""
+    return 2 * 2 * d
 
 
 def parallax_flops_per_pair(d: int, dv: int) -> int:
@@ -103,8 +114,14 @@ def kernel_source_sha(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel_file: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+def shape_key(w) -> str:
+    """The workload shape a traffic record belongs to, e.g. "B4 H8 T4096 d64 dv64 bf16"."""
+    return f"B{w.B} H{w.H} T{w.T} d{w.d} dv{w.dv} {w.dtype}"
+
+
+def recorded_traffic(kernel_file: str, w=None):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source and
+    was captured on this workload's shape (bytes of one shape say nothing about another)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -113,6 +130,8 @@ def recorded_traffic(kernel_file: str):
         return None
     ent = rec.get(kernel_file)
     if not ent or ent.get("source_sha") != kernel_source_sha(kernel_file):
+        return None
+    if w is not None and ent.get("shape") != shape_key(w):
         return None
     # a step that also launches kernels of other files is current only if they are unchanged too
     for other, sha in ent.get("depends", {}).items():
@@ -137,7 +156,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -205,6 +224,13 @@ def _oracle_rows(args):
     return time.perf_counter() - t0
 
 
+def _oracle_values(args):
+    h, lam, rows = args
+    from oracle import lla_forward_oracle
+    q, k, v = _POOL_INPUTS["qkv"]
+    return lla_forward_oracle(q, k, v, h, lam, rows=rows)
+
+
 class OracleTimer:
     """The float64 oracle, as it stands, on bounded row samples of a workload: one chunk of rows
     per host core, in spawned single-threaded worker processes that regenerate the workload
@@ -256,9 +282,52 @@ class OracleTimer:
                   f"{how}, {self.cores} single-threaded processes, {wall:.1f} s")
         return len(rows) / wall, self.cores, sample
 
+    def values(self, rows, h, lam):
+        """The oracle's outputs at flat query rows (for the parity check of the timed output)."""
+        import numpy as np
+        chunks = [rows[i::self.cores] for i in range(self.cores)]
+        parts = self.pool.map(_oracle_values, [(h, lam, c) for c in chunks if c])
+        out = np.zeros((len(rows), self.w.dv))
+        it = iter(parts)
+        for i in range(self.cores):
+            if chunks[i]:
+                out[i::self.cores] = next(it)
+        return out
+
     def close(self):
         self.pool.terminate()
         self.pool.join()
+
+
+# ----------------------------------------------------------------------------- timing, parity
+MIN_TIMED_S = 2.0   # device time the timed region spans at least (clock samples under load)
+PARITY_ROWS = 96    # sampled rows of the timed output checked against the oracle
+
+
+def timed_repeats(warm_step_ms: float, steps: int, world: int) -> int:
+    """Repetitions of the K-step timed loop so that the timed region lasts >= MIN_TIMED_S
+    (each repetition times exactly K steps; the same count on every rank)."""
+    est = max(warm_step_ms, 1e-3) * max(steps, 1)
+    reps = int(min(200, max(1, math.ceil(MIN_TIMED_S * 1e3 / est))))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([reps], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        reps = int(t.item())
+    return reps
+
+
+def parity_summary(got, ref, v, bound: float, nrows: int) -> dict:
+    """Relative Frobenius error and the worst row's error (||do_i|| / (||o_i|| + rms V)) of
+    sampled rows of the benchmarked output against the oracle."""
+    import numpy as np
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    rms = float(np.sqrt(np.mean(v.astype(np.float64) ** 2)))
+    row = float((np.linalg.norm(got - ref, axis=1) / (np.linalg.norm(ref, axis=1) + rms)).max())
+    return {"rows": nrows, "rel_frob": rel, "row_max": row, "bound": bound,
+            "ok": bool(rel <= bound), "sample": "uniform over (head, position), seed 77, "
+            "incl. the first and last position of the first and last head"}
 
 
 # ----------------------------------------------------------------------------- main
@@ -394,7 +463,7 @@ def run_parallax(args, w, cpu, world, rank):
                 "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
                                f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
     roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                 "traffic": recorded_traffic("lla_parallax.cu"), "avg_launch_ms": ms_per_step})
+                 "traffic": recorded_traffic("lla_parallax.cu", w), "avg_launch_ms": ms_per_step})
     if rank == 0:
         line = {
             "metric": METRIC_PARALLAX, "value": value, "unit": UNIT, "n_gpus": world,
@@ -535,7 +604,7 @@ def run_parallax_backward(args, w, world, rank):
                                f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
     roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                  "executed_tflops": causal_pairs(w) * exe / (ms_per_step / 1e3) / 1e12,
-                 "traffic": recorded_traffic("lla_parallax_bwd_tc.cu") if tensor_path else None,
+                 "traffic": recorded_traffic("lla_parallax_bwd_tc.cu", w) if tensor_path else None,
                  "avg_launch_ms": ms_per_step / 3})
     if rank == 0:
         line = {
@@ -760,13 +829,17 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    # The oracle's process pool is spawned before any GPU work (rank 0, one GPU only).
+    # The oracle's process pool is spawned before any GPU work (rank 0, one GPU only). It stays
+    # up for the LLA forward, whose timed output it then checks on sampled rows (parity).
     cpu = None
+    timer = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         timer = OracleTimer(args.workload, args.op)
         v, cores, sample = timer.measure(float(os.environ.get("LLA_ORACLE_BUDGET_S", "20")), 900)
-        timer.close()
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        if args.op != "lla" or args.shape:
+            timer.close()
+            timer = None
 
     from local_linear_attention_gb300 import binding as lla
     from local_linear_attention_gb300 import build as lla_build
@@ -780,11 +853,11 @@ def main(argv=None):
         return run_decode(args, world, rank)
 
     lam, h = w.points[0]
+    opts = {}
     if args.strategy == "cg":
-        lla.lla_set_moments_path(lla.PATH_CG)
-        lla.lla_set_cg(args.cg_iters, args.cg_tol)
+        opts.update(path=lla.PATH_CG, cg=(args.cg_iters, args.cg_tol))
     if args.form == "page":
-        lla.lla_set_form(lla.FORM_PAGE)
+        opts.update(form=lla.FORM_PAGE)
     q, k, v = W.make_inputs(w)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     out = torch.empty(w.B, w.H, w.T, w.dv, dtype=dq.dtype, device="cuda")
@@ -792,15 +865,21 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
 
     def step():
-        lla.lla_forward(dq, dk, dv, h, lam, out=out, stream=stream)
+        lla.lla_forward(dq, dk, dv, h, lam, out=out, stream=stream, **opts)
 
-    for _ in range(args.warmup):
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            w0.record(stream)
         step()
+    w1.record(stream)
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during warm-up")
+    reps = timed_repeats(w0.elapsed_time(w1), args.steps, world)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(args.steps * reps)]
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     time.sleep(0.3)
@@ -810,7 +889,7 @@ def main(argv=None):
     n_launch0 = lla.launch_count()
     lla.profile_enable(True)
     t_wall = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(args.steps * reps):
         flush.zero_()
         ev[i][0].record(stream)
         step()
@@ -826,7 +905,10 @@ def main(argv=None):
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during the timed steps")
 
-    ms = sum(a.elapsed_time(b) for a, b in ev)
+    # each repetition times exactly K steps; the line reports the median repetition
+    rep_ms = [sum(a.elapsed_time(b) for a, b in ev[r * args.steps:(r + 1) * args.steps])
+              for r in range(reps)]
+    ms = statistics.median(rep_ms)
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -834,10 +916,19 @@ def main(argv=None):
     ms_per_step = ms / args.steps
     value = w.queries * world / (ms_per_step / 1e3)
 
+    parity = None
+    if timer is not None:  # the oracle leg: sampled rows of the timed output vs the oracle
+        rows = W.sample_rows(w.B * w.H, w.T, PARITY_ROWS, seed=77)
+        ref = timer.values(rows, h, lam)
+        got = out.float().reshape(-1, w.dv)[torch.tensor(rows, device=out.device)]
+        parity = parity_summary(got.cpu().double().numpy(), ref, v.float().numpy(),
+                                1e-3 if w.dtype == "f32" else 2e-2, len(rows))
+        timer.close()
+
     # end to end through the C ABI on pinned host buffers (H2D + compute + D2H every step)
     e2e = None
     eb = q.element_size()
-    if not args.no_e2e:
+    if not args.no_e2e and not opts:  # the host entry point runs the default options only
         hq, hk, hv = (t.pin_memory() for t in (q, k, v))
         hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         for _ in range(2):
@@ -858,24 +949,41 @@ def main(argv=None):
 
     peaks, peak_src = load_peaks()
     tensor_path = w.dtype == "bf16" and w.d == 64
-    mom_ms = stage_ms["moments"] / max(n_calls, 1)
-    mom_flops = causal_pairs(w) * moments_flops_per_pair(w.d)
-    achieved = mom_flops / (mom_ms / 1e3) / 1e12
+    per_call = {k_: v_ / max(n_calls, 1) for k_, v_ in stage_ms.items()}
+    pairs = causal_pairs(w)
     if tensor_path:
-        kernel_file = "lla_moments_tc.cu"
+        # the dominant kernel is the moment contraction; the weight sweeps are their own launch
+        kernel_file = "lla_moments_pass_tc.cu"
+        con_ms, w_ms = per_call["moments"], per_call["weights"]
+        achieved = pairs * contraction_flops_per_pair(w.d) / (con_ms / 1e3) / 1e12
         peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
-        roof = {"kernel": "moments (lla_moments_tc.cu, tcgen05)", "bound": "tensor",
-                "peak_source": f"bf16 dense, burst ({peak_src})",
-                "executed_tflops": causal_pairs(w) * tc_executed_flops_per_pair(w.d)
-                / (mom_ms / 1e3) / 1e12}
+        stage_ms_total = con_ms + w_ms
+        roof = {"kernel": "moment contraction (lla_moments_pass_tc.cu: tcgen05 cta_group::2, TMA)",
+                "bound": "tensor", "peak_source": f"bf16 dense, burst ({peak_src})",
+                "flops_per_unit": contraction_flops_per_pair(w.d), "unit_of_work": "causal pair",
+                "units_per_launch": pairs,
+                "executed_tflops": pairs * tc_executed_flops_per_pair(w.d) / (con_ms / 1e3) / 1e12,
+                "moments_stage": {
+                    "what": "weight sweeps (lla_moments_tc.cu) + contraction, the logit counted "
+                            "once: 2d + 2(1 + d + d(d+1)/2) flop per pair",
+                    "ms": stage_ms_total, "weights_ms": w_ms,
+                    "tflops": pairs * moments_flops_per_pair(w.d) / (stage_ms_total / 1e3) / 1e12,
+                    "frac": pairs * moments_flops_per_pair(w.d) / (stage_ms_total / 1e3) / 1e12
+                    / peak}}
+        avg_ms = con_ms
     else:
         kernel_file = "lla_moments_ffma.cu"
+        mom_ms = per_call["moments"]
+        achieved = pairs * moments_flops_per_pair(w.d) / (mom_ms / 1e3) / 1e12
         peak = fp32_alu_peak_tflops(peaks)
         roof = {"kernel": "moments (lla_moments_ffma.cu)", "bound": "alu",
                 "peak_source": f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)"}
+                               f"{peaks.get('sm_max_mhz', 2070)} MHz ({peak_src} clock)",
+                "flops_per_unit": moments_flops_per_pair(w.d), "unit_of_work": "causal pair",
+                "units_per_launch": pairs}
+        avg_ms = mom_ms
     roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                 "traffic": recorded_traffic(kernel_file), "avg_launch_ms": mom_ms})
+                 "traffic": recorded_traffic(kernel_file, w), "avg_launch_ms": avg_ms})
     if args.strategy == "cg":
         # The moments stage is reduced to its two weight sweeps; the CG passes vary in number.
         roof = None
@@ -903,8 +1011,12 @@ def main(argv=None):
             "roofline": roof,
             "stage_ms_per_step": {k_: v_ / max(n_calls, 1) for k_, v_ in stage_ms.items()},
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": e2e,
             "gpu_launches": n_launch,
+            "timed_repeats": {"repeats": reps, "steps_each": args.steps,
+                              "ms_per_step_each": [x / args.steps for x in rep_ms],
+                              "gpu_launches_per_repeat": n_launch // reps},
             "clocks": clk,
             "wall_s_timed": t_wall,
         }

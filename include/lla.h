@@ -47,7 +47,7 @@ extern "C" {
 #endif
 
 #define LLA_VERSION_MAJOR 0
-#define LLA_VERSION_MINOR 1
+#define LLA_VERSION_MINOR 2
 #define LLA_VERSION_PATCH 0
 
 typedef enum {
@@ -61,8 +61,53 @@ typedef enum {
 
 typedef enum { LLA_F32 = 0, LLA_BF16 = 1 } lla_dtype;
 
-/* Number of timed stages recorded per lla_forward call by the profiling hooks below. */
-#define LLA_NUM_STAGES 4 /* 0 prep, 1 moments, 2 solve, 3 readout */
+/* Implementation choices (lla_options.path). */
+typedef enum {
+  LLA_PATH_AUTO = 0,        /* tensor cores for bf16 with d = 64 (d = dv = 64 for the other ops),
+                               CUDA cores otherwise */
+  LLA_PATH_CUDA_CORE = 1,   /* CUDA cores always */
+  LLA_PATH_TENSOR_CORE = 2, /* tensor cores wherever supported (currently the same as AUTO) */
+  LLA_PATH_CG = 3           /* lla_forward*_ex only: matrix-free conjugate gradients for the ridge
+                               systems (bf16, d = dv = 64; as AUTO elsewhere) */
+} lla_path;
+
+/* Closed form of the LLA intercept that a forward evaluates (lla_options.form). */
+typedef enum { LLA_FORM_CENTRED = 0, LLA_FORM_PAGE = 1 } lla_form;
+
+/* Test-only faults (lla_options.test_fault). */
+typedef enum {
+  LLA_FAULT_NONE = 0,
+  LLA_FAULT_WITHHOLD_KEYS = 1 /* the tensor-core moments stage's key loader never stages its first
+                                 key block, so the waits on it run out (see lla_forward_ex) */
+} lla_test_fault;
+
+/*
+ * Per-call options of the *_ex entry points. An all-zero struct (or a NULL pointer) selects the
+ * defaults, which are what the entry points without options use. Options belong to the one call
+ * they are passed to: nothing is remembered between calls, so concurrent callers cannot change
+ * each other's results.
+ *   path         lla_path (the operations other than the forward accept AUTO, CUDA_CORE and
+ *                TENSOR_CORE; CUDA_CORE selects their CUDA-core kernels).
+ *   form         lla_form (forward only), see lla_forward_ex.
+ *   cg_max_iters conjugate-gradient iteration cap, 1..1024 (0 = 1024), LLA_PATH_CG only.
+ *   cg_rel_tol   CG stopping tolerance in (0, 1) (0 = 1e-3), LLA_PATH_CG only.
+ *   test_fault   lla_test_fault (forward only; 0 in normal use).
+ * Any other value of a field makes the call return LLA_ERR_INVALID_ARG before any work.
+ */
+typedef struct lla_options {
+  int path;
+  int form;
+  int cg_max_iters;
+  float cg_rel_tol;
+  int test_fault;
+  int reserved[3]; /* must be zero */
+} lla_options;
+
+/* Number of timed stages recorded per lla_forward call by the profiling hooks below:
+ * 0 prep (per-head means, CUDA-core path), 1 weights (tensor-core path: row maxima, the weights
+ * and their sums), 2 moments (the moment contraction; on the CUDA-core path also the weights),
+ * 3 solve, 4 readout. A stage that a path does not have records zero time. */
+#define LLA_NUM_STAGES 5
 
 /*
  * Causal LLA forward (the operation defined at the top of this header).
@@ -87,6 +132,41 @@ int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B
                    int d, int dv, float h, float lambda, int dtype, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/*
+ * lla_forward / lla_forward_ws with per-call options (opts may be NULL: the defaults). workspace
+ * may be NULL (scratch from the stream-ordered allocator, as lla_forward) or caller-provided as
+ * for lla_forward_ws (the size does not depend on the options).
+ *
+ * - opts->path: LLA_PATH_CUDA_CORE forces the CUDA-core moments, solve and readout for every
+ *   shape; LLA_PATH_CG solves the per-query ridge systems by conjugate gradients instead of
+ *   accumulating the d x d moments and factoring them: each product with C_kk is one streaming
+ *   pass over the prefix, as the "Parallax" blog (s.2 "Difficulties in Scaling LLA") describes
+ *   exact LLA being computed. Each query row iterates until ||r|| <= cg_rel_tol ||r_0|| (r the
+ *   residual of (C_kk + lambda' I) y = q - kbar, r_0 = q - kbar) or cg_max_iters passes have run.
+ *   A call on this path synchronises its stream every 8 iterations on the host to test whether any
+ *   query tile is still iterating, so it blocks the calling thread and cannot be captured in a
+ *   CUDA graph. Paths AUTO, CUDA_CORE and TENSOR_CORE compute the same moments; CG solves the
+ *   same systems iteratively.
+ * - opts->form ("Parallax" blog, s.2 Canonical Formulation and Appendix B; both forms equal the
+ *   intercept of the weighted ridge regression):
+ *     LLA_FORM_CENTRED (default) o = vbar + C_vk y,  (C_kk + lambda' I) y = q - kbar;
+ *     LLA_FORM_PAGE  o = sum w (1 - z.rho*) v / sum w (1 - z.rho*),  z = k - q,
+ *       (sum w z z^T + lambda' I) rho* = sum w z, evaluated as the exact-LLA two-branch epilogue
+ *       (O1 - O2) / (d1 - d2). It runs on the tensor-core dense strategy only (bf16, d = dv = 64,
+ *       path AUTO or TENSOR_CORE; otherwise LLA_ERR_UNSUPPORTED). Its system carries the rank-one
+ *       term w (kbar - q)(kbar - q)^T on top of the centred one, so it is worse conditioned for
+ *       queries far from the weighted key mean.
+ * - opts->test_fault = LLA_FAULT_WITHHOLD_KEYS exercises the bounded device waits: the
+ *   tensor-core moments stage (bf16, d = 64; LLA_ERR_UNSUPPORTED on other paths) never stages
+ *   its first key block, so every wait that needs it gives up after the wait limit (~2 s), the
+ *   stage returns early without issuing the tensor-core work that depends on it, and
+ *   LLA_ERR_TIMEOUT is recorded in the status word (lla_stream_status). The output of such a call
+ *   is undefined; the stream and the device stay usable. For tests only.
+ */
+int lla_forward_ex(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                   int d, int dv, float h, float lambda, int dtype, const lla_options* opts,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the fixed device scratch that lla_forward_noalloc uses: 64 MiB. */
 #define LLA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 
@@ -104,7 +184,7 @@ int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B
  *
  * - Size limit: returns LLA_ERR_UNSUPPORTED, before touching the device, when
  *   lla_workspace_size(B, H, T, d, dv, dtype) exceeds LLA_NOALLOC_SCRATCH_BYTES (e.g. bf16
- *   d = dv = 64 fits T <= 4352 at B*H = 1 and T <= 711 at B*H = 8; the tensor-core path's weight
+ *   d = dv = 64 fits T <= 4343 at B*H = 1 and T <= 704 at B*H = 8; the tensor-core path's weight
  *   scratch grows with B*H*T^2). Other argument errors are those of lla_forward.
  * - Set-up: the first call on each device looks up the scratch array's device address (with that
  *   device current) and caches it; make that first call before any stream capture.
@@ -154,12 +234,15 @@ int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx,
  * q, k, r: [B,H,T,d]; v, out: [B,H,T,dv]; all device, element type `dtype`, 16-byte aligned; the
  * conventions at the top of this header apply (lambda plays no part). bf16 inputs with
  * d = dv = 64 run on the tensor cores (weights rounded to bf16, P2 as an exact hi/lo bf16 pair,
- * fp32 accumulation) unless lla_set_moments_path(1) forces the CUDA cores; everything else runs
- * on the CUDA cores in fp32. Allocates nothing. Non-finite inputs give non-finite outputs; no
- * status is recorded.
+ * fp32 accumulation); everything else runs on the CUDA cores in fp32 (lla_parallax_forward_ex
+ * with path LLA_PATH_CUDA_CORE forces them for every shape). Allocates nothing. Non-finite inputs
+ * give non-finite outputs; no status is recorded.
  */
 int lla_parallax_forward(const void* q, const void* k, const void* v, const void* r, void* out,
                          int B, int H, int T, int d, int dv, float h, int dtype, void* stream);
+int lla_parallax_forward_ex(const void* q, const void* k, const void* v, const void* r, void* out,
+                            int B, int H, int T, int d, int dv, float h, int dtype,
+                            const lla_options* opts, void* stream);
 
 /*
  * Decode: one query per head against a key/value cache of L positions that the query attends to
@@ -172,13 +255,16 @@ int lla_parallax_forward(const void* q, const void* k, const void* v, const void
  * a maximum logit of the chunk); the last CTA of the head to finish merges them and solves the
  * ridge system in float64 (split-KV with a last-arriver merge, as the blog's decode kernel,
  * Appendix C). For bf16 with d = dv = 64 the chunk's second moments run on the tensor cores
- * (weights rounded to bf16, exact products, float32 sums) unless lla_set_moments_path(1) is in
- * effect; otherwise on the CUDA cores with float32 weights. Asynchronous on `stream`; scratch from the stream-ordered pool. B*H = 0 is a
+ * (weights rounded to bf16, exact products, float32 sums) unless lla_decode_ex is given path
+ * LLA_PATH_CUDA_CORE; otherwise on the CUDA cores with float32 weights. Asynchronous on `stream`; scratch from the stream-ordered pool. B*H = 0 is a
  * no-op; L = 0 with B*H > 0 is LLA_ERR_INVALID_ARG. A non-positive pivot (non-finite inputs)
  * makes that head's output NaN and records LLA_ERR_NUMERICAL.
  */
 int lla_decode(const void* q, const void* k, const void* v, void* out, int B, int H, int L, int d,
                int dv, float h, float lambda, int dtype, void* stream);
+int lla_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int H, int L,
+                  int d, int dv, float h, float lambda, int dtype, const lla_options* opts,
+                  void* stream);
 
 /*
  * Parallax decode with probe r ([B,H,d], same dtype): o = vbar - Sigma_KV r over all L cached
@@ -189,6 +275,9 @@ int lla_decode(const void* q, const void* k, const void* v, void* out, int B, in
  */
 int lla_parallax_decode(const void* q, const void* k, const void* v, const void* r, void* out,
                         int B, int H, int L, int d, int dv, float h, int dtype, void* stream);
+int lla_parallax_decode_ex(const void* q, const void* k, const void* v, const void* r, void* out,
+                           int B, int H, int L, int d, int dv, float h, int dtype,
+                           const lla_options* opts, void* stream);
 
 /*
  * Causal Parallax backward ("Parallax" blog, Appendix F "Parallax backward (closed form)": a
@@ -201,12 +290,20 @@ int lla_parallax_decode(const void* q, const void* k, const void* v, const void*
  * row-major, 16-byte aligned, of the dtype given (gradients in the inputs' dtype; fp32
  * arithmetic); the caller owns them; outputs must not alias inputs. d, dv in {16, 32, 64}
  * (else LLA_ERR_UNSUPPORTED); h > 0 and finite, B, H, T >= 0 (else LLA_ERR_INVALID_ARG). Three
- * launches on CUDA cores, asynchronous on `stream`, with a scratch of 32 bytes per query row
- * from the stream-ordered pool. Returns LLA_OK, LLA_ERR_* for invalid arguments, LLA_ERR_CUDA.
+ * launches, asynchronous on `stream`, with a scratch of 32 bytes per query row from the
+ * stream-ordered pool: for bf16 with d = dv = 64, the tensor-core forward kernel caching the row
+ * records, then tensor-core row-tile and column-tile passes (tcgen05; weights rounded to bf16,
+ * fp32 accumulation); for every other shape (or with path LLA_PATH_CUDA_CORE through
+ * lla_parallax_backward_ex), the same three passes on the CUDA cores in fp32. Returns LLA_OK,
+ * LLA_ERR_* for invalid arguments, LLA_ERR_CUDA.
  */
 int lla_parallax_backward(const void* q, const void* k, const void* v, const void* r,
                           const void* dout, void* dq, void* dk, void* dv, void* dr, int B, int H,
                           int T, int d, int dv_, float h, int dtype, void* stream);
+int lla_parallax_backward_ex(const void* q, const void* k, const void* v, const void* r,
+                             const void* dout, void* dq, void* dk, void* dv, void* dr, int B,
+                             int H, int T, int d, int dv_, float h, int dtype,
+                             const lla_options* opts, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status word.
@@ -220,49 +317,6 @@ const char* lla_status_string(int status);
 
 /* LLA_VERSION_MAJOR*10000 + LLA_VERSION_MINOR*100 + LLA_VERSION_PATCH. */
 int lla_version(void);
-
-/*
- * Selects the implementation of the moments stage for lla_forward* calls made afterwards by this
- * process: 0 = automatic (tensor cores -- tcgen05 with exact bf16 hi/lo products -- for bf16
- * inputs with d = 64, CUDA cores otherwise), 1 = CUDA cores always, 2 = tensor cores wherever
- * supported (currently the same as 0), 3 = the matrix-free conjugate-gradient strategy for bf16
- * inputs with d = dv = 64 (as 0 elsewhere): the per-query ridge systems are solved by CG, each
- * product with C_kk being one streaming pass over the prefix, as the "Parallax" blog (s.2
- * "Difficulties in Scaling LLA") describes exact LLA being computed, instead of accumulating the
- * d x d moments and factoring them (see lla_set_cg). Paths 0-2 compute the same moments; 3 solves
- * the same systems iteratively. The choice exists for testing and measurement; a workspace for
- * lla_forward_ws must be sized (lla_workspace_size) under the path it is used with. The same
- * choice applies to lla_parallax_forward, lla_parallax_backward and lla_decode (1 selects their
- * CUDA-core kernels; 2 and 3 as 0). Returns LLA_ERR_INVALID_ARG for any other value. Host-only.
- */
-int lla_set_moments_path(int path);
-
-/*
- * Parameters of the conjugate-gradient strategy (lla_set_moments_path(3)) for later calls by this
- * process: each query row iterates until ||r|| <= rel_tol ||r_0|| (r the residual of
- * (C_kk + lambda' I) y = q - kbar, r_0 = q - kbar) or max_iters streaming passes have run
- * (defaults 1024 and 1e-3). A call with this strategy synchronises its stream every 8 iterations to
- * test whether any query tile is still iterating, so it cannot be captured in a CUDA graph.
- * 1 <= max_iters <= 1024, 0 < rel_tol < 1; otherwise LLA_ERR_INVALID_ARG. Host-only.
- * No counterpart on the pages beyond the CG solve itself (see above).
- */
-int lla_set_cg(int max_iters, float rel_tol);
-
-/*
- * Which exact closed form of the LLA intercept later lla_forward / lla_forward_ws calls by this
- * process evaluate ("Parallax" blog, s.2 Canonical Formulation and Appendix B; both equal the
- * intercept of the weighted ridge regression):
- *   0 (default) the centred form  o = vbar + C_vk y,  (C_kk + lambda' I) y = q - kbar;
- *   1 the page form  o = sum w (1 - z.rho*) v / sum w (1 - z.rho*),  z = k - q,
- *     (sum w z z^T + lambda' I) rho* = sum w z, which the readout evaluates as the exact-LLA
- *     two-branch epilogue (O1 - O2) / (d1 - d2).
- * Form 1 runs on the tensor-core dense strategy only (bf16, d = dv = 64, moments path 0 or 2);
- * a call that would take another path returns LLA_ERR_UNSUPPORTED while it is set. Its system
- * carries the rank-one term w (kbar - q)(kbar - q)^T on top of the centred one, so it is worse
- * conditioned for queries far from the weighted key mean. Returns LLA_ERR_INVALID_ARG for any
- * other value. Host-only.
- */
-int lla_set_form(int form);
 
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 unsigned long long lla_launch_count(void);

@@ -10,7 +10,8 @@ _BINDING = {
     "lla_forward", "lla_forward_ws", "lla_workspace_size", "lla_moments", "lla_forward_host",
     "lla_stream_status", "lla_status_string", "lla_version", "LlaError", "library_path",
     "launch_count", "profile_enable", "profile_collect", "lla_forward_noalloc",
-    "lla_set_moments_path", "lla_parallax_forward",
+    "lla_parallax_forward", "lla_decode", "lla_parallax_decode", "lla_parallax_backward",
+    "Options",
 }
 
 

@@ -15,29 +15,52 @@ __all__ = [
     "LlaError", "library_path", "lla_forward", "lla_forward_ws", "lla_workspace_size",
     "lla_forward_host", "lla_moments", "lla_stream_status", "lla_status_string", "lla_version",
     "launch_count", "profile_enable", "profile_collect", "EXPORTED_SYMBOLS", "DTYPE_CODES",
-    "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "lla_set_moments_path", "PATH_AUTO",
-    "PATH_CUDA_CORE", "PATH_TENSOR_CORE", "PATH_CG", "lla_set_cg", "lla_parallax_forward",
-    "lla_decode", "lla_parallax_decode", "lla_set_form", "FORM_CENTRED", "FORM_PAGE",
-    "lla_parallax_backward",
+    "lla_forward_noalloc", "NOALLOC_SCRATCH_BYTES", "PATH_AUTO", "PATH_CUDA_CORE",
+    "PATH_TENSOR_CORE", "PATH_CG", "lla_parallax_forward", "lla_decode", "lla_parallax_decode",
+    "FORM_CENTRED", "FORM_PAGE", "FAULT_WITHHOLD_KEYS", "lla_parallax_backward", "Options",
 ]
 
 LLA_OK = 0
 DTYPE_CODES = {torch.float32: 0, torch.bfloat16: 1}
-NUM_STAGES = 4
-STAGE_NAMES = ("prep", "moments", "solve", "readout")
+NUM_STAGES = 5
+STAGE_NAMES = ("prep", "weights", "moments", "solve", "readout")
 
 # Every function include/lla.h declares.
 EXPORTED_SYMBOLS = (
     "lla_forward", "lla_workspace_size", "lla_forward_ws", "lla_forward_host", "lla_moments",
     "lla_stream_status", "lla_status_string", "lla_version", "lla_launch_count",
-    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_set_moments_path", "lla_set_cg", "lla_decode", "lla_parallax_decode",
-    "lla_parallax_forward", "lla_set_form", "lla_parallax_backward",
+    "lla_profile_enable", "lla_profile_collect", "lla_forward_noalloc", "lla_decode",
+    "lla_parallax_decode", "lla_parallax_forward", "lla_parallax_backward", "lla_forward_ex",
+    "lla_parallax_forward_ex", "lla_decode_ex", "lla_parallax_decode_ex",
+    "lla_parallax_backward_ex",
 )
 
 # LLA_NOALLOC_SCRATCH_BYTES in include/lla.h: the fixed scratch of lla_forward_noalloc.
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
+
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CG = 0, 1, 2, 3
+FORM_CENTRED, FORM_PAGE = 0, 1
+FAULT_WITHHOLD_KEYS = 1
+
+
+class Options(ctypes.Structure):
+    """lla_options: per-call choices of the *_ex entry points (all zero = the defaults)."""
+    _fields_ = [("path", ctypes.c_int), ("form", ctypes.c_int), ("cg_max_iters", ctypes.c_int),
+                ("cg_rel_tol", ctypes.c_float), ("test_fault", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
+
+
+def _options(path=0, form=0, cg=None, test_fault=0):
+    """An Options struct, or None when every choice is the default (the plain entry point)."""
+    if not path and not form and cg is None and not test_fault:
+        return None
+    o = Options()
+    o.path, o.form, o.test_fault = int(path), int(form), int(test_fault)
+    if cg is not None:
+        o.cg_max_iters, o.cg_rel_tol = int(cg[0]), float(cg[1])
+    return o
 
 
 class LlaError(RuntimeError):
@@ -62,6 +85,7 @@ def _load():
     lib = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     fp = ctypes.POINTER(ctypes.c_float)
+    op = ctypes.POINTER(Options)
     sig = {
         "lla_forward": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_workspace_size": (sz, [i, i, i, i, i, i]),
@@ -75,13 +99,15 @@ def _load():
         "lla_profile_enable": (i, [i]),
         "lla_profile_collect": (i, [fp, i, ctypes.POINTER(ctypes.c_int)]),
         "lla_forward_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
-        "lla_set_moments_path": (i, [i]),
-        "lla_set_cg": (i, [i, ctypes.c_float]),
-        "lla_set_form": (i, [i]),
         "lla_parallax_forward": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "lla_decode": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, vp]),
         "lla_parallax_decode": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "lla_parallax_backward": (i, [vp] * 9 + [i, i, i, i, i, f, i, vp]),
+        "lla_forward_ex": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, op, vp, sz, vp]),
+        "lla_parallax_forward_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, op, vp]),
+        "lla_decode_ex": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, i, op, vp]),
+        "lla_parallax_decode_ex": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, op, vp]),
+        "lla_parallax_backward_ex": (i, [vp] * 9 + [i, i, i, i, i, f, i, op, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -96,29 +122,6 @@ def lla_status_string(status: int) -> str:
 
 def lla_version() -> int:
     return _load().lla_version()
-
-
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_CG = 0, 1, 2, 3
-
-
-def lla_set_moments_path(path: int):
-    """Select the moments stage (0 auto, 1 CUDA cores, 2 tensor cores where supported, 3 the
-    matrix-free conjugate-gradient strategy for bf16 d = dv = 64)."""
-    _check(_load().lla_set_moments_path(int(path)), "lla_set_moments_path")
-
-
-def lla_set_cg(max_iters: int, rel_tol: float):
-    """Iteration cap and relative residual tolerance of the conjugate-gradient strategy."""
-    _check(_load().lla_set_cg(int(max_iters), float(rel_tol)), "lla_set_cg")
-
-
-FORM_CENTRED, FORM_PAGE = 0, 1
-
-
-def lla_set_form(form: int):
-    """Closed form the forward evaluates: 0 the centred form (default), 1 the page form with the
-    exact-LLA two-branch epilogue (tensor-core dense strategy, bf16 d = dv = 64 only)."""
-    _check(_load().lla_set_form(int(form)), "lla_set_form")
 
 
 def launch_count() -> int:
@@ -154,27 +157,56 @@ def _device_inputs(q, k, v):
     return _shapes(q, k, v)
 
 
-def lla_forward(q, k, v, h: float, lam: float, out=None, stream=None):
-    """Causal LLA forward on device tensors; returns `out` ([B,H,T,dv], dtype of the inputs)."""
+def _check_out(out, shape, like):
+    if (tuple(out.shape) != tuple(shape) or out.dtype != like.dtype or out.device != like.device
+            or not out.is_contiguous()):
+        raise ValueError(f"out must be a contiguous tensor of shape {tuple(shape)}, dtype "
+                         f"{like.dtype} on {like.device}")
+
+
+def lla_forward(q, k, v, h: float, lam: float, out=None, stream=None, *, path=0, form=0, cg=None,
+                test_fault=0, workspace=None):
+    """Causal LLA forward on device tensors; returns `out` ([B,H,T,dv], dtype of the inputs).
+
+    path / form / cg=(max_iters, rel_tol) / test_fault are this call's lla_options (defaults:
+    automatic path, centred form); with any of them, or a workspace tensor, the call goes through
+    lla_forward_ex, otherwise through lla_forward."""
     B, H, T, d, dv, code = _device_inputs(q, k, v)
     if out is None:
         out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
-    st = _load().lla_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, d,
-                             dv, float(h), float(lam), code, _stream_ptr(stream))
-    _check(st, "lla_forward")
+    _check_out(out, (B, H, T, dv), q)
+    opts = _options(path, form, cg, test_fault)
+    if opts is None and workspace is None:
+        st = _load().lla_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                                 T, d, dv, float(h), float(lam), code, _stream_ptr(stream))
+        _check(st, "lla_forward")
+        return out
+    wp, wb = (None, 0) if workspace is None else (
+        workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = _load().lla_forward_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T,
+                                d, dv, float(h), float(lam), code,
+                                ctypes.byref(opts) if opts is not None else None, wp, wb,
+                                _stream_ptr(stream))
+    _check(st, "lla_forward_ex")
     return out
 
 
-def lla_parallax_forward(q, k, v, r, h: float, out=None, stream=None):
-    """Causal Parallax forward with probe r ([B,H,T,d], like q); returns `out` ([B,H,T,dv])."""
+def lla_parallax_forward(q, k, v, r, h: float, out=None, stream=None, *, path=0):
+    """Causal Parallax forward with probe r ([B,H,T,d], like q); returns `out` ([B,H,T,dv]).
+    path=PATH_CUDA_CORE forces the CUDA-core kernel (lla_parallax_forward_ex)."""
     B, H, T, d, dv, code = _device_inputs(q, k, v)
     if r.shape != q.shape or r.dtype != q.dtype or not r.is_cuda or not r.is_contiguous():
         raise ValueError("r must be a contiguous CUDA tensor shaped and typed like q")
     if out is None:
         out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
-    st = _load().lla_parallax_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
-                                      out.data_ptr(), B, H, T, d, dv, float(h), code,
-                                      _stream_ptr(stream))
+    _check_out(out, (B, H, T, dv), q)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(), out.data_ptr(), B, H, T, d,
+            dv, float(h), code)
+    opts = _options(path)
+    if opts is None:
+        st = _load().lla_parallax_forward(*args, _stream_ptr(stream))
+    else:
+        st = _load().lla_parallax_forward_ex(*args, ctypes.byref(opts), _stream_ptr(stream))
     _check(st, "lla_parallax_forward")
     return out
 
@@ -193,32 +225,44 @@ def _decode_inputs(q, k, v):
     return B, H, k.shape[2], d, v.shape[3], DTYPE_CODES[q.dtype]
 
 
-def lla_decode(q, k, v, h: float, lam: float, out=None, stream=None):
-    """LLA decode: q [B,H,d] against the cache k [B,H,L,d], v [B,H,L,dv]; returns [B,H,dv]."""
+def lla_decode(q, k, v, h: float, lam: float, out=None, stream=None, *, path=0):
+    """LLA decode: q [B,H,d] against the cache k [B,H,L,d], v [B,H,L,dv]; returns [B,H,dv].
+    path=PATH_CUDA_CORE forces the CUDA-core split kernel (lla_decode_ex)."""
     B, H, L, d, dv, code = _decode_inputs(q, k, v)
     if out is None:
         out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
-    st = _load().lla_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, d,
-                            dv, float(h), float(lam), code, _stream_ptr(stream))
+    _check_out(out, (B, H, dv), q)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, L, d, dv, float(h),
+            float(lam), code)
+    opts = _options(path)
+    if opts is None:
+        st = _load().lla_decode(*args, _stream_ptr(stream))
+    else:
+        st = _load().lla_decode_ex(*args, ctypes.byref(opts), _stream_ptr(stream))
     _check(st, "lla_decode")
     return out
 
 
-def lla_parallax_decode(q, k, v, r, h: float, out=None, stream=None):
+def lla_parallax_decode(q, k, v, r, h: float, out=None, stream=None, *, path=0):
     """Parallax decode with probe r [B,H,d] (like q); returns [B,H,dv]."""
     B, H, L, d, dv, code = _decode_inputs(q, k, v)
     if r.shape != q.shape or r.dtype != q.dtype or not r.is_cuda or not r.is_contiguous():
         raise ValueError("r must be a contiguous CUDA tensor shaped and typed like q")
     if out is None:
         out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
-    st = _load().lla_parallax_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
-                                     out.data_ptr(), B, H, L, d, dv, float(h), code,
-                                     _stream_ptr(stream))
+    _check_out(out, (B, H, dv), q)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(), out.data_ptr(), B, H, L, d,
+            dv, float(h), code)
+    opts = _options(path)
+    if opts is None:
+        st = _load().lla_parallax_decode(*args, _stream_ptr(stream))
+    else:
+        st = _load().lla_parallax_decode_ex(*args, ctypes.byref(opts), _stream_ptr(stream))
     _check(st, "lla_parallax_decode")
     return out
 
 
-def lla_parallax_backward(q, k, v, r, dout, h: float, stream=None):
+def lla_parallax_backward(q, k, v, r, dout, h: float, stream=None, *, path=0):
     """Gradients (dq, dk, dv, dr) of the causal Parallax forward for the upstream gradient dout
     ([B,H,T,dv], like the forward's output); each is shaped and typed like q, k, v, r."""
     B, H, T, d, dv, code = _device_inputs(q, k, v)
@@ -229,20 +273,31 @@ def lla_parallax_backward(q, k, v, r, dout, h: float, stream=None):
             raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {tuple(shape)} "
                              f"and dtype {q.dtype}")
     dq, dk, dvv, dr = (torch.empty_like(x) for x in (q, k, v, r))
-    st = _load().lla_parallax_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
-                                       dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                       dvv.data_ptr(), dr.data_ptr(), B, H, T, d, dv, float(h),
-                                       code, _stream_ptr(stream))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(), dout.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dvv.data_ptr(), dr.data_ptr(), B, H, T, d, dv, float(h),
+            code)
+    opts = _options(path)
+    if opts is None:
+        st = _load().lla_parallax_backward(*args, _stream_ptr(stream))
+    else:
+        st = _load().lla_parallax_backward_ex(*args, ctypes.byref(opts), _stream_ptr(stream))
     _check(st, "lla_parallax_backward")
     return dq, dk, dvv, dr
 
 
 def lla_forward_noalloc(q, k, v, h: float, lam: float, out, stream=None):
     """lla_forward for callers that must not allocate device memory: the library's fixed scratch
-    array is used, and `out` (a preallocated [B,H,T,dv] tensor) is required."""
+    array is used, and `out` (a preallocated contiguous [B,H,T,dv] tensor of q's dtype on q's
+    device) is required. The call runs with q's device current, so that the scratch array of
+    that device is the one used."""
     B, H, T, d, dv, code = _device_inputs(q, k, v)
-    st = _load().lla_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B,
-                                     H, T, d, dv, float(h), float(lam), code, _stream_ptr(stream))
+    if not (k.device == q.device and v.device == q.device):
+        raise ValueError("q, k, v must be on one device")
+    _check_out(out, (B, H, T, dv), q)
+    with torch.cuda.device(q.device):
+        st = _load().lla_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         B, H, T, d, dv, float(h), float(lam), code,
+                                         _stream_ptr(stream))
     _check(st, "lla_forward_noalloc")
     return out
 
@@ -257,6 +312,7 @@ def lla_forward_ws(q, k, v, h: float, lam: float, workspace, out=None, stream=No
     B, H, T, d, dv, code = _device_inputs(q, k, v)
     if out is None:
         out = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    _check_out(out, (B, H, T, dv), q)
     st = _load().lla_forward_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T,
                                 d, dv, float(h), float(lam), code, workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream_ptr(stream))

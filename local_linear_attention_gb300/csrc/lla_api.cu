@@ -16,10 +16,6 @@ __device__ int g_status;
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
-std::atomic<int> g_path_request{0};  // 0 auto, kPathCudaCore, kPathTensorCore, kPathCG
-std::atomic<int> g_cg_max_iters{1024};
-std::atomic<float> g_cg_rel_tol{1e-3f};
-std::atomic<int> g_form{0};  // kFormCentred or kFormPage
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -39,9 +35,21 @@ cudaError_t device_status(int** out) {
     if (err != cudaSuccess) return err;
     g_status_ptr[dev] = static_cast<int*>(p);
   }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+// Once per device, for the entry points that take their scratch from the stream-ordered
+// allocator: memory freed with cudaFreeAsync stays in the device's default pool instead of going
+// back to the driver at every synchronisation, so repeated calls reuse their scratch. (Entry
+// points that allocate nothing leave the pool's settings alone.)
+cudaError_t ensure_pool() {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
   if (!g_pool_ready[dev]) {
-    // Keep memory freed with cudaFreeAsync in the device's default pool instead of returning it
-    // to the driver at every synchronisation, so repeated calls reuse their scratch.
     cudaMemPool_t pool;
     if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
       unsigned long long thr = ~0ULL;
@@ -49,8 +57,33 @@ cudaError_t device_status(int** out) {
     }
     g_pool_ready[dev] = true;
   }
-  *out = g_status_ptr[dev];
   return cudaSuccess;
+}
+
+// Validates per-call options into `a` (forward: every field; other operations: path only).
+int apply_options(const lla_options* o, bool forward, Args* a) {
+  if (!o) return LLA_OK;
+  for (int r : o->reserved)
+    if (r != 0) return LLA_ERR_INVALID_ARG;
+  if (o->path < LLA_PATH_AUTO || o->path > LLA_PATH_CG) return LLA_ERR_INVALID_ARG;
+  if (!forward) {
+    if (o->path == LLA_PATH_CG || o->form != 0 || o->cg_max_iters != 0 || o->cg_rel_tol != 0.f ||
+        o->test_fault != 0)
+      return LLA_ERR_INVALID_ARG;
+    a->path_req = o->path;
+    return LLA_OK;
+  }
+  if (o->form != LLA_FORM_CENTRED && o->form != LLA_FORM_PAGE) return LLA_ERR_INVALID_ARG;
+  if (o->cg_max_iters < 0 || o->cg_max_iters > 1024) return LLA_ERR_INVALID_ARG;
+  if (!(o->cg_rel_tol >= 0.f && o->cg_rel_tol < 1.f)) return LLA_ERR_INVALID_ARG;
+  if (o->test_fault != LLA_FAULT_NONE && o->test_fault != LLA_FAULT_WITHHOLD_KEYS)
+    return LLA_ERR_INVALID_ARG;
+  a->path_req = o->path;
+  a->form = o->form;
+  a->cg_iters = o->cg_max_iters > 0 ? o->cg_max_iters : 1024;
+  a->cg_tol = o->cg_rel_tol > 0.f ? o->cg_rel_tol : 1e-3f;
+  a->fault = o->test_fault;
+  return LLA_OK;
 }
 
 // ------------------------------------------------------------------------- stage timing
@@ -104,6 +137,7 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
   Workspace ws;
   carve_workspace(a, base, &ws);
   if (ws.form == kFormPage && !(ws.path == kPathTensorCore && a.dv == 64)) return LLA_ERR_UNSUPPORTED;
+  if (a.fault != 0 && ws.path != kPathTensorCore) return LLA_ERR_UNSUPPORTED;
   if (device_status(&ws.status) != cudaSuccess) return LLA_ERR_CUDA;
   ProfRec rec;
   bool prof = false;
@@ -116,17 +150,21 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
       if (cudaEventCreate(&e) != cudaSuccess) return LLA_ERR_CUDA;
     cudaEventRecord(rec.ev[0], s);
   }
+  auto none = [](const Args&, const Workspace&, cudaStream_t) { return cudaSuccess; };
+  const bool tc = ws.path == kPathTensorCore;
   cudaError_t (*stages[LLA_NUM_STAGES])(const Args&, const Workspace&, cudaStream_t) = {
       launch_prep,
-      ws.path == kPathTensorCore ? launch_moments_tc : launch_moments_ffma,
+      tc ? launch_weights_tc : +none,
+      tc ? launch_moments_pass_tc : launch_moments_ffma,
       launch_solve,
-      (ws.path == kPathTensorCore && a.dv == 64) ? launch_readout_tc : launch_readout};
+      (tc && a.dv == 64) ? launch_readout_tc : launch_readout};
   if (ws.path == kPathCG) {  // matrix-free CG for the ridge systems (bf16, d = dv = 64)
     stages[1] = launch_weights_tc;
-    stages[2] = [](const Args& a2, const Workspace& w2, cudaStream_t s2) {
-      return launch_cg_solve(a2, w2, s2, g_cg_max_iters.load(), g_cg_rel_tol.load());
+    stages[2] = none;
+    stages[3] = [](const Args& a2, const Workspace& w2, cudaStream_t s2) {
+      return launch_cg_solve(a2, w2, s2, a2.cg_iters, a2.cg_tol);
     };
-    stages[3] = launch_readout_tc;
+    stages[4] = launch_readout_tc;
   }
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
     if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
@@ -145,7 +183,7 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int choose_path(const Args& a) {
   const bool tc_ok = tc_eligible(a);
-  const int req = g_path_request.load();
+  const int req = a.path_req;
   if (req == kPathCudaCore || !tc_ok) return kPathCudaCore;
   if (req == kPathCG && a.dv == 64) return kPathCG;
   return kPathTensorCore;
@@ -167,6 +205,10 @@ size_t workspace_bytes(const Args& a) {
     n += align_up(R * 3 * a.d * 2);                      // ytc
     n += align_up(R * sizeof(float));                    // cy
     n += align_up(moments_tc_pscratch_bytes(a.BH(), a.T));  // pscr
+    n += align_up(R * a.d * 2);                          // ksh
+    n += align_up(BH * a.d * sizeof(float));             // kref
+    n += align_up(BH * kKeyStatChunks * 2 * a.d * sizeof(float));  // kstat
+    n += align_up((1 + kMaxRepairRows) * sizeof(int));   // rep
   }
   return n;
 }
@@ -188,9 +230,13 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->ytc = tc ? reinterpret_cast<uint32_t*>(take(R * 3 * a.d * 2)) : nullptr;
   ws->cy = tc ? take(R * sizeof(float)) : nullptr;
   ws->pscr = tc ? take(moments_tc_pscratch_bytes(a.BH(), a.T)) : nullptr;
+  ws->ksh = tc ? reinterpret_cast<__nv_bfloat16*>(take(R * a.d * 2)) : nullptr;
+  ws->kref = tc ? take(BH * a.d * sizeof(float)) : nullptr;
+  ws->kstat = tc ? take(BH * kKeyStatChunks * 2 * a.d * sizeof(float)) : nullptr;
+  ws->rep = tc ? reinterpret_cast<int*>(take((1 + kMaxRepairRows) * sizeof(int))) : nullptr;
   ws->status = nullptr;
   ws->path = choose_path(a);
-  ws->form = g_form.load();
+  ws->form = a.form;
 }
 
 }  // namespace lla
@@ -205,31 +251,45 @@ size_t lla_workspace_size(int B, int H, int T, int d, int dv, int dtype) {
   return a.rows() == 0 ? 0 : workspace_bytes(a);
 }
 
-int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
-                   int d, int dv, float h, float lambda, int dtype, void* workspace,
-                   size_t workspace_bytes_, void* stream) {
-  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
-  int st = check_forward(a);
-  if (st != LLA_OK || a.rows() == 0) return st;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 256) != 0 ||
-      workspace_bytes_ < workspace_bytes(a))
-    return LLA_ERR_INVALID_ARG;
-  return run_forward(a, workspace, static_cast<cudaStream_t>(stream));
-}
-
-int lla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int d,
-                int dv, float h, float lambda, int dtype, void* stream) {
-  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
-  int st = check_forward(a);
+int lla_forward_ex(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                   int d, int dv, float h, float lambda, int dtype, const lla_options* opts,
+                   void* workspace, size_t workspace_bytes_, void* stream) {
+  Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
+  int st = apply_options(opts, true, &a);
+  if (st != LLA_OK) return st;
+  st = check_forward(a);
   if (st != LLA_OK || a.rows() == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int* dummy;
-  if (device_status(&dummy) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) % 256) != 0 ||
+        workspace_bytes_ < workspace_bytes(a))
+      return LLA_ERR_INVALID_ARG;
+    return run_forward(a, workspace, s);
+  }
+  if (ensure_pool() != cudaSuccess) return LLA_ERR_CUDA;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
   st = run_forward(a, ws, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
   return st;
+}
+
+int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
+                   int d, int dv, float h, float lambda, int dtype, void* workspace,
+                   size_t workspace_bytes_, void* stream) {
+  if (!workspace) {  // lla_forward_ex would allocate; this entry point never does
+    const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, lambda, dtype);
+    const int st = check_forward(a);
+    return (st != LLA_OK || a.rows() == 0) ? st : LLA_ERR_INVALID_ARG;
+  }
+  return lla_forward_ex(q, k, v, out, B, H, T, d, dv, h, lambda, dtype, nullptr, workspace,
+                        workspace_bytes_, stream);
+}
+
+int lla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int d,
+                int dv, float h, float lambda, int dtype, void* stream) {
+  return lla_forward_ex(q, k, v, out, B, H, T, d, dv, h, lambda, dtype, nullptr, nullptr, 0,
+                        stream);
 }
 
 int lla_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
@@ -243,7 +303,7 @@ int lla_forward_host(const void* q_host, const void* k_host, const void* v_host,
   if (!q_host || !k_host || !v_host || !out_host) return LLA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = nullptr;
-  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;
+  if (device_status(&status) != cudaSuccess || ensure_pool() != cudaSuccess) return LLA_ERR_CUDA;
   const size_t eb = elem_bytes(dtype);
   const size_t nqk = (size_t)a.rows() * d * eb, nv = (size_t)a.rows() * dv * eb;
   const size_t off_k = align_up(nqk), off_v = off_k + align_up(nqk), off_o = off_v + align_up(nv);
@@ -283,22 +343,33 @@ int lla_moments(const void* q, const void* k, const void* v, const int64_t* idx,
              : LLA_ERR_CUDA;
 }
 
-int lla_parallax_forward(const void* q, const void* k, const void* v, const void* r, void* out,
-                         int B, int H, int T, int d, int dv, float h, int dtype, void* stream) {
-  const Args a = make_args(q, k, v, out, B, H, T, d, dv, h, 1.f, dtype);
-  int st = check_forward(a);
+int lla_parallax_forward_ex(const void* q, const void* k, const void* v, const void* r, void* out,
+                            int B, int H, int T, int d, int dv, float h, int dtype,
+                            const lla_options* opts, void* stream) {
+  Args a = make_args(q, k, v, out, B, H, T, d, dv, h, 1.f, dtype);
+  int st = apply_options(opts, false, &a);
+  if (st != LLA_OK) return st;
+  st = check_forward(a);
   if (st != LLA_OK || a.rows() == 0) return st;
   if (!r || !aligned16(r)) return LLA_ERR_INVALID_ARG;
   int* status = nullptr;
   if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;
-  const int path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
+  const int path = a.path_req == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
   return launch_parallax(a, r, path, status, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? LLA_OK
              : LLA_ERR_CUDA;
 }
 
+int lla_parallax_forward(const void* q, const void* k, const void* v, const void* r, void* out,
+                         int B, int H, int T, int d, int dv, float h, int dtype, void* stream) {
+  return lla_parallax_forward_ex(q, k, v, r, out, B, H, T, d, dv, h, dtype, nullptr, stream);
+}
+
 namespace {
-int run_decode(const DecodeArgs& a, void* stream) {
+int run_decode(const DecodeArgs& a, const lla_options* opts, void* stream) {
+  Args oa;
+  const int ost = apply_options(opts, false, &oa);
+  if (ost != LLA_OK) return ost;
   if (a.B < 0 || a.H < 0 || a.L < 0) return LLA_ERR_INVALID_ARG;
   if (a.dtype != LLA_F32 && a.dtype != LLA_BF16) return LLA_ERR_INVALID_ARG;
   if (!(a.d == 16 || a.d == 32 || a.d == 64) || !(a.dv == 16 || a.dv == 32 || a.dv == 64))
@@ -312,9 +383,9 @@ int run_decode(const DecodeArgs& a, void* stream) {
     return LLA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = nullptr;
-  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  if (device_status(&status) != cudaSuccess || ensure_pool() != cudaSuccess) return LLA_ERR_CUDA;
   DecodeArgs b = a;
-  b.path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
+  b.path = oa.path_req == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, decode_workspace_bytes(b), s) != cudaSuccess) return LLA_ERR_CUDA;
   int st = launch_decode(b, ws, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
@@ -323,24 +394,40 @@ int run_decode(const DecodeArgs& a, void* stream) {
 }
 }  // namespace
 
+int lla_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int H, int L,
+                  int d, int dv, float h, float lambda, int dtype, const lla_options* opts,
+                  void* stream) {
+  DecodeArgs a{q, k, v, nullptr, out, B, H, L, d, dv, h, lambda, dtype};
+  return run_decode(a, opts, stream);
+}
+
 int lla_decode(const void* q, const void* k, const void* v, void* out, int B, int H, int L, int d,
                int dv, float h, float lambda, int dtype, void* stream) {
-  DecodeArgs a{q, k, v, nullptr, out, B, H, L, d, dv, h, lambda, dtype};
-  return run_decode(a, stream);
+  return lla_decode_ex(q, k, v, out, B, H, L, d, dv, h, lambda, dtype, nullptr, stream);
+}
+
+int lla_parallax_decode_ex(const void* q, const void* k, const void* v, const void* r, void* out,
+                           int B, int H, int L, int d, int dv, float h, int dtype,
+                           const lla_options* opts, void* stream) {
+  if (B > 0 && H > 0 && (!r || !aligned16(r))) return LLA_ERR_INVALID_ARG;
+  DecodeArgs a{q, k, v, r, out, B, H, L, d, dv, h, 1.f, dtype};
+  if (!r) return LLA_ERR_INVALID_ARG;
+  return run_decode(a, opts, stream);
 }
 
 int lla_parallax_decode(const void* q, const void* k, const void* v, const void* r, void* out,
                         int B, int H, int L, int d, int dv, float h, int dtype, void* stream) {
-  if (B > 0 && H > 0 && (!r || !aligned16(r))) return LLA_ERR_INVALID_ARG;
-  DecodeArgs a{q, k, v, r, out, B, H, L, d, dv, h, 1.f, dtype};
-  if (!r) return LLA_ERR_INVALID_ARG;
-  return run_decode(a, stream);
+  return lla_parallax_decode_ex(q, k, v, r, out, B, H, L, d, dv, h, dtype, nullptr, stream);
 }
 
-int lla_parallax_backward(const void* q, const void* k, const void* v, const void* r,
-                          const void* dout, void* dq, void* dk, void* dv, void* dr, int B, int H,
-                          int T, int d, int dv_, float h, int dtype, void* stream) {
-  int st = check_shape(B, H, T, d, dv_, dtype);
+int lla_parallax_backward_ex(const void* q, const void* k, const void* v, const void* r,
+                             const void* dout, void* dq, void* dk, void* dv, void* dr, int B,
+                             int H, int T, int d, int dv_, float h, int dtype,
+                             const lla_options* opts, void* stream) {
+  Args oa;
+  int st = apply_options(opts, false, &oa);
+  if (st != LLA_OK) return st;
+  st = check_shape(B, H, T, d, dv_, dtype);
   if (st != LLA_OK) return st;
   if (!is_finite_pos(h)) return LLA_ERR_INVALID_ARG;
   if ((long long)B * H * T == 0) return LLA_OK;
@@ -349,14 +436,21 @@ int lla_parallax_backward(const void* q, const void* k, const void* v, const voi
     if (!p || !aligned16(p)) return LLA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = nullptr;
-  if (device_status(&status) != cudaSuccess) return LLA_ERR_CUDA;  // sets up the pool
+  if (device_status(&status) != cudaSuccess || ensure_pool() != cudaSuccess) return LLA_ERR_CUDA;
   const ParallaxBwdArgs a{q, k, v, r, dout, dq, dk, dv, dr, B, H, T, d, dv_, h, dtype};
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, parallax_bwd_workspace_bytes(a), s) != cudaSuccess) return LLA_ERR_CUDA;
-  const int path = g_path_request.load() == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
+  const int path = oa.path_req == kPathCudaCore ? kPathCudaCore : kPathTensorCore;
   st = launch_parallax_bwd(a, ws, path, status, s) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
   return st;
+}
+
+int lla_parallax_backward(const void* q, const void* k, const void* v, const void* r,
+                          const void* dout, void* dq, void* dk, void* dv, void* dr, int B, int H,
+                          int T, int d, int dv_, float h, int dtype, void* stream) {
+  return lla_parallax_backward_ex(q, k, v, r, dout, dq, dk, dv, dr, B, H, T, d, dv_, h, dtype,
+                                  nullptr, stream);
 }
 
 int lla_stream_status(void* stream) {
@@ -391,26 +485,6 @@ int lla_version(void) {
 }
 
 unsigned long long lla_launch_count(void) { return g_launches.load(); }
-
-int lla_set_moments_path(int path) {
-  if (path < 0 || path > 3) return LLA_ERR_INVALID_ARG;
-  g_path_request.store(path);
-  return LLA_OK;
-}
-
-int lla_set_cg(int max_iters, float rel_tol) {
-  if (max_iters < 1 || max_iters > 1024 || !(rel_tol > 0.f) || !(rel_tol < 1.f))
-    return LLA_ERR_INVALID_ARG;
-  g_cg_max_iters.store(max_iters);
-  g_cg_rel_tol.store(rel_tol);
-  return LLA_OK;
-}
-
-int lla_set_form(int form) {
-  if (form != kFormCentred && form != kFormPage) return LLA_ERR_INVALID_ARG;
-  g_form.store(form);
-  return LLA_OK;
-}
 
 int lla_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);

@@ -1,5 +1,5 @@
 // Matrix-free conjugate-gradient strategy for the ridge systems of the causal LLA forward
-// (bf16 inputs, d = dv = 64; selected with lla_set_moments_path(3)).
+// (bf16 inputs, d = dv = 64; selected per call with lla_options.path = LLA_PATH_CG).
 //
 // The closed form o_i = vbar_i + C_vk y_i needs y_i = (C_kk + lambda' I)^-1 (q_i - kbar_i) per
 // query. The dense strategy accumulates C_kk (d x d per query) on the tensor cores and factors it.

@@ -26,6 +26,12 @@ struct Args {
   int B, H, T, d, dv;
   float h, lam;
   int dtype;  // lla_dtype
+  // Per-call options (lla_options), validated by the API layer.
+  int path_req = 0;      // lla_path requested (0 = automatic)
+  int form = 0;          // kFormCentred or kFormPage
+  int cg_iters = 1024;   // conjugate-gradient strategy: iteration cap
+  float cg_tol = 1e-3f;  //   and relative residual tolerance
+  int fault = 0;         // test-only fault of the tensor-core moments stage (lla_test_fault)
   long long BH() const { return (long long)B * H; }
   long long rows() const { return (long long)B * H * T; }
 };
@@ -57,6 +63,11 @@ struct Workspace {
   float* cy;      // [BH*T]         tensor-core path: kbar . y
   void* pscr;     // tensor-core path: the kernel weights P of feature pass 0, bf16, one 8 KiB
                   // image per (head, query tile, key block), reused by the later passes
+  __nv_bfloat16* ksh;  // [BH*T, d]  tensor-core path: the keys in the head's frame, bf16(k - c)
+  float* kref;         // [BH, d]    tensor-core path: the head's reference key c (bf16 values)
+  float* kstat;        // [BH, kKeyStatChunks, 2, d]  partial sums of k and k^2 for choosing c
+  int* rep;            // tensor-core path: [1 + kMaxRepairRows] count, then rows whose
+                       // factorisation the precise repair pass redoes
   int* status;    // device status word of the current device
   int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
   int form;       // kFormCentred or kFormPage: which closed form the solve and readout evaluate
@@ -79,34 +90,44 @@ void carve_workspace(const Args& a, void* base, Workspace* ws);
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+// The moment contraction of the tensor-core path (lla_moments_pass_tc.cu): reads the weight
+// images that launch_weights_tc wrote and fills the moment rows.
+cudaError_t launch_moments_pass_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 size_t moments_tc_row_floats();
 size_t moments_tc_pscratch_bytes(long long BH, int T);
 
 // Layout of the tensor-core path's weight scratch: the bf16 kernel weights P of every (head,
-// query tile, key block), written by the moments stage and read back by its feature passes and by
-// the readout. Query tiles of 128 rows go in pairs (ptile: 256 queries); a pair streams key
-// blocks 0..nb-1 of 32 keys, nb = ceil(min(T, 256 (ptile + 1)) / 32). A pair's rank-0 tile's nb
-// blocks come first, then its rank-1 tile's; the pairs of a head follow one another (a full pair
-// p holds 2 x 8 (p + 1) blocks). A block is an 8 KiB image in which 16-byte chunk kc (keys
-// 8kc..8kc+7) of row r sits at kc * 2048 + r * 16: the no-swizzle K-major core-matrix layout of a
-// 128 x 32 bf16 tcgen05 operand (K-adjacent core matrices 2048 B apart, M-adjacent 128 B).
+// query tile, key block), written by the moments stage's weight sweeps and read back by the moment
+// contraction, the readout and the precise repair pass. Query tiles of 128 rows go in pairs
+// (ptile: 256 queries); a pair streams key blocks 0..nb-1 of 32 keys, nb = 2 ceil(min(T,
+// 256 (ptile + 1)) / 64) (an even count: the contraction takes key blocks two at a time; a block
+// past the pair's last key holds zero weights). A pair's rank-0 tile's nb blocks come first, then
+// its rank-1 tile's; the pairs of a head follow one another (a full pair p holds 2 x 8 (p + 1)
+// blocks). A block is an 8 KiB image in which 16-byte chunk kc (keys 8kc..8kc+7) of row r sits at
+// kc * 2048 + r * 16: the no-swizzle K-major core-matrix layout of a 128 x 32 bf16 tcgen05
+// operand (K-adjacent core matrices 2048 B apart, M-adjacent 128 B).
 namespace pscr {
 constexpr int kRows = 128;
 constexpr int kKeys = 32;
 constexpr int kBlockBytes = kRows * kKeys * 2;
 __host__ __device__ inline int pair_blocks(int T, int ptile) {
   const int jend = T < 256 * (ptile + 1) ? T : 256 * (ptile + 1);
-  return (jend + kKeys - 1) / kKeys;
+  return 2 * ((jend + 2 * kKeys - 1) / (2 * kKeys));
 }
 __host__ __device__ inline long long blocks_per_head(int T) {
   const long long np = (T + 255) / 256;
-  return np > 0 ? 8 * (np - 1) * np + 2ll * ((T + kKeys - 1) / kKeys) : 0;
+  return np > 0 ? 8 * (np - 1) * np + 2ll * pair_blocks(T, (int)np - 1) : 0;
 }
 // Index (in blocks) of block 0 of tile (ptile, rank) of head bh.
 __host__ __device__ inline long long first_block(long long bh, int T, int ptile, int rank) {
   return bh * blocks_per_head(T) + 8ll * ptile * (ptile + 1) + (long long)rank * pair_blocks(T, ptile);
 }
 }  // namespace pscr
+// Chunks of a head's keys whose partial statistics choose the tensor-core path's key reference.
+constexpr int kKeyStatChunks = 16;
+// Rows per call whose tensor-core ridge factorisation may be redone by the precise repair pass
+// (more failing rows than this are reported as LLA_ERR_NUMERICAL and left NaN).
+constexpr int kMaxRepairRows = 4096;
 // The tensor-core stage may run for these sizes (whatever path is requested at call time).
 inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64; }
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);

@@ -306,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
                   int BH, float inv_h, float* __restrict__ m_out,
                   float* __restrict__ omega_out, float* __restrict__ mom, uint4* __restrict__ pimg,
-                  int npass, int* __restrict__ status) {
+                  int npass, int fault, int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
@@ -323,7 +323,7 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int i0 = i0p + rank * BM;                // this CTA's first query row
   const int nq = max(0, min(BM, T - i0));
   const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
-  const int nb = (jend + KB - 1) / KB;
+  const int nb = pscr::pair_blocks(T, ptile);     // even: a last block past jend has zero weights
   // key blocks streamed: max sweep, weight sweep (each padded with zero blocks to nb4, whole
   // chunks of SCH), npass feature passes (NPASS for the moments, 0 when only the weights, m and
   // omega are wanted)
@@ -492,11 +492,14 @@ moments_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // copies of a block complete on the stage's barrier (cp.async.mbarrier.arrive), so the loader
     // never waits for its own copies; the consumers that read through the async proxy (Q K^T)
     // fence after their wait (cp.async writes belong to the generic proxy).
+    // With the test-only fault LLA_FAULT_WITHHOLD_KEYS the first key block is never staged: every
+    // wait that needs it runs out after the wait limit, so the timeout path can be tested.
     const __nv_bfloat16* kb = k + base * D;
     for (int g = 0; g < G; ++g) {
       const int st = g % KS;
       const int b = g < 2 * nb4 ? g % nb4 : (g - 2 * nb4) % nb;  // sweep blocks >= nb: zeros
       if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
+      if (g == 0 && fault == LLA_FAULT_WITHHOLD_KEYS) continue;
       uint8_t* dst = smem + SM_K;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
@@ -769,7 +772,7 @@ cudaError_t launch_tc(const Args& a, const Workspace& ws, cudaStream_t s, int np
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
       (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, ws.mom, static_cast<uint4*>(ws.pscr), npass,
-      ws.status);
+      a.fault, ws.status);
   count_launch();
   return cudaGetLastError();
 }

@@ -376,8 +376,9 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
 }
 
 template <typename TOut, bool kMatvec, bool kPage = false>
-cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* v,
-                      const uint32_t* ytc, const float* cy, TOut* out, const int* tile_active) {
+cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* keys,
+                      const void* v, const uint32_t* ytc, const float* cy, TOut* out,
+                      const int* tile_active) {
   auto kern = readout_tc_kernel<TOut, kMatvec, kPage>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -385,7 +386,7 @@ cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const 
   const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
-      static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(v),
+      static_cast<const __nv_bfloat16*>(keys), static_cast<const __nv_bfloat16*>(v),
       static_cast<const uint4*>(ws.pscr), ytc, cy, a.T, (int)a.BH(), out, tile_active,
       ws.status);
   count_launch();
@@ -396,16 +397,19 @@ cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const 
 
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  // the keys in the frame the moments and the solve used (unshifted for the CG strategy)
+  const void* keys = ws.path == kPathTensorCore ? static_cast<const void*>(ws.ksh) : a.k;
   return ws.form == kFormPage
-             ? launch_ro<__nv_bfloat16, false, true>(a, ws, s, a.v, ws.ytc, ws.cy, out, nullptr)
-             : launch_ro<__nv_bfloat16, false>(a, ws, s, a.v, ws.ytc, ws.cy, out, nullptr);
+             ? launch_ro<__nv_bfloat16, false, true>(a, ws, s, keys, a.v, ws.ytc, ws.cy, out,
+                                                     nullptr)
+             : launch_ro<__nv_bfloat16, false>(a, ws, s, keys, a.v, ws.ytc, ws.cy, out, nullptr);
 }
 
 cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,
                                   const void* v, const uint32_t* ytc, const float* cy, float* out,
                                   const int* tile_active, bool matvec) {
-  return matvec ? launch_ro<float, true>(a, ws, s, v, ytc, cy, out, tile_active)
-                : launch_ro<float, false>(a, ws, s, v, ytc, cy, out, tile_active);
+  return matvec ? launch_ro<float, true>(a, ws, s, a.k, v, ytc, cy, out, tile_active)
+                : launch_ro<float, false>(a, ws, s, a.k, v, ytc, cy, out, tile_active);
 }
 
 }  // namespace lla

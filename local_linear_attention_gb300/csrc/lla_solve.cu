@@ -51,6 +51,91 @@ mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, 
   }
 }
 
+// ----------------------------------------------------------------------------- key frame
+// The tensor-core path accumulates exact products of bf16 keys in fp32. When a head's keys sit
+// far from the origin, the raw second moment sum p k k^T is much larger than its centred part
+// C_kk = S - s s^T / omega, and fp32 rounding of S can exceed the smallest eigenvalues of
+// C_kk + lambda' I (queries beyond the keys, small ridge): the factorisation then fails. So the
+// path works in a per-head frame: a reference key c (feature a shifted by the key mean rounded to
+// bf16 when that mean exceeds a quarter of the feature's spread, else 0) is subtracted once, and
+// the moments, the solve and the readout all use kt = bf16(k - c). Shifting leaves the centred
+// moments, and hence LLA, unchanged; rounding the shifted keys to bf16 (exact when c = 0 or when
+// k - c is representable) perturbs the keys, consistently for every stage. Non-finite keys stay
+// non-finite in the frame.
+
+// Partial sums of k and k^2 per feature over chunk blockIdx.y of head blockIdx.x (finite keys).
+__global__ void __launch_bounds__(256)
+key_stats_kernel(const __nv_bfloat16* __restrict__ k, int T, float* __restrict__ part,
+                 int* __restrict__ rep_count) {
+  constexpr int D = 64;
+  __shared__ float red[2][256];
+  const int tid = threadIdx.x, a = tid & (D - 1), r0 = tid >> 6;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *rep_count = 0;  // this call's repair list
+  const long long bh = blockIdx.x;
+  const int ch = blockIdx.y;
+  const int t0 = (int)((long long)T * ch / kKeyStatChunks);
+  const int t1 = (int)((long long)T * (ch + 1) / kKeyStatChunks);
+  float s = 0.f, s2 = 0.f;
+  for (int j = t0 + r0; j < t1; j += 256 / D) {
+    const float x = __bfloat162float(k[(bh * T + j) * D + a]);
+    if (isfinite(x)) {
+      s += x;
+      s2 = fmaf(x, x, s2);
+    }
+  }
+  red[0][tid] = s;
+  red[1][tid] = s2;
+  __syncthreads();
+  if (tid < 2 * D) {
+    const int w = tid / D;  // 0: sum, 1: sum of squares
+    float t = 0.f;
+    for (int r = 0; r < 256 / D; ++r) t += red[w][r * D + a];
+    part[((bh * kKeyStatChunks + ch) * 2 + w) * D + a] = t;
+  }
+}
+
+// The head's reference key c from the partial sums (every CTA of the head derives it in the same
+// order, so all agree), then its chunk of the shifted keys kt = bf16(k - c), eight at a time.
+constexpr int kShiftChunks = 8;
+__global__ void __launch_bounds__(256)
+shift_keys_kernel(const __nv_bfloat16* __restrict__ k, int T, const float* __restrict__ part,
+                  float* __restrict__ kref, __nv_bfloat16* __restrict__ ksh) {
+  constexpr int D = 64;
+  __shared__ float cs[D];
+  const int tid = threadIdx.x;
+  const long long bh = blockIdx.x;
+  if (tid < D) {
+    double s = 0.0, s2 = 0.0;
+    for (int ch = 0; ch < kKeyStatChunks; ++ch) {
+      s += part[((bh * kKeyStatChunks + ch) * 2) * D + tid];
+      s2 += part[((bh * kKeyStatChunks + ch) * 2 + 1) * D + tid];
+    }
+    const double mean = s / T, var = fmax(s2 / T - mean * mean, 0.0);
+    const float c = 16.0 * mean * mean > var ? __bfloat162float(__float2bfloat16_rn((float)mean)) : 0.f;
+    cs[tid] = c;
+    if (blockIdx.y == 0) kref[bh * D + tid] = c;
+  }
+  __syncthreads();
+  const long long n8 = (long long)T * D / 8;  // groups of eight keys' features of this head
+  const long long g0 = n8 * blockIdx.y / kShiftChunks, g1 = n8 * (blockIdx.y + 1) / kShiftChunks;
+  const uint4* src = reinterpret_cast<const uint4*>(k + bh * T * D);
+  uint4* dst = reinterpret_cast<uint4*>(ksh + bh * T * D);
+  for (long long g = g0 + tid; g < g1; g += 256) {
+    const uint4 x = src[g];
+    const int a0 = (int)((g * 8) & (D - 1));
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float lo = __uint_as_float(w[t] << 16) - cs[a0 + 2 * t];
+      const float hi = __uint_as_float(w[t] & 0xFFFF0000u) - cs[a0 + 2 * t + 1];
+      const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+      o[t] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    dst[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ----------------------------------------------------------------------------- solve
 constexpr int kWarpsPerBlock = 4;
 
@@ -447,10 +532,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // and cy = q . rho*, so that the readout's t_ij = k_j . rho* - cy is the page's z_ij . rho*.
 template <bool PAGE>
 __global__ void __launch_bounds__(stc::WARPS * 32, 3)
-solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ mom, const float* __restrict__ omega,
-                const float* __restrict__ mrow, long long rows, float lam, uint32_t* __restrict__ ytc,
+solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kref,
+                const float* __restrict__ mom, const float* __restrict__ omega,
+                const float* __restrict__ mrow, long long rows, int T, float lam,
+                uint32_t* __restrict__ ytc,
                 float* __restrict__ cy_out, float* __restrict__ y_out, float* __restrict__ kbar_out,
-                int* __restrict__ status) {
+                int* __restrict__ rep, int* __restrict__ status) {
   using namespace stc;
   __shared__ __align__(16) float sh[WARPS][WARP_FLOATS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -475,8 +562,10 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   const float d0 = __ldcs(g + tc_slot(L.r0, L.r0)), d1 = __ldcs(g + tc_slot(L.r1, L.r1));
   const float s0 = __ldcs(g + run_base(L.r0) + D), s1 = __ldcs(g + run_base(L.r1) + D);
   const float om = omega[row];
-  const float qa = ldf(q, row * D + L.r0);  // keys are not shifted on this path (c = 0)
-  const float qb = ldf(q, row * D + L.r1);
+  // the query in the head's key frame (the moments are those of kt = bf16(k - c))
+  const int bh = (int)row / T;  // rows < 2^31
+  const float qa = ldf(q, row * D + L.r0) - kref[bh * D + L.r0];
+  const float qb = ldf(q, row * D + L.r1) - kref[bh * D + L.r1];
   double lpd = (double)lam * exp(-(double)mrow[row]);  // ridge scaled by exp(-m)
   lpd = fmin(fmax(lpd, (double)FLT_MIN), (double)FLT_MAX);
   const float lp = (float)lpd;
@@ -533,6 +622,16 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   stc::column<0>(L, cbuf, Lt);
   uint32_t* yrow = ytc + row * 3 * (D / 2);
   if (!L.ok) {
+    // A non-positive pivot: fp32 rounding of the tensor-core sums can exceed the smallest
+    // eigenvalues of a very ill-conditioned system. The row goes to the precise repair pass
+    // (repair_kernel), which overwrites this row's y; if its list is full, the row is NaN.
+    int slot = kMaxRepairRows;
+    if (lane == 0) slot = atomicAdd(rep, 1);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (slot < kMaxRepairRows) {
+      if (lane == 0) rep[1 + slot] = (int)row;
+      return;
+    }
     if (lane == 0) {
       atomicOr(status, kStatusNumerical);
       cy_out[row] = __int_as_float(0x7fc00000);
@@ -576,13 +675,229 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ m
   }
 }
 
+// ----------------------------------------------------------------------------- precise repair
+// Rows whose tensor-core factorisation met a non-positive pivot are solved again here, exactly
+// enough for any conditioning the fp64 factorisation can handle: the same weighted problem (the
+// bf16 weights of the weight images, the same bf16 keys in the head's frame, so that the readout
+// stays consistent with it) with the sums formed without rounding error worth the name. Each
+// term p_j x_a x_b is a product of three bf16 values, 24 significant bits, hence exact in fp32; the
+// terms are summed in compensated fp32 pairs (TwoSum), centred and factored in fp64. One CTA per
+// row (the CTAs stride over the list); nothing runs when the list is empty.
+namespace rep {
+constexpr int D = 64;
+constexpr int NE = 1 + D + D * (D + 1) / 2;  // omega, s, upper triangle of S
+constexpr int NT = 256;
+constexpr int EPT = (NE + NT - 1) / NT;      // entries per thread
+constexpr int KC = 64;                       // keys per staged chunk
+}  // namespace rep
+constexpr int kRepairGrid = 152;
+
+template <bool PAGE>
+__global__ void __launch_bounds__(rep::NT)
+repair_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ ksh,
+              const float* __restrict__ kref, const uint8_t* __restrict__ pimg,
+              const float* __restrict__ mrow, const int* __restrict__ rep, int T, float lam,
+              uint32_t* __restrict__ ytc, float* __restrict__ cy_out, float* __restrict__ y_out,
+              float* __restrict__ kbar_out, int* __restrict__ status) {
+  using namespace rep;
+  // the staged key chunk during the sums, then the fp64 system (the two are never live together)
+  __shared__ __align__(16) double buf[D * (D + 1)];
+  __shared__ float ps[KC];
+  __shared__ double vs[D], zs[D];
+  __shared__ int fail;
+  float (*ks)[D + 1] = reinterpret_cast<float (*)[D + 1]>(buf);
+  double (*C)[D + 1] = reinterpret_cast<double (*)[D + 1]>(buf);
+  static_assert(sizeof(float) * KC * (D + 1) <= sizeof(double) * D * (D + 1), "buffer reuse");
+  const int tid = threadIdx.x;
+  const int count = min(rep[0], kMaxRepairRows);
+
+  // this thread's entries: e = 0 omega, 1..D the s_a, then S_ab (a <= b) row by row
+  int ea[EPT], eb[EPT];
+#pragma unroll
+  for (int m = 0; m < EPT; ++m) {
+    int e = tid + m * NT, a = -1, b = -1;
+    if (e >= NE) { a = -2; }
+    else if (e >= 1 && e <= D) { a = e - 1; }
+    else if (e > D) {
+      int t = e - 1 - D;
+      a = 0;
+      while (t >= D - a) { t -= D - a; ++a; }
+      b = a + t;
+    }
+    ea[m] = a;
+    eb[m] = b;
+  }
+
+  for (int slot = blockIdx.x; slot < count; slot += gridDim.x) {
+    const long long row = rep[1 + slot];
+    const long long bh = row / T;
+    const int i = (int)(row % T);
+    const int ptile = i / 256, rank = (i % 256) / 128, r = i % 128;
+    const uint8_t* img0 = pimg + pscr::first_block(bh, T, ptile, rank) * pscr::kBlockBytes;
+    float hi[EPT], lo[EPT];
+#pragma unroll
+    for (int m = 0; m < EPT; ++m) hi[m] = lo[m] = 0.f;
+    for (int j0 = 0; j0 <= i; j0 += KC) {
+      __syncthreads();
+      for (int e = tid; e < KC * D; e += NT) {
+        const int jj = e / D, a = e % D, j = j0 + jj;
+        ks[jj][a] = j <= i ? __bfloat162float(ksh[(bh * T + j) * D + a]) : 0.f;
+      }
+      for (int jj = tid; jj < KC; jj += NT) {
+        const int j = j0 + jj;
+        float p = 0.f;
+        if (j <= i) {
+          const int b = j / pscr::kKeys, c = j % pscr::kKeys;
+          const __nv_bfloat16* w = reinterpret_cast<const __nv_bfloat16*>(
+              img0 + (size_t)b * pscr::kBlockBytes + (c / 8) * 2048 + r * 16) + (c % 8);
+          p = __bfloat162float(*w);
+        }
+        ps[jj] = p;
+      }
+      __syncthreads();
+      const int jn = min(KC, i + 1 - j0);
+      for (int jj = 0; jj < jn; ++jj) {
+        const float p = ps[jj];
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) {
+          if (ea[m] < -1) continue;
+          float x = p;                                  // exact: three bf16 factors at most
+          if (ea[m] >= 0) x *= ks[jj][ea[m]];
+          if (eb[m] >= 0) x *= ks[jj][eb[m]];
+          const float t = hi[m] + x, z = t - hi[m];     // TwoSum into (hi, lo)
+          lo[m] += (hi[m] - (t - z)) + (x - z);
+          hi[m] = t;
+        }
+      }
+    }
+    __syncthreads();
+    // the sums into the fp64 system: C[a][b] = S_ab (a <= b), C[a][D] = s_a, C[0][0..] etc.
+    double om_local = 0.0;
+#pragma unroll
+    for (int m = 0; m < EPT; ++m) {
+      const double v = (double)hi[m] + (double)lo[m];
+      if (ea[m] == -1) vs[0] = v;  // omega kept apart in vs[0] until zs is formed
+      else if (ea[m] >= 0 && eb[m] < 0) C[ea[m]][D] = v;
+      else if (ea[m] >= 0) C[ea[m]][eb[m]] = v;
+      (void)om_local;
+    }
+    __syncthreads();
+    const double om = vs[0];
+    __syncthreads();
+    const double lp = fmin(fmax((double)lam * exp(-(double)mrow[row]), (double)FLT_MIN), (double)FLT_MAX);
+    if (tid < D) {
+      const double qa = (double)__bfloat162float(q[row * D + tid]) - (double)kref[bh * D + tid];
+      const double sa = C[tid][D];
+      vs[tid] = sa / om;                               // kbar (head frame)
+      zs[tid] = PAGE ? sa - om * qa : qa - sa / om;    // page: mu = s - omega q; centred: q - kbar
+    }
+    __syncthreads();
+    // centred system (page form: plus mu mu^T / omega), lower triangle, ridge on the diagonal
+    for (int e = tid; e < D * D; e += NT) {
+      const int a = e / D, b = e % D;
+      if (b > a) continue;
+      double v = C[b][a] - C[a][D] * C[b][D] / om;  // S stored at [min][max]
+      if (PAGE) v += zs[a] * zs[b] / om;
+      if (a == b) v += lp;
+      C[a][b] = v;
+    }
+    if (tid == 0) fail = 0;
+    __syncthreads();
+    // Cholesky C = L L^T in place (lower triangle), column by column
+    for (int kk = 0; kk < D; ++kk) {
+      if (tid == 0) {
+        const double d = C[kk][kk];
+        if (!(d > 0.0)) fail = 1;
+        C[kk][kk] = d > 0.0 ? sqrt(d) : 1.0;
+      }
+      __syncthreads();
+      const double lkk = C[kk][kk];
+      for (int a = kk + 1 + tid; a < D; a += NT) C[a][kk] /= lkk;
+      __syncthreads();
+      for (int e = tid; e < D * D; e += NT) {
+        const int a = e / D, b = e % D;
+        if (a > kk && b > kk && b <= a) C[a][b] -= C[a][kk] * C[b][kk];
+      }
+      __syncthreads();
+    }
+    if (tid < 32) {
+      // forward and backward substitution (one warp; lane t owns rows t and t + 32)
+      double w0 = zs[tid], w1 = zs[tid + 32];
+      for (int kk = 0; kk < D; ++kk) {
+        const double own = kk < 32 ? w0 : w1;
+        const double xk = __shfl_sync(0xffffffffu, own, kk & 31) / C[kk][kk];
+        if (tid == (kk & 31)) { if (kk < 32) w0 = xk; else w1 = xk; }
+        if (tid > kk) w0 -= C[tid][kk] * xk;
+        if (tid + 32 > kk) w1 -= C[tid + 32][kk] * xk;
+      }
+      for (int kk = D - 1; kk >= 0; --kk) {
+        const double own = kk < 32 ? w0 : w1;
+        const double yk = __shfl_sync(0xffffffffu, own, kk & 31) / C[kk][kk];
+        if (tid == (kk & 31)) { if (kk < 32) w0 = yk; else w1 = yk; }
+        if (tid < kk) w0 -= C[kk][tid] * yk;
+        if (tid + 32 < kk) w1 -= C[kk][tid + 32] * yk;
+      }
+      zs[tid] = w0;       // y
+      zs[tid + 32] = w1;
+    }
+    __syncthreads();
+    uint32_t* yrow = ytc + row * 3 * (D / 2);
+    if (fail) {
+      if (tid == 0) {
+        atomicOr(status, kStatusNumerical);
+        cy_out[row] = __int_as_float(0x7fc00000);
+      }
+      if (tid < 3 * (D / 2)) yrow[tid] = 0x7FC07FC0u;  // bf16 NaN pairs
+      if (y_out && tid < D) {
+        y_out[row * D + tid] = __int_as_float(0x7fc00000);
+        kbar_out[row * D + tid] = __int_as_float(0x7fc00000);
+      }
+      continue;
+    }
+    if (tid < 32) {
+      // y as three bf16 parts, lane l writing elements 2l and 2l + 1 of each; cy = kbar . y
+      // (page form: q . rho*, q in the head's frame)
+      const float ya = (float)zs[2 * tid], yb = (float)zs[2 * tid + 1];
+      const uint32_t p1 = pack_bf16(ya, yb);
+      const float ra = ya - __uint_as_float(p1 << 16), rb = yb - __uint_as_float(p1 & 0xFFFF0000u);
+      const uint32_t p2 = pack_bf16(ra, rb);
+      const uint32_t p3 =
+          pack_bf16(ra - __uint_as_float(p2 << 16), rb - __uint_as_float(p2 & 0xFFFF0000u));
+      yrow[tid] = p1;
+      yrow[D / 2 + tid] = p2;
+      yrow[D + tid] = p3;
+      double c = 0.0;
+      for (int a = tid; a < D; a += 32) {
+        const double qa = (double)__bfloat162float(q[row * D + a]) - (double)kref[bh * D + a];
+        c += (PAGE ? qa : vs[a]) * zs[a];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (tid == 0) cy_out[row] = (float)c;
+    }
+    if (y_out && tid < D) {
+      y_out[row * D + tid] = (float)zs[tid];
+      kbar_out[row * D + tid] = (float)vs[tid];
+    }
+  }
+}
+
 cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long rows = a.rows();
   const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
   auto kern = ws.form == kFormPage ? solve_tc_kernel<true> : solve_tc_kernel<false>;
   kern<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a.q), ws.mom, ws.omega, ws.m, rows, a.lam, ws.ytc, ws.cy,
-      a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.status);
+      static_cast<const __nv_bfloat16*>(a.q), ws.kref, ws.mom, ws.omega, ws.m, rows, a.T, a.lam,
+      ws.ytc, ws.cy,
+      a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.rep, ws.status);
+  count_launch();
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  auto rk = ws.form == kFormPage ? repair_kernel<true> : repair_kernel<false>;
+  rk<<<kRepairGrid, rep::NT, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), ws.ksh, ws.kref, static_cast<const uint8_t*>(ws.pscr),
+      ws.m, ws.rep, a.T, a.lam, ws.ytc, ws.cy, a.dv == 64 ? nullptr : ws.y,
+      a.dv == 64 ? nullptr : ws.kbar, ws.status);
   count_launch();
   return cudaGetLastError();
 }
@@ -605,8 +920,19 @@ cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
-  // The tensor-core paths leave keys unshifted, and their readout (dv = 64) forms every value
-  // term from centred weights, so they need neither reference point.
+  if (ws.path == kPathTensorCore) {  // the keys in the head's frame (see key_stats_kernel)
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+    key_stats_kernel<<<dim3((unsigned)a.BH(), kKeyStatChunks), 256, 0, s>>>(k, a.T, ws.kstat,
+                                                                          ws.rep);
+    count_launch();
+    shift_keys_kernel<<<dim3((unsigned)a.BH(), kShiftChunks), 256, 0, s>>>(k, a.T, ws.kstat,
+                                                                           ws.kref, ws.ksh);
+    count_launch();
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  // The tensor-core readout (dv = 64) forms every value term from centred weights and needs no
+  // value reference point; the CG strategy keeps its keys unshifted.
   if (ws.path != kPathCudaCore && a.dv == 64) return cudaSuccess;
   const dim3 grid((unsigned)a.BH(), 2);
   if (a.dtype == LLA_F32)
@@ -618,7 +944,12 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
         static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v), a.T, a.d,
         a.dv, ws.kmean, ws.vmean, ws.path == kPathTensorCore);
   count_launch();
-  return cudaGetLastError();
+  cudaError_t err = cudaGetLastError();
+  // The CUDA-core readout after the tensor-core solve (dv != 64) works in the solve's key frame.
+  if (err == cudaSuccess && ws.path == kPathTensorCore)
+    err = cudaMemcpyAsync(ws.kmean, ws.kref, a.BH() * a.d * sizeof(float),
+                          cudaMemcpyDeviceToDevice, s);
+  return err;
 }
 
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s) {

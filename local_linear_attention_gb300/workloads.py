@@ -95,7 +95,7 @@ def make_probe(B, H, T, d, dtype, seed):
 
 
 def make_stress(B, H, T, d, dv, dtype, seed, rank: int = 8, key_noise: float = 1e-3,
-                value_noise: float = 0.01):
+                value_noise: float = 0.01, return_u1: bool = False):
     """Ill-conditioned keys, half of the queries outside the key cloud, near-affine values.
 
     Per (b, h), in this draw order from one float64 generator: an orthonormal basis
@@ -103,11 +103,12 @@ def make_stress(B, H, T, d, dv, dtype, seed, rank: int = 8, key_noise: float = 1
     coordinates and query noise, A [dv, d] ~ N(0, 1/d), c [dv] ~ N(0, 1), value noise.
     k = U g + key_noise * n; q likewise; then every key is moved along u_1 by
     median_i(q_i . u_1) - min_j(k_j . u_1), which puts half of the queries beyond all keys
-    along u_1. v = A k + c + value_noise * n.
+    along u_1. v = A k + c + value_noise * n. With return_u1, also returns the shift directions
+    u_1 [B, H, d] (float64).
     """
     g = torch.Generator().manual_seed(seed)
     f64 = torch.float64
-    qs, ks, vs = [], [], []
+    qs, ks, vs, us = [], [], [], []
     for _ in range(B * H):
         U, _ = torch.linalg.qr(torch.randn(d, rank, generator=g, dtype=f64))
         gk = torch.randn(T, rank, generator=g, dtype=f64)
@@ -122,9 +123,10 @@ def make_stress(B, H, T, d, dv, dtype, seed, rank: int = 8, key_noise: float = 1
         u1 = U[:, 0]
         k = k + (torch.median(q @ u1) - torch.min(k @ u1)) * u1
         v = k @ A.T + c + value_noise * nv
-        qs.append(q), ks.append(k), vs.append(v)
+        qs.append(q), ks.append(k), vs.append(v), us.append(u1)
     shape = lambda xs, w: torch.stack(xs).reshape(B, H, T, w)  # noqa: E731
-    return (_cast(shape(qs, d), dtype), _cast(shape(ks, d), dtype), _cast(shape(vs, dv), dtype))
+    out = (_cast(shape(qs, d), dtype), _cast(shape(ks, d), dtype), _cast(shape(vs, dv), dtype))
+    return out + (torch.stack(us).reshape(B, H, d),) if return_u1 else out
 
 
 def make_inputs(w: Workload):

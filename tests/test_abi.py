@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strings(lib):
     lib.lla_version.restype = ctypes.c_int
-    assert lib.lla_version() == 100
+    assert lib.lla_version() == 200
     lib.lla_status_string.restype = ctypes.c_char_p
     for st in range(6):
         assert lib.lla_status_string(st).decode().startswith("LLA_")
@@ -123,3 +123,83 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     with pytest.raises(ImportError):
         b.lla_version()
     importlib.reload(b)
+
+
+def _fwd_ex(lib, opts, T=4, d=16, dtype=0):
+    from local_linear_attention_gb300.binding import Options
+    vp = ctypes.c_void_p
+    f = lib.lla_forward_ex
+    f.restype = ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp] + [ctypes.c_int] * 5 + [ctypes.c_float] * 2 + \
+        [ctypes.c_int, ctypes.POINTER(Options), vp, ctypes.c_size_t, vp]
+    p = ctypes.c_void_p(16)
+    return f(p, p, p, p, 1, 1, T, d, d, 4.0, 0.01, dtype,
+             ctypes.byref(opts) if opts is not None else None, None, 0, None)
+
+
+def test_options_struct_layout():
+    from local_linear_attention_gb300.binding import Options
+    assert ctypes.sizeof(Options) == 32  # 5 fields + 3 reserved ints, as lla_options
+
+
+def test_invalid_options_rejected_on_the_host(lib):
+    """Options are validated before any device work (these calls would otherwise need a GPU)."""
+    from local_linear_attention_gb300.binding import Options
+    INVALID = 1
+
+    def opts(**kw):
+        o = Options()
+        for key, val in kw.items():
+            setattr(o, key, val)
+        return o
+    assert _fwd_ex(lib, opts(path=4)) == INVALID
+    assert _fwd_ex(lib, opts(path=-1)) == INVALID
+    assert _fwd_ex(lib, opts(form=2)) == INVALID
+    assert _fwd_ex(lib, opts(cg_max_iters=1025)) == INVALID
+    assert _fwd_ex(lib, opts(cg_rel_tol=1.0)) == INVALID
+    assert _fwd_ex(lib, opts(cg_rel_tol=float("nan"))) == INVALID
+    assert _fwd_ex(lib, opts(test_fault=2)) == INVALID
+    o = opts()
+    o.reserved[1] = 5
+    assert _fwd_ex(lib, o) == INVALID
+    # empty problems with valid options stay a no-op
+    assert _fwd_ex(lib, opts(path=1), T=0) == 0
+    assert _fwd_ex(lib, None, T=0) == 0
+    # the other operations accept a path only
+    vp = ctypes.c_void_p
+    f = lib.lla_parallax_forward_ex
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                    ctypes.POINTER(Options), vp]
+    p = vp(16)
+    assert f(p, p, p, p, p, 1, 1, 4, 16, 16, 4.0, 0, ctypes.byref(opts(form=1)), None) == INVALID
+    assert f(p, p, p, p, p, 1, 1, 4, 16, 16, 4.0, 0, ctypes.byref(opts(path=3)), None) == INVALID
+    g = lib.lla_decode_ex
+    g.restype = ctypes.c_int
+    g.argtypes = [vp] * 4 + [ctypes.c_int] * 5 + [ctypes.c_float] * 2 + [
+        ctypes.c_int, ctypes.POINTER(Options), vp]
+    assert g(p, p, p, p, 1, 1, 4, 16, 16, 4.0, 0.01, 0, ctypes.byref(opts(test_fault=1)),
+             None) == INVALID
+
+
+def test_noalloc_size_limits_match_the_documented_ones(lib):
+    """lla_forward_noalloc's documented limits (bf16 d = dv = 64: T <= 4343 at B*H = 1,
+    T <= 704 at B*H = 8) follow from lla_workspace_size and the fixed scratch size, and the
+    entry point refuses the next size up before touching any device."""
+    from local_linear_attention_gb300.binding import NOALLOC_SCRATCH_BYTES
+    ws = lib.lla_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.c_int] * 6
+    with open(os.path.join(ROOT, "include", "lla.h")) as fh:
+        header = fh.read()
+    assert "#define LLA_NOALLOC_SCRATCH_BYTES (64ull << 20)" in header
+    assert NOALLOC_SCRATCH_BYTES == 64 << 20
+    for BH, tmax in ((1, 4343), (8, 704)):
+        assert ws(1, BH, tmax, 64, 64, 1) <= NOALLOC_SCRATCH_BYTES < ws(1, BH, tmax + 1, 64, 64, 1)
+    vp = ctypes.c_void_p
+    f = lib.lla_forward_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [vp] * 4 + [ctypes.c_int] * 5 + [ctypes.c_float] * 2 + [ctypes.c_int, vp]
+    p = vp(16)
+    assert f(p, p, p, p, 1, 1, 4344, 64, 64, 8.0, 0.01, 1, None) == 2   # LLA_ERR_UNSUPPORTED
+    assert f(p, p, p, p, 1, 8, 705, 64, 64, 8.0, 0.01, 1, None) == 2

@@ -16,8 +16,12 @@ import bench  # noqa: E402
 def test_flops_per_pair_counts():
     # moments: the logit (2d) and omega, sum w k, the upper triangle of sum w k k^T (2 each)
     assert bench.moments_flops_per_pair(64) == 128 + 2 * (1 + 64 + 64 * 65 // 2) == 4418
-    # executed on the tensor cores: two Q K^T sweeps, hi and lo over 2208 feature slots
-    assert bench.tc_executed_flops_per_pair(64) == 2 * 2 * 64 + 2 * 2 * 2208 == 9088
+    # the contraction alone: omega, sum w k, the upper triangle of sum w k k^T
+    assert bench.contraction_flops_per_pair(64) == 2 * (1 + 64 + 64 * 65 // 2) == 4290
+    # executed on the tensor cores: hi and lo over 5 passes of 448 feature columns; the weight
+    # sweeps run Q K^T twice
+    assert bench.tc_executed_flops_per_pair(64) == 2 * 2 * 5 * 448 == 8960
+    assert bench.tc_weights_executed_flops_per_pair(64) == 2 * 2 * 64
     # Parallax forward: q.k, r.k, P1 V, P2 V
     assert bench.parallax_flops_per_pair(64, 64) == 512
     # Parallax backward: the record pass (4d + 4dv), then q.k, r.k, dO.v once, dq, dr, dk, dv

@@ -1,4 +1,4 @@
-"""GPU parity of the matrix-free conjugate-gradient strategy (lla_set_moments_path(3)).
+"""GPU parity of the matrix-free conjugate-gradient strategy (lla_forward_ex with path LLA_PATH_CG).
 
 The strategy solves each query's ridge system (C_kk + lambda' I) y = q - kbar by CG, every
 product with C_kk being one streaming pass over the prefix, instead of accumulating and
@@ -25,13 +25,22 @@ def lla():
     return binding
 
 
+class _WithOptions:
+    """The binding with fixed per-call options on lla_forward."""
+
+    def __init__(self, lla, **opts):
+        self._lla, self._opts = lla, opts
+
+    def lla_forward(self, *args, **kw):
+        return self._lla.lla_forward(*args, **{**self._opts, **kw})
+
+    def __getattr__(self, name):
+        return getattr(self._lla, name)
+
+
 @pytest.fixture
 def cg(lla):
-    lla.lla_set_moments_path(lla.PATH_CG)
-    lla.lla_set_cg(1024, 1e-3)
-    yield lla
-    lla.lla_set_moments_path(lla.PATH_AUTO)
-    lla.lla_set_cg(1024, 1e-3)
+    return _WithOptions(lla, path=lla.PATH_CG, cg=(1024, 1e-3))
 
 
 def rel_err(got, ref):
@@ -65,11 +74,7 @@ def test_cg_headline_sampled_rows(cg):
 def test_cg_agrees_with_dense(lla):
     q, k, v = W.make_iid(2, 2, 512, 64, 64, "bf16", seed=31)
     dense = run(lla, q, k, v, 8.0, 1e-2)
-    lla.lla_set_moments_path(lla.PATH_CG)
-    try:
-        it = run(lla, q, k, v, 8.0, 1e-2)
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    it = run(_WithOptions(lla, path=lla.PATH_CG), q, k, v, 8.0, 1e-2)
     assert rel_err(it.reshape(-1, 64), dense.reshape(-1, 64)) <= TOL_BF16
 
 
@@ -93,6 +98,8 @@ def test_cg_nonfinite_input_reports_numerical(cg):
 
 
 def test_cg_parameters_are_checked(lla):
-    for bad in ((0, 1e-3), (2000, 1e-3), (10, 0.0), (10, 1.5)):
-        with pytest.raises(lla.LlaError):
-            lla.lla_set_cg(*bad)
+    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3))
+    for bad in ((-1, 1e-3), (2000, 1e-3), (10, -0.5), (10, 1.5)):
+        with pytest.raises(lla.LlaError) as ei:
+            lla.lla_forward(q, k, v, 8.0, 1e-2, path=lla.PATH_CG, cg=bad)
+        assert ei.value.status == 1  # LLA_ERR_INVALID_ARG

@@ -133,12 +133,8 @@ def test_lla_decode_tensor_cores_match_oracle_and_cuda_cores(lla, L):
     qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
     tc = lla.lla_decode(qc, kc, vc, h, lam)
     assert lla.lla_stream_status() == 0
-    lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
-    try:
-        cc = lla.lla_decode(qc, kc, vc, h, lam)
-        assert lla.lla_stream_status() == 0
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    cc = lla.lla_decode(qc, kc, vc, h, lam, path=lla.PATH_CUDA_CORE)
+    assert lla.lla_stream_status() == 0
     Q, K, V = f64(q).reshape(-1, d), f64(k).reshape(-1, L, d), f64(v).reshape(-1, L, d)
     ref = np.stack([lla_row(Q[i], K[i], V[i], h, lam) for i in range(B * H)])
     got_tc, got_cc = f64(tc).reshape(-1, d), f64(cc).reshape(-1, d)
@@ -174,13 +170,9 @@ def test_lla_decode_long_cache_with_empty_splits(lla, path):
     B, H, L, d = 1, 1, 100000, 64
     q, k, v, _ = make(B, H, L, d, d, "bf16", seed=61)
     h, lam = 8.0, 1e-2
-    if path == "cuda":
-        lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
-    try:
-        out = lla.lla_decode(q.cuda(), k.cuda(), v.cuda(), h, lam)
-        assert lla.lla_stream_status() == 0
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    out = lla.lla_decode(q.cuda(), k.cuda(), v.cuda(), h, lam,
+                         path=lla.PATH_CUDA_CORE if path == "cuda" else lla.PATH_AUTO)
+    assert lla.lla_stream_status() == 0
     got = f64(out).reshape(-1, d)
     assert np.isfinite(got).all()
     ref = lla_row(f64(q).reshape(d), f64(k).reshape(L, d), f64(v).reshape(L, d), h, lam)

@@ -1,4 +1,4 @@
-"""GPU parity of the page form of the LLA intercept (lla_set_form(1)).
+"""GPU parity of the page form of the LLA intercept (lla_forward_ex with form LLA_FORM_PAGE).
 
 The page form solves (sum w z z^T + lambda' I) rho* = sum w z with the query-centred z = k - q and
 evaluates o = sum w (1 - z.rho*) v / sum w (1 - z.rho*) as the exact-LLA two-branch epilogue
@@ -25,11 +25,22 @@ def lla():
     return binding
 
 
+class _WithOptions:
+    """The binding with fixed per-call options on lla_forward."""
+
+    def __init__(self, lla, **opts):
+        self._lla, self._opts = lla, opts
+
+    def lla_forward(self, *args, **kw):
+        return self._lla.lla_forward(*args, **{**self._opts, **kw})
+
+    def __getattr__(self, name):
+        return getattr(self._lla, name)
+
+
 @pytest.fixture
 def page(lla):
-    lla.lla_set_form(lla.FORM_PAGE)
-    yield lla
-    lla.lla_set_form(lla.FORM_CENTRED)
+    return _WithOptions(lla, form=lla.FORM_PAGE)
 
 
 def rel_err(got, ref):
@@ -63,11 +74,7 @@ def test_page_form_headline_sampled_rows(page):
 def test_page_form_agrees_with_centred(lla):
     q, k, v = W.make_iid(2, 2, 512, 64, 64, "bf16", seed=41)
     centred = run(lla, q, k, v, 8.0, 1e-2)
-    lla.lla_set_form(lla.FORM_PAGE)
-    try:
-        pg = run(lla, q, k, v, 8.0, 1e-2)
-    finally:
-        lla.lla_set_form(lla.FORM_CENTRED)
+    pg = run(_WithOptions(lla, form=lla.FORM_PAGE), q, k, v, 8.0, 1e-2)
     assert rel_err(pg.reshape(-1, 64), centred.reshape(-1, 64)) <= TOL_BF16
 
 
@@ -85,16 +92,15 @@ def test_page_form_other_paths_unsupported(page):
         q, k, v = W.make_iid(1, 1, 64, d, d, dtype, seed=2)
         with pytest.raises(page.LlaError):
             page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2)
-    page.lla_set_moments_path(page.PATH_CG)
-    try:
-        q, k, v = W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3)
-        with pytest.raises(page.LlaError):
-            page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2)
-    finally:
-        page.lla_set_moments_path(page.PATH_AUTO)
+    q, k, v = W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3)
+    with pytest.raises(page.LlaError) as ei:
+        page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2, path=page.PATH_CG)
+    assert ei.value.status == 2  # LLA_ERR_UNSUPPORTED
 
 
-def test_set_form_rejects_other_values(lla):
+def test_form_option_rejects_other_values(lla):
+    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3))
     for bad in (-1, 2, 7):
-        with pytest.raises(lla.LlaError):
-            lla.lla_set_form(bad)
+        with pytest.raises(lla.LlaError) as ei:
+            lla.lla_forward(q, k, v, 8.0, 1e-2, form=bad)
+        assert ei.value.status == 1  # LLA_ERR_INVALID_ARG

@@ -125,11 +125,7 @@ def test_parallax_backward_tensor_cores_matches_oracle(lla, T):
 def test_parallax_backward_tensor_and_cuda_cores_agree(lla):
     xs = [x.cuda() for x in make(2, 2, 777, 64, 64, "bf16", seed=8)]
     tc = lla.lla_parallax_backward(*xs, 8.0)
-    lla.lla_set_moments_path(lla.PATH_CUDA_CORE)
-    try:
-        cc = lla.lla_parallax_backward(*xs, 8.0)
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    cc = lla.lla_parallax_backward(*xs, 8.0, path=lla.PATH_CUDA_CORE)
     assert lla.lla_stream_status() == 0
     for name, a, b in zip(("dq", "dk", "dv", "dr"), tc, cc):
         assert rel_err(f64(a), f64(b)) <= TOL["bf16"], name

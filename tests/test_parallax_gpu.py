@@ -30,8 +30,8 @@ def rel_err(got, ref):
     return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
 
-def run(lla, q, k, v, r, h):
-    out = lla.lla_parallax_forward(q.cuda(), k.cuda(), v.cuda(), r.cuda(), h)
+def run(lla, q, k, v, r, h, path=0):
+    out = lla.lla_parallax_forward(q.cuda(), k.cuda(), v.cuda(), r.cuda(), h, path=path)
     assert lla.lla_stream_status() == 0
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -93,13 +93,8 @@ def test_short_sequences_tensor_core(lla, T):
 
 def test_paths_agree(lla):
     q, k, v, r = inputs(1, 2, 257, 64, 64, "bf16", seed=77)
-    outs = {}
-    try:
-        for path in (lla.PATH_CUDA_CORE, lla.PATH_TENSOR_CORE):
-            lla.lla_set_moments_path(path)
-            outs[path] = run(lla, q, k, v, r, 8.0)
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    outs = {path: run(lla, q, k, v, r, 8.0, path=path)
+            for path in (lla.PATH_CUDA_CORE, lla.PATH_TENSOR_CORE)}
     ref = parallax_forward_oracle(q, k, v, r, 8.0).reshape(outs[1].shape)
     for path, o in outs.items():
         assert rel_err(o, ref) <= 2e-2, (path, rel_err(o, ref))

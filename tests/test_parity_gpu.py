@@ -13,6 +13,7 @@ import torch
 
 from local_linear_attention_gb300 import workloads as W
 from oracle import lla_forward_oracle, lla_moments_oracle
+from parity import record, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -26,12 +27,8 @@ def lla():
     return binding
 
 
-def rel_err(got, ref):
-    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
-
-
-def run(lla, q, k, v, h, lam):
-    out = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), h, lam)
+def run(lla, q, k, v, h, lam, **opts):
+    out = lla.lla_forward(q.cuda(), k.cuda(), v.cuda(), h, lam, **opts)
     assert lla.lla_stream_status() == 0
     return out.float().cpu().numpy().astype(np.float64)
 
@@ -45,9 +42,7 @@ def check(lla, q, k, v, h, lam, dtype, rows=None, tol=None):
     else:
         ref = lla_forward_oracle(q, k, v, h, lam, rows=rows)
         flat = flat[rows]
-    err = rel_err(flat, ref)
-    assert np.isfinite(flat).all()
-    assert err <= (tol or TOL[dtype]), f"relative error {err:.3e}"
+    err, _ = record(flat, ref, v.float().numpy(), tol or TOL[dtype])
     return err
 
 
@@ -192,13 +187,8 @@ def test_moments_bad_index_sets_status(lla):
 def test_moments_paths_agree(lla, T):
     """The tensor-core and CUDA-core moments stages give the same forward (bf16, d = 64)."""
     q, k, v = W.make_iid(1, 2, T, 64, 64, "bf16", seed=40 + T)
-    outs = {}
-    try:
-        for path in (lla.PATH_CUDA_CORE, lla.PATH_TENSOR_CORE):
-            lla.lla_set_moments_path(path)
-            outs[path] = run(lla, q, k, v, 8.0, 0.01)
-    finally:
-        lla.lla_set_moments_path(lla.PATH_AUTO)
+    outs = {path: run(lla, q, k, v, 8.0, 0.01, path=path)
+            for path in (lla.PATH_CUDA_CORE, lla.PATH_TENSOR_CORE)}
     ref = lla_forward_oracle(q, k, v, 8.0, 0.01).reshape(outs[1].shape)
     for path, o in outs.items():
         assert rel_err(o, ref) <= 2e-2, (path, rel_err(o, ref))
@@ -214,6 +204,7 @@ def test_profiling_and_launch_count(lla):
     lla.profile_enable(False)
     stages, calls = lla.profile_collect()
     assert calls == 3 and all(t >= 0 for t in stages.values())
-    assert all(stages[s] > 0 for s in ("moments", "solve", "readout"))
-    # bf16, d = dv = 64: moments, solve and readout; this path needs no reference points (prep)
-    assert lla.launch_count() - n0 == 3 * 3
+    assert all(stages[s] > 0 for s in ("prep", "weights", "moments", "solve", "readout"))
+    # bf16, d = dv = 64: the key frame (statistics, shifted keys), the weights, the moment
+    # contraction, the solve and its repair pass (empty here), the readout
+    assert lla.launch_count() - n0 == 3 * 7

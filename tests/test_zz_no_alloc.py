@@ -4,7 +4,9 @@ Such callers (a plugin that its host application only hands input and output buf
 latency-critical loop that must not call the allocator while it runs) get an entry point whose
 scratch is a fixed array owned by the library. These tests check it through the C ABI against
 lla_forward on two calls in a row (the second with different inputs, so nothing carried over in
-the shared scratch can pass unnoticed), and that an oversized problem is refused up front.
+the shared scratch can pass unnoticed), and that an oversized problem is refused up front. Both
+entry points run the same stages in the same order on the same inputs, so their outputs must be
+bitwise equal (the parity bound against the oracle is checked as well).
 This file is collected last on purpose.
 """
 import ctypes
@@ -41,7 +43,18 @@ def test_noalloc_matches_forward_on_consecutive_calls(lla, dtype, shape):
         lla.lla_forward_noalloc(q, k, v, 8.0, 0.01, out)
         assert lla.lla_stream_status() == 0
         assert torch.isfinite(out).all()
+        assert torch.equal(out, ref)
         assert rel_err(out, ref) <= TOL[dtype]
+
+
+@pytest.mark.gpu
+def test_noalloc_checks_out(lla):
+    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 16, 16, "f32", seed=23))
+    for bad in (torch.empty(1, 1, 64, 8, device="cuda"),                      # wrong shape
+                torch.empty(1, 1, 64, 16, device="cuda", dtype=torch.bfloat16),  # wrong dtype
+                torch.empty(1, 1, 16, 64, device="cuda").transpose(2, 3)):     # not contiguous
+        with pytest.raises(ValueError):
+            lla.lla_forward_noalloc(q, k, v, 4.0, 0.01, bad)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lla):
