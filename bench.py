@@ -964,7 +964,7 @@ def main(argv=None):
                 "units_per_launch": pairs,
                 "executed_tflops": pairs * tc_executed_flops_per_pair(w.d) / (con_ms / 1e3) / 1e12,
                 "moments_stage": {
-                    "what": "weight sweeps (lla_moments_tc.cu) + contraction, the logit counted "
+                    "what": "weight sweeps (lla_weights_tc.cu) + contraction, the logit counted "
                             "once: 2d + 2(1 + d + d(d+1)/2) flop per pair",
                     "ms": stage_ms_total, "weights_ms": w_ms,
                     "tflops": pairs * moments_flops_per_pair(w.d) / (stage_ms_total / 1e3) / 1e12,

@@ -89,11 +89,9 @@ void carve_workspace(const Args& a, void* base, Workspace* ws);
 // Kernel launchers (one per stage). Each returns the launch error, if any.
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);
-cudaError_t launch_moments_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 // The moment contraction of the tensor-core path (lla_moments_pass_tc.cu): reads the weight
 // images that launch_weights_tc wrote and fills the moment rows.
 cudaError_t launch_moments_pass_tc(const Args& a, const Workspace& ws, cudaStream_t s);
-size_t moments_tc_row_floats();
 size_t moments_tc_pscratch_bytes(long long BH, int T);
 
 // Layout of the tensor-core path's weight scratch: the bf16 kernel weights P of every (head,
@@ -139,7 +137,7 @@ cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s
 cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,
                                   const void* v, const uint32_t* ytc, const float* cy, float* out,
                                   const int* tile_active, bool matvec);
-// The moments stage reduced to its two sweeps: m, omega and the weight images only.
+// The weight sweeps of the tensor-core path (lla_weights_tc.cu): m, omega and the weight images.
 cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s);
 // Conjugate-gradient strategy for the ridge systems (bf16, d = dv = 64): fills ytc and cy like
 // the tensor-core solve, with its state in the moments region of the workspace.

@@ -167,19 +167,6 @@ __device__ __forceinline__ void generate(int pass, int rank, int fw, const uint3
 }
 static_assert(NPASS == 5, "generate() dispatches five passes");
 
-// Wait executed by all 32 lanes of a warp, with a warp-uniform outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, kStatusTimeout, abort));
-}
-
-// Arrival of one of this CTA's producers on a barrier of the leader (what the leader consumes is
-// complete before the arrival, so a relaxed remote arrive suffices).
-__device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader) {
-  if (leader) mbar_arrive(bar);
-  else mbar_arrive_cluster_relaxed(bar, 0);
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 moments_pass_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap pmap,
@@ -332,7 +319,7 @@ moments_pass_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int swz = key & 7;                                   // its 128-byte swizzle
     for (int r = 0; r < R; ++r) {
       const int k = r % NKS, u = r % NRS;
-      if (!warp_wait(&bar.kfull[k], (r / NKS) & 1, status, abort_p)) break;
+      if (!warp_wait(&bar.kfull[k], (r / NKS) & 1, status, TO, abort_p)) break;
       const uint8_t* kst = smem + SM_K + k * K_BYTES + key * 128;
       uint32_t kw[33];
 #pragma unroll
@@ -344,7 +331,7 @@ moments_pass_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.kempty[k]);
       // the round slot's previous features (round r - NRS) have been consumed
-      if (r >= NRS && !warp_wait(&bar.empty[u], ((r / NRS) - 1) & 1, status, abort_p)) break;
+      if (r >= NRS && !warp_wait(&bar.empty[u], ((r / NRS) - 1) & 1, status, TO, abort_p)) break;
       uint8_t* fhi = smem + SM_R + u * SLOT + 2 * P_BYTES + g * F_STEP;
       generate(r / nr, rank, fw, kw, fhi, fhi + F_HALF, row_off);
       fence_proxy_async_smem();  // the generic-proxy stores, before the MMA's async-proxy reads
@@ -363,7 +350,7 @@ moments_pass_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int swz = lane & 7;
     constexpr int C0 = NCH / 2;  // columns per half
     for (int pass = 0; pass < NPASS; ++pass) {
-      if (!warp_wait(&bar.accfull, pass & 1, status, abort_p)) break;
+      if (!warp_wait(&bar.accfull, pass & 1, status, TO, abort_p)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int c = half * C0; c < half * C0 + C0; c += 32) {

@@ -375,6 +375,30 @@ __device__ __forceinline__ bool mbar_wait2_cluster(uint64_t* a, uint32_t pa, uin
   return (ra || mbar_wait_cluster(a, pa, status, bit, abort)) &&
          (rb || mbar_wait_cluster(b, pb, status, bit, abort));
 }
+// Wait executed by all 32 lanes of a warp; the outcome is made warp-uniform so that an abort seen
+// by one lane takes the whole warp out of its loop together. `bit` is the timeout status bit.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int bit,
+                                          volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, bit, abort));
+}
+// Arrival of one of a CTA pair's producers on a barrier of the leader (the even CTA, which issues
+// the pair's MMAs). Every producer has completed what the leader consumes before it arrives (see
+// mbar_arrive_cluster_relaxed), so the peer's arrival needs no cluster-wide release; the leader's
+// own producers arrive locally.
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, bool leader) {
+  if (leader) mbar_arrive(bar);
+  else mbar_arrive_cluster_relaxed(bar, 0);
+}
+// Warp-wide: thread t of the warp reads 8 consecutive 32-bit columns of TMEM lane
+// (lane field of taddr) + t.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr));
+}
+
 // Pair allocation: one warp of each CTA executes these; each CTA gets the same columns.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -1,0 +1,365 @@
+// Weight sweeps of the tensor-core moments stage of the causal LLA forward (bf16 inputs, d = 64;
+// tcgen05 + TMEM).
+//
+// For every query i and its causal prefix j <= i this kernel computes the kernel weights of the
+// closed form of LLA ("Parallax" blog, s.2 Canonical Formulation), max-shifted:
+//     p_ij = exp((q_i . k_j - m_i) / h),  m_i = max_{j <= i} q_i . k_j,
+// rounded to bf16 and stored as tcgen05 operand images (the weight scratch, pscr:: in the internal
+// header), which the moment contraction and the readout read back; and per row m_i / h and
+// omega_i = sum_j p_ij (the sum of the rounded weights, so that every later stage describes one
+// weighted problem). Keys are the original bf16 keys: the weights do not depend on the key frame.
+//
+// Two sweeps over the key prefix: the first finds the exact row max, the second forms the weights.
+// Q K^T runs on chunks of four 32-key blocks (N = 128; a tcgen05.mma costs about as long at N = 32
+// as at N = 128) on CTA pairs (cluster of two, cta_group::2, M = 256): each CTA holds 128 query rows
+// (its tensor-memory lanes) and stages half of every key block (16 keys), and the even CTA (the
+// leader) issues the MMAs. The logits of a chunk land in one of three tensor-memory buffers, so
+// Q K^T runs ahead of the softmax warps.
+//
+// Warp roles per CTA (18 warps): 0 issues Q K^T (leader; one thread) and owns the tensor-memory
+// allocation, and in the peer relays its landed key blocks to the leader; 1 stages key blocks by
+// cp.async, each lane's copies completing on the stage's mbarrier (every stage in flight);
+// 2-17 are the softmax warps: four per tensor-memory lane quarter, each taking 8 keys of every
+// block (one thread per query row), so that a block's chain of tensor-memory load, exponentials,
+// packing and stores is short. Every mbarrier wait is bounded.
+#include <cstdint>
+
+#include "lla_internal.cuh"
+#include "lla_tc_ptx.cuh"
+
+namespace lla {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 64;
+constexpr int BM = 128;                     // query rows per CTA = TMEM lanes
+constexpr int PM = 2 * BM;                  // query rows per CTA pair = MMA M
+constexpr int KB = 32;                      // keys per block
+constexpr int SCH = 4;                      // key blocks per sweep chunk (one Q K^T of N = 128)
+constexpr int KS = 12;                      // key-tile pipeline stages (three sweep chunks)
+constexpr int NSM = 16;                     // softmax warps: four per TMEM lane quarter
+constexpr int NPART = NSM / 4;              // parts of a block's keys (8 keys each)
+constexpr int NWARPS = 2 + NSM;             // + Q K^T issuer, key loader
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int NSC = 3;                      // S buffers (SCH blocks each)
+static_assert(BM == pscr::kRows && KB == pscr::kKeys && PM == 2 * BM, "weight scratch layout");
+static_assert(KB == 8 * NPART, "a part is one 16-byte chunk of a block's image row");
+
+// tensor-memory columns (the same in both CTAs of a pair)
+constexpr uint32_t T_S = 0;                       // NSC x 128 columns of fp32 logits
+constexpr uint32_t T_Q = NSC * SCH * KB;          // 32 columns: the Q tile, A operand of Q K^T
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
+
+// shared-memory layout (bytes; the same offsets in both CTAs of a pair)
+constexpr int SM_K = 0;                              // KS x (32 x 64 bf16)
+constexpr int K_STAGE = KB * D * 2;
+constexpr int SM_BAR = SM_K + KS * K_STAGE;
+constexpr int SMEM_BYTES = SM_BAR + 8192;
+// More than half of an SM's shared memory, so that at most one CTA (and one TMEM allocation of
+// all 512 columns) is resident per SM.
+constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
+constexpr int P_BLOCK = BM * KB * 2;  // one 8 KiB image
+
+// Byte offset, from the first key stage, of 16-byte chunk c (elements 8c..8c+7) of row r of key
+// stage st. Each stage is a K-major tile of 32 rows x 64 elements in 8-row groups of eight
+// 128-byte core matrices (chunks 128 bytes apart). The stages form chunks of SCH = 4 consecutive
+// stages (16 KiB), and within a chunk the row groups are ordered (rows 0..15 of stages 0..3, then
+// rows 16..31 of stages 0..3): the 16 rows that a CTA contributes to Q K^T from each of the 4
+// stages are then 8 row groups 1024 bytes apart, one N = 128 operand for the pair.
+__device__ __forceinline__ int kst_off(int st, int r, int c) {
+  return (st >> 2) * (SCH * K_STAGE) + (r >> 4) * (SCH * K_STAGE / 2) +
+         (2 * (st & 3) + ((r >> 3) & 1)) * 1024 + c * 128 + (r & 7) * 16;
+}
+static_assert(KS % SCH == 0 && SCH == 4 && K_STAGE == 4096, "key stage layout");
+
+// Barriers marked (L) are used in the leader CTA only and collect arrivals from both CTAs; those
+// marked (M) are arrived on by multicast commits from the leader's Q K^T issuer in both CTAs.
+struct Barriers {
+  uint64_t kfull[KS];       // key block staged by this CTA's loader
+  uint64_t kfull_peer[KS];  // (L) key block staged by the peer's loader
+  uint64_t kempty[KS];      // (M) key stage consumed by Q K^T
+  uint64_t sfull[NSC];      // (M) S = Q K^T of a sweep chunk in tensor memory
+  uint64_t sfree[NSC];      // (L) S read by both CTAs' softmax warps
+  uint64_t qready;          // (L) both CTAs' Q tiles in tensor memory
+  uint64_t done_qk;         // (M) every MMA of the Q K^T issuer completed
+  uint64_t rowx;            // this CTA's softmax parts exchanged row max / omega
+  uint32_t tmem_base;
+  int abort_flag;
+  float part_m[NPART][BM];  // per-row partial maxima of the parts
+  float part_o[NPART][BM];  // per-row partial weight sums of the parts (a separate array: a fast
+                            // warp may finish the weight sweep before a slow one has read the maxima)
+};
+static_assert(sizeof(Barriers) <= 8192, "barrier region");
+
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
+                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ omega_out,
+                  uint4* __restrict__ pimg, int fault, int* __restrict__ status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)cluster_ctarank();
+  const bool leader = rank == 0;
+  const int npairs = (T + PM - 1) / PM;
+  const int pair_lin = (int)(blockIdx.x >> 1);
+  const int ptile = npairs - 1 - pair_lin / BH;  // longest causal prefixes first
+  const long long bh = pair_lin % BH;
+  const int i0p = ptile * PM;
+  const int i0 = i0p + rank * BM;                // this CTA's first query row
+  const int nq = max(0, min(BM, T - i0));
+  const int jend = min(T, i0p + PM);             // both CTAs stream the pair's key prefix
+  const int nb = pscr::pair_blocks(T, ptile);    // even: a last block past jend has zero weights
+  const int nb4 = (nb + SCH - 1) / SCH * SCH;    // each sweep padded with zero blocks to chunks
+  const int G = 2 * nb4;                         // key blocks streamed: max sweep, weight sweep
+  const long long base = bh * T;
+  uint4* const ptile_p = pimg + pscr::first_block(bh, T, ptile, rank) * (P_BLOCK / 16);
+  // Rows of this CTA's key stage: the Q K^T operand takes rows 0..15 of each CTA's stage as its
+  // N/2 keys, so CTA 1 keeps keys 16..31 of a block in rows 0..15 (row = key ^ 16 * rank).
+  const int krot = 16 * rank;
+
+  if (tid == 0) {
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar.kfull[s], 32);  // one cp.async completion arrival per loader lane
+      mbar_init(&bar.kfull_peer[s], 1);
+      mbar_init(&bar.kempty[s], 1);
+    }
+    for (int s = 0; s < NSC; ++s) {
+      mbar_init(&bar.sfull[s], 1);
+      mbar_init(&bar.sfree[s], 2 * NSM);
+    }
+    mbar_init(&bar.qready, 2 * 4);
+    mbar_init(&bar.done_qk, 1);
+    mbar_init(&bar.rowx, NSM);
+    bar.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair(&bar.tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers initialised before any cross-CTA arrival
+  tc_fence_after();
+  const uint32_t tbase = bar.tmem_base;
+  volatile int* abort_p = &bar.abort_flag;
+  const int TO = kStatusTimeout;
+
+  if (warp == 0) {
+    if (leader && lane == 0) {
+      // ---------------------------------------------------------------- Q K^T issuer (leader)
+      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
+      constexpr uint32_t id_qk = idesc_bf16(PM, SCH * KB, false, false);
+      const uint32_t t_s = tbase + T_S, t_q = tbase + T_Q;
+      bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);
+      const int nchunks = G / SCH;
+      for (int u = 0; u < nchunks && ok; ++u) {
+        // chunk u: key blocks g = SCH u .. SCH u + 3 in stages st0 .. st0 + 3 (fill g / KS)
+        const int sb = u % NSC, st0 = (SCH * u) % KS;
+        const uint32_t kpar = (uint32_t)((SCH * u / KS) & 1);
+        for (int t = 0; t < SCH && ok; ++t)
+          ok = mbar_wait2(&bar.kfull[st0 + t], kpar, &bar.kfull_peer[st0 + t], kpar, status, TO,
+                          abort_p);
+        if (ok && u >= NSC)
+          ok = mbar_wait(&bar.sfree[sb], ((u / NSC) - 1) & 1, status, TO, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+        fence_proxy_async_smem();  // the stages' cp.async writes, before the async-proxy reads
+        // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
+        // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
+        const uint64_t kst = kd + (uint64_t)((st0 / SCH) * (SCH * K_STAGE >> 4));
+        const uint32_t ts = t_s + sb * (SCH * KB);
+        mma2_ts(ts, t_q, kst, id_qk, 0u);
+        mma2_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
+        mma2_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
+        mma2_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
+        mma2_commit_both(&bar.sfull[sb]);
+        for (int t = 0; t < SCH; ++t) mma2_commit_both(&bar.kempty[st0 + t]);
+      }
+      if (!ok) *abort_p = 1;
+      mma2_commit_both(&bar.done_qk);
+    } else if (!leader && lane == 0) {
+      // Relay (the peer CTA): the leader's Q K^T reads this CTA's half of every block, so each
+      // landed block is fenced for the async proxy and reported to the leader. A stage is refilled
+      // only after the Q K^T that needs this report, so no phase is skipped.
+      for (int g = 0; g < G; ++g) {
+        const int st = g % KS;
+        if (!mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p)) break;
+        fence_proxy_async_smem();
+        mbar_arrive_cluster_relaxed(&bar.kfull_peer[st], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ key-tile loader
+    // cp.async 16-byte copies, every stage in flight. Lane -> (row, chunk) mapping:
+    // rows (lane & 7) + 8 * (t & 3), chunks (lane >> 3) + 4 * (t >> 2): each 8-lane phase writes
+    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors. Each lane's
+    // copies of a block complete on the stage's barrier (cp.async.mbarrier.arrive), so the loader
+    // never waits for its own copies; the consumers that read through the async proxy (Q K^T)
+    // fence after their wait (cp.async writes belong to the generic proxy).
+    // With the test-only fault LLA_FAULT_WITHHOLD_KEYS the first key block is never staged: every
+    // wait that needs it runs out after the wait limit, so the timeout path can be tested.
+    const __nv_bfloat16* kb = k + base * D;
+    for (int g = 0; g < G; ++g) {
+      const int st = g % KS;
+      const int b = g % nb4;  // sweep blocks >= nb: zeros
+      if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, TO, abort_p)) break;
+      if (g == 0 && fault == LLA_FAULT_WITHHOLD_KEYS) continue;
+      uint8_t* dst = smem + SM_K;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
+        const int j = b * KB + (r ^ krot);
+        const bool in = j < jend;
+        cp_async16(dst + kst_off(st, r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
+      }
+      cp_async_mbar_arrive(&bar.kfull[st]);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
+  } else {
+    // ------------------------------------------------------------------ softmax warps
+    // Four warps per TMEM lane quarter: part p takes keys 8p .. 8p + 7 of each block (one 16-byte
+    // chunk of the block's image row). Row max and omega are combined across the parts through
+    // shared memory (barrier rowx: phase 0 after the max sweep, phase 1 at the end).
+    const int quarter = warp & 3, part = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int i = i0 + r;
+    const bool valid = r < nq;
+    const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
+    const float c2 = inv_h * 1.4426950408889634f;  // log2(e) / h
+    if (part == 0) {  // this row of Q into tensor memory (packed bf16 pairs, 32 columns)
+      const uint4* qr = reinterpret_cast<const uint4*>(q + (base + (valid ? i : 0)) * D);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+        if (valid) { v0 = qr[2 * c]; v1 = qr[2 * c + 1]; }
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        tmem_st8(lane_base + T_Q + 8 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_leader(&bar.qready, leader);
+    }
+    float m = -INFINITY, om = 0.f;
+    bool ok = true;
+    // Sweep chunk u covers key blocks b0 .. b0 + SCH - 1. Column n of its S buffer holds key
+    // 16 (n / 64) + n % 16 of block (n % 64) / 16 (the pair's B operand: 64 rows from each CTA),
+    // so this thread's 8 logits of block b0 + t are columns 64 (part / 2) + 16 t + 8 (part % 2).
+    const int col_part = 64 * (part >> 1) + 8 * (part & 1);
+    constexpr int kChunk = 2048 / 16;  // chunk stride of an image, in 16-byte units
+    for (int u = 0; u < G / SCH && ok; ++u) {
+      const int sb = u % NSC;
+      if (!warp_wait(&bar.sfull[sb], (u / NSC) & 1, status, TO, abort_p)) { ok = false; break; }
+      tc_fence_after();
+      const bool max_sweep = SCH * u < nb4;
+      const int b0 = (SCH * u) % nb4;
+      for (int t = 0; t < SCH && ok; ++t) {
+        uint32_t sv[8];
+        tmem_ld8(lane_base + T_S + sb * (SCH * KB) + col_part + t * 16, sv);
+        tmem_ld_wait();
+        if (t == SCH - 1) {  // the chunk's S is read: the buffer is free
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
+        }
+        const int b = b0 + t;
+        if (b >= nb) continue;  // padding block of the chunk
+        const int j0 = b * KB + 8 * part;
+        if (max_sweep) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+          if (b == nb - 1) {  // combine the parts' row maxima
+            bar.part_m[part][r] = m;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.rowx);
+            if (!warp_wait(&bar.rowx, 0, status, TO, abort_p)) { ok = false; break; }
+#pragma unroll
+            for (int p2 = 0; p2 < NPART; ++p2) m = fmaxf(m, bar.part_m[p2][r]);
+          }
+          continue;
+        }
+        const float mc = m * c2;
+        uint32_t pw[4];
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+          const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+          const float p1 =
+              (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+          pw[c / 2] = pack_bf16(p0, p1);
+          om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
+        }
+        // This row's 8 weights as chunk `part` of the block's image.
+        ptile_p[(long long)b * (P_BLOCK / 16) + part * kChunk + r] =
+            make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      }
+    }
+    if (ok) {  // combine the parts' omega
+      bar.part_o[part][r] = om;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.rowx);
+      if (warp_wait(&bar.rowx, 1, status, TO, abort_p) && part == 0 && valid) {
+        float s = 0.f;
+#pragma unroll
+        for (int p2 = 0; p2 < NPART; ++p2) s += bar.part_o[p2][r];
+        m_out[base + i] = m * inv_h;
+        omega_out[base + i] = s;
+      }
+    }
+  }
+
+  // Teardown: tensor memory is released only after every MMA of the pair has completed (bounded
+  // wait, whatever the abort flag says), and neither CTA exits before the other has made its last
+  // arrival on it.
+  if (warp == 0 && lane == 0) {
+    volatile int never = 0;
+    mbar_wait(&bar.done_qk, 0, status, TO, &never);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+size_t moments_tc_pscratch_bytes(long long BH, int T) {
+  return (size_t)BH * (size_t)pscr::blocks_per_head(T) * P_BLOCK;
+}
+
+cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  auto kern = weights_tc_kernel;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
+  if (err != cudaSuccess) return err;
+  const long long blocks = 2ll * ((a.T + PM - 1) / PM) * a.BH();
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
+      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, static_cast<uint4*>(ws.pscr), a.fault, ws.status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace lla
