@@ -304,11 +304,11 @@ MIN_TIMED_S = 2.0   # device time the timed region spans at least (clock samples
 PARITY_ROWS = 96    # sampled rows of the timed output checked against the oracle
 
 
-def timed_repeats(warm_step_ms: float, steps: int, world: int) -> int:
-    """Repetitions of the K-step timed loop so that the timed region lasts >= MIN_TIMED_S
+def timed_repeats(warm_step_ms: float, steps: int, world: int, min_s: float = MIN_TIMED_S) -> int:
+    """Repetitions of the K-step timed loop so that the timed region lasts >= min_s
     (each repetition times exactly K steps; the same count on every rank)."""
     est = max(warm_step_ms, 1e-3) * max(steps, 1)
-    reps = int(min(200, max(1, math.ceil(MIN_TIMED_S * 1e3 / est))))
+    reps = int(min(200, max(1, math.ceil(min_s * 1e3 / est))))
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -796,6 +796,9 @@ def main(argv=None):
                          "the exact-LLA two-branch epilogue (dense strategy, bf16 d = dv = 64)")
     ap.add_argument("--cg-iters", type=int, default=1024)
     ap.add_argument("--cg-tol", type=float, default=1e-3)
+    ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                    help="repeat the K-step timed loop until this much device time is timed "
+                         "(0: one repetition, e.g. for profiler launch lists)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--shape", default=None,
@@ -876,7 +879,7 @@ def main(argv=None):
     w1.record(stream)
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during warm-up")
-    reps = timed_repeats(w0.elapsed_time(w1), args.steps, world)
+    reps = timed_repeats(w0.elapsed_time(w1), args.steps, world, args.min_timed_s)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * reps)]

@@ -38,6 +38,7 @@ constexpr int PM = 2 * BM;                  // query rows per CTA pair = MMA M
 constexpr int KB = 32;                      // keys per block
 constexpr int SCH = 4;                      // key blocks per sweep chunk (one Q K^T of N = 128)
 constexpr int KS = 12;                      // key-tile pipeline stages (three sweep chunks)
+constexpr int KC = KS / 4;                  // chunk slots: the stages of a chunk fill and free together
 constexpr int NSM = 16;                     // softmax warps: four per TMEM lane quarter
 constexpr int NPART = NSM / 4;              // parts of a block's keys (8 keys each)
 constexpr int NWARPS = 2 + NSM;             // + Q K^T issuer, key loader
@@ -77,9 +78,9 @@ static_assert(KS % SCH == 0 && SCH == 4 && K_STAGE == 4096, "key stage layout");
 // Barriers marked (L) are used in the leader CTA only and collect arrivals from both CTAs; those
 // marked (M) are arrived on by multicast commits from the leader's Q K^T issuer in both CTAs.
 struct Barriers {
-  uint64_t kfull[KS];       // key block staged by this CTA's loader
-  uint64_t kfull_peer[KS];  // (L) key block staged by the peer's loader
-  uint64_t kempty[KS];      // (M) key stage consumed by Q K^T
+  uint64_t kfull[KC];       // the chunk's four key blocks staged by this CTA's loader
+  uint64_t kfull_peer[KC];  // (L) the same in the peer
+  uint64_t kempty[KC];      // (M) the chunk's stages consumed by Q K^T
   uint64_t sfull[NSC];      // (M) S = Q K^T of a sweep chunk in tensor memory
   uint64_t sfree[NSC];      // (L) S read by both CTAs' softmax warps
   uint64_t qready;          // (L) both CTAs' Q tiles in tensor memory
@@ -132,8 +133,8 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int krot = 16 * rank;
 
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(&bar.kfull[s], 32);  // one cp.async completion arrival per loader lane
+    for (int s = 0; s < KC; ++s) {
+      mbar_init(&bar.kfull[s], 4 * 32);  // one cp.async completion arrival per loader lane and block
       mbar_init(&bar.kfull_peer[s], 1);
       mbar_init(&bar.kempty[s], 1);
     }
@@ -169,12 +170,10 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);
       const int nchunks = G / SCH;
       for (int u = 0; u < nchunks && ok; ++u) {
-        // chunk u: key blocks g = SCH u .. SCH u + 3 in stages st0 .. st0 + 3 (fill g / KS)
-        const int sb = u % NSC, st0 = (SCH * u) % KS;
-        const uint32_t kpar = (uint32_t)((SCH * u / KS) & 1);
-        for (int t = 0; t < SCH && ok; ++t)
-          ok = mbar_wait2(&bar.kfull[st0 + t], kpar, &bar.kfull_peer[st0 + t], kpar, status, TO,
-                          abort_p);
+        // chunk u: key blocks g = SCH u .. SCH u + 3 in chunk slot cs (stages 4 cs .. 4 cs + 3)
+        const int sb = u % NSC, cs = u % KC, st0 = SCH * cs;
+        const uint32_t kpar = (uint32_t)((u / KC) & 1);
+        ok = mbar_wait2(&bar.kfull[cs], kpar, &bar.kfull_peer[cs], kpar, status, TO, abort_p);
         if (ok && u >= NSC)
           ok = mbar_wait(&bar.sfree[sb], ((u / NSC) - 1) & 1, status, TO, abort_p);
         if (!ok) break;
@@ -189,19 +188,19 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         mma2_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
         mma2_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
         mma2_commit_both(&bar.sfull[sb]);
-        for (int t = 0; t < SCH; ++t) mma2_commit_both(&bar.kempty[st0 + t]);
+        mma2_commit_both(&bar.kempty[cs]);
       }
       if (!ok) *abort_p = 1;
       mma2_commit_both(&bar.done_qk);
     } else if (!leader && lane == 0) {
       // Relay (the peer CTA): the leader's Q K^T reads this CTA's half of every block, so each
-      // landed block is fenced for the async proxy and reported to the leader. A stage is refilled
-      // only after the Q K^T that needs this report, so no phase is skipped.
-      for (int g = 0; g < G; ++g) {
-        const int st = g % KS;
-        if (!mbar_wait(&bar.kfull[st], (g / KS) & 1, status, TO, abort_p)) break;
+      // landed chunk is fenced for the async proxy and reported to the leader. A chunk slot is
+      // refilled only after the Q K^T that needs this report, so no phase is skipped.
+      for (int u = 0; u < G / SCH; ++u) {
+        const int cs = u % KC;
+        if (!mbar_wait(&bar.kfull[cs], (u / KC) & 1, status, TO, abort_p)) break;
         fence_proxy_async_smem();
-        mbar_arrive_cluster_relaxed(&bar.kfull_peer[st], 0);
+        mbar_arrive_cluster_relaxed(&bar.kfull_peer[cs], 0);
       }
     }
     __syncwarp();
@@ -217,9 +216,11 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // wait that needs it runs out after the wait limit, so the timeout path can be tested.
     const __nv_bfloat16* kb = k + base * D;
     for (int g = 0; g < G; ++g) {
-      const int st = g % KS;
+      const int st = g % KS, u = g / SCH, cs = u % KC;
       const int b = g % nb4;  // sweep blocks >= nb: zeros
-      if (g >= KS && !warp_wait(&bar.kempty[st], ((g / KS) - 1) & 1, status, TO, abort_p)) break;
+      if (g % SCH == 0 && u >= KC &&
+          !warp_wait(&bar.kempty[cs], ((u / KC) - 1) & 1, status, TO, abort_p))
+        break;
       if (g == 0 && fault == LLA_FAULT_WITHHOLD_KEYS) continue;
       uint8_t* dst = smem + SM_K;
 #pragma unroll
@@ -229,7 +230,7 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const bool in = j < jend;
         cp_async16(dst + kst_off(st, r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
       }
-      cp_async_mbar_arrive(&bar.kfull[st]);
+      cp_async_mbar_arrive(&bar.kfull[cs]);
     }
     cp_async_commit();
     cp_async_wait<0>();  // nothing of this warp is in flight at teardown
@@ -271,22 +272,25 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       tc_fence_after();
       const bool max_sweep = SCH * u < nb4;
       const int b0 = (SCH * u) % nb4;
-      for (int t = 0; t < SCH && ok; ++t) {
-        uint32_t sv[8];
-        tmem_ld8(lane_base + T_S + sb * (SCH * KB) + col_part + t * 16, sv);
-        tmem_ld_wait();
-        if (t == SCH - 1) {  // the chunk's S is read: the buffer is free
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
-        }
+      // the chunk's logits of this thread, all four loads in flight before one wait; the buffer
+      // is free as soon as they have completed
+      uint32_t sv[SCH][8];
+#pragma unroll
+      for (int t = 0; t < SCH; ++t)
+        tmem_ld8(lane_base + T_S + sb * (SCH * KB) + col_part + t * 16, sv[t]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_leader(&bar.sfree[sb], leader);
+#pragma unroll
+      for (int t = 0; t < SCH; ++t) {
         const int b = b0 + t;
-        if (b >= nb) continue;  // padding block of the chunk
+        if (b >= nb) break;  // padding blocks of the chunk
         const int j0 = b * KB + 8 * part;
         if (max_sweep) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+            if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[t][c]));
           if (b == nb - 1) {  // combine the parts' row maxima
             bar.part_m[part][r] = m;
             __syncwarp();
@@ -301,9 +305,10 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         uint32_t pw[4];
 #pragma unroll
         for (int c = 0; c < 8; c += 2) {
-          const float p0 = (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+          const float p0 =
+              (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)) : 0.f;
           const float p1 =
-              (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+              (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc)) : 0.f;
           pw[c / 2] = pack_bf16(p0, p1);
           om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
         }
