@@ -470,7 +470,7 @@ def run_parallax(args, w, cpu, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v, probe "
+            "config": {"workload": f"{w.name}: {w.describe()}, {w.recipe()}, probe "
                                    f"N(0,1/d) seed {w.seed + 100}, h={h}, seed {w.seed}",
                        "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
                        "l2": "flushed between steps (256 MiB write outside the step events)",
@@ -612,7 +612,7 @@ def run_parallax_backward(args, w, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v and dO, probe "
+            "config": {"workload": f"{w.name}: {w.describe()}, {w.recipe()} and dO, probe "
                                    f"N(0,1/d) seed {w.seed + 100}, h={h}, seed {w.seed}",
                        "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
                        "l2": "flushed between steps (256 MiB write outside the step events)",
@@ -999,7 +999,7 @@ def main(argv=None):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if tensor_path else "f32",
             "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.describe()}, i.i.d. N(0,1) q/k/v, h={h}, "
+            "config": {"workload": f"{w.name}: {w.describe()}, {w.recipe()}, h={h}, "
                                    f"lambda={lam}, seed {w.seed}",
                        "B": w.B, "H": w.H, "T": w.T, "d": w.d, "dv": w.dv, "io_dtype": w.dtype,
                        "l2": "flushed between steps (256 MiB write outside the step events)",

@@ -58,6 +58,13 @@ class Workload:
     def describe(self) -> str:
         return f"B{self.B} H{self.H} T{self.T} d{self.d} dv{self.dv} {self.dtype}"
 
+    def recipe(self) -> str:
+        """How the inputs are drawn, in a few words."""
+        if self.kind == "stress":
+            return ("rank-8 keys + 1e-3 noise, half the queries outside the key cloud, "
+                    "v = A k + c + 0.01 N(0,1)")
+        return "i.i.d. N(0,1) q/k/v"
+
 
 WORKLOADS = {
     1: Workload("tiny", 1, 1, 128, 16, 16, "f32", 0, "iid", h=4.0, lam=1e-2),
