@@ -398,32 +398,38 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
 
 // ----------------------------------------------------------------------------- solve, tensor-core rows
 // d = 64 with the tensor-core stage's moment rows (2208 floats in the order tc_slot() decodes;
-// omega and the row max in their own arrays). Same factorisation as solve_kernel (lane l owns rows
-// l and 63 - l, column k broadcast through shared memory, forward substitution as an extra
-// column), arranged for throughput:
+// omega and the row max in their own arrays). One warp per query; lane l owns rows l and 63 - l
+// of the matrix (a balanced share of the triangle) and factors it column by column (right-looking
+// Cholesky, the right-hand side riding along as the forward substitution). Arranged so that the
+// warp issues few instructions per query:
 //  * the moment row goes from global memory straight into the registers that hold the matrix (for
 //    a fixed triangle row j the slots of (j, r), r > j, are consecutive, so each load of a warp is
-//    one contiguous run), instead of being staged in shared memory;
+//    one contiguous run). The loads and the assembly are unpredicated: a lane's entries past its
+//    row's diagonal are padding, computed and never read, and the odd diagonal entries (which sit
+//    outside the rows' runs) enter as a correction added to the pivot;
+//  * column k of the factor goes to shared memory once (column-major, rows padded to 68 floats),
+//    where the trailing update reads it as a broadcast and the backward substitution reads four
+//    columns of a row per vector load, conflict-free;
 //  * the trailing updates run as packed fp32 pairs (fma.rn.f32x2: the same single-rounded FMA on
 //    two lanes of a 64-bit register pair), which halves their instruction count;
-//  * the factor goes to shared memory as a packed triangle (row r at r(r+1)/2): a warp's stores of
-//    one column and its loads of one row are both free of bank conflicts (the triangular numbers
-//    0..31 are distinct mod 32), and it needs 8 KB per warp instead of 17, so that 16 warps fit
-//    on an SM.
+//  * the pivots' reciprocal square roots and the forward-substituted right-hand side are kept per
+//    column in shared memory (every lane stores the same value), the solution per row likewise,
+//    so that no lane has to pick out the values of its own rows with compare-and-select.
 namespace stc {
 constexpr int D = 64;
 constexpr int WARPS = 4;                 // warps (queries) per block
-constexpr int TRI = D * (D + 1) / 2;     // packed lower triangle of L
-constexpr int WARP_FLOATS = TRI + 2 * D + 2 * D;  // L, two column buffers, s = sum p k, mu
+constexpr int LDC = D + 4;               // column stride of the factor in shared memory
+constexpr int WARP_FLOATS = D * LDC + 2 * D + D;  // factor; (z', 1/L_kk) per column; y
+constexpr size_t SMEM_BYTES = sizeof(float) * WARPS * WARP_FLOATS;
 
-__host__ __device__ constexpr int tri(int r) { return r * (r + 1) / 2; }
 // Slot of (a, b) in a tensor-core moment row for b >= a + (a & 1) (the run of row a):
-// run_base(a) + b.
+// run_base(a) + b. For every a and 0 <= b < 64, run_base(a) + b stays inside the row.
 __host__ __device__ constexpr int run_base(int a) {
   const int t = a >> 1;
   const int rs = 65 * t - t * (t - 1) + ((a & 1) ? 33 - t : 0);
   return 2 * rs - (a + (a & 1));
 }
+static_assert(run_base(D - 1) + D - 1 < TC_ROW, "unpredicated loads stay inside the row");
 
 // x -= s * c on a packed pair (x0, x1) with c = (c0, c1); ns = -s. One packed fp32 FMA (the same
 // single-rounded FMA on both lanes of a 64-bit register pair).
@@ -455,61 +461,66 @@ __device__ __forceinline__ void trail(float (&a)[N], float ns, const float* cb) 
 }
 
 struct Lane {
-  float a0[32];   // row r0 = lane (entries 0..r0; the rest is padding, updated and never read)
-  float a1[64];   // row r1 = 63 - lane (entries 0..r1)
-  float z0, z1;   // right-hand sides, then the forward-substituted z'
-  float inv0, inv1;  // 1 / L[r][r]
+  float a0[32];   // row r0 = lane: entries 0..r0 (the rest is padding)
+  float a1[64];   // row r1 = 63 - lane: entries 0..r1
+  float dg0, dg1; // correction of the rows' diagonal entries, added to the pivot
+  float z0, z1;   // right-hand sides, updated by the forward substitution until used
   int r0, r1;
   bool ok;
 };
 
+// Column K: pivot from its owner, scale, store the column, update the trailing matrix and the
+// right-hand side. Entries of rows above K are padding throughout and harmless to update. `mine`
+// is this lane's candidate pivot (only the owner's is used). The owner of column K + 1 forms the
+// next pivot from its own registers (row K + 1's entries K and K + 1: the same fused operation
+// the trailing update applies to it), so the chain from pivot to pivot does not wait for the
+// column's broadcast through shared memory.
 template <int K>
-__device__ __forceinline__ void column(Lane& L, float* cbuf, float* Lt) {
+__device__ __forceinline__ void column(Lane& L, float* Lc, float2* zi, float mine) {
   constexpr bool lo = K < 32;
   constexpr int owner = lo ? K : D - 1 - K;
-  float piv = __shfl_sync(0xffffffffu, lo ? L.a0[lo ? K : 0] : L.a1[K], owner);
-  if (!(piv > 0.f)) { L.ok = false; piv = 1.f; }  // rows of a failed factorisation become NaN
+  const float piv = __shfl_sync(0xffffffffu, mine, owner);
+  L.ok = L.ok && piv > 0.f;  // false for NaN too; a failed row is solved again by the repair pass
   const float inv = rsqrtf(piv);
   const float zk = __shfl_sync(0xffffffffu, lo ? L.z0 : L.z1, owner) * inv;
-  float* cb = cbuf + (K & 1) * D;
-  // Column K of the factor is final: into the column buffer (for the trailing update) and, for
-  // rows at or below the diagonal, into the packed triangle (for the backward substitution), so
-  // that its registers are free from here on.
+  zi[K] = make_float2(zk, inv);  // every lane stores the same value
+  float* cb = Lc + K * LDC;
   if constexpr (lo) {
-    L.a0[K] *= inv;  // the owner's entry becomes piv * inv = L[K][K]
-    if (L.r0 == K) { L.inv0 = inv; L.z0 = zk; }
+    L.a0[K] *= inv;
     cb[L.r0] = L.a0[K];
-    if (L.r0 >= K) Lt[tri(L.r0) + K] = L.a0[K];
   }
   L.a1[K] *= inv;
-  if (L.r1 == K) { L.inv1 = inv; L.z1 = zk; }
   cb[L.r1] = L.a1[K];
-  if (L.r1 >= K) Lt[tri(L.r1) + K] = L.a1[K];
+  float next = 0.f;
+  if constexpr (K + 1 < 32) next = fmaf(-L.a0[K], L.a0[K], L.a0[K + 1]) + L.dg0;
+  else if constexpr (K + 1 < D) next = fmaf(-L.a1[K], L.a1[K], L.a1[K + 1]) + L.dg1;
   __syncwarp();
   if constexpr (lo) {
     trail<32, K>(L.a0, -L.a0[K], cb);
-    if (L.r0 > K) L.z0 = fmaf(-L.a0[K], zk, L.z0);
+    L.z0 = fmaf(-L.a0[K], zk, L.z0);
   }
   trail<64, K>(L.a1, -L.a1[K], cb);
-  if (L.r1 > K) L.z1 = fmaf(-L.a1[K], zk, L.z1);
-  if constexpr (K + 1 < D) column<K + 1>(L, cbuf, Lt);
+  L.z1 = fmaf(-L.a1[K], zk, L.z1);
+  if constexpr (K + 1 < D) column<K + 1>(L, Lc, zi, next);
 }
 
-// Backward substitution L^T y = z' from the last row: y_K = w_K / L[K][K], then
-// w_r -= L[K][r] y_K for r < K, with row K of L read from the packed triangle. A runtime loop:
-// unrolled, the compiler would hoist the triangle loads of many rows at once and spill.
-__device__ __forceinline__ void back(const Lane& L, const float* Lt, float& w0, float& w1,
-                                     float& y0, float& y1) {
-#pragma unroll 2
-  for (int K = D - 1; K >= 0; --K) {
-    const bool lo = K < 32;
+// Backward substitution L^T y = z' over the rows K = KB + 3 .. KB, KB a multiple of 4:
+// y_K = w_K / L_KK from the row's owner, then w_r -= L[K][r] y_K for every row r (rows at or
+// below K are done and absorb the update harmlessly). lane_row is r0 (K < 32) or r1; the four
+// factor entries L[KB..KB+3][r] of each own row come from one vector load of column r.
+__device__ __forceinline__ void back_block(int KB, bool lo, const float* Lc, int r0, int r1,
+                                           float i0, float i1, float& w0, float& w1, float* ys) {
+  const float4 c0 = *reinterpret_cast<const float4*>(Lc + r0 * LDC + KB);
+  const float4 c1 = *reinterpret_cast<const float4*>(Lc + r1 * LDC + KB);
+  const float e0[4] = {c0.x, c0.y, c0.z, c0.w}, e1[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int t = 3; t >= 0; --t) {
+    const int K = KB + t;
     const int owner = lo ? K : D - 1 - K;
-    const float yk = __shfl_sync(0xffffffffu, lo ? w0 * L.inv0 : w1 * L.inv1, owner);
-    const float* rowK = Lt + tri(K);
-    if (L.r0 == K) y0 = yk;
-    if (L.r1 == K) y1 = yk;
-    if (L.r0 < K) w0 = fmaf(-rowK[L.r0], yk, w0);
-    if (L.r1 < K) w1 = fmaf(-rowK[L.r1], yk, w1);
+    const float yk = __shfl_sync(0xffffffffu, lo ? w0 * i0 : w1 * i1, owner);
+    ys[K] = yk;  // every lane stores the same value
+    w0 = fmaf(-e0[t], yk, w0);
+    w1 = fmaf(-e1[t], yk, w1);
   }
 }
 }  // namespace stc
@@ -539,13 +550,15 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
                 float* __restrict__ cy_out, float* __restrict__ y_out, float* __restrict__ kbar_out,
                 int* __restrict__ rep, int* __restrict__ status) {
   using namespace stc;
-  __shared__ __align__(16) float sh[WARPS][WARP_FLOATS];
+  extern __shared__ float4 smem4[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * WARPS + warp;
   if (row >= rows) return;  // whole warp leaves together
-  float* Lt = sh[warp];
-  float* cbuf = Lt + TRI;
-  float* sv = cbuf + 2 * D;
+  float* Lc = reinterpret_cast<float*>(smem4) + warp * WARP_FLOATS;
+  float2* zi = reinterpret_cast<float2*>(Lc + D * LDC);
+  float* ys = Lc + D * LDC + 2 * D;
+  // before the factorisation the (z', 1/L_kk) area holds s and (page form) mu
+  float* sv = reinterpret_cast<float*>(zi);
   float* muv = sv + D;
   const float* g = mom + row * TC_ROW;
 
@@ -553,22 +566,26 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
   L.r0 = lane;
   L.r1 = D - 1 - lane;
   L.ok = true;
-  L.inv0 = L.inv1 = 1.f;
-  // Every load of the row first (predicated, all in flight together), then the arithmetic.
+  // Every load of the row first (all in flight together), then the arithmetic.
 #pragma unroll
-  for (int j = 0; j < 32; ++j) L.a0[j] = j <= L.r0 ? __ldcs(g + run_base(j) + L.r0) : 0.f;
+  for (int j = 0; j < 32; ++j) L.a0[j] = __ldcs(g + run_base(j) + L.r0);
 #pragma unroll
-  for (int j = 0; j < D; ++j) L.a1[j] = j <= L.r1 ? __ldcs(g + run_base(j) + L.r1) : 0.f;
+  for (int j = 0; j < D; ++j) L.a1[j] = __ldcs(g + run_base(j) + L.r1);
+  // the true diagonal entries and what the run loads put in their place
   const float d0 = __ldcs(g + tc_slot(L.r0, L.r0)), d1 = __ldcs(g + tc_slot(L.r1, L.r1));
+  const float x0 = __ldcs(g + run_base(L.r0) + L.r0), x1 = __ldcs(g + run_base(L.r1) + L.r1);
   const float s0 = __ldcs(g + run_base(L.r0) + D), s1 = __ldcs(g + run_base(L.r1) + D);
   const float om = omega[row];
   // the query in the head's key frame (the moments are those of kt = bf16(k - c))
   const int bh = (int)row / T;  // rows < 2^31
   const float qa = ldf(q, row * D + L.r0) - kref[bh * D + L.r0];
   const float qb = ldf(q, row * D + L.r1) - kref[bh * D + L.r1];
-  double lpd = (double)lam * exp(-(double)mrow[row]);  // ridge scaled by exp(-m)
-  lpd = fmin(fmax(lpd, (double)FLT_MIN), (double)FLT_MAX);
-  const float lp = (float)lpd;
+  // the ridge scaled by exp(-m), formed in the exponent so that no intermediate overflows
+  const float lp = fminf(fmaxf(expf(logf(lam) - mrow[row]), FLT_MIN), FLT_MAX);
+  // x is d for even rows and the zero padding slot before the run for odd rows, so the correction
+  // is exactly lambda' or d + lambda'; the ridge enters after the trailing updates' cancellation.
+  L.dg0 = (d0 - x0) + lp;
+  L.dg1 = (d1 - x1) + lp;
   sv[L.r0] = s0;
   sv[L.r1] = s1;
   const float mu0 = fmaf(-om, qa, s0), mu1 = fmaf(-om, qb, s1);  // page form: mu = s - omega q
@@ -582,25 +599,8 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
   const float mo0 = mu0 * inv_om, mo1 = mu1 * inv_om;
   L.z0 = PAGE ? mu0 : qa - kb0;
   L.z1 = PAGE ? mu1 : qb - kb1;
-  // C_kk + lambda' I = S - s s^T / omega + lambda' I (page form: + mu mu^T / omega), row by row
-  // (the odd diagonal entries sit outside the rows' runs).
-#pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
-    const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
-    float mj[4] = {0.f, 0.f, 0.f, 0.f};
-    if (PAGE) {
-      const float4 m4 = *reinterpret_cast<const float4*>(muv + j);
-      mj[0] = m4.x; mj[1] = m4.y; mj[2] = m4.z; mj[3] = m4.w;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float v = L.r0 == j + u ? d0 + lp : L.a0[j + u];
-      v = fmaf(-sj[u], kb0, v);
-      if (PAGE) v = fmaf(mj[u], mo0, v);
-      L.a0[j + u] = j + u <= L.r0 ? v : 0.f;
-    }
-  }
+  // C_kk = S - s s^T / omega (page form: + mu mu^T / omega); lambda' and the odd diagonal
+  // entries come in through dg0 and dg1.
 #pragma unroll
   for (int j = 0; j < D; j += 4) {
     const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
@@ -612,16 +612,21 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      float v = L.r1 == j + u ? d1 + lp : L.a1[j + u];
-      v = fmaf(-sj[u], kb1, v);
+      if (j + u < 32) {
+        float v = fmaf(-sj[u], kb0, L.a0[(j + u) & 31]);
+        if (PAGE) v = fmaf(mj[u], mo0, v);
+        L.a0[(j + u) & 31] = v;
+      }
+      float v = fmaf(-sj[u], kb1, L.a1[j + u]);
       if (PAGE) v = fmaf(mj[u], mo1, v);
-      L.a1[j + u] = j + u <= L.r1 ? v : 0.f;
+      L.a1[j + u] = v;
     }
   }
+  __syncwarp();  // s and mu are read; the area now takes (z', 1/L_kk)
 
-  stc::column<0>(L, cbuf, Lt);
+  stc::column<0>(L, Lc, zi, L.a0[0] + L.dg0);
   uint32_t* yrow = ytc + row * 3 * (D / 2);
-  if (!L.ok) {
+  if (!__all_sync(0xffffffffu, L.ok)) {
     // A non-positive pivot: fp32 rounding of the tensor-core sums can exceed the smallest
     // eigenvalues of a very ill-conditioned system. The row goes to the precise repair pass
     // (repair_kernel), which overwrites this row's y; if its list is full, the row is NaN.
@@ -647,14 +652,20 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
     return;
   }
   __syncwarp();
-  float w0 = L.z0, w1 = L.z1, y0 = 0.f, y1 = 0.f;
-  stc::back(L, Lt, w0, w1, y0, y1);
-  // Lane l writes elements 2l and 2l + 1 of each part (element e < 32 is row e of lane e,
-  // element e >= 32 row e of lane 63 - e), so that each part's row is one coalesced store.
-  const int e0 = 2 * lane, e1 = 2 * lane + 1;
-  const float a_lo = __shfl_sync(0xffffffffu, y0, e0 & 31), a_hi = __shfl_sync(0xffffffffu, y1, (D - 1 - e0) & 31);
-  const float b_lo = __shfl_sync(0xffffffffu, y0, e1 & 31), b_hi = __shfl_sync(0xffffffffu, y1, (D - 1 - e1) & 31);
-  const float ya = e0 < 32 ? a_lo : a_hi, yb = e1 < 32 ? b_lo : b_hi;
+  const float2 zr0 = zi[L.r0], zr1 = zi[L.r1];
+  float w0 = zr0.x, w1 = zr1.x;
+  // rows 63..32 are owned through r1, rows 31..0 through r0
+#pragma unroll 2
+  for (int KB = D - 4; KB >= 32; KB -= 4)
+    back_block(KB, false, Lc, L.r0, L.r1, zr0.y, zr1.y, w0, w1, ys);
+#pragma unroll 2
+  for (int KB = 28; KB >= 0; KB -= 4)
+    back_block(KB, true, Lc, L.r0, L.r1, zr0.y, zr1.y, w0, w1, ys);
+  __syncwarp();
+  // Lane l writes elements 2l and 2l + 1 of each part, so that each part's row is one
+  // coalesced store.
+  const float2 yab = *reinterpret_cast<const float2*>(ys + 2 * lane);
+  const float ya = yab.x, yb = yab.y;
   const uint32_t p1 = pack_bf16(ya, yb);
   const float ra = ya - __uint_as_float(p1 << 16), rb = yb - __uint_as_float(p1 & 0xFFFF0000u);
   const uint32_t p2 = pack_bf16(ra, rb);
@@ -663,6 +674,7 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
   yrow[lane] = p1;
   yrow[D / 2 + lane] = p2;
   yrow[D + lane] = p3;
+  const float y0 = ys[L.r0], y1 = ys[L.r1];
   float c = PAGE ? fmaf(qa, y0, qb * y1) : fmaf(kb0, y0, kb1 * y1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
@@ -886,12 +898,15 @@ cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) 
   const long long rows = a.rows();
   const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
   auto kern = ws.form == kFormPage ? solve_tc_kernel<true> : solve_tc_kernel<false>;
-  kern<<<(unsigned)blocks, stc::WARPS * 32, 0, s>>>(
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)stc::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  kern<<<(unsigned)blocks, stc::WARPS * 32, stc::SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), ws.kref, ws.mom, ws.omega, ws.m, rows, a.T, a.lam,
       ws.ytc, ws.cy,
       a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.rep, ws.status);
   count_launch();
-  cudaError_t err = cudaGetLastError();
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   auto rk = ws.form == kFormPage ? repair_kernel<true> : repair_kernel<false>;
   rk<<<kRepairGrid, rep::NT, 0, s>>>(
