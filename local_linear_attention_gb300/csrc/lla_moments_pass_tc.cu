@@ -48,14 +48,12 @@
 //
 // Output per query row: mom[row][slot] (fp32, slots in the feature order of lla_features.cuh; the
 // row stride is 2208 floats).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cstdint>
 
 #include "lla_features.cuh"
 #include "lla_internal.cuh"
 #include "lla_tc_ptx.cuh"
+#include "lla_tmap.cuh"
 
 namespace lla {
 namespace {
@@ -399,24 +397,10 @@ moments_pass_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 static_assert(NCH % 64 == 0, "drain blocks of 32 columns per half");
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
 }  // namespace
 
 cudaError_t launch_moments_pass_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
-  auto encode = encode_fn();
+  auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   const cuuint32_t ones[3] = {1, 1, 1};
   // keys in the head's frame (the prep stage's bf16(k - c)): [BH][T][64] bf16, boxes of 32 keys

@@ -147,6 +147,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
+// 5-D box into this CTA's shared memory; completion counted on this CTA's `bar`.
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, int c4, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_u32(bar))
+      : "memory");
+}
 // Prefetch of a 3-D box into L2 (no shared memory written, nothing to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
@@ -256,6 +266,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // version
   return d;                // layout type 0 (no swizzle), base offset 0
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzled layout that a
+// TMA tensor copy with CU_TENSOR_MAP_SWIZZLE_128B writes: 128-byte rows, 8-row atoms of 1024
+// bytes (1024-byte aligned), SBO = the distance between atoms; LBO is not used by this layout.
+// The k-th 16-element (32-byte) slice of K starts at the atom's address + 32 k.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;  // LBO: 16 bytes (unused)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // version
+  d |= (uint64_t)2 << 61;  // layout type: 128-byte swizzle
+  return d;
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 accumulator.

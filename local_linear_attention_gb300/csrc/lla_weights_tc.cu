@@ -18,7 +18,7 @@
 //
 // Warp roles per CTA (18 warps): 0 issues Q K^T (leader; one thread) and owns the tensor-memory
 // allocation, and in the peer relays its landed key blocks to the leader; 1 stages key blocks by
-// cp.async, each lane's copies completing on the stage's mbarrier (every stage in flight);
+// TMA tensor copies (one thread; 128-byte swizzled, the layout the Q K^T B operand reads);
 // 2-17 are the softmax warps: four per tensor-memory lane quarter, each taking 8 keys of every
 // block (one thread per query row), so that a block's chain of tensor-memory load, exponentials,
 // packing and stores is short. Every mbarrier wait is bounded.
@@ -26,6 +26,7 @@
 
 #include "lla_internal.cuh"
 #include "lla_tc_ptx.cuh"
+#include "lla_tmap.cuh"
 
 namespace lla {
 namespace {
@@ -37,7 +38,7 @@ constexpr int BM = 128;                     // query rows per CTA = TMEM lanes
 constexpr int PM = 2 * BM;                  // query rows per CTA pair = MMA M
 constexpr int KB = 32;                      // keys per block
 constexpr int SCH = 4;                      // key blocks per sweep chunk (one Q K^T of N = 128)
-constexpr int KS = 12;                      // key-tile pipeline stages (three sweep chunks)
+constexpr int KS = 32;                      // key-tile pipeline stages (eight sweep chunks)
 constexpr int KC = KS / 4;                  // chunk slots: the stages of a chunk fill and free together
 constexpr int NSM = 16;                     // softmax warps: four per TMEM lane quarter
 constexpr int NPART = NSM / 4;              // parts of a block's keys (8 keys each)
@@ -54,26 +55,22 @@ constexpr uint32_t TMEM_COLS = 512;
 static_assert(T_Q + D / 2 <= TMEM_COLS, "tensor memory budget");
 
 // shared-memory layout (bytes; the same offsets in both CTAs of a pair)
-constexpr int SM_K = 0;                              // KS x (32 x 64 bf16)
-constexpr int K_STAGE = KB * D * 2;
+constexpr int SM_K = 0;                              // KS x (16 x 64 bf16)
+constexpr int K_STAGE = KB / 2 * D * 2;              // the 16 keys of a block this CTA contributes
+constexpr int K_SLOT = SCH * K_STAGE;                // a chunk slot: 64 keys, 8 KiB
 constexpr int SM_BAR = SM_K + KS * K_STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 8192;
 // More than half of an SM's shared memory, so that at most one CTA (and one TMEM allocation of
 // all 512 columns) is resident per SM.
-constexpr int SMEM_LAUNCH = SMEM_BYTES > 120 * 1024 ? SMEM_BYTES : 120 * 1024;
+constexpr int SMEM_LAUNCH = SMEM_BYTES + 1024 > 120 * 1024 ? SMEM_BYTES + 1024 : 120 * 1024;
 constexpr int P_BLOCK = BM * KB * 2;  // one 8 KiB image
 
-// Byte offset, from the first key stage, of 16-byte chunk c (elements 8c..8c+7) of row r of key
-// stage st. Each stage is a K-major tile of 32 rows x 64 elements in 8-row groups of eight
-// 128-byte core matrices (chunks 128 bytes apart). The stages form chunks of SCH = 4 consecutive
-// stages (16 KiB), and within a chunk the row groups are ordered (rows 0..15 of stages 0..3, then
-// rows 16..31 of stages 0..3): the 16 rows that a CTA contributes to Q K^T from each of the 4
-// stages are then 8 row groups 1024 bytes apart, one N = 128 operand for the pair.
-__device__ __forceinline__ int kst_off(int st, int r, int c) {
-  return (st >> 2) * (SCH * K_STAGE) + (r >> 4) * (SCH * K_STAGE / 2) +
-         (2 * (st & 3) + ((r >> 3) & 1)) * 1024 + c * 128 + (r & 7) * 16;
-}
-static_assert(KS % SCH == 0 && SCH == 4 && K_STAGE == 4096, "key stage layout");
+// A key stage holds the 16 keys of a block that this CTA contributes to Q K^T: 16 rows of 128
+// bytes in the 128-byte swizzled layout of the TMA copy (two 1024-byte atoms of 8 rows). The
+// stages form chunk slots of SCH = 4 consecutive stages (8 KiB), so that a slot is one K-major
+// N = 128 operand for the pair (64 keys from each CTA, atoms 1024 bytes apart).
+static_assert(KS % SCH == 0 && SCH == 4 && K_STAGE == 2048 && K_SLOT == SCH * K_STAGE,
+              "key stage layout");
 
 // Barriers marked (L) are used in the leader CTA only and collect arrivals from both CTAs; those
 // marked (M) are arrived on by multicast commits from the leader's Q K^T issuer in both CTAs.
@@ -106,10 +103,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T,
-                  int BH, float inv_h, float* __restrict__ m_out, float* __restrict__ omega_out,
-                  uint4* __restrict__ pimg, int fault, int* __restrict__ status) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap kmap5, bool chunk_copies, int T, int BH, float inv_h, float* __restrict__ m_out,
+                  float* __restrict__ omega_out, uint4* __restrict__ pimg, int fault,
+                  int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  // the swizzled key stages need 1024-byte alignment
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -134,7 +134,7 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 
   if (tid == 0) {
     for (int s = 0; s < KC; ++s) {
-      mbar_init(&bar.kfull[s], 4 * 32);  // one cp.async completion arrival per loader lane and block
+      mbar_init(&bar.kfull[s], 1);  // the loader's arrival with the chunk's transaction bytes
       mbar_init(&bar.kfull_peer[s], 1);
       mbar_init(&bar.kempty[s], 1);
     }
@@ -164,7 +164,7 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (warp == 0) {
     if (leader && lane == 0) {
       // ---------------------------------------------------------------- Q K^T issuer (leader)
-      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
+      const uint64_t kd = smem_desc_sw128(smem_u32(smem + SM_K), 1024);
       constexpr uint32_t id_qk = idesc_bf16(PM, SCH * KB, false, false);
       const uint32_t t_s = tbase + T_S, t_q = tbase + T_Q;
       bool ok = mbar_wait(&bar.qready, 0, status, TO, abort_p);
@@ -181,12 +181,12 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         fence_proxy_async_smem();  // the stages' cp.async writes, before the async-proxy reads
         // Every descriptor is a base descriptor plus a start-address offset (16-byte units, which
         // cannot carry out of the 14-bit field since shared memory is below 256 KiB).
-        const uint64_t kst = kd + (uint64_t)((st0 / SCH) * (SCH * K_STAGE >> 4));
+        const uint64_t kst = kd + (uint64_t)((st0 / SCH) * (K_SLOT >> 4));
         const uint32_t ts = t_s + sb * (SCH * KB);
-        mma2_ts(ts, t_q, kst, id_qk, 0u);
-        mma2_ts(ts, t_q + 8, kst + 16, id_qk, 1u);
-        mma2_ts(ts, t_q + 16, kst + 32, id_qk, 1u);
-        mma2_ts(ts, t_q + 24, kst + 48, id_qk, 1u);
+        mma2_ts(ts, t_q, kst, id_qk, 0u);  // K-steps of 16 features: 32 bytes within the rows
+        mma2_ts(ts, t_q + 8, kst + 2, id_qk, 1u);
+        mma2_ts(ts, t_q + 16, kst + 4, id_qk, 1u);
+        mma2_ts(ts, t_q + 24, kst + 6, id_qk, 1u);
         mma2_commit_both(&bar.sfull[sb]);
         mma2_commit_both(&bar.kempty[cs]);
       }
@@ -206,34 +206,43 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ key-tile loader
-    // cp.async 16-byte copies, every stage in flight. Lane -> (row, chunk) mapping:
-    // rows (lane & 7) + 8 * (t & 3), chunks (lane >> 3) + 4 * (t >> 2): each 8-lane phase writes
-    // 8 distinct bank groups, and each warp request reads whole 32-byte sectors. Each lane's
-    // copies of a block complete on the stage's barrier (cp.async.mbarrier.arrive), so the loader
-    // never waits for its own copies; the consumers that read through the async proxy (Q K^T)
-    // fence after their wait (cp.async writes belong to the generic proxy).
-    // With the test-only fault LLA_FAULT_WITHHOLD_KEYS the first key block is never staged: every
-    // wait that needs it runs out after the wait limit, so the timeout path can be tested.
-    const __nv_bfloat16* kb = k + base * D;
-    for (int g = 0; g < G; ++g) {
-      const int st = g % KS, u = g / SCH, cs = u % KC;
-      const int b = g % nb4;  // sweep blocks >= nb: zeros
-      if (g % SCH == 0 && u >= KC &&
-          !warp_wait(&bar.kempty[cs], ((u / KC) - 1) & 1, status, TO, abort_p))
-        break;
-      if (g == 0 && fault == LLA_FAULT_WITHHOLD_KEYS) continue;
-      uint8_t* dst = smem + SM_K;
+    // One thread: per chunk one arrival with the chunk's transaction bytes, then the chunk's keys
+    // that this CTA contributes (16 of every block) by TMA: one copy of the whole chunk when T is
+    // a multiple of 32 (kmap5 views a head's keys as blocks x halves x 16 rows), else one copy per
+    // block. Rows past the head's end read as zeros; keys past the pair's causal end are real
+    // keys whose logits the softmax masks. The loader shares its scheduler with busy softmax
+    // warps and gets few issue slots, so its loop runs once per chunk with few instructions.
+    // With the test-only fault LLA_FAULT_WITHHOLD_KEYS the first key block (the first chunk, with
+    // chunk copies) is never copied: every wait that needs it runs out after the wait limit, so
+    // the timeout path can be tested.
+    if (lane == 0) {
+      tma_prefetch_map(chunk_copies ? &kmap5 : &kmap);
+      int issued = 0;  // chunks whose copies were started
+      for (int u = 0; u < G / SCH; ++u) {
+        const int cs = u % KC;
+        if (u >= KC && !mbar_wait(&bar.kempty[cs], ((u / KC) - 1) & 1, status, TO, abort_p)) break;
+        mbar_arrive_expect_tx(&bar.kfull[cs], K_SLOT);
+        issued = u + 1;
+        const int b0 = (SCH * u) % nb4;  // sweep blocks >= nb: never read
+        uint8_t* dst = smem + SM_K + cs * K_SLOT;
+        const bool withhold = u == 0 && fault == LLA_FAULT_WITHHOLD_KEYS;
+        if (chunk_copies) {  // blocks b0 .. b0 + 3, half `rank`
+          if (!withhold) tma_load_5d(dst, &kmap5, 0, 0, rank, b0, (int)bh, &bar.kfull[cs]);
+        } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int r = (lane & 7) + 8 * (t & 3), c = (lane >> 3) + 4 * (t >> 2);
-        const int j = b * KB + (r ^ krot);
-        const bool in = j < jend;
-        cp_async16(dst + kst_off(st, r, c), kb + (long long)(in ? j : 0) * D + c * 8, in ? 16u : 0u);
+          for (int t = 0; t < SCH; ++t)
+            if (!(withhold && t == 0))
+              tma_load_3d(dst + t * K_STAGE, &kmap, 0, (b0 + t) * KB + krot, (int)bh,
+                          &bar.kfull[cs]);
+        }
       }
-      cp_async_mbar_arrive(&bar.kfull[cs]);
+      // Nothing may land in this CTA's shared memory after it exits: wait (bounded) for the
+      // copies of the last chunks started; a normal run finds them complete.
+      volatile int never = 0;
+      for (int u = issued > KC ? issued - KC : 0; u < issued; ++u)
+        mbar_wait(&bar.kfull[u % KC], (u / KC) & 1, status, TO, &never);
     }
-    cp_async_commit();
-    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax warps
     // Four warps per TMEM lane quarter: part p takes keys 8p .. 8p + 7 of each block (one 16-byte
@@ -287,10 +296,18 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const int b = b0 + t;
         if (b >= nb) break;  // padding blocks of the chunk
         const int j0 = b * KB + 8 * part;
+        // keys j0 .. j0 + 7 all at or before this row: no causal mask (rows past the tile's end
+        // have zero queries and finite logits, and nothing of theirs is stored)
+        const bool full = j0 + 7 <= i;
         if (max_sweep) {
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[t][c]));
+            for (int c = 0; c < 8; ++c) m = fmaxf(m, __uint_as_float(sv[t][c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              if (valid && j0 + c <= i) m = fmaxf(m, __uint_as_float(sv[t][c]));
+          }
           if (b == nb - 1) {  // combine the parts' row maxima
             bar.part_m[part][r] = m;
             __syncwarp();
@@ -303,15 +320,25 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
         const float mc = m * c2;
         uint32_t pw[4];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) {
-          const float p0 =
-              (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)) : 0.f;
-          const float p1 =
-              (valid && j0 + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc)) : 0.f;
-          pw[c / 2] = pack_bf16(p0, p1);
-          om += __uint_as_float(pw[c / 2] << 16) + __uint_as_float(pw[c / 2] & 0xFFFF0000u);
+          for (int c = 0; c < 8; c += 2)
+            pw[c / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)),
+                                  ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc)));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; c += 2) {
+            const float p0 =
+                (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)) : 0.f;
+            const float p1 = (valid && j0 + c + 1 <= i)
+                                 ? ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc))
+                                 : 0.f;
+            pw[c / 2] = pack_bf16(p0, p1);
+          }
         }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          om += __uint_as_float(pw[c] << 16) + __uint_as_float(pw[c] & 0xFFFF0000u);
         // This row's 8 weights as chunk `part` of the block's image.
         ptile_p[(long long)b * (P_BLOCK / 16) + part * kChunk + r] =
             make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -354,6 +381,34 @@ size_t moments_tc_pscratch_bytes(long long BH, int T) {
 }
 
 cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  // the original keys: [BH][T][64] bf16, boxes of 16 keys x 64 features, 128-byte swizzled
+  CUtensorMap kmap;
+  const cuuint32_t ones[3] = {1, 1, 1};
+  const cuuint64_t kdims[3] = {(cuuint64_t)D, (cuuint64_t)a.T, (cuuint64_t)a.BH()};
+  const cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.T * D * 2};
+  const cuuint32_t kbox[3] = {(cuuint32_t)D, (cuuint32_t)(KB / 2), 1};
+  if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k), kdims, kstr, kbox,
+             ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // When T is a multiple of 32: a head's keys as [T / 32 blocks][2 halves][16 rows][64], so that
+  // one box {64, 16, 1, 4, 1} is a sweep chunk's 16-key halves of four blocks.
+  CUtensorMap kmap5 = kmap;
+  const bool chunk_copies = a.T % KB == 0;
+  if (chunk_copies) {
+    const cuuint32_t ones5[5] = {1, 1, 1, 1, 1};
+    const cuuint64_t dims5[5] = {(cuuint64_t)D, (cuuint64_t)(KB / 2), 2, (cuuint64_t)(a.T / KB),
+                                 (cuuint64_t)a.BH()};
+    const cuuint64_t str5[4] = {(cuuint64_t)D * 2, (cuuint64_t)(KB / 2) * D * 2,
+                                (cuuint64_t)KB * D * 2, (cuuint64_t)a.T * D * 2};
+    const cuuint32_t box5[5] = {(cuuint32_t)D, (cuuint32_t)(KB / 2), 1, (cuuint32_t)SCH, 1};
+    if (encode(&kmap5, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a.k), dims5, str5,
+               box5, ones5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   auto kern = weights_tc_kernel;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
@@ -361,8 +416,8 @@ cudaError_t launch_weights_tc(const Args& a, const Workspace& ws, cudaStream_t s
   const long long blocks = 2ll * ((a.T + PM - 1) / PM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k), a.T,
-      (int)a.BH(), 1.0f / a.h, ws.m, ws.omega, static_cast<uint4*>(ws.pscr), a.fault, ws.status);
+      static_cast<const __nv_bfloat16*>(a.q), kmap, kmap5, chunk_copies, a.T, (int)a.BH(),
+      1.0f / a.h, ws.m, ws.omega, static_cast<uint4*>(ws.pscr), a.fault, ws.status);
   count_launch();
   return cudaGetLastError();
 }
