@@ -68,7 +68,8 @@ def contraction_flops_per_pair(d: int) -> int:
 
 def tc_executed_flops_per_pair(d: int) -> int:
     """Tensor flops the tcgen05 moment contraction executes per causal pair: hi + lo over
-    5 passes x 448 feature columns (2208 slots and 32 of padding)."""
+    5 passes x 448 feature columns (2208 slots and 32 of padding); the same for d < 64, which
+    runs zero-padded to d = 64."""
     return 2 * 2 * 5 * 448
 
 
@@ -951,7 +952,8 @@ def main(argv=None):
                "d2h_bytes_per_step": out.numel() * eb}
 
     peaks, peak_src = load_peaks()
-    tensor_path = w.dtype == "bf16" and w.d == 64
+    # bf16 runs on the tensor cores (d < 64: on zero-padded d = dv = 64 copies of q, k, v)
+    tensor_path = w.dtype == "bf16"
     per_call = {k_: v_ / max(n_calls, 1) for k_, v_ in stage_ms.items()}
     pairs = causal_pairs(w)
     if tensor_path:
@@ -961,7 +963,8 @@ def main(argv=None):
         achieved = pairs * contraction_flops_per_pair(w.d) / (con_ms / 1e3) / 1e12
         peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
         stage_ms_total = con_ms + w_ms
-        roof = {"kernel": "moment contraction (lla_moments_pass_tc.cu: tcgen05 cta_group::2, TMA)",
+        roof = {"kernel": "moment contraction (lla_moments_pass_tc.cu: tcgen05 cta_group::2, TMA)"
+                          + (f"; d = {w.d} zero-padded to 64" if w.d < 64 else ""),
                 "bound": "tensor", "peak_source": f"bf16 dense, burst ({peak_src})",
                 "flops_per_unit": contraction_flops_per_pair(w.d), "unit_of_work": "causal pair",
                 "units_per_launch": pairs,

@@ -19,9 +19,11 @@
  * - Layout: q, k are [B, H, T, d] and v, out are [B, H, T, dv], contiguous, row-major
  *   (innermost index = feature). Element type is given by `dtype` (lla_dtype) and is the same
  *   for q, k, v and out. Sums are accumulated in fp32 (in compensated fp32 pairs for the fp32
- *   element type). For bf16 inputs with d = 64 the moments run on the tensor cores: the kernel
- *   weights enter the contraction rounded to bf16, the key products k_a*k_b exactly (as an exact
- *   pair of bf16 values).
+ *   element type). For bf16 inputs the forward runs on the tensor cores: the kernel weights enter
+ *   the contraction rounded to bf16, the key products k_a*k_b exactly (as an exact pair of bf16
+ *   values). With d < 64 it runs on zero-padded copies of q, k and v (d = dv = 64; zero features
+ *   leave the intercept unchanged: their moments are exactly zero, so the ridge system is block-
+ *   diagonal with a zero right-hand side on the padded block), at the cost of the padded work.
  * - Pointers named *_host are host memory; every other data pointer is device memory of the
  *   current CUDA device, 16-byte aligned. The caller owns every buffer; `out` must not overlap
  *   an input.
@@ -63,12 +65,12 @@ typedef enum { LLA_F32 = 0, LLA_BF16 = 1 } lla_dtype;
 
 /* Implementation choices (lla_options.path). */
 typedef enum {
-  LLA_PATH_AUTO = 0,        /* tensor cores for bf16 with d = 64 (d = dv = 64 for the other ops),
-                               CUDA cores otherwise */
+  LLA_PATH_AUTO = 0,        /* tensor cores for bf16 (the forward: any d, zero-padded to 64 when
+                               d < 64; the other ops: d = dv = 64), CUDA cores otherwise */
   LLA_PATH_CUDA_CORE = 1,   /* CUDA cores always */
   LLA_PATH_TENSOR_CORE = 2, /* tensor cores wherever supported (currently the same as AUTO) */
   LLA_PATH_CG = 3           /* lla_forward*_ex only: matrix-free conjugate gradients for the ridge
-                               systems (bf16, d = dv = 64; as AUTO elsewhere) */
+                               systems (bf16 with dv = 64 or d < 64; as AUTO elsewhere) */
 } lla_path;
 
 /* Closed form of the LLA intercept that a forward evaluates (lla_options.form). */
@@ -152,12 +154,12 @@ int lla_forward_ws(const void* q, const void* k, const void* v, void* out, int B
  *     LLA_FORM_CENTRED (default) o = vbar + C_vk y,  (C_kk + lambda' I) y = q - kbar;
  *     LLA_FORM_PAGE  o = sum w (1 - z.rho*) v / sum w (1 - z.rho*),  z = k - q,
  *       (sum w z z^T + lambda' I) rho* = sum w z, evaluated as the exact-LLA two-branch epilogue
- *       (O1 - O2) / (d1 - d2). It runs on the tensor-core dense strategy only (bf16, d = dv = 64,
- *       path AUTO or TENSOR_CORE; otherwise LLA_ERR_UNSUPPORTED). Its system carries the rank-one
+ *       (O1 - O2) / (d1 - d2). It runs on the tensor-core dense strategy only (bf16 with dv = 64
+ *       or d < 64, path AUTO or TENSOR_CORE; otherwise LLA_ERR_UNSUPPORTED). Its system carries the rank-one
  *       term w (kbar - q)(kbar - q)^T on top of the centred one, so it is worse conditioned for
  *       queries far from the weighted key mean.
  * - opts->test_fault = LLA_FAULT_WITHHOLD_KEYS exercises the bounded device waits: the
- *   tensor-core moments stage (bf16, d = 64; LLA_ERR_UNSUPPORTED on other paths) never stages
+ *   tensor-core moments stage (bf16; LLA_ERR_UNSUPPORTED on other paths) never stages
  *   its first key block, so every wait that needs it gives up after the wait limit (~2 s), the
  *   stage returns early without issuing the tensor-core work that depends on it, and
  *   LLA_ERR_TIMEOUT is recorded in the status word (lla_stream_status). The output of such a call

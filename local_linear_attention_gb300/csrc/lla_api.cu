@@ -132,8 +132,10 @@ Args make_args(const void* q, const void* k, const void* v, void* out, int B, in
 
 size_t elem_bytes(int dtype) { return dtype == LLA_F32 ? 4 : 2; }
 
-// Runs every stage on `s` with scratch `base`.
-int run_forward(const Args& a, void* base, cudaStream_t s) {
+// Runs every stage on `s` with scratch `base`. `user` (non-null) is the caller's call when `a` is
+// its zero-padded d = dv = 64 form: the padding runs with the first stage, the copy of the
+// output's columns back with the last.
+int run_stages(const Args& a, void* base, cudaStream_t s, const Args* user) {
   Workspace ws;
   carve_workspace(a, base, &ws);
   if (ws.form == kFormPage && !(ws.path == kPathTensorCore && a.dv == 64)) return LLA_ERR_UNSUPPORTED;
@@ -167,7 +169,12 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
     stages[4] = launch_readout_tc;
   }
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
+    if (i == 0 && user && launch_pad_inputs(*user, const_cast<void*>(a.q), const_cast<void*>(a.k),
+                                            const_cast<void*>(a.v), s) != cudaSuccess)
+      return LLA_ERR_CUDA;
     if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
+    if (i == LLA_NUM_STAGES - 1 && user && launch_unpad_output(*user, a.out, s) != cudaSuccess)
+      return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);
   }
   if (prof) {
@@ -175,6 +182,27 @@ int run_forward(const Args& a, void* base, cudaStream_t s) {
     g_prof.push_back(rec);
   }
   return LLA_OK;
+}
+
+// The padded form of a call: d = dv = 64, q, k, v and out in the first four regions of `base`.
+Args padded_args(const Args& a, void* base, void** rest) {
+  const size_t row = align_up((size_t)a.rows() * 64 * 2);
+  char* p = static_cast<char*>(base);
+  Args a64 = a;
+  a64.d = a64.dv = 64;
+  a64.q = p;
+  a64.k = p + row;
+  a64.v = p + 2 * row;
+  a64.out = p + 3 * row;
+  *rest = p + 4 * row;
+  return a64;
+}
+
+int run_forward(const Args& a, void* base, cudaStream_t s) {
+  if (!pad_eligible(a)) return run_stages(a, base, s, nullptr);
+  void* rest = nullptr;
+  const Args a64 = padded_args(a, base, &rest);
+  return run_stages(a64, rest, s, &a);
 }
 
 }  // namespace
@@ -190,6 +218,11 @@ int choose_path(const Args& a) {
 }
 
 size_t workspace_bytes(const Args& a) {
+  if (pad_eligible(a)) {  // four padded [rows][64] bf16 tensors, then the d = 64 scratch
+    Args a64 = a;
+    a64.d = a64.dv = 64;
+    return 4 * align_up((size_t)a.rows() * 64 * 2) + workspace_bytes(a64);
+  }
   const size_t BH = (size_t)a.BH(), R = (size_t)a.rows();
   const size_t G = (size_t)gram_floats(a.d);
   size_t n = 0;

@@ -86,6 +86,15 @@ int choose_path(const Args& a);
 size_t workspace_bytes(const Args& a);
 void carve_workspace(const Args& a, void* base, Workspace* ws);
 
+// bf16 inputs with d < 64 run on the d = dv = 64 tensor-core path with zero-padded copies of q,
+// k and v (lla_pad.cu; the padded features change nothing). Copies a's q, k, v ([rows][d] and
+// [rows][dv] bf16) to [rows][64] with zeros after, and the first dv columns of o64 back to a.out.
+inline bool pad_eligible(const Args& a) {
+  return a.dtype == LLA_BF16 && a.d < 64 && a.path_req != kPathCudaCore;
+}
+cudaError_t launch_pad_inputs(const Args& a, void* q64, void* k64, void* v64, cudaStream_t s);
+cudaError_t launch_unpad_output(const Args& a, const void* o64, cudaStream_t s);
+
 // Kernel launchers (one per stage). Each returns the launch error, if any.
 cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_moments_ffma(const Args& a, const Workspace& ws, cudaStream_t s);

@@ -109,11 +109,11 @@ def test_page_form_large_ridge_is_softmax(page):
 
 
 def test_page_form_other_paths_unsupported(page):
-    # fp32 inputs and d = 32 take the CUDA-core stage, which has no page form.
-    for dtype, d in (("f32", 64), ("bf16", 32)):
+    # fp32 inputs and the CUDA-core path have no page form.
+    for dtype, d, path in (("f32", 64, page.PATH_AUTO), ("bf16", 32, page.PATH_CUDA_CORE)):
         q, k, v = W.make_iid(1, 1, 64, d, d, dtype, seed=2)
         with pytest.raises(page.LlaError):
-            page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2)
+            page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2, path=path)
     q, k, v = W.make_iid(1, 1, 64, 64, 64, "bf16", seed=3)
     with pytest.raises(page.LlaError) as ei:
         page.lla_forward(q.cuda(), k.cuda(), v.cuda(), 8.0, 1e-2, path=page.PATH_CG)

@@ -47,7 +47,13 @@ def test_withheld_keys_time_out_and_the_stream_stays_usable(lla):
 
 
 def test_fault_needs_the_tensor_core_moments(lla):
-    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 32, 32, "bf16", seed=92))
+    # fp32 inputs, and bf16 on the CUDA-core path, have no tensor-core moments stage
+    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 32, 32, "f32", seed=92))
     with pytest.raises(lla.LlaError) as ei:
         lla.lla_forward(q, k, v, 8.0, 1e-2, test_fault=lla.FAULT_WITHHOLD_KEYS)
-    assert ei.value.status == 2  # LLA_ERR_UNSUPPORTED: no tensor-core moments stage for d = 32
+    assert ei.value.status == 2  # LLA_ERR_UNSUPPORTED
+    q, k, v = (t.cuda() for t in W.make_iid(1, 1, 64, 32, 32, "bf16", seed=92))
+    with pytest.raises(lla.LlaError) as ei:
+        lla.lla_forward(q, k, v, 8.0, 1e-2, test_fault=lla.FAULT_WITHHOLD_KEYS,
+                        path=lla.PATH_CUDA_CORE)
+    assert ei.value.status == 2
