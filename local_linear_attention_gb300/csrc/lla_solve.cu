@@ -398,29 +398,30 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
 
 // ----------------------------------------------------------------------------- solve, tensor-core rows
 // d = 64 with the tensor-core stage's moment rows (2208 floats in the order tc_slot() decodes;
-// omega and the row max in their own arrays). One warp per query; lane l owns rows l and 63 - l
-// of the matrix (a balanced share of the triangle) and factors it column by column (right-looking
-// Cholesky, the right-hand side riding along as the forward substitution). Arranged so that the
-// warp issues few instructions per query:
+// omega and the row max in their own arrays). A right-looking Cholesky per query, the right-hand
+// side riding along as the forward substitution, two queries per warp: half-warp h solves query
+// 2w + h, lane l of a half owning rows l, 31 - l, 32 + l and 63 - l of its matrix (four rows, a
+// balanced share of the triangle). Shared memory bounds this factorisation -- every column is
+// broadcast to the lanes that update the trailing rows -- so it is arranged for that:
+//  * a column broadcast is one shared-memory load for both queries of a warp (each half reads its
+//    own query's column); with one query per warp the broadcasts saturated the L1/shared data pipe
+//    at half the rate per query;
 //  * the moment row goes from global memory straight into the registers that hold the matrix (for
-//    a fixed triangle row j the slots of (j, r), r > j, are consecutive, so each load of a warp is
-//    one contiguous run). The loads and the assembly are unpredicated: a lane's entries past its
-//    row's diagonal are padding, computed and never read, and the odd diagonal entries (which sit
-//    outside the rows' runs) enter as a correction added to the pivot;
-//  * column k of the factor goes to shared memory once (column-major, rows padded to 68 floats),
-//    where the trailing update reads it as a broadcast and the backward substitution reads four
-//    columns of a row per vector load, conflict-free;
+//    a fixed triangle row j the slots of (j, r), r > j, are consecutive). The loads and the
+//    assembly are unpredicated: a lane's entries past its row's diagonal are padding, computed and
+//    never read, and the odd diagonal entries (which sit outside the rows' runs) enter as a
+//    correction added to the pivot;
+//  * column k of the factor goes to shared memory once (column-major, packed: column c holds rows
+//    4 floor(c / 4) .. 63), where the trailing update reads it and the backward substitution reads
+//    four entries of a row per vector load;
 //  * the trailing updates run as packed fp32 pairs (fma.rn.f32x2: the same single-rounded FMA on
 //    two lanes of a 64-bit register pair), which halves their instruction count;
 //  * the pivots' reciprocal square roots and the forward-substituted right-hand side are kept per
-//    column in shared memory (every lane stores the same value), the solution per row likewise,
-//    so that no lane has to pick out the values of its own rows with compare-and-select.
+//    column in shared memory, the solution per row likewise, so that no lane has to pick out the
+//    values of its own rows with compare-and-select; and the next pivot is formed from its owner's
+//    registers, so the chain from pivot to pivot does not wait for the column's broadcast.
 namespace stc {
 constexpr int D = 64;
-constexpr int WARPS = 4;                 // warps (queries) per block
-constexpr int LDC = D + 4;               // column stride of the factor in shared memory
-constexpr int WARP_FLOATS = D * LDC + 2 * D + D;  // factor; (z', 1/L_kk) per column; y
-constexpr size_t SMEM_BYTES = sizeof(float) * WARPS * WARP_FLOATS;
 
 // Slot of (a, b) in a tensor-core moment row for b >= a + (a & 1) (the run of row a):
 // run_base(a) + b. For every a and 0 <= b < 64, run_base(a) + b stays inside the row.
@@ -460,69 +461,6 @@ __device__ __forceinline__ void trail(float (&a)[N], float ns, const float* cb) 
   }
 }
 
-struct Lane {
-  float a0[32];   // row r0 = lane: entries 0..r0 (the rest is padding)
-  float a1[64];   // row r1 = 63 - lane: entries 0..r1
-  float dg0, dg1; // correction of the rows' diagonal entries, added to the pivot
-  float z0, z1;   // right-hand sides, updated by the forward substitution until used
-  int r0, r1;
-  bool ok;
-};
-
-// Column K: pivot from its owner, scale, store the column, update the trailing matrix and the
-// right-hand side. Entries of rows above K are padding throughout and harmless to update. `mine`
-// is this lane's candidate pivot (only the owner's is used). The owner of column K + 1 forms the
-// next pivot from its own registers (row K + 1's entries K and K + 1: the same fused operation
-// the trailing update applies to it), so the chain from pivot to pivot does not wait for the
-// column's broadcast through shared memory.
-template <int K>
-__device__ __forceinline__ void column(Lane& L, float* Lc, float2* zi, float mine) {
-  constexpr bool lo = K < 32;
-  constexpr int owner = lo ? K : D - 1 - K;
-  const float piv = __shfl_sync(0xffffffffu, mine, owner);
-  L.ok = L.ok && piv > 0.f;  // false for NaN too; a failed row is solved again by the repair pass
-  const float inv = rsqrtf(piv);
-  const float zk = __shfl_sync(0xffffffffu, lo ? L.z0 : L.z1, owner) * inv;
-  zi[K] = make_float2(zk, inv);  // every lane stores the same value
-  float* cb = Lc + K * LDC;
-  if constexpr (lo) {
-    L.a0[K] *= inv;
-    cb[L.r0] = L.a0[K];
-  }
-  L.a1[K] *= inv;
-  cb[L.r1] = L.a1[K];
-  float next = 0.f;
-  if constexpr (K + 1 < 32) next = fmaf(-L.a0[K], L.a0[K], L.a0[K + 1]) + L.dg0;
-  else if constexpr (K + 1 < D) next = fmaf(-L.a1[K], L.a1[K], L.a1[K + 1]) + L.dg1;
-  __syncwarp();
-  if constexpr (lo) {
-    trail<32, K>(L.a0, -L.a0[K], cb);
-    L.z0 = fmaf(-L.a0[K], zk, L.z0);
-  }
-  trail<64, K>(L.a1, -L.a1[K], cb);
-  L.z1 = fmaf(-L.a1[K], zk, L.z1);
-  if constexpr (K + 1 < D) column<K + 1>(L, Lc, zi, next);
-}
-
-// Backward substitution L^T y = z' over the rows K = KB + 3 .. KB, KB a multiple of 4:
-// y_K = w_K / L_KK from the row's owner, then w_r -= L[K][r] y_K for every row r (rows at or
-// below K are done and absorb the update harmlessly). lane_row is r0 (K < 32) or r1; the four
-// factor entries L[KB..KB+3][r] of each own row come from one vector load of column r.
-__device__ __forceinline__ void back_block(int KB, bool lo, const float* Lc, int r0, int r1,
-                                           float i0, float i1, float& w0, float& w1, float* ys) {
-  const float4 c0 = *reinterpret_cast<const float4*>(Lc + r0 * LDC + KB);
-  const float4 c1 = *reinterpret_cast<const float4*>(Lc + r1 * LDC + KB);
-  const float e0[4] = {c0.x, c0.y, c0.z, c0.w}, e1[4] = {c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-  for (int t = 3; t >= 0; --t) {
-    const int K = KB + t;
-    const int owner = lo ? K : D - 1 - K;
-    const float yk = __shfl_sync(0xffffffffu, lo ? w0 * i0 : w1 * i1, owner);
-    ys[K] = yk;  // every lane stores the same value
-    w0 = fmaf(-e0[t], yk, w0);
-    w1 = fmaf(-e1[t], yk, w1);
-  }
-}
 }  // namespace stc
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -530,6 +468,111 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+namespace stc4 {
+constexpr int D = 64;
+constexpr int WARPS = 2;                   // warps per block, two queries each
+constexpr int QPB = 2 * WARPS;             // queries per block
+constexpr int LC = 2176;                   // packed factor
+// factor; (z', 1/L_kk) per column; y; 4 floats of padding, so that the two queries of a warp
+// start 16 bytes apart in the banks and their halves' column broadcasts do not conflict
+constexpr int Q_FLOATS = LC + 2 * D + D + 4;
+constexpr size_t SMEM_BYTES = sizeof(float) * QPB * Q_FLOATS;
+
+__host__ __device__ constexpr int col_start(int c) { return 4 * (c / 4); }
+// first float of column c: the sum of the lengths 64 - col_start(k) of the columns k < c
+__host__ __device__ constexpr int col_base(int c) {
+  return 256 * (c / 4) - 8 * (c / 4) * (c / 4 - 1) + (c % 4) * (D - 4 * (c / 4));
+}
+static_assert(col_base(D) == LC, "packed factor size");
+// the rows of lane group g (array g) span [16 g, 16 g + 15]; array g holds entries 0 .. 16 g + 15
+__host__ __device__ constexpr int group_of(int r) { return r >> 4; }
+
+using stc::fma2;
+using stc::run_base;
+using stc::trail;
+
+struct Lane {
+  float a0[16], a1[32], a2[48], a3[64];  // rows l, 31 - l, 32 + l, 63 - l (entries past the
+                                         // diagonal are padding, computed and never read)
+  float dg[4];  // diagonal corrections (the odd diagonals and lambda'), added to the pivot
+  float z[4];   // right-hand sides, updated by the forward substitution until used
+  int l;        // lane within the half-warp
+  int hb;       // first lane of the half-warp
+  bool ok;
+};
+
+template <int G, int J>
+__device__ __forceinline__ float& at(Lane& L) {
+  if constexpr (G == 0) return L.a0[J < 16 ? J : 0];
+  else if constexpr (G == 1) return L.a1[J < 32 ? J : 0];
+  else if constexpr (G == 2) return L.a2[J < 48 ? J : 0];
+  else return L.a3[J];
+}
+// row of array G for lane l
+__device__ __forceinline__ int row_of(int G, int l) {
+  return G == 0 ? l : G == 1 ? 31 - l : G == 2 ? 32 + l : 63 - l;
+}
+template <int K>
+__host__ __device__ constexpr int owner_of() {
+  constexpr int g = group_of(K);
+  return g == 0 ? K : g == 1 ? 31 - K : g == 2 ? K - 32 : 63 - K;
+}
+
+// Column K's entry of array G's row: scale it and store it into the packed column (rows at or
+// past the column's first stored row; a row of array G can lie before it only when K is in the
+// same 16-row group).
+template <int G, int K>
+__device__ __forceinline__ void scale_store(Lane& L, float inv, float* cb) {
+  if constexpr (K < 16 * G + 16) {
+    float& x = at<G, K>(L);
+    x *= inv;
+    constexpr int cs = col_start(K);
+    if constexpr (16 * G >= cs) {
+      cb[row_of(G, L.l)] = x;
+    } else {
+      const int r = row_of(G, L.l);
+      if (r >= cs) cb[r] = x;
+    }
+  }
+}
+template <int G, int K>
+__device__ __forceinline__ void update(Lane& L, const float* cb, float zk) {
+  if constexpr (K < 16 * G + 15) {
+    if constexpr (G == 0) trail<16, K>(L.a0, -L.a0[K], cb);
+    else if constexpr (G == 1) trail<32, K>(L.a1, -L.a1[K], cb);
+    else if constexpr (G == 2) trail<48, K>(L.a2, -L.a2[K], cb);
+    else trail<64, K>(L.a3, -L.a3[K], cb);
+  }
+  if constexpr (K < 16 * G + 16) L.z[G] = fmaf(-at<G, K>(L), zk, L.z[G]);
+}
+
+template <int K>
+__device__ __forceinline__ void column(Lane& L, float* Lc, float2* zi, float mine) {
+  constexpr int g = group_of(K);
+  const float piv = __shfl_sync(0xffffffffu, mine, L.hb + owner_of<K>());
+  L.ok = L.ok && piv > 0.f;  // false for NaN too; a failed query is solved again by the repair pass
+  const float inv = rsqrtf(piv);
+  const float zk = __shfl_sync(0xffffffffu, L.z[g], L.hb + owner_of<K>()) * inv;
+  if (L.l == 0) zi[K] = make_float2(zk, inv);
+  float* cb = Lc + col_base(K) - col_start(K);  // cb[r] = entry (r, K)
+  scale_store<0, K>(L, inv, cb);
+  scale_store<1, K>(L, inv, cb);
+  scale_store<2, K>(L, inv, cb);
+  scale_store<3, K>(L, inv, cb);
+  float next = 0.f;  // the next pivot from its owner's registers (row K + 1's entries K, K + 1)
+  if constexpr (K + 1 < D) {
+    constexpr int ng = group_of(K + 1);
+    next = fmaf(-at<ng, K>(L), at<ng, K>(L), at<ng, K + 1>(L)) + L.dg[ng];
+  }
+  __syncwarp();
+  update<0, K>(L, cb, zk);
+  update<1, K>(L, cb, zk);
+  update<2, K>(L, cb, zk);
+  update<3, K>(L, cb, zk);
+  if constexpr (K + 1 < D) column<K + 1>(L, Lc, zi, next);
+}
+}  // namespace stc4
 
 // Output for the tensor-core readout: y as three exact bf16 parts (y = y1 + y2 + y3; 24
 // significant bits, so that the readout's Y K^T keeps y's precision on the tensor cores), each
@@ -542,65 +585,59 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // + lambda' I: the centred matrix plus one rank-one term. The output is then rho* in place of y
 // and cy = q . rho*, so that the readout's t_ij = k_j . rho* - cy is the page's z_ij . rho*.
 template <bool PAGE>
-__global__ void __launch_bounds__(stc::WARPS * 32, 3)
-solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kref,
-                const float* __restrict__ mom, const float* __restrict__ omega,
-                const float* __restrict__ mrow, long long rows, int T, float lam,
-                uint32_t* __restrict__ ytc,
-                float* __restrict__ cy_out, float* __restrict__ y_out, float* __restrict__ kbar_out,
-                int* __restrict__ rep, int* __restrict__ status) {
-  using namespace stc;
+__global__ void __launch_bounds__(stc4::WARPS * 32, 4)
+solve_tc4_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kref,
+                 const float* __restrict__ mom, const float* __restrict__ omega,
+                 const float* __restrict__ mrow, long long rows, int T, float lam,
+                 uint32_t* __restrict__ ytc, float* __restrict__ cy_out,
+                 float* __restrict__ y_out, float* __restrict__ kbar_out, int* __restrict__ rep,
+                 int* __restrict__ status) {
+  using namespace stc4;
   extern __shared__ float4 smem4[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * WARPS + warp;
-  if (row >= rows) return;  // whole warp leaves together
-  float* Lc = reinterpret_cast<float*>(smem4) + warp * WARP_FLOATS;
-  float2* zi = reinterpret_cast<float2*>(Lc + D * LDC);
-  float* ys = Lc + D * LDC + 2 * D;
-  // before the factorisation the (z', 1/L_kk) area holds s and (page form) mu
-  float* sv = reinterpret_cast<float*>(zi);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, half = lane >> 4;
+  const long long row_req = (long long)blockIdx.x * QPB + 2 * warp + half;
+  const bool live = row_req < rows;
+  const long long row = live ? row_req : rows - 1;  // a half past the end mirrors the last row
+  if (__all_sync(0xffffffffu, !live)) return;        // whole warp past the end
+  float* Lc = reinterpret_cast<float*>(smem4) + (2 * warp + half) * Q_FLOATS;
+  float2* zi = reinterpret_cast<float2*>(Lc + LC);
+  float* ys = Lc + LC + 2 * D;
+  float* sv = reinterpret_cast<float*>(zi);  // before the factorisation: s, then (page) mu
   float* muv = sv + D;
   const float* g = mom + row * TC_ROW;
 
   Lane L;
-  L.r0 = lane;
-  L.r1 = D - 1 - lane;
+  L.l = lane & 15;
+  L.hb = lane & 16;
   L.ok = true;
-  // Every load of the row first (all in flight together), then the arithmetic.
+  const int r[4] = {L.l, 31 - L.l, 32 + L.l, 63 - L.l};
 #pragma unroll
-  for (int j = 0; j < 32; ++j) L.a0[j] = __ldcs(g + run_base(j) + L.r0);
+  for (int j = 0; j < 16; ++j) L.a0[j] = __ldcs(g + run_base(j) + r[0]);
 #pragma unroll
-  for (int j = 0; j < D; ++j) L.a1[j] = __ldcs(g + run_base(j) + L.r1);
-  // the true diagonal entries and what the run loads put in their place
-  const float d0 = __ldcs(g + tc_slot(L.r0, L.r0)), d1 = __ldcs(g + tc_slot(L.r1, L.r1));
-  const float x0 = __ldcs(g + run_base(L.r0) + L.r0), x1 = __ldcs(g + run_base(L.r1) + L.r1);
-  const float s0 = __ldcs(g + run_base(L.r0) + D), s1 = __ldcs(g + run_base(L.r1) + D);
+  for (int j = 0; j < 32; ++j) L.a1[j] = __ldcs(g + run_base(j) + r[1]);
+#pragma unroll
+  for (int j = 0; j < 48; ++j) L.a2[j] = __ldcs(g + run_base(j) + r[2]);
+#pragma unroll
+  for (int j = 0; j < 64; ++j) L.a3[j] = __ldcs(g + run_base(j) + r[3]);
   const float om = omega[row];
-  // the query in the head's key frame (the moments are those of kt = bf16(k - c))
-  const int bh = (int)row / T;  // rows < 2^31
-  const float qa = ldf(q, row * D + L.r0) - kref[bh * D + L.r0];
-  const float qb = ldf(q, row * D + L.r1) - kref[bh * D + L.r1];
-  // the ridge scaled by exp(-m), formed in the exponent so that no intermediate overflows
   const float lp = fminf(fmaxf(expf(logf(lam) - mrow[row]), FLT_MIN), FLT_MAX);
-  // x is d for even rows and the zero padding slot before the run for odd rows, so the correction
-  // is exactly lambda' or d + lambda'; the ridge enters after the trailing updates' cancellation.
-  L.dg0 = (d0 - x0) + lp;
-  L.dg1 = (d1 - x1) + lp;
-  sv[L.r0] = s0;
-  sv[L.r1] = s1;
-  const float mu0 = fmaf(-om, qa, s0), mu1 = fmaf(-om, qb, s1);  // page form: mu = s - omega q
-  if (PAGE) {
-    muv[L.r0] = mu0;
-    muv[L.r1] = mu1;
+  const int bh = (int)row / T;  // rows < 2^31
+  float kb[4], qa[4], mu[4];
+  const float inv_om = 1.f / om;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float d = __ldcs(g + tc_slot(r[i], r[i])), x = __ldcs(g + run_base(r[i]) + r[i]);
+    const float s = __ldcs(g + run_base(r[i]) + D);
+    L.dg[i] = (d - x) + lp;  // x is d for even rows, the zero slot before the run for odd rows
+    qa[i] = ldf(q, row * D + r[i]) - kref[bh * D + r[i]];
+    mu[i] = fmaf(-om, qa[i], s);  // page form: mu = s - omega q
+    kb[i] = s * inv_om;
+    sv[r[i]] = s;
+    if (PAGE) muv[r[i]] = mu[i];
+    L.z[i] = PAGE ? mu[i] : qa[i] - kb[i];
   }
   __syncwarp();
-  const float inv_om = 1.f / om;
-  const float kb0 = s0 * inv_om, kb1 = s1 * inv_om;
-  const float mo0 = mu0 * inv_om, mo1 = mu1 * inv_om;
-  L.z0 = PAGE ? mu0 : qa - kb0;
-  L.z1 = PAGE ? mu1 : qb - kb1;
-  // C_kk = S - s s^T / omega (page form: + mu mu^T / omega); lambda' and the odd diagonal
-  // entries come in through dg0 and dg1.
+  // C_kk = S - s s^T / omega (page form: + mu mu^T / omega) on every array entry
 #pragma unroll
   for (int j = 0; j < D; j += 4) {
     const float4 s4 = *reinterpret_cast<const float4*>(sv + j);
@@ -612,78 +649,102 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if (j + u < 32) {
-        float v = fmaf(-sj[u], kb0, L.a0[(j + u) & 31]);
-        if (PAGE) v = fmaf(mj[u], mo0, v);
-        L.a0[(j + u) & 31] = v;
-      }
-      float v = fmaf(-sj[u], kb1, L.a1[j + u]);
-      if (PAGE) v = fmaf(mj[u], mo1, v);
-      L.a1[j + u] = v;
+      const int jj = j + u;
+      auto upd = [&](float& a, int i) {
+        float v = fmaf(-sj[u], kb[i], a);
+        if (PAGE) v = fmaf(mj[u], mu[i] * inv_om, v);
+        a = v;
+      };
+      if (jj < 16) upd(L.a0[jj & 15], 0);
+      if (jj < 32) upd(L.a1[jj & 31], 1);
+      if (jj < 48) upd(L.a2[jj < 48 ? jj : 0], 2);
+      upd(L.a3[jj], 3);
     }
   }
   __syncwarp();  // s and mu are read; the area now takes (z', 1/L_kk)
 
-  stc::column<0>(L, Lc, zi, L.a0[0] + L.dg0);
+  stc4::column<0>(L, Lc, zi, L.a0[0] + L.dg[0]);
+  const unsigned fails = __ballot_sync(0xffffffffu, !L.ok);
+  const bool my_fail = ((fails >> L.hb) & 0xFFFFu) != 0;
+  __syncwarp();
+  // Backward substitution L^T y = z', four rows at a time from the bottom; each lane reads the
+  // factor entries L[KB..KB+3][r] of its rows r (column r of the packed factor).
+  float w[4], iv[4];
+  const float* lcr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = zi[r[i]];
+    w[i] = t.x;
+    iv[i] = t.y;
+    lcr[i] = Lc + col_base(r[i]) - col_start(r[i]);
+  }
+#pragma unroll
+  for (int KB = D - 4; KB >= 0; KB -= 4) {
+    float e[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 c = *reinterpret_cast<const float4*>(lcr[i] + KB);
+      e[i][0] = c.x; e[i][1] = c.y; e[i][2] = c.z; e[i][3] = c.w;
+    }
+#pragma unroll
+    for (int t = 3; t >= 0; --t) {
+      const int K = KB + t;
+      const int gk = K >> 4;
+      const int owner = gk == 0 ? K : gk == 1 ? 31 - K : gk == 2 ? K - 32 : 63 - K;
+      const float yk = __shfl_sync(0xffffffffu, w[gk] * iv[gk], L.hb + owner);
+      if (L.l == 0) ys[K] = yk;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = fmaf(-e[i][t], yk, w[i]);
+    }
+  }
+  __syncwarp();
   uint32_t* yrow = ytc + row * 3 * (D / 2);
-  if (!__all_sync(0xffffffffu, L.ok)) {
-    // A non-positive pivot: fp32 rounding of the tensor-core sums can exceed the smallest
-    // eigenvalues of a very ill-conditioned system. The row goes to the precise repair pass
-    // (repair_kernel), which overwrites this row's y; if its list is full, the row is NaN.
-    int slot = kMaxRepairRows;
-    if (lane == 0) slot = atomicAdd(rep, 1);
-    slot = __shfl_sync(0xffffffffu, slot, 0);
-    if (slot < kMaxRepairRows) {
-      if (lane == 0) rep[1 + slot] = (int)row;
-      return;
-    }
-    if (lane == 0) {
-      atomicOr(status, kStatusNumerical);
-      cy_out[row] = __int_as_float(0x7fc00000);
-    }
-    for (int p = 0; p < 3; ++p) yrow[p * (D / 2) + lane] = 0x7FC07FC0u;  // bf16 NaN pairs
-    if (y_out) {
-      const float qn = __int_as_float(0x7fc00000);
-      y_out[row * D + L.r0] = qn;
-      y_out[row * D + L.r1] = qn;
-      kbar_out[row * D + L.r0] = qn;
-      kbar_out[row * D + L.r1] = qn;
+  if (my_fail) {
+    // A non-positive pivot: the query goes to the precise repair pass (repair_kernel), which
+    // overwrites its y; if the repair list is full, the query is NaN.
+    if (live && L.l == 0) {
+      const int slot = atomicAdd(rep, 1);
+      if (slot < kMaxRepairRows) {
+        rep[1 + slot] = (int)row;
+      } else {
+        atomicOr(status, kStatusNumerical);
+        cy_out[row] = __int_as_float(0x7fc00000);
+        for (int p = 0; p < 3 * (D / 2); ++p) yrow[p] = 0x7FC07FC0u;  // bf16 NaN pairs
+        if (y_out)
+          for (int a = 0; a < D; ++a)
+            y_out[row * D + a] = kbar_out[row * D + a] = __int_as_float(0x7fc00000);
+      }
     }
     return;
   }
-  __syncwarp();
-  const float2 zr0 = zi[L.r0], zr1 = zi[L.r1];
-  float w0 = zr0.x, w1 = zr1.x;
-  // rows 63..32 are owned through r1, rows 31..0 through r0
-#pragma unroll 2
-  for (int KB = D - 4; KB >= 32; KB -= 4)
-    back_block(KB, false, Lc, L.r0, L.r1, zr0.y, zr1.y, w0, w1, ys);
-#pragma unroll 2
-  for (int KB = 28; KB >= 0; KB -= 4)
-    back_block(KB, true, Lc, L.r0, L.r1, zr0.y, zr1.y, w0, w1, ys);
-  __syncwarp();
-  // Lane l writes elements 2l and 2l + 1 of each part, so that each part's row is one
-  // coalesced store.
-  const float2 yab = *reinterpret_cast<const float2*>(ys + 2 * lane);
-  const float ya = yab.x, yb = yab.y;
-  const uint32_t p1 = pack_bf16(ya, yb);
-  const float ra = ya - __uint_as_float(p1 << 16), rb = yb - __uint_as_float(p1 & 0xFFFF0000u);
-  const uint32_t p2 = pack_bf16(ra, rb);
-  const uint32_t p3 =
-      pack_bf16(ra - __uint_as_float(p2 << 16), rb - __uint_as_float(p2 & 0xFFFF0000u));
-  yrow[lane] = p1;
-  yrow[D / 2 + lane] = p2;
-  yrow[D + lane] = p3;
-  const float y0 = ys[L.r0], y1 = ys[L.r1];
-  float c = PAGE ? fmaf(qa, y0, qb * y1) : fmaf(kb0, y0, kb1 * y1);
+  // Lane l of a half writes elements 4l .. 4l + 3 of each part (two packed pairs).
+  const float4 y4 = *reinterpret_cast<const float4*>(ys + 4 * L.l);
+  const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+  uint32_t p1[2], p2[2], p3[2];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if (lane == 0) cy_out[row] = c;
+  for (int h = 0; h < 2; ++h) {
+    const float ya = yv[2 * h], yb = yv[2 * h + 1];
+    p1[h] = pack_bf16(ya, yb);
+    const float ra = ya - __uint_as_float(p1[h] << 16), rb = yb - __uint_as_float(p1[h] & 0xFFFF0000u);
+    p2[h] = pack_bf16(ra, rb);
+    p3[h] = pack_bf16(ra - __uint_as_float(p2[h] << 16), rb - __uint_as_float(p2[h] & 0xFFFF0000u));
+  }
+  float c = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c = fmaf(PAGE ? qa[i] : kb[i], ys[r[i]], c);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if (!live) return;
+  reinterpret_cast<uint2*>(yrow)[L.l] = make_uint2(p1[0], p1[1]);
+  reinterpret_cast<uint2*>(yrow + D / 2)[L.l] = make_uint2(p2[0], p2[1]);
+  reinterpret_cast<uint2*>(yrow + D)[L.l] = make_uint2(p3[0], p3[1]);
+  if (L.l == 0) cy_out[row] = c;
   if (y_out) {
-    y_out[row * D + L.r0] = y0;
-    y_out[row * D + L.r1] = y1;
-    kbar_out[row * D + L.r0] = kb0;
-    kbar_out[row * D + L.r1] = kb1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      y_out[row * D + r[i]] = ys[r[i]];
+      kbar_out[row * D + r[i]] = kb[i];
+    }
   }
 }
 
@@ -896,12 +957,12 @@ repair_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
 
 cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long rows = a.rows();
-  const long long blocks = (rows + stc::WARPS - 1) / stc::WARPS;
-  auto kern = ws.form == kFormPage ? solve_tc_kernel<true> : solve_tc_kernel<false>;
+  const long long blocks = (rows + stc4::QPB - 1) / stc4::QPB;
+  auto kern = ws.form == kFormPage ? solve_tc4_kernel<true> : solve_tc4_kernel<false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)stc::SMEM_BYTES);
+                                         (int)stc4::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  kern<<<(unsigned)blocks, stc::WARPS * 32, stc::SMEM_BYTES, s>>>(
+  kern<<<(unsigned)blocks, stc4::WARPS * 32, stc4::SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), ws.kref, ws.mom, ws.omega, ws.m, rows, a.T, a.lam,
       ws.ytc, ws.cy,
       a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.rep, ws.status);
