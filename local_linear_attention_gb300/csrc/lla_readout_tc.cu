@@ -31,7 +31,9 @@
 // One CTA per 128-query tile; keys in chunks of 64 (two weight images). Warp roles (7 warps):
 // 0 issues T = Y K^T (12 MMAs per chunk, N = 64) and owns the TMEM allocation; 6 issues
 // O1 += P V (P straight from shared memory) and O2 += P2 V (P2 from tensor memory), 12 MMAs per
-// chunk; 1 stages the key, value and weight chunks; 2-5 (one thread per query = TMEM lane) turn
+// chunk; 1 stages the key and value chunks by TMA tensor copies (128-byte swizzled, read by the
+// MMAs through swizzled descriptors) and the weight images by a bulk copy; 2-5 (one thread per
+// query = TMEM lane) turn
 // T and P into P2 and write the output. Two issuing threads, because each tcgen05.mma costs its
 // issuing thread about as long as the tensor core takes to run one of these. All waits are
 // bounded.
@@ -39,6 +41,7 @@
 
 #include "lla_internal.cuh"
 #include "lla_tc_ptx.cuh"
+#include "lla_tmap.cuh"
 
 namespace lla {
 namespace {
@@ -72,7 +75,10 @@ constexpr int STAGE = 2 * KV_BYTES + P_BYTES;       // K, V, P of one chunk
 constexpr int SM_ST = SM_Y + 3 * TILE;
 constexpr int SM_BAR = SM_ST + KS * STAGE;
 constexpr int SMEM_BYTES = SM_BAR + 256;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+constexpr int SMEM_LAUNCH = SMEM_BYTES + 1024;  // slack for aligning the base to 1024 bytes
+static_assert(SMEM_LAUNCH <= 227 * 1024, "shared memory budget");
+static_assert(SM_ST % 1024 == 0 && STAGE % 1024 == 0 && KV_BYTES % 1024 == 0,
+              "128-byte swizzled stages on 1024-byte boundaries");
 
 // Byte offset of 16-byte chunk c (elements 8c..8c+7) of row r in a K-major tile whose rows hold
 // 64 elements: core matrix (r / 8, c) of 128 bytes, row groups 1024 bytes apart.
@@ -102,11 +108,12 @@ static_assert(sizeof(Barriers) <= 256, "barrier region");
 
 template <typename TOut, bool kMatvec, bool kPage>
 __global__ void __launch_bounds__(NTHREADS, 1)
-readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const uint4* __restrict__ pimg, const uint32_t* __restrict__ ytc,
                   const float* __restrict__ cy_in, int T, int BH, TOut* __restrict__ out,
                   const int* __restrict__ tile_active, int* __restrict__ status) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -138,7 +145,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
   cp_async_wait<0>();
   if (tid == 0) {
     for (int s = 0; s < KS; ++s) {
-      mbar_init(&bar.kvfull[s], 32);  // one cp.async completion arrival per loader lane
+      mbar_init(&bar.kvfull[s], 1);  // the loader's arrival with the key and value bytes
       mbar_init(&bar.kvempty[s], 1);
       mbar_init(&bar.pfull[s], 1);
     }
@@ -171,7 +178,7 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     if (lane == 0) {
       // Base descriptors plus start-address offsets in 16-byte units (see the moments stage).
       const uint64_t yd = smem_desc(smem_u32(smem + SM_Y), 128, 1024);
-      const uint64_t kd = smem_desc(smem_u32(smem + SM_ST), 128, 1024);
+      const uint64_t kd = smem_desc_sw128(smem_u32(smem + SM_ST), 1024);
       constexpr uint32_t id_t = idesc_bf16(BM, CK, false, false);
       constexpr uint32_t tile16 = TILE >> 4;
       bool ok = true;
@@ -189,7 +196,8 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
         for (int part = 0; part < 3; ++part)
 #pragma unroll
           for (int s = 0; s < D / 16; ++s)
-            mma_ss(tt, yd + part * tile16 + 16 * s, kst + 16 * s, id_t, (part > 0 || s > 0) ? 1u : 0u);
+            mma_ss(tt, yd + part * tile16 + 16 * s, kst + 2 * s, id_t,  // K-steps: 32 B in a row
+                   (part > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar.tfull[tb]);
       }
       if (!ok) *abort_p = 1;
@@ -200,10 +208,10 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     // ------------------------------------------------------------------ O1, O2 issuer
     if (lane == 0) {
       // P images as the K-major A operand (K-adjacent core matrices 2048 B apart, M-adjacent
-      // 128 B); the V chunk as the MN-major B operand: K = keys (8-key groups 1024 B apart),
-      // N = value features (8-feature groups 128 B apart).
+      // 128 B); the V chunk as the MN-major B operand, 128-byte swizzled: a key's 64 values are
+      // one 128-byte row, 8-key atoms 1024 B apart.
       const uint64_t pd = smem_desc(smem_u32(smem + SM_ST + 2 * KV_BYTES), 2048, 128);
-      const uint64_t vd = smem_desc(smem_u32(smem + SM_ST + KV_BYTES), 1024, 128);
+      const uint64_t vd = smem_desc_sw128(smem_u32(smem + SM_ST + KV_BYTES), 1024);
       constexpr uint32_t id_o = idesc_bf16(BM, DV, false, true);
       bool ok = true;
       for (int c = 0; c < nck && ok; ++c) {
@@ -236,47 +244,38 @@ readout_tc_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __re
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V/P loader
-    // K and V: cp.async copies, every stage in flight, rows to the core-matrix layout (lane ->
-    // (row, 16-byte chunk) mapping conflict-free per 8-lane phase); each lane's copies of a chunk
-    // complete on the stage's barrier (cp.async.mbarrier.arrive, kvfull), and the MMA issuers
-    // fence the async proxy after their wait. The two weight images are one contiguous bulk copy
-    // into the stage as they are (pfull, counted in transaction bytes); a missing second image
-    // (past the pair's last block) is zero-filled by cp.async copies that read nothing.
-    const __nv_bfloat16* kbp = k + base * D;
-    const __nv_bfloat16* vbp = v + base * DV;
-    for (int c = 0; c < nck; ++c) {
-      {
+    // One thread: per chunk a TMA tensor copy of the 64 keys and one of the 64 values (rows past
+    // the head read as zeros; keys past the tile's causal end have zero weights), completing on
+    // the stage's barrier kvfull, and one bulk copy of the chunk's two weight images as they are
+    // (pfull). A tile's images cover its chunks: pair_blocks counts blocks up to the pair's last
+    // key, in pairs.
+    if (lane == 0) {
+      tma_prefetch_map(&kmap);
+      tma_prefetch_map(&vmap);
+      int issued = 0;
+      for (int c = 0; c < nck; ++c) {
         const int st = c % KS;
-        if (c >= KS && !warp_wait(&bar.kvempty[st], ((c / KS) - 1) & 1, status, abort_p)) break;
+        if (c >= KS && !mbar_wait(&bar.kvempty[st], ((c / KS) - 1) & 1, status, kStatusTimeout,
+                                  abort_p))
+          break;
         uint8_t* kdst = smem + SM_ST + st * STAGE;
-        uint8_t* vdst = kdst + KV_BYTES;
-        uint8_t* pdst = kdst + 2 * KV_BYTES;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int r = (lane & 7) + 8 * (t & 7), cc = (lane >> 3) + 4 * (t >> 3);
-          const int j = c * CK + r;
-          const bool in = j < jend;
-          const long long jj = in ? j : 0;
-          cp_async16(kdst + kmaj_off(r, cc), kbp + jj * D + cc * 8, in ? 16u : 0u);
-          cp_async16(vdst + kmaj_off(r, cc), vbp + jj * DV + cc * 8, in ? 16u : 0u);
-        }
-        const int have = min(2, nimg - 2 * c);  // weight images of this chunk (>= 1)
-        if (have < 2) {
-#pragma unroll
-          for (int t = 0; t < pscr::kBlockBytes / 16 / 32; ++t)
-            cp_async16(pdst + pscr::kBlockBytes + 16 * (t * 32 + lane), pt, 0u);
-        }
-        cp_async_mbar_arrive(&bar.kvfull[st]);
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t bytes = (uint32_t)have * pscr::kBlockBytes;
-          mbar_arrive_expect_tx(&bar.pfull[st], bytes);
-          bulk_g2s(pdst, pt + (long long)2 * c * (pscr::kBlockBytes / 16), bytes, &bar.pfull[st]);
-        }
+        mbar_arrive_expect_tx(&bar.kvfull[st], 2 * KV_BYTES);
+        tma_load_3d(kdst, &kmap, 0, c * CK, (int)bh, &bar.kvfull[st]);
+        tma_load_3d(kdst + KV_BYTES, &vmap, 0, c * CK, (int)bh, &bar.kvfull[st]);
+        mbar_arrive_expect_tx(&bar.pfull[st], P_BYTES);
+        bulk_g2s(kdst + 2 * KV_BYTES, pt + (long long)2 * c * (pscr::kBlockBytes / 16), P_BYTES,
+                 &bar.pfull[st]);
+        issued = c + 1;
+      }
+      // Nothing may land in this CTA's shared memory after it exits: wait (bounded) for the
+      // copies of the last stages filled; a normal run finds them complete.
+      volatile int never = 0;
+      for (int c = issued > KS ? issued - KS : 0; c < issued; ++c) {
+        mbar_wait(&bar.kvfull[c % KS], (c / KS) & 1, status, kStatusTimeout, &never);
+        mbar_wait(&bar.pfull[c % KS], (c / KS) & 1, status, kStatusTimeout, &never);
       }
     }
-    cp_async_commit();
-    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ weights + output
     const int quarter = warp & 3;
@@ -379,15 +378,29 @@ template <typename TOut, bool kMatvec, bool kPage = false>
 cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* keys,
                       const void* v, const uint32_t* ytc, const float* cy, TOut* out,
                       const int* tile_active) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  // keys and values: [BH][T][64] bf16, boxes of 64 rows x 64 features, 128-byte swizzled
+  CUtensorMap kmap, vmap;
+  const cuuint32_t ones[3] = {1, 1, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.T, (cuuint64_t)a.BH()};
+  const cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.T * D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)CK, 1};
+  static_assert(D == DV, "one tensor-map shape for keys and values");
+  for (int t = 0; t < 2; ++t)
+    if (encode(t ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(t ? v : keys), dims, str, box, ones,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
   auto kern = readout_tc_kernel<TOut, kMatvec, kPage>;
   cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
   if (err != cudaSuccess) return err;
   const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, s>>>(
-      static_cast<const __nv_bfloat16*>(keys), static_cast<const __nv_bfloat16*>(v),
-      static_cast<const uint4*>(ws.pscr), ytc, cy, a.T, (int)a.BH(), out, tile_active,
+  kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
+      kmap, vmap, static_cast<const uint4*>(ws.pscr), ytc, cy, a.T, (int)a.BH(), out, tile_active,
       ws.status);
   count_launch();
   return cudaGetLastError();
