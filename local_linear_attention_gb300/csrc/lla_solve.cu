@@ -586,7 +586,7 @@ __device__ __forceinline__ void column(Lane& L, float* Lc, float2* zi, float min
 // and cy = q . rho*, so that the readout's t_ij = k_j . rho* - cy is the page's z_ij . rho*.
 template <bool PAGE>
 __global__ void __launch_bounds__(stc4::WARPS * 32, 4)
-solve_tc4_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kref,
+solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kref,
                  const float* __restrict__ mom, const float* __restrict__ omega,
                  const float* __restrict__ mrow, long long rows, int T, float lam,
                  uint32_t* __restrict__ ytc, float* __restrict__ cy_out,
@@ -958,7 +958,7 @@ repair_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
 cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long rows = a.rows();
   const long long blocks = (rows + stc4::QPB - 1) / stc4::QPB;
-  auto kern = ws.form == kFormPage ? solve_tc4_kernel<true> : solve_tc4_kernel<false>;
+  auto kern = ws.form == kFormPage ? solve_tc_kernel<true> : solve_tc_kernel<false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)stc4::SMEM_BYTES);
   if (err != cudaSuccess) return err;
