@@ -20,9 +20,11 @@
 //    per query (each owns a quarter of the q, r, O1 and O2 coordinates), fp32 accumulation.
 // All mbarrier waits are bounded.
 #include <cstdint>
+#include <type_traits>
 
 #include "lla_internal.cuh"
 #include "lla_tc_ptx.cuh"
+#include "lla_tmap.cuh"
 
 namespace lla {
 namespace {
@@ -61,6 +63,9 @@ constexpr int SM_BAR = SM_V + KS * KV_STAGE;
 constexpr int SM_X = SM_BAR + 256;  // [2 halves][5 values][BM] per-row partials of the two halves
 constexpr int NXV = 5;              // m, d1, d2, and (STATS) dout . vbar, dout . o
 constexpr int SMEM_BYTES = SM_X + 2 * NXV * BM * 4;
+constexpr int SMEM_LAUNCH = SMEM_BYTES + 1024;  // slack for aligning the base to 1024 bytes
+static_assert(SM_K % 1024 == 0 && SM_V % 1024 == 0 && KV_STAGE % 1024 == 0,
+              "128-byte swizzled key and value stages on 1024-byte boundaries");
 
 __device__ __forceinline__ int kmaj_off(int r, int c) { return (r >> 3) * 1024 + c * 128 + (r & 7) * 16; }
 
@@ -100,12 +105,13 @@ static_assert(sizeof(Barriers) <= SM_X - SM_BAR, "barrier region");
 // G = dout . vbar with vbar = O1/d1, and D = dout . o + G tbar with o = (1 + tbar) vbar - O2/d1.
 template <bool STATS>
 __global__ void __launch_bounds__(NTHREADS, 1)
-parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ rp,
+parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const __nv_bfloat16* __restrict__ rp,
                    int T, int BH, float inv_h, __nv_bfloat16* __restrict__ out,
                    const __nv_bfloat16* __restrict__ dout, float* __restrict__ stats,
                    int* __restrict__ status) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -130,7 +136,7 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     *reinterpret_cast<uint4*>(smem + (which ? SM_R : SM_Q) + kmaj_off(r, c)) = val;
   }
   if (tid == 0) {
-    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 32); mbar_init(&bar.kvempty[s], 1); }
+    for (int s = 0; s < KS; ++s) { mbar_init(&bar.kvfull[s], 1); mbar_init(&bar.kvempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.sfull[s], 1);
       mbar_init(&bar.sfree[s], 8);
@@ -162,10 +168,11 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       // Base descriptors plus start-address offsets in 16-byte units.
       const uint64_t qd = smem_desc(smem_u32(smem + SM_Q), 128, 1024);
       const uint64_t rd = smem_desc(smem_u32(smem + SM_R), 128, 1024);
-      const uint64_t kd = smem_desc(smem_u32(smem + SM_K), 128, 1024);
-      // V block as the MN-major B operand: K = keys (8-key groups 1024 B apart), N = value
-      // features (8-feature groups 128 B apart).
-      const uint64_t vd = smem_desc(smem_u32(smem + SM_V), 1024, 128);
+      // key and value blocks 128-byte swizzled (the TMA copies' layout): K-major keys, the V
+      // block as the MN-major B operand (a key's 64 values one 128-byte row, 8-key atoms 1024 B
+      // apart)
+      const uint64_t kd = smem_desc_sw128(smem_u32(smem + SM_K), 1024);
+      const uint64_t vd = smem_desc_sw128(smem_u32(smem + SM_V), 1024);
       constexpr uint32_t id_s = idesc_bf16(BM, KB, false, false);
       constexpr uint32_t id_o = idesc_bf16(BM, DV, false, true);
       constexpr uint32_t stage16 = KV_STAGE >> 4;
@@ -184,10 +191,10 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
           const uint64_t kst = kd + (uint64_t)(st * stage16);
           const uint32_t ts = tbase + T_S + sb * KB, tt = tbase + T_T + sb * KB;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s) mma_ss(ts, qd + 16 * s, kst + 16 * s, id_s, s > 0);
+          for (int s = 0; s < D / 16; ++s) mma_ss(ts, qd + 16 * s, kst + 2 * s, id_s, s > 0);
           if (g >= nb) {
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s) mma_ss(tt, rd + 16 * s, kst + 16 * s, id_s, s > 0);
+            for (int s = 0; s < D / 16; ++s) mma_ss(tt, rd + 16 * s, kst + 2 * s, id_s, s > 0);
           }
           mma_commit(&bar.sfull[sb]);
           if (g < nb) mma_commit(&bar.kvempty[st]);  // max sweep: only Q K^T reads the stage
@@ -220,31 +227,31 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ K/V loader
-    // cp.async copies, every stage in flight (same conflict-free lane mapping as the LLA stages;
-    // each lane's copies of a block complete on the stage's barrier, and the MMA issuer fences
-    // the async proxy after its wait); V only in the main sweep.
-    const __nv_bfloat16* kbp = k + base * D;
-    const __nv_bfloat16* vbp = v + base * DV;
-    for (int g = 0; g < 2 * nb; ++g) {
-      {
+    // One thread: per block a TMA tensor copy of the 64 keys (and in the main sweep one of the 64
+    // values), completing on the stage's barrier kvfull (rows past the head read as zeros; keys
+    // past the tile's causal end are masked by the softmax warps).
+    if (lane == 0) {
+      tma_prefetch_map(&kmap);
+      tma_prefetch_map(&vmap);
+      int issued = 0;
+      for (int g = 0; g < 2 * nb; ++g) {
         const int st = g % KS, b = g < nb ? g : g - nb;
-        if (g >= KS && !warp_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, abort_p)) break;
-        uint8_t* kdst = smem + SM_K + st * KV_STAGE;
-        uint8_t* vdst = smem + SM_V + st * KV_STAGE;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int r = (lane & 7) + 8 * (t & 7), c = (lane >> 3) + 4 * (t >> 3);
-          const int j = b * KB + r;
-          const bool in = j < jend;
-          const long long jj = in ? j : 0;
-          cp_async16(kdst + kmaj_off(r, c), kbp + jj * D + c * 8, in ? 16u : 0u);
-          if (g >= nb) cp_async16(vdst + kmaj_off(r, c), vbp + jj * DV + c * 8, in ? 16u : 0u);
-        }
-        cp_async_mbar_arrive(&bar.kvfull[st]);  // this lane's copies of the block, on completion
+        if (g >= KS && !mbar_wait(&bar.kvempty[st], ((g / KS) - 1) & 1, status, TO, abort_p))
+          break;
+        const bool withv = g >= nb;
+        mbar_arrive_expect_tx(&bar.kvfull[st], withv ? 2 * KV_STAGE : KV_STAGE);
+        tma_load_3d(smem + SM_K + st * KV_STAGE, &kmap, 0, b * KB, (int)bh, &bar.kvfull[st]);
+        if (withv)
+          tma_load_3d(smem + SM_V + st * KV_STAGE, &vmap, 0, b * KB, (int)bh, &bar.kvfull[st]);
+        issued = g + 1;
       }
+      // Nothing may land in this CTA's shared memory after it exits: wait (bounded) for the
+      // copies of the last stages filled; a normal run finds them complete.
+      volatile int never = 0;
+      for (int g = issued > KS ? issued - KS : 0; g < issued; ++g)
+        mbar_wait(&bar.kvfull[g % KS], (g / KS) & 1, status, TO, &never);
     }
-    cp_async_commit();
-    cp_async_wait<0>();  // nothing of this warp is in flight at teardown
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ weights + output
     // Two warps per tensor-memory lane quarter (one thread per query row each): `hf` takes
@@ -279,10 +286,18 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.sfree[sb]);
       const int jb = (main_sweep ? h : g) * KB + 32 * hf;
+      // keys jb .. jb + 31 all at or before this row: no causal mask (rows past the tile's end
+      // have zero queries and finite logits, and nothing of theirs is stored)
+      const bool full = jb + 31 <= i;
       if (!main_sweep) {  // max sweep
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (valid && jb + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+          for (int c = 0; c < 32; ++c) m = fmaxf(m, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (valid && jb + c <= i) m = fmaxf(m, __uint_as_float(sv[c]));
+        }
         if (g == nb - 1) {  // the two halves' maxima
           xput(0, m);
           __syncwarp();
@@ -293,22 +308,31 @@ parallax_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         continue;
       }
       uint32_t pw[16], hw[16], lw[16];
+      auto weights = [&](auto masked) {
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float p0 = (valid && jb + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
-        const float p1 =
-            (valid && jb + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
-        const uint32_t w = pack_bf16(p0, p1);
-        pw[c / 2] = w;
-        const float r0 = bf16_lo(w), r1 = bf16_hi(w);
-        d1 += r0 + r1;
-        const float q0 = r0 * __uint_as_float(tv[c]);
-        const float q1 = r1 * __uint_as_float(tv[c + 1]);
-        d2 += q0 + q1;
-        const uint32_t hh = pack_bf16(q0, q1);
-        hw[c / 2] = hh;
-        lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
-      }
+        for (int c = 0; c < 32; c += 2) {
+          float p0, p1;
+          if constexpr (decltype(masked)::value) {
+            p0 = (valid && jb + c <= i) ? ex2(fmaf(__uint_as_float(sv[c]), c2, -mc)) : 0.f;
+            p1 = (valid && jb + c + 1 <= i) ? ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc)) : 0.f;
+          } else {
+            p0 = ex2(fmaf(__uint_as_float(sv[c]), c2, -mc));
+            p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc));
+          }
+          const uint32_t w = pack_bf16(p0, p1);
+          pw[c / 2] = w;
+          const float r0 = bf16_lo(w), r1 = bf16_hi(w);
+          d1 += r0 + r1;
+          const float q0 = r0 * __uint_as_float(tv[c]);
+          const float q1 = r1 * __uint_as_float(tv[c + 1]);
+          d2 += q0 + q1;
+          const uint32_t hh = pack_bf16(q0, q1);
+          hw[c / 2] = hh;
+          lw[c / 2] = pack_bf16(q0 - bf16_lo(hh), q1 - bf16_hi(hh));
+        }
+      };
+      if (full) weights(std::false_type{});
+      else weights(std::true_type{});
       // one P buffer: the previous block's P V MMAs must have completed
       if (h >= 1 && !warp_wait(&bar.pfree, (h - 1) & 1, status, abort_p)) break;
       tc_fence_after();
@@ -517,20 +541,41 @@ cudaError_t dispatch_d(const Args& a, const void* r, cudaStream_t s) {
 
 }  // namespace pcc
 
+// Tensor maps of the keys and values ([BH][T][64] bf16, boxes of 64 rows x 64 features, 128-byte
+// swizzled) for the tensor-core kernel.
+cudaError_t parallax_kv_maps(const void* k, const void* v, int T, long long BH, CUtensorMap* kmap,
+                             CUtensorMap* vmap) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint32_t ones[3] = {1, 1, 1};
+  const cuuint64_t dims[3] = {(cuuint64_t)ptc::D, (cuuint64_t)T, (cuuint64_t)BH};
+  const cuuint64_t str[2] = {(cuuint64_t)ptc::D * 2, (cuuint64_t)T * ptc::D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)ptc::D, (cuuint32_t)ptc::KB, 1};
+  static_assert(ptc::D == ptc::DV, "one tensor-map shape for keys and values");
+  for (int t = 0; t < 2; ++t)
+    if (encode(t ? vmap : kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(t ? v : k),
+               dims, str, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 // The backward's row scalars (bf16, d = dv = 64): the tensor-core forward with the STATS epilogue.
 cudaError_t launch_parallax_stats_tc(const ParallaxBwdArgs& a, float* stats, int* status,
                                      cudaStream_t s) {
+  CUtensorMap kmap, vmap;
+  cudaError_t err = parallax_kv_maps(a.k, a.v, a.T, a.BH(), &kmap, &vmap);
+  if (err != cudaSuccess) return err;
   auto kern = ptc::parallax_tc_kernel<true>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_BYTES);
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_LAUNCH);
   if (err != cudaSuccess) return err;
   const long long blocks = (long long)((a.T + ptc::BM - 1) / ptc::BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_BYTES, s>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-      static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(a.r), a.T,
+  kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_LAUNCH, s>>>(
+      static_cast<const __nv_bfloat16*>(a.q), kmap, vmap,
+      static_cast<const __nv_bfloat16*>(a.r), a.T,
       (int)a.BH(), 1.0f / a.h, nullptr, static_cast<const __nv_bfloat16*>(a.dout), stats, status);
   count_launch();
   return cudaGetLastError();
@@ -538,15 +583,17 @@ cudaError_t launch_parallax_stats_tc(const ParallaxBwdArgs& a, float* stats, int
 
 cudaError_t launch_parallax(const Args& a, const void* r, int path, int* status, cudaStream_t s) {
   if (path == kPathTensorCore && a.dtype == LLA_BF16 && a.d == 64 && a.dv == 64) {
+    CUtensorMap kmap, vmap;
+    cudaError_t err = parallax_kv_maps(a.k, a.v, a.T, a.BH(), &kmap, &vmap);
+    if (err != cudaSuccess) return err;
     auto kern = ptc::parallax_tc_kernel<false>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_BYTES);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM_LAUNCH);
     if (err != cudaSuccess) return err;
     const long long blocks = (long long)((a.T + ptc::BM - 1) / ptc::BM) * a.BH();
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_BYTES, s>>>(
-        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-        static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(r), a.T,
+    kern<<<(unsigned)blocks, ptc::NTHREADS, ptc::SMEM_LAUNCH, s>>>(
+        static_cast<const __nv_bfloat16*>(a.q), kmap, vmap, static_cast<const __nv_bfloat16*>(r),
+        a.T,
         (int)a.BH(), 1.0f / a.h, static_cast<__nv_bfloat16*>(a.out), nullptr, nullptr, status);
     count_launch();
     return cudaGetLastError();
