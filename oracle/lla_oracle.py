@@ -25,12 +25,25 @@ the intercept of this weighted ridge problem is the plainest reading of "the pre
 local linear estimator at q_i", and it agrees with the pages' additive-correction form and
 their softmax / affine limits, which the oracle's tests check.)
 
-The oracle solves that least-squares problem directly, one query at a time, with
-``numpy.linalg.lstsq`` on the square-root-weighted augmented design: no normal equations, no
-moments, no blocking. Multiplying the whole objective by ``exp(-m_i)`` with
-``m_i = max_j q_i . k_j / h`` leaves the minimiser unchanged and keeps ``exp`` finite; the
-ridge term is scaled by the same factor, so lambda stays absolute against the raw kernel
-weights ``exp(q . k / h)`` as written on the pages.
+The oracle solves that problem one query at a time in two exact textbook steps: no normal
+equations, no moments, no blocking. (1) The intercept is not penalised, so for any slope W the
+best b is ``vbar - W (kbar - q_i)`` with kbar, vbar the weighted means of the keys and values;
+putting it back leaves a ridge regression of the weighted-centred values on the
+weighted-centred keys, whose slope is ``W^T = V S (S^2 + lambda I)^-1 U^T Vw`` through the thin
+SVD ``Xw = U S V^T`` of the square-root-weighted centred keys Xw (Vw the same for the values).
+(2) The prediction is ``b = vbar + W (q_i - kbar)``. Multiplying the whole objective by
+``exp(-m_i)`` with ``m_i = max_j q_i . k_j / h`` leaves the minimiser unchanged and keeps
+``exp`` finite; the ridge term is scaled by the same factor, so lambda stays absolute against
+the raw kernel weights ``exp(q . k / h)`` as written on the pages.
+
+Singular values of Xw at the rounding level of the centring carry no data: the centring makes
+``sum_j w_j (k_j - kbar) = 0`` (one exact null vector), and linearly dependent keys add more; in
+exact arithmetic the values' part along them is zero, so the ridge solution gives them zero
+weight. Below ``eps * max(n, d) * |W^(1/2) K|_F`` they are cut (given zero weight) instead of
+dividing rounding noise by a ridge that may be far smaller than it (with lambda e^-m ~ 1e-22, as
+on early prefixes seen by a query aligned with a large common key offset). A joint least-squares
+solve over (b, W) instead would return, once sqrt(lambda e^-m) fell below its own rank cut, the
+minimum-norm (b, W) rather than this ridge limit.
 
 Parity pins: every function here is pinned by the CPU tests in ``tests/test_oracle_pins.py``
 (library routines, closed-form limits printed on the pages, invariants, brute force).
@@ -64,21 +77,20 @@ def lla_row(q_i: np.ndarray, K: np.ndarray, V: np.ndarray, h: float, lam: float)
     Minimises  sum_j w_j ||v_j - b - W (k_j - q_i)||^2 + lam ||W||_F^2  over (b, W) and returns b.
     """
     n, d = K.shape
-    e = V.shape[1]
     s = K @ q_i / h                      # logits q_i . k_j / h
     m = s.max()
     w = np.exp(s - m)                    # kernel weights times the common factor exp(-m)
     lam_t = lam * np.exp(-m)             # ridge scaled by the same factor
+    omega = w.sum()
+    kbar, vbar = w @ K / omega, w @ V / omega
     sw = np.sqrt(w)
-    # rows 0..n-1: sqrt(w_j) * [1, (k_j - q_i)^T] ; rows n..n+d-1: sqrt(lam_t) * [0, I]
-    A = np.zeros((n + d, d + 1))
-    A[:n, 0] = sw
-    A[:n, 1:] = sw[:, None] * (K - q_i[None, :])
-    A[n:, 1:] = np.sqrt(lam_t) * np.eye(d)
-    Bm = np.zeros((n + d, e))
-    Bm[:n] = sw[:, None] * V
-    x, *_ = np.linalg.lstsq(A, Bm, rcond=None)
-    return x[0]                          # the intercept b
+    Xw = sw[:, None] * (K - kbar)        # square-root-weighted centred keys   [n, d]
+    Vw = sw[:, None] * (V - vbar)        # square-root-weighted centred values [n, e]
+    U, S, Vt = np.linalg.svd(Xw, full_matrices=False)
+    cut = np.finfo(np.float64).eps * max(n, d) * np.linalg.norm(sw[:, None] * K)
+    f = np.where(S > cut, S / (S * S + lam_t), 0.0)
+    Wt = Vt.T @ (f[:, None] * (U.T @ Vw))  # the slope, transposed [d, e]
+    return vbar + (q_i - kbar) @ Wt        # the intercept b
 
 
 def _flatten(q, k, v):

@@ -151,6 +151,57 @@ def pin_constant_values(row_fn):
     return np.abs(o - c).max()
 
 
+def _offset_prefix(seed, n, d, e, offset):
+    """n keys N(0,1) + `offset` in every coordinate and a query aligned with that offset, so that
+    the max logit m is large and the effective ridge lambda e^-m tiny; values N(0,1)."""
+    K = rnd(seed, n, d) + offset
+    q = rnd(seed + 1, d) + offset / 8.0
+    V = rnd(seed + 2, n, e)
+    return q, K, V
+
+
+def pin_min_norm_interpolation(row_fn):
+    # Fewer keys than dimensions and lambda e^-m ~ 1e-100: the fit interpolates every key,
+    # b + W (k_j - q) = v_j, and the ridge picks the smallest |W|_F among the interpolants, whose
+    # closed form needs neither the weights nor the centring: W^T = pinv(K_{1:} - k_0) (V_{1:} - v_0),
+    # b = v_0 + W (q - k_0).
+    d, e, h, lam = 64, 8, 8.0, 1e-2
+    worst = 0.0
+    for seed, n in enumerate([2, 9, 24, 40]):
+        q, K, V = _offset_prefix(200 + 3 * seed, n, d, e, 16.0)
+        Wt = np.linalg.pinv(K[1:] - K[0]) @ (V[1:] - V[0])
+        ref = V[0] + (q - K[0]) @ Wt
+        worst = max(worst, np.abs(row_fn(q, K, V, h, lam) - ref).max() / np.abs(ref).max())
+    return worst
+
+
+def pin_exact_normal_equations(row_fn):
+    # The objective's stationarity conditions over (b, W), uncentred and unshifted (raw weights
+    # exp(q.k/h), absolute lambda), solved in 50-digit arithmetic: prefixes shorter than d under a
+    # tiny effective ridge, one with a moderate ridge and one longer than d.
+    mp = pytest.importorskip("mpmath")
+    worst = 0.0
+    with mp.workdps(50):
+        for seed, (n, d, e, h, lam, off) in enumerate([(4, 6, 2, 1.0, 1e-2, 12.0),
+                                                      (3, 5, 2, 0.5, 1e-3, 9.0),
+                                                      (5, 6, 3, 2.0, 0.3, 1.0),
+                                                      (9, 4, 2, 1.5, 1e-4, 6.0)]):
+            q, K, V = _offset_prefix(300 + 3 * seed, n, d, e, off)
+            X = mp.matrix([[1] + [mp.mpf(K[j, a]) - mp.mpf(q[a]) for a in range(d)]
+                           for j in range(n)])
+            w = [mp.exp(mp.fsum(mp.mpf(K[j, a]) * mp.mpf(q[a]) for a in range(d)) / h)
+                 for j in range(n)]
+            M = X.T * mp.diag(w) * X
+            for a in range(1, d + 1):
+                M[a, a] += lam
+            got = row_fn(q, K, V, h, lam)
+            for c in range(e):
+                rhs = X.T * mp.diag(w) * mp.matrix(V[:, c].tolist())
+                b = float(mp.lu_solve(M, rhs)[0])
+                worst = max(worst, abs(got[c] - b) / max(1.0, abs(b)))
+    return worst
+
+
 PINS = {
     "first_token": (pin_first_token, 1e-10),
     "large_ridge_softmax": (pin_large_ridge_softmax, 1e-8),
@@ -160,6 +211,8 @@ PINS = {
     "page_weighted_form": (pin_page_weighted_form, 1e-9),
     "additive_correction": (pin_additive_correction, 1e-9),
     "constant_values": (pin_constant_values, 1e-10),
+    "min_norm_interpolation": (pin_min_norm_interpolation, 1e-9),
+    "exact_normal_equations": (pin_exact_normal_equations, 1e-9),
 }
 
 
@@ -288,29 +341,48 @@ def test_moments_centred_form_reproduces_forward():
 
 
 def _mutant(kind):
+    """The oracle's row with one plausible mistake planted (or, for "joint_lstsq", the joint
+    least-squares solve over (b, W), which leaves the ridge limit once sqrt(lambda e^-m) falls
+    below its rank cut)."""
+    def joint(q_i, K, V, h, lam):
+        n, d = K.shape
+        s = K @ q_i / h
+        m = s.max()
+        sw = np.sqrt(np.exp(s - m))
+        A = np.zeros((n + d, d + 1))
+        A[:n, 0] = sw
+        A[:n, 1:] = sw[:, None] * (K - q_i[None, :])
+        A[n:, 1:] = np.sqrt(lam * np.exp(-m)) * np.eye(d)
+        Bm = np.zeros((n + d, V.shape[1]))
+        Bm[:n] = sw[:, None] * V
+        return np.linalg.lstsq(A, Bm, rcond=None)[0][0]
+
     def row(q_i, K, V, h, lam):
         n, d = K.shape
-        e = V.shape[1]
         s = K @ q_i / (h * h if kind == "h_squared" else h)
         m = s.max()
         w = np.exp(s - m)
         lam_t = {"lam_unscaled": lam, "lam_relative": lam * w.sum()}.get(kind, lam * np.exp(-m))
+        p = {"unweighted_means": np.full(n, 1.0 / n), "means_unnormalised": w}.get(kind, w / w.sum())
+        kbar, vbar = p @ K, p @ V
         sw = w if kind == "weights_squared" else np.sqrt(w)
-        A = np.zeros((n + d + 1, d + 1))
-        A[:n, 0] = sw
-        A[:n, 1:] = sw[:, None] * (K if kind == "uncentred" else (K - q_i[None, :]))
-        A[n:n + d, 1:] = (lam_t if kind == "ridge_not_sqrt" else np.sqrt(lam_t)) * np.eye(d)
-        if kind == "ridge_on_intercept":
-            A[n + d, 0] = np.sqrt(lam_t)
-        Bm = np.zeros((n + d + 1, e))
-        Bm[:n] = sw[:, None] * V
-        x, *_ = np.linalg.lstsq(A, Bm, rcond=None)
-        return x[0]
-    return row
+        Xw = sw[:, None] * (K - (q_i if kind == "keys_centred_at_query" else kbar))
+        Vw = sw[:, None] * (V - vbar)
+        U, S, Vt = np.linalg.svd(Xw, full_matrices=False)
+        cut = 0.0 if kind == "no_rank_cut" else \
+            np.finfo(np.float64).eps * max(n, d) * np.linalg.norm(sw[:, None] * K)
+        ridge = lam_t * lam_t if kind == "ridge_squared" else lam_t
+        f = np.where(S > cut, S / (S * S + ridge), 0.0)
+        Wt = Vt.T @ (f[:, None] * (U.T @ Vw))
+        sign = -1.0 if kind == "intercept_sign" else 1.0
+        return vbar + sign * (q_i - kbar) @ Wt
+    return joint if kind == "joint_lstsq" else row
 
 
 @pytest.mark.parametrize("kind", ["h_squared", "lam_unscaled", "lam_relative", "weights_squared",
-                                  "uncentred", "ridge_not_sqrt", "ridge_on_intercept"])
+                                  "unweighted_means", "means_unnormalised",
+                                  "keys_centred_at_query", "ridge_squared",
+                                  "intercept_sign", "no_rank_cut", "joint_lstsq"])
 def test_pins_catch_planted_mistakes(kind):
     row = _mutant(kind)
     failed = [name for name, (fn, tol) in PINS.items() if not fn(row) < tol]
