@@ -22,6 +22,39 @@ std::mutex g_dev_mu;
 int* g_status_ptr[kMaxDevices] = {};
 bool g_pool_ready[kMaxDevices] = {};
 
+// The exact pass over short rank-deficient prefixes (lla_short.cu) runs on a side stream of the
+// current device, concurrently with the readout: `fork` orders it after the solve on the call's
+// stream, `join` orders the rest of the call after it. One side stream and event pair per device,
+// created on first use, the stream at the device's highest priority: both grids become ready when
+// the solve ends, and the pass's CTAs (which cannot share an SM with a readout CTA) must be
+// dispatched before the readout's waves fill the GPU, not after them. g_side_mu is held from the
+// fork to the join's wait so that concurrent calls cannot wait on each other's records.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+// The current device's side stream (call with g_side_mu held).
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& sd = g_side[dev];
+  if (!sd.s) {
+    int least = 0, greatest = 0;
+    if ((err = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return err;
+    if ((err = cudaStreamCreateWithPriority(&sd.s, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+      return err;
+    if ((err = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return err;
+    if ((err = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return err;
+  }
+  *out = &sd;
+  return cudaSuccess;
+}
+
 // Address of the status word on the current device (resolved once per device).
 cudaError_t device_status(int** out) {
   int dev = 0;
@@ -172,7 +205,19 @@ int run_stages(const Args& a, void* base, cudaStream_t s, const Args* user) {
     if (i == 0 && user && launch_pad_inputs(*user, const_cast<void*>(a.q), const_cast<void*>(a.k),
                                             const_cast<void*>(a.v), s) != cudaSuccess)
       return LLA_ERR_CUDA;
-    if (stages[i](a, ws, s) != cudaSuccess) return LLA_ERR_CUDA;
+    if (i == LLA_NUM_STAGES - 1 && ws.path != kPathCG) {
+      // the readout, with the exact pass over the rows the solve listed beside it
+      std::lock_guard<std::mutex> lk(g_side_mu);
+      SideStream* sd = nullptr;
+      if (side_stream(&sd) != cudaSuccess || cudaEventRecord(sd->fork, s) != cudaSuccess ||
+          cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess ||
+          launch_short_prefix(a, ws, sd->s) != cudaSuccess ||
+          cudaEventRecord(sd->join, sd->s) != cudaSuccess || stages[i](a, ws, s) != cudaSuccess ||
+          cudaStreamWaitEvent(s, sd->join, 0) != cudaSuccess)
+        return LLA_ERR_CUDA;
+    } else if (stages[i](a, ws, s) != cudaSuccess) {
+      return LLA_ERR_CUDA;
+    }
     if (i == LLA_NUM_STAGES - 1 && user && launch_unpad_output(*user, a.out, s) != cudaSuccess)
       return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);
@@ -241,7 +286,9 @@ size_t workspace_bytes(const Args& a) {
     n += align_up(R * a.d * 2);                          // ksh
     n += align_up(BH * a.d * sizeof(float));             // kref
     n += align_up(BH * kKeyStatChunks * 2 * a.d * sizeof(float));  // kstat
-    n += align_up((1 + kMaxRepairRows) * sizeof(int));   // rep
+    n += align_up((2 + kMaxRepairRows) * sizeof(int));   // rep, then the short-row count
+  } else {
+    n += align_up(short_list_ints(a) * sizeof(int));     // short-row count and list
   }
   return n;
 }
@@ -266,7 +313,14 @@ void carve_workspace(const Args& a, void* base, Workspace* ws) {
   ws->ksh = tc ? reinterpret_cast<__nv_bfloat16*>(take(R * a.d * 2)) : nullptr;
   ws->kref = tc ? take(BH * a.d * sizeof(float)) : nullptr;
   ws->kstat = tc ? take(BH * kKeyStatChunks * 2 * a.d * sizeof(float)) : nullptr;
-  ws->rep = tc ? reinterpret_cast<int*>(take((1 + kMaxRepairRows) * sizeof(int))) : nullptr;
+  ws->rep = tc ? reinterpret_cast<int*>(take((2 + kMaxRepairRows) * sizeof(int))) : nullptr;
+  if (tc) {
+    ws->short_count = ws->rep + 1 + kMaxRepairRows;
+    ws->short_rows = reinterpret_cast<int*>(ws->kstat);
+  } else {
+    ws->short_count = reinterpret_cast<int*>(take(short_list_ints(a) * sizeof(int)));
+    ws->short_rows = ws->short_count + 1;
+  }
   ws->status = nullptr;
   ws->path = choose_path(a);
   ws->form = a.form;

@@ -67,7 +67,11 @@ struct Workspace {
   float* kref;         // [BH, d]    tensor-core path: the head's reference key c (bf16 values)
   float* kstat;        // [BH, kKeyStatChunks, 2, d]  partial sums of k and k^2 for choosing c
   int* rep;            // tensor-core path: [1 + kMaxRepairRows] count, then rows whose
-                       // factorisation the precise repair pass redoes
+                       // factorisation the precise repair pass redoes; one more int after them
+  int* short_count;    // rows listed for the exact pass (lla_short.cu) ...
+  int* short_rows;     // ... and their flat indices, at most BH * min(T, 64) (tensor-core path:
+                       // the int after rep's rows, and kstat, free once the key frame is chosen;
+                       // CUDA-core path: a region of its own)
   int* status;    // device status word of the current device
   int path;       // kPathCudaCore or kPathTensorCore: which moments stage (and layout) is used
   int form;       // kFormCentred or kFormPage: which closed form the solve and readout evaluate
@@ -135,11 +139,34 @@ constexpr int kKeyStatChunks = 16;
 // Rows per call whose tensor-core ridge factorisation may be redone by the precise repair pass
 // (more failing rows than this are reported as LLA_ERR_NUMERICAL and left NaN).
 constexpr int kMaxRepairRows = 4096;
+// Rows whose causal prefix holds at most kShortMaxKeys keys may be recomputed exactly
+// (lla_short.cu); the solve lists them: with at most d keys (the centred key covariance then has
+// rank below d), every row of an fp32 call and the rows of a bf16 call whose factorisation failed;
+// besides, any such row whose |y|_inf (|kbar - c|_1 + sqrt(d tr(C_kk) / omega)) -- the size of
+// k . y against which the readout's k . y - kbar . y must cancel -- exceeds kShortY (bf16) or
+// kShortY32 (fp32). Measured on bf16 inputs, rows below kShortY stay within about 1e-2 of the
+// exact output (about 1e-7 of the statistic at worst); rows above it (a tiny effective ridge with
+// the query far from kbar, as with a large common key offset) reached 0.11.
+constexpr int kShortMaxKeys = 64;
+constexpr float kShortY = 1e6f;
+constexpr float kShortY32 = 1e3f;
+// The solves mark a listed row for the readouts with this quiet-NaN pattern (in cy on the
+// tensor-core readout's input, in kbar[row][0] on the CUDA-core readout's): the readout then
+// leaves the row's output to the exact pass, which runs concurrently. A row whose solve failed
+// outright (repair list full) carries the plain NaN 0x7fc00000 instead and is stored as NaN.
+constexpr uint32_t kListedBits = 0x7fc0beefu;
 // The tensor-core stage may run for these sizes (whatever path is requested at call time).
 inline bool tc_eligible(const Args& a) { return a.dtype == LLA_BF16 && a.d == 64; }
 cudaError_t launch_solve(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout(const Args& a, const Workspace& ws, cudaStream_t s);
 cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s);
+// The exact pass over the rows the solve listed (after the readout; overwrites their output).
+cudaError_t launch_short_prefix(const Args& a, const Workspace& ws, cudaStream_t s);
+// Entries of the CUDA-core path's short-row region: the count, then at most
+// BH * min(T, kShortMaxKeys) rows.
+inline size_t short_list_ints(const Args& a) {
+  return 1 + (size_t)a.BH() * (size_t)(a.T < kShortMaxKeys ? a.T : kShortMaxKeys);
+}
 // The tensor-core readout pass with fp32 output, values `v` (bf16, [B,H,T,64]), y given as
 // three bf16 parts and kbar . y, tiles with tile_active[tile] == 0 skipped (null: none); matvec:
 // only the covariance branch (out = C_vk y, which is C_kk y for v = k).

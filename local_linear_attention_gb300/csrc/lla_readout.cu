@@ -155,7 +155,8 @@ readout_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* 
 #pragma unroll
   for (int r = 0; r < RPT; ++r) {
     const int rr = rg + r * C::NRG;
-    if (rr < nq) {
+    // a row listed for the exact pass (kbar[row][0] == kListedBits) is written by that pass
+    if (rr < nq && __float_as_uint(KBs[rr * D]) != kListedBits) {
       const long long o = (base + i0 + rr) * DV + ec * 4;
       const float inv = 1.f / om[r];
 #pragma unroll

@@ -284,6 +284,7 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const bool valid = r < nq;
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const float cy = valid ? cy_in[base + i] : 0.f;  // kbar . y (page form: q . rho*)
+    const bool store = valid && __float_as_uint(cy) != kListedBits;  // else the exact pass writes
     float om = 0.f, d2 = 0.f;
     bool ok = true;
     for (int c = 0; c < nck; ++c) {
@@ -347,7 +348,7 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (!kMatvec) tmem_ld16(lane_base + T_O1 + c0, o1);
         tmem_ld16(lane_base + T_O2 + c0, o2);
         tmem_ld_wait();
-        if (valid) {
+        if (store) {
 #pragma unroll
           for (int t = 0; t < 16; ++t)
             stf(out, (base + i) * DV + c0 + t,

@@ -27,8 +27,10 @@ namespace {
 template <typename TIn>
 __global__ void __launch_bounds__(256)
 mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, int DV,
-            float* __restrict__ kmean, float* __restrict__ vmean, int zero_keys) {
+            float* __restrict__ kmean, float* __restrict__ vmean, int zero_keys,
+            int* __restrict__ short_count) {
   extern __shared__ float red[];  // [256]
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *short_count = 0;  // this call's list
   const bool val = blockIdx.y == 1;
   const int W = val ? DV : D;
   const long long bh = blockIdx.x;
@@ -66,11 +68,14 @@ mean_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v, int T, int D, 
 // Partial sums of k and k^2 per feature over chunk blockIdx.y of head blockIdx.x (finite keys).
 __global__ void __launch_bounds__(256)
 key_stats_kernel(const __nv_bfloat16* __restrict__ k, int T, float* __restrict__ part,
-                 int* __restrict__ rep_count) {
+                 int* __restrict__ rep_count, int* __restrict__ short_count) {
   constexpr int D = 64;
   __shared__ float red[2][256];
   const int tid = threadIdx.x, a = tid & (D - 1), r0 = tid >> 6;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *rep_count = 0;  // this call's repair list
+  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {  // this call's repair and short lists
+    rep_count[0] = 0;
+    *short_count = 0;
+  }
   const long long bh = blockIdx.x;
   const int ch = blockIdx.y;
   const int t0 = (int)((long long)T * ch / kKeyStatChunks);
@@ -270,6 +275,7 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
              const float* __restrict__ mom, const float* __restrict__ mom_lo,
              const float* __restrict__ omega, const float* __restrict__ mrow, int T,
              long long rows, float lam, float* __restrict__ y_out, float* __restrict__ kbar_out,
+             int* __restrict__ short_count, int* __restrict__ short_rows,
              int* __restrict__ status) {
   using C = SolveCfg<D, PRECISE, FMT>;
   constexpr int NS = CholLane<D>::NS;
@@ -325,6 +331,7 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   rr[0] = L.rr0;
   if (NS == 2) rr[NS - 1] = L.rr1;
   float kb[NS];
+  float kb1 = 0.f, ctr = 0.f;  // this lane's share of |kbar|_1 and tr(C_kk) (short-prefix rule)
 #pragma unroll
   for (int t = 0; t < NS; ++t) {
     L.invd[t] = 1.f;
@@ -333,6 +340,8 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
     const R sr = M(r, D);
     const R kbar = sr * inv_om;
     kb[t] = (float)kbar;
+    kb1 += fabsf((float)kbar);
+    ctr += (float)(M(r, r) - sr * kbar);
     L.z[t] = (float)((R)ldf(q, row * D + r) - (R)kmean[bh * D + r] - kbar);
   }
 #pragma unroll
@@ -361,6 +370,25 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   // Factorisation, with the forward substitution (L z' = z) as an extra column.
   __syncwarp();  // every lane is done with the staged moments; the buffer now holds L's rows
   chol_column<D, 0>(L, colbuf);
+  // A prefix of at most d keys (rank-deficient centred covariance) goes to the exact pass
+  // (lla_short.cu), which writes its output: every such row of fp32 inputs; so does any prefix
+  // of at most kShortMaxKeys keys whose factorisation failed or whose |k . y| the readout could
+  // not cancel against kbar . y (kShortY, kShortY32). Its y is zero and kbar[row][0]
+  // kListedBits, which the readout skips.
+  constexpr bool kF32 = std::is_same<TIn, float>::value;
+  const int n_keys = (int)(row - bh * T) + 1;
+  const bool short_prefix = n_keys <= kShortMaxKeys;
+  auto list_short = [&]() {
+    if (lane == 0) short_rows[atomicAdd(short_count, 1)] = (int)row;
+    for (int a = lane; a < D; a += 32) {
+      y_out[row * D + a] = 0.f;
+      kbar_out[row * D + a] = a == 0 ? __uint_as_float(kListedBits) : 0.f;
+    }
+  };
+  if ((kF32 && n_keys <= D) || (short_prefix && !L.ok)) {
+    list_short();
+    return;
+  }
   if (!L.ok) {
     if (lane == 0) atomicOr(status, kStatusNumerical);
     const float qn = __int_as_float(0x7fc00000);
@@ -386,6 +414,21 @@ solve_kernel(const TIn* __restrict__ q, const float* __restrict__ kmean,
   // Backward substitution L^T y = z'.
   float w0 = L.z[0], w1 = L.z[NS - 1], y0 = 0.f, y1 = 0.f;
   back_column<D, D - 1>(L, Lrows, w0, w1, y0, y1);
+  if (short_prefix) {
+    float ymax = fmaxf(live0 ? fabsf(y0) : 0.f, NS == 2 ? fabsf(y1) : 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, o));
+      kb1 += __shfl_xor_sync(0xffffffffu, kb1, o);
+      ctr += __shfl_xor_sync(0xffffffffu, ctr, o);
+    }
+    // |kbar|_1 + sqrt(d tr(C_kk) / omega): the scale of the frame keys
+    const float kscale = kb1 + sqrtf(fmaxf((float)D * ctr * (float)inv_om, 0.f));
+    if (!(ymax * kscale <= (kF32 ? kShortY32 : kShortY))) {
+      list_short();
+      return;
+    }
+  }
   if (live0) {
     y_out[row * D + rr[0]] = y0;
     kbar_out[row * D + rr[0]] = kb[0];
@@ -475,7 +518,8 @@ constexpr int WARPS = 2;                   // warps per block, two queries each
 constexpr int QPB = 2 * WARPS;             // queries per block
 constexpr int LC = 2176;                   // packed factor
 // factor; (z', 1/L_kk) per column; y; 4 floats of padding, so that the two queries of a warp
-// start 16 bytes apart in the banks and their halves' column broadcasts do not conflict
+// start 16 bytes apart in the banks and their halves' column broadcasts do not conflict (the
+// first of them holds the query's key scale for the short-prefix rule)
 constexpr int Q_FLOATS = LC + 2 * D + D + 4;
 constexpr size_t SMEM_BYTES = sizeof(float) * QPB * Q_FLOATS;
 
@@ -591,6 +635,7 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
                  const float* __restrict__ mrow, long long rows, int T, float lam,
                  uint32_t* __restrict__ ytc, float* __restrict__ cy_out,
                  float* __restrict__ y_out, float* __restrict__ kbar_out, int* __restrict__ rep,
+                 int* __restrict__ short_count, int* __restrict__ short_rows,
                  int* __restrict__ status) {
   using namespace stc4;
   extern __shared__ float4 smem4[];
@@ -624,10 +669,13 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
   const int bh = (int)row / T;  // rows < 2^31
   float kb[4], qa[4], mu[4];
   const float inv_om = 1.f / om;
+  float kb1 = 0.f, ctr = 0.f;  // |kbar|_1 and tr(C_kk), for the key scale of the short-prefix rule
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float d = __ldcs(g + tc_slot(r[i], r[i])), x = __ldcs(g + run_base(r[i]) + r[i]);
     const float s = __ldcs(g + run_base(r[i]) + D);
+    kb1 += fabsf(s * inv_om);
+    ctr += fmaf(-s, s * inv_om, d);
     L.dg[i] = (d - x) + lp;  // x is d for even rows, the zero slot before the run for odd rows
     qa[i] = ldf(q, row * D + r[i]) - kref[bh * D + r[i]];
     mu[i] = fmaf(-om, qa[i], s);  // page form: mu = s - omega q
@@ -636,6 +684,14 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
     if (PAGE) muv[r[i]] = mu[i];
     L.z[i] = PAGE ? mu[i] : qa[i] - kb[i];
   }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    kb1 += __shfl_xor_sync(0xffffffffu, kb1, o);
+    ctr += __shfl_xor_sync(0xffffffffu, ctr, o);
+  }
+  // |kbar|_1 + sqrt(d tr(C_kk) / omega), at least |kbar|_1 + sum_a sqrt(C_aa / omega) (equal for
+  // isotropic keys); parked in the query's padding until the end
+  if (L.l == 0) Lc[LC + 3 * D] = kb1 + sqrtf(fmaxf(D * ctr * inv_om, 0.f));
   __syncwarp();
   // C_kk = S - s s^T / omega (page form: + mu mu^T / omega) on every array entry
 #pragma unroll
@@ -662,7 +718,6 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
     }
   }
   __syncwarp();  // s and mu are read; the area now takes (z', 1/L_kk)
-
   stc4::column<0>(L, Lc, zi, L.a0[0] + L.dg[0]);
   const unsigned fails = __ballot_sync(0xffffffffu, !L.ok);
   const bool my_fail = ((fails >> L.hb) & 0xFFFFu) != 0;
@@ -699,6 +754,33 @@ solve_tc_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ k
   }
   __syncwarp();
   uint32_t* yrow = ytc + row * 3 * (D / 2);
+  // A prefix of at most d keys whose factorisation failed, or whose |k . y| the readout could
+  // not cancel against kbar . y (kShortY), goes to the exact pass (lla_short.cu), which writes
+  // its output; its y is zero and its cy (kbar[row][0] for a CUDA-core readout) kListedBits.
+  bool short_row = false;
+  if ((int)(row - (long long)bh * T) + 1 <= D) {
+    const float4 t4 = *reinterpret_cast<const float4*>(ys + 4 * L.l);  // y[4l .. 4l + 3]
+    float ymax = fmaxf(fmaxf(fabsf(t4.x), fabsf(t4.y)), fmaxf(fabsf(t4.z), fabsf(t4.w)));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) ymax = fmaxf(ymax, __shfl_xor_sync(0xffffffffu, ymax, o));
+    short_row = my_fail || !(ymax * Lc[LC + 3 * D] <= kShortY);
+  }
+  if (short_row) {
+    if (!live) return;
+    if (L.l == 0) {
+      short_rows[atomicAdd(short_count, 1)] = (int)row;
+      cy_out[row] = __uint_as_float(kListedBits);
+    }
+    reinterpret_cast<uint2*>(yrow)[L.l] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2*>(yrow + D / 2)[L.l] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2*>(yrow + D)[L.l] = make_uint2(0u, 0u);
+    if (y_out)
+      for (int i = 0; i < 4; ++i) {
+        y_out[row * D + r[i]] = 0.f;
+        kbar_out[row * D + r[i]] = r[i] == 0 ? __uint_as_float(kListedBits) : 0.f;
+      }
+    return;
+  }
   if (my_fail) {
     // A non-positive pivot: the query goes to the precise repair pass (repair_kernel), which
     // overwrites its y; if the repair list is full, the query is NaN.
@@ -965,7 +1047,8 @@ cudaError_t launch_solve_tc(const Args& a, const Workspace& ws, cudaStream_t s) 
   kern<<<(unsigned)blocks, stc4::WARPS * 32, stc4::SMEM_BYTES, s>>>(
       static_cast<const __nv_bfloat16*>(a.q), ws.kref, ws.mom, ws.omega, ws.m, rows, a.T, a.lam,
       ws.ytc, ws.cy,
-      a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.rep, ws.status);
+      a.dv == 64 ? nullptr : ws.y, a.dv == 64 ? nullptr : ws.kbar, ws.rep, ws.short_count,
+      ws.short_rows, ws.status);
   count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -988,7 +1071,7 @@ cudaError_t launch_solve_t(const Args& a, const Workspace& ws, cudaStream_t s) {
   const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
   kern<<<(unsigned)blocks, kWarpsPerBlock * 32, smem, s>>>(
       static_cast<const TIn*>(a.q), ws.kmean, ws.mom, ws.mom_lo, ws.omega, ws.m, a.T, rows, a.lam,
-      ws.y, ws.kbar, ws.status);
+      ws.y, ws.kbar, ws.short_count, ws.short_rows, ws.status);
   count_launch();
   return cudaGetLastError();
 }
@@ -999,7 +1082,7 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
   if (ws.path == kPathTensorCore) {  // the keys in the head's frame (see key_stats_kernel)
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
     key_stats_kernel<<<dim3((unsigned)a.BH(), kKeyStatChunks), 256, 0, s>>>(k, a.T, ws.kstat,
-                                                                          ws.rep);
+                                                                          ws.rep, ws.short_count);
     count_launch();
     shift_keys_kernel<<<dim3((unsigned)a.BH(), kShiftChunks), 256, 0, s>>>(k, a.T, ws.kstat,
                                                                            ws.kref, ws.ksh);
@@ -1014,11 +1097,11 @@ cudaError_t launch_prep(const Args& a, const Workspace& ws, cudaStream_t s) {
   if (a.dtype == LLA_F32)
     mean_kernel<float><<<grid, 256, 256 * sizeof(float), s>>>(
         static_cast<const float*>(a.k), static_cast<const float*>(a.v), a.T, a.d, a.dv, ws.kmean,
-        ws.vmean, ws.path == kPathTensorCore);
+        ws.vmean, ws.path == kPathTensorCore, ws.short_count);
   else
     mean_kernel<__nv_bfloat16><<<grid, 256, 256 * sizeof(float), s>>>(
         static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v), a.T, a.d,
-        a.dv, ws.kmean, ws.vmean, ws.path == kPathTensorCore);
+        a.dv, ws.kmean, ws.vmean, ws.path == kPathTensorCore, ws.short_count);
   count_launch();
   cudaError_t err = cudaGetLastError();
   // The CUDA-core readout after the tensor-core solve (dv != 64) works in the solve's key frame.

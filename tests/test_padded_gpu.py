@@ -72,6 +72,6 @@ def test_padded_launches_and_stream_order(lla):
     with torch.cuda.stream(s):
         out = lla.lla_forward(q, k, v, float(np.sqrt(32)), 1e-2)
     s.synchronize()
-    assert lla.launch_count() - n0 == 7 + 2
+    assert lla.launch_count() - n0 == 8 + 2
     assert lla.lla_stream_status() == 0
     assert torch.isfinite(out).all() and out.shape == (1, 2, 256, 32)

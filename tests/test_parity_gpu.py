@@ -206,5 +206,6 @@ def test_profiling_and_launch_count(lla):
     assert calls == 3 and all(t >= 0 for t in stages.values())
     assert all(stages[s] > 0 for s in ("prep", "weights", "moments", "solve", "readout"))
     # bf16, d = dv = 64: the key frame (statistics, shifted keys), the weights, the moment
-    # contraction, the solve and its repair pass (empty here), the readout
-    assert lla.launch_count() - n0 == 3 * 7
+    # contraction, the solve and its repair pass (empty here), the readout and its exact pass
+    # over short rank-deficient prefixes (empty here)
+    assert lla.launch_count() - n0 == 3 * 8
