@@ -5,6 +5,8 @@
 // Canonical Formulation)
 //   o_i = vbar_i + C_vk y_i = O1_i / omega_i + O2_i,
 //   O1 = P V,  O2 = (P .* t) V,  t_ij = k_j . y_i - kbar_i . y_i,
+// and, since omega_i (the sum of the rounded weights) is known before this pass, as one product
+//   o_i = (P .* A) V,  a_ij = 1 / omega_i + t_ij  (kFused: the centred form's bf16 output),
 // where P holds the kernel weights exactly as the moments stage rounded them: the pass reads them
 // back from the moments stage's weight scratch (bf16 images already in the layout of a tcgen05
 // operand), so the fitted moments and this pass describe one weighted problem (and
@@ -16,7 +18,8 @@
 // outside the span of the keys must cancel between k_j . y and kbar . y; y therefore enters the
 // Y K^T contraction as three exact bf16 parts (y = y1 + y2 + y3, 24 significant bits; the solve
 // writes them, with cy = kbar . y), and the covariance-branch weights p * t enter P2 V as an
-// exact-to-16-bits hi/lo pair.
+// exact-to-16-bits hi/lo pair (kFused: the fused weights p * (1/omega + t) as that pair, which
+// rounds the softmax part p / omega to 2^-17 of |p (1/omega + t)|, ~1e-5 of the output).
 //
 // With the page form of the solve (y := rho* = Sigma^-1 mu, cy := q . rho*; kPage), t_ij is the
 // page's z_ij . rho* with z = k - q, and the same two branches give the page's exact-LLA epilogue
@@ -106,12 +109,14 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 256, "barrier region");
 
-template <typename TOut, bool kMatvec, bool kPage>
+template <typename TOut, bool kMatvec, bool kPage, bool kFused>
 __global__ void __launch_bounds__(NTHREADS, 1)
 readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const uint4* __restrict__ pimg, const uint32_t* __restrict__ ytc,
-                  const float* __restrict__ cy_in, int T, int BH, TOut* __restrict__ out,
-                  const int* __restrict__ tile_active, int* __restrict__ status) {
+                  const float* __restrict__ cy_in, const float* __restrict__ omega_in, int T,
+                  int BH, TOut* __restrict__ out, const int* __restrict__ tile_active,
+                  int* __restrict__ status) {
+  static_assert(!kFused || (!kMatvec && !kPage), "the fused product is the centred form's");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + SM_BAR);
@@ -230,7 +235,7 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
           // keys 16s..16s+15: image s / 2, K-adjacent core matrices 2 (s % 2), 2 (s % 2) + 1
           const uint64_t pds = pst + (uint64_t)((s >> 1) * (pscr::kBlockBytes >> 4) + (s & 1) * (4096 >> 4));
           const uint32_t acc = (c > 0 || s > 0) ? 1u : 0u;
-          if (!kMatvec) mma_ss(tbase + T_O1, pds, vds, id_o, acc);
+          if (!kMatvec && !kFused) mma_ss(tbase + T_O1, pds, vds, id_o, acc);
           mma_ts(tbase + T_O2, tbase + T_P2H + pb * (CK / 2) + s * 8, vds, id_o, acc);
           mma_ts(tbase + T_O2, tbase + T_P2L + pb * (CK / 2) + s * 8, vds, id_o, 1u);
         }
@@ -285,6 +290,7 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const float cy = valid ? cy_in[base + i] : 0.f;  // kbar . y (page form: q . rho*)
     const bool store = valid && __float_as_uint(cy) != kListedBits;  // else the exact pass writes
+    const float inv_om = kFused && valid ? 1.f / omega_in[base + i] : 0.f;
     float om = 0.f, d2 = 0.f;
     bool ok = true;
     for (int c = 0; c < nck; ++c) {
@@ -314,9 +320,9 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         for (int u = 0; u < 4; ++u) {
           const int j = 8 * kc + 2 * u;
           const float r0 = bf16_lo(pw[u]), r1 = bf16_hi(pw[u]);
-          om += r0 + r1;
-          const float q0 = r0 * (__uint_as_float(tv[j]) - cy);
-          const float q1 = r1 * (__uint_as_float(tv[j + 1]) - cy);
+          if (!kFused) om += r0 + r1;
+          const float q0 = r0 * ((__uint_as_float(tv[j]) - cy) + inv_om);
+          const float q1 = r1 * ((__uint_as_float(tv[j + 1]) - cy) + inv_om);
           if (kPage) d2 += q0 + q1;
           const uint32_t hh = pack_bf16(q0, q1);
           hw[j / 2] = hh;
@@ -345,14 +351,14 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 #pragma unroll
       for (int c0 = 0; c0 < DV; c0 += 16) {
         uint32_t o1[16], o2[16];
-        if (!kMatvec) tmem_ld16(lane_base + T_O1 + c0, o1);
+        if (!kMatvec && !kFused) tmem_ld16(lane_base + T_O1 + c0, o1);
         tmem_ld16(lane_base + T_O2 + c0, o2);
         tmem_ld_wait();
         if (store) {
 #pragma unroll
           for (int t = 0; t < 16; ++t)
             stf(out, (base + i) * DV + c0 + t,
-                kMatvec ? __uint_as_float(o2[t])
+                (kMatvec || kFused) ? __uint_as_float(o2[t])
                 : kPage ? (__uint_as_float(o1[t]) - __uint_as_float(o2[t])) * inv
                         : fmaf(__uint_as_float(o1[t]), inv, __uint_as_float(o2[t])));
         }
@@ -375,7 +381,7 @@ readout_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   }
 }
 
-template <typename TOut, bool kMatvec, bool kPage = false>
+template <typename TOut, bool kMatvec, bool kPage = false, bool kFused = false>
 cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const void* keys,
                       const void* v, const uint32_t* ytc, const float* cy, TOut* out,
                       const int* tile_active) {
@@ -394,15 +400,15 @@ cudaError_t launch_ro(const Args& a, const Workspace& ws, cudaStream_t s, const 
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  auto kern = readout_tc_kernel<TOut, kMatvec, kPage>;
+  auto kern = readout_tc_kernel<TOut, kMatvec, kPage, kFused>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LAUNCH);
   if (err != cudaSuccess) return err;
   const long long blocks = (long long)((a.T + BM - 1) / BM) * a.BH();
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)blocks, NTHREADS, SMEM_LAUNCH, s>>>(
-      kmap, vmap, static_cast<const uint4*>(ws.pscr), ytc, cy, a.T, (int)a.BH(), out, tile_active,
-      ws.status);
+      kmap, vmap, static_cast<const uint4*>(ws.pscr), ytc, cy, ws.omega, a.T, (int)a.BH(), out,
+      tile_active, ws.status);
   count_launch();
   return cudaGetLastError();
 }
@@ -416,7 +422,8 @@ cudaError_t launch_readout_tc(const Args& a, const Workspace& ws, cudaStream_t s
   return ws.form == kFormPage
              ? launch_ro<__nv_bfloat16, false, true>(a, ws, s, keys, a.v, ws.ytc, ws.cy, out,
                                                      nullptr)
-             : launch_ro<__nv_bfloat16, false>(a, ws, s, keys, a.v, ws.ytc, ws.cy, out, nullptr);
+             : launch_ro<__nv_bfloat16, false, false, true>(a, ws, s, keys, a.v, ws.ytc, ws.cy, out,
+                                                            nullptr);
 }
 
 cudaError_t launch_readout_tc_f32(const Args& a, const Workspace& ws, cudaStream_t s,
