@@ -117,6 +117,12 @@ typedef struct lla_options {
  * Scratch memory is taken from the CUDA stream-ordered allocator on `stream`
  * (cudaMallocAsync/cudaFreeAsync, released at the end of the call in stream order);
  * lla_workspace_size() tells how much. Use lla_forward_ws() to supply it yourself.
+ * Rows whose causal prefix holds few keys may be recomputed exactly in float64 (the solve lists
+ * them); that pass runs on a library-owned side stream of the current device, at its highest
+ * priority, ordered after this call's solve and before the rest of the call by two events, so
+ * that to the caller the whole call is still ordered on `stream`. The side stream and its events
+ * are created on a device's first forward call (make that call before any stream capture); a
+ * call captured into a CUDA graph forks to the side stream and joins back within the capture.
  */
 int lla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T,
                 int d, int dv, float h, float lambda, int dtype, void* stream);
@@ -189,7 +195,8 @@ int lla_forward_ex(const void* q, const void* k, const void* v, void* out, int B
  *   d = dv = 64 fits T <= 4343 at B*H = 1 and T <= 704 at B*H = 8; the tensor-core path's weight
  *   scratch grows with B*H*T^2). Other argument errors are those of lla_forward.
  * - Set-up: the first call on each device looks up the scratch array's device address (with that
- *   device current) and caches it; make that first call before any stream capture.
+ *   device current) and caches it, and (as any first forward call) creates the side stream of the
+ *   exact short-prefix pass; make that first call before any stream capture.
  * - Sharing: all calls on a device share the one array. Calls whose work overlaps on the GPU
  *   (other streams, other host threads, without ordering between them) race on it and corrupt
  *   each other's results; order them on one stream or synchronise between them. Each call

@@ -93,3 +93,24 @@ def test_short_prefixes_with_repeated_keys(lla, dtype):
     for j in range(5, 64, 7):
         k[:, :, j] = k[:, :, j - 4]
     check(lla, q, k, v, 8.0, 1e-2, dtype)
+
+
+@pytest.mark.gpu
+def test_forward_with_listed_rows_replays_from_a_cuda_graph(lla):
+    """The exact pass runs on the library's side stream, forked after the solve and joined after
+    the readout; captured into a CUDA graph (rows listed: large common key offset), the fork and
+    join stay inside the capture and a replay reproduces the eager call bit for bit."""
+    q, k, v = (t.cuda() for t in offset_inputs(1001, 64, 16.0, "all", "bf16"))
+    out = torch.empty_like(v)
+    lla.lla_forward(q, k, v, 8.0, 1e-2, out=out)  # first call: creates the side stream
+    torch.cuda.synchronize()
+    ref = out.clone()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        lla.lla_forward(q, k, v, 8.0, 1e-2, out=out, stream=s)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert lla.lla_stream_status() == 0
+    assert torch.equal(out, ref)
