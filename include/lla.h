@@ -106,9 +106,11 @@ typedef struct lla_options {
 } lla_options;
 
 /* Number of timed stages recorded per lla_forward call by the profiling hooks below:
- * 0 prep (per-head means, CUDA-core path), 1 weights (tensor-core path: row maxima, the weights
- * and their sums), 2 moments (the moment contraction; on the CUDA-core path also the weights),
- * 3 solve, 4 readout. A stage that a path does not have records zero time. */
+ * 0 prep (per-head means, CUDA-core path; the tensor-core path's key frame runs beside stage 1
+ * and is counted there), 1 weights (tensor-core path: row maxima, the weights and their sums),
+ * 2 moments (the moment contraction; on the CUDA-core path also the weights), 3 solve,
+ * 4 readout (with the exact pass over listed short prefixes beside it). A stage that a path does
+ * not have records zero time. */
 #define LLA_NUM_STAGES 5
 
 /*

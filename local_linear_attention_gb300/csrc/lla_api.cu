@@ -201,23 +201,33 @@ int run_stages(const Args& a, void* base, cudaStream_t s, const Args* user) {
     };
     stages[4] = launch_readout_tc;
   }
+  // `main` on the call's stream with `side` beside it on the side stream: both ordered after
+  // what the call's stream has enqueued so far, and the rest of the call after both.
+  auto beside = [&](cudaError_t (*main)(const Args&, const Workspace&, cudaStream_t),
+                    cudaError_t (*side)(const Args&, const Workspace&, cudaStream_t)) {
+    std::lock_guard<std::mutex> lk(g_side_mu);
+    SideStream* sd = nullptr;
+    return side_stream(&sd) == cudaSuccess && cudaEventRecord(sd->fork, s) == cudaSuccess &&
+           cudaStreamWaitEvent(sd->s, sd->fork, 0) == cudaSuccess &&
+           side(a, ws, sd->s) == cudaSuccess && cudaEventRecord(sd->join, sd->s) == cudaSuccess &&
+           main(a, ws, s) == cudaSuccess && cudaStreamWaitEvent(s, sd->join, 0) == cudaSuccess;
+  };
   for (int i = 0; i < LLA_NUM_STAGES; ++i) {
     if (i == 0 && user && launch_pad_inputs(*user, const_cast<void*>(a.q), const_cast<void*>(a.k),
                                             const_cast<void*>(a.v), s) != cudaSuccess)
       return LLA_ERR_CUDA;
-    if (i == LLA_NUM_STAGES - 1 && ws.path != kPathCG) {
+    bool ok = true;
+    if (tc && i == 0) {
+      // the key frame runs beside the weight sweeps, which read the original keys (stage 1)
+    } else if (tc && i == 1) {
+      ok = beside(stages[1], stages[0]);
+    } else if (i == LLA_NUM_STAGES - 1 && ws.path != kPathCG) {
       // the readout, with the exact pass over the rows the solve listed beside it
-      std::lock_guard<std::mutex> lk(g_side_mu);
-      SideStream* sd = nullptr;
-      if (side_stream(&sd) != cudaSuccess || cudaEventRecord(sd->fork, s) != cudaSuccess ||
-          cudaStreamWaitEvent(sd->s, sd->fork, 0) != cudaSuccess ||
-          launch_short_prefix(a, ws, sd->s) != cudaSuccess ||
-          cudaEventRecord(sd->join, sd->s) != cudaSuccess || stages[i](a, ws, s) != cudaSuccess ||
-          cudaStreamWaitEvent(s, sd->join, 0) != cudaSuccess)
-        return LLA_ERR_CUDA;
-    } else if (stages[i](a, ws, s) != cudaSuccess) {
-      return LLA_ERR_CUDA;
+      ok = beside(stages[i], launch_short_prefix);
+    } else {
+      ok = stages[i](a, ws, s) == cudaSuccess;
     }
+    if (!ok) return LLA_ERR_CUDA;
     if (i == LLA_NUM_STAGES - 1 && user && launch_unpad_output(*user, a.out, s) != cudaSuccess)
       return LLA_ERR_CUDA;
     if (prof) cudaEventRecord(rec.ev[i + 1], s);

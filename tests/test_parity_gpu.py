@@ -204,7 +204,8 @@ def test_profiling_and_launch_count(lla):
     lla.profile_enable(False)
     stages, calls = lla.profile_collect()
     assert calls == 3 and all(t >= 0 for t in stages.values())
-    assert all(stages[s] > 0 for s in ("prep", "weights", "moments", "solve", "readout"))
+    # the key frame (prep) runs beside the weight sweeps on the side stream and is timed with them
+    assert all(stages[s] > 0 for s in ("weights", "moments", "solve", "readout"))
     # bf16, d = dv = 64: the key frame (statistics, shifted keys), the weights, the moment
     # contraction, the solve and its repair pass (empty here), the readout and its exact pass
     # over short rank-deficient prefixes (empty here)
