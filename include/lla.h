@@ -33,8 +33,11 @@
  * - Errors: every call returns an lla_status. Argument errors are detected on the host before
  *   any work is enqueued and leave all buffers untouched. Numerical failures inside a kernel
  *   (a non-positive pivot in a ridge solve, e.g. from non-finite inputs) are recorded in a
- *   per-device status word read by lla_stream_status(); the affected output rows are NaN.
- *   No entry point aborts, traps or exits.
+ *   per-device status word read by lla_stream_status(); the affected output rows are NaN. (The
+ *   forward first retries such a row: in float64 from its moments on the tensor-core path, or,
+ *   when its causal prefix holds at most 64 keys, exactly from q, k and v; only a row that still
+ *   fails -- non-finite inputs, or a longer prefix with fewer than d + 1 affinely independent
+ *   keys under a tiny effective ridge -- is reported.) No entry point aborts, traps or exits.
  * - Supported sizes: d, dv in {16, 32, 64}; B, H, T >= 0 with B*H*T < 2^31 (B*H*T == 0 is a
  *   no-op that returns LLA_OK); h > 0 and lambda > 0, both finite.
  */

@@ -1,9 +1,9 @@
 // Exact outputs of early rows with short causal prefixes (the forward, both paths).
 //
 // With n <= d keys the centred key covariance C_kk has rank below d (and with a few more it is
-// nearly singular), and the primal ridge
-// solution y = (C_kk + lambda' I)^-1 (q - kbar) carries a component outside the keys' span of
-// size about |q - kbar| / lambda' (lambda' = lambda e^-m, the ridge of the max-shifted weights),
+// nearly singular), and the primal ridge solution y = (C_kk + lambda' I)^-1 (q - kbar) carries a
+// component outside the keys' span of size about |q - kbar| / lambda' (lambda' = lambda e^-m, the
+// ridge of the max-shifted weights),
 // which the readout's k . y - kbar . y must cancel: fp32 cannot once lambda' is small against
 // |q - kbar| |k| (a large common key offset seen by an aligned query makes m large), and the fp32
 // factorisation of the nearly singular system may fail outright. The same intercept of the
