@@ -27,29 +27,42 @@ bool g_pool_ready[kMaxDevices] = {};
 // stream, `join` orders the rest of the call after it. One side stream and event pair per device,
 // created on first use, the stream at the device's highest priority: both grids become ready when
 // the solve ends, and the pass's CTAs (which cannot share an SM with a readout CTA) must be
-// dispatched before the readout's waves fill the GPU, not after them. g_side_mu is held from the
-// fork to the join's wait so that concurrent calls cannot wait on each other's records.
+// dispatched before the readout's waves fill the GPU, not after them. The device's `mu` is held
+// from the fork to the join's wait so that concurrent calls cannot wait on each other's records.
+// The stream and events live until the process exits.
 struct SideStream {
+  std::mutex mu;
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-std::mutex g_side_mu;
+std::mutex g_side_mu;  // guards creation
 SideStream g_side[kMaxDevices];
 
-// The current device's side stream (call with g_side_mu held).
+// The current device's side stream, created on first use (all three objects, or none).
 cudaError_t side_stream(SideStream** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   SideStream& sd = g_side[dev];
+  std::lock_guard<std::mutex> lk(g_side_mu);
   if (!sd.s) {
     int least = 0, greatest = 0;
-    if ((err = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return err;
-    if ((err = cudaStreamCreateWithPriority(&sd.s, cudaStreamNonBlocking, greatest)) != cudaSuccess)
+    cudaStream_t st = nullptr;
+    cudaEvent_t ef = nullptr, ej = nullptr;
+    err = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (err == cudaSuccess) err = cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ef, cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ej, cudaEventDisableTiming);
+    if (err != cudaSuccess) {
+      if (ej) cudaEventDestroy(ej);
+      if (ef) cudaEventDestroy(ef);
+      if (st) cudaStreamDestroy(st);
       return err;
-    if ((err = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess) return err;
-    if ((err = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess) return err;
+    }
+    sd.fork = ef;
+    sd.join = ej;
+    sd.s = st;
   }
   *out = &sd;
   return cudaSuccess;
@@ -205,9 +218,10 @@ int run_stages(const Args& a, void* base, cudaStream_t s, const Args* user) {
   // what the call's stream has enqueued so far, and the rest of the call after both.
   auto beside = [&](cudaError_t (*main)(const Args&, const Workspace&, cudaStream_t),
                     cudaError_t (*side)(const Args&, const Workspace&, cudaStream_t)) {
-    std::lock_guard<std::mutex> lk(g_side_mu);
     SideStream* sd = nullptr;
-    return side_stream(&sd) == cudaSuccess && cudaEventRecord(sd->fork, s) == cudaSuccess &&
+    if (side_stream(&sd) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(sd->mu);
+    return cudaEventRecord(sd->fork, s) == cudaSuccess &&
            cudaStreamWaitEvent(sd->s, sd->fork, 0) == cudaSuccess &&
            side(a, ws, sd->s) == cudaSuccess && cudaEventRecord(sd->join, sd->s) == cudaSuccess &&
            main(a, ws, s) == cudaSuccess && cudaStreamWaitEvent(s, sd->join, 0) == cudaSuccess;
