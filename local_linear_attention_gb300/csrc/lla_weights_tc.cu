@@ -268,7 +268,8 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ C
       __syncwarp();
       if (lane == 0) arrive_leader(&bar.qready, leader);
     }
-    float m = -INFINITY, om = 0.f;
+    float m = -INFINITY;
+    float2 om2 = make_float2(0.f, 0.f);  // omega as two partial sums (packed fp32 adds)
     bool ok = true;
     // Sweep chunk u covers key blocks b0 .. b0 + SCH - 1. Column n of its S buffer holds key
     // 16 (n / 64) + n % 16 of block (n % 64) / 16 (the pair's B operand: 64 rows from each CTA),
@@ -318,34 +319,38 @@ weights_tc_kernel(const __nv_bfloat16* __restrict__ q, const __grid_constant__ C
           }
           continue;
         }
-        const float mc = m * c2;
+        // exponents (s - m) c2 of a key pair in one packed fp32 FMA, the rounded weights' sum in
+        // packed fp32 adds (the softmax warps are issue-bound)
+        const float2 c22 = make_float2(c2, c2), nmc2 = make_float2(-m * c2, -m * c2);
         uint32_t pw[4];
         if (full) {
 #pragma unroll
-          for (int c = 0; c < 8; c += 2)
-            pw[c / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)),
-                                  ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc)));
+          for (int c = 0; c < 8; c += 2) {
+            const float2 e = __ffma2_rn(
+                make_float2(__uint_as_float(sv[t][c]), __uint_as_float(sv[t][c + 1])), c22, nmc2);
+            pw[c / 2] = pack_bf16(ex2(e.x), ex2(e.y));
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < 8; c += 2) {
-            const float p0 =
-                (valid && j0 + c <= i) ? ex2(fmaf(__uint_as_float(sv[t][c]), c2, -mc)) : 0.f;
-            const float p1 = (valid && j0 + c + 1 <= i)
-                                 ? ex2(fmaf(__uint_as_float(sv[t][c + 1]), c2, -mc))
-                                 : 0.f;
+            const float2 e = __ffma2_rn(
+                make_float2(__uint_as_float(sv[t][c]), __uint_as_float(sv[t][c + 1])), c22, nmc2);
+            const float p0 = (valid && j0 + c <= i) ? ex2(e.x) : 0.f;
+            const float p1 = (valid && j0 + c + 1 <= i) ? ex2(e.y) : 0.f;
             pw[c / 2] = pack_bf16(p0, p1);
           }
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          om += __uint_as_float(pw[c] << 16) + __uint_as_float(pw[c] & 0xFFFF0000u);
+          om2 = __fadd2_rn(om2, make_float2(__uint_as_float(pw[c] << 16),
+                                            __uint_as_float(pw[c] & 0xFFFF0000u)));
         // This row's 8 weights as chunk `part` of the block's image.
         ptile_p[(long long)b * (P_BLOCK / 16) + part * kChunk + r] =
             make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
     }
     if (ok) {  // combine the parts' omega
-      bar.part_o[part][r] = om;
+      bar.part_o[part][r] = om2.x + om2.y;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.rowx);
       if (warp_wait(&bar.rowx, 1, status, TO, abort_p) && part == 0 && valid) {
