@@ -277,7 +277,8 @@ class OracleTimer:
             self.per_row = wall / len(rows)
             if wall >= 0.5 * budget_s or n >= w.queries:
                 break
-        how = ("one float64 lstsq per row" if self.op == "lla"
+        how = ("one float64 ridge solve per row (SVD of the weighted centred keys)"
+               if self.op == "lla"
                else "float64 softmax weights and explicit covariance per row")
         sample = (f"{len(rows)} uniformly sampled query rows of {w.describe()} (of {w.queries}), "
                   f"{how}, {self.cores} single-threaded processes, {wall:.1f} s")

@@ -321,7 +321,7 @@ def test_moments_first_query_and_loops():
 
 
 def test_moments_centred_form_reproduces_forward():
-    """vbar + C_vk (C_kk + lam e^-m I)^-1 (q - kbar) from the moments equals the lstsq oracle."""
+    """vbar + C_vk (C_kk + lam e^-m I)^-1 (q - kbar) from the moments equals the oracle."""
     T, d, e, h, lam = 20, 4, 3, 1.6, 0.04
     q, k, v = rnd(180, 1, 2, T, d), rnd(181, 1, 2, T, d), rnd(182, 1, 2, T, e)
     idx = list(range(2 * T))
