@@ -114,3 +114,25 @@ def test_forward_with_listed_rows_replays_from_a_cuda_graph(lla):
     torch.cuda.synchronize()
     assert lla.lla_stream_status() == 0
     assert torch.equal(out, ref)
+
+
+@pytest.mark.gpu
+def test_concurrent_forwards_on_two_streams_share_the_side_stream(lla):
+    """Two forwards with listed rows, on two streams with no ordering between them, each fork
+    to and join back from the one side stream of the device: each result equals its own call run
+    alone, bit for bit."""
+    a = [t.cuda() for t in offset_inputs(1101, 64, 16.0, "all", "bf16")]
+    b = [t.cuda() for t in offset_inputs(1102, 64, 32.0, "one", "bf16")]
+    ref_a = lla.lla_forward(*a, 8.0, 1e-2)
+    ref_b = lla.lla_forward(*b, 8.0, 1e-2)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    out_a, out_b = torch.empty_like(ref_a), torch.empty_like(ref_b)
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            lla.lla_forward(*a, 8.0, 1e-2, out=out_a, stream=s1)
+        with torch.cuda.stream(s2):
+            lla.lla_forward(*b, 8.0, 1e-2, out=out_b, stream=s2)
+    torch.cuda.synchronize()
+    assert lla.lla_stream_status() == 0
+    assert torch.equal(out_a, ref_a) and torch.equal(out_b, ref_b)
