@@ -27,10 +27,12 @@
 // rounding of the right-hand side along them would be divided by lambda'. So the known null
 // vector is deflated (tr(K') s s^T added, s = W^(1/2) 1 / |.|, an eigenvector whose right-hand
 // side component is zero) and the ridge is floored at kFloor times the largest diagonal entry:
-// the remaining null directions then carry rounding / floor, about 1e-6 of the output at most,
-// while a direction of the keys with variance sigma^2 is biased by floor / sigma^2 (negligible
-// unless sigma^2 is below about 1e-10 of the largest). A non-finite K' or right-hand side
-// (non-finite inputs) gives NaN and LLA_ERR_NUMERICAL.
+// the remaining null directions then carry rounding / floor, and a direction of the keys whose
+// variance is a fraction f of the largest is biased by about kFloor / f. kFloor = 1e-12 balances
+// the two (float64 rounding of K' is ~n eps ~ 1e-14 of its largest entry; n = d random keys leave
+// f ~ 1e-5): against the oracle, 1e-10 gave 2.5e-3 on such a prefix, 1e-14 7e-3 from rounding,
+// 1e-12 at most 9e-5 over offset, i.i.d., repeated-key and n > d prefixes. A non-finite K' or
+// right-hand side (non-finite inputs) gives NaN and LLA_ERR_NUMERICAL.
 #include <cuda_bf16.h>
 
 #include "lla_internal.cuh"
@@ -42,7 +44,7 @@ constexpr int NT = 256;
 constexpr int NMAX = kShortMaxKeys;  // keys of a listed row's prefix, at most
 constexpr int LD = 65;               // row stride (doubles) of the centred keys, values and K'
 constexpr int kGrid = 152;
-constexpr double kFloor = 1e-10;     // ridge floor, relative to the largest diagonal entry of K'
+constexpr double kFloor = 1e-12;     // ridge floor, relative to the largest diagonal entry of K'
 
 // xc, vc, kk [NMAX][LD]; sw, z, lg, dinv [NMAX]; g, kb, vb [64]; red [NT / 32]
 constexpr size_t kSmem = sizeof(double) * (3 * NMAX * LD + 4 * NMAX + 3 * 64 + NT / 32);
