@@ -306,18 +306,32 @@ MIN_TIMED_S = 2.0   # device time the timed region spans at least (clock samples
 PARITY_ROWS = 96    # sampled rows of the timed output checked against the oracle
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (a job's time is that of its slowest rank); x itself when
+    there is one rank. The reduction runs on the process group's device: CUDA under NCCL, the
+    host under gloo."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed (the same on each) over the slowest
+    rank's time."""
+    return units_per_rank * world / seconds
+
+
 def timed_repeats(warm_step_ms: float, steps: int, world: int, min_s: float = MIN_TIMED_S) -> int:
     """Repetitions of the K-step timed loop so that the timed region lasts >= min_s
     (each repetition times exactly K steps; the same count on every rank)."""
     est = max(warm_step_ms, 1e-3) * max(steps, 1)
     reps = int(min(200, max(1, math.ceil(min_s * 1e3 / est))))
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([reps], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        reps = int(t.item())
-    return reps
+    return int(max_over_ranks(reps, world))
 
 
 def parity_summary(got, ref, v, bound: float, nrows: int) -> dict:
@@ -417,12 +431,9 @@ def run_parallax(args, w, cpu, world, rank):
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during the timed steps")
     ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
-    value = w.queries * world / (ms_per_step / 1e3)
+    value = job_rate(w.queries, world, ms_per_step / 1e3)
 
     e2e = None
     eb = q.element_size()
@@ -444,11 +455,8 @@ def run_parallax(args, w, cpu, world, rank):
         for _ in range(e2e_steps):
             e2e_step()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks(e2e_s, world)
+        e2e = {"value": job_rate(w.queries, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel() + r.numel()) * eb,
                "d2h_bytes_per_step": out.numel() * eb}
 
@@ -553,12 +561,9 @@ def run_parallax_backward(args, w, world, rank):
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during the timed steps")
     ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
-    value = w.queries * world / (ms_per_step / 1e3)
+    value = job_rate(w.queries, world, ms_per_step / 1e3)
 
     e2e = None
     eb = q.element_size()
@@ -581,11 +586,8 @@ def run_parallax_backward(args, w, world, rank):
         for _ in range(e2e_steps):
             e2e_step()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks(e2e_s, world)
+        e2e = {"value": job_rate(w.queries, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": sum(x.numel() for x in (q, k, v, r, do)) * eb,
                "d2h_bytes_per_step": sum(x.numel() for x in (q, k, v, r)) * eb}
 
@@ -693,13 +695,10 @@ def run_decode(args, world, rank):
     if lla.lla_stream_status() != 0:
         raise RuntimeError("liblla reported an error during the timed steps")
     ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
     queries = B * H
-    value = queries * world / (ms_per_step / 1e3)
+    value = job_rate(queries, world, ms_per_step / 1e3)
     eb = q.element_size()
 
     e2e = None
@@ -721,7 +720,7 @@ def run_decode(args, world, rank):
         for _ in range(n_e2e):
             e2e_step()
         e2e_s = (time.perf_counter() - t0) / n_e2e
-        e2e = {"value": queries * world / e2e_s, "unit": UNIT,
+        e2e = {"value": job_rate(queries, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": (q.numel() * (2 if px else 1) + k.numel() + v.numel()) * eb,
                "d2h_bytes_per_step": out.numel() * eb}
 
@@ -914,12 +913,9 @@ def main(argv=None):
     rep_ms = [sum(a.elapsed_time(b) for a, b in ev[r * args.steps:(r + 1) * args.steps])
               for r in range(reps)]
     ms = statistics.median(rep_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
-    value = w.queries * world / (ms_per_step / 1e3)
+    value = job_rate(w.queries, world, ms_per_step / 1e3)
 
     parity = None
     if timer is not None:  # the oracle leg: sampled rows of the timed output vs the oracle
@@ -944,11 +940,8 @@ def main(argv=None):
         for _ in range(e2e_steps):
             lla.lla_forward_host(hq, hk, hv, h, lam, out=hout, stream=stream)
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": w.queries * world / e2e_s, "unit": UNIT,
+        e2e_s = max_over_ranks(e2e_s, world)
+        e2e = {"value": job_rate(w.queries, world, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * eb,
                "d2h_bytes_per_step": out.numel() * eb}
 
